@@ -1,0 +1,468 @@
+"""Plain fp64 CPU oracle of the sparse Mixture-of-Experts FFN layer.
+
+TEST INFRASTRUCTURE ONLY.  This module is the checker the CUDA path is
+compared against.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import it; the library itself never calls
+it, and it shares no code with the CUDA path.
+
+Everything is numpy float64, single pass, written in the order the pages
+state the method.  Library primitives used as single steps: ``@`` (matmul),
+``np.lexsort`` (a sort), ``math.erf``/``np.exp``.  Inputs arrive as the
+stored bits the GPU reads (fp32 or bf16 decoded exactly to fp64), so both
+sides start from identical values.
+
+Sources (page title -- section):
+  [P1] "'More parameters is better' is not the story: the expert group
+       quietly activated inside a large model" (mlqm.cn) -- 3.1 Router,
+       3.3 Gate, 4.2 model definition, 4.3 training configuration.
+  [P2] "MoE mixture-of-experts architecture: principles and engineering
+       practice" (cnnetsun.cn) -- 3.2 router, 4.2 building an MoE model.
+  [P3] "MoE architecture revealed: why total parameters != active
+       parameters" (rkmt.cn) -- 2.3 router design, 3.3 TinyMoE.
+  [P4] "GPT-4 has 1.8 trillion parameters and uses 2% of them per token"
+       (wmrh.cn) -- 2.2 the meaning of 2% and dynamic routing, 5.1 MVP.
+  [P5] "Training a 200B LLM from scratch 5/25: how does MoE compute with
+       part of its parameters?" (shanhuang.net) -- "Who decides which
+       experts to call?", "Shared experts", "200B is still there".
+
+Readings of points the pages leave open (each also listed in the design
+notes): no router bias (P1 4.2); top-k weights renormalised to sum to 1
+(P1 3.3, 4.2; P3 3.3); ties broken towards the lower expert index, selection
+on logits; Gumbel noise added to the logits before both selection and
+weights (P3 2.3); capacity C = max(min_capacity, ceil(cf*T*k/E)), no limit
+when cf <= 0 (P3 2.3); overflow decided in slot-major priority (all first
+choices in token order, then all second choices); a dropped slot adds zero
+and the kept weight is not renormalised; GeLU is the exact erf form;
+SwiGLU is W2 (silu(W1 v) * (W3 v)); the shared expert is added with weight
+1 (P5 "Shared experts"); usage statistic lambda*std_{n-1}(f)/(mean(f)+1e-8)
+on pre-capacity counts f = counts/T (P1 3.1, 4.2); a token whose logits are
+not all finite is routed to no expert.
+
+Backward (training workload): the loss is L = <dY, y> + lambda*CV(I/T) with
+I[e] = sum of the routing weights of the slots routed to e (P4 2.2's
+"importance"), CV = std_{n-1}/(mean + 1e-8) -- the differentiable reading of
+P1's balance term; its forward statistic stays the count-based one.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# decoding of stored inputs
+# ----------------------------------------------------------------------------
+
+
+def decode(a) -> np.ndarray:
+    """Stored tensor -> fp64 ndarray.  Accepts numpy arrays or torch tensors
+    (fp32, or bf16 whose 16-bit patterns are widened exactly)."""
+    if hasattr(a, "detach"):  # torch tensor, decoded without torch arithmetic
+        t = a.detach().cpu()
+        if str(t.dtype) == "torch.bfloat16":
+            bits = t.contiguous().view(dtype=__import__("torch").int16).numpy()
+            u32 = (bits.astype(np.uint16).astype(np.uint32)) << 16
+            return u32.view(np.float32).astype(np.float64)
+        return t.numpy().astype(np.float64)
+    return np.asarray(a, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------
+# routing  ([P1] 3.1, 3.3, 4.2; [P3] 2.3, 3.3)
+# ----------------------------------------------------------------------------
+
+
+def router_logits(x, Wr, expert_bias=None, noise=None) -> np.ndarray:
+    """l[t,e] = sum_i x[t,i] Wr[e,i] (+ bias[e]) (+ G[t,e]).
+
+    [P1] 3.1: "logits = h W_r"; [P3] 2.3: Gumbel noise is added to the router
+    score before top-k.  The per-expert bias is an explicit input (a workload
+    of skewed load)."""
+    x = decode(x)
+    Wr = decode(Wr)
+    l = x @ Wr.T
+    if expert_bias is not None:
+        l = l + decode(expert_bias)[None, :]
+    if noise is not None:
+        l = l + decode(noise)
+    return l
+
+
+def top_k_route(l: np.ndarray, k: int):
+    """Top-k experts per token and their renormalised weights.
+
+    Experts are ordered by (logit descending, index ascending); the first k
+    are selected ([P1] 4.2 takes top-k of softmax(l); softmax is monotone, so
+    ordering the logits gives the same set).  Weights are the softmax of the
+    selected logits, w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0), which is
+    [P1] 3.3's p_i/(p_i+p_j) and [P3] 3.3's softmax over the top-k logits.
+
+    Returns idx [T,k] int64 (-1 for a token with a non-finite logit), w [T,k]
+    fp64 (0 there), finite [T] bool."""
+    T, E = l.shape
+    idx = np.full((T, k), -1, dtype=np.int64)
+    w = np.zeros((T, k), dtype=np.float64)
+    finite = np.all(np.isfinite(l), axis=1)
+    experts = np.arange(E)
+    for t in range(T):
+        if not finite[t]:
+            continue
+        order = np.lexsort((experts, -l[t]))  # primary: -l, secondary: index
+        sel = order[:k]
+        idx[t] = sel
+        z = np.exp(l[t, sel] - l[t, sel[0]])
+        w[t] = z / z.sum()
+    return idx, w, finite
+
+
+def softmax(l: np.ndarray) -> np.ndarray:
+    """Row softmax over all experts ([P1] 3.1 p_i)."""
+    z = np.exp(l - l.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+# ----------------------------------------------------------------------------
+# capacity and dispatch  ([P3] 2.3; [P1] 4.3; [P2] 4.2)
+# ----------------------------------------------------------------------------
+
+
+def expert_capacity(T: int, k: int, E: int, capacity_factor: float, min_capacity: int = 0) -> int:
+    """C = max(min_capacity, ceil(cf * T * k / E)); no limit (C = T) if cf <= 0.
+
+    [P3] 2.3's worked case: batch 1024, k=2, 16 experts -> (1024*2)/16 = 128."""
+    if capacity_factor <= 0:
+        return T
+    c = math.ceil(capacity_factor * T * k / E - 1e-9)
+    return max(int(min_capacity), int(c))
+
+
+def usage_counts(idx: np.ndarray, E: int) -> np.ndarray:
+    """counts[e] = number of (t, j) slots routed to e, before capacity."""
+    counts = np.zeros(E, dtype=np.int64)
+    for e in idx.reshape(-1):
+        if e >= 0:
+            counts[e] += 1
+    return counts
+
+
+def assign_capacity(idx: np.ndarray, E: int, C: int):
+    """Queue simulation in slot-major priority.
+
+    for j in 0..k-1, for t in 0..T-1: the slot (t, j) gets the next free
+    place of its expert if fewer than C are taken, else it is dropped
+    ([P3] 2.3 / [P1] 4.3: tokens beyond capacity are dropped).
+    Returns rank [T,k] (-1 dropped or unrouted) and fill[E] (kept per expert)."""
+    T, k = idx.shape
+    rank = np.full((T, k), -1, dtype=np.int64)
+    fill = np.zeros(E, dtype=np.int64)
+    for j in range(k):
+        for t in range(T):
+            e = idx[t, j]
+            if e < 0:
+                continue
+            if fill[e] < C:
+                rank[t, j] = fill[e]
+                fill[e] += 1
+    return rank, fill
+
+
+def dispatch_positions(idx: np.ndarray, rank: np.ndarray, fill: np.ndarray):
+    """offsets = exclusive prefix sum of the kept counts (experts in index
+    order); a kept slot's row in the expert-contiguous buffer is
+    offsets[e] + rank.  Returns offsets [E+1], pos [T,k] (-1 if not kept)."""
+    E = fill.shape[0]
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + fill[e]
+    pos = np.where(rank >= 0, offsets[np.maximum(idx, 0)] + rank, -1)
+    return offsets, pos
+
+
+def balance_stat(counts: np.ndarray, T: int, lam: float) -> float:
+    """lambda * std(f) / (mean(f) + 1e-8), f = counts / T, std with n-1.
+
+    [P1] 3.1: L_balance = lambda * std(usage)/mean(usage); [P1] 4.2's code
+    averages the one-hot selection over tokens and adds 1e-8 to the mean;
+    torch.std there is the n-1 form."""
+    f = counts.astype(np.float64) / T
+    E = f.shape[0]
+    if E < 2:
+        return 0.0  # one expert: nothing to balance (n-1 = 0)
+    mean = f.sum() / E
+    var = ((f - mean) ** 2).sum() / (E - 1)
+    return lam * math.sqrt(var) / (mean + 1e-8)
+
+
+# ----------------------------------------------------------------------------
+# experts and combine  ([P2] 4.2; [P3] 3.3; [P1] 3.2; [P5])
+# ----------------------------------------------------------------------------
+
+
+def gelu(z):
+    """Exact GeLU z * Phi(z) = z * (1 + erf(z / sqrt 2)) / 2 (nn.GELU default form)."""
+    erf = np.vectorize(math.erf, otypes=[np.float64])
+    return z * 0.5 * (1.0 + erf(z / math.sqrt(2.0)))
+
+
+def gelu_grad(z):
+    erf = np.vectorize(math.erf, otypes=[np.float64])
+    return 0.5 * (1.0 + erf(z / math.sqrt(2.0))) + z * np.exp(-0.5 * z * z) / math.sqrt(2.0 * math.pi)
+
+
+def silu(z):
+    """silu(z) = z / (1 + exp(-z))."""
+    return z / (1.0 + np.exp(-z))
+
+
+def silu_grad(z):
+    s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * (1.0 - s))
+
+
+def expert_ffn(v: np.ndarray, act: str, W1, W2, W3=None, b1=None, b2=None) -> np.ndarray:
+    """One expert FFN on rows v [n, d] -> [n, d].
+
+    GeLU: W2 gelu(W1 v + b1) + b2 ([P2] 4.2, [P3] 3.3: Linear, GELU, Linear).
+    SwiGLU: W2 (silu(W1 v) * (W3 v)) (gate W1, up W3, no biases)."""
+    if act == "gelu":
+        z = v @ W1.T
+        if b1 is not None:
+            z = z + b1[None, :]
+        out = gelu(z) @ W2.T
+        if b2 is not None:
+            out = out + b2[None, :]
+        return out
+    if act == "swiglu":
+        return (silu(v @ W1.T) * (v @ W3.T)) @ W2.T
+    raise ValueError(act)
+
+
+def combine(expert_out: np.ndarray, w: np.ndarray, kept: np.ndarray, shared: Optional[np.ndarray] = None):
+    """y = sum over kept slots j of w_j * expert_out_j (+ shared).
+
+    [P5] "Who decides which experts to call?": the two chosen experts'
+    outputs are mixed with the routing proportions; [P5] "Shared experts":
+    the shared expert's output is added.  expert_out [T,k,d], w [T,k],
+    kept [T,k] bool."""
+    T, k, d = expert_out.shape
+    y = np.zeros((T, d), dtype=np.float64)
+    for j in range(k):
+        y += np.where(kept[:, j:j + 1], w[:, j:j + 1] * expert_out[:, j, :], 0.0)
+    if shared is not None:
+        y += shared
+    return y
+
+
+# ----------------------------------------------------------------------------
+# the layer
+# ----------------------------------------------------------------------------
+
+
+def route_and_dispatch(cfg: dict, x, Wr, expert_bias=None, noise=None) -> Dict[str, np.ndarray]:
+    """Router, top-k, capacity and dispatch of the whole batch (no experts)."""
+    T, E, k = cfg["T"], cfg["E"], cfg["k"]
+    l = router_logits(x, Wr, expert_bias, noise)
+    idx, w, finite = top_k_route(l, k)
+    counts = usage_counts(idx, E)
+    C = expert_capacity(T, k, E, cfg.get("capacity_factor", 0.0), cfg.get("min_capacity", 0))
+    rank, fill = assign_capacity(idx, E, C)
+    offsets, pos = dispatch_positions(idx, rank, fill)
+    routed = int(counts.sum())
+    kept_total = int(fill.sum())
+    stats = dict(
+        routed_slots=routed,
+        kept_slots=kept_total,
+        dropped_slots=T * k - kept_total,
+        capacity=C,
+        drop_rate=(T * k - kept_total) / (T * k),
+        balance_stat=balance_stat(counts, T, cfg.get("lam", 0.01)),
+        numeric_error=int((~finite).sum()),
+    )
+    return dict(logits=l, idx=idx, w=w, counts=counts, kept=fill, capacity=C,
+                rank=rank, offsets=offsets, pos=pos, stats=stats)
+
+
+def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None,
+                  tokens: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """The whole forward pass; expert outputs computed for ``tokens`` only
+    (all tokens if None).  Returns the routing results for the whole batch
+    and y [len(tokens), d]."""
+    r = route_and_dispatch(cfg, x, weights["Wr"], expert_bias, noise)
+    X = decode(x)
+    T, k, d = cfg["T"], cfg["k"], cfg["d"]
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    act = cfg["act"]
+    out = np.zeros((len(toks), k, d), dtype=np.float64)
+    kept = r["pos"][toks] >= 0
+    idx = r["idx"][toks]
+    touched = np.zeros(len(toks), dtype=np.int64)
+    for e in range(cfg["E"]):
+        rows, slots = np.nonzero((idx == e) & kept)
+        if rows.size == 0:
+            continue
+        We = expert_params(weights, e, act)
+        out[rows, slots] = expert_ffn(X[toks[rows]], act, **We)
+        np.add.at(touched, rows, sum(a.size for a in We.values() if a is not None))
+    shared = None
+    if cfg.get("has_shared"):
+        Ws = shared_params(weights, act)
+        shared = expert_ffn(X[toks], act, **Ws)
+        touched += sum(a.size for a in Ws.values() if a is not None)
+    y = combine(out, r["w"][toks], kept, shared)
+    r.update(y=y, tokens=toks, expert_out=out, shared_out=shared, params_touched=touched)
+    return r
+
+
+def expert_params(weights: dict, e: int, act: str) -> dict:
+    p = dict(W1=decode(weights["W1"][e]), W2=decode(weights["W2"][e]))
+    if act == "swiglu":
+        p["W3"] = decode(weights["W3"][e])
+    else:
+        p["b1"] = decode(weights["b1"][e]) if weights.get("b1") is not None else None
+        p["b2"] = decode(weights["b2"][e]) if weights.get("b2") is not None else None
+    return p
+
+
+def shared_params(weights: dict, act: str) -> dict:
+    p = dict(W1=decode(weights["Ws1"]), W2=decode(weights["Ws2"]))
+    if act == "swiglu":
+        p["W3"] = decode(weights["Ws3"])
+    else:
+        p["b1"] = decode(weights["bs1"]) if weights.get("bs1") is not None else None
+        p["b2"] = decode(weights["bs2"]) if weights.get("bs2") is not None else None
+    return p
+
+
+# ----------------------------------------------------------------------------
+# backward (training workload)
+# ----------------------------------------------------------------------------
+
+
+def expert_ffn_backward(v: np.ndarray, g_out: np.ndarray, act: str, W1, W2, W3=None, b1=None, b2=None):
+    """Chain rule through one expert for rows v [n,d] with upstream g_out [n,d].
+
+    Returns dict with dv [n,d], dW1, dW2 (and dW3 or db1/db2), plus the
+    forward output of the rows (used by the routing-weight gradient)."""
+    g = {}
+    if act == "swiglu":
+        a = v @ W1.T
+        b = v @ W3.T
+        hact = silu(a) * b
+        out = hact @ W2.T
+        dh = g_out @ W2
+        da = dh * b * silu_grad(a)
+        db = dh * silu(a)
+        g["dW2"] = g_out.T @ hact
+        g["dW1"] = da.T @ v
+        g["dW3"] = db.T @ v
+        g["dv"] = da @ W1 + db @ W3
+    else:
+        z = v @ W1.T
+        if b1 is not None:
+            z = z + b1[None, :]
+        hact = gelu(z)
+        out = hact @ W2.T
+        if b2 is not None:
+            out = out + b2[None, :]
+        dh = g_out @ W2
+        dz = dh * gelu_grad(z)
+        g["dW2"] = g_out.T @ hact
+        g["dW1"] = dz.T @ v
+        g["db1"] = dz.sum(axis=0)
+        g["db2"] = g_out.sum(axis=0)
+        g["dv"] = dz @ W1
+    g["out"] = out
+    return g
+
+
+def importance_cv_grad(idx: np.ndarray, w: np.ndarray, E: int, T: int, lam: float):
+    """Value and gradient of lambda * std_{n-1}(I/T) / (mean(I/T) + 1e-8) with
+    respect to each slot's weight, I[e] = sum of w over slots routed to e."""
+    f = np.zeros(E, dtype=np.float64)
+    for t in range(idx.shape[0]):
+        for j in range(idx.shape[1]):
+            if idx[t, j] >= 0:
+                f[idx[t, j]] += w[t, j]
+    f /= T
+    mean = f.sum() / E
+    dev = f - mean
+    std = math.sqrt((dev ** 2).sum() / (E - 1))
+    val = lam * std / (mean + 1e-8)
+    # d val / d f_e
+    if std > 0:
+        dstd = dev / ((E - 1) * std)
+    else:
+        dstd = np.zeros(E)
+    dval_df = lam * (dstd / (mean + 1e-8) - std / (mean + 1e-8) ** 2 / E)
+    dval_dw = np.where(idx >= 0, dval_df[np.maximum(idx, 0)] / T, 0.0)
+    return val, dval_dw
+
+
+def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None) -> Dict[str, np.ndarray]:
+    """Gradients of L = <dY, y> + lambda*CV(I/T) for the whole (small) batch.
+
+    Per slot: G[t,j] = [kept] <dY[t], FFN_e(x[t])> + d(lambda CV)/dw[t,j];
+    logit gradient dl[t, idx_j] = w_j (G_j - sum_j' w_j' G_j') (softmax over
+    the selected logits), other logits 0; dWr = dl^T x; dX = dl Wr + the
+    experts' input gradients (routed rows scaled by w) + the shared expert's."""
+    T, d, E, k = cfg["T"], cfg["d"], cfg["E"], cfg["k"]
+    act = cfg["act"]
+    lam = cfg.get("lam", 0.01)
+    r = route_and_dispatch(cfg, x, weights["Wr"], expert_bias, noise)
+    X = decode(x)
+    DY = decode(dY)
+    idx, w, pos = r["idx"], r["w"], r["pos"]
+    kept = pos >= 0
+    dX = np.zeros((T, d))
+    G = np.zeros((T, k))
+    grads = {}
+    for name in ("W1", "W3", "W2"):
+        if name in weights and weights[name] is not None:
+            grads["d" + name] = np.zeros(decode(weights[name]).shape)
+    if act == "gelu":
+        grads["db1"] = np.zeros((E, cfg["h"]))
+        grads["db2"] = np.zeros((E, d))
+    y = np.zeros((T, d))
+    for e in range(E):
+        rows, slots = np.nonzero((idx == e) & kept)
+        if rows.size == 0:
+            continue
+        We = expert_params(weights, e, act)
+        g_out = w[rows, slots][:, None] * DY[rows]
+        g = expert_ffn_backward(X[rows], g_out, act, **We)
+        G[rows, slots] += np.einsum("nd,nd->n", DY[rows], g["out"])
+        y[rows] += w[rows, slots][:, None] * g["out"]
+        np.add.at(dX, rows, g["dv"])
+        for name in ("W1", "W3", "W2", "b1", "b2"):
+            if "d" + name in g and "d" + name in grads:
+                grads["d" + name][e] += g["d" + name]
+    if cfg.get("has_shared"):
+        Ws = shared_params(weights, act)
+        g = expert_ffn_backward(X, DY, act, **Ws)
+        dX += g["dv"]
+        y += g["out"]
+        grads["dWs1"] = g["dW1"]
+        grads["dWs2"] = g["dW2"]
+        if act == "swiglu":
+            grads["dWs3"] = g["dW3"]
+    val, dcv = importance_cv_grad(idx, w, E, T, lam)
+    G += dcv
+    dl = np.zeros((T, E))
+    for t in range(T):
+        if idx[t, 0] < 0:
+            continue
+        s = (w[t] * G[t]).sum()
+        for j in range(k):
+            dl[t, idx[t, j]] += w[t, j] * (G[t, j] - s)
+    Wr = decode(weights["Wr"])
+    grads["dWr"] = dl.T @ X
+    dX += dl @ Wr
+    grads["dX"] = dX
+    grads["dlogits"] = dl
+    grads["y"] = y
+    grads["loss"] = float((DY * y).sum() + val)
+    grads["balance_term"] = val
+    grads.update(route=r)
+    return grads
