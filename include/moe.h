@@ -1,0 +1,210 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts FFN layer.
+ *
+ * One layer, forward (and backward for training): router -> softmax/top-k ->
+ * capacity-limited dispatch -> k expert FFNs (GeLU or SwiGLU) + an optional
+ * always-on shared expert -> weighted combine -> load statistics.
+ *
+ * Sources (page title -- section):
+ *   [P1] "'More parameters is better' is not the story: the expert group
+ *        quietly activated inside a large model" (mlqm.cn) -- 3.1 Router,
+ *        3.3 Gate, 4.2 model definition, 4.3 training configuration.
+ *   [P2] "MoE mixture-of-experts architecture: principles and engineering
+ *        practice" (cnnetsun.cn) -- 3.2 router, 4.1 expert fusion, 4.2
+ *        building an MoE model.
+ *   [P3] "MoE architecture revealed: why total parameters != active
+ *        parameters" (rkmt.cn) -- 2.3 router design, 3.3 TinyMoE.
+ *   [P4] "GPT-4 has 1.8 trillion parameters and uses 2% of them per token"
+ *        (wmrh.cn) -- 2.2 dynamic routing, 5.1 MVP.
+ *   [P5] "Training a 200B LLM from scratch 5/25: how does MoE compute with
+ *        part of its parameters?" (shanhuang.net) -- "Who decides which
+ *        experts to call?", "Shared experts".
+ *
+ * Conventions (every entry point):
+ *  - Ownership: the caller allocates every buffer, the workspace included.
+ *    The library never allocates or frees device memory and keeps no state
+ *    between calls, apart from a per-process cache of driver entry points.
+ *  - Pointers: device pointers unless stated, 16-byte aligned.  Tensors are
+ *    dense row-major.  Storage type = cfg->dtype (fp32 or bf16) for
+ *    activations and weights; routing weights, noise, the expert bias and
+ *    statistics are always fp32; indices int32.
+ *  - Weight layout ("out x in", the contraction dimension contiguous):
+ *    Wr[E,d]; W1 (gate), W3 (up) [E,h,d]; W2 [E,d,h]; b1 [E,h]; b2 [E,d];
+ *    shared Ws1, Ws3 [h,d]; Ws2 [d,h]; bs1 [h]; bs2 [d].
+ *  - Asynchrony: work is enqueued on `stream`; no call synchronises the host
+ *    except moe_check_error.  Statistics are written to device memory.
+ *  - Errors: argument checks happen before any launch and return
+ *    MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE with no
+ *    work enqueued.  A failed launch returns MOE_ERR_CUDA.  Non-finite router
+ *    logits never trap: that token is routed to no expert (idx = -1, w = 0)
+ *    and counted in moe_stats.numeric_error.  Kernels that wait on on-chip
+ *    barriers give up after a bounded time and record a nonzero code in the
+ *    workspace error word (read it with moe_check_error).
+ *  - Fixed rules: top-k ties go to the lower expert index; capacity is
+ *    granted in slot-major priority (every token's first choice in token
+ *    order, then every second choice, ...).
+ *  - Limits: 1 <= k <= min(E, 8); 1 <= E <= 1024; T >= 1; T*k <= 2^30; for
+ *    bf16, d and h multiples of 8 (16-byte rows).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* = cudaStream_t; NULL = legacy default */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_CUDA = 3,
+  MOE_ERR_WORKSPACE = 4,
+  MOE_ERR_TIMEOUT = 5
+} moe_status;
+
+enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 };
+enum { MOE_F32 = 0, MOE_BF16 = 1 };
+
+/* Layer shape and routing rule.  [P2] 4.2 (capacity_factor, min_capacity),
+ * [P1] 4.3 (load_balancing_loss_coef 0.01). */
+typedef struct {
+  int T;                 /* tokens in the batch                                */
+  int d;                 /* model width                                        */
+  int h;                 /* expert hidden width                                */
+  int E;                 /* routed experts                                     */
+  int k;                 /* experts per token                                  */
+  int act;               /* MOE_ACT_GELU | MOE_ACT_SWIGLU                      */
+  int dtype;             /* MOE_F32 | MOE_BF16                                 */
+  float capacity_factor; /* C = max(min_capacity, ceil(cf*T*k/E)); <= 0: C = T */
+  int min_capacity;      /* floor on C (0 = none)                              */
+  float lambda_balance;  /* lambda of the usage statistic (0.01)               */
+  int has_shared;        /* 1: add the always-on shared expert                 */
+} moe_config;
+
+typedef struct {
+  const void* Wr;            /* [E,d]                                   */
+  const void* W1;            /* [E,h,d] gate (GeLU: the only input proj) */
+  const void* W3;            /* [E,h,d] up (SwiGLU only)                 */
+  const void* W2;            /* [E,d,h]                                  */
+  const void* b1;            /* [E,h] GeLU only, nullable                */
+  const void* b2;            /* [E,d] GeLU only, nullable                */
+  const void* Ws1;           /* [h,d] shared expert                      */
+  const void* Ws3;           /* [h,d]                                    */
+  const void* Ws2;           /* [d,h]                                    */
+  const void* bs1;           /* [h] nullable                             */
+  const void* bs2;           /* [d] nullable                             */
+  const float* expert_bias;  /* [E] fp32 added to every token's logits, nullable */
+} moe_weights;
+
+/* Activations a training forward keeps for the backward (device, caller-owned). */
+typedef struct {
+  int* idx;      /* [T,k]  selected experts (-1: none)                     */
+  float* w;      /* [T,k]  routing weights                                 */
+  int* counts;   /* [E]    slots routed to each expert (before capacity)   */
+  int* kept;     /* [E]    slots kept after capacity                       */
+  int* offsets;  /* [E+1]  first row of each expert in Xp/H/Yp             */
+  int* pos;      /* [T,k]  row of slot (t,j) in Xp/H/Yp, -1 if dropped     */
+  void* Xp;      /* [T*k, d] tokens permuted to expert-contiguous order    */
+  void* H;       /* [T*k, h] activated hidden rows                         */
+  void* Yp;      /* [T*k, d] expert outputs, permuted order                */
+  void* Sx;      /* [T, d]   shared-expert output (has_shared)             */
+} moe_saved;
+
+/* Load statistics ([P1] 3.1, 4.2; [P3] 2.3 drop monitoring). */
+typedef struct {
+  long long routed_slots;  /* sum of counts                                 */
+  long long kept_slots;    /* sum of kept                                   */
+  long long dropped_slots; /* T*k - kept_slots                              */
+  int capacity;            /* C                                             */
+  int numeric_error;       /* tokens with a non-finite logit                */
+  double drop_rate;        /* dropped_slots / (T*k)                         */
+  double balance_stat;     /* lambda * std_{n-1}(counts/T) / (mean + 1e-8)  */
+} moe_stats;
+
+/* C = max(min_capacity, ceil(cf*T*k/E)) or T when cf <= 0 ([P3] 2.3:
+ * (1024*2)/16 = 128).  Host only.  MOE_ERR_INVALID_ARG on a bad config. */
+moe_status moe_capacity(const moe_config* cfg, int* C_out);
+
+/* Bytes of workspace the entry points below need for this config.
+ * training = 0: moe_layer_fwd with saved == NULL keeps every intermediate in
+ * the workspace.  training = 1: intermediates live in moe_saved; the
+ * workspace holds scratch only. */
+moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes);
+
+/* Router ([P1] 3.1 "logits = h W_r", softmax, top-k; [P1] 3.3 weights
+ * renormalised over the top-k; [P3] 2.3 Gumbel noise on the router score).
+ *   l[t,e] = x[t].Wr[e] (+ expert_bias[e]) (+ noise[t,e])  (fp32 accumulate)
+ *   idx[t,:] = the k largest l[t,:], larger first, ties -> lower index
+ *   w[t,j]   = exp(l[idx_j] - l[idx_0]) / sum_j' exp(l[idx_j'] - l[idx_0])
+ *   counts[e] = #slots routed to e (zeroed by this call)
+ * x [T,d], Wr [E,d] in cfg->dtype; expert_bias [E], noise [T,E] fp32,
+ * both nullable.  Outputs idx [T,k] int32, w [T,k] fp32, counts [E] int32.
+ * ws: unused, may be NULL. */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr,
+                     const float* expert_bias, const float* noise, int* idx,
+                     float* w, int* counts, void* ws, moe_stream_t stream);
+
+/* Capacity and dispatch ([P3] 2.3 capacity and dropped tokens; [P1] 4.2
+ * step 2, grouping the tokens bound for the same expert).
+ *   slot-major ranks -> kept[e] = min(routed to e, C), offsets = exclusive
+ *   scan of kept, pos[t,j] = offsets[e] + rank or -1, Xp[pos[t,j]] = x[t].
+ * idx [T,k] int32 from moe_route; x [T,d].  Outputs kept [E], offsets [E+1],
+ * pos [T,k] int32; Xp [T*k, d] (rows >= offsets[E] untouched); stats:
+ * device moe_stats*, nullable.  ws: >= moe_workspace_size(cfg, 1) bytes. */
+moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x,
+                        int* kept, int* offsets, int* pos, void* Xp,
+                        moe_stats* stats, void* ws, moe_stream_t stream);
+
+/* Grouped expert FFN over expert-contiguous rows ([P2] 4.2 and [P3] 3.3:
+ * Linear -> GELU -> Linear; SwiGLU gate/up; [P2] 4.1 all experts' weights
+ * in one contiguous tensor).  For every expert e and row r in
+ * [offsets[e], offsets[e+1]):
+ *   GeLU:   H[r] = gelu(W1[e] Xp[r] + b1[e]);   Yp[r] = W2[e] H[r] + b2[e]
+ *   SwiGLU: H[r] = silu(W1[e] Xp[r]) * (W3[e] Xp[r]);  Yp[r] = W2[e] H[r]
+ * offsets is a device array of E+1 nondecreasing int32 with offsets[0] = 0
+ * (rows past T*k are never written).  Xp, Yp [T*k, d], H [T*k, h] in
+ * cfg->dtype; rows past offsets[E] are not written.  bf16 runs on the
+ * tcgen05 tensor cores with fp32 accumulation; fp32 runs on the CUDA cores
+ * in fp32.  ws: >= moe_workspace_size(cfg, 1) bytes (its error word is
+ * reset here). */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offsets,
+                          const void* W1, const void* W3, const void* b1,
+                          const void* W2, const void* b2, void* H, void* Yp,
+                          void* ws, moe_stream_t stream);
+
+/* Weighted combine / un-permute ([P5] "Who decides which experts to call?":
+ * 0.75*[0.8,0.2,-0.4] + 0.25*[0.4,0.6,0.8] = [0.7,0.3,-0.1]; [P5] "Shared
+ * experts": the shared path is added).
+ *   y[t] = sum_{j: pos[t,j] >= 0} w[t,j] * Yp[pos[t,j]]  (+ Sx[t])
+ * summed in fp32 in slot order j = 0..k-1, stored in cfg->dtype.  pos
+ * entries index rows of Yp (< T*k).  Sx nullable. */
+moe_status moe_combine(const moe_config* cfg, const void* Yp, const int* pos,
+                       const float* w, const void* Sx, void* y, moe_stream_t stream);
+
+/* The whole forward: route, dispatch, experts, shared expert, combine,
+ * statistics.  noise [T,E] fp32 nullable.  saved: NULL (inference: every
+ * intermediate lives in ws) or the buffers a backward needs.  stats:
+ * device moe_stats*, nullable.  ws_bytes >= moe_workspace_size(cfg, saved
+ * != NULL). */
+moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const void* x,
+                         const float* noise, void* y, moe_saved* saved,
+                         moe_stats* stats, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* Synchronises `stream`, then reads the workspace error word left by the
+ * last call that used `ws`: MOE_OK, or MOE_ERR_TIMEOUT if a kernel gave up
+ * a bounded wait (code_out receives the raw word, nullable). */
+moe_status moe_check_error(const void* ws, int* code_out, moe_stream_t stream);
+
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

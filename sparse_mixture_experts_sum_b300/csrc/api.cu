@@ -1,0 +1,249 @@
+// C ABI of the sparse-MoE layer (declared and documented in include/moe.h).
+// Argument checks, workspace carving and the launch sequence; every step of
+// the computation runs in this library's kernels.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+moe_status validate(const moe_config* cfg) {
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  if (cfg->T < 1 || cfg->d < 1 || cfg->h < 1 || cfg->E < 1 || cfg->E > 1024) return MOE_ERR_INVALID_ARG;
+  if (cfg->k < 1 || cfg->k > 8 || cfg->k > cfg->E) return MOE_ERR_INVALID_ARG;
+  if (cfg->act != MOE_ACT_GELU && cfg->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype != MOE_F32 && cfg->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (cfg->min_capacity < 0 || !(cfg->capacity_factor == cfg->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(cfg->T) * cfg->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->dtype == MOE_BF16 && ((cfg->d % 8) || (cfg->h % 8))) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int capacity_of(const moe_config* cfg) {
+  if (cfg->capacity_factor <= 0.f) return cfg->T;
+  // ceil(cf*T*k/E) in double, guarded against representation noise
+  const double v = static_cast<double>(cfg->capacity_factor) * cfg->T * cfg->k / cfg->E;
+  long long c = static_cast<long long>(ceil(v - 1e-9));
+  if (c < cfg->min_capacity) c = cfg->min_capacity;
+  if (c > 2147483647LL) c = 2147483647LL;
+  return static_cast<int>(c);
+}
+
+size_t esize(const moe_config* cfg) { return cfg->dtype == MOE_BF16 ? 2 : 4; }
+
+// Workspace carving: [header | dispatch scratch | (inference) intermediates | shared hidden]
+struct WsLayout {
+  size_t dispatch_off;
+  size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs, total;
+};
+
+WsLayout layout(const moe_config* cfg, int training) {
+  WsLayout L{};
+  size_t o = kWsHeader;
+  L.dispatch_off = o;
+  o += align_up(dispatch_scratch_bytes(*cfg), 256);
+  const size_t T = cfg->T, k = cfg->k, E = cfg->E, d = cfg->d, h = cfg->h, es = esize(cfg);
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes, 256);
+    return at;
+  };
+  if (!training) {
+    L.idx = take(T * k * 4);
+    L.w = take(T * k * 4);
+    L.counts = take(E * 4);
+    L.kept = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.pos = take(T * k * 4);
+    L.Xp = take(T * k * d * es);
+    L.H = take(T * k * h * es);
+    L.Yp = take(T * k * d * es);
+    L.Sx = cfg->has_shared ? take(T * d * es) : 0;
+  }
+  L.Hs = cfg->has_shared ? take(T * h * es) : 0;
+  L.total = o;
+  return L;
+}
+
+inline void* at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, const int* offsets, int G, int rows,
+                   const void* W1, const void* W3, const void* b1, const void* W2, const void* b2, void* H,
+                   void* Yp, int* err, cudaStream_t st) {
+  const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
+  GemmParams g1{};
+  g1.offsets = offsets;
+  g1.G = G;
+  g1.rows = rows;
+  g1.N = cfg->h;
+  g1.K = cfg->d;
+  g1.mode = swiglu ? kModeSwiGLU : kModeGeLU;
+  g1.out = H;
+  g1.bias = swiglu ? nullptr : b1;
+  g1.err = err;
+  GemmParams g2 = g1;
+  g2.N = cfg->d;
+  g2.K = cfg->h;
+  g2.mode = kModePlain;
+  g2.out = Yp;
+  g2.bias = swiglu ? nullptr : b2;
+  moe_status s;
+  if (cfg->dtype == MOE_BF16) {
+    s = launch_grouped_gemm_tc(g1, Xp, a_rows, W1, swiglu ? W3 : nullptr, static_cast<long long>(G) * cfg->h, st);
+    if (s != MOE_OK) return s;
+    s = launch_grouped_gemm_tc(g2, H, a_rows, W2, nullptr, static_cast<long long>(G) * cfg->d, st);
+  } else {
+    s = launch_grouped_gemm_f32(g1, Xp, a_rows, W1, swiglu ? W3 : nullptr, st);
+    if (s != MOE_OK) return s;
+    s = launch_grouped_gemm_f32(g2, H, a_rows, W2, nullptr, st);
+  }
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_capacity(const moe_config* cfg, int* C_out) {
+  const moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!C_out) return MOE_ERR_INVALID_ARG;
+  *C_out = capacity_of(cfg);
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes) {
+  const moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = layout(cfg, training).total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr, const float* expert_bias,
+                     const float* noise, int* idx, float* w, int* counts, void* ws, moe_stream_t stream) {
+  (void)ws;
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!x || !Wr || !idx || !w || !counts) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wr)) return MOE_ERR_INVALID_ARG;
+  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x, int* kept, int* offsets, int* pos,
+                        void* Xp, moe_stats* stats, void* ws, moe_stream_t stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!idx || !x || !kept || !offsets || !pos || !Xp || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Xp) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(cfg, 1);
+  return launch_dispatch(*cfg, capacity_of(cfg), idx, x, kept, offsets, pos, Xp, stats, at(ws, L.dispatch_off),
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offsets, const void* W1,
+                          const void* W3, const void* b1, const void* W2, const void* b2, void* H, void* Yp,
+                          void* ws, moe_stream_t stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
+  if (!Xp || !offsets || !W1 || !W2 || !H || !Yp || !ws || (swiglu && !W3)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(Xp) || !aligned16(W1) || !aligned16(W2) || !aligned16(H) || !aligned16(Yp) ||
+      (swiglu && !aligned16(W3)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
+  return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, W1, W3, b1, W2, b2, H, Yp, err, st);
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* Yp, const int* pos, const float* w, const void* Sx,
+                       void* y, moe_stream_t stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!Yp || !pos || !w || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(Yp) || !aligned16(y) || (Sx && !aligned16(Sx))) return MOE_ERR_INVALID_ARG;
+  return launch_combine(*cfg, Yp, pos, w, Sx, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const void* x, const float* noise, void* y,
+                         moe_saved* saved, moe_stats* stats, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!wts || !x || !y || !ws || !wts->Wr || !wts->W1 || !wts->W2) return MOE_ERR_INVALID_ARG;
+  const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
+  if (swiglu && !wts->W3) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_shared && (!wts->Ws1 || !wts->Ws2 || (swiglu && !wts->Ws3))) return MOE_ERR_INVALID_ARG;
+  const int training = saved != nullptr;
+  const WsLayout L = layout(cfg, training);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws) || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+
+  moe_saved S;
+  if (training) {
+    S = *saved;
+    if (!S.idx || !S.w || !S.counts || !S.kept || !S.offsets || !S.pos || !S.Xp || !S.H || !S.Yp ||
+        (cfg->has_shared && !S.Sx))
+      return MOE_ERR_INVALID_ARG;
+  } else {
+    S.idx = static_cast<int*>(at(ws, L.idx));
+    S.w = static_cast<float*>(at(ws, L.w));
+    S.counts = static_cast<int*>(at(ws, L.counts));
+    S.kept = static_cast<int*>(at(ws, L.kept));
+    S.offsets = static_cast<int*>(at(ws, L.offsets));
+    S.pos = static_cast<int*>(at(ws, L.pos));
+    S.Xp = at(ws, L.Xp);
+    S.H = at(ws, L.H);
+    S.Yp = at(ws, L.Yp);
+    S.Sx = cfg->has_shared ? at(ws, L.Sx) : nullptr;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  s = launch_route(*cfg, x, wts->Wr, wts->expert_bias, noise, S.idx, S.w, S.counts, st);
+  if (s != MOE_OK) return s;
+  s = launch_dispatch(*cfg, capacity_of(cfg), S.idx, x, S.kept, S.offsets, S.pos, S.Xp, stats,
+                      at(ws, L.dispatch_off), st);
+  if (s != MOE_OK) return s;
+  const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
+  s = run_ffn(cfg, S.Xp, a_rows, S.offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, S.H, S.Yp, err,
+              st);
+  if (s != MOE_OK) return s;
+  if (cfg->has_shared) {
+    s = run_ffn(cfg, x, cfg->T, nullptr, 1, cfg->T, wts->Ws1, wts->Ws3, wts->bs1, wts->Ws2, wts->bs2,
+                at(ws, L.Hs), S.Sx, err, st);
+    if (s != MOE_OK) return s;
+  }
+  return launch_combine(*cfg, S.Yp, S.pos, S.w, cfg->has_shared ? S.Sx : nullptr, y, st);
+}
+
+moe_status moe_check_error(const void* ws, int* code_out, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (code_out) *code_out = code;
+  return code ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

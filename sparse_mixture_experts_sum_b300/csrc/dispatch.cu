@@ -1,0 +1,322 @@
+// Capacity-limited dispatch and the weighted combine.
+//
+// Dispatch ([P3] "MoE architecture revealed..." 2.3: every expert has a
+// capacity C and the tokens beyond it are dropped; [P1] "'More parameters is
+// better' is not the story..." 4.2 step 2: the tokens bound for the same
+// expert are grouped together).  Slots are ordered slot-major -- s = j*T + t,
+// every token's first choice in token order, then every second choice -- and
+// a slot's rank is the number of earlier slots routed to the same expert.
+// A slot is kept iff rank < C; kept rows are laid out expert by expert:
+//   offsets = exclusive scan of kept[e] = min(routed[e], C)
+//   pos[t,j] = offsets[e] + rank, or -1 when dropped / unrouted
+//   Xp[pos[t,j]] = x[t]
+// Four launches, all integer and deterministic (no order-visible atomics):
+//   slot_hist   per 4096-slot chunk, per-expert counts (+ unrouted)
+//   scan        per-expert exclusive scan over chunks, kept, offsets, stats
+//   assign      in-chunk ranks (warp match + per-warp counts), pos
+//   permute     one warp per token copies its row to its k destinations
+//
+// Combine ([P5] "Training a 200B LLM from scratch 5/25", "Who decides which
+// experts to call?": y = 0.75*E1(x) + 0.25*E3(x); "Shared experts": the
+// always-on path is added):
+//   y[t] = sum_{j: pos >= 0} w[t,j] * Yp[pos[t,j]]  (+ Sx[t]), fp32, j ascending.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int CH = 4096;     // slots per chunk
+constexpr int DT = 256;      // threads of the chunk kernels
+constexpr int DW = DT / 32;  // warps of the chunk kernels
+
+__device__ __forceinline__ int slot_expert(const int* idx, int T, int k, long long s, int& t, int& j) {
+  j = static_cast<int>(s / T);
+  t = static_cast<int>(s - static_cast<long long>(j) * T);
+  return idx[static_cast<size_t>(t) * k + j];
+}
+
+__global__ void __launch_bounds__(DT) slot_hist_kernel(const int* __restrict__ idx, int T, int k, int E,
+                                                       int* __restrict__ blockhist) {
+  extern __shared__ int hist[];  // E + 1 (last: unrouted)
+  for (int e = threadIdx.x; e <= E; e += DT) hist[e] = 0;
+  __syncthreads();
+  const long long nslots = static_cast<long long>(T) * k;
+  const long long s0 = static_cast<long long>(blockIdx.x) * CH;
+  for (int i = threadIdx.x; i < CH; i += DT) {
+    const long long s = s0 + i;
+    if (s >= nslots) break;
+    int t, j;
+    const int e = slot_expert(idx, T, k, s, t, j);
+    atomicAdd(&hist[(e >= 0 && e < E) ? e : E], 1);
+  }
+  __syncthreads();
+  int* out = blockhist + static_cast<size_t>(blockIdx.x) * (E + 1);
+  for (int e = threadIdx.x; e <= E; e += DT) out[e] = hist[e];
+}
+
+__global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restrict__ blockhist, int nb, int T,
+                                                             int k, int E, int C, float lam,
+                                                             int* __restrict__ base, int* __restrict__ kept,
+                                                             int* __restrict__ offsets, moe_stats* stats) {
+  __shared__ int tot[1024];
+  __shared__ int warp_sums[32];
+  __shared__ int unrouted;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int my_kept = 0;
+  if (tid < E) {
+    int run = 0;
+    for (int b = 0; b < nb; ++b) {
+      base[static_cast<size_t>(b) * E + tid] = run;
+      run += blockhist[static_cast<size_t>(b) * (E + 1) + tid];
+    }
+    tot[tid] = run;
+    my_kept = run < C ? run : C;
+  }
+  if (tid == 0) {
+    int u = 0;
+    for (int b = 0; b < nb; ++b) u += blockhist[static_cast<size_t>(b) * (E + 1) + E];
+    unrouted = u;
+  }
+  // exclusive scan of kept over experts (block-wide, experts in index order)
+  int incl = my_kept;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int ws = warp_sums[lane];
+    int wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_sums[lane] = wi - ws;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int excl = warp_sums[warp] + incl - my_kept;
+  if (tid < E) {
+    kept[tid] = my_kept;
+    offsets[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + my_kept;
+  }
+  if (tid == 0 && stats) {
+    long long routed = 0, kept_total = 0;
+    for (int e = 0; e < E; ++e) {
+      routed += tot[e];
+      kept_total += tot[e] < C ? tot[e] : C;
+    }
+    const long long nslots = static_cast<long long>(T) * k;
+    double mean = 0.0;
+    for (int e = 0; e < E; ++e) mean += static_cast<double>(tot[e]) / T;
+    mean /= E;
+    double var = 0.0;
+    for (int e = 0; e < E; ++e) {
+      const double dv = static_cast<double>(tot[e]) / T - mean;
+      var += dv * dv;
+    }
+    const double sd = E > 1 ? sqrt(var / (E - 1)) : 0.0;
+    moe_stats st;
+    st.routed_slots = routed;
+    st.kept_slots = kept_total;
+    st.dropped_slots = nslots - kept_total;
+    st.capacity = C;
+    st.numeric_error = unrouted / k;
+    st.drop_rate = static_cast<double>(nslots - kept_total) / static_cast<double>(nslots);
+    st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
+    *stats = st;
+  }
+}
+
+__global__ void __launch_bounds__(DT) assign_kernel(const int* __restrict__ idx, int T, int k, int E,
+                                                    const int* __restrict__ base, const int* __restrict__ kept,
+                                                    const int* __restrict__ offsets, int* __restrict__ pos) {
+  extern __shared__ int sm[];
+  int* runcnt = sm;       // [E]
+  int* warpcnt = sm + E;  // [DW][E]
+  for (int i = threadIdx.x; i < E * (DW + 1); i += DT) sm[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long nslots = static_cast<long long>(T) * k;
+  const long long s0 = static_cast<long long>(blockIdx.x) * CH;
+  const int* bbase = base + static_cast<size_t>(blockIdx.x) * E;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r = 0; r < CH / DT; ++r) {
+    if (s0 + static_cast<long long>(r) * DT >= nslots) break;  // uniform across the block
+    const long long s = s0 + static_cast<long long>(r) * DT + threadIdx.x;
+    int t = 0, j = 0, e = -1;
+    const bool in = s < nslots;
+    if (in) {
+      e = slot_expert(idx, T, k, s, t, j);
+      if (e >= E) e = -1;
+    }
+    const int key = in ? e : -2;
+    const unsigned same = __match_any_sync(0xffffffffu, key);
+    const int lrank = __popc(same & lt_mask);
+    if (e >= 0 && lane == __ffs(same) - 1) warpcnt[warp * E + e] = __popc(same);
+    __syncthreads();
+    if (in) {
+      int p = -1;
+      if (e >= 0) {
+        int prefix = 0;
+        for (int w2 = 0; w2 < warp; ++w2) prefix += warpcnt[w2 * E + e];
+        const int rank = bbase[e] + runcnt[e] + prefix + lrank;
+        // kept[e] = min(routed[e], C): a slot is kept iff its rank is below it,
+        // which also keeps every position inside [offsets[e], offsets[e+1])
+        if (rank < kept[e]) p = offsets[e] + rank;
+      }
+      pos[static_cast<size_t>(t) * k + j] = p;
+    }
+    __syncthreads();
+    for (int e2 = threadIdx.x; e2 < E; e2 += DT) {
+      int add = 0;
+      for (int w2 = 0; w2 < DW; ++w2) {
+        add += warpcnt[w2 * E + e2];
+        warpcnt[w2 * E + e2] = 0;
+      }
+      runcnt[e2] += add;
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per token: copy row x[t] to its kept destinations in Xp.
+template <typename V>
+__global__ void permute_kernel(const V* __restrict__ x, int T, int k, int vec_per_row, const int* __restrict__ pos,
+                               V* __restrict__ Xp) {
+  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int p[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
+  const V* src = x + static_cast<size_t>(t) * vec_per_row;
+  for (int v = lane; v < vec_per_row; v += 32) {
+    const V val = src[v];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (p[j] >= 0) Xp[static_cast<size_t>(p[j]) * vec_per_row + v] = val;
+  }
+}
+
+// One warp per token: y[t] = sum_j w[t,j] Yp[pos[t,j]] (+ Sx[t]); 8 bf16 per lane step.
+__global__ void combine_bf16_kernel(const uint4* __restrict__ Yp, const int* __restrict__ pos,
+                                    const float* __restrict__ w, const uint4* __restrict__ Sx, int T, int k,
+                                    int vec_per_row, uint4* __restrict__ y) {
+  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int p[8];
+  float wt[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
+    wt[j] = j < k ? w[static_cast<size_t>(t) * k + j] : 0.f;
+  }
+  for (int v = lane; v < vec_per_row; v += 32) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (p[j] >= 0) {
+        const uint4 q = Yp[static_cast<size_t>(p[j]) * vec_per_row + v];
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          a[2 * i] = fmaf(wt[j], bf16lo(u[i]), a[2 * i]);
+          a[2 * i + 1] = fmaf(wt[j], bf16hi(u[i]), a[2 * i + 1]);
+        }
+      }
+    }
+    if (Sx) {
+      const uint4 q = Sx[static_cast<size_t>(t) * vec_per_row + v];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[2 * i] += bf16lo(u[i]);
+        a[2 * i + 1] += bf16hi(u[i]);
+      }
+    }
+    y[static_cast<size_t>(t) * vec_per_row + v] =
+        make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
+  }
+}
+
+__global__ void combine_f32_kernel(const float* __restrict__ Yp, const int* __restrict__ pos,
+                                   const float* __restrict__ w, const float* __restrict__ Sx, int T, int k, int d,
+                                   float* __restrict__ y) {
+  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  for (int c = lane; c < d; c += 32) {
+    float a = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int p = pos[static_cast<size_t>(t) * k + j];
+      if (p >= 0) a = fmaf(w[static_cast<size_t>(t) * k + j], Yp[static_cast<size_t>(p) * d + c], a);
+    }
+    if (Sx) a += Sx[static_cast<size_t>(t) * d + c];
+    y[static_cast<size_t>(t) * d + c] = a;
+  }
+}
+
+inline int n_chunks(const moe_config& cfg) {
+  const long long n = static_cast<long long>(cfg.T) * cfg.k;
+  return static_cast<int>((n + CH - 1) / CH);
+}
+
+inline unsigned warp_grid(int T) { return static_cast<unsigned>((static_cast<long long>(T) * 32 + 255) / 256); }
+
+}  // namespace
+
+size_t dispatch_scratch_bytes(const moe_config& cfg) {
+  const size_t nb = n_chunks(cfg);
+  return align_up(nb * (cfg.E + 1) * sizeof(int), 256) + align_up(nb * cfg.E * sizeof(int), 256);
+}
+
+moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const void* x, int* kept, int* offsets,
+                           int* pos, void* Xp, moe_stats* stats, void* scratch, cudaStream_t stream) {
+  const int nb = n_chunks(cfg);
+  int* blockhist = static_cast<int*>(scratch);
+  int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) +
+                                     align_up(static_cast<size_t>(nb) * (cfg.E + 1) * sizeof(int), 256));
+  slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(idx, cfg.T, cfg.k, cfg.E, blockhist);
+  capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance, base,
+                                               kept, offsets, stats);
+  const size_t asmem = static_cast<size_t>(cfg.E) * (DW + 1) * sizeof(int);
+  assign_kernel<<<nb, DT, asmem, stream>>>(idx, cfg.T, cfg.k, cfg.E, base, kept, offsets, pos);
+  if (Xp) {
+    const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
+    const long long row_bytes = static_cast<long long>(cfg.d) * es;
+    if (row_bytes % 16 == 0)
+      permute_kernel<uint4><<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const uint4*>(x), cfg.T, cfg.k,
+                                                                  static_cast<int>(row_bytes / 16), pos,
+                                                                  static_cast<uint4*>(Xp));
+    else
+      permute_kernel<uint32_t><<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const uint32_t*>(x), cfg.T,
+                                                                     cfg.k, static_cast<int>(row_bytes / 4), pos,
+                                                                     static_cast<uint32_t*>(Xp));
+  }
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos, const float* w, const void* Sx,
+                          void* y, cudaStream_t stream) {
+  if (cfg.dtype == MOE_BF16) {
+    combine_bf16_kernel<<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const uint4*>(Yp), pos, w,
+                                                              static_cast<const uint4*>(Sx), cfg.T, cfg.k,
+                                                              cfg.d / 8, static_cast<uint4*>(y));
+  } else {
+    combine_f32_kernel<<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const float*>(Yp), pos, w,
+                                                             static_cast<const float*>(Sx), cfg.T, cfg.k, cfg.d,
+                                                             static_cast<float*>(y));
+  }
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

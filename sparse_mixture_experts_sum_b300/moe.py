@@ -1,0 +1,206 @@
+"""ctypes binding of the sparse-MoE layer's C ABI (include/moe.h).
+
+Argument marshalling only: every function forwards torch tensors' device
+pointers and the current CUDA stream to the entry point of the same name in
+libmoe_b300.so.  No arithmetic of the layer happens here, and there is no
+fallback: if the library is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE, MOE_ERR_TIMEOUT = range(6)
+ACT = {"gelu": 0, "swiglu": 1}
+DTYPE = {"f32": 0, "bf16": 1}
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("h", ctypes.c_int), ("E", ctypes.c_int),
+                ("k", ctypes.c_int), ("act", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int),
+                ("lambda_balance", ctypes.c_float), ("has_shared", ctypes.c_int)]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2", "expert_bias")]
+
+
+class MoeSaved(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("idx", "w", "counts", "kept", "offsets", "pos", "Xp", "H", "Yp", "Sx")]
+
+
+class MoeStats(ctypes.Structure):
+    _fields_ = [("routed_slots", ctypes.c_longlong), ("kept_slots", ctypes.c_longlong),
+                ("dropped_slots", ctypes.c_longlong), ("capacity", ctypes.c_int),
+                ("numeric_error", ctypes.c_int), ("drop_rate", ctypes.c_double),
+                ("balance_stat", ctypes.c_double)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn",
+           "moe_combine", "moe_layer_fwd", "moe_check_error", "moe_status_string")
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe_b300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python __graft_entry__.py` "
+                               "or sparse_mixture_experts_sum_b300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        cfgp = ctypes.POINTER(MoeConfig)
+        sig = {
+            "moe_capacity": [cfgp, ctypes.POINTER(i)],
+            "moe_workspace_size": [cfgp, i, ctypes.POINTER(sz)],
+            "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_expert_ffn": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_combine": [cfgp, vp, vp, vp, vp, vp, vp],
+            "moe_layer_fwd": [cfgp, ctypes.POINTER(MoeWeights), vp, vp, vp, ctypes.POINTER(MoeSaved), vp, vp,
+                              sz, vp],
+            "moe_check_error": [vp, ctypes.POINTER(i), vp],
+            "moe_status_string": [i],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_char_p if name == "moe_status_string" else ctypes.c_int
+        _lib = L
+    return _lib
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {lib().moe_status_string(status).decode()} (status {status})")
+
+
+def _check(fn, status):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_config(T, d, h, E, k, act="swiglu", dtype="bf16", capacity_factor=0.0, min_capacity=0,
+                lambda_balance=0.01, has_shared=False) -> MoeConfig:
+    return MoeConfig(T, d, h, E, k, ACT[act], DTYPE[dtype], capacity_factor, min_capacity,
+                     lambda_balance, int(bool(has_shared)))
+
+
+def config_of(wl) -> MoeConfig:
+    """MoeConfig of a moe_synth.Workload."""
+    return make_config(wl.T, wl.d, wl.h, wl.E, wl.k, wl.act, wl.dtype, wl.capacity_factor,
+                       wl.min_capacity, wl.lam, wl.has_shared)
+
+
+def moe_capacity(cfg: MoeConfig) -> int:
+    c = ctypes.c_int()
+    _check("moe_capacity", lib().moe_capacity(ctypes.byref(cfg), ctypes.byref(c)))
+    return c.value
+
+
+def moe_workspace_size(cfg: MoeConfig, training: bool = False) -> int:
+    n = ctypes.c_size_t()
+    _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(cfg), int(training), ctypes.byref(n)))
+    return n.value
+
+
+def workspace(cfg: MoeConfig, training=False, device="cuda") -> torch.Tensor:
+    return torch.empty(moe_workspace_size(cfg, training), dtype=torch.uint8, device=device)
+
+
+def stats_buffer(device="cuda") -> torch.Tensor:
+    return torch.zeros(ctypes.sizeof(MoeStats), dtype=torch.uint8, device=device)
+
+
+def read_stats(buf: torch.Tensor) -> dict:
+    raw = bytes(buf.cpu().numpy().tobytes())
+    return MoeStats.from_buffer_copy(raw).as_dict()
+
+
+def moe_route(cfg, x, Wr, expert_bias, noise, idx, w, counts, ws=None, stream=None):
+    _check("moe_route", lib().moe_route(ctypes.byref(cfg), _p(x), _p(Wr), _p(expert_bias), _p(noise),
+                                        _p(idx), _p(w), _p(counts), _p(ws), _stream(stream)))
+
+
+def moe_dispatch(cfg, idx, x, kept, offsets, pos, Xp, stats, ws, stream=None):
+    _check("moe_dispatch", lib().moe_dispatch(ctypes.byref(cfg), _p(idx), _p(x), _p(kept), _p(offsets),
+                                              _p(pos), _p(Xp), _p(stats), _p(ws), _stream(stream)))
+
+
+def moe_expert_ffn(cfg, Xp, offsets, W1, W3, b1, W2, b2, H, Yp, ws, stream=None):
+    _check("moe_expert_ffn", lib().moe_expert_ffn(ctypes.byref(cfg), _p(Xp), _p(offsets), _p(W1), _p(W3),
+                                                  _p(b1), _p(W2), _p(b2), _p(H), _p(Yp), _p(ws),
+                                                  _stream(stream)))
+
+
+def moe_combine(cfg, Yp, pos, w, Sx, y, stream=None):
+    _check("moe_combine", lib().moe_combine(ctypes.byref(cfg), _p(Yp), _p(pos), _p(w), _p(Sx), _p(y),
+                                            _stream(stream)))
+
+
+def weights_struct(t: dict) -> MoeWeights:
+    return MoeWeights(*[(t[n].data_ptr() if t.get(n) is not None else None) for n, _ in MoeWeights._fields_])
+
+
+def saved_struct(t: dict) -> MoeSaved:
+    return MoeSaved(*[(t[n].data_ptr() if t.get(n) is not None else None) for n, _ in MoeSaved._fields_])
+
+
+def moe_layer_fwd(cfg, weights: dict, x, noise, y, saved: Optional[dict], stats, ws, stream=None):
+    W = weights_struct(weights)
+    S = saved_struct(saved) if saved is not None else None
+    _check("moe_layer_fwd", lib().moe_layer_fwd(ctypes.byref(cfg), ctypes.byref(W), _p(x), _p(noise), _p(y),
+                                                ctypes.byref(S) if S is not None else None, _p(stats), _p(ws),
+                                                ws.numel(), _stream(stream)))
+
+
+def moe_check_error(ws, stream=None) -> int:
+    code = ctypes.c_int()
+    st = lib().moe_check_error(_p(ws), ctypes.byref(code), _stream(stream))
+    if st not in (MOE_OK, MOE_ERR_TIMEOUT):
+        raise MoeError("moe_check_error", st)
+    return code.value
+
+
+def alloc_saved(cfg: MoeConfig, device="cuda") -> dict:
+    """Caller-owned buffers of one forward (the moe_saved set)."""
+    T, k, E, d, h = cfg.T, cfg.k, cfg.E, cfg.d, cfg.h
+    dt = torch.bfloat16 if cfg.dtype == DTYPE["bf16"] else torch.float32
+    out = dict(idx=torch.empty(T, k, dtype=torch.int32, device=device),
+               w=torch.empty(T, k, dtype=torch.float32, device=device),
+               counts=torch.empty(E, dtype=torch.int32, device=device),
+               kept=torch.empty(E, dtype=torch.int32, device=device),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=device),
+               pos=torch.empty(T, k, dtype=torch.int32, device=device),
+               Xp=torch.empty(T * k, d, dtype=dt, device=device),
+               H=torch.empty(T * k, h, dtype=dt, device=device),
+               Yp=torch.empty(T * k, d, dtype=dt, device=device))
+    if cfg.has_shared:
+        out["Sx"] = torch.empty(T, d, dtype=dt, device=device)
+    return out

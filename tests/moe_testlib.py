@@ -1,0 +1,64 @@
+"""Shared helpers of the parity tests: seeded inputs with the top-k margin
+guard, comparison metrics."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import moe_synth as S
+from oracle import moe_oracle as O
+
+MARGIN = 1e-3
+
+
+def oracle_cfg(wl) -> dict:
+    # the C ABI carries lambda and the capacity factor as fp32 values; the
+    # oracle gets those same values
+    return dict(T=wl.T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act,
+                capacity_factor=float(np.float32(wl.capacity_factor)),
+                min_capacity=wl.min_capacity, lam=float(np.float32(wl.lam)), has_shared=wl.has_shared)
+
+
+def small_gaps(l: np.ndarray, k: int, margin: float = MARGIN) -> np.ndarray:
+    """Tokens whose adjacent gaps among the top-(k+1) sorted logits fall below
+    `margin` -- where an fp32 and an fp64 router could order differently."""
+    kk = min(k + 1, l.shape[1])
+    top = -np.sort(-l, axis=1)[:, :kk]
+    gaps = top[:, :-1] - top[:, 1:]
+    return np.nonzero((gaps < margin).any(axis=1))[0]
+
+
+def guard(wl, t: dict, max_attempts=50) -> dict:
+    """Redraw (in place) every row of t['x'] whose top-k margins are below
+    1e-3, from counter attempt a = 1, 2, ..., until none is left."""
+    for a in range(1, max_attempts + 1):
+        l = O.router_logits(t["x"], t["Wr"], t.get("expert_bias"), t.get("noise"))
+        bad = small_gaps(l, wl.k)
+        if bad.size == 0:
+            return t
+        S.redraw_rows(wl, t["x"], torch.as_tensor(bad), a)
+    raise RuntimeError("margin guard did not converge")
+
+
+def guarded_inputs(wl, device="cpu", parts=None):
+    """Inputs of workload `wl` with every token's top-k margin >= 1e-3."""
+    return guard(wl, S.make_inputs(wl, device, parts))
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return O.decode(t)
+
+
+def rel_frob(a: np.ndarray, b: np.ndarray) -> float:
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+def max_abs(a: np.ndarray, b: np.ndarray) -> float:
+    return float(np.abs(a - b).max()) if a.size else 0.0
+
+
+def assert_close_bf16(got: np.ndarray, ref: np.ndarray, what: str, rel=1e-2, mabs=2e-2):
+    rf, ma = rel_frob(got, ref), max_abs(got, ref)
+    assert rf <= rel and ma <= mabs, f"{what}: rel-Frobenius {rf:.3e} (<= {rel}), max-abs {ma:.3e} (<= {mabs})"

@@ -1,0 +1,118 @@
+"""The C-ABI library loads without a GPU, exports every entry point that
+include/moe.h declares, agrees with the header on struct layouts, and
+rejects bad arguments before launching anything."""
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+from oracle import moe_oracle as O
+
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def M():
+    import sparse_mixture_experts_sum_b300 as pkg
+    from sparse_mixture_experts_sum_b300 import build
+    build.build()
+    pkg.moe.lib()
+    return pkg
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(M):
+    names = declared_functions()
+    assert "moe_layer_fwd" in names and "moe_route" in names
+    lib = ctypes.CDLL(M.moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(M.moe.EXPORTS) <= set(names)
+
+
+def test_struct_layouts_match_header(M):
+    """Compile a C program against the header (gcc, no CUDA) that prints
+    sizeof/offsetof of the public structs; compare with the ctypes mirror."""
+    prog = r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "moe.h"
+int main(void) {
+  printf("%zu %zu %zu %zu\n", sizeof(moe_config), sizeof(moe_weights), sizeof(moe_saved), sizeof(moe_stats));
+  printf("%zu %zu %zu %zu\n", offsetof(moe_config, has_shared), offsetof(moe_stats, drop_rate),
+         offsetof(moe_stats, balance_stat), offsetof(moe_weights, expert_bias));
+  return 0;
+}'''
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(c, "w").write(prog)
+        subprocess.check_call(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), c, "-o", exe])
+        out = subprocess.check_output([exe], text=True).split()
+    m = M.moe
+    got = [ctypes.sizeof(m.MoeConfig), ctypes.sizeof(m.MoeWeights), ctypes.sizeof(m.MoeSaved),
+           ctypes.sizeof(m.MoeStats), m.MoeConfig.has_shared.offset, m.MoeStats.drop_rate.offset,
+           m.MoeStats.balance_stat.offset, m.MoeWeights.expert_bias.offset]
+    assert [int(v) for v in out] == got
+
+
+@pytest.mark.parametrize("T,k,E,cf,minc", [(1024, 2, 16, 1.0, 0), (4096, 2, 16, 1.0, 0), (16384, 2, 64, 1.25, 0),
+                                           (32768, 2, 16, 1.25, 0), (64, 2, 4, 0.0, 0), (10, 2, 16, 1.0, 4),
+                                           (1000, 3, 7, 1.1, 0), (333, 6, 384, 1.0, 0)])
+def test_capacity_matches_oracle(M, T, k, E, cf, minc):
+    cfg = M.make_config(T, 64, 64, E, k, capacity_factor=cf, min_capacity=minc)
+    assert M.moe_capacity(cfg) == O.expert_capacity(T, k, E, float(np.float32(cf)), minc)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=5, E=4), 1), (dict(k=9, E=16), 1), (dict(E=1025), 1), (dict(T=0), 1),
+    (dict(d=100), 2), (dict(h=36), 2), (dict(act=7), 1)])
+def test_bad_configs_rejected(M, kw, status):
+    base = dict(T=64, d=64, h=64, E=8, k=2)
+    base.update({k: v for k, v in kw.items() if k in base})
+    cfg = M.make_config(**base)
+    if "act" in kw:
+        cfg.act = kw["act"]
+    with pytest.raises(M.moe.MoeError) as ei:
+        M.moe_workspace_size(cfg)
+    assert ei.value.status == status
+
+
+def test_null_pointers_rejected_before_launch(M):
+    cfg = M.make_config(64, 64, 64, 8, 2)
+    lib = M.moe.lib()
+    st = lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None)
+    assert st == M.moe.MOE_ERR_INVALID_ARG
+    st = lib.moe_layer_fwd(ctypes.byref(cfg), None, None, None, None, None, None, None, 0, None)
+    assert st == M.moe.MOE_ERR_INVALID_ARG
+    st = lib.moe_expert_ffn(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, None, None)
+    assert st == M.moe.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_too_small_rejected(M):
+    cfg = M.make_config(64, 64, 64, 8, 2)
+    lib = M.moe.lib()
+    W = M.moe.MoeWeights(*([16] * 12))
+    st = lib.moe_layer_fwd(ctypes.byref(cfg), ctypes.byref(W), ctypes.c_void_p(16), None, ctypes.c_void_p(16),
+                           None, None, ctypes.c_void_p(256), 10, None)
+    assert st == M.moe.MOE_ERR_WORKSPACE
+
+
+def test_workspace_sizes(M):
+    cfg = M.make_config(16384, 4096, 14336, 64, 2, capacity_factor=1.25)
+    inf = M.moe_workspace_size(cfg, False)
+    tr = M.moe_workspace_size(cfg, True)
+    # inference keeps Xp, H, Yp in the workspace: at least T*k*(2d + h) bf16
+    assert inf >= 16384 * 2 * (2 * 4096 + 14336) * 2
+    assert tr < inf

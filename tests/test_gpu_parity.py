@@ -1,0 +1,304 @@
+"""Parity of the CUDA path (called through the C ABI) with the fp64 oracle.
+
+Routing, dispatch and counts must match bit for bit; routing weights within
+2e-6; outputs within max-abs 1e-4 for fp32 storage and within
+relative-Frobenius 1e-2 and max-abs 2e-2 for bf16 storage with fp32
+accumulation.  Inputs keep every token's top-k logit margins >= 1e-3
+(except the dedicated tie cases), so an fp32 router and an fp64 router
+order the experts identically.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import moe_synth as S
+import sparse_mixture_experts_sum_b300 as M
+from moe_testlib import assert_close_bf16, guard, guarded_inputs, max_abs, oracle_cfg, to_np
+from oracle import moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+WEIGHT_NAMES = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2", "expert_bias")
+
+
+def run_layer(wl, t):
+    cfg = M.config_of(wl)
+    sv = M.moe.alloc_saved(cfg)
+    y = torch.empty(wl.T, wl.d, dtype=M.moe.TORCH_DTYPE[wl.dtype], device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg, training=True)
+    M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], t.get("noise"), y, sv, st, ws)
+    assert M.moe_check_error(ws) == 0
+    return y, sv, M.moe.read_stats(st)
+
+
+def check_routing(r, sv, stats, x=None):
+    np.testing.assert_array_equal(sv["idx"].cpu().numpy(), r["idx"])
+    np.testing.assert_allclose(sv["w"].cpu().numpy(), r["w"], atol=2e-6, rtol=0)
+    np.testing.assert_array_equal(sv["counts"].cpu().numpy(), r["counts"])
+    np.testing.assert_array_equal(sv["kept"].cpu().numpy(), r["kept"])
+    np.testing.assert_array_equal(sv["offsets"].cpu().numpy(), r["offsets"])
+    np.testing.assert_array_equal(sv["pos"].cpu().numpy(), r["pos"])
+    ref = r["stats"]
+    for key in ("routed_slots", "kept_slots", "dropped_slots", "capacity", "numeric_error"):
+        assert stats[key] == ref[key], key
+    assert abs(stats["drop_rate"] - ref["drop_rate"]) <= 1e-15
+    assert abs(stats["balance_stat"] - ref["balance_stat"]) <= 1e-12 * max(1.0, abs(ref["balance_stat"]))
+    if x is not None:
+        # every kept slot's row is an exact copy of its token
+        pos = sv["pos"].long()
+        t_idx, j_idx = torch.nonzero(pos >= 0, as_tuple=True)
+        assert torch.equal(sv["Xp"][pos[t_idx, j_idx]], x[t_idx])
+
+
+def oracle_weights(t):
+    return {n: t.get(n) for n in WEIGHT_NAMES if t.get(n) is not None}
+
+
+# ---------------------------------------------------------------------------
+# full workloads
+# ---------------------------------------------------------------------------
+
+
+def test_tiny_fp32_layer():
+    wl = S.WORKLOADS["tiny_fp32"]
+    t = {n: v.to(DEV) for n, v in guarded_inputs(wl, "cpu").items()}
+    y, sv, st = run_layer(wl, t)
+    r = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"])
+    check_routing(r, sv, st, t["x"])
+    assert max_abs(to_np(y), r["y"]) <= 1e-4
+
+
+def test_small_prefill_layer():
+    wl = S.WORKLOADS["small_prefill"]
+    t = guarded_inputs(wl, DEV)
+    y, sv, st = run_layer(wl, t)
+    r = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"])
+    check_routing(r, sv, st, t["x"])
+    assert st["capacity"] == 512
+    assert_close_bf16(to_np(y), r["y"], "y")
+    # determinism: a second run gives the same bits
+    y2, sv2, _ = run_layer(wl, t)
+    assert torch.equal(y, y2) and torch.equal(sv["pos"], sv2["pos"])
+
+
+def _sample_tokens(r, experts, extra=16, seed=0):
+    """Tokens whose kept slots all go to `experts`, plus the tokens holding
+    each of those experts' last kept row, plus a few dropped slots."""
+    idx, pos = r["idx"], r["pos"]
+    ok = np.all((pos < 0) | np.isin(idx, experts), axis=1) & (pos >= 0).any(axis=1)
+    cand = np.nonzero(ok)[0]
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(cand, size=min(len(cand), 48), replace=False).tolist())
+    off = r["offsets"]
+    for e in experts:
+        if off[e + 1] > off[e]:
+            tt, _ = np.nonzero(pos == off[e + 1] - 1)
+            pick.add(int(tt[0]))
+    dropped = np.nonzero((pos < 0).any(axis=1) & ok)[0]
+    pick.update(dropped[:extra].tolist())
+    return np.array(sorted(pick))
+
+
+def _sampled_layer_check(wl, experts, seed):
+    t = guarded_inputs(wl, DEV)
+    y, sv, st = run_layer(wl, t)
+    r = O.route_and_dispatch(oracle_cfg(wl), t["x"], t["Wr"], t.get("expert_bias"), t.get("noise"))
+    check_routing(r, sv, st, t["x"])
+    toks = _sample_tokens(r, experts, seed=seed)
+    assert len(toks) >= 16
+    ro = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"], t.get("expert_bias"), t.get("noise"),
+                         tokens=toks)
+    assert_close_bf16(to_np(y[torch.as_tensor(toks, device=DEV)]), ro["y"], "y (sampled)")
+    return r, st
+
+
+@pytest.mark.slow
+def test_large_prefill_layer_sampled():
+    wl = S.WORKLOADS["large_prefill"]
+    r, st = _sampled_layer_check(wl, experts=[0, 1, 5, 17, 40, 63], seed=2)
+    assert st["capacity"] == 640
+    assert st["dropped_slots"] > 0  # the Zipf bias overfills the popular experts
+
+
+@pytest.mark.slow
+def test_decode_layer_sampled():
+    wl = S.WORKLOADS["decode"]
+    t = guarded_inputs(wl, DEV)
+    y, sv, st = run_layer(wl, t)
+    r = O.route_and_dispatch(oracle_cfg(wl), t["x"], t["Wr"])
+    check_routing(r, sv, st, t["x"])
+    assert st["dropped_slots"] == 0
+    toks = np.arange(0, 64, 4)
+    ro = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"], tokens=toks)
+    assert_close_bf16(to_np(y[torch.as_tensor(toks, device=DEV)]), ro["y"], "y (sampled)")
+
+
+@pytest.mark.slow
+def test_training_forward_sampled():
+    wl = S.WORKLOADS["training"]
+    r, st = _sampled_layer_check(wl, experts=[0, 3, 7, 12], seed=4)
+    assert st["capacity"] == 5120
+
+
+# ---------------------------------------------------------------------------
+# kernels in isolation, ragged shapes and edge cases
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu"])
+def test_expert_ffn_ragged_tiles(act):
+    """Per-expert row counts 0, 1, 130, 257, 37 (empty, single row, several
+    M tiles, ragged tails); d = 200 and h = 328 leave K and N tails."""
+    T, k, E, d, h = 300, 2, 5, 200, 328
+    rows = [0, 1, 130, 257, 37]
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    cfg = M.make_config(T, d, h, E, k, act, "bf16")
+    g = torch.Generator().manual_seed(5)
+    bf = torch.bfloat16
+    Xp = torch.randn(T * k, d, generator=g).to(bf).to(DEV)
+    W1 = (torch.randn(E, h, d, generator=g) / d ** 0.5).to(bf).to(DEV)
+    W3 = (torch.randn(E, h, d, generator=g) / d ** 0.5).to(bf).to(DEV)
+    W2 = (torch.randn(E, d, h, generator=g) / h ** 0.5).to(bf).to(DEV)
+    b1 = (torch.randn(E, h, generator=g) * 0.3).to(bf).to(DEV) if act == "gelu" else None
+    b2 = (torch.randn(E, d, generator=g) * 0.3).to(bf).to(DEV) if act == "gelu" else None
+    H = torch.full((T * k, h), 7.0, dtype=bf, device=DEV)
+    Yp = torch.full((T * k, d), 7.0, dtype=bf, device=DEV)
+    ws = M.moe.workspace(cfg)
+    offs = torch.as_tensor(off, device=DEV)
+    M.moe_expert_ffn(cfg, Xp, offs, W1, W3 if act == "swiglu" else None, b1, W2, b2, H, Yp, ws)
+    assert M.moe_check_error(ws) == 0
+    Xn = to_np(Xp)
+    Hn, Yn = to_np(H), to_np(Yp)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b == a:
+            continue
+        p = dict(W1=to_np(W1[e]), W2=to_np(W2[e]))
+        if act == "swiglu":
+            p["W3"] = to_np(W3[e])
+            Href = O.silu(Xn[a:b] @ p["W1"].T) * (Xn[a:b] @ p["W3"].T)
+        else:
+            p["b1"], p["b2"] = to_np(b1[e]), to_np(b2[e])
+            Href = O.gelu(Xn[a:b] @ p["W1"].T + p["b1"])
+        assert_close_bf16(Hn[a:b], Href, f"H expert {e}")
+        assert_close_bf16(Yn[a:b], O.expert_ffn(Xn[a:b], act, **p), f"Yp expert {e}")
+    # rows past offsets[E] are never written
+    assert (Hn[off[-1]:] == 7.0).all() and (Yn[off[-1]:] == 7.0).all()
+
+
+def test_combine_worked_example_on_gpu():
+    """[P5] worked example: 0.75*[0.8,0.2,-0.4] + 0.25*[0.4,0.6,0.8] = [0.7,0.3,-0.1]."""
+    cfg = M.make_config(1, 4, 8, 4, 2, "gelu", "f32")
+    Yp = torch.tensor([[0.8, 0.2, -0.4, 0.0], [0.4, 0.6, 0.8, 0.0]], device=DEV)
+    pos = torch.tensor([[0, 1]], dtype=torch.int32, device=DEV)
+    w = torch.tensor([[0.75, 0.25]], device=DEV)
+    y = torch.empty(1, 4, device=DEV)
+    M.moe_combine(cfg, Yp, pos, w, None, y)
+    np.testing.assert_allclose(y.cpu().numpy()[0, :3], [0.7, 0.3, -0.1], atol=1e-7)
+    # a dropped slot adds nothing and the kept weight is not renormalised
+    pos2 = torch.tensor([[0, -1]], dtype=torch.int32, device=DEV)
+    M.moe_combine(cfg, Yp, pos2, w, None, y)
+    np.testing.assert_allclose(y.cpu().numpy()[0, :3], [0.6, 0.15, -0.3], atol=1e-7)
+
+
+def test_ties_and_nonfinite_tokens():
+    """All-zero router: every logit ties -> experts (0,1), weights (1/2,1/2).
+    A token with a NaN input routes nowhere and is counted."""
+    wl = S.WORKLOADS["tiny_fp32"].replace(T=40, dtype="bf16", act="swiglu", d=64, h=64, E=8)
+    t = S.make_inputs(wl, DEV)
+    t["Wr"].zero_()
+    t["x"][7, 3] = float("nan")
+    y, sv, st = run_layer(wl, t)
+    idx = sv["idx"].cpu().numpy()
+    w = sv["w"].cpu().numpy()
+    good = np.arange(40) != 7
+    assert (idx[good] == [0, 1]).all() and (w[good] == 0.5).all()
+    assert (idx[7] == -1).all() and (w[7] == 0).all()
+    assert st["numeric_error"] == 1 and st["routed_slots"] == 78
+    r = O.route_and_dispatch(oracle_cfg(wl), t["x"], t["Wr"])
+    check_routing(r, sv, st)
+
+
+@pytest.mark.parametrize("T,d,E,k", [(1000, 520, 300, 8), (77, 64, 3, 1), (130, 136, 130, 4)])
+def test_route_shapes(T, d, E, k):
+    """Expert chunks beyond 128, odd expert counts, k from 1 to 8, token and
+    d tails against the 64-token / 64-wide tiles."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=T, d=d, E=E, k=k, seed=11)
+    t = guarded_inputs(wl, "cpu", parts=["x", "Wr"])
+    cfg = M.config_of(wl)
+    x, Wr = t["x"].to(DEV), t["Wr"].to(DEV)
+    idx = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, device=DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    M.moe_route(cfg, x, Wr, None, None, idx, w, counts)
+    l = O.router_logits(t["x"], t["Wr"])
+    ridx, rw, _ = O.top_k_route(l, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, atol=2e-6, rtol=0)
+    np.testing.assert_array_equal(counts.cpu().numpy(), O.usage_counts(ridx, E))
+
+
+@pytest.mark.parametrize("T,E,k,cf,minc", [(3000, 6, 3, 0.5, 0), (513, 5, 2, 0.1, 40), (9000, 16, 2, 1.0, 0)])
+def test_dispatch_capacity_exact(T, E, k, cf, minc):
+    """Capacity binds hard (skewed router bias); positions must equal the
+    oracle's slot-major queue exactly, across several 4096-slot chunks."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=T, d=64, h=64, E=E, k=k, capacity_factor=cf,
+                                              min_capacity=minc, seed=13)
+    t = S.make_inputs(wl, "cpu", parts=["x", "Wr"])
+    bias = torch.linspace(1.5, 0.0, E, dtype=torch.float32)
+    t["expert_bias"] = bias
+    t = guard(wl, t)
+    cfg = M.config_of(wl)
+    x, Wr, eb = t["x"].to(DEV), t["Wr"].to(DEV), bias.to(DEV)
+    idx = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, device=DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    M.moe_route(cfg, x, Wr, eb, None, idx, w, counts)
+    kept = torch.empty(E, dtype=torch.int32, device=DEV)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    pos = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    Xp = torch.empty(T * k, 64, dtype=torch.bfloat16, device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg)
+    M.moe_dispatch(cfg, idx, x, kept, offs, pos, Xp, st, ws)
+    r = O.route_and_dispatch(oracle_cfg(wl), t["x"], t["Wr"], bias)
+    sv = dict(idx=idx, w=w, counts=counts, kept=kept, offsets=offs, pos=pos, Xp=Xp)
+    stats = M.moe.read_stats(st)
+    check_routing(r, sv, stats, x)
+    assert stats["dropped_slots"] > 0
+    if minc:
+        assert stats["capacity"] == minc
+
+
+def test_gelu_bf16_layer_with_biases_and_shared():
+    """GeLU experts with nonzero biases plus a GeLU shared expert, bf16."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=200, d=128, h=192, E=6, act="gelu", has_shared=True,
+                                              capacity_factor=1.0, seed=21)
+    t = guarded_inputs(wl, "cpu")
+    g = torch.Generator().manual_seed(3)
+    bf = torch.bfloat16
+    t["b1"] = (torch.randn(6, 192, generator=g) * 0.2).to(bf)
+    t["b2"] = (torch.randn(6, 128, generator=g) * 0.2).to(bf)
+    t["bs1"] = (torch.randn(192, generator=g) * 0.2).to(bf)
+    t["bs2"] = (torch.randn(128, generator=g) * 0.2).to(bf)
+    t = {n: v.to(DEV) for n, v in t.items()}
+    y, sv, st = run_layer(wl, t)
+    r = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"])
+    check_routing(r, sv, st, t["x"])
+    assert_close_bf16(to_np(y), r["y"], "y")
+
+
+def test_inference_workspace_path_matches_training_path():
+    """saved == NULL keeps every intermediate in the workspace; the output is
+    the same bits as with caller-owned saved buffers."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=300, d=256, h=256, E=8, has_shared=True, seed=23)
+    t = guarded_inputs(wl, DEV)
+    y, _, _ = run_layer(wl, t)
+    cfg = M.config_of(wl)
+    y2 = torch.empty_like(y)
+    ws = M.moe.workspace(cfg, training=False)
+    M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], None, y2, None, None, ws)
+    assert M.moe_check_error(ws) == 0
+    assert torch.equal(y, y2)
