@@ -1,0 +1,437 @@
+"""Benchmark of the sparse-MoE layer forward on B300 (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload large_prefill] [--no-decode] [--no-cpu-baseline]
+
+A step is one forward of the whole layer (router -> top-k -> capacity
+dispatch -> grouped expert FFNs (+ shared expert) -> combine -> statistics)
+over one batch of the workload, through the public C ABI (moe_layer_fwd),
+inputs and weights already resident in HBM.  The headline workload is the
+E=64 top-2 bf16 prefill layer (T=16384, d=4096, SwiGLU h=14336, capacity
+factor 1.25, Zipf(1.1) logit bias); its weights (22.5 GB) and activations are
+far larger than the 126 MB L2, so no flush is needed between steps.
+
+Multi-GPU: the layer does not shard in this build; with torchrun every rank
+runs an independent replica ("replicas only"), value = all ranks' tokens /
+the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the checker) on the host cores
+on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at E=64 top-2 bf16; grouped-GEMM % peak; decode % HBM BW"
+WEIGHTS = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2", "expert_bias")
+# our kernel launches per forward: route 1, dispatch 4, GEMMs 2 (+2 shared), combine 1
+LAUNCHES_PER_STEP = 8
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+
+def expert_ffn_flops(wl, kept):
+    return 2.0 * kept * wl.d * wl.h * (3 if wl.act == "swiglu" else 2)
+
+
+def shared_flops(wl):
+    return 2.0 * wl.T * wl.d * wl.h * (3 if wl.act == "swiglu" else 2) if wl.has_shared else 0.0
+
+
+def run_gpu(args, wl_name, world, rank, local, main=True):
+    import torch
+    import moe_synth as S
+    import sparse_mixture_experts_sum_b300 as M
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = S.WORKLOADS[wl_name]
+    t = S.make_inputs(wl, dev)
+    cfg = M.config_of(wl)
+    weights = {n: t.get(n) for n in WEIGHTS}
+    x, noise = t["x"], t.get("noise")
+    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=dev)
+    st = M.moe.stats_buffer(dev)
+    saved = M.moe.alloc_saved(cfg, dev)
+    ws = M.moe.workspace(cfg, training=True, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        M.moe_layer_fwd(cfg, weights, x, noise, y, saved, st, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert M.moe_check_error(ws) == 0, "a kernel gave up a bounded wait"
+    stats = M.moe.read_stats(st)
+    kept = stats["kept_slots"]
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    # --- timed region: K forwards back to back ---
+    sampler = ClockSampler(local)
+    with sampler:
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    ms_total = e0.elapsed_time(e1)
+    clocks = sampler.summary()
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+
+    # --- per-component breakdown (same work, component entry points, events between) ---
+    comp = {"route": 0.0, "dispatch": 0.0, "expert_ffn": 0.0, "shared_ffn": 0.0, "combine": 0.0}
+    ws_b = M.moe.workspace(cfg, training=True, device=dev)
+    Hs = torch.empty(wl.T, wl.h, dtype=torch.bfloat16, device=dev) if wl.has_shared else None
+    sh_off = torch.tensor([0, wl.T], dtype=torch.int32, device=dev)
+    sh_cfg = M.make_config(wl.T, wl.d, wl.h, 1, 1, wl.act, wl.dtype)
+    ws_sh = M.moe.workspace(sh_cfg, device=dev) if wl.has_shared else None
+    sv = saved
+    reps = max(3, min(args.steps, 10))
+    for rep in range(reps + 1):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        ev[0].record(stream)
+        M.moe_route(cfg, x, weights["Wr"], weights.get("expert_bias"), noise, sv["idx"], sv["w"], sv["counts"])
+        ev[1].record(stream)
+        M.moe_dispatch(cfg, sv["idx"], x, sv["kept"], sv["offsets"], sv["pos"], sv["Xp"], st, ws_b)
+        ev[2].record(stream)
+        M.moe_expert_ffn(cfg, sv["Xp"], sv["offsets"], weights["W1"], weights.get("W3"), weights.get("b1"),
+                         weights["W2"], weights.get("b2"), sv["H"], sv["Yp"], ws_b)
+        ev[3].record(stream)
+        if wl.has_shared:
+            M.moe_expert_ffn(sh_cfg, x, sh_off, weights["Ws1"], weights.get("Ws3"), weights.get("bs1"),
+                             weights["Ws2"], weights.get("bs2"), Hs, sv["Sx"], ws_sh)
+        ev[4].record(stream)
+        M.moe_combine(cfg, sv["Yp"], sv["pos"], sv["w"], sv.get("Sx"), y)
+        ev[5].record(stream)
+        torch.cuda.synchronize(dev)
+        if rep == 0:
+            continue  # warm-up pass of the instrumented sequence
+        for i, name in enumerate(comp):
+            comp[name] += ev[i].elapsed_time(ev[i + 1]) / reps
+    assert M.moe_check_error(ws_b) == 0
+
+    peaks = load_peaks()
+    tokens = wl.T * world
+    out = {
+        "ms_per_step": ms_step,
+        "tokens_per_s": tokens / (ms_step * 1e-3),
+        "stats": stats,
+        "components_ms": comp,
+        "clocks": clocks,
+        "wl": wl,
+    }
+    gemm_flops = expert_ffn_flops(wl, kept)
+    gemm_ms = comp["expert_ffn"]
+    out["gemm"] = {"flops": gemm_flops, "ms": gemm_ms, "tflops": gemm_flops / (gemm_ms * 1e-3) / 1e12}
+    # touched expert weights (bytes): experts with >= 1 kept row, plus the shared expert
+    kept_per_e = saved["kept"].cpu()
+    n_touched = int((kept_per_e > 0).sum().item())
+    per_expert_bytes = wl.d * wl.h * (3 if wl.act == "swiglu" else 2) * 2
+    out["touched_weight_bytes"] = (n_touched + (1 if wl.has_shared else 0)) * per_expert_bytes
+    out["n_touched"] = n_touched
+
+    # --- e2e: pinned host input -> device, forward, device -> pinned host output ---
+    xh = x.cpu().pin_memory()
+    yh = torch.empty(wl.T, wl.d, dtype=torch.bfloat16).pin_memory()
+    nh = noise.cpu().pin_memory() if noise is not None else None
+    xd = torch.empty_like(x)
+    nd = torch.empty_like(noise) if noise is not None else None
+    for _ in range(2):
+        xd.copy_(xh, non_blocking=True)
+        M.moe_layer_fwd(cfg, weights, xd, nd, y, saved, st, ws)
+        yh.copy_(y, non_blocking=True)
+    barrier()
+    e2e0, e2e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e0.record(stream)
+    for _ in range(args.steps):
+        xd.copy_(xh, non_blocking=True)
+        if nh is not None:
+            nd.copy_(nh, non_blocking=True)
+        M.moe_layer_fwd(cfg, weights, xd, nd, y, saved, st, ws)
+        yh.copy_(y, non_blocking=True)
+    e2e1.record(stream)
+    barrier()
+    e2e_ms = e2e0.elapsed_time(e2e1) / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = xh.numel() * xh.element_size() + (nh.numel() * nh.element_size() if nh is not None else 0)
+    out["e2e"] = {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": yh.numel() * yh.element_size()}
+    out["peaks"] = peaks
+    out["tensors"] = dict(t=t, saved=saved)
+    return out
+
+
+def cpu_baseline(wl_name, gpu_tensors=None, max_rows=None, budget_s=20.0):
+    """fp64 oracle on the host cores, on a bounded sample of the workload:
+    router, top-k, capacity and dispatch of the whole batch, then the expert
+    FFN of the kept rows of the two busiest experts (at most `max_rows` rows,
+    stopping after `budget_s`).  Whole-layer tokens/s is extrapolated per
+    token: routing share + (expert rows per token) x (measured cost per row).
+    Inputs come from the GPU run when given (the oracle copies only the
+    expert slices it reads); otherwise a 2048-token batch and the two
+    experts' weight slices are drawn on the host."""
+    import numpy as np
+    import torch
+    import moe_synth as S
+    from oracle import moe_oracle as O
+
+    wl = S.WORKLOADS[wl_name]
+    if gpu_tensors is not None:
+        t = gpu_tensors
+        T = wl.T
+    else:
+        T = min(wl.T, 2048)
+        t = S.make_inputs(wl.replace(T=T), "cpu", parts=["x", "Wr", "expert_bias", "noise"])
+    cfg = dict(T=T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act,
+               capacity_factor=float(np.float32(wl.capacity_factor)), min_capacity=wl.min_capacity,
+               lam=float(np.float32(wl.lam)), has_shared=wl.has_shared)
+    t0 = time.perf_counter()
+    r = O.route_and_dispatch(cfg, t["x"], t["Wr"], t.get("expert_bias"), t.get("noise"))
+    t_route = time.perf_counter() - t0
+    experts = [int(e) for e in np.argsort(-r["kept"], kind="stable")[:2]]
+    if gpu_tensors is not None:
+        weights = {n: t[n] for n in ("W1", "W3", "W2", "b1", "b2") if t.get(n) is not None}
+    else:
+        weights = {}
+        dt, d, h = wl.dtype, wl.d, wl.h
+        for name, (rows, cols, fan) in dict(W1=(h, d, d), W3=(h, d, d), W2=(d, h, h)).items():
+            if name == "W3" and wl.act != "swiglu":
+                continue
+            weights[name] = {e: S.tensor("normal", wl.seed, S.TID[name], (rows, cols), dt, wl.std(fan),
+                                         "cpu", start=e * rows * cols) for e in experts}
+    X = None
+    slots = 0
+    t1 = time.perf_counter()
+    for e in experts:
+        rows, _ = np.nonzero((r["idx"] == e) & (r["pos"] >= 0))
+        if max_rows is not None:
+            rows = rows[:max_rows]
+        src = t["x"][torch.as_tensor(rows, device=t["x"].device)] if rows.size else t["x"][:0]
+        p = O.expert_params(weights, e, wl.act)
+        O.expert_ffn(O.decode(src), wl.act, **p)
+        slots += rows.size
+        if time.perf_counter() - t1 > budget_s:
+            break
+    t_ffn = time.perf_counter() - t1
+    per_row = t_ffn / max(slots, 1)
+    rows_per_token = float(r["kept"].sum()) / T + (1 if wl.has_shared else 0)
+    per_token = t_route / T + per_row * rows_per_token
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        cores = os.cpu_count() or 1
+    return {"value": 1.0 / per_token, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 numpy oracle: router+top-k+capacity+dispatch of all {T} tokens ({t_route:.2f} s), "
+                      f"expert FFN of {slots} kept rows of experts {experts} ({t_ffn:.2f} s); whole-layer "
+                      f"tokens/s extrapolated per token at {rows_per_token:.3f} expert rows/token"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="large_prefill")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import torch
+        dev_ok = torch.cuda.is_available()
+        t0 = time.time()
+        vals = []
+        cb = None
+        gt = None
+        if dev_ok:
+            import moe_synth as S
+            torch.cuda.set_device(local)
+            gt = S.make_inputs(S.WORKLOADS[args.workload], torch.device("cuda", local))
+        for i in range(args.warmup + args.steps):
+            cb = cpu_baseline(args.workload, gt, max_rows=128, budget_s=max(1.0, 60.0 / (args.steps + args.warmup)))
+            if i >= args.warmup:
+                vals.append(cb["value"])
+        v = statistics.median(vals)
+        cb["value"] = v
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+                          "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": args.workload}, "cpu_baseline": cb,
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0},
+                          "wall_s": time.time() - t0}))
+        return 0
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    r = run_gpu(args, args.workload, world, rank, local)
+    wl = r["wl"]
+    peaks = r["peaks"]
+    gemm = r["gemm"]
+    peak = peaks["bf16_sus"]
+    line = {
+        "metric": METRIC,
+        "value": r["tokens_per_s"],
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name}: T={wl.T} d={wl.d} h={wl.h} E={wl.E} top-{wl.k} {wl.act} "
+                               f"cf={wl.capacity_factor} zipf_bias={wl.zipf_s} {wl.dtype}",
+                   "global_batch_tokens": wl.T * world, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (weights 22.5 GB, x 134 MB), no flush"},
+        "roofline": {"bound": "tensor", "achieved": gemm["tflops"], "peak": peak, "unit": "TFLOP/s",
+                     "frac": gemm["tflops"] / peak, "traffic": None,
+                     "kernel": "grouped_gemm_tc_kernel (GEMM-1 SwiGLU + GEMM-2, one moe_expert_ffn call)",
+                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "frac_of_burst": gemm["tflops"] / peaks["bf16"]},
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "components_ms": {k: round(v, 4) for k, v in r["components_ms"].items()},
+        "layer_stats": {k: r["stats"][k] for k in ("kept_slots", "dropped_slots", "capacity", "drop_rate",
+                                                    "balance_stat")},
+    }
+    # whole-layer roofline: max(flops / tensor peak, bytes / HBM) vs measured step time
+    flops = gemm["flops"] + 2.0 * wl.T * wl.d * wl.E
+    bytes_ = r["touched_weight_bytes"] + 2 * wl.T * wl.d * 2
+    t_roof = max(flops / (peak * 1e12), bytes_ / (peaks["hbm_gbs"] * 1e9))
+    line["layer_roofline_frac"] = t_roof / (r["ms_per_step"] * 1e-3)
+
+    del r["tensors"]
+    if not args.no_decode:
+        d = run_gpu(args, "decode", world, rank, local)
+        dwl = d["wl"]
+        ffn_ms = d["components_ms"]["expert_ffn"] + d["components_ms"]["shared_ffn"]
+        gbs = d["touched_weight_bytes"] / (ffn_ms * 1e-3) / 1e9
+        line["decode"] = {"workload": f"decode: T={dwl.T} d={dwl.d} h={dwl.h} E={dwl.E}+1 shared top-{dwl.k}",
+                          "ms_per_step": d["ms_per_step"], "tokens_per_s": d["tokens_per_s"],
+                          "touched_experts": d["n_touched"] + 1,
+                          "touched_weight_gb": d["touched_weight_bytes"] / 1e9,
+                          "expert_ffn_ms": ffn_ms, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+                          "layer_hbm_frac": d["touched_weight_bytes"] / (d["ms_per_step"] * 1e-3) / 1e9
+                          / peaks["hbm_gbs"],
+                          "components_ms": {k: round(v, 4) for k, v in d["components_ms"].items()},
+                          "clocks": d["clocks"]}
+        del d["tensors"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import moe_synth as S
+        gt = S.make_inputs(S.WORKLOADS[args.workload], torch.device("cuda", local))
+        line["cpu_baseline"] = cpu_baseline(args.workload, gt)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
