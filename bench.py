@@ -5,8 +5,13 @@
 
 A step is one forward of the whole layer (router -> top-k -> capacity
 dispatch -> grouped expert FFNs (+ shared expert) -> combine -> statistics)
-over one batch of the workload, through the public C ABI (moe_layer_fwd),
-inputs and weights already resident in HBM.  The headline workload is the
+over one batch of the workload, through the public C ABI: the timed steps
+call the stage entry points (moe_route, moe_dispatch, moe_expert_ffn,
+moe_combine) in the order moe_layer_fwd runs them, with a CUDA event after
+every stage, so that each kernel's share of the timed region is measured on
+its own stream; the single-call moe_layer_fwd is timed beside it as a
+cross-check, and end to end (pinned host input in, output back to the host)
+as `e2e`.  Inputs and weights are resident in HBM.  The headline workload is the
 E=64 top-2 bf16 prefill layer (T=16384, d=4096, SwiGLU h=14336, capacity
 factor 1.25, Zipf(1.1) logit bias); its weights (22.5 GB) and activations are
 far larger than the 126 MB L2, so no flush is needed between steps.
@@ -36,8 +41,14 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s at E=64 top-2 bf16; grouped-GEMM % peak; decode % HBM BW"
 WEIGHTS = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2", "expert_bias")
-# our kernel launches per forward: route 1, dispatch 4, GEMMs 2 (+2 shared), combine 1
-LAUNCHES_PER_STEP = 8
+# dram bytes (read + write) per grouped_gemm_tc_kernel launch at the large
+# prefill shapes, from an ncu capture of the four-expert slice scaled by the
+# kept rows, keyed by the sha256 of the kernel source it was taken on (the
+# figure is reported only while the source is unchanged)
+GEMM_TRAFFIC = {
+    # profiles/grouped_gemm_large_prefill_slice.md
+    "eb278a83fa9c4a2ae4fb389792258663da7717e1e94350276120610a3986202a": 12.55e9,
+}
 
 
 def load_peaks():
@@ -52,7 +63,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """nvidia-smi clock / throttle samples every 100 ms while running."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -67,7 +78,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -97,6 +108,16 @@ class ClockSampler:
         reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(self.rows)}
+
+
+def gemm_traffic():
+    import hashlib
+    src = os.path.join(ROOT, "sparse_mixture_experts_sum_b300", "csrc", "gemm_tc.cu")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return GEMM_TRAFFIC.get(h)
 
 
 def dist_setup():
@@ -137,8 +158,31 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     ws = M.moe.workspace(cfg, training=True, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    Hs = torch.empty(wl.T, wl.h, dtype=torch.bfloat16, device=dev) if wl.has_shared else None
+    sh_off = torch.tensor([0, wl.T], dtype=torch.int32, device=dev)
+    sh_cfg = M.make_config(wl.T, wl.d, wl.h, 1, 1, wl.act, wl.dtype)
+    ws_sh = M.moe.workspace(sh_cfg, device=dev) if wl.has_shared else None
+    sv = saved
+
+    # one step = the layer's C-ABI stages in the order moe_layer_fwd runs them
+    stages = [
+        ("route", lambda: M.moe_route(cfg, x, weights["Wr"], weights.get("expert_bias"), noise, sv["idx"], sv["w"],
+                                      sv["counts"])),
+        ("dispatch", lambda: M.moe_dispatch(cfg, sv["idx"], x, sv["kept"], sv["offsets"], sv["pos"], sv["Xp"], st,
+                                            ws)),
+        ("expert_ffn", lambda: M.moe_expert_ffn(cfg, sv["Xp"], sv["offsets"], weights["W1"], weights.get("W3"),
+                                                weights.get("b1"), weights["W2"], weights.get("b2"), sv["H"],
+                                                sv["Yp"], ws)),
+    ]
+    if wl.has_shared:
+        stages.append(("shared_ffn", lambda: M.moe_expert_ffn(sh_cfg, x, sh_off, weights["Ws1"], weights.get("Ws3"),
+                                                              weights.get("bs1"), weights["Ws2"],
+                                                              weights.get("bs2"), Hs, sv["Sx"], ws_sh)))
+    stages.append(("combine", lambda: M.moe_combine(cfg, sv["Yp"], sv["pos"], sv["w"], sv.get("Sx"), y)))
+
     def step():
-        M.moe_layer_fwd(cfg, weights, x, noise, y, saved, st, ws)
+        for _, fn in stages:
+            fn()
 
     for _ in range(args.warmup):
         step()
@@ -152,60 +196,51 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    # --- timed region: K forwards back to back ---
+    # --- timed region: K steps back to back, an event after every stage ---
+    steps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages))] for _ in range(steps)]
     sampler = ClockSampler(local)
     with sampler:
         barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
+        for i in range(steps):
+            for j, (_, fn) in enumerate(stages):
+                fn()
+                evs[i][j].record(stream)
         barrier()
-    ms_total = e0.elapsed_time(e1)
+    ms_total = e0.elapsed_time(evs[-1][-1])
     clocks = sampler.summary()
+    comp = {name: 0.0 for name, _ in stages}
+    prev = e0
+    for i in range(steps):
+        for j, (name, _) in enumerate(stages):
+            comp[name] += prev.elapsed_time(evs[i][j]) / steps
+            prev = evs[i][j]
     if world > 1:
         tt = torch.tensor([ms_total], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         ms_total = float(tt.item())
-    ms_step = ms_total / args.steps
+    ms_step = ms_total / steps
+    assert M.moe_check_error(ws) == 0, "a kernel gave up a bounded wait"
 
-    # --- per-component breakdown (same work, component entry points, events between) ---
-    comp = {"route": 0.0, "dispatch": 0.0, "expert_ffn": 0.0, "shared_ffn": 0.0, "combine": 0.0}
-    ws_b = M.moe.workspace(cfg, training=True, device=dev)
-    Hs = torch.empty(wl.T, wl.h, dtype=torch.bfloat16, device=dev) if wl.has_shared else None
-    sh_off = torch.tensor([0, wl.T], dtype=torch.int32, device=dev)
-    sh_cfg = M.make_config(wl.T, wl.d, wl.h, 1, 1, wl.act, wl.dtype)
-    ws_sh = M.moe.workspace(sh_cfg, device=dev) if wl.has_shared else None
-    sv = saved
-    reps = max(3, min(args.steps, 10))
-    for rep in range(reps + 1):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-        ev[0].record(stream)
-        M.moe_route(cfg, x, weights["Wr"], weights.get("expert_bias"), noise, sv["idx"], sv["w"], sv["counts"])
-        ev[1].record(stream)
-        M.moe_dispatch(cfg, sv["idx"], x, sv["kept"], sv["offsets"], sv["pos"], sv["Xp"], st, ws_b)
-        ev[2].record(stream)
-        M.moe_expert_ffn(cfg, sv["Xp"], sv["offsets"], weights["W1"], weights.get("W3"), weights.get("b1"),
-                         weights["W2"], weights.get("b2"), sv["H"], sv["Yp"], ws_b)
-        ev[3].record(stream)
-        if wl.has_shared:
-            M.moe_expert_ffn(sh_cfg, x, sh_off, weights["Ws1"], weights.get("Ws3"), weights.get("bs1"),
-                             weights["Ws2"], weights.get("bs2"), Hs, sv["Sx"], ws_sh)
-        ev[4].record(stream)
-        M.moe_combine(cfg, sv["Yp"], sv["pos"], sv["w"], sv.get("Sx"), y)
-        ev[5].record(stream)
-        torch.cuda.synchronize(dev)
-        if rep == 0:
-            continue  # warm-up pass of the instrumented sequence
-        for i, name in enumerate(comp):
-            comp[name] += ev[i].elapsed_time(ev[i + 1]) / reps
-    assert M.moe_check_error(ws_b) == 0
+    # --- cross-check: the same forward through the single moe_layer_fwd call ---
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(steps):
+        M.moe_layer_fwd(cfg, weights, x, noise, y, saved, st, ws)
+    f1.record(stream)
+    barrier()
+    layer_fwd_ms = f0.elapsed_time(f1) / steps
+    assert M.moe_check_error(ws) == 0
 
     peaks = load_peaks()
     tokens = wl.T * world
     out = {
         "ms_per_step": ms_step,
+        "layer_fwd_ms": layer_fwd_ms,
+        "launches_per_step": 8 + (2 if wl.has_shared else 0),
         "tokens_per_s": tokens / (ms_step * 1e-3),
         "stats": stats,
         "components_ms": comp,
@@ -221,6 +256,7 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     per_expert_bytes = wl.d * wl.h * (3 if wl.act == "swiglu" else 2) * 2
     out["touched_weight_bytes"] = (n_touched + (1 if wl.has_shared else 0)) * per_expert_bytes
     out["n_touched"] = n_touched
+    out["weight_bytes"] = wl.E * per_expert_bytes
 
     # --- e2e: pinned host input -> device, forward, device -> pinned host output ---
     xh = x.cpu().pin_memory()
@@ -325,7 +361,7 @@ def cpu_baseline(wl_name, gpu_tensors=None, max_rows=None, budget_s=20.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large_prefill")
@@ -379,6 +415,7 @@ def main():
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": r["ms_per_step"],
+        "layer_fwd_ms": r["layer_fwd_ms"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -387,15 +424,16 @@ def main():
         "config": {"workload": f"{wl.name}: T={wl.T} d={wl.d} h={wl.h} E={wl.E} top-{wl.k} {wl.act} "
                                f"cf={wl.capacity_factor} zipf_bias={wl.zipf_s} {wl.dtype}",
                    "global_batch_tokens": wl.T * world, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (weights 22.5 GB, x 134 MB), no flush"},
+                   "l2": f"inputs larger than L2 (expert weights {r['weight_bytes'] / 1e9:.2f} GB, "
+                         f"x {wl.T * wl.d * 2 / 1e6:.0f} MB vs 126 MB L2), no flush"},
         "roofline": {"bound": "tensor", "achieved": gemm["tflops"], "peak": peak, "unit": "TFLOP/s",
-                     "frac": gemm["tflops"] / peak, "traffic": None,
+                     "frac": gemm["tflops"] / peak, "traffic": gemm_traffic(),
                      "kernel": "grouped_gemm_tc_kernel (GEMM-1 SwiGLU + GEMM-2, one moe_expert_ffn call)",
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
                      "frac_of_burst": gemm["tflops"] / peaks["bf16"]},
         "clocks": r["clocks"],
         "e2e": r["e2e"],
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": r["launches_per_step"] * args.steps,
         "components_ms": {k: round(v, 4) for k, v in r["components_ms"].items()},
         "layer_stats": {k: r["stats"][k] for k in ("kept_slots", "dropped_slots", "capacity", "drop_rate",
                                                     "balance_stat")},
@@ -408,7 +446,9 @@ def main():
 
     del r["tensors"]
     if not args.no_decode:
-        d = run_gpu(args, "decode", world, rank, local)
+        dargs = argparse.Namespace(**vars(args))
+        dargs.steps = max(args.steps, 100)  # >= 0.25 s timed, so the clock sampler sees it
+        d = run_gpu(dargs, "decode", world, rank, local)
         dwl = d["wl"]
         ffn_ms = d["components_ms"]["expert_ffn"] + d["components_ms"]["shared_ffn"]
         gbs = d["touched_weight_bytes"] / (ffn_ms * 1e-3) / 1e9

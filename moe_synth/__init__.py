@@ -190,6 +190,10 @@ WORKLOADS: Dict[str, Workload] = {
     # T=16384, d=4096, E=64, SwiGLU h=14336, cf=1.25 (C=640), Zipf(1.1) logit bias
     "large_prefill": Workload("large_prefill", 16384, 4096, 14336, 64, 2, "swiglu", "bf16",
                               1.25, 0, 0.01, False, 2, None, 1.1, False, False),
+    # four experts of the large prefill layer at its rows per expert (~512):
+    # the same GEMM tile shapes at 1/16 of the device memory (profiling case)
+    "large_prefill_slice": Workload("large_prefill_slice", 1024, 4096, 14336, 4, 2, "swiglu", "bf16",
+                                    1.25, 0, 0.01, False, 2, None, 1.1, False, False),
     # T=64, d=4096, E=128 routed + 1 shared, SwiGLU h=8192, no capacity limit
     "decode": Workload("decode", 64, 4096, 8192, 128, 2, "swiglu", "bf16", 0.0, 0, 0.01,
                        True, 3, None, None, False, False),
