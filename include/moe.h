@@ -23,7 +23,8 @@
  * Conventions (every entry point):
  *  - Ownership: the caller allocates every buffer, the workspace included.
  *    The library never allocates or frees device memory and keeps no state
- *    between calls, apart from a per-process cache of driver entry points.
+ *    between calls, apart from a per-process cache of driver entry points
+ *    and the fixed scratch array behind moe_dispatch_static.
  *  - Pointers: device pointers unless stated, 16-byte aligned.  Tensors are
  *    dense row-major.  Storage type = cfg->dtype (fp32 or bf16) for
  *    activations and weights; routing weights, noise, the expert bias and
@@ -159,6 +160,30 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr,
 moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x,
                         int* kept, int* offsets, int* pos, void* Xp,
                         moe_stats* stats, void* ws, moe_stream_t stream);
+
+/* moe_dispatch without a workspace argument.  The pages have no counterpart
+ * of this call: it exists for callers that cannot allocate device memory
+ * at the point where they dispatch -- for example a plugin or custom-op
+ * host that hands an operator only its input and output buffers, or a
+ * serving loop that reserves all of its device memory up front and forbids
+ * cudaMalloc afterwards.  Same arguments, results and rules as moe_dispatch
+ * (kept, offsets, pos, Xp, stats are bit-identical), minus `ws`.
+ *   Scratch: a fixed array of 2,098,432 bytes inside this library, which
+ *   every GPU that loads the library holds until the process exits.  A
+ *   call whose scratch need exceeds it returns MOE_ERR_UNSUPPORTED before
+ *   any launch; every T*k <= 2^20 (1,048,576 slots) fits at any E <= 1024.
+ *   Allocation: none -- no cudaMalloc, cudaFree or allocating library call.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, device current); make that first call before
+ *   any stream capture.
+ *   Sharing: all calls on a device share the one array and it keeps the
+ *   last call's contents; nothing in it has to start at zero (each call
+ *   writes every word it later reads).  Calls whose work overlaps on the
+ *   GPU -- on different streams, or from different host threads -- race
+ *   on it: order them on one stream or with events. */
+moe_status moe_dispatch_static(const moe_config* cfg, const int* idx, const void* x,
+                               int* kept, int* offsets, int* pos, void* Xp,
+                               moe_stats* stats, moe_stream_t stream);
 
 /* Grouped expert FFN over expert-contiguous rows ([P2] 4.2 and [P3] 3.3:
  * Linear -> GELU -> Linear; SwiGLU gate/up; [P2] 4.1 all experts' weights

@@ -146,6 +146,19 @@ moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x, in
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+moe_status moe_dispatch_static(const moe_config* cfg, const int* idx, const void* x, int* kept, int* offsets,
+                               int* pos, void* Xp, moe_stats* stats, moe_stream_t stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!idx || !x || !kept || !offsets || !pos || !Xp) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Xp)) return MOE_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  s = static_dispatch_scratch(dispatch_scratch_bytes(*cfg), &scratch);
+  if (s != MOE_OK) return s;
+  return launch_dispatch(*cfg, capacity_of(cfg), idx, x, kept, offsets, pos, Xp, stats, scratch,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
 moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offsets, const void* W1,
                           const void* W3, const void* b1, const void* W2, const void* b2, void* H, void* Yp,
                           void* ws, moe_stream_t stream) {

@@ -20,6 +20,8 @@
 // experts to call?": y = 0.75*E1(x) + 0.25*E3(x); "Shared experts": the
 // always-on path is added):
 //   y[t] = sum_{j: pos >= 0} w[t,j] * Yp[pos[t,j]]  (+ Sx[t]), fp32, j ascending.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -303,6 +305,33 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
                                                                      static_cast<uint32_t*>(Xp));
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Fixed device scratch for moe_dispatch_static: the chunk histograms and
+// per-chunk bases of the kernels above, held in a file-scope array of this
+// library instead of caller workspace.  Every word a dispatch reads from it
+// was written earlier in the same call (slot_hist writes all (E+1) counters
+// of every chunk, the scan writes every base), so nothing needs clearing.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_dispatch_scratch[kStaticDispatchScratchBytes];
+
+moe_status static_dispatch_scratch(size_t need, void** ptr) {
+  if (need > kStaticDispatchScratchBytes) return MOE_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  // the array's name is a host-side stand-in in host code; its device
+  // address is looked up once per device, with that device current
+  static void* addr[64] = {nullptr};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return MOE_OK;
 }
 
 moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos, const float* w, const void* Sx,

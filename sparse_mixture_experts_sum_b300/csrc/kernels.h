@@ -43,6 +43,13 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
                            int* offsets, int* pos, void* Xp, moe_stats* stats, void* scratch,
                            cudaStream_t stream);
 
+// Size of the library's own dispatch scratch (moe_dispatch_static): enough
+// for T*k <= 2^20 slots (256 chunks of 4096) at any E <= 1024.
+constexpr size_t kStaticDispatchScratchBytes = 256u * 1025u * 4u + 256u * 1024u * 4u + 256u;
+// Device address of that scratch on the current device (looked up on the
+// first call per device); MOE_ERR_UNSUPPORTED if `need` bytes do not fit.
+moe_status static_dispatch_scratch(size_t need, void** ptr);
+
 // Combine / un-permute.
 moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos, const float* w,
                           const void* Sx, void* y, cudaStream_t stream);

@@ -50,7 +50,8 @@ class MoeStats(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
-EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn",
+EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_static",
+           "moe_expert_ffn",
            "moe_combine", "moe_layer_fwd", "moe_check_error", "moe_status_string")
 
 _lib = None
@@ -71,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_size": [cfgp, i, ctypes.POINTER(sz)],
             "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_dispatch_static": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_expert_ffn": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_combine": [cfgp, vp, vp, vp, vp, vp, vp],
             "moe_layer_fwd": [cfgp, ctypes.POINTER(MoeWeights), vp, vp, vp, ctypes.POINTER(MoeSaved), vp, vp,
@@ -151,6 +153,13 @@ def moe_route(cfg, x, Wr, expert_bias, noise, idx, w, counts, ws=None, stream=No
 def moe_dispatch(cfg, idx, x, kept, offsets, pos, Xp, stats, ws, stream=None):
     _check("moe_dispatch", lib().moe_dispatch(ctypes.byref(cfg), _p(idx), _p(x), _p(kept), _p(offsets),
                                               _p(pos), _p(Xp), _p(stats), _p(ws), _stream(stream)))
+
+
+def moe_dispatch_static(cfg, idx, x, kept, offsets, pos, Xp, stats, stream=None):
+    """moe_dispatch with the library's own fixed scratch (no workspace)."""
+    _check("moe_dispatch_static", lib().moe_dispatch_static(ctypes.byref(cfg), _p(idx), _p(x), _p(kept),
+                                                            _p(offsets), _p(pos), _p(Xp), _p(stats),
+                                                            _stream(stream)))
 
 
 def moe_expert_ffn(cfg, Xp, offsets, W1, W3, b1, W2, b2, H, Yp, ws, stream=None):
