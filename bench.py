@@ -1,7 +1,7 @@
 """Benchmark of the sparse-MoE layer forward on B300 (one JSON line).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload large_prefill] [--no-decode] [--no-cpu-baseline]
+                    [--workload large_prefill] [--no-decode] [--no-training] [--no-cpu-baseline]
 
 A step is one forward of the whole layer (router -> top-k -> capacity
 dispatch -> grouped expert FFNs (+ shared expert) -> combine -> statistics)
@@ -292,6 +292,73 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     return out
 
 
+def run_training(args, world, rank, local):
+    """Training-shaped step (forward with saved activations + backward) of
+    the training workload through moe_layer_fwd / moe_layer_bwd, with an
+    event between the two halves.  Returns timings and algorithmic FLOPs."""
+    import torch
+    import moe_synth as S
+    import sparse_mixture_experts_sum_b300 as M
+
+    dev = torch.device("cuda", local)
+    wl = S.WORKLOADS["training"]
+    t = S.make_inputs(wl, dev)
+    cfg = M.config_of(wl)
+    weights = {n: t.get(n) for n in WEIGHTS}
+    x, noise, dY = t["x"], t.get("noise"), t["dY"]
+    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=dev)
+    st = M.moe.stats_buffer(dev)
+    saved = M.moe.alloc_saved(cfg, dev, backward=True)
+    grads = M.moe.alloc_grads(cfg, dev)
+    ws_f = M.moe.workspace(cfg, 1, device=dev)
+    ws_b = M.moe.workspace(cfg, 2, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        M.moe_layer_fwd(cfg, weights, x, noise, y, saved, st, ws_f)
+
+    def bwd():
+        M.moe_layer_bwd(cfg, weights, x, saved, dY, grads, ws_b)
+
+    for _ in range(max(3, args.warmup)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    assert M.moe_check_error(ws_f) == 0 and M.moe_check_error(ws_b) == 0
+    stats = M.moe.read_stats(st)
+    steps = max(3, min(args.steps, 10))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(local)
+    with sampler:
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            fwd()
+            ev[i][0].record(stream)
+            bwd()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    assert M.moe_check_error(ws_b) == 0
+    f_ms = b_ms = 0.0
+    prev = e0
+    for a, b in ev:
+        f_ms += prev.elapsed_time(a) / steps
+        b_ms += a.elapsed_time(b) / steps
+        prev = b
+    kept = stats["kept_slots"]
+    per = 2.0 * wl.d * wl.h * (3 if wl.act == "swiglu" else 2)
+    fwd_flops = per * (kept + (wl.T if wl.has_shared else 0)) + 2.0 * wl.T * wl.d * wl.E
+    bwd_flops = 2.0 * per * (kept + (wl.T if wl.has_shared else 0)) + 4.0 * wl.T * wl.d * wl.E
+    return {"workload": f"training: T={wl.T} d={wl.d} h={wl.h} E={wl.E}+1 shared top-{wl.k} {wl.act} "
+                        f"cf={wl.capacity_factor} gumbel bf16, fp32 grads",
+            "steps": steps, "ms_per_step": f_ms + b_ms, "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "tokens_per_s": wl.T / ((f_ms + b_ms) * 1e-3),
+            "tflops": (fwd_flops + bwd_flops) / ((f_ms + b_ms) * 1e-3) / 1e12,
+            "bwd_tflops": bwd_flops / (b_ms * 1e-3) / 1e12, "kept_slots": kept,
+            "clocks": sampler.summary()}
+
+
 def cpu_baseline(wl_name, gpu_tensors=None, max_rows=None, budget_s=20.0):
     """fp64 oracle on the host cores, on a bounded sample of the workload:
     router, top-k, capacity and dispatch of the whole batch, then the expert
@@ -367,6 +434,7 @@ def main():
     ap.add_argument("--workload", default="large_prefill")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-training", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
@@ -462,6 +530,10 @@ def main():
                           "components_ms": {k: round(v, 4) for k, v in d["components_ms"].items()},
                           "clocks": d["clocks"]}
         del d["tensors"]
+    if not args.no_training:
+        tr = run_training(args, world, rank, local)
+        tr["frac_of_sustained"] = tr["tflops"] / peaks["bf16_sus"]
+        line["training"] = tr
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import moe_synth as S
         gt = S.make_inputs(S.WORKLOADS[args.workload], torch.device("cuda", local))

@@ -45,7 +45,8 @@
  *    granted in slot-major priority (every token's first choice in token
  *    order, then every second choice, ...).
  *  - Limits: 1 <= k <= min(E, 8); 1 <= E <= 1024; T >= 1; T*k <= 2^30; for
- *    bf16, d and h multiples of 8 (16-byte rows).
+ *    bf16, d and h multiples of 8 (16-byte rows); moe_layer_bwd: bf16 with
+ *    d and h multiples of 64.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -114,7 +115,30 @@ typedef struct {
   void* H;       /* [T*k, h] activated hidden rows                         */
   void* Yp;      /* [T*k, d] expert outputs, permuted order                */
   void* Sx;      /* [T, d]   shared-expert output (has_shared)             */
+  /* Pre-activations and the shared hidden rows, written by a training
+   * forward when non-NULL and read by moe_layer_bwd (bf16 only):          */
+  void* Z;       /* [T*k, 2h] SwiGLU gate | up  (GeLU: [T*k, h], W1 v + b1) */
+  void* Hs;      /* [T, h]   shared expert's activated hidden rows          */
+  void* Zs;      /* [T, 2h]  shared expert's pre-activations (GeLU [T, h])  */
 } moe_saved;
+
+/* Gradients written by moe_layer_bwd (device, fp32, caller-owned).  Every
+ * listed tensor is overwritten, including the experts that received no
+ * rows (zero). */
+typedef struct {
+  float* dX;    /* [T,d]                                                    */
+  float* dWr;   /* [E,d]                                                    */
+  float* dW1;   /* [E,h,d]                                                  */
+  float* dW3;   /* [E,h,d] SwiGLU                                           */
+  float* dW2;   /* [E,d,h]                                                  */
+  float* db1;   /* [E,h] GeLU, nullable                                     */
+  float* db2;   /* [E,d] GeLU, nullable                                     */
+  float* dWs1;  /* [h,d] has_shared                                         */
+  float* dWs3;  /* [h,d] has_shared, SwiGLU                                 */
+  float* dWs2;  /* [d,h] has_shared                                         */
+  float* dbs1;  /* [h] has_shared, GeLU, nullable                           */
+  float* dbs2;  /* [d] has_shared, GeLU, nullable                           */
+} moe_grads;
 
 /* Load statistics ([P1] 3.1, 4.2; [P3] 2.3 drop monitoring). */
 typedef struct {
@@ -134,7 +158,8 @@ moe_status moe_capacity(const moe_config* cfg, int* C_out);
 /* Bytes of workspace the entry points below need for this config.
  * training = 0: moe_layer_fwd with saved == NULL keeps every intermediate in
  * the workspace.  training = 1: intermediates live in moe_saved; the
- * workspace holds scratch only. */
+ * workspace holds scratch only (also enough for moe_dispatch and
+ * moe_expert_ffn).  training = 2: moe_layer_bwd's scratch. */
 moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes);
 
 /* Router ([P1] 3.1 "logits = h W_r", softmax, top-k; [P1] 3.3 weights
@@ -220,6 +245,26 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
                          const float* noise, void* y, moe_saved* saved,
                          moe_stats* stats, void* ws, size_t ws_bytes,
                          moe_stream_t stream);
+
+/* The whole backward of the layer (bf16; d and h multiples of 64), for the
+ * loss L = <dY, y> + lambda * CV(I / T) where I[e] is the sum of the routing
+ * weights of the slots routed to e ([P4] 2.2's importance, in [P1] 3.1's
+ * std/mean form: std with n-1, mean + 1e-8); gradients reach the router and
+ * the chosen experts ([P1] 3.3).  Per routed slot (t,j) -> e:
+ *   G[t,j]  = [kept] <dY[t], Yp[pos[t,j]]> + d(lambda CV)/dw[t,j]
+ *   dl[t,j] = w[t,j] (G[t,j] - sum_j' w[t,j'] G[t,j'])  (other logits: 0)
+ *   dWr = sum_t dl[t]^T x[t];   dX[t] = sum_j dl[t,j] Wr[idx_j]
+ *         + sum_{kept j} J_e(x[t])^T (w[t,j] dY[t]) + J_shared(x[t])^T dY[t]
+ *   expert weights: the chain rule through W2 (act(...)) with
+ *   silu'(z) = s (1 + z (1 - s)) and gelu'(z) = Phi(z) + z phi(z).
+ * Noise and the expert bias are additive constants of the logits and get no
+ * gradient.  x, wts: the forward's inputs; saved: the forward's moe_saved
+ * with Z (and Hs, Zs with a shared expert) filled; dY [T,d] bf16.  Sums run
+ * in a fixed order (integers for the importance), so repeated calls give
+ * the same bits.  ws_bytes >= moe_workspace_size(cfg, 2). */
+moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const void* x,
+                         const moe_saved* saved, const void* dY, const moe_grads* grads,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronises `stream`, then reads the workspace error word left by the
  * last call that used `ws`: MOE_OK, or MOE_ERR_TIMEOUT if a kernel gave up

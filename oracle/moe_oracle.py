@@ -447,6 +447,9 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
         grads["dWs2"] = g["dW2"]
         if act == "swiglu":
             grads["dWs3"] = g["dW3"]
+        else:
+            grads["dbs1"] = g["db1"]
+            grads["dbs2"] = g["db2"]
     val, dcv = importance_cv_grad(idx, w, E, T, lam)
     G += dcv
     dl = np.zeros((T, E))
@@ -466,3 +469,105 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
     grads["balance_term"] = val
     grads.update(route=r)
     return grads
+
+
+# ----------------------------------------------------------------------------
+# sampled backward entries (for batches too large for layer_backward)
+# ----------------------------------------------------------------------------
+
+
+def expert_grad_slices(cfg: dict, weights: dict, x, dY, route: dict, e: int, cols) -> Dict[str, np.ndarray]:
+    """Weight gradients of expert e restricted to hidden units `cols`, summed
+    over all of the expert's kept rows: dW1[e][cols,:], dW3[e][cols,:] (or
+    db1[e][cols] for GeLU) and dW2[e][:,cols].  The chain rule of
+    expert_ffn_backward with the upstream gradient w[t,j] dY[t] of each kept
+    slot; a hidden unit's gradients depend only on that unit's row of W1/W3
+    and column of W2, so the slice is exact."""
+    act = cfg["act"]
+    cols = np.asarray(cols)
+    rows, slots = np.nonzero((route["idx"] == e) & (route["pos"] >= 0))
+    X = decode(x)[rows] if not hasattr(x, "index_select") else decode(x[_as_index(x, rows)])
+    Y = decode(dY)[rows] if not hasattr(dY, "index_select") else decode(dY[_as_index(dY, rows)])
+    g_out = route["w"][rows, slots][:, None] * Y
+    W1 = decode(weights["W1"][e][_as_index(weights["W1"], cols)])
+    W2 = decode(weights["W2"][e][:, _as_index(weights["W2"], cols)])
+    dh = g_out @ W2
+    out = {}
+    if act == "swiglu":
+        W3 = decode(weights["W3"][e][_as_index(weights["W3"], cols)])
+        a = X @ W1.T
+        b = X @ W3.T
+        hact = silu(a) * b
+        out["dW1"] = (dh * b * silu_grad(a)).T @ X
+        out["dW3"] = (dh * silu(a)).T @ X
+    else:
+        z = X @ W1.T
+        if weights.get("b1") is not None:
+            z = z + decode(weights["b1"][e])[cols][None, :]
+        hact = gelu(z)
+        dz = dh * gelu_grad(z)
+        out["dW1"] = dz.T @ X
+        out["db1"] = dz.sum(axis=0)
+    out["dW2"] = g_out.T @ hact
+    return out
+
+
+def token_input_grads(cfg: dict, weights: dict, x, dY, route: dict, tokens) -> np.ndarray:
+    """dX[t] for the listed tokens: the router term sum_j dl[t,j] Wr[idx_j]
+    (dl from layer_backward's rule, with the balance term over the whole
+    batch), plus each kept slot's expert input gradient for w[t,j] dY[t],
+    plus the shared expert's for dY[t]."""
+    T, k, E = cfg["T"], cfg["k"], cfg["E"]
+    act = cfg["act"]
+    toks = np.asarray(tokens)
+    idx, w, pos = route["idx"], route["w"], route["pos"]
+    X = decode(x[_as_index(x, toks)]) if hasattr(x, "index_select") else decode(x)[toks]
+    Y = decode(dY[_as_index(dY, toks)]) if hasattr(dY, "index_select") else decode(dY)[toks]
+    dX = np.zeros_like(X)
+    G = np.zeros((len(toks), k))
+    for e in sorted(set(idx[toks][pos[toks] >= 0].tolist())):
+        rr, ss = np.nonzero((idx[toks] == e) & (pos[toks] >= 0))
+        We = expert_params(weights, e, act)
+        g = _input_grad_rows(X[rr], w[toks[rr], ss][:, None] * Y[rr], act, We)
+        np.add.at(dX, rr, g["dv"])
+        G[rr, ss] += np.einsum("nd,nd->n", Y[rr], g["out"])
+    if cfg.get("has_shared"):
+        g = _input_grad_rows(X, Y, act, shared_params(weights, act))
+        dX += g["dv"]
+    _, dcv = importance_cv_grad(idx, w, E, T, cfg.get("lam", 0.01))
+    G += dcv[toks]
+    Wr = decode(weights["Wr"])
+    for i, t in enumerate(toks):
+        if idx[t, 0] < 0:
+            continue
+        s = (w[t] * G[i]).sum()
+        for j in range(k):
+            dX[i] += w[t, j] * (G[i, j] - s) * Wr[idx[t, j]]
+    return dX
+
+
+def _input_grad_rows(v, g_out, act, p):
+    """Input gradient and output of one expert on rows v (no weight grads)."""
+    if act == "swiglu":
+        a = v @ p["W1"].T
+        b = v @ p["W3"].T
+        out = (silu(a) * b) @ p["W2"].T
+        dh = g_out @ p["W2"]
+        dv = (dh * b * silu_grad(a)) @ p["W1"] + (dh * silu(a)) @ p["W3"]
+    else:
+        z = v @ p["W1"].T
+        if p.get("b1") is not None:
+            z = z + p["b1"][None, :]
+        out = gelu(z) @ p["W2"].T
+        if p.get("b2") is not None:
+            out = out + p["b2"][None, :]
+        dv = ((g_out @ p["W2"]) * gelu_grad(z)) @ p["W1"]
+    return dict(dv=dv, out=out)
+
+
+def _as_index(t, ix):
+    """Index array in the form `t` accepts (a torch tensor on t's device, or numpy)."""
+    if hasattr(t, "index_select"):
+        import torch
+        return torch.as_tensor(np.asarray(ix), device=t.device)
+    return np.asarray(ix)

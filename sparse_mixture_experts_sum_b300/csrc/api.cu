@@ -34,23 +34,41 @@ int capacity_of(const moe_config* cfg) {
 
 size_t esize(const moe_config* cfg) { return cfg->dtype == MOE_BF16 ? 2 : 4; }
 
-// Workspace carving: [header | dispatch scratch | (inference) intermediates | shared hidden]
+// Workspace carving.  training 0/1 (forward): [header | dispatch scratch |
+// (inference) intermediates | shared hidden].  training 2 (backward):
+// [header | dYp | dAB | dXp | dot | dl | importance | coef | router partials
+// | shared dAB].
 struct WsLayout {
   size_t dispatch_off;
-  size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs, total;
+  size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs;
+  size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs;
+  size_t total;
 };
 
 WsLayout layout(const moe_config* cfg, int training) {
   WsLayout L{};
   size_t o = kWsHeader;
-  L.dispatch_off = o;
-  o += align_up(dispatch_scratch_bytes(*cfg), 256);
   const size_t T = cfg->T, k = cfg->k, E = cfg->E, d = cfg->d, h = cfg->h, es = esize(cfg);
+  const size_t hz = cfg->act == MOE_ACT_SWIGLU ? 2 * h : h;  // width of the pre-activation rows
   auto take = [&](size_t bytes) {
     const size_t at = o;
     o += align_up(bytes, 256);
     return at;
   };
+  if (training == 2) {
+    L.dYp = take(T * k * d * es);
+    L.dAB = take(T * k * hz * es);
+    L.dXp = take(T * k * d * 4);
+    L.dot = take(T * k * 4);
+    L.dl = take(T * k * 4);
+    L.imp = take(E * 8);
+    L.coef = take(E * 4);
+    L.rpart = take(router_wgrad_partial_bytes(*cfg));
+    L.dABs = cfg->has_shared ? take(T * hz * es) : 0;
+    L.total = o;
+    return L;
+  }
+  L.dispatch_off = take(dispatch_scratch_bytes(*cfg));
   if (!training) {
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
@@ -74,7 +92,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, const int* offsets, int G, int rows,
                    const void* W1, const void* W3, const void* b1, const void* W2, const void* b2, void* H,
-                   void* Yp, int* err, cudaStream_t st) {
+                   void* Yp, void* Z, int* err, cudaStream_t st) {
   const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
   GemmParams g1{};
   g1.offsets = offsets;
@@ -84,6 +102,8 @@ moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, cons
   g1.K = cfg->d;
   g1.mode = swiglu ? kModeSwiGLU : kModeGeLU;
   g1.out = H;
+  g1.zsave = Z;
+  g1.ldz = swiglu ? 2LL * cfg->h : cfg->h;
   g1.bias = swiglu ? nullptr : b1;
   g1.err = err;
   GemmParams g2 = g1;
@@ -91,18 +111,104 @@ moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, cons
   g2.K = cfg->h;
   g2.mode = kModePlain;
   g2.out = Yp;
+  g2.zsave = nullptr;
   g2.bias = swiglu ? nullptr : b2;
   moe_status s;
   if (cfg->dtype == MOE_BF16) {
-    s = launch_grouped_gemm_tc(g1, Xp, a_rows, W1, swiglu ? W3 : nullptr, static_cast<long long>(G) * cfg->h, st);
+    s = launch_grouped_gemm_tc(g1, kKindFwd, Xp, a_rows, W1, swiglu ? W3 : nullptr,
+                               static_cast<long long>(G) * cfg->h, st);
     if (s != MOE_OK) return s;
-    s = launch_grouped_gemm_tc(g2, H, a_rows, W2, nullptr, static_cast<long long>(G) * cfg->d, st);
+    s = launch_grouped_gemm_tc(g2, kKindFwd, H, a_rows, W2, nullptr, static_cast<long long>(G) * cfg->d, st);
   } else {
+    if (Z) return MOE_ERR_UNSUPPORTED;
     s = launch_grouped_gemm_f32(g1, Xp, a_rows, W1, swiglu ? W3 : nullptr, st);
     if (s != MOE_OK) return s;
     s = launch_grouped_gemm_f32(g2, H, a_rows, W2, nullptr, st);
   }
   return s;
+}
+
+// Backward of one expert group set (routed: G experts over offsets; shared:
+// G = 1 over `rows` rows).  dYp [a_rows, d] is the upstream gradient in
+// expert order, Z the saved pre-activations, H the saved hidden rows, Xin
+// the forward input rows.  Writes dAB (scratch), dXin (fp32, [a_rows, d]),
+// dW1/dW3/dW2 (fp32) and, for GeLU, db1/db2.
+moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offsets, int G, int rows,
+                       const void* dYp, const void* Z, const void* H, const void* Xin, const void* W1,
+                       const void* W3, const void* W2, void* dAB, float* dXin, float* dW1, float* dW3, float* dW2,
+                       float* db1, float* db2, int* err, cudaStream_t st) {
+  const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
+  const int h = cfg->h, d = cfg->d;
+  const long long hz = swiglu ? 2LL * h : h;
+  // dH = dYp . W2_g -> activation backward -> dAB = [dA | dB] (or dZ)
+  GemmParams a{};
+  a.offsets = offsets;
+  a.G = G;
+  a.rows = rows;
+  a.N = h;
+  a.K = d;
+  a.mode = swiglu ? kModeSwiGLUBwd : kModeGeLUBwd;
+  a.out = dAB;
+  a.ldo = hz;
+  a.zin = Z;
+  a.ldz = hz;
+  a.err = err;
+  moe_status s = launch_grouped_gemm_tc(a, kKindDgrad, dYp, a_rows, W2, nullptr, static_cast<long long>(G) * d, st);
+  if (s != MOE_OK) return s;
+  // dXin = dA . W1_g + dB . W3_g  (fp32)
+  GemmParams b{};
+  b.offsets = offsets;
+  b.G = G;
+  b.rows = rows;
+  b.N = d;
+  b.K = static_cast<int>(hz);
+  b.k_split = swiglu ? h : 0;
+  b.mode = kModePlain;
+  b.out_f32 = 1;
+  b.out = dXin;
+  b.err = err;
+  s = launch_grouped_gemm_tc(b, kKindDgrad, dAB, a_rows, W1, swiglu ? W3 : nullptr, static_cast<long long>(G) * h,
+                             st);
+  if (s != MOE_OK) return s;
+  // dW2_g = dYp_g^T . H_g
+  GemmParams c{};
+  c.offsets = offsets;
+  c.G = G;
+  c.rows = rows;
+  c.M = d;
+  c.N = h;
+  c.mode = kModePlain;
+  c.out_f32 = 1;
+  c.out = dW2;
+  c.err = err;
+  s = launch_grouped_gemm_tc(c, kKindWgrad, dYp, a_rows, H, nullptr, a_rows, st);
+  if (s != MOE_OK) return s;
+  // [dW1; dW3]_g = [dA | dB]_g^T . Xin_g
+  GemmParams w{};
+  w.offsets = offsets;
+  w.G = G;
+  w.rows = rows;
+  w.M = static_cast<int>(hz);
+  w.N = d;
+  w.m_split = swiglu ? h : 0;
+  w.mode = kModePlain;
+  w.out_f32 = 1;
+  w.out = dW1;
+  w.out2 = swiglu ? dW3 : nullptr;
+  w.err = err;
+  s = launch_grouped_gemm_tc(w, kKindWgrad, dAB, a_rows, Xin, nullptr, a_rows, st);
+  if (s != MOE_OK) return s;
+  if (!swiglu) {
+    if (db1) {
+      s = launch_group_colsum(dAB, hz, offsets, G, rows, h, db1, st);
+      if (s != MOE_OK) return s;
+    }
+    if (db2) {
+      s = launch_group_colsum(dYp, d, offsets, G, rows, d, db2, st);
+      if (s != MOE_OK) return s;
+    }
+  }
+  return MOE_OK;
 }
 
 }  // namespace
@@ -121,6 +227,7 @@ moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes
   const moe_status s = validate(cfg);
   if (s != MOE_OK) return s;
   if (!bytes) return MOE_ERR_INVALID_ARG;
+  if (training < 0 || training > 2) return MOE_ERR_INVALID_ARG;
   *bytes = layout(cfg, training).total;
   return MOE_OK;
 }
@@ -173,7 +280,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offs
   int* err = static_cast<int*>(ws);
   if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
-  return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, W1, W3, b1, W2, b2, H, Yp, err, st);
+  return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, W1, W3, b1, W2, b2, H, Yp, nullptr, err, st);
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* Yp, const int* pos, const float* w, const void* Sx,
@@ -215,6 +322,7 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
     S.H = at(ws, L.H);
     S.Yp = at(ws, L.Yp);
     S.Sx = cfg->has_shared ? at(ws, L.Sx) : nullptr;
+    S.Z = S.Hs = S.Zs = nullptr;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
@@ -226,15 +334,67 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
                       at(ws, L.dispatch_off), st);
   if (s != MOE_OK) return s;
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
-  s = run_ffn(cfg, S.Xp, a_rows, S.offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, S.H, S.Yp, err,
-              st);
+  s = run_ffn(cfg, S.Xp, a_rows, S.offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, S.H, S.Yp,
+              training ? S.Z : nullptr, err, st);
   if (s != MOE_OK) return s;
   if (cfg->has_shared) {
-    s = run_ffn(cfg, x, cfg->T, nullptr, 1, cfg->T, wts->Ws1, wts->Ws3, wts->bs1, wts->Ws2, wts->bs2,
-                at(ws, L.Hs), S.Sx, err, st);
+    void* Hs = training && S.Hs ? S.Hs : at(ws, L.Hs);
+    s = run_ffn(cfg, x, cfg->T, nullptr, 1, cfg->T, wts->Ws1, wts->Ws3, wts->bs1, wts->Ws2, wts->bs2, Hs, S.Sx,
+                training ? S.Zs : nullptr, err, st);
     if (s != MOE_OK) return s;
   }
   return launch_combine(*cfg, S.Yp, S.pos, S.w, cfg->has_shared ? S.Sx : nullptr, y, st);
+}
+
+moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const void* x, const moe_saved* saved,
+                         const void* dY, const moe_grads* grads, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!wts || !x || !saved || !dY || !grads || !ws) return MOE_ERR_INVALID_ARG;
+  const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if ((cfg->d % 64) || (cfg->h % 64)) return MOE_ERR_UNSUPPORTED;
+  if (!wts->Wr || !wts->W1 || !wts->W2 || (swiglu && !wts->W3)) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_shared && (!wts->Ws1 || !wts->Ws2 || (swiglu && !wts->Ws3))) return MOE_ERR_INVALID_ARG;
+  const moe_saved& S = *saved;
+  if (!S.idx || !S.w || !S.offsets || !S.pos || !S.Xp || !S.H || !S.Yp || !S.Z) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_shared && (!S.Hs || !S.Zs)) return MOE_ERR_INVALID_ARG;
+  const moe_grads& g = *grads;
+  if (!g.dX || !g.dWr || !g.dW1 || !g.dW2 || (swiglu && !g.dW3)) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_shared && (!g.dWs1 || !g.dWs2 || (swiglu && !g.dWs3))) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(cfg, 2);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws) || !aligned16(x) || !aligned16(dY) || !aligned16(g.dX)) return MOE_ERR_INVALID_ARG;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  void* dYp = at(ws, L.dYp);
+  void* dAB = at(ws, L.dAB);
+  float* dXp = static_cast<float*>(at(ws, L.dXp));
+  float* dot = static_cast<float*>(at(ws, L.dot));
+  float* dl = static_cast<float*>(at(ws, L.dl));
+  const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
+
+  // routing-weight gradients and the router
+  s = launch_bwd_gather(*cfg, dY, S.Yp, S.pos, S.w, dYp, dot, st);
+  if (s != MOE_OK) return s;
+  s = launch_router_bwd(*cfg, S.idx, S.w, dot, static_cast<unsigned long long*>(at(ws, L.imp)),
+                        static_cast<float*>(at(ws, L.coef)), dl, st);
+  if (s != MOE_OK) return s;
+  s = launch_router_wgrad(*cfg, x, S.idx, dl, static_cast<float*>(at(ws, L.rpart)), g.dWr, st);
+  if (s != MOE_OK) return s;
+  // routed experts
+  s = run_ffn_bwd(cfg, a_rows, S.offsets, cfg->E, 0, dYp, S.Z, S.H, S.Xp, wts->W1, wts->W3, wts->W2, dAB, dXp, g.dW1,
+                  g.dW3, g.dW2, g.db1, g.db2, err, st);
+  if (s != MOE_OK) return s;
+  // shared expert: its input gradient lands in dX directly
+  if (cfg->has_shared) {
+    s = run_ffn_bwd(cfg, cfg->T, nullptr, 1, cfg->T, dY, S.Zs, S.Hs, x, wts->Ws1, wts->Ws3, wts->Ws2,
+                    at(ws, L.dABs), g.dX, g.dWs1, g.dWs3, g.dWs2, g.dbs1, g.dbs2, err, st);
+    if (s != MOE_OK) return s;
+  }
+  return launch_bwd_dx(*cfg, dXp, S.pos, S.idx, dl, wts->Wr, cfg->has_shared ? 1 : 0, g.dX, st);
 }
 
 moe_status moe_check_error(const void* ws, int* code_out, moe_stream_t stream) {

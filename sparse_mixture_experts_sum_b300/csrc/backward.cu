@@ -1,0 +1,343 @@
+// Backward of the MoE layer outside the expert GEMMs: the gather of the
+// upstream gradient into expert order, the routing-weight and router
+// gradients (with the load-balance term), the router weight gradient, the
+// GeLU bias gradients, and the assembly of dX.
+//
+// Loss: L = <dY, y> + lambda * CV(I / T), I[e] = the sum of the routing
+// weights of the slots routed to e -- the importance of [P4] "GPT-4 has 1.8
+// trillion parameters..." 2.2, in the std/mean form of [P1] "'More
+// parameters is better' is not the story..." 3.1 (std with n-1, +1e-8 on the
+// mean).  Gradients flow back to the router and to the chosen experts
+// ([P1] 3.3).  Per slot (t, j) routed to e:
+//   dot[t,j] = <dY[t], Yp[pos[t,j]]>          (kept slots; 0 when dropped)
+//   G[t,j]   = dot[t,j] + d(lambda CV)/dw[t,j]
+//   dl[t,j]  = w[t,j] (G[t,j] - sum_j' w[t,j'] G[t,j'])   (softmax over the
+//              selected logits, [P1] 3.3; the other logits get no gradient)
+//   dWr[e]  += dl[t,j] x[t];   dX[t] += dl[t,j] Wr[e]
+// Every reduction runs in a fixed order or in integers, so the results are
+// the same bits on every run.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr double kImpScale = 4294967296.0;  // routing weights accumulate as 2^-32 fixed point
+
+// One warp per token: dot[t,j] = <dY[t], Yp[pos]>, dYp[pos] = w[t,j] dY[t].
+__global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ Yp,
+                                  const int* __restrict__ pos, const float* __restrict__ w, int T, int k,
+                                  int vec_per_row, uint4* __restrict__ dYp, float* __restrict__ dot) {
+  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int p[8];
+  float wt[8], acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
+    wt[j] = j < k ? w[static_cast<size_t>(t) * k + j] : 0.f;
+    acc[j] = 0.f;
+  }
+  for (int v = lane; v < vec_per_row; v += 32) {
+    const uint4 q = dY[static_cast<size_t>(t) * vec_per_row + v];
+    const uint32_t g[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (p[j] < 0) continue;
+      const uint4 yq = Yp[static_cast<size_t>(p[j]) * vec_per_row + v];
+      const uint32_t y[4] = {yq.x, yq.y, yq.z, yq.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[j] = fmaf(bf16lo(g[i]), bf16lo(y[i]), acc[j]);
+        acc[j] = fmaf(bf16hi(g[i]), bf16hi(y[i]), acc[j]);
+        o[i] = pack_bf16(wt[j] * bf16lo(g[i]), wt[j] * bf16hi(g[i]));
+      }
+      dYp[static_cast<size_t>(p[j]) * vec_per_row + v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float s = acc[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0 && j < k) dot[static_cast<size_t>(t) * k + j] = p[j] >= 0 ? s : 0.f;
+  }
+}
+
+// I[e] = sum of w over the slots routed to e, in 2^-32 fixed point (integer
+// sums are exact, so the order of the atomics does not show).
+__global__ void importance_kernel(const int* __restrict__ idx, const float* __restrict__ w, long long nslots, int E,
+                                  unsigned long long* __restrict__ imp) {
+  extern __shared__ unsigned long long simp[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) simp[e] = 0ull;
+  __syncthreads();
+  for (long long s = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; s < nslots;
+       s += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int e = idx[s];
+    if (e >= 0 && e < E) {
+      const unsigned long long q = static_cast<unsigned long long>(static_cast<double>(w[s]) * kImpScale + 0.5);
+      atomicAdd(&simp[e], q);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (simp[e]) atomicAdd(&imp[e], simp[e]);
+}
+
+// coef[e] = d(lambda CV(f))/d f_e / T with f = I/T, CV = std_{n-1}(f)/(mean(f) + 1e-8).
+// One block of 1024 threads, one expert per thread (E <= 1024); fp64 sums
+// in a fixed order (warp shuffles, then the warp partials in warp order).
+__global__ void __launch_bounds__(1024) balance_coef_kernel(const unsigned long long* __restrict__ imp, int E,
+                                                            int T, float lam, float* __restrict__ coef) {
+  __shared__ double red[32];
+  __shared__ double mean_s, std_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const double scale = 1.0 / (kImpScale * static_cast<double>(T));
+  const double fe = tid < E ? static_cast<double>(imp[tid]) * scale : 0.0;
+  double v = fe;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (tid == 0) {
+    double m = 0.0;
+    for (int w2 = 0; w2 < nwarps; ++w2) m += red[w2];
+    mean_s = m / E;
+  }
+  __syncthreads();
+  const double m = mean_s;
+  double dv2 = tid < E ? (fe - m) * (fe - m) : 0.0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dv2 += __shfl_xor_sync(0xffffffffu, dv2, o);
+  if (lane == 0) red[warp] = dv2;
+  __syncthreads();
+  if (tid == 0) {
+    double var = 0.0;
+    for (int w2 = 0; w2 < nwarps; ++w2) var += red[w2];
+    std_s = E > 1 ? sqrt(var / (E - 1)) : 0.0;
+  }
+  __syncthreads();
+  const double sd = std_s, den = m + 1e-8;
+  if (tid < E) {
+    double g = 0.0;
+    if (E > 1 && sd > 0.0) {
+      const double dstd = (fe - m) / ((E - 1) * sd);
+      g = static_cast<double>(lam) * (dstd / den - sd / (den * den) / E);
+    }
+    coef[tid] = static_cast<float>(g / T);
+  }
+}
+
+// One thread per token: dl[t,j] = w_j (G_j - sum_j' w_j' G_j').
+__global__ void router_bwd_kernel(const int* __restrict__ idx, const float* __restrict__ w,
+                                  const float* __restrict__ dot, const float* __restrict__ coef, int T, int k, int E,
+                                  float* __restrict__ dl) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  float G[8], wt[8];
+  float s = 0.f;
+  const bool routed = idx[static_cast<size_t>(t) * k] >= 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    G[j] = 0.f;
+    wt[j] = 0.f;
+    if (j < k && routed) {
+      const int e = idx[static_cast<size_t>(t) * k + j];
+      wt[j] = w[static_cast<size_t>(t) * k + j];
+      G[j] = dot[static_cast<size_t>(t) * k + j] + (e >= 0 && e < E ? coef[e] : 0.f);
+      s = fmaf(wt[j], G[j], s);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < k) dl[static_cast<size_t>(t) * k + j] = routed ? wt[j] * (G[j] - s) : 0.f;
+}
+
+constexpr int RW_TOK = 1024;  // tokens per block of the router weight gradient
+constexpr int RW_EXP = 32;    // experts per block (32 KB of per-warp accumulators)
+constexpr int RW_WARPS = 8;
+
+// partial[chunk][e][c] = sum over the chunk's tokens t (ascending, per warp
+// t = warp mod 8) of sum_j [idx=e] dl[t,j] x[t][c]; 32 columns per block,
+// one per lane; every warp accumulates privately in shared memory and the
+// warps are summed in a fixed order.
+template <typename Tx>
+__global__ void __launch_bounds__(RW_WARPS * 32)
+router_wgrad_partial_kernel(const Tx* __restrict__ x, const int* __restrict__ idx, const float* __restrict__ dl,
+                            int T, int d, int k, int E, float* __restrict__ partial) {
+  __shared__ float acc[RW_WARPS][RW_EXP][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.y * 32 + lane;
+  const int e0 = blockIdx.z * RW_EXP;
+  const int t0 = blockIdx.x * RW_TOK;
+  for (int i = lane; i < RW_EXP * 32; i += 32) (&acc[warp][0][0])[i] = 0.f;
+  __syncwarp();
+  const int t1 = min(T, t0 + RW_TOK);
+  for (int t = t0 + warp; t < t1; t += RW_WARPS) {
+    float xv = 0.f;
+    if (c < d) {
+      if constexpr (sizeof(Tx) == 2) xv = __bfloat162float(x[static_cast<size_t>(t) * d + c]);
+      else xv = x[static_cast<size_t>(t) * d + c];
+    }
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[static_cast<size_t>(t) * k + j] - e0;
+      if (e >= 0 && e < RW_EXP && e0 + e < E)
+        acc[warp][e][lane] = fmaf(dl[static_cast<size_t>(t) * k + j], xv, acc[warp][e][lane]);
+    }
+  }
+  __syncthreads();
+  const int ne = min(RW_EXP, E - e0);
+  for (int i = threadIdx.x; i < ne * 32; i += blockDim.x) {
+    const int e = i >> 5, l = i & 31;
+    const int cc = blockIdx.y * 32 + l;
+    float s = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < RW_WARPS; ++w2) s += acc[w2][e][l];
+    if (cc < d) partial[(static_cast<size_t>(blockIdx.x) * E + e0 + e) * d + cc] = s;
+  }
+}
+
+// dWr[e][c] = sum over chunks (ascending) of partial[chunk][e][c].
+__global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, int nchunks, long long Ed,
+                                           float* __restrict__ dWr) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= Ed) return;
+  float s = 0.f;
+  for (int b = 0; b < nchunks; ++b) s += partial[static_cast<size_t>(b) * Ed + i];
+  dWr[i] = s;
+}
+
+// One warp per token: dX[t] (+)= sum_{kept j} dXp[pos] + sum_j dl[t,j] Wr[idx_j] (fp32, j ascending).
+template <typename Tw>
+__global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restrict__ pos, const int* __restrict__ idx,
+                              const float* __restrict__ dl, const Tw* __restrict__ Wr, int T, int k, int d, int E,
+                              int accumulate, float* __restrict__ dX) {
+  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int p[8], e[8];
+  float g[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
+    e[j] = j < k ? idx[static_cast<size_t>(t) * k + j] : -1;
+    g[j] = j < k ? dl[static_cast<size_t>(t) * k + j] : 0.f;
+  }
+  float* out = dX + static_cast<size_t>(t) * d;
+  for (int c = lane * 4; c < d; c += 128) {
+    float4 a = accumulate ? *reinterpret_cast<const float4*>(out + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (p[j] >= 0) {
+        const float4 v = *reinterpret_cast<const float4*>(dXp + static_cast<size_t>(p[j]) * d + c);
+        a.x += v.x;
+        a.y += v.y;
+        a.z += v.z;
+        a.w += v.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (e[j] >= 0 && e[j] < E) {
+        const Tw* wr = Wr + static_cast<size_t>(e[j]) * d + c;
+        float w0, w1, w2, w3;
+        if constexpr (sizeof(Tw) == 2) {
+          w0 = __bfloat162float(wr[0]);
+          w1 = __bfloat162float(wr[1]);
+          w2 = __bfloat162float(wr[2]);
+          w3 = __bfloat162float(wr[3]);
+        } else {
+          w0 = wr[0];
+          w1 = wr[1];
+          w2 = wr[2];
+          w3 = wr[3];
+        }
+        a.x = fmaf(g[j], w0, a.x);
+        a.y = fmaf(g[j], w1, a.y);
+        a.z = fmaf(g[j], w2, a.z);
+        a.w = fmaf(g[j], w3, a.w);
+      }
+    }
+    *reinterpret_cast<float4*>(out + c) = a;
+  }
+}
+
+// out[g][n] = sum of src[r][n] over the rows r of group g (ascending).
+__global__ void group_colsum_kernel(const bf16* __restrict__ src, long long ld, const int* __restrict__ offsets,
+                                    int rows, int N, float* __restrict__ out) {
+  const int g = blockIdx.y;
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  const int r0 = offsets ? offsets[g] : 0;
+  const int r1 = offsets ? offsets[g + 1] : rows;
+  float s = 0.f;
+  for (int r = r0; r < r1; ++r) s += __bfloat162float(src[static_cast<size_t>(r) * ld + n]);
+  out[static_cast<size_t>(g) * N + n] = s;
+}
+
+inline unsigned warp_grid(int T) { return static_cast<unsigned>((static_cast<long long>(T) * 32 + 255) / 256); }
+
+}  // namespace
+
+size_t router_wgrad_partial_bytes(const moe_config& cfg) {
+  const size_t nchunks = (static_cast<size_t>(cfg.T) + RW_TOK - 1) / RW_TOK;
+  return nchunks * cfg.E * cfg.d * sizeof(float);
+}
+
+moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* Yp, const int* pos, const float* w,
+                             void* dYp, float* dot, cudaStream_t st) {
+  bwd_gather_kernel<<<warp_grid(cfg.T), 256, 0, st>>>(static_cast<const uint4*>(dY), static_cast<const uint4*>(Yp),
+                                                       pos, w, cfg.T, cfg.k, cfg.d / 8, static_cast<uint4*>(dYp), dot);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_router_bwd(const moe_config& cfg, const int* idx, const float* w, const float* dot,
+                             unsigned long long* imp, float* coef, float* dl, cudaStream_t st) {
+  const long long nslots = static_cast<long long>(cfg.T) * cfg.k;
+  if (cudaMemsetAsync(imp, 0, sizeof(unsigned long long) * cfg.E, st) != cudaSuccess) return MOE_ERR_CUDA;
+  long long blocks = (nslots + 255) / 256;
+  if (blocks > 1184) blocks = 1184;
+  importance_kernel<<<static_cast<unsigned>(blocks), 256, sizeof(unsigned long long) * cfg.E, st>>>(idx, w, nslots,
+                                                                                                    cfg.E, imp);
+  balance_coef_kernel<<<1, 1024, 0, st>>>(imp, cfg.E, cfg.T, cfg.lambda_balance, coef);
+  router_bwd_kernel<<<(cfg.T + 255) / 256, 256, 0, st>>>(idx, w, dot, coef, cfg.T, cfg.k, cfg.E, dl);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl, float* partial,
+                               float* dWr, cudaStream_t st) {
+  const int nchunks = (cfg.T + RW_TOK - 1) / RW_TOK;
+  dim3 grid(nchunks, (cfg.d + 31) / 32, (cfg.E + RW_EXP - 1) / RW_EXP);
+  if (cfg.dtype == MOE_BF16)
+    router_wgrad_partial_kernel<bf16><<<grid, RW_WARPS * 32, 0, st>>>(static_cast<const bf16*>(x), idx, dl, cfg.T,
+                                                                      cfg.d, cfg.k, cfg.E, partial);
+  else
+    router_wgrad_partial_kernel<float><<<grid, RW_WARPS * 32, 0, st>>>(static_cast<const float*>(x), idx, dl, cfg.T,
+                                                                       cfg.d, cfg.k, cfg.E, partial);
+  const long long Ed = static_cast<long long>(cfg.E) * cfg.d;
+  router_wgrad_reduce_kernel<<<static_cast<unsigned>((Ed + 255) / 256), 256, 0, st>>>(partial, nchunks, Ed, dWr);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,
+                         const void* Wr, int accumulate, float* dX, cudaStream_t st) {
+  if (cfg.dtype == MOE_BF16)
+    bwd_dx_kernel<bf16><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, static_cast<const bf16*>(Wr), cfg.T,
+                                                          cfg.k, cfg.d, cfg.E, accumulate, dX);
+  else
+    bwd_dx_kernel<float><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, static_cast<const float*>(Wr), cfg.T,
+                                                           cfg.k, cfg.d, cfg.E, accumulate, dX);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_group_colsum(const void* src, long long ld, const int* offsets, int G, int rows, int N, float* out,
+                               cudaStream_t st) {
+  dim3 grid((N + 255) / 256, G);
+  group_colsum_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(src), ld, offsets, rows, N, out);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

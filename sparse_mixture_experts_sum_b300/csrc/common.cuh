@@ -46,6 +46,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 __device__ __forceinline__ float gelu_f(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// d/dz gelu(z) = Phi(z) + z phi(z)
+__device__ __forceinline__ float gelu_grad_f(float z) {
+  return 0.5f * (1.0f + erff(z * 0.70710678118654752f)) + z * 0.39894228040143268f * expf(-0.5f * z * z);
+}
+// sigmoid, and d/dz silu(z) = s (1 + z (1 - s))
+__device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
 
 // ---------------------------------------------------------------------------
 // shared-memory addresses, mbarrier
@@ -190,11 +196,31 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile written by
+// TMA with 128-byte swizzling: each K row holds 64 consecutive M (or N)
+// elements in one 128-byte line; 8 K rows form a 1024-byte swizzle atom;
+// the tile stores 64-element MN blocks of 64 K rows (8 KB each) one after
+// another.  Leading byte offset = 8192 (bits 16-29, between MN blocks),
+// stride byte offset = 1024 (bits 32-45, between 8-row K groups), version 1
+// (bit 46), swizzle mode 2 = 128B (bits 61-63).  Advancing K by 16 rows
+// adds 2048 bytes to the start address.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), both K-major, N >> 3 at
-// bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+// A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), A major (bit 15) and B
+// major (bit 16): 0 = K-major, 1 = MN-major; N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn = 0, int b_mn = 0) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn & 1) << 15) |
+         (static_cast<uint32_t>(b_mn & 1) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 

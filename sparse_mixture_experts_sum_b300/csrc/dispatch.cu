@@ -107,31 +107,69 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
     offsets[tid] = excl;
     if (tid == E - 1) offsets[E] = excl + my_kept;
   }
-  if (tid == 0 && stats) {
-    long long routed = 0, kept_total = 0;
-    for (int e = 0; e < E; ++e) {
-      routed += tot[e];
-      kept_total += tot[e] < C ? tot[e] : C;
-    }
+  if (stats) {
+    // load statistics: fp64, one division, fixed-order reductions (each
+    // thread owns one expert; warps reduce by shuffles, then warp 0 sums
+    // the warp partials in warp order)
+    __shared__ double red[32];
+    __shared__ long long redl[32][2];
     const long long nslots = static_cast<long long>(T) * k;
-    double mean = 0.0;
-    for (int e = 0; e < E; ++e) mean += static_cast<double>(tot[e]) / T;
-    mean /= E;
-    double var = 0.0;
-    for (int e = 0; e < E; ++e) {
-      const double dv = static_cast<double>(tot[e]) / T - mean;
-      var += dv * dv;
+    const double invT = 1.0 / static_cast<double>(T);
+    const int nwarps = (blockDim.x + 31) >> 5;
+    long long r_cnt = tid < E ? tot[tid] : 0, k_cnt = tid < E ? my_kept : 0;
+    double fsum = tid < E ? static_cast<double>(tot[tid]) * invT : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      r_cnt += __shfl_xor_sync(0xffffffffu, r_cnt, o);
+      k_cnt += __shfl_xor_sync(0xffffffffu, k_cnt, o);
+      fsum += __shfl_xor_sync(0xffffffffu, fsum, o);
     }
-    const double sd = E > 1 ? sqrt(var / (E - 1)) : 0.0;
-    moe_stats st;
-    st.routed_slots = routed;
-    st.kept_slots = kept_total;
-    st.dropped_slots = nslots - kept_total;
-    st.capacity = C;
-    st.numeric_error = unrouted / k;
-    st.drop_rate = static_cast<double>(nslots - kept_total) / static_cast<double>(nslots);
-    st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
-    *stats = st;
+    if (lane == 0) {
+      red[warp] = fsum;
+      redl[warp][0] = r_cnt;
+      redl[warp][1] = k_cnt;
+    }
+    __syncthreads();
+    __shared__ double mean_s;
+    __shared__ long long routed_s, kept_s;
+    if (tid == 0) {
+      double fs = 0.0;
+      long long rc = 0, kc = 0;
+      for (int w2 = 0; w2 < nwarps; ++w2) {
+        fs += red[w2];
+        rc += redl[w2][0];
+        kc += redl[w2][1];
+      }
+      mean_s = fs / E;
+      routed_s = rc;
+      kept_s = kc;
+    }
+    __syncthreads();
+    const double mean = mean_s;
+    double dv2 = 0.0;
+    if (tid < E) {
+      const double dv = static_cast<double>(tot[tid]) * invT - mean;
+      dv2 = dv * dv;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dv2 += __shfl_xor_sync(0xffffffffu, dv2, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = dv2;
+    __syncthreads();
+    if (tid == 0) {
+      double var = 0.0;
+      for (int w2 = 0; w2 < nwarps; ++w2) var += red[w2];
+      const double sd = E > 1 ? sqrt(var / (E - 1)) : 0.0;
+      moe_stats st;
+      st.routed_slots = routed_s;
+      st.kept_slots = kept_s;
+      st.dropped_slots = nslots - kept_s;
+      st.capacity = C;
+      st.numeric_error = unrouted / k;
+      st.drop_rate = static_cast<double>(nslots - kept_s) / static_cast<double>(nslots);
+      st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
+      *stats = st;
+    }
   }
 }
 

@@ -1,29 +1,42 @@
-// Grouped expert GEMM on the sm_103a tensor cores (tcgen05 + TMEM, fed by TMA).
+// Grouped expert GEMMs on the sm_103a tensor cores (tcgen05 + TMEM, fed by TMA).
 //
-// out[r, :] = act( A[r, :] . B_g^T )   for every group g and row r of g,
-// where the rows of group g are [offsets[g], offsets[g+1]) of the
-// expert-contiguous activation matrix A, and B_g is group g's weight block.
-// This is the expert loop of the MoE layer: "[P2] 4.2 / [P3] 3.3 Linear ->
-// GELU -> Linear" per expert, with all experts' weights in one contiguous
-// tensor ([P2] 4.1 expert fusion) sliced by the group index.
+// The expert loop of the MoE layer -- "[P2] 4.2 / [P3] 3.3 Linear -> GELU ->
+// Linear" per expert, with all experts' weights in one contiguous tensor
+// ([P2] 4.1 expert fusion) sliced by the group index -- and the same loop's
+// backward ([P1] 3.3: gradients flow back to the chosen experts).  Group g
+// (an expert) owns rows [offsets[g], offsets[g+1]) of the expert-contiguous
+// activation matrices.  Three operand geometries share one kernel:
+//
+//   Fwd   out[r,:] = act( A[r,:] . B_g^T )   A [rows,K], B_g [N,K]  (K-major)
+//   Dgrad out[r,:] = act( A[r,:] . B_g )     A [rows,K] K-major, B_g [K,N] (MN-major)
+//   Wgrad out_g    = A_g^T . B_g             A_g [rows_g,M], B_g [rows_g,N] (both MN-major),
+//                                             contraction over the group's rows
+//
+// Dgrad reads the weights in their stored layout (W2 [E,d,h] as B_g [K=d, N=h];
+// W1/W3 [E,h,d] as [K=h, N=d]) through MN-major shared-memory descriptors, so
+// no transposed copy of any weight is made.  Its K range may be split
+// between two weight tensors (dXp = dA.W1 + dB.W3 with A = [dA | dB]).
 //
 // Design (one persistent CTA per SM, 192 threads):
 //   warp 0  : TMA producer -- A tile 128x64 and B tile 256x64 (bf16, 128-byte
 //             swizzle) per k-block into a 4-stage shared-memory ring;
 //   warp 1  : owns 512 TMEM columns; one lane issues tcgen05.mma
 //             (M=128, N=256, K=16) into one of two 128x256 fp32 accumulators;
-//   warps 2-5: epilogue -- tcgen05.ld the accumulator, apply the activation,
-//             round to bf16, store the rows that belong to the group.
+//             for Wgrad the warp first clears the rows of a group's last
+//             k-block that belong to the next group;
+//   warps 2-5: epilogue -- tcgen05.ld the accumulator, apply the epilogue
+//             mode, store the rows / columns inside the output.
 // Accumulators are double-buffered so the epilogue of tile i overlaps the
-// MMAs of tile i+1.  The tile list (group, n-tile, m-tile) is derived on the
-// device from offsets[], so no host round-trip is needed for the
-// data-dependent per-expert row counts; m is the fastest index so that the
-// CTAs running at the same time share each weight tile through L2.
+// MMAs of tile i+1.  The tile list is derived on the device from offsets[],
+// so no host round-trip is needed for the data-dependent per-expert row
+// counts.  Fwd/Dgrad tiles run m fastest, so the CTAs running together share
+// each weight tile through L2; Wgrad tiles run along the smaller of M and N
+// fastest, so that operand stays in L2 while the other streams once.
 //
-// Modes:
-//   SwiGLU: B rows [0,128) come from W1 (gate) and [128,256) from W3 (up) at
-//           the same 128 output columns; out = silu(gate) * up.
-//   GeLU  : out = gelu(acc + bias);  Plain: out = acc (+ bias).
+// Epilogue modes (GemmMode): plain (+bias), SwiGLU (B rows [0,128) from W1
+// and [128,256) from W3 at the same 128 output columns: silu(gate) * up),
+// GeLU (gelu(acc + bias)), and the backward of both activations, which read
+// the pre-activations the forward saved.
 //
 // Every wait on a barrier is bounded (1 s); on expiry the kernel records an
 // error code in the workspace error word, drains its in-flight copies and
@@ -41,6 +54,7 @@ constexpr int STAGES = 4;
 constexpr int A_TILE_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_HALF_BYTES = 128 * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_TILE_BYTES + 2 * B_HALF_BYTES;
+constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN block of 64 K rows: 8 KB
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_GROUPS = 1024;
@@ -64,21 +78,67 @@ struct Tile {
   int g, n, m;
 };
 
-__device__ __forceinline__ Tile tile_coords(const Ctl& c, int G, int n_tiles, int tile) {
-  int lo = 0, hi = G;  // largest g with tile_start[g] <= tile (always a non-empty group)
+// Tile index -> (group, n-tile, m-tile).  Fwd/Dgrad: a group has
+// ceil(rows/BM) m-tiles per n-tile, m fastest.  Wgrad: every group has
+// m_tiles x n_tiles tiles, n fastest when n_fast.
+template <int KIND>
+__device__ __forceinline__ Tile tile_coords(const Ctl& c, int G, int n_tiles, int m_tiles, bool n_fast, int tile) {
+  int lo = 0, hi = G;  // largest g with tile_start[g] <= tile (a group with tiles)
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (c.tile_start[mid] <= tile) lo = mid; else hi = mid;
   }
   const int local = tile - c.tile_start[lo];
-  const int mt = (c.tile_start[lo + 1] - c.tile_start[lo]) / n_tiles;
   Tile t;
   t.g = lo;
-  t.n = local / mt;
-  t.m = local - t.n * mt;
+  if (KIND == kKindWgrad) {
+    if (n_fast) {
+      t.m = local / n_tiles;
+      t.n = local - t.m * n_tiles;
+    } else {
+      t.n = local / m_tiles;
+      t.m = local - t.n * m_tiles;
+    }
+  } else {
+    const int mt = (c.tile_start[lo + 1] - c.tile_start[lo]) / n_tiles;
+    t.n = local / mt;
+    t.m = local - t.n * mt;
+  }
   return t;
 }
 
+__device__ __forceinline__ void store_bf16x32(bf16* dst, int col, int N, const uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (col + q * 8 + 8 <= N)
+      *reinterpret_cast<uint4*>(dst + col + q * 8) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  }
+}
+
+__device__ __forceinline__ void store_f32x32(float* dst, int col, int N, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    if (col + q * 4 + 4 <= N)
+      *reinterpret_cast<float4*>(dst + col + q * 4) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
+
+// 32 consecutive bf16 (16-byte aligned) -> fp32; groups of 8 past N read as 0.
+__device__ __forceinline__ void load_bf16x32(const bf16* src, int col, int N, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (col + q * 8 + 8 <= N) u = *reinterpret_cast<const uint4*>(src + col + q * 8);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[q * 8 + 2 * i] = bf16lo(w[i]);
+      v[q * 8 + 2 * i + 1] = bf16hi(w[i]);
+    }
+  }
+}
+
+template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
                        const __grid_constant__ CUtensorMap mapB1, const GemmParams p) {
@@ -90,9 +150,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.G;
-  const bool swiglu = p.mode == kModeSwiGLU;
-  const int n_tiles = swiglu ? (p.N + 127) / 128 : (p.N + BN - 1) / BN;
-  const int nk = (p.K + BK - 1) / BK;
+  const bool swiglu_fwd = KIND == kKindFwd && p.mode == kModeSwiGLU;
+  const int n_tiles = swiglu_fwd ? (p.N + 127) / 128 : (p.N + BN - 1) / BN;
+  const int m_tiles_w = KIND == kKindWgrad ? (p.M + BM - 1) / BM : 1;
+  const bool n_fast = KIND == kKindWgrad && p.M > p.N;
+  const int nk_fixed = (p.K + BK - 1) / BK;
 
   // ---------------- set-up ----------------
   if (threadIdx.x == 0) {
@@ -125,9 +187,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
       if (g <= G) row = p.offsets ? p.offsets[g] : (g == 0 ? 0 : p.rows);
       int tiles_g = 0;
       if (g < G) {
-        const int r1 = p.offsets ? p.offsets[g + 1] : p.rows;
-        const int rows = r1 - row;
-        tiles_g = rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+        if (KIND == kKindWgrad) {
+          tiles_g = m_tiles_w * n_tiles;
+        } else {
+          const int r1 = p.offsets ? p.offsets[g + 1] : p.rows;
+          const int rows = r1 - row;
+          tiles_g = rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+        }
       }
       int incl = tiles_g;
 #pragma unroll
@@ -155,19 +221,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     if (lane == 0) {
       uint32_t it = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const Tile t = tile_coords(c, G, n_tiles, tile);
-        const int a_row = c.grp_row[t.g] + t.m * BM;
-        int b_row0, b_row1;
-        const CUtensorMap* mb1;
-        if (swiglu) {
-          b_row0 = t.g * p.N + t.n * 128;
-          b_row1 = b_row0;
-          mb1 = &mapB1;
-        } else {
-          b_row0 = t.g * p.N + t.n * BN;
-          b_row1 = b_row0 + 128;
-          mb1 = &mapB0;
-        }
+        const Tile t = tile_coords<KIND>(c, G, n_tiles, m_tiles_w, n_fast, tile);
+        const int grow = c.grp_row[t.g];
+        const int nk = KIND == kKindWgrad ? (c.grp_row[t.g + 1] - grow + BK - 1) / BK : nk_fixed;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -177,10 +233,39 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             break;
           }
           uint8_t* sa = tiles + s * STAGE_BYTES;
+          uint8_t* sb = sa + A_TILE_BYTES;
           mbar_arrive_expect_tx(&c.full[s], STAGE_BYTES);
-          tma_load_2d(sa, &mapA, &c.full[s], kb * BK, a_row);
-          tma_load_2d(sa + A_TILE_BYTES, &mapB0, &c.full[s], kb * BK, b_row0);
-          tma_load_2d(sa + A_TILE_BYTES + B_HALF_BYTES, mb1, &c.full[s], kb * BK, b_row1);
+          if (KIND == kKindFwd) {
+            tma_load_2d(sa, &mapA, &c.full[s], kb * BK, grow + t.m * BM);
+            if (swiglu_fwd) {
+              const int b_row = t.g * p.N + t.n * 128;
+              tma_load_2d(sb, &mapB0, &c.full[s], kb * BK, b_row);
+              tma_load_2d(sb + B_HALF_BYTES, &mapB1, &c.full[s], kb * BK, b_row);
+            } else {
+              const int b_row = t.g * p.N + t.n * BN;
+              tma_load_2d(sb, &mapB0, &c.full[s], kb * BK, b_row);
+              tma_load_2d(sb + B_HALF_BYTES, &mapB0, &c.full[s], kb * BK, b_row + 128);
+            }
+          } else if (KIND == kKindDgrad) {
+            tma_load_2d(sa, &mapA, &c.full[s], kb * BK, grow + t.m * BM);
+            int k0 = kb * BK;
+            const CUtensorMap* mb = &mapB0;
+            const int kb_rows = p.k_split ? p.k_split : p.K;
+            if (p.k_split && k0 >= p.k_split) {
+              mb = &mapB1;
+              k0 -= p.k_split;
+            }
+            const int y = t.g * kb_rows + k0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tma_load_2d(sb + i * MN_BLOCK_BYTES, mb, &c.full[s], t.n * BN + 64 * i, y);
+          } else {
+            const int y = grow + kb * BK;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) tma_load_2d(sa + i * MN_BLOCK_BYTES, &mapA, &c.full[s], t.m * BM + 64 * i, y);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              tma_load_2d(sb + i * MN_BLOCK_BYTES, &mapB0, &c.full[s], t.n * BN + 64 * i, y);
+          }
         }
       }
       if (*abort_flag) {
@@ -192,126 +277,241 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-      uint32_t it = 0, local = 0;
-      bool issued = false;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
-        const uint32_t acc = local & 1u;
-        const uint32_t aph = (local >> 1) & 1u;
-        if (!mbar_wait(&c.tmem_empty[acc], aph ^ 1u)) {
-          record_error(p.err, kErrWaitMma);
+    // ---------------- MMA issuer (lane 0 issues; the warp clears Wgrad tails) ----------------
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, KIND == kKindWgrad ? 1 : 0, KIND == kKindFwd ? 0 : 1);
+    uint32_t it = 0, local = 0;
+    bool issued = false;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      // one read of the abort flag for the whole warp keeps its lanes together
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const Tile t = tile_coords<KIND>(c, G, n_tiles, m_tiles_w, n_fast, tile);
+      const int grows = c.grp_row[t.g + 1] - c.grp_row[t.g];
+      const int nk = KIND == kKindWgrad ? (grows + BK - 1) / BK : nk_fixed;
+      const uint32_t acc = local & 1u;
+      const uint32_t aph = (local >> 1) & 1u;
+      bool ok = lane == 0 ? mbar_wait(&c.tmem_empty[acc], aph ^ 1u) : true;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) record_error(p.err, kErrWaitMma);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const uint32_t s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1u;
+        bool okf = lane == 0 ? mbar_wait(&c.full[s], ph) : true;
+        okf = __shfl_sync(0xffffffffu, okf, 0);
+        if (!okf) {
+          if (lane == 0) record_error(p.err, kErrWaitMma);
           *abort_flag = 1;
+          ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const uint32_t s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&c.full[s], ph)) {
-            record_error(p.err, kErrWaitMma);
-            *abort_flag = 1;
-            ok = false;
-            break;
+        uint8_t* sa = tiles + s * STAGE_BYTES;
+        uint8_t* sb = sa + A_TILE_BYTES;
+        if (KIND == kKindWgrad) {
+          const int valid = grows - kb * BK;  // in (0, BK]
+          if (valid < BK) {
+            // rows [valid, BK) of this k-block belong to the next group (or
+            // lie past the tensor): clear them in all six 64-row MN blocks.
+            // The phase completed already, so this wait returns at once and
+            // makes the copy's data visible to every lane.
+            mbar_wait(&c.full[s], ph);
+            const int nrow = BK - valid;
+            const int per_block = nrow * 8;  // 16-byte chunks
+            for (int q = lane; q < 6 * per_block; q += 32) {
+              const int blk = q / per_block;
+              const int rem = q - blk * per_block;
+              const int r = valid + (rem >> 3);
+              uint8_t* base = blk < 2 ? sa + blk * MN_BLOCK_BYTES : sb + (blk - 2) * MN_BLOCK_BYTES;
+              *reinterpret_cast<uint4*>(base + r * 128 + (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
           }
+          __syncwarp();
+        }
+        if (lane == 0) {
           tc_fence_after();
-          const uint32_t a_base = smem_u32(tiles + s * STAGE_BYTES);
-          const uint32_t b_base = a_base + A_TILE_BYTES;
+          const uint32_t a_base = smem_u32(sa);
+          const uint32_t b_base = smem_u32(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sw128_kmajor_desc(a_base + kk * 32);
-            const uint64_t bd = sw128_kmajor_desc(b_base + kk * 32);
+            const uint64_t ad =
+                KIND == kKindWgrad ? sw128_mnmajor_desc(a_base + kk * 2048) : sw128_kmajor_desc(a_base + kk * 32);
+            const uint64_t bd =
+                KIND == kKindFwd ? sw128_kmajor_desc(b_base + kk * 32) : sw128_mnmajor_desc(b_base + kk * 2048);
             tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          issued = true;
           tc_commit(&c.empty[s]);
         }
-        if (!ok) break;
-        tc_commit(&c.tmem_full[acc]);
+        __syncwarp();
+        issued = true;
       }
-      if (*abort_flag && issued) {
-        tc_commit(&c.drain);
-        if (!mbar_wait(&c.drain, 0)) record_error(p.err, kErrWaitDrain);
-      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&c.tmem_full[acc]);
+      __syncwarp();
+    }
+    if (*abort_flag && issued && lane == 0) {
+      tc_commit(&c.drain);
+      if (!mbar_wait(&c.drain, 0)) record_error(p.err, kErrWaitDrain);
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32)
     uint32_t local = 0;
-    for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
-      const Tile t = tile_coords(c, G, n_tiles, tile);
-      const long long row_end = min(static_cast<long long>(c.grp_row[t.g + 1]), p.rows_alloc);
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      // tcgen05.ld is warp-collective: the warp decides to stop as one
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const Tile t = tile_coords<KIND>(c, G, n_tiles, m_tiles_w, n_fast, tile);
+      const int grow = c.grp_row[t.g];
+      const int gend = c.grp_row[t.g + 1];
       const uint32_t acc = local & 1u;
       const uint32_t aph = (local >> 1) & 1u;
-      if (!mbar_wait(&c.tmem_full[acc], aph)) {
-        record_error(p.err, kErrWaitEpilogue);
+      if (!__all_sync(0xffffffffu, mbar_wait(&c.tmem_full[acc], aph))) {
+        if (lane == 0) record_error(p.err, kErrWaitEpilogue);
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const int row = c.grp_row[t.g] + t.m * BM + quarter * 32 + lane;
-      const bool valid = row < row_end;
+      const int rt = quarter * 32 + lane;  // accumulator row of this thread
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      bf16* orow = static_cast<bf16*>(p.out) + static_cast<size_t>(row) * p.N;
-      if (swiglu) {
-        const int col0 = t.n * 128;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t gr[32], ur[32];
-          tmem_ld_32x32b_x32(taddr + cc * 32, gr);
-          tmem_ld_32x32b_x32(taddr + 128 + cc * 32, ur);
-          tmem_ld_wait();
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
-            const float u0 = __uint_as_float(ur[2 * i]), u1 = __uint_as_float(ur[2 * i + 1]);
-            pk[i] = pack_bf16(silu_f(g0) * u0, silu_f(g1) * u1);
-          }
-          if (valid) {
-            const int col = col0 + cc * 32;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (col + q * 8 + 8 <= p.N)
-                *reinterpret_cast<uint4*>(orow + col + q * 8) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
-          }
+
+      if (KIND == kKindWgrad) {
+        // out_g[m, n] fp32; a group with no rows has a zero gradient
+        const bool empty = gend == grow;
+        const int m = t.m * BM + rt;
+        const bool valid = m < p.M;
+        float* orow = nullptr;
+        if (valid) {
+          const int M1 = p.m_split ? p.m_split : p.M;
+          if (m < M1)
+            orow = static_cast<float*>(p.out) + (static_cast<size_t>(t.g) * M1 + m) * p.N;
+          else
+            orow = static_cast<float*>(p.out2) + (static_cast<size_t>(t.g) * (p.M - M1) + (m - M1)) * p.N;
         }
-      } else {
-        const int col0 = t.n * BN;
-        const bool gelu = p.mode == kModeGeLU;
-        const bf16* brow = p.bias ? static_cast<const bf16*>(p.bias) + static_cast<size_t>(t.g) * p.N : nullptr;
 #pragma unroll 1
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int cc = 0; cc < BN / 32; ++cc) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + cc * 32, r);
           tmem_ld_wait();
-          const int col = col0 + cc * 32;
-          uint32_t pk[16];
+          float v[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float v0 = __uint_as_float(r[2 * i]), v1 = __uint_as_float(r[2 * i + 1]);
-            if (brow) {
-              const int c0 = col + 2 * i;
-              if (c0 < p.N) v0 += __bfloat162float(brow[c0]);
-              if (c0 + 1 < p.N) v1 += __bfloat162float(brow[c0 + 1]);
+          for (int i = 0; i < 32; ++i) v[i] = empty ? 0.f : __uint_as_float(r[i]);
+          if (valid) store_f32x32(orow, t.n * BN + cc * 32, p.N, v);
+        }
+      } else {
+        const long long row_end = min(static_cast<long long>(gend), p.rows_alloc);
+        const int row = grow + t.m * BM + rt;
+        const bool valid = row < row_end;
+        if (swiglu_fwd) {
+          bf16* orow = static_cast<bf16*>(p.out) + static_cast<size_t>(row) * p.ldo;
+          bf16* zrow = p.zsave ? static_cast<bf16*>(p.zsave) + static_cast<size_t>(row) * p.ldz : nullptr;
+          const int col0 = t.n * 128;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t gr[32], ur[32];
+            tmem_ld_32x32b_x32(taddr + cc * 32, gr);
+            tmem_ld_32x32b_x32(taddr + 128 + cc * 32, ur);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
+              const float u0 = __uint_as_float(ur[2 * i]), u1 = __uint_as_float(ur[2 * i + 1]);
+              pk[i] = pack_bf16(silu_f(g0) * u0, silu_f(g1) * u1);
             }
-            if (gelu) {
-              v0 = gelu_f(v0);
-              v1 = gelu_f(v1);
+            const int col = col0 + cc * 32;
+            if (valid) {
+              store_bf16x32(orow, col, p.N, pk);
+              if (zrow) {
+                uint32_t zg[16], zu[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  zg[i] = pack_bf16(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
+                  zu[i] = pack_bf16(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
+                }
+                store_bf16x32(zrow, col, p.N, zg);
+                store_bf16x32(zrow + p.N, col, p.N, zu);
+              }
             }
-            pk[i] = pack_bf16(v0, v1);
           }
-          if (valid) {
+        } else {
+          const int col0 = t.n * BN;
+          const int mode = p.mode;
+          const bf16* brow =
+              p.bias ? static_cast<const bf16*>(p.bias) + static_cast<size_t>(t.g) * p.N : nullptr;
+          const bf16* zin = (mode == kModeSwiGLUBwd || mode == kModeGeLUBwd) && valid
+                                ? static_cast<const bf16*>(p.zin) + static_cast<size_t>(row) * p.ldz
+                                : nullptr;
+          bf16* zrow = p.zsave && mode == kModeGeLU && valid
+                           ? static_cast<bf16*>(p.zsave) + static_cast<size_t>(row) * p.ldz
+                           : nullptr;
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + cc * 32, r);
+            tmem_ld_wait();
+            const int col = col0 + cc * 32;
+            float v[32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (col + q * 8 + 8 <= p.N)
-                *reinterpret_cast<uint4*>(orow + col + q * 8) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            if (!valid) continue;
+            if (mode == kModeSwiGLUBwd) {
+              // dH = acc; gate g, up u: dA = dH u silu'(g), dB = dH silu(g)
+              float g[32], u[32];
+              load_bf16x32(zin, col, p.N, g);
+              load_bf16x32(zin + p.N, col, p.N, u);
+              uint32_t pa[16], pb[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float da[2], db[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  const int e = 2 * i + h2;
+                  const float sg = sigmoid_f(g[e]);
+                  const float sl = g[e] * sg;
+                  da[h2] = v[e] * u[e] * (sg * (1.0f + g[e] * (1.0f - sg)));
+                  db[h2] = v[e] * sl;
+                }
+                pa[i] = pack_bf16(da[0], da[1]);
+                pb[i] = pack_bf16(db[0], db[1]);
+              }
+              bf16* orow = static_cast<bf16*>(p.out) + static_cast<size_t>(row) * p.ldo;
+              store_bf16x32(orow, col, p.N, pa);
+              store_bf16x32(orow + p.N, col, p.N, pb);
+              continue;
+            }
+            if (mode == kModeGeLUBwd) {
+              float z[32];
+              load_bf16x32(zin, col, p.N, z);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(z[i]);
+            } else {
+              if (brow) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col + i < p.N) v[i] += __bfloat162float(brow[col + i]);
+              }
+              if (mode == kModeGeLU) {
+                if (zrow) {
+                  uint32_t zp[16];
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) zp[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+                  store_bf16x32(zrow, col, p.N, zp);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+              }
+            }
+            if (p.out_f32) {
+              store_f32x32(static_cast<float*>(p.out) + static_cast<size_t>(row) * p.ldo, col, p.N, v);
+            } else {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+              store_bf16x32(static_cast<bf16*>(p.out) + static_cast<size_t>(row) * p.ldo, col, p.N, pk);
             }
           }
         }
@@ -329,42 +529,75 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
   }
 }
 
+template <int KIND>
+moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
+                       long long tiles_bound, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return MOE_ERR_CUDA;
+  static bool attr_set[64] = {false};
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  long long grid = tiles_bound;
+  if (grid > sms) grid = sms;
+  if (grid < 1) grid = 1;
+  grouped_gemm_tc_kernel<KIND><<<static_cast<unsigned>(grid), NUM_THREADS, kSmemBytes, stream>>>(mA, mB0, mB1, p);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-moe_status launch_grouped_gemm_tc(const GemmParams& p_in, const void* A, long long a_rows, const void* B0,
+moe_status launch_grouped_gemm_tc(const GemmParams& p_in, int kind, const void* A, long long a_rows, const void* B0,
                                   const void* B1, long long b_rows, cudaStream_t stream) {
   GemmParams p = p_in;
   p.rows_alloc = a_rows;
-  if (p.G < 1 || p.G > MAX_GROUPS || p.N < 8 || p.K < 8 || (p.N % 8) || (p.K % 8)) return MOE_ERR_UNSUPPORTED;
+  if (p.ldo == 0) p.ldo = p.N;
+  if (p.G < 1 || p.G > MAX_GROUPS || p.N < 8 || (p.N % 8) || !p.out) return MOE_ERR_UNSUPPORTED;
   if (a_rows <= 0) return MOE_OK;
+  if (a_rows > 2147483647LL || b_rows > 2147483647LL) return MOE_ERR_UNSUPPORTED;
   CUtensorMap mA, mB0, mB1;
-  if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BM)) return MOE_ERR_CUDA;
-  if (!make_tma_2d_bf16(&mB0, B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
-  if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
-
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  const int sms = device_sm_count(dev);
-  if (sms <= 0) return MOE_ERR_CUDA;
-  static thread_local int attr_set_dev = -1;
-  if (attr_set_dev != dev) {
-    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set_dev = dev;
+  const int n_tiles_swiglu = (p.N + 127) / 128;
+  const long long n_tiles = (kind == kKindFwd && p.mode == kModeSwiGLU) ? n_tiles_swiglu : (p.N + BN - 1) / BN;
+  if (kind == kKindFwd) {
+    if (p.K < 8 || (p.K % 8)) return MOE_ERR_UNSUPPORTED;
+    if (p.mode == kModeSwiGLUBwd || p.mode == kModeGeLUBwd) return MOE_ERR_UNSUPPORTED;
+    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BM)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB0, B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
+    const long long rows_bound = p.offsets ? a_rows : p.rows;
+    const long long m_tiles_bound = (rows_bound + BM - 1) / BM + (p.offsets ? p.G : 0);
+    return launch_kind<kKindFwd>(p, mA, mB0, mB1, m_tiles_bound * n_tiles, stream);
   }
-  const bool swiglu = p.mode == kModeSwiGLU;
-  const long long n_tiles = swiglu ? (p.N + 127) / 128 : (p.N + BN - 1) / BN;
-  const long long rows_bound = p.offsets ? a_rows : p.rows;
-  const long long m_tiles_bound = (rows_bound + BM - 1) / BM + (p.offsets ? p.G : 0);
-  long long grid = m_tiles_bound * n_tiles;
-  if (grid > sms) grid = sms;
-  if (grid < 1) grid = 1;
-  grouped_gemm_tc_kernel<<<static_cast<unsigned>(grid), NUM_THREADS, kSmemBytes, stream>>>(mA, mB0, mB1, p);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (kind == kKindDgrad) {
+    // whole 64-deep k-blocks per weight tensor, so a block never mixes groups or tensors
+    if (p.K < BK || (p.K % BK) || (p.k_split && (p.k_split % BK || p.K != 2 * p.k_split))) return MOE_ERR_UNSUPPORTED;
+    if (p.k_split && !B1) return MOE_ERR_INVALID_ARG;
+    if (p.mode == kModeSwiGLU || p.mode == kModeGeLU) return MOE_ERR_UNSUPPORTED;
+    if ((p.mode == kModeSwiGLUBwd || p.mode == kModeGeLUBwd) && !p.zin) return MOE_ERR_INVALID_ARG;
+    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BM)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB0, B0, p.N, b_rows, 64, BK)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.N, b_rows, 64, BK)) return MOE_ERR_CUDA;
+    const long long rows_bound = p.offsets ? a_rows : p.rows;
+    const long long m_tiles_bound = (rows_bound + BM - 1) / BM + (p.offsets ? p.G : 0);
+    return launch_kind<kKindDgrad>(p, mA, mB0, mB1, m_tiles_bound * n_tiles, stream);
+  }
+  if (kind == kKindWgrad) {
+    if (p.M < 8 || (p.M % 8) || !p.out_f32 || p.mode != kModePlain) return MOE_ERR_UNSUPPORTED;
+    if (p.m_split && (p.m_split % 8 || p.m_split >= p.M || !p.out2)) return MOE_ERR_UNSUPPORTED;
+    if (!make_tma_2d_bf16(&mA, A, p.M, a_rows, 64, BK)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB0, B0, p.N, a_rows, 64, BK)) return MOE_ERR_CUDA;
+    const long long tiles = static_cast<long long>(p.G) * ((p.M + BM - 1) / BM) * n_tiles;
+    return launch_kind<kKindWgrad>(p, mA, mB0, mB0, tiles, stream);
+  }
+  return MOE_ERR_INVALID_ARG;
 }
 
 }  // namespace moe

@@ -9,24 +9,51 @@
 
 namespace moe {
 
-enum GemmMode : int { kModePlain = 0, kModeSwiGLU = 1, kModeGeLU = 2 };
+// Epilogue of a grouped GEMM (acc = the fp32 accumulator of one output element).
+enum GemmMode : int {
+  kModePlain = 0,      // out = acc (+ bias)
+  kModeSwiGLU = 1,     // out = silu(gate) * up (B tile pairs W1 and W3 rows); zsave: gate | up
+  kModeGeLU = 2,       // out = gelu(acc + bias); zsave: acc + bias
+  kModeSwiGLUBwd = 3,  // g = zin[r,n], u = zin[r,N+n]: out[r,n] = acc*u*silu'(g), out[r,N+n] = acc*silu(g)
+  kModeGeLUBwd = 4,    // out = acc * gelu'(zin[r,n])
+};
 
-// One grouped GEMM: out[r, :] = act(A[r, :] . B_g^T) for the rows r of each group.
+// Operand geometry of a grouped GEMM launch.
+enum GemmKind : int {
+  kKindFwd = 0,    // out[r,:] = A[r,:] . B_g^T; A [rows,K] and B_g [N,K] both K-contiguous
+  kKindDgrad = 1,  // out[r,:] = A[r,:] . B_g;   A [rows,K] K-contiguous, B_g [K,N] N-contiguous
+  kKindWgrad = 2,  // out_g = A_g^T . B_g over the group's rows; A [rows,M], B [rows,N]
+};
+
+// One grouped GEMM.  Groups (experts) own the row ranges [offsets[g],
+// offsets[g+1]) of the activation matrices: the output rows (Fwd, Dgrad) or
+// the contraction (Wgrad).
 struct GemmParams {
   const int* offsets;    // [G+1] device row offsets, or nullptr: one group of `rows` rows
   int G;                 // groups (experts)
   int rows;              // rows of the single group when offsets == nullptr
-  long long rows_alloc;  // rows allocated in A and out: no row at or past it is written (set by the launcher)
-  int N;                 // output columns per group (rows of B per group)
-  int K;                 // contraction length
+  long long rows_alloc;  // rows allocated in the activation operands (set by the launcher)
+  int M;                 // Wgrad: output rows per group
+  int N;                 // output columns (per group)
+  int K;                 // Fwd/Dgrad: contraction length
+  int k_split;           // Dgrad: k < k_split reads B0 rows, k >= k_split reads B1 rows k - k_split (0: B0 only)
+  int m_split;           // Wgrad: output rows m >= m_split go to out2 (row m - m_split); 0: all to out
   int mode;              // GemmMode
-  void* out;             // [*, N] row-major, storage type of the path
+  int out_f32;           // output element type: 1 fp32, 0 bf16
+  void* out;             // Fwd/Dgrad: [rows, ldo]; Wgrad: [G, M or m_split, N]
+  void* out2;            // Wgrad second output [G, M - m_split, N]
+  long long ldo;         // Fwd/Dgrad row stride of out (elements); 0: N
+  void* zsave;           // Fwd SwiGLU/GeLU: pre-activations out (bf16), nullable
+  const void* zin;       // *Bwd modes: saved pre-activations (bf16)
+  long long ldz;         // row stride of zsave / zin (elements)
   const void* bias;      // [G, N] nullable (GeLU / plain)
   int* err;              // workspace error word
 };
 
-// sm_103a tensor-core path (bf16 in, fp32 accumulate, bf16 out).
-moe_status launch_grouped_gemm_tc(const GemmParams& p, const void* A, long long a_rows, const void* B0,
+// sm_103a tensor-core path (bf16 in, fp32 accumulate).  A: the activation
+// operand (a_rows rows); B0/B1: weights (b_rows rows each) for Fwd/Dgrad, or
+// B0 = the second activation operand (a_rows rows) for Wgrad.
+moe_status launch_grouped_gemm_tc(const GemmParams& p, int kind, const void* A, long long a_rows, const void* B0,
                                   const void* B1, long long b_rows, cudaStream_t stream);
 
 // fp32 CUDA-core path (fp32 storage and arithmetic).
@@ -53,6 +80,19 @@ moe_status static_dispatch_scratch(size_t need, void** ptr);
 // Combine / un-permute.
 moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos, const float* w,
                           const void* Sx, void* y, cudaStream_t stream);
+
+// Backward pieces outside the expert GEMMs (backward.cu).
+size_t router_wgrad_partial_bytes(const moe_config& cfg);
+moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* Yp, const int* pos, const float* w,
+                             void* dYp, float* dot, cudaStream_t st);
+moe_status launch_router_bwd(const moe_config& cfg, const int* idx, const float* w, const float* dot,
+                             unsigned long long* imp, float* coef, float* dl, cudaStream_t st);
+moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl, float* partial,
+                               float* dWr, cudaStream_t st);
+moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,
+                         const void* Wr, int accumulate, float* dX, cudaStream_t st);
+moe_status launch_group_colsum(const void* src, long long ld, const int* offsets, int G, int rows, int N, float* out,
+                               cudaStream_t st);
 
 // TMA descriptor of a row-major bf16 matrix [rows, inner] with a
 // (box_inner x box_rows) box and 128-byte swizzling.

@@ -37,7 +37,12 @@ class MoeWeights(ctypes.Structure):
 
 class MoeSaved(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("idx", "w", "counts", "kept", "offsets", "pos", "Xp", "H", "Yp", "Sx")]
+                ("idx", "w", "counts", "kept", "offsets", "pos", "Xp", "H", "Yp", "Sx", "Z", "Hs", "Zs")]
+
+
+class MoeGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("dX", "dWr", "dW1", "dW3", "dW2", "db1", "db2", "dWs1", "dWs3", "dWs2", "dbs1", "dbs2")]
 
 
 class MoeStats(ctypes.Structure):
@@ -52,7 +57,7 @@ class MoeStats(ctypes.Structure):
 
 EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_static",
            "moe_expert_ffn",
-           "moe_combine", "moe_layer_fwd", "moe_check_error", "moe_status_string")
+           "moe_combine", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error", "moe_status_string")
 
 _lib = None
 
@@ -77,6 +82,8 @@ def lib() -> ctypes.CDLL:
             "moe_combine": [cfgp, vp, vp, vp, vp, vp, vp],
             "moe_layer_fwd": [cfgp, ctypes.POINTER(MoeWeights), vp, vp, vp, ctypes.POINTER(MoeSaved), vp, vp,
                               sz, vp],
+            "moe_layer_bwd": [cfgp, ctypes.POINTER(MoeWeights), vp, ctypes.POINTER(MoeSaved), vp,
+                              ctypes.POINTER(MoeGrads), vp, sz, vp],
             "moe_check_error": [vp, ctypes.POINTER(i), vp],
             "moe_status_string": [i],
         }
@@ -126,14 +133,15 @@ def moe_capacity(cfg: MoeConfig) -> int:
     return c.value
 
 
-def moe_workspace_size(cfg: MoeConfig, training: bool = False) -> int:
+def moe_workspace_size(cfg: MoeConfig, training: int = 0) -> int:
+    """training: 0 inference forward, 1 training forward, 2 backward."""
     n = ctypes.c_size_t()
     _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(cfg), int(training), ctypes.byref(n)))
     return n.value
 
 
-def workspace(cfg: MoeConfig, training=False, device="cuda") -> torch.Tensor:
-    return torch.empty(moe_workspace_size(cfg, training), dtype=torch.uint8, device=device)
+def workspace(cfg: MoeConfig, training=0, device="cuda") -> torch.Tensor:
+    return torch.empty(moe_workspace_size(cfg, int(training)), dtype=torch.uint8, device=device)
 
 
 def stats_buffer(device="cuda") -> torch.Tensor:
@@ -189,6 +197,41 @@ def moe_layer_fwd(cfg, weights: dict, x, noise, y, saved: Optional[dict], stats,
                                                 ws.numel(), _stream(stream)))
 
 
+def grads_struct(t: dict) -> MoeGrads:
+    return MoeGrads(*[(t[n].data_ptr() if t.get(n) is not None else None) for n, _ in MoeGrads._fields_])
+
+
+def moe_layer_bwd(cfg, weights: dict, x, saved: dict, dY, grads: dict, ws, stream=None):
+    W = weights_struct(weights)
+    S = saved_struct(saved)
+    G = grads_struct(grads)
+    _check("moe_layer_bwd", lib().moe_layer_bwd(ctypes.byref(cfg), ctypes.byref(W), _p(x), ctypes.byref(S), _p(dY),
+                                                ctypes.byref(G), _p(ws), ws.numel(), _stream(stream)))
+
+
+def alloc_grads(cfg: MoeConfig, device="cuda") -> dict:
+    """Caller-owned fp32 gradient buffers of one backward (the moe_grads set)."""
+    T, E, d, h = cfg.T, cfg.E, cfg.d, cfg.h
+    f = dict(dtype=torch.float32, device=device)
+    swiglu = cfg.act == ACT["swiglu"]
+    out = dict(dX=torch.empty(T, d, **f), dWr=torch.empty(E, d, **f), dW1=torch.empty(E, h, d, **f),
+               dW2=torch.empty(E, d, h, **f))
+    if swiglu:
+        out["dW3"] = torch.empty(E, h, d, **f)
+    else:
+        out["db1"] = torch.empty(E, h, **f)
+        out["db2"] = torch.empty(E, d, **f)
+    if cfg.has_shared:
+        out["dWs1"] = torch.empty(h, d, **f)
+        out["dWs2"] = torch.empty(d, h, **f)
+        if swiglu:
+            out["dWs3"] = torch.empty(h, d, **f)
+        else:
+            out["dbs1"] = torch.empty(h, **f)
+            out["dbs2"] = torch.empty(d, **f)
+    return out
+
+
 def moe_check_error(ws, stream=None) -> int:
     code = ctypes.c_int()
     st = lib().moe_check_error(_p(ws), ctypes.byref(code), _stream(stream))
@@ -197,8 +240,10 @@ def moe_check_error(ws, stream=None) -> int:
     return code.value
 
 
-def alloc_saved(cfg: MoeConfig, device="cuda") -> dict:
-    """Caller-owned buffers of one forward (the moe_saved set)."""
+def alloc_saved(cfg: MoeConfig, device="cuda", backward=False) -> dict:
+    """Caller-owned buffers of one forward (the moe_saved set); with
+    backward=True also the pre-activations and shared hidden rows that
+    moe_layer_bwd reads."""
     T, k, E, d, h = cfg.T, cfg.k, cfg.E, cfg.d, cfg.h
     dt = torch.bfloat16 if cfg.dtype == DTYPE["bf16"] else torch.float32
     out = dict(idx=torch.empty(T, k, dtype=torch.int32, device=device),
@@ -212,4 +257,10 @@ def alloc_saved(cfg: MoeConfig, device="cuda") -> dict:
                Yp=torch.empty(T * k, d, dtype=dt, device=device))
     if cfg.has_shared:
         out["Sx"] = torch.empty(T, d, dtype=dt, device=device)
+    if backward:
+        hz = 2 * h if cfg.act == ACT["swiglu"] else h
+        out["Z"] = torch.empty(T * k, hz, dtype=dt, device=device)
+        if cfg.has_shared:
+            out["Hs"] = torch.empty(T, h, dtype=dt, device=device)
+            out["Zs"] = torch.empty(T, hz, dtype=dt, device=device)
     return out

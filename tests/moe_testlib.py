@@ -62,3 +62,30 @@ def max_abs(a: np.ndarray, b: np.ndarray) -> float:
 def assert_close_bf16(got: np.ndarray, ref: np.ndarray, what: str, rel=1e-2, mabs=2e-2):
     rf, ma = rel_frob(got, ref), max_abs(got, ref)
     assert rf <= rel and ma <= mabs, f"{what}: rel-Frobenius {rf:.3e} (<= {rel}), max-abs {ma:.3e} (<= {mabs})"
+
+
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 -> bf16 (round to nearest even) -> fp64."""
+    return torch.tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def bf16_storage_model_expert_grads(t: dict, route: dict, dY, e: int) -> dict:
+    """Expert e's SwiGLU weight gradients computed in fp64 but with the
+    values rounded to bf16 wherever the layer stores them in bf16 between
+    kernels: the saved gate/up pre-activations, the hidden rows H, the
+    scaled upstream rows w*dY, and dA/dB.  A model of the storage
+    arithmetic (not the oracle): it explains the layer's deviation from the
+    fp64 oracle, so the GPU must match it much more tightly."""
+    rows, slots = np.nonzero((route["idx"] == e) & (route["pos"] >= 0))
+    v = O.decode(t["x"])[rows]
+    W1, W3, W2 = (O.decode(t[n][e]) for n in ("W1", "W3", "W2"))
+    a = v @ W1.T
+    b = v @ W3.T
+    g, u = round_bf16(a), round_bf16(b)
+    H = round_bf16(O.silu(a) * b)
+    w32 = route["w"][rows, slots].astype(np.float32).astype(np.float64)
+    dYp = round_bf16(w32[:, None] * O.decode(dY)[rows])
+    dH = dYp @ W2
+    dA = round_bf16(dH * u * O.silu_grad(g))
+    dB = round_bf16(dH * O.silu(g))
+    return dict(dW1=dA.T @ v, dW3=dB.T @ v, dW2=dYp.T @ H)

@@ -438,3 +438,36 @@ def test_backward_balance_term_isolated():
     # a dZero upstream leaves only the balance term
     gz = O.layer_backward(dict(base, lam=0.01), w, x, np.zeros_like(dY))
     np.testing.assert_allclose(gz["dWr"], g1["dWr"] - g0["dWr"], atol=1e-12)
+
+
+@pytest.mark.parametrize("act,shared", [("swiglu", True), ("gelu", False)])
+def test_sampled_backward_entries_match_full_backward(act, shared):
+    """The sampled-entry functions used at full size agree with the
+    finite-difference-pinned layer_backward on a tiny batch."""
+    rng = _rng(71)
+    T, d, h, E, k = 30, 6, 10, 4, 2
+    w = dict(Wr=rng.normal(size=(E, d)), W1=rng.normal(size=(E, h, d)) / 2, W2=rng.normal(size=(E, d, h)) / 3)
+    if act == "swiglu":
+        w["W3"] = rng.normal(size=(E, h, d)) / 2
+    else:
+        w["b1"] = rng.normal(size=(E, h)) * 0.1
+        w["b2"] = rng.normal(size=(E, d)) * 0.1
+    if shared:
+        w.update(Ws1=rng.normal(size=(h, d)) / 2, Ws3=rng.normal(size=(h, d)) / 2, Ws2=rng.normal(size=(d, h)) / 3)
+    cfg = dict(T=T, d=d, h=h, E=E, k=k, act=act, capacity_factor=0.75, has_shared=shared, lam=0.05)
+    x = rng.normal(size=(T, d))
+    dY = rng.normal(size=(T, d))
+    full = O.layer_backward(cfg, w, x, dY)
+    r = full["route"]
+    assert (r["pos"] < 0).any()
+    for e in range(E):
+        cols = [1, 4, 7]
+        sl = O.expert_grad_slices(cfg, w, x, dY, r, e, cols)
+        np.testing.assert_allclose(sl["dW1"], full["dW1"][e][cols], atol=1e-12)
+        np.testing.assert_allclose(sl["dW2"], full["dW2"][e][:, cols], atol=1e-12)
+        if act == "swiglu":
+            np.testing.assert_allclose(sl["dW3"], full["dW3"][e][cols], atol=1e-12)
+        else:
+            np.testing.assert_allclose(sl["db1"], full["db1"][e][cols], atol=1e-12)
+    toks = [0, 3, 11, 29]
+    np.testing.assert_allclose(O.token_input_grads(cfg, w, x, dY, r, toks), full["dX"][toks], atol=1e-12)
