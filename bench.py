@@ -159,9 +159,6 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     stream = torch.cuda.current_stream(dev)
 
     Hs = torch.empty(wl.T, wl.h, dtype=torch.bfloat16, device=dev) if wl.has_shared else None
-    sh_off = torch.tensor([0, wl.T], dtype=torch.int32, device=dev)
-    sh_cfg = M.make_config(wl.T, wl.d, wl.h, 1, 1, wl.act, wl.dtype)
-    ws_sh = M.moe.workspace(sh_cfg, device=dev) if wl.has_shared else None
     sv = saved
 
     # one step = the layer's C-ABI stages in the order moe_layer_fwd runs them
@@ -175,9 +172,9 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
                                                 sv["Yp"], ws)),
     ]
     if wl.has_shared:
-        stages.append(("shared_ffn", lambda: M.moe_expert_ffn(sh_cfg, x, sh_off, weights["Ws1"], weights.get("Ws3"),
-                                                              weights.get("bs1"), weights["Ws2"],
-                                                              weights.get("bs2"), Hs, sv["Sx"], ws_sh)))
+        # routed experts and the shared expert in the same two launches
+        stages[-1] = ("expert_ffn", lambda: M.moe.moe_expert_ffn_shared(cfg, sv["Xp"], sv["offsets"], weights,
+                                                                         sv["H"], sv["Yp"], x, Hs, sv["Sx"], ws))
     stages.append(("combine", lambda: M.moe_combine(cfg, sv["Yp"], sv["pos"], sv["w"], sv.get("Sx"), y)))
 
     def step():
@@ -240,7 +237,7 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     out = {
         "ms_per_step": ms_step,
         "layer_fwd_ms": layer_fwd_ms,
-        "launches_per_step": 8 + (2 if wl.has_shared else 0),
+        "launches_per_step": 8,
         "tokens_per_s": tokens / (ms_step * 1e-3),
         "stats": stats,
         "components_ms": comp,
@@ -518,7 +515,7 @@ def main():
         dargs.steps = max(args.steps, 100)  # >= 0.25 s timed, so the clock sampler sees it
         d = run_gpu(dargs, "decode", world, rank, local)
         dwl = d["wl"]
-        ffn_ms = d["components_ms"]["expert_ffn"] + d["components_ms"]["shared_ffn"]
+        ffn_ms = d["components_ms"]["expert_ffn"]
         gbs = d["touched_weight_bytes"] / (ffn_ms * 1e-3) / 1e9
         line["decode"] = {"workload": f"decode: T={dwl.T} d={dwl.d} h={dwl.h} E={dwl.E}+1 shared top-{dwl.k}",
                           "ms_per_step": d["ms_per_step"], "tokens_per_s": d["tokens_per_s"],

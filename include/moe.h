@@ -170,7 +170,10 @@ moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes
  *   counts[e] = #slots routed to e (zeroed by this call)
  * x [T,d], Wr [E,d] in cfg->dtype; expert_bias [E], noise [T,E] fp32,
  * both nullable.  Outputs idx [T,k] int32, w [T,k] fp32, counts [E] int32.
- * ws: unused, may be NULL. */
+ * ws: NULL, or >= moe_workspace_size(cfg, 1) bytes; with it a batch too
+ * small to fill the GPU splits the contraction over more CTAs (the
+ * partial logits are summed in a fixed order, so results repeat bit for
+ * bit either way). */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr,
                      const float* expert_bias, const float* noise, int* idx,
                      float* w, int* counts, void* ws, moe_stream_t stream);
@@ -226,6 +229,19 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offs
                           const void* W1, const void* W3, const void* b1,
                           const void* W2, const void* b2, void* H, void* Yp,
                           void* ws, moe_stream_t stream);
+
+/* moe_expert_ffn plus the always-on shared expert ([P5] "Shared experts":
+ * every token also passes through one more FFN), in the same two launches:
+ * the shared expert is one more group of T rows with its own operands, so
+ * its weight streaming overlaps the routed experts'.  In addition to
+ * moe_expert_ffn's outputs:
+ *   Hs[t] = act(Ws1 x[t] ...) [T,h];   Sx[t] = Ws2 Hs[t] (+ bs2)  [T,d]
+ * bf16 only (MOE_ERR_UNSUPPORTED otherwise).  wts supplies W1, W3, b1, W2,
+ * b2 and Ws1, Ws3, Ws2, bs1, bs2 (Wr and expert_bias are not read).
+ * ws: >= moe_workspace_size(cfg, 1) bytes. */
+moe_status moe_expert_ffn_shared(const moe_config* cfg, const void* Xp, const int* offsets,
+                                 const moe_weights* wts, void* H, void* Yp, const void* x,
+                                 void* Hs, void* Sx, void* ws, moe_stream_t stream);
 
 /* Weighted combine / un-permute ([P5] "Who decides which experts to call?":
  * 0.75*[0.8,0.2,-0.4] + 0.25*[0.4,0.6,0.8] = [0.7,0.3,-0.1]; [P5] "Shared

@@ -194,6 +194,11 @@ WORKLOADS: Dict[str, Workload] = {
     # the same GEMM tile shapes at 1/16 of the device memory (profiling case)
     "large_prefill_slice": Workload("large_prefill_slice", 1024, 4096, 14336, 4, 2, "swiglu", "bf16",
                                     1.25, 0, 0.01, False, 2, None, 1.1, False, False),
+    # fine-grained routing: E=384 routed experts, top-6, plus 1 shared expert;
+    # T=8192, d=4096, SwiGLU h=1024 (the widths are this workload's choice),
+    # cf=1.25 (C=160)
+    "fine_grained": Workload("fine_grained", 8192, 4096, 1024, 384, 6, "swiglu", "bf16", 1.25, 0,
+                             0.01, True, 5, None, None, False, False),
     # T=64, d=4096, E=128 routed + 1 shared, SwiGLU h=8192, no capacity limit
     "decode": Workload("decode", 64, 4096, 8192, 128, 2, "swiglu", "bf16", 0.0, 0, 0.01,
                        True, 3, None, None, False, False),

@@ -39,7 +39,7 @@ size_t esize(const moe_config* cfg) { return cfg->dtype == MOE_BF16 ? 2 : 4; }
 // [header | dYp | dAB | dXp | dot | dl | importance | coef | router partials
 // | shared dAB].
 struct WsLayout {
-  size_t dispatch_off;
+  size_t dispatch_off, route_off;
   size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs;
   size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs;
   size_t total;
@@ -69,6 +69,7 @@ WsLayout layout(const moe_config* cfg, int training) {
     return L;
   }
   L.dispatch_off = take(dispatch_scratch_bytes(*cfg));
+  L.route_off = take(route_scratch_bytes(*cfg));
   if (!training) {
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
@@ -90,9 +91,19 @@ inline void* at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Shared expert riding along in the routed launches (bf16): its input rows,
+// weights and outputs.
+struct SharedFfn {
+  const void* x;  // [T, d]
+  const moe_weights* w;
+  void* Hs;       // [T, h]
+  void* Sx;       // [T, d]
+  void* Zs;       // pre-activations, nullable
+};
+
 moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, const int* offsets, int G, int rows,
                    const void* W1, const void* W3, const void* b1, const void* W2, const void* b2, void* H,
-                   void* Yp, void* Z, int* err, cudaStream_t st) {
+                   void* Yp, void* Z, int* err, cudaStream_t st, const SharedFfn* sh = nullptr) {
   const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
   GemmParams g1{};
   g1.offsets = offsets;
@@ -115,12 +126,28 @@ moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, cons
   g2.bias = swiglu ? nullptr : b2;
   moe_status s;
   if (cfg->dtype == MOE_BF16) {
+    GemmExtra x1{}, x2{};
+    if (sh) {
+      // the shared expert is one more group of T rows in each launch
+      g1.xrows = g2.xrows = cfg->T;
+      g1.xout = sh->Hs;
+      g1.xzsave = sh->Zs;
+      g1.xbias = swiglu ? nullptr : sh->w->bs1;
+      g2.xout = sh->Sx;
+      g2.xbias = swiglu ? nullptr : sh->w->bs2;
+      x1.A = sh->x;
+      x1.B0 = sh->w->Ws1;
+      x1.B1 = swiglu ? sh->w->Ws3 : nullptr;
+      x2.A = sh->Hs;
+      x2.B0 = sh->w->Ws2;
+    }
     s = launch_grouped_gemm_tc(g1, kKindFwd, Xp, a_rows, W1, swiglu ? W3 : nullptr,
-                               static_cast<long long>(G) * cfg->h, st);
+                               static_cast<long long>(G) * cfg->h, st, sh ? &x1 : nullptr);
     if (s != MOE_OK) return s;
-    s = launch_grouped_gemm_tc(g2, kKindFwd, H, a_rows, W2, nullptr, static_cast<long long>(G) * cfg->d, st);
+    s = launch_grouped_gemm_tc(g2, kKindFwd, H, a_rows, W2, nullptr, static_cast<long long>(G) * cfg->d, st,
+                               sh ? &x2 : nullptr);
   } else {
-    if (Z) return MOE_ERR_UNSUPPORTED;
+    if (Z || sh) return MOE_ERR_UNSUPPORTED;
     s = launch_grouped_gemm_f32(g1, Xp, a_rows, W1, swiglu ? W3 : nullptr, st);
     if (s != MOE_OK) return s;
     s = launch_grouped_gemm_f32(g2, H, a_rows, W2, nullptr, st);
@@ -234,12 +261,15 @@ moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr, const float* expert_bias,
                      const float* noise, int* idx, float* w, int* counts, void* ws, moe_stream_t stream) {
-  (void)ws;
   moe_status s = validate(cfg);
   if (s != MOE_OK) return s;
   if (!x || !Wr || !idx || !w || !counts) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(Wr)) return MOE_ERR_INVALID_ARG;
-  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, reinterpret_cast<cudaStream_t>(stream));
+  if (!aligned16(x) || !aligned16(Wr) || (ws && !aligned16(ws))) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* scratch = ws && route_scratch_bytes(*cfg) ? at(ws, layout(cfg, 1).route_off) : nullptr;
+  int* err = ws ? static_cast<int*>(ws) : nullptr;
+  if (err && cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, scratch, err, st);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x, int* kept, int* offsets, int* pos,
@@ -281,6 +311,27 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offs
   if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
   return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, W1, W3, b1, W2, b2, H, Yp, nullptr, err, st);
+}
+
+moe_status moe_expert_ffn_shared(const moe_config* cfg, const void* Xp, const int* offsets, const moe_weights* wts,
+                                 void* H, void* Yp, const void* x, void* Hs, void* Sx, void* ws, moe_stream_t stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
+  if (!Xp || !offsets || !wts || !H || !Yp || !x || !Hs || !Sx || !ws) return MOE_ERR_INVALID_ARG;
+  if (!wts->W1 || !wts->W2 || (swiglu && !wts->W3) || !wts->Ws1 || !wts->Ws2 || (swiglu && !wts->Ws3))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {Xp, H, Yp, x, Hs, Sx, wts->W1, wts->W2, wts->Ws1, wts->Ws2};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
+  SharedFfn sh{x, wts, Hs, Sx, nullptr};
+  return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, H, Yp, nullptr,
+                 err, st, &sh);
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* Yp, const int* pos, const float* w, const void* Sx,
@@ -328,20 +379,29 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
   int* err = static_cast<int*>(ws);
   if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
 
-  s = launch_route(*cfg, x, wts->Wr, wts->expert_bias, noise, S.idx, S.w, S.counts, st);
+  s = launch_route(*cfg, x, wts->Wr, wts->expert_bias, noise, S.idx, S.w, S.counts,
+                   route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr, err, st);
   if (s != MOE_OK) return s;
   s = launch_dispatch(*cfg, capacity_of(cfg), S.idx, x, S.kept, S.offsets, S.pos, S.Xp, stats,
                       at(ws, L.dispatch_off), st);
   if (s != MOE_OK) return s;
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
-  s = run_ffn(cfg, S.Xp, a_rows, S.offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, S.H, S.Yp,
-              training ? S.Z : nullptr, err, st);
-  if (s != MOE_OK) return s;
-  if (cfg->has_shared) {
-    void* Hs = training && S.Hs ? S.Hs : at(ws, L.Hs);
-    s = run_ffn(cfg, x, cfg->T, nullptr, 1, cfg->T, wts->Ws1, wts->Ws3, wts->bs1, wts->Ws2, wts->bs2, Hs, S.Sx,
-                training ? S.Zs : nullptr, err, st);
+  if (cfg->has_shared && cfg->dtype == MOE_BF16) {
+    // bf16: the shared expert runs inside the routed launches
+    SharedFfn sh{x, wts, training && S.Hs ? S.Hs : at(ws, L.Hs), S.Sx, training ? S.Zs : nullptr};
+    s = run_ffn(cfg, S.Xp, a_rows, S.offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, S.H, S.Yp,
+                training ? S.Z : nullptr, err, st, &sh);
     if (s != MOE_OK) return s;
+  } else {
+    s = run_ffn(cfg, S.Xp, a_rows, S.offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, S.H, S.Yp,
+                training ? S.Z : nullptr, err, st);
+    if (s != MOE_OK) return s;
+    if (cfg->has_shared) {
+      void* Hs = training && S.Hs ? S.Hs : at(ws, L.Hs);
+      s = run_ffn(cfg, x, cfg->T, nullptr, 1, cfg->T, wts->Ws1, wts->Ws3, wts->bs1, wts->Ws2, wts->bs2, Hs, S.Sx,
+                  training ? S.Zs : nullptr, err, st);
+      if (s != MOE_OK) return s;
+    }
   }
   return launch_combine(*cfg, S.Yp, S.pos, S.w, cfg->has_shared ? S.Sx : nullptr, y, st);
 }

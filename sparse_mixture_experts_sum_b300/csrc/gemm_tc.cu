@@ -47,18 +47,31 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_TILE_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_HALF_BYTES = 128 * BK * 2;  // 16 KB
-constexpr int STAGE_BYTES = A_TILE_BYTES + 2 * B_HALF_BYTES;
+constexpr int B_HALF_BYTES = 128 * BK * 2;   // 16 KB
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN block of 64 K rows: 8 KB
-constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_GROUPS = 1024;
 
+// Tile shape per BM (output rows per tile):
+//   BM = 128: 4-stage ring of 48 KB, two 128x256 accumulators (the epilogue
+//             of one tile overlaps the MMAs of the next), 4 epilogue warps;
+//   BM = 256: 3-stage ring of 64 KB, one 256x256 accumulator (two M=128
+//             MMAs per K step share the B tile: 2x the MACs per byte of
+//             shared memory filled), 8 epilogue warps.
+template <int BM_>
+struct TileCfg {
+  static constexpr int BM = BM_;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + 2 * B_HALF_BYTES;
+  static constexpr int STAGES = BM == 128 ? 4 : 3;
+  static constexpr int NACC = BM == 128 ? 2 : 1;
+  static constexpr int EPI_WARPS = BM / 32;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+};
+
+template <int STAGES>
 struct __align__(8) Ctl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -68,11 +81,16 @@ struct __align__(8) Ctl {
   uint32_t tmem_base;
   int abort;
   int total_tiles;
+  int x_tile0;  // first tile of the extra group (= tiles of the routed groups)
   int grp_row[MAX_GROUPS + 1];     // first row of each group (+ end)
   int tile_start[MAX_GROUPS + 1];  // first tile of each group (+ total)
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(Ctl);
+template <int BM_>
+constexpr size_t smem_bytes() {
+  return 1024 + static_cast<size_t>(TileCfg<BM_>::STAGES) * TileCfg<BM_>::STAGE_BYTES +
+         sizeof(Ctl<TileCfg<BM_>::STAGES>);
+}
 
 struct Tile {
   int g, n, m;
@@ -81,8 +99,19 @@ struct Tile {
 // Tile index -> (group, n-tile, m-tile).  Fwd/Dgrad: a group has
 // ceil(rows/BM) m-tiles per n-tile, m fastest.  Wgrad: every group has
 // m_tiles x n_tiles tiles, n fastest when n_fast.
-template <int KIND>
-__device__ __forceinline__ Tile tile_coords(const Ctl& c, int G, int n_tiles, int m_tiles, bool n_fast, int tile) {
+template <int KIND, int BM, typename C>
+__device__ __forceinline__ Tile tile_coords(const C& c, int G, int n_tiles, int m_tiles, bool n_fast, int tile,
+                                            int xrows) {
+  if (KIND == kKindFwd && tile >= c.x_tile0) {
+    // the extra group (g = G): ceil(xrows/BM) m-tiles per n-tile, m fastest
+    const int local = tile - c.x_tile0;
+    const int mt = (xrows + BM - 1) / BM;
+    Tile t;
+    t.g = G;
+    t.n = local / mt;
+    t.m = local - t.n * mt;
+    return t;
+  }
   int lo = 0, hi = G;  // largest g with tile_start[g] <= tile (a group with tiles)
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -138,13 +167,21 @@ __device__ __forceinline__ void load_bf16x32(const bf16* src, int col, int N, fl
   }
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int KIND, int BM_>
+__global__ void __launch_bounds__(TileCfg<BM_>::THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
-                       const __grid_constant__ CUtensorMap mapB1, const GemmParams p) {
+                       const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapXA,
+                       const __grid_constant__ CUtensorMap mapXB0, const __grid_constant__ CUtensorMap mapXB1,
+                       const GemmParams p) {
+  using TC = TileCfg<BM_>;
+  constexpr int BM = TC::BM;
+  constexpr int STAGES = TC::STAGES;
+  constexpr int STAGE_BYTES = TC::STAGE_BYTES;
+  constexpr int A_TILE_BYTES = TC::A_BYTES;
+  constexpr int NACC = TC::NACC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl& c = *reinterpret_cast<Ctl*>(tiles + static_cast<size_t>(STAGES) * STAGE_BYTES);
+  Ctl<STAGES>& c = *reinterpret_cast<Ctl<STAGES>*>(tiles + static_cast<size_t>(STAGES) * STAGE_BYTES);
   volatile int* abort_flag = &c.abort;
 
   const int warp = threadIdx.x >> 5;
@@ -164,7 +201,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&c.tmem_full[a], 1);
-      mbar_init(&c.tmem_empty[a], 128);
+      mbar_init(&c.tmem_empty[a], 32 * TC::EPI_WARPS);
     }
     mbar_init(&c.drain, 1);
     c.abort = 0;
@@ -207,7 +244,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
       }
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) c.total_tiles = carry;
+    if (lane == 0) {
+      c.x_tile0 = carry;
+      c.total_tiles = carry + (KIND == kKindFwd && p.xrows > 0 ? ((p.xrows + BM - 1) / BM) * n_tiles : 0);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -221,33 +261,29 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     if (lane == 0) {
       uint32_t it = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const Tile t = tile_coords<KIND>(c, G, n_tiles, m_tiles_w, n_fast, tile);
-        const int grow = c.grp_row[t.g];
+        const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile, p.xrows);
+        const bool xg = KIND == kKindFwd && t.g == G;  // the extra group
+        const int grow = xg ? 0 : c.grp_row[t.g];
         const int nk = KIND == kKindWgrad ? (c.grp_row[t.g + 1] - grow + BK - 1) / BK : nk_fixed;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const uint32_t s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&c.empty[s], ph ^ 1u)) {
-            record_error(p.err, kErrWaitProducer);
-            *abort_flag = 1;
-            break;
-          }
-          uint8_t* sa = tiles + s * STAGE_BYTES;
-          uint8_t* sb = sa + A_TILE_BYTES;
-          mbar_arrive_expect_tx(&c.full[s], STAGE_BYTES);
+        // every box of k-block kb, handed to emit(dst offset in the stage, map, x, y)
+        auto boxes = [&](int kb, auto&& emit) {
           if (KIND == kKindFwd) {
-            tma_load_2d(sa, &mapA, &c.full[s], kb * BK, grow + t.m * BM);
+            const CUtensorMap* ma = xg ? &mapXA : &mapA;
+            const CUtensorMap* mb0 = xg ? &mapXB0 : &mapB0;
+            const CUtensorMap* mb1 = xg ? &mapXB1 : &mapB1;
+            const int g_row = xg ? 0 : t.g * p.N;
+            emit(0, ma, kb * BK, grow + t.m * BM);
             if (swiglu_fwd) {
-              const int b_row = t.g * p.N + t.n * 128;
-              tma_load_2d(sb, &mapB0, &c.full[s], kb * BK, b_row);
-              tma_load_2d(sb + B_HALF_BYTES, &mapB1, &c.full[s], kb * BK, b_row);
+              const int b_row = g_row + t.n * 128;
+              emit(A_TILE_BYTES, mb0, kb * BK, b_row);
+              emit(A_TILE_BYTES + B_HALF_BYTES, mb1, kb * BK, b_row);
             } else {
-              const int b_row = t.g * p.N + t.n * BN;
-              tma_load_2d(sb, &mapB0, &c.full[s], kb * BK, b_row);
-              tma_load_2d(sb + B_HALF_BYTES, &mapB0, &c.full[s], kb * BK, b_row + 128);
+              const int b_row = g_row + t.n * BN;
+              emit(A_TILE_BYTES, mb0, kb * BK, b_row);
+              emit(A_TILE_BYTES + B_HALF_BYTES, mb0, kb * BK, b_row + 128);
             }
           } else if (KIND == kKindDgrad) {
-            tma_load_2d(sa, &mapA, &c.full[s], kb * BK, grow + t.m * BM);
+            emit(0, &mapA, kb * BK, grow + t.m * BM);
             int k0 = kb * BK;
             const CUtensorMap* mb = &mapB0;
             const int kb_rows = p.k_split ? p.k_split : p.K;
@@ -257,15 +293,26 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             }
             const int y = t.g * kb_rows + k0;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tma_load_2d(sb + i * MN_BLOCK_BYTES, mb, &c.full[s], t.n * BN + 64 * i, y);
+            for (int i = 0; i < 4; ++i) emit(A_TILE_BYTES + i * MN_BLOCK_BYTES, mb, t.n * BN + 64 * i, y);
           } else {
             const int y = grow + kb * BK;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) tma_load_2d(sa + i * MN_BLOCK_BYTES, &mapA, &c.full[s], t.m * BM + 64 * i, y);
+            for (int i = 0; i < BM / 64; ++i) emit(i * MN_BLOCK_BYTES, &mapA, t.m * BM + 64 * i, y);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tma_load_2d(sb + i * MN_BLOCK_BYTES, &mapB0, &c.full[s], t.n * BN + 64 * i, y);
+            for (int i = 0; i < 4; ++i) emit(A_TILE_BYTES + i * MN_BLOCK_BYTES, &mapB0, t.n * BN + 64 * i, y);
           }
+        };
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const uint32_t s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&c.empty[s], ph ^ 1u)) {
+            record_error(p.err, kErrWaitProducer);
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* st_base = tiles + s * STAGE_BYTES;
+          mbar_arrive_expect_tx(&c.full[s], STAGE_BYTES);
+          boxes(kb, [&](int off, const CUtensorMap* m, int x, int y) { tma_load_2d(st_base + off, m, &c.full[s], x, y); });
         }
       }
       if (*abort_flag) {
@@ -278,17 +325,22 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (lane 0 issues; the warp clears Wgrad tails) ----------------
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, KIND == kKindWgrad ? 1 : 0, KIND == kKindFwd ? 0 : 1);
+    // every MMA is M=128 x N=256 (a BM=256 tile issues two per K step); a
+    // problem narrower than one tile (e.g. the router's N = E logits) uses
+    // N = its width rounded up to 16, so no MMA work is spent on columns
+    // that are never stored
+    const int n_mma = (p.N < BN && !swiglu_fwd) ? ((p.N + 15) / 16) * 16 : BN;
+    const uint32_t IDESC = idesc_bf16_f32(128, n_mma, KIND == kKindWgrad ? 1 : 0, KIND == kKindFwd ? 0 : 1);
     uint32_t it = 0, local = 0;
     bool issued = false;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       // one read of the abort flag for the whole warp keeps its lanes together
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = tile_coords<KIND>(c, G, n_tiles, m_tiles_w, n_fast, tile);
-      const int grows = c.grp_row[t.g + 1] - c.grp_row[t.g];
+      const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile, p.xrows);
+      const int grows = KIND == kKindWgrad ? c.grp_row[t.g + 1] - c.grp_row[t.g] : 0;
       const int nk = KIND == kKindWgrad ? (grows + BK - 1) / BK : nk_fixed;
-      const uint32_t acc = local & 1u;
-      const uint32_t aph = (local >> 1) & 1u;
+      const uint32_t acc = local % NACC;
+      const uint32_t aph = (local / NACC) & 1u;
       bool ok = lane == 0 ? mbar_wait(&c.tmem_empty[acc], aph ^ 1u) : true;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -319,13 +371,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             // The phase completed already, so this wait returns at once and
             // makes the copy's data visible to every lane.
             mbar_wait(&c.full[s], ph);
+            constexpr int ABLK = BM / 64;  // MN blocks of the A tile (the B tile has 4)
             const int nrow = BK - valid;
             const int per_block = nrow * 8;  // 16-byte chunks
-            for (int q = lane; q < 6 * per_block; q += 32) {
+            for (int q = lane; q < (ABLK + 4) * per_block; q += 32) {
               const int blk = q / per_block;
               const int rem = q - blk * per_block;
               const int r = valid + (rem >> 3);
-              uint8_t* base = blk < 2 ? sa + blk * MN_BLOCK_BYTES : sb + (blk - 2) * MN_BLOCK_BYTES;
+              uint8_t* base = blk < ABLK ? sa + blk * MN_BLOCK_BYTES : sb + (blk - ABLK) * MN_BLOCK_BYTES;
               *reinterpret_cast<uint4*>(base + r * 128 + (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
@@ -338,11 +391,17 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
           const uint32_t b_base = smem_u32(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad =
-                KIND == kKindWgrad ? sw128_mnmajor_desc(a_base + kk * 2048) : sw128_kmajor_desc(a_base + kk * 32);
+            const uint32_t a_k = KIND == kKindWgrad ? a_base + kk * 2048 : a_base + kk * 32;
             const uint64_t bd =
                 KIND == kKindFwd ? sw128_kmajor_desc(b_base + kk * 32) : sw128_mnmajor_desc(b_base + kk * 2048);
-            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            // rows 128h..128h+127 of A: +16 KB in both layouts (128 rows of
+            // 128 B K-major, or two 64-wide MN blocks)
+#pragma unroll
+            for (int hh = 0; hh < BM / 128; ++hh) {
+              const uint64_t ad = KIND == kKindWgrad ? sw128_mnmajor_desc(a_k + hh * 16384)
+                                                     : sw128_kmajor_desc(a_k + hh * 16384);
+              tc_mma_bf16(d_tmem + hh * BN, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&c.empty[s]);
         }
@@ -359,24 +418,28 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
-    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32)
+    const int quarter = warp & 3;          // TMEM lanes [32*quarter, 32*quarter+32)
+    const int half = (warp - 2) >> 2;      // BM = 256: accumulator rows 128*half.. (columns 256*half..)
     uint32_t local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       // tcgen05.ld is warp-collective: the warp decides to stop as one
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = tile_coords<KIND>(c, G, n_tiles, m_tiles_w, n_fast, tile);
-      const int grow = c.grp_row[t.g];
-      const int gend = c.grp_row[t.g + 1];
-      const uint32_t acc = local & 1u;
-      const uint32_t aph = (local >> 1) & 1u;
+      const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile, p.xrows);
+      const bool xg = KIND == kKindFwd && t.g == G;  // the extra group
+      const int grow = xg ? 0 : c.grp_row[t.g];
+      const int gend = xg ? p.xrows : c.grp_row[t.g + 1];
+      void* const out_p = xg ? p.xout : p.out;
+      void* const zsave_p = xg ? p.xzsave : p.zsave;
+      const uint32_t acc = local % NACC;
+      const uint32_t aph = (local / NACC) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(&c.tmem_full[acc], aph))) {
         if (lane == 0) record_error(p.err, kErrWaitEpilogue);
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const int rt = quarter * 32 + lane;  // accumulator row of this thread
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      const int rt = half * 128 + quarter * 32 + lane;  // tile row of this thread
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + (acc + half) * BN;
 
       if (KIND == kKindWgrad) {
         // out_g[m, n] fp32; a group with no rows has a zero gradient
@@ -402,12 +465,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
           if (valid) store_f32x32(orow, t.n * BN + cc * 32, p.N, v);
         }
       } else {
-        const long long row_end = min(static_cast<long long>(gend), p.rows_alloc);
+        const long long row_end = xg ? static_cast<long long>(gend) : min(static_cast<long long>(gend), p.rows_alloc);
         const int row = grow + t.m * BM + rt;
         const bool valid = row < row_end;
         if (swiglu_fwd) {
-          bf16* orow = static_cast<bf16*>(p.out) + static_cast<size_t>(row) * p.ldo;
-          bf16* zrow = p.zsave ? static_cast<bf16*>(p.zsave) + static_cast<size_t>(row) * p.ldz : nullptr;
+          bf16* orow = static_cast<bf16*>(out_p) + static_cast<size_t>(row) * p.ldo;
+          bf16* zrow = zsave_p ? static_cast<bf16*>(zsave_p) + static_cast<size_t>(row) * p.ldz : nullptr;
           const int col0 = t.n * 128;
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
@@ -420,7 +483,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             for (int i = 0; i < 16; ++i) {
               const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
               const float u0 = __uint_as_float(ur[2 * i]), u1 = __uint_as_float(ur[2 * i + 1]);
-              pk[i] = pack_bf16(silu_f(g0) * u0, silu_f(g1) * u1);
+              pk[i] = pack_bf16(silu_fast(g0) * u0, silu_fast(g1) * u1);
             }
             const int col = col0 + cc * 32;
             if (valid) {
@@ -440,13 +503,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         } else {
           const int col0 = t.n * BN;
           const int mode = p.mode;
-          const bf16* brow =
-              p.bias ? static_cast<const bf16*>(p.bias) + static_cast<size_t>(t.g) * p.N : nullptr;
+          const bf16* brow = xg ? static_cast<const bf16*>(p.xbias)
+                                : (p.bias ? static_cast<const bf16*>(p.bias) + static_cast<size_t>(t.g) * p.N : nullptr);
           const bf16* zin = (mode == kModeSwiGLUBwd || mode == kModeGeLUBwd) && valid
                                 ? static_cast<const bf16*>(p.zin) + static_cast<size_t>(row) * p.ldz
                                 : nullptr;
-          bf16* zrow = p.zsave && mode == kModeGeLU && valid
-                           ? static_cast<bf16*>(p.zsave) + static_cast<size_t>(row) * p.ldz
+          bf16* zrow = zsave_p && mode == kModeGeLU && valid
+                           ? static_cast<bf16*>(zsave_p) + static_cast<size_t>(row) * p.ldz
                            : nullptr;
 #pragma unroll 1
           for (int cc = 0; cc < BN / 32; ++cc) {
@@ -470,7 +533,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                   const int e = 2 * i + h2;
-                  const float sg = sigmoid_f(g[e]);
+                  const float sg = sigmoid_fast(g[e]);
                   const float sl = g[e] * sg;
                   da[h2] = v[e] * u[e] * (sg * (1.0f + g[e] * (1.0f - sg)));
                   db[h2] = v[e] * sl;
@@ -506,12 +569,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
               }
             }
             if (p.out_f32) {
-              store_f32x32(static_cast<float*>(p.out) + static_cast<size_t>(row) * p.ldo, col, p.N, v);
+              store_f32x32(static_cast<float*>(out_p) + static_cast<size_t>(row) * p.ldo, col, p.N, v);
             } else {
               uint32_t pk[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-              store_bf16x32(static_cast<bf16*>(p.out) + static_cast<size_t>(row) * p.ldo, col, p.N, pk);
+              store_bf16x32(static_cast<bf16*>(out_p) + static_cast<size_t>(row) * p.ldo, col, p.N, pk);
             }
           }
         }
@@ -529,24 +592,27 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
   }
 }
 
-template <int KIND>
+template <int KIND, int BM_>
 moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
-                       long long tiles_bound, cudaStream_t stream) {
+                       const CUtensorMap& mXA, const CUtensorMap& mXB0, const CUtensorMap& mXB1, long long tiles_bound,
+                       cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return MOE_ERR_CUDA;
+  constexpr size_t smem = smem_bytes<BM_>();
   static bool attr_set[64] = {false};
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<KIND, BM_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr_set[dev] = true;
   }
   long long grid = tiles_bound;
   if (grid > sms) grid = sms;
   if (grid < 1) grid = 1;
-  grouped_gemm_tc_kernel<KIND><<<static_cast<unsigned>(grid), NUM_THREADS, kSmemBytes, stream>>>(mA, mB0, mB1, p);
+  grouped_gemm_tc_kernel<KIND, BM_>
+      <<<static_cast<unsigned>(grid), TileCfg<BM_>::THREADS, smem, stream>>>(mA, mB0, mB1, mXA, mXB0, mXB1, p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -555,26 +621,74 @@ moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtenso
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+namespace {
+
+// Tile height for a launch: 256 when the groups average at least 256 output
+// rows and the epilogue is plain, else 128.
+template <int KIND>
+moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows, const void* B0, const void* B1,
+                           long long b_rows, long long avg_rows, const GemmExtra* extra, cudaStream_t stream) {
+  // BM = 256 feeds the tensor cores with 2/3 of the shared-memory traffic
+  // per MAC but has a single accumulator, so its epilogue does not overlap
+  // the next tile's MMAs: take it for the light (plain) epilogues only.
+  const bool tall = avg_rows >= 256 && p.mode == kModePlain;
+  const int BMv = tall ? 256 : 128;
+  CUtensorMap mA, mB0, mB1, mXA, mXB0, mXB1;
+  const long long n_tiles = (KIND == kKindFwd && p.mode == kModeSwiGLU) ? (p.N + 127) / 128 : (p.N + BN - 1) / BN;
+  long long tiles = 0;
+  if (KIND == kKindFwd) {
+    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BMv)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB0, B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
+  } else if (KIND == kKindDgrad) {
+    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BMv)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB0, B0, p.N, b_rows, 64, BK)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.N, b_rows, 64, BK)) return MOE_ERR_CUDA;
+  } else {
+    if (!make_tma_2d_bf16(&mA, A, p.M, a_rows, 64, BK)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mB0, B0, p.N, a_rows, 64, BK)) return MOE_ERR_CUDA;
+    mB1 = mB0;
+  }
+  if (KIND == kKindFwd && p.xrows > 0) {
+    const long long n_rows = p.N;  // rows of the extra group's weights [N, K]
+    if (!make_tma_2d_bf16(&mXA, extra->A, p.K, p.xrows, BK, BMv)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mXB0, extra->B0, p.K, n_rows, BK, 128)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mXB1, extra->B1 ? extra->B1 : extra->B0, p.K, n_rows, BK, 128)) return MOE_ERR_CUDA;
+  } else {
+    mXA = mA;
+    mXB0 = mB0;
+    mXB1 = mB1;
+  }
+  if (KIND == kKindWgrad) {
+    tiles = static_cast<long long>(p.G) * ((p.M + BMv - 1) / BMv) * n_tiles;
+  } else {
+    const long long rows_bound = p.offsets ? a_rows : p.rows;
+    tiles = ((rows_bound + BMv - 1) / BMv + (p.offsets ? p.G : 0)) * n_tiles;
+    if (KIND == kKindFwd && p.xrows > 0) tiles += ((p.xrows + BMv - 1) / BMv) * n_tiles;
+  }
+  return tall ? launch_kind<KIND, 256>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream)
+              : launch_kind<KIND, 128>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream);
+}
+
+}  // namespace
+
 moe_status launch_grouped_gemm_tc(const GemmParams& p_in, int kind, const void* A, long long a_rows, const void* B0,
-                                  const void* B1, long long b_rows, cudaStream_t stream) {
+                                  const void* B1, long long b_rows, cudaStream_t stream, const GemmExtra* extra) {
   GemmParams p = p_in;
+  if (p.xrows < 0 || (p.xrows > 0 && (kind != kKindFwd || !extra || !extra->A || !extra->B0 || !p.xout)))
+    return MOE_ERR_INVALID_ARG;
+  if (p.xrows == 0) extra = nullptr;
   p.rows_alloc = a_rows;
   if (p.ldo == 0) p.ldo = p.N;
   if (p.G < 1 || p.G > MAX_GROUPS || p.N < 8 || (p.N % 8) || !p.out) return MOE_ERR_UNSUPPORTED;
   if (a_rows <= 0) return MOE_OK;
   if (a_rows > 2147483647LL || b_rows > 2147483647LL) return MOE_ERR_UNSUPPORTED;
-  CUtensorMap mA, mB0, mB1;
-  const int n_tiles_swiglu = (p.N + 127) / 128;
-  const long long n_tiles = (kind == kKindFwd && p.mode == kModeSwiGLU) ? n_tiles_swiglu : (p.N + BN - 1) / BN;
+  // output rows per group on average (Wgrad: M, the same for every group)
+  const long long avg_rows = kind == kKindWgrad ? p.M : (p.offsets ? a_rows / p.G : p.rows);
   if (kind == kKindFwd) {
     if (p.K < 8 || (p.K % 8)) return MOE_ERR_UNSUPPORTED;
     if (p.mode == kModeSwiGLUBwd || p.mode == kModeGeLUBwd) return MOE_ERR_UNSUPPORTED;
-    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BM)) return MOE_ERR_CUDA;
-    if (!make_tma_2d_bf16(&mB0, B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
-    if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
-    const long long rows_bound = p.offsets ? a_rows : p.rows;
-    const long long m_tiles_bound = (rows_bound + BM - 1) / BM + (p.offsets ? p.G : 0);
-    return launch_kind<kKindFwd>(p, mA, mB0, mB1, m_tiles_bound * n_tiles, stream);
+    return launch_geometry<kKindFwd>(p, A, a_rows, B0, B1, b_rows, avg_rows, extra, stream);
   }
   if (kind == kKindDgrad) {
     // whole 64-deep k-blocks per weight tensor, so a block never mixes groups or tensors
@@ -582,20 +696,12 @@ moe_status launch_grouped_gemm_tc(const GemmParams& p_in, int kind, const void* 
     if (p.k_split && !B1) return MOE_ERR_INVALID_ARG;
     if (p.mode == kModeSwiGLU || p.mode == kModeGeLU) return MOE_ERR_UNSUPPORTED;
     if ((p.mode == kModeSwiGLUBwd || p.mode == kModeGeLUBwd) && !p.zin) return MOE_ERR_INVALID_ARG;
-    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BM)) return MOE_ERR_CUDA;
-    if (!make_tma_2d_bf16(&mB0, B0, p.N, b_rows, 64, BK)) return MOE_ERR_CUDA;
-    if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.N, b_rows, 64, BK)) return MOE_ERR_CUDA;
-    const long long rows_bound = p.offsets ? a_rows : p.rows;
-    const long long m_tiles_bound = (rows_bound + BM - 1) / BM + (p.offsets ? p.G : 0);
-    return launch_kind<kKindDgrad>(p, mA, mB0, mB1, m_tiles_bound * n_tiles, stream);
+    return launch_geometry<kKindDgrad>(p, A, a_rows, B0, B1, b_rows, avg_rows, nullptr, stream);
   }
   if (kind == kKindWgrad) {
     if (p.M < 8 || (p.M % 8) || !p.out_f32 || p.mode != kModePlain) return MOE_ERR_UNSUPPORTED;
     if (p.m_split && (p.m_split % 8 || p.m_split >= p.M || !p.out2)) return MOE_ERR_UNSUPPORTED;
-    if (!make_tma_2d_bf16(&mA, A, p.M, a_rows, 64, BK)) return MOE_ERR_CUDA;
-    if (!make_tma_2d_bf16(&mB0, B0, p.N, a_rows, 64, BK)) return MOE_ERR_CUDA;
-    const long long tiles = static_cast<long long>(p.G) * ((p.M + BM - 1) / BM) * n_tiles;
-    return launch_kind<kKindWgrad>(p, mA, mB0, mB0, tiles, stream);
+    return launch_geometry<kKindWgrad>(p, A, a_rows, B0, B1, b_rows, avg_rows, nullptr, stream);
   }
   return MOE_ERR_INVALID_ARG;
 }

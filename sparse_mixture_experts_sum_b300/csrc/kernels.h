@@ -48,21 +48,40 @@ struct GemmParams {
   long long ldz;         // row stride of zsave / zin (elements)
   const void* bias;      // [G, N] nullable (GeLU / plain)
   int* err;              // workspace error word
+  // Fwd only: one more group with its own operands (the shared expert):
+  // xrows rows of its own A, its own weights, output xout [xrows, ldo],
+  // pre-activations xzsave, bias xbias [N].  xrows = 0: none.
+  int xrows;
+  void* xout;
+  void* xzsave;
+  const void* xbias;
+};
+
+// Operands of the extra group of a Fwd launch.
+struct GemmExtra {
+  const void* A;     // [xrows, K]
+  const void* B0;    // [N, K]
+  const void* B1;    // [N, K] (SwiGLU up), nullable
 };
 
 // sm_103a tensor-core path (bf16 in, fp32 accumulate).  A: the activation
 // operand (a_rows rows); B0/B1: weights (b_rows rows each) for Fwd/Dgrad, or
 // B0 = the second activation operand (a_rows rows) for Wgrad.
 moe_status launch_grouped_gemm_tc(const GemmParams& p, int kind, const void* A, long long a_rows, const void* B0,
-                                  const void* B1, long long b_rows, cudaStream_t stream);
+                                  const void* B1, long long b_rows, cudaStream_t stream,
+                                  const GemmExtra* extra = nullptr);
 
 // fp32 CUDA-core path (fp32 storage and arithmetic).
 moe_status launch_grouped_gemm_f32(const GemmParams& p, const void* A, long long a_rows, const void* B0,
                                    const void* B1, cudaStream_t stream);
 
-// Router: logits, top-k, weights, routed counts.
+// Router: logits, top-k, weights, routed counts.  scratch (nullable, at
+// least route_scratch_bytes) holds the fp32 logits of the tensor-core path;
+// err: the workspace error word of that path's GEMM (nullable).
+size_t route_scratch_bytes(const moe_config& cfg);
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
-                        const float* noise, int* idx, float* w, int* counts, cudaStream_t stream);
+                        const float* noise, int* idx, float* w, int* counts, void* scratch, int* err,
+                        cudaStream_t stream);
 
 // Dispatch: slot-major capacity ranks, offsets, positions, statistics, permute.
 size_t dispatch_scratch_bytes(const moe_config& cfg);

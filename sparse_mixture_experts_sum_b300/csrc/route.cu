@@ -11,11 +11,14 @@
 // (Gumbel noise added to the router score before top-k).  Selecting on the
 // logits equals selecting on softmax(l), which is monotone.
 //
-// bf16: a CTA owns 64 tokens; 4 warps compute the 64 x 128 logit block of
-// an expert chunk with mma.sync m16n8k16 (fp32 accumulate) from
-// double-buffered cp.async tiles of x and Wr, then 64 threads merge the
-// chunk into each token's running top-k.  x is read from HBM once (the
-// kernel is bound by that read); Wr stays in L2.
+// bf16 with E a multiple of 8 (and workspace given): the logits x . Wr^T
+// run on the tcgen05 grouped GEMM (one group of T rows, N = E, fp32 out into
+// the workspace; x streams from HBM through TMA), then route_topk_kernel
+// takes each token's top-k with one warp.  Otherwise a CTA owns 64 tokens;
+// 4 warps compute the 64 x 128 logit block of an expert chunk with
+// mma.sync m16n8k16 (fp32 accumulate) from a 3- to 5-stage cp.async ring of
+// x and Wr tiles, then 64 threads merge the chunk into each token's running
+// top-k.
 // fp32: one warp per token on the CUDA cores (tiny workloads).
 #include "common.cuh"
 #include "kernels.h"
@@ -98,25 +101,47 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-struct RouteSmem {
-  bf16 xs[2][RT_TM][RT_LD];
-  bf16 ws[2][RT_NE][RT_LD];
-  float L[RT_TM][RT_NE + 1];
+// Shared-memory layout of route_bf16_kernel (dynamic): a ring of STAGES
+// stages, each an x tile [64][RT_LD] and a Wr tile [nep][RT_LD] (nep = the
+// expert chunk width, <= 128, a multiple of 8); after the K loop the ring
+// is reused for the chunk's logits L[64][nep+1]; then E ints of histogram.
+struct RouteLayout {
+  int nep;
+  size_t stage_bytes, ring_bytes, total;
+  __host__ __device__ RouteLayout(int E, int stages) {
+    nep = ((E < RT_NE ? E : RT_NE) + 7) / 8 * 8;
+    stage_bytes = static_cast<size_t>(RT_TM + nep) * RT_LD * 2;
+    const size_t lbytes = static_cast<size_t>(RT_TM) * (nep + 1) * 4;
+    ring_bytes = stages * stage_bytes > lbytes ? stages * stage_bytes : lbytes;
+    total = ring_bytes + static_cast<size_t>(E) * 4;
+  }
 };
 
+// Logits of 64 tokens against all experts (chunks of 128), over the K
+// blocks of this CTA's split (blockIdx.y of gridDim.y); cp.async ring of
+// STAGES stages.  partial == nullptr: add bias and noise, take the top-k and
+// count.  Otherwise write the raw partial logits partial[split][t][e].
+template <int STAGES>
 __global__ void __launch_bounds__(128)
 route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const float* __restrict__ ebias,
                   const float* __restrict__ noise, int T, int d, int E, int k, int* __restrict__ idx,
-                  float* __restrict__ w, int* __restrict__ counts) {
-  extern __shared__ uint8_t smem_raw[];
-  RouteSmem& S = *reinterpret_cast<RouteSmem*>(smem_raw);
-  int* hist = reinterpret_cast<int*>(smem_raw + sizeof(RouteSmem));
+                  float* __restrict__ w, int* __restrict__ counts, int kb_per_split, float* __restrict__ partial) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const RouteLayout Lay(E, STAGES);
+  const int nep = Lay.nep;
+  int* hist = reinterpret_cast<int*>(smem_raw + Lay.ring_bytes);
+  float* L = reinterpret_cast<float*>(smem_raw);  // [64][nep+1], aliases the ring after the K loop
+  auto xs = [&](int st) { return reinterpret_cast<bf16*>(smem_raw + st * Lay.stage_bytes); };
+  auto wsm = [&](int st) { return reinterpret_cast<bf16*>(smem_raw + st * Lay.stage_bytes) + RT_TM * RT_LD; };
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c4 = lane & 3;
   const int t0 = blockIdx.x * RT_TM;
-  const int nk = (d + RT_BK - 1) / RT_BK;
+  const int nk_all = (d + RT_BK - 1) / RT_BK;
+  const int kb0 = blockIdx.y * kb_per_split;
+  const int kb1 = min(nk_all, kb0 + kb_per_split);
+  const int nk = kb1 - kb0;
 
   for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
 
@@ -137,56 +162,62 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
     for (int f = 0; f < RT_NE / 8; ++f) acc[f][0] = acc[f][1] = acc[f][2] = acc[f][3] = 0.f;
 
     auto load_stage = [&](int stage, int kb) {
-      const int k0 = kb * RT_BK;
+      const int k0 = (kb0 + kb) * RT_BK;
+      bf16* xd = xs(stage);
+      bf16* wd = wsm(stage);
       // x tile: 64 rows x 8 chunks of 16 B; out-of-range chunks are zero-filled
       for (int q = tid; q < RT_TM * 8; q += 128) {
         const int r = q >> 3, ch = q & 7;
         const int t = t0 + r, kk = k0 + ch * 8;
         const bool ok = t < T && kk < d;
         const bf16* src = ok ? x + static_cast<size_t>(t) * d + kk : x;
-        cp_async16(&S.xs[stage][r][ch * 8], src, ok);
+        cp_async16(xd + r * RT_LD + ch * 8, src, ok);
       }
-      for (int q = tid; q < RT_NE * 8; q += 128) {
+      for (int q = tid; q < nep * 8; q += 128) {
         const int r = q >> 3, ch = q & 7;
         const int e = e0 + r, kk = k0 + ch * 8;
         const bool ok = r < ne && kk < d;
         const bf16* src = ok ? Wr + static_cast<size_t>(e) * d + kk : Wr;
-        cp_async16(&S.ws[stage][r][ch * 8], src, ok);
+        cp_async16(wd + r * RT_LD + ch * 8, src, ok);
       }
-      cp_async_commit();
     };
 
-    load_stage(0, 0);
+    // multistage ring: STAGES-1 blocks in flight ahead of the one computed
+#pragma unroll
+    for (int s0 = 0; s0 < STAGES - 1; ++s0) {
+      if (s0 < nk) load_stage(s0, s0);
+      cp_async_commit();
+    }
     for (int kb = 0; kb < nk; ++kb) {
-      if (kb + 1 < nk) {
-        load_stage((kb + 1) & 1, kb + 1);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
+      cp_async_wait<STAGES - 2>();
       __syncthreads();
-      const int st = kb & 1;
+      const int nxt = kb + STAGES - 1;
+      if (nxt < nk) load_stage(nxt % STAGES, nxt);
+      cp_async_commit();
+      const bf16* xa = xs(kb % STAGES);
+      const bf16* wb = wsm(kb % STAGES);
       const int r0 = warp * 16;
 #pragma unroll
       for (int kk = 0; kk < RT_BK / 16; ++kk) {
         uint32_t a[4];
-        a[0] = *reinterpret_cast<const uint32_t*>(&S.xs[st][r0 + g][kk * 16 + 2 * c4]);
-        a[1] = *reinterpret_cast<const uint32_t*>(&S.xs[st][r0 + g + 8][kk * 16 + 2 * c4]);
-        a[2] = *reinterpret_cast<const uint32_t*>(&S.xs[st][r0 + g][kk * 16 + 2 * c4 + 8]);
-        a[3] = *reinterpret_cast<const uint32_t*>(&S.xs[st][r0 + g + 8][kk * 16 + 2 * c4 + 8]);
+        a[0] = *reinterpret_cast<const uint32_t*>(xa + (r0 + g) * RT_LD + kk * 16 + 2 * c4);
+        a[1] = *reinterpret_cast<const uint32_t*>(xa + (r0 + g + 8) * RT_LD + kk * 16 + 2 * c4);
+        a[2] = *reinterpret_cast<const uint32_t*>(xa + (r0 + g) * RT_LD + kk * 16 + 2 * c4 + 8);
+        a[3] = *reinterpret_cast<const uint32_t*>(xa + (r0 + g + 8) * RT_LD + kk * 16 + 2 * c4 + 8);
 #pragma unroll
         for (int f = 0; f < RT_NE / 8; ++f) {
           if (f < nfrag) {
-            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&S.ws[st][f * 8 + g][kk * 16 + 2 * c4]);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&S.ws[st][f * 8 + g][kk * 16 + 2 * c4 + 8]);
+            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wb + (f * 8 + g) * RT_LD + kk * 16 + 2 * c4);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wb + (f * 8 + g) * RT_LD + kk * 16 + 2 * c4 + 8);
             mma_bf16_16816(acc[f], a, b0, b1);
           }
         }
       }
-      __syncthreads();
     }
+    cp_async_wait<0>();
+    __syncthreads();  // the ring becomes L
 
-    // logits of this chunk (+ bias, + noise) -> smem
+    // logits of this chunk (+ bias, + noise unless partial) -> L
     {
       const int r0 = warp * 16;
 #pragma unroll
@@ -199,30 +230,114 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
             const int e = e0 + col;
             const int t = t0 + r;
             float v = acc[f][q];
-            if (e < E && t < T) {
+            if (!partial && e < E && t < T) {
               if (ebias) v += ebias[e];
               if (noise) v += noise[static_cast<size_t>(t) * E + e];
             }
-            S.L[r][col] = v;
+            L[r * (nep + 1) + col] = v;
           }
         }
       }
     }
     __syncthreads();
-    if (tid < RT_TM && t0 + tid < T) {
+    if (partial) {
+      float* pp = partial + static_cast<size_t>(blockIdx.y) * T * E;
+      for (int q = tid; q < RT_TM * ne; q += blockDim.x) {
+        const int r = q / ne, col = q - r * ne;
+        if (t0 + r < T) pp[static_cast<size_t>(t0 + r) * E + e0 + col] = L[r * (nep + 1) + col];
+      }
+    } else if (tid < RT_TM && t0 + tid < T) {
       for (int col = 0; col < ne; ++col) {
-        const float v = S.L[tid][col];
+        const float v = L[tid * (nep + 1) + col];
         if (!isfinite(v)) finite = false;
         topk_insert(tv, tix, k, v, e0 + col);
       }
     }
-    __syncthreads();
+    __syncthreads();  // L is the ring again for the next expert chunk
   }
 
+  if (partial) return;
   if (tid < RT_TM && t0 + tid < T) topk_finish(tv, tix, k, finite, t0 + tid, idx, w, hist);
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x)
     if (hist[e]) atomicAdd(&counts[e], hist[e]);
+}
+
+// Top-k of precomputed logits, one warp per token: l[t,e] = logits[t,e]
+// (+ bias[e]) (+ noise[t,e]); each lane keeps the top-k of its experts
+// (e = lane, lane+32, ... in increasing order), then k rounds of a warp
+// argmax by (value desc, index asc) merge the lanes' lists.  Lane 0 writes
+// idx, the renormalised weights and the block histogram.
+__global__ void __launch_bounds__(256)
+route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ ebias, const float* __restrict__ noise,
+                  int T, int E, int k, int* __restrict__ idx, float* __restrict__ w, int* __restrict__ counts) {
+  extern __shared__ int hist_s[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (t < T) {
+    float tv[MAXK];
+    int tix[MAXK];
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+      tv[j] = -INFINITY;
+      tix[j] = -1;
+    }
+    bool finite = true;
+    const float* lr = logits + static_cast<size_t>(t) * E;
+    const float* nr = noise ? noise + static_cast<size_t>(t) * E : nullptr;
+    for (int e = lane; e < E; e += 32) {
+      float v = lr[e];
+      if (ebias) v += ebias[e];
+      if (nr) v += nr[e];
+      if (!isfinite(v)) finite = false;
+      topk_insert(tv, tix, k, v, e);
+    }
+    finite = __all_sync(0xffffffffu, finite);
+    float sel_v[MAXK];
+    int sel_i[MAXK];
+    int head = 0;  // next unconsumed entry of this lane's list
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+      if (j < k) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int q = 0; q < MAXK; ++q)
+          if (q == head && tix[q] >= 0) {
+            bv = tv[q];
+            bi = tix[q];
+          }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        sel_v[j] = bv;
+        sel_i[j] = bi;
+        // the lane that held the winner advances its list
+        if (head < MAXK && tix[head] == bi) ++head;
+      }
+    }
+    if (lane == 0) {
+      if (!finite) {
+        for (int j = 0; j < k; ++j) {
+          idx[static_cast<size_t>(t) * k + j] = -1;
+          w[static_cast<size_t>(t) * k + j] = 0.f;
+        }
+      } else {
+        topk_finish(sel_v, sel_i, k, true, t, idx, w, hist_s);
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (hist_s[e]) atomicAdd(&counts[e], hist_s[e]);
 }
 
 // fp32 storage: one warp per token, fp32 dot products on the CUDA cores.
@@ -259,24 +374,65 @@ __global__ void route_f32_kernel(const float* __restrict__ x, const float* __res
 
 }  // namespace
 
+namespace {
+
+template <int STAGES>
+moe_status launch_route_stages(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
+                               const float* noise, int* idx, float* w, int* counts, cudaStream_t stream) {
+  const RouteLayout Lay(cfg.E, STAGES);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!attr_set[dev]) {
+    const RouteLayout Lmax(1024, STAGES);
+    if (cudaFuncSetAttribute(route_bf16_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Lmax.total)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  const int nk = (cfg.d + RT_BK - 1) / RT_BK;
+  dim3 grid((cfg.T + RT_TM - 1) / RT_TM, 1);
+  route_bf16_kernel<STAGES><<<grid, 128, Lay.total, stream>>>(
+      static_cast<const bf16*>(x), static_cast<const bf16*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E, cfg.k,
+      idx, w, counts, nk, nullptr);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// bf16 logits on the tensor cores need E a multiple of 8 (a TMA and
+// epilogue granule) and scratch for the fp32 logits.
+bool route_on_tensor_cores(const moe_config& cfg) { return cfg.dtype == MOE_BF16 && cfg.E % 8 == 0; }
+
+}  // namespace
+
+size_t route_scratch_bytes(const moe_config& cfg) {
+  return route_on_tensor_cores(cfg) ? static_cast<size_t>(cfg.T) * cfg.E * sizeof(float) : 0;
+}
+
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
-                        const float* noise, int* idx, float* w, int* counts, cudaStream_t stream) {
+                        const float* noise, int* idx, float* w, int* counts, void* scratch, int* err,
+                        cudaStream_t stream) {
   if (cudaMemsetAsync(counts, 0, sizeof(int) * cfg.E, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cfg.dtype == MOE_BF16) {
-    const size_t smem = sizeof(RouteSmem) + sizeof(int) * cfg.E;
-    static thread_local int attr_dev = -1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (attr_dev != dev) {
-      if (cudaFuncSetAttribute(route_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(sizeof(RouteSmem) + sizeof(int) * 1024)) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      attr_dev = dev;
-    }
-    const int grid = (cfg.T + RT_TM - 1) / RT_TM;
-    route_bf16_kernel<<<grid, 128, smem, stream>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(Wr),
-                                                   expert_bias, noise, cfg.T, cfg.d, cfg.E, cfg.k, idx, w,
-                                                   counts);
+  if (route_on_tensor_cores(cfg) && scratch) {
+    // logits = x . Wr^T on the tcgen05 grouped GEMM (one group of T rows,
+    // N = E, fp32 out), then the top-k per token
+    GemmParams g{};
+    g.G = 1;
+    g.rows = cfg.T;
+    g.N = cfg.E;
+    g.K = cfg.d;
+    g.mode = kModePlain;
+    g.out_f32 = 1;
+    g.out = scratch;
+    g.err = err;
+    moe_status s = launch_grouped_gemm_tc(g, kKindFwd, x, cfg.T, Wr, nullptr, cfg.E, stream);
+    if (s != MOE_OK) return s;
+    const unsigned grid = static_cast<unsigned>((static_cast<long long>(cfg.T) * 32 + 255) / 256);
+    route_topk_kernel<<<grid, 256, sizeof(int) * cfg.E, stream>>>(static_cast<const float*>(scratch), expert_bias,
+                                                                   noise, cfg.T, cfg.E, cfg.k, idx, w, counts);
+  } else if (cfg.dtype == MOE_BF16) {
+    const int nep = ((cfg.E < RT_NE ? cfg.E : RT_NE) + 7) / 8 * 8;
+    return nep <= 64 ? launch_route_stages<5>(cfg, x, Wr, expert_bias, noise, idx, w, counts, stream)
+                     : launch_route_stages<3>(cfg, x, Wr, expert_bias, noise, idx, w, counts, stream);
   } else {
     const int threads = 256;
     const long long grid = (static_cast<long long>(cfg.T) * 32 + threads - 1) / threads;

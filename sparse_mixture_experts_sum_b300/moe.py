@@ -56,7 +56,7 @@ class MoeStats(ctypes.Structure):
 
 
 EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_static",
-           "moe_expert_ffn",
+           "moe_expert_ffn", "moe_expert_ffn_shared",
            "moe_combine", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error", "moe_status_string")
 
 _lib = None
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_dispatch_static": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_expert_ffn": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_expert_ffn_shared": [cfgp, vp, vp, ctypes.POINTER(MoeWeights), vp, vp, vp, vp, vp, vp, vp],
             "moe_combine": [cfgp, vp, vp, vp, vp, vp, vp],
             "moe_layer_fwd": [cfgp, ctypes.POINTER(MoeWeights), vp, vp, vp, ctypes.POINTER(MoeSaved), vp, vp,
                               sz, vp],
@@ -174,6 +175,13 @@ def moe_expert_ffn(cfg, Xp, offsets, W1, W3, b1, W2, b2, H, Yp, ws, stream=None)
     _check("moe_expert_ffn", lib().moe_expert_ffn(ctypes.byref(cfg), _p(Xp), _p(offsets), _p(W1), _p(W3),
                                                   _p(b1), _p(W2), _p(b2), _p(H), _p(Yp), _p(ws),
                                                   _stream(stream)))
+
+
+def moe_expert_ffn_shared(cfg, Xp, offsets, weights: dict, H, Yp, x, Hs, Sx, ws, stream=None):
+    W = weights_struct(weights)
+    _check("moe_expert_ffn_shared", lib().moe_expert_ffn_shared(ctypes.byref(cfg), _p(Xp), _p(offsets), ctypes.byref(W),
+                                                                _p(H), _p(Yp), _p(x), _p(Hs), _p(Sx), _p(ws),
+                                                                _stream(stream)))
 
 
 def moe_combine(cfg, Yp, pos, w, Sx, y, stream=None):

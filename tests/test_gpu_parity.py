@@ -305,3 +305,107 @@ def test_inference_workspace_path_matches_training_path():
     M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], None, y2, None, None, ws)
     assert M.moe_check_error(ws) == 0
     assert torch.equal(y, y2)
+
+
+# ---------------------------------------------------------------------------
+# fine-grained routing: 384 routed experts, top-6, one shared expert
+# ---------------------------------------------------------------------------
+
+
+def test_fine_grained_small_layer():
+    """E=384 top-6 + shared at a size the oracle runs whole: three 128-expert
+    router chunks, k=6, capacity binding (cf 1.0), 1-16 rows per expert."""
+    wl = S.WORKLOADS["fine_grained"].replace(T=512, d=128, h=128, capacity_factor=1.0, seed=25)
+    t = guarded_inputs(wl, DEV)
+    y, sv, st = run_layer(wl, t)
+    r = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"])
+    check_routing(r, sv, st, t["x"])
+    assert st["dropped_slots"] > 0
+    assert_close_bf16(to_np(y), r["y"], "y")
+
+
+@pytest.mark.slow
+def test_fine_grained_layer_sampled():
+    """The fine-grained workload at full size (T=8192, d=4096, h=1024):
+    routing and dispatch bit-exact, y on 24 sampled tokens."""
+    wl = S.WORKLOADS["fine_grained"]
+    t = guarded_inputs(wl, DEV)
+    y, sv, st = run_layer(wl, t)
+    r = O.route_and_dispatch(oracle_cfg(wl), t["x"], t["Wr"])
+    check_routing(r, sv, st, t["x"])
+    assert st["capacity"] == 160
+    toks = np.sort(np.random.default_rng(5).choice(wl.T, size=24, replace=False))
+    ro = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"], tokens=toks)
+    assert_close_bf16(to_np(y[torch.as_tensor(toks, device=DEV)]), ro["y"], "y (sampled)")
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu"])
+def test_expert_ffn_shared_matches_oracle(act):
+    """Routed experts and the shared expert in the same launches: the routed
+    rows (ragged groups, an empty one) and the shared expert's rows of all
+    T tokens both match the oracle's expert FFN."""
+    T, k, E, d, h = 300, 2, 5, 192, 320
+    rows = [0, 1, 130, 257, 37]
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    cfg = M.make_config(T, d, h, E, k, act, "bf16", has_shared=True)
+    g = torch.Generator().manual_seed(9)
+    bf = torch.bfloat16
+    W = dict(W1=(torch.randn(E, h, d, generator=g) / d ** 0.5), W2=(torch.randn(E, d, h, generator=g) / h ** 0.5),
+             Ws1=(torch.randn(h, d, generator=g) / d ** 0.5), Ws2=(torch.randn(d, h, generator=g) / h ** 0.5))
+    if act == "swiglu":
+        W["W3"] = torch.randn(E, h, d, generator=g) / d ** 0.5
+        W["Ws3"] = torch.randn(h, d, generator=g) / d ** 0.5
+    else:
+        W.update(b1=torch.randn(E, h, generator=g) * 0.2, b2=torch.randn(E, d, generator=g) * 0.2,
+                 bs1=torch.randn(h, generator=g) * 0.2, bs2=torch.randn(d, generator=g) * 0.2)
+    W = {n: v.to(bf).to(DEV) for n, v in W.items()}
+    x = torch.randn(T, d, generator=g).to(bf).to(DEV)
+    Xp = torch.randn(T * k, d, generator=g).to(bf).to(DEV)
+    H = torch.empty(T * k, h, dtype=bf, device=DEV)
+    Yp = torch.empty(T * k, d, dtype=bf, device=DEV)
+    Hs = torch.empty(T, h, dtype=bf, device=DEV)
+    Sx = torch.empty(T, d, dtype=bf, device=DEV)
+    ws = M.moe.workspace(cfg, 1)
+    M.moe.moe_expert_ffn_shared(cfg, Xp, torch.as_tensor(off, device=DEV), W, H, Yp, x, Hs, Sx, ws)
+    assert M.moe_check_error(ws) == 0
+    Wn = {n: to_np(v) for n, v in W.items()}
+    Xn = to_np(Xp)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            p = O.expert_params(Wn, e, act)
+            assert_close_bf16(to_np(Yp)[a:b], O.expert_ffn(Xn[a:b], act, **p), f"Yp expert {e}")
+    ps = O.shared_params(Wn, act)
+    assert_close_bf16(to_np(Sx), O.expert_ffn(to_np(x), act, **ps), "Sx (shared expert)")
+
+
+@pytest.mark.parametrize("T,d,E,k", [(64, 4096, 128, 2), (200, 1024, 130, 4), (1000, 512, 384, 6),
+                                     (4500, 1024, 64, 2)])
+def test_route_with_workspace(T, d, E, k):
+    """With a workspace and E a multiple of 8 the logits run on the tcgen05
+    GEMM and a warp per token takes the top-k (E = 130 keeps the mma.sync
+    kernel): same routing as the oracle, and the same bits on a second run."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=T, d=d, E=E, k=k, seed=19)
+    t = guarded_inputs(wl, "cpu", parts=["x", "Wr"])
+    cfg = M.config_of(wl)
+    x, Wr = t["x"].to(DEV), t["Wr"].to(DEV)
+    eb = torch.linspace(0.3, 0.0, E, dtype=torch.float32)
+    ws = M.moe.workspace(cfg, 1)
+    outs = []
+    for _ in range(2):
+        idx = torch.empty(T, k, dtype=torch.int32, device=DEV)
+        w = torch.empty(T, k, device=DEV)
+        counts = torch.empty(E, dtype=torch.int32, device=DEV)
+        M.moe_route(cfg, x, Wr, eb.to(DEV), None, idx, w, counts, ws)
+        outs.append((idx, w, counts))
+    l = O.router_logits(t["x"], t["Wr"], eb)
+    ridx, rw, _ = O.top_k_route(l, k)
+    from moe_testlib import small_gaps
+    safe = np.setdiff1d(np.arange(T), small_gaps(l, k))
+    idx, w, counts = outs[0]
+    np.testing.assert_array_equal(idx.cpu().numpy()[safe], ridx[safe])
+    np.testing.assert_allclose(w.cpu().numpy()[safe], rw[safe], atol=W_TOL, rtol=0)
+    if len(safe) == T:
+        np.testing.assert_array_equal(counts.cpu().numpy(), O.usage_counts(ridx, E))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
