@@ -72,6 +72,15 @@ typedef enum {
 enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 };
 enum { MOE_F32 = 0, MOE_BF16 = 1 };
 
+/* Routing variants (moe_config.route_flags, a bit set; 0 = the defaults).
+ *  MOE_ROUTE_RAW_PROBS: the weights are the selected entries of the softmax
+ *    over all E experts, not renormalised over the k ([P2] 3.2: output =
+ *    p1*e1 + p2*e2; [P4] 5.1 uses the top-k probabilities as they are).
+ *    Forward only: moe_layer_bwd returns MOE_ERR_UNSUPPORTED.
+ *  MOE_ROUTE_TOKEN_MAJOR: capacity is granted token by token (all of token
+ *    t's choices, in order, before token t+1's) instead of slot-major. */
+enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2 };
+
 /* Layer shape and routing rule.  [P2] 4.2 (capacity_factor, min_capacity),
  * [P1] 4.3 (load_balancing_loss_coef 0.01). */
 typedef struct {
@@ -86,6 +95,7 @@ typedef struct {
   int min_capacity;      /* floor on C (0 = none)                              */
   float lambda_balance;  /* lambda of the usage statistic (0.01)               */
   int has_shared;        /* 1: add the always-on shared expert                 */
+  int route_flags;       /* MOE_ROUTE_* bits, 0 = renormalised, slot-major     */
 } moe_config;
 
 typedef struct {
@@ -149,6 +159,10 @@ typedef struct {
   int numeric_error;       /* tokens with a non-finite logit                */
   double drop_rate;        /* dropped_slots / (T*k)                         */
   double balance_stat;     /* lambda * std_{n-1}(counts/T) / (mean + 1e-8)  */
+  double router_entropy;   /* mean over tokens with finite logits of
+                              -sum_e p_e ln p_e, p = softmax over all E
+                              ([P3] monitoring: alert below 0.3); written by
+                              moe_layer_fwd; moe_dispatch alone leaves NaN  */
 } moe_stats;
 
 /* C = max(min_capacity, ceil(cf*T*k/E)) or T when cf <= 0 ([P3] 2.3:
@@ -168,15 +182,20 @@ moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes
  *   idx[t,:] = the k largest l[t,:], larger first, ties -> lower index
  *   w[t,j]   = exp(l[idx_j] - l[idx_0]) / sum_j' exp(l[idx_j'] - l[idx_0])
  *   counts[e] = #slots routed to e (zeroed by this call)
+ * (cfg->route_flags MOE_ROUTE_RAW_PROBS: w[t,j] = softmax over all E of
+ * l[t,:] at idx_j.)
  * x [T,d], Wr [E,d] in cfg->dtype; expert_bias [E], noise [T,E] fp32,
- * both nullable.  Outputs idx [T,k] int32, w [T,k] fp32, counts [E] int32.
+ * both nullable.  Outputs idx [T,k] int32, w [T,k] fp32, counts [E] int32,
+ * entropy [T] fp32 (nullable): -sum_e p_e ln p_e of each token's softmax
+ * over all experts, NaN for a token with a non-finite logit.
  * ws: NULL, or >= moe_workspace_size(cfg, 1) bytes; with it a batch too
  * small to fill the GPU splits the contraction over more CTAs (the
  * partial logits are summed in a fixed order, so results repeat bit for
  * bit either way). */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr,
                      const float* expert_bias, const float* noise, int* idx,
-                     float* w, int* counts, void* ws, moe_stream_t stream);
+                     float* w, int* counts, float* entropy, void* ws,
+                     moe_stream_t stream);
 
 /* Capacity and dispatch ([P3] 2.3 capacity and dropped tokens; [P1] 4.2
  * step 2, grouping the tokens bound for the same expert).

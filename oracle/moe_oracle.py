@@ -90,14 +90,17 @@ def router_logits(x, Wr, expert_bias=None, noise=None) -> np.ndarray:
     return l
 
 
-def top_k_route(l: np.ndarray, k: int):
-    """Top-k experts per token and their renormalised weights.
+def top_k_route(l: np.ndarray, k: int, raw_probs: bool = False):
+    """Top-k experts per token and their weights.
 
     Experts are ordered by (logit descending, index ascending); the first k
     are selected ([P1] 4.2 takes top-k of softmax(l); softmax is monotone, so
-    ordering the logits gives the same set).  Weights are the softmax of the
-    selected logits, w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0), which is
-    [P1] 3.3's p_i/(p_i+p_j) and [P3] 3.3's softmax over the top-k logits.
+    ordering the logits gives the same set).  Weights (default) are the
+    softmax of the selected logits, w_j = exp(l_j - l_0) / sum_j'
+    exp(l_j' - l_0), which is [P1] 3.3's p_i/(p_i+p_j) and [P3] 3.3's softmax
+    over the top-k logits.  raw_probs: the selected entries of the softmax
+    over all E experts, not renormalised ([P2] 3.2: output = p1*e1 + p2*e2;
+    [P4] 5.1 uses the top-k probabilities as they are).
 
     Returns idx [T,k] int64 (-1 for a token with a non-finite logit), w [T,k]
     fp64 (0 there), finite [T] bool."""
@@ -112,9 +115,27 @@ def top_k_route(l: np.ndarray, k: int):
         order = np.lexsort((experts, -l[t]))  # primary: -l, secondary: index
         sel = order[:k]
         idx[t] = sel
-        z = np.exp(l[t, sel] - l[t, sel[0]])
-        w[t] = z / z.sum()
+        if raw_probs:
+            z = np.exp(l[t] - l[t, sel[0]])
+            w[t] = z[sel] / z.sum()
+        else:
+            z = np.exp(l[t, sel] - l[t, sel[0]])
+            w[t] = z / z.sum()
     return idx, w, finite
+
+
+def router_entropy(l: np.ndarray) -> float:
+    """Mean over the tokens with finite logits of the entropy of the router's
+    distribution, H_t = -sum_e p_te ln p_te with p_t = softmax(l_t) over all
+    experts ([P3] 4.x monitoring: router_entropy, alert below 0.3).  NaN when
+    no token has finite logits."""
+    finite = np.all(np.isfinite(l), axis=1)
+    if not finite.any():
+        return float("nan")
+    p = softmax(l[finite])
+    with np.errstate(divide="ignore", invalid="ignore"):
+        h = -np.where(p > 0, p * np.log(p), 0.0).sum(axis=1)
+    return float(h.mean())
 
 
 def softmax(l: np.ndarray) -> np.ndarray:
@@ -147,24 +168,26 @@ def usage_counts(idx: np.ndarray, E: int) -> np.ndarray:
     return counts
 
 
-def assign_capacity(idx: np.ndarray, E: int, C: int):
-    """Queue simulation in slot-major priority.
+def assign_capacity(idx: np.ndarray, E: int, C: int, token_major: bool = False):
+    """Queue simulation of the capacity rule.
 
-    for j in 0..k-1, for t in 0..T-1: the slot (t, j) gets the next free
-    place of its expert if fewer than C are taken, else it is dropped
+    Slot-major priority (default): for j in 0..k-1, for t in 0..T-1; token-
+    major: for t in 0..T-1, for j in 0..k-1.  The slot (t, j) gets the next
+    free place of its expert if fewer than C are taken, else it is dropped
     ([P3] 2.3 / [P1] 4.3: tokens beyond capacity are dropped).
     Returns rank [T,k] (-1 dropped or unrouted) and fill[E] (kept per expert)."""
     T, k = idx.shape
     rank = np.full((T, k), -1, dtype=np.int64)
     fill = np.zeros(E, dtype=np.int64)
-    for j in range(k):
-        for t in range(T):
-            e = idx[t, j]
-            if e < 0:
-                continue
-            if fill[e] < C:
-                rank[t, j] = fill[e]
-                fill[e] += 1
+    order = [(t, j) for t in range(T) for j in range(k)] if token_major else \
+        [(t, j) for j in range(k) for t in range(T)]
+    for t, j in order:
+        e = idx[t, j]
+        if e < 0:
+            continue
+        if fill[e] < C:
+            rank[t, j] = fill[e]
+            fill[e] += 1
     return rank, fill
 
 
@@ -264,10 +287,10 @@ def route_and_dispatch(cfg: dict, x, Wr, expert_bias=None, noise=None) -> Dict[s
     """Router, top-k, capacity and dispatch of the whole batch (no experts)."""
     T, E, k = cfg["T"], cfg["E"], cfg["k"]
     l = router_logits(x, Wr, expert_bias, noise)
-    idx, w, finite = top_k_route(l, k)
+    idx, w, finite = top_k_route(l, k, raw_probs=cfg.get("raw_probs", False))
     counts = usage_counts(idx, E)
     C = expert_capacity(T, k, E, cfg.get("capacity_factor", 0.0), cfg.get("min_capacity", 0))
-    rank, fill = assign_capacity(idx, E, C)
+    rank, fill = assign_capacity(idx, E, C, token_major=cfg.get("token_major", False))
     offsets, pos = dispatch_positions(idx, rank, fill)
     routed = int(counts.sum())
     kept_total = int(fill.sum())
@@ -279,6 +302,7 @@ def route_and_dispatch(cfg: dict, x, Wr, expert_bias=None, noise=None) -> Dict[s
         drop_rate=(T * k - kept_total) / (T * k),
         balance_stat=balance_stat(counts, T, cfg.get("lam", 0.01)),
         numeric_error=int((~finite).sum()),
+        router_entropy=router_entropy(l),
     )
     return dict(logits=l, idx=idx, w=w, counts=counts, kept=fill, capacity=C,
                 rank=rank, offsets=offsets, pos=pos, stats=stats)
@@ -410,6 +434,8 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
     T, d, E, k = cfg["T"], cfg["d"], cfg["E"], cfg["k"]
     act = cfg["act"]
     lam = cfg.get("lam", 0.01)
+    if cfg.get("raw_probs"):
+        raise NotImplementedError("the backward covers renormalised top-k weights only")
     r = route_and_dispatch(cfg, x, weights["Wr"], expert_bias, noise)
     X = decode(x)
     DY = decode(dY)

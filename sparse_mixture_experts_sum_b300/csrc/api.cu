@@ -19,6 +19,7 @@ moe_status validate(const moe_config* cfg) {
   if (cfg->min_capacity < 0 || !(cfg->capacity_factor == cfg->capacity_factor)) return MOE_ERR_INVALID_ARG;
   if (static_cast<long long>(cfg->T) * cfg->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
   if (cfg->dtype == MOE_BF16 && ((cfg->d % 8) || (cfg->h % 8))) return MOE_ERR_UNSUPPORTED;
+  if (cfg->route_flags & ~(MOE_ROUTE_RAW_PROBS | MOE_ROUTE_TOKEN_MAJOR)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -39,7 +40,7 @@ size_t esize(const moe_config* cfg) { return cfg->dtype == MOE_BF16 ? 2 : 4; }
 // [header | dYp | dAB | dXp | dot | dl | importance | coef | router partials
 // | shared dAB].
 struct WsLayout {
-  size_t dispatch_off, route_off;
+  size_t dispatch_off, route_off, ent;
   size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs;
   size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs;
   size_t total;
@@ -70,6 +71,7 @@ WsLayout layout(const moe_config* cfg, int training) {
   }
   L.dispatch_off = take(dispatch_scratch_bytes(*cfg));
   L.route_off = take(route_scratch_bytes(*cfg));
+  L.ent = take(T * 4);
   if (!training) {
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
@@ -260,7 +262,8 @@ moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr, const float* expert_bias,
-                     const float* noise, int* idx, float* w, int* counts, void* ws, moe_stream_t stream) {
+                     const float* noise, int* idx, float* w, int* counts, float* entropy, void* ws,
+                     moe_stream_t stream) {
   moe_status s = validate(cfg);
   if (s != MOE_OK) return s;
   if (!x || !Wr || !idx || !w || !counts) return MOE_ERR_INVALID_ARG;
@@ -269,7 +272,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr, const
   void* scratch = ws && route_scratch_bytes(*cfg) ? at(ws, layout(cfg, 1).route_off) : nullptr;
   int* err = ws ? static_cast<int*>(ws) : nullptr;
   if (err && cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
-  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, scratch, err, st);
+  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, entropy, scratch, err, st);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x, int* kept, int* offsets, int* pos,
@@ -379,12 +382,17 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
   int* err = static_cast<int*>(ws);
   if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
 
-  s = launch_route(*cfg, x, wts->Wr, wts->expert_bias, noise, S.idx, S.w, S.counts,
+  float* ent = stats ? static_cast<float*>(at(ws, L.ent)) : nullptr;
+  s = launch_route(*cfg, x, wts->Wr, wts->expert_bias, noise, S.idx, S.w, S.counts, ent,
                    route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr, err, st);
   if (s != MOE_OK) return s;
   s = launch_dispatch(*cfg, capacity_of(cfg), S.idx, x, S.kept, S.offsets, S.pos, S.Xp, stats,
                       at(ws, L.dispatch_off), st);
   if (s != MOE_OK) return s;
+  if (stats) {
+    s = launch_entropy_mean(ent, cfg->T, stats, st);
+    if (s != MOE_OK) return s;
+  }
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
   if (cfg->has_shared && cfg->dtype == MOE_BF16) {
     // bf16: the shared expert runs inside the routed launches
@@ -414,6 +422,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
   if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if ((cfg->d % 64) || (cfg->h % 64)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->route_flags & MOE_ROUTE_RAW_PROBS) return MOE_ERR_UNSUPPORTED;
   if (!wts->Wr || !wts->W1 || !wts->W2 || (swiglu && !wts->W3)) return MOE_ERR_INVALID_ARG;
   if (cfg->has_shared && (!wts->Ws1 || !wts->Ws2 || (swiglu && !wts->Ws3))) return MOE_ERR_INVALID_ARG;
   const moe_saved& S = *saved;

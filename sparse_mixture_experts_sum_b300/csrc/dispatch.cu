@@ -32,14 +32,22 @@ constexpr int CH = 4096;     // slots per chunk
 constexpr int DT = 256;      // threads of the chunk kernels
 constexpr int DW = DT / 32;  // warps of the chunk kernels
 
-__device__ __forceinline__ int slot_expert(const int* idx, int T, int k, long long s, int& t, int& j) {
-  j = static_cast<int>(s / T);
-  t = static_cast<int>(s - static_cast<long long>(j) * T);
+// Slot s in priority order -> (t, j) and its expert.  Slot-major: s = j*T + t;
+// token-major: s = t*k + j (the row-major order of idx).
+__device__ __forceinline__ int slot_expert(const int* idx, int T, int k, bool token_major, long long s, int& t,
+                                           int& j) {
+  if (token_major) {
+    t = static_cast<int>(s / k);
+    j = static_cast<int>(s - static_cast<long long>(t) * k);
+  } else {
+    j = static_cast<int>(s / T);
+    t = static_cast<int>(s - static_cast<long long>(j) * T);
+  }
   return idx[static_cast<size_t>(t) * k + j];
 }
 
 __global__ void __launch_bounds__(DT) slot_hist_kernel(const int* __restrict__ idx, int T, int k, int E,
-                                                       int* __restrict__ blockhist) {
+                                                       bool token_major, int* __restrict__ blockhist) {
   extern __shared__ int hist[];  // E + 1 (last: unrouted)
   for (int e = threadIdx.x; e <= E; e += DT) hist[e] = 0;
   __syncthreads();
@@ -49,7 +57,7 @@ __global__ void __launch_bounds__(DT) slot_hist_kernel(const int* __restrict__ i
     const long long s = s0 + i;
     if (s >= nslots) break;
     int t, j;
-    const int e = slot_expert(idx, T, k, s, t, j);
+    const int e = slot_expert(idx, T, k, token_major, s, t, j);
     atomicAdd(&hist[(e >= 0 && e < E) ? e : E], 1);
   }
   __syncthreads();
@@ -168,13 +176,15 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
       st.numeric_error = unrouted / k;
       st.drop_rate = static_cast<double>(nslots - kept_s) / static_cast<double>(nslots);
       st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
+      st.router_entropy = __longlong_as_double(0x7ff8000000000000LL);  // set by the layer forward
       *stats = st;
     }
   }
 }
 
 __global__ void __launch_bounds__(DT) assign_kernel(const int* __restrict__ idx, int T, int k, int E,
-                                                    const int* __restrict__ base, const int* __restrict__ kept,
+                                                    bool token_major, const int* __restrict__ base,
+                                                    const int* __restrict__ kept,
                                                     const int* __restrict__ offsets, int* __restrict__ pos) {
   extern __shared__ int sm[];
   int* runcnt = sm;       // [E]
@@ -192,7 +202,7 @@ __global__ void __launch_bounds__(DT) assign_kernel(const int* __restrict__ idx,
     int t = 0, j = 0, e = -1;
     const bool in = s < nslots;
     if (in) {
-      e = slot_expert(idx, T, k, s, t, j);
+      e = slot_expert(idx, T, k, token_major, s, t, j);
       if (e >= E) e = -1;
     }
     const int key = in ? e : -2;
@@ -305,6 +315,44 @@ __global__ void combine_f32_kernel(const float* __restrict__ Yp, const int* __re
   }
 }
 
+// stats->router_entropy = the mean of the finite entries of ent[0..T):
+// each thread sums a strided subset in fp64, then warps and the block
+// reduce in a fixed order (NaN when no token is finite).
+__global__ void __launch_bounds__(1024) entropy_mean_kernel(const float* __restrict__ ent, int T,
+                                                            moe_stats* stats) {
+  __shared__ double rs[32];
+  __shared__ int rc[32];
+  double s = 0.0;
+  int c = 0;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    const float v = ent[t];
+    if (isfinite(v)) {
+      s += v;
+      ++c;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    c += __shfl_xor_sync(0xffffffffu, c, o);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    rs[warp] = s;
+    rc[warp] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double ts = 0.0;
+    long long tc = 0;
+    for (int w2 = 0; w2 < (blockDim.x >> 5); ++w2) {
+      ts += rs[w2];
+      tc += rc[w2];
+    }
+    stats->router_entropy = tc > 0 ? ts / tc : __longlong_as_double(0x7ff8000000000000LL);
+  }
+}
+
 inline int n_chunks(const moe_config& cfg) {
   const long long n = static_cast<long long>(cfg.T) * cfg.k;
   return static_cast<int>((n + CH - 1) / CH);
@@ -325,11 +373,12 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
   int* blockhist = static_cast<int*>(scratch);
   int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) +
                                      align_up(static_cast<size_t>(nb) * (cfg.E + 1) * sizeof(int), 256));
-  slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(idx, cfg.T, cfg.k, cfg.E, blockhist);
+  const bool tm = (cfg.route_flags & MOE_ROUTE_TOKEN_MAJOR) != 0;
+  slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, blockhist);
   capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance, base,
                                                kept, offsets, stats);
   const size_t asmem = static_cast<size_t>(cfg.E) * (DW + 1) * sizeof(int);
-  assign_kernel<<<nb, DT, asmem, stream>>>(idx, cfg.T, cfg.k, cfg.E, base, kept, offsets, pos);
+  assign_kernel<<<nb, DT, asmem, stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, base, kept, offsets, pos);
   if (Xp) {
     const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
     const long long row_bytes = static_cast<long long>(cfg.d) * es;
@@ -370,6 +419,11 @@ moe_status static_dispatch_scratch(size_t need, void** ptr) {
   }
   *ptr = addr[dev];
   return MOE_OK;
+}
+
+moe_status launch_entropy_mean(const float* ent, int T, moe_stats* stats, cudaStream_t stream) {
+  entropy_mean_kernel<<<1, 1024, 0, stream>>>(ent, T, stats);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos, const float* w, const void* Sx,

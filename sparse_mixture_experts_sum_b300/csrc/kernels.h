@@ -80,8 +80,10 @@ moe_status launch_grouped_gemm_f32(const GemmParams& p, const void* A, long long
 // err: the workspace error word of that path's GEMM (nullable).
 size_t route_scratch_bytes(const moe_config& cfg);
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
-                        const float* noise, int* idx, float* w, int* counts, void* scratch, int* err,
+                        const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* err,
                         cudaStream_t stream);
+// stats->router_entropy = mean of the finite ent[0..T) (fixed-order fp64 sum).
+moe_status launch_entropy_mean(const float* ent, int T, moe_stats* stats, cudaStream_t stream);
 
 // Dispatch: slot-major capacity ranks, offsets, positions, statistics, permute.
 size_t dispatch_scratch_bytes(const moe_config& cfg);

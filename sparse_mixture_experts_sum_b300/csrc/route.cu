@@ -53,13 +53,49 @@ __device__ __forceinline__ void topk_insert(float (&v)[MAXK], int (&ix)[MAXK], i
   }
 }
 
+// Running softmax statistics over a token's logits (any order):
+//   m = max l,  Z = sum exp(l - m),  S = sum exp(l - m) (l - m),
+// so that p_e = exp(l_e - m) / Z and the entropy -sum p ln p = ln Z - S/Z.
+struct SoftStat {
+  float m, Z, S;
+  __device__ __forceinline__ SoftStat() : m(-INFINITY), Z(0.f), S(0.f) {}
+  __device__ __forceinline__ void add(float v) { merge(v, 1.f, 0.f); }
+  __device__ __forceinline__ void merge(float m2, float Z2, float S2) {
+    if (Z2 == 0.f) return;
+    if (Z == 0.f) {
+      m = m2;
+      Z = Z2;
+      S = S2;
+      return;
+    }
+    if (m2 > m) {
+      const float sc = expf(m - m2);
+      S = sc * (S + (m - m2) * Z) + S2;
+      Z = sc * Z + Z2;
+      m = m2;
+    } else {
+      const float sc = expf(m2 - m);
+      S += sc * (S2 + (m2 - m) * Z2);
+      Z += sc * Z2;
+    }
+  }
+  __device__ __forceinline__ float entropy() const { return logf(Z) - S / Z; }
+};
+
+// Weights, indices, entropy and histogram of one token from its sorted
+// top-k (v descending, ix).  raw: w_j = p_{ix_j} from the softmax over all
+// experts (st holds its statistics); otherwise the softmax over the k
+// selected logits.  ent (nullable) receives the token's router entropy (NaN
+// for a token with a non-finite logit, which is routed nowhere).
 __device__ __forceinline__ void topk_finish(const float (&v)[MAXK], const int (&ix)[MAXK], int k, bool finite,
-                                            int t, int* idx, float* w, int* hist) {
+                                            int t, int* idx, float* w, int* hist, bool raw, const SoftStat& st,
+                                            float* ent) {
   if (!finite) {
     for (int j = 0; j < k; ++j) {
       idx[static_cast<size_t>(t) * k + j] = -1;
       w[static_cast<size_t>(t) * k + j] = 0.f;
     }
+    if (ent) ent[t] = __int_as_float(0x7fc00000);
     return;
   }
   float ex[MAXK];
@@ -67,11 +103,11 @@ __device__ __forceinline__ void topk_finish(const float (&v)[MAXK], const int (&
 #pragma unroll
   for (int j = 0; j < MAXK; ++j) {
     if (j < k) {
-      ex[j] = expf(v[j] - v[0]);
+      ex[j] = expf(v[j] - (raw ? st.m : v[0]));
       s += ex[j];
     }
   }
-  const float inv = 1.0f / s;
+  const float inv = 1.0f / (raw ? st.Z : s);
 #pragma unroll
   for (int j = 0; j < MAXK; ++j) {
     if (j < k) {
@@ -80,6 +116,7 @@ __device__ __forceinline__ void topk_finish(const float (&v)[MAXK], const int (&
       atomicAdd(&hist[ix[j]], 1);
     }
   }
+  if (ent) ent[t] = st.entropy();
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -125,7 +162,8 @@ template <int STAGES>
 __global__ void __launch_bounds__(128)
 route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const float* __restrict__ ebias,
                   const float* __restrict__ noise, int T, int d, int E, int k, int* __restrict__ idx,
-                  float* __restrict__ w, int* __restrict__ counts, int kb_per_split, float* __restrict__ partial) {
+                  float* __restrict__ w, int* __restrict__ counts, int kb_per_split, float* __restrict__ partial,
+                  int raw, float* __restrict__ ent) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const RouteLayout Lay(E, STAGES);
   const int nep = Lay.nep;
@@ -153,6 +191,8 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
     tix[j] = -1;
   }
   bool finite = true;
+  const bool need_stat = raw || ent;
+  SoftStat sst;
 
   for (int e0 = 0; e0 < E; e0 += RT_NE) {
     const int ne = min(RT_NE, E - e0);
@@ -251,13 +291,14 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
         const float v = L[tid * (nep + 1) + col];
         if (!isfinite(v)) finite = false;
         topk_insert(tv, tix, k, v, e0 + col);
+        if (need_stat && finite) sst.add(v);
       }
     }
     __syncthreads();  // L is the ring again for the next expert chunk
   }
 
   if (partial) return;
-  if (tid < RT_TM && t0 + tid < T) topk_finish(tv, tix, k, finite, t0 + tid, idx, w, hist);
+  if (tid < RT_TM && t0 + tid < T) topk_finish(tv, tix, k, finite, t0 + tid, idx, w, hist, raw, sst, ent);
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x)
     if (hist[e]) atomicAdd(&counts[e], hist[e]);
@@ -270,7 +311,8 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
 // idx, the renormalised weights and the block histogram.
 __global__ void __launch_bounds__(256)
 route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ ebias, const float* __restrict__ noise,
-                  int T, int E, int k, int* __restrict__ idx, float* __restrict__ w, int* __restrict__ counts) {
+                  int T, int E, int k, int* __restrict__ idx, float* __restrict__ w, int* __restrict__ counts,
+                  int raw, float* __restrict__ ent) {
   extern __shared__ int hist_s[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
   __syncthreads();
@@ -285,6 +327,8 @@ route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ eb
       tix[j] = -1;
     }
     bool finite = true;
+    const bool need_stat = raw || ent;
+    SoftStat sst;
     const float* lr = logits + static_cast<size_t>(t) * E;
     const float* nr = noise ? noise + static_cast<size_t>(t) * E : nullptr;
     for (int e = lane; e < E; e += 32) {
@@ -293,8 +337,18 @@ route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ eb
       if (nr) v += nr[e];
       if (!isfinite(v)) finite = false;
       topk_insert(tv, tix, k, v, e);
+      if (need_stat && finite) sst.add(v);
     }
     finite = __all_sync(0xffffffffu, finite);
+    if (need_stat && finite) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, sst.m, o);
+        const float Z2 = __shfl_xor_sync(0xffffffffu, sst.Z, o);
+        const float S2 = __shfl_xor_sync(0xffffffffu, sst.S, o);
+        sst.merge(m2, Z2, S2);
+      }
+    }
     float sel_v[MAXK];
     int sel_i[MAXK];
     int head = 0;  // next unconsumed entry of this lane's list
@@ -324,16 +378,7 @@ route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ eb
         if (head < MAXK && tix[head] == bi) ++head;
       }
     }
-    if (lane == 0) {
-      if (!finite) {
-        for (int j = 0; j < k; ++j) {
-          idx[static_cast<size_t>(t) * k + j] = -1;
-          w[static_cast<size_t>(t) * k + j] = 0.f;
-        }
-      } else {
-        topk_finish(sel_v, sel_i, k, true, t, idx, w, hist_s);
-      }
-    }
+    if (lane == 0) topk_finish(sel_v, sel_i, k, finite, t, idx, w, hist_s, raw, sst, ent);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -344,7 +389,7 @@ route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ eb
 __global__ void route_f32_kernel(const float* __restrict__ x, const float* __restrict__ Wr,
                                  const float* __restrict__ ebias, const float* __restrict__ noise, int T, int d,
                                  int E, int k, int* __restrict__ idx, float* __restrict__ w,
-                                 int* __restrict__ counts) {
+                                 int* __restrict__ counts, int raw, float* __restrict__ ent) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -357,6 +402,8 @@ __global__ void route_f32_kernel(const float* __restrict__ x, const float* __res
     tix[j] = -1;
   }
   bool finite = true;
+  const bool need_stat = raw || ent;
+  SoftStat sst;
   const float* xr = x + static_cast<size_t>(t) * d;
   for (int e = 0; e < E; ++e) {
     const float* wr = Wr + static_cast<size_t>(e) * d;
@@ -368,8 +415,9 @@ __global__ void route_f32_kernel(const float* __restrict__ x, const float* __res
     if (noise) s += noise[static_cast<size_t>(t) * E + e];
     if (!isfinite(s)) finite = false;
     topk_insert(tv, tix, k, s, e);
+    if (need_stat && finite) sst.add(s);
   }
-  if (lane == 0) topk_finish(tv, tix, k, finite, t, idx, w, counts);
+  if (lane == 0) topk_finish(tv, tix, k, finite, t, idx, w, counts, raw, sst, ent);
 }
 
 }  // namespace
@@ -378,7 +426,7 @@ namespace {
 
 template <int STAGES>
 moe_status launch_route_stages(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
-                               const float* noise, int* idx, float* w, int* counts, cudaStream_t stream) {
+                               const float* noise, int* idx, float* w, int* counts, float* ent, cudaStream_t stream) {
   const RouteLayout Lay(cfg.E, STAGES);
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -394,7 +442,7 @@ moe_status launch_route_stages(const moe_config& cfg, const void* x, const void*
   dim3 grid((cfg.T + RT_TM - 1) / RT_TM, 1);
   route_bf16_kernel<STAGES><<<grid, 128, Lay.total, stream>>>(
       static_cast<const bf16*>(x), static_cast<const bf16*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E, cfg.k,
-      idx, w, counts, nk, nullptr);
+      idx, w, counts, nk, nullptr, (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0, ent);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -409,8 +457,9 @@ size_t route_scratch_bytes(const moe_config& cfg) {
 }
 
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
-                        const float* noise, int* idx, float* w, int* counts, void* scratch, int* err,
+                        const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* err,
                         cudaStream_t stream) {
+  const int raw = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0;
   if (cudaMemsetAsync(counts, 0, sizeof(int) * cfg.E, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (route_on_tensor_cores(cfg) && scratch) {
     // logits = x . Wr^T on the tcgen05 grouped GEMM (one group of T rows,
@@ -428,17 +477,18 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     if (s != MOE_OK) return s;
     const unsigned grid = static_cast<unsigned>((static_cast<long long>(cfg.T) * 32 + 255) / 256);
     route_topk_kernel<<<grid, 256, sizeof(int) * cfg.E, stream>>>(static_cast<const float*>(scratch), expert_bias,
-                                                                   noise, cfg.T, cfg.E, cfg.k, idx, w, counts);
+                                                                   noise, cfg.T, cfg.E, cfg.k, idx, w, counts, raw,
+                                                                   ent);
   } else if (cfg.dtype == MOE_BF16) {
     const int nep = ((cfg.E < RT_NE ? cfg.E : RT_NE) + 7) / 8 * 8;
-    return nep <= 64 ? launch_route_stages<5>(cfg, x, Wr, expert_bias, noise, idx, w, counts, stream)
-                     : launch_route_stages<3>(cfg, x, Wr, expert_bias, noise, idx, w, counts, stream);
+    return nep <= 64 ? launch_route_stages<5>(cfg, x, Wr, expert_bias, noise, idx, w, counts, ent, stream)
+                     : launch_route_stages<3>(cfg, x, Wr, expert_bias, noise, idx, w, counts, ent, stream);
   } else {
     const int threads = 256;
     const long long grid = (static_cast<long long>(cfg.T) * 32 + threads - 1) / threads;
     route_f32_kernel<<<static_cast<unsigned>(grid), threads, 0, stream>>>(
         static_cast<const float*>(x), static_cast<const float*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E,
-        cfg.k, idx, w, counts);
+        cfg.k, idx, w, counts, raw, ent);
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

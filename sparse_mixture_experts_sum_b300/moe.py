@@ -27,7 +27,7 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("h", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("act", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int),
-                ("lambda_balance", ctypes.c_float), ("has_shared", ctypes.c_int)]
+                ("lambda_balance", ctypes.c_float), ("has_shared", ctypes.c_int), ("route_flags", ctypes.c_int)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -49,7 +49,7 @@ class MoeStats(ctypes.Structure):
     _fields_ = [("routed_slots", ctypes.c_longlong), ("kept_slots", ctypes.c_longlong),
                 ("dropped_slots", ctypes.c_longlong), ("capacity", ctypes.c_int),
                 ("numeric_error", ctypes.c_int), ("drop_rate", ctypes.c_double),
-                ("balance_stat", ctypes.c_double)]
+                ("balance_stat", ctypes.c_double), ("router_entropy", ctypes.c_double)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -75,7 +75,7 @@ def lib() -> ctypes.CDLL:
         sig = {
             "moe_capacity": [cfgp, ctypes.POINTER(i)],
             "moe_workspace_size": [cfgp, i, ctypes.POINTER(sz)],
-            "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_dispatch_static": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_expert_ffn": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
@@ -116,10 +116,14 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+ROUTE_RAW_PROBS, ROUTE_TOKEN_MAJOR = 1, 2
+
+
 def make_config(T, d, h, E, k, act="swiglu", dtype="bf16", capacity_factor=0.0, min_capacity=0,
-                lambda_balance=0.01, has_shared=False) -> MoeConfig:
+                lambda_balance=0.01, has_shared=False, raw_probs=False, token_major=False) -> MoeConfig:
+    flags = (ROUTE_RAW_PROBS if raw_probs else 0) | (ROUTE_TOKEN_MAJOR if token_major else 0)
     return MoeConfig(T, d, h, E, k, ACT[act], DTYPE[dtype], capacity_factor, min_capacity,
-                     lambda_balance, int(bool(has_shared)))
+                     lambda_balance, int(bool(has_shared)), flags)
 
 
 def config_of(wl) -> MoeConfig:
@@ -154,9 +158,9 @@ def read_stats(buf: torch.Tensor) -> dict:
     return MoeStats.from_buffer_copy(raw).as_dict()
 
 
-def moe_route(cfg, x, Wr, expert_bias, noise, idx, w, counts, ws=None, stream=None):
+def moe_route(cfg, x, Wr, expert_bias, noise, idx, w, counts, ws=None, stream=None, entropy=None):
     _check("moe_route", lib().moe_route(ctypes.byref(cfg), _p(x), _p(Wr), _p(expert_bias), _p(noise),
-                                        _p(idx), _p(w), _p(counts), _p(ws), _stream(stream)))
+                                        _p(idx), _p(w), _p(counts), _p(entropy), _p(ws), _stream(stream)))
 
 
 def moe_dispatch(cfg, idx, x, kept, offsets, pos, Xp, stats, ws, stream=None):

@@ -52,6 +52,8 @@ int main(void) {
   printf("%zu %zu %zu %zu\n", sizeof(moe_config), sizeof(moe_weights), sizeof(moe_saved), sizeof(moe_stats));
   printf("%zu %zu %zu %zu\n", offsetof(moe_config, has_shared), offsetof(moe_stats, drop_rate),
          offsetof(moe_stats, balance_stat), offsetof(moe_weights, expert_bias));
+  printf("%zu %zu %zu %zu\n", offsetof(moe_config, route_flags), offsetof(moe_stats, router_entropy),
+         offsetof(moe_saved, Zs), sizeof(moe_grads));
   return 0;
 }'''
     with tempfile.TemporaryDirectory() as d:
@@ -63,7 +65,9 @@ int main(void) {
     m = M.moe
     got = [ctypes.sizeof(m.MoeConfig), ctypes.sizeof(m.MoeWeights), ctypes.sizeof(m.MoeSaved),
            ctypes.sizeof(m.MoeStats), m.MoeConfig.has_shared.offset, m.MoeStats.drop_rate.offset,
-           m.MoeStats.balance_stat.offset, m.MoeWeights.expert_bias.offset]
+           m.MoeStats.balance_stat.offset, m.MoeWeights.expert_bias.offset,
+           m.MoeConfig.route_flags.offset, m.MoeStats.router_entropy.offset, m.MoeSaved.Zs.offset,
+           ctypes.sizeof(m.MoeGrads)]
     assert [int(v) for v in out] == got
 
 
@@ -77,13 +81,15 @@ def test_capacity_matches_oracle(M, T, k, E, cf, minc):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(k=5, E=4), 1), (dict(k=9, E=16), 1), (dict(E=1025), 1), (dict(T=0), 1),
-    (dict(d=100), 2), (dict(h=36), 2), (dict(act=7), 1)])
+    (dict(d=100), 2), (dict(h=36), 2), (dict(act=7), 1), (dict(route_flags=4), 1)])
 def test_bad_configs_rejected(M, kw, status):
     base = dict(T=64, d=64, h=64, E=8, k=2)
     base.update({k: v for k, v in kw.items() if k in base})
     cfg = M.make_config(**base)
     if "act" in kw:
         cfg.act = kw["act"]
+    if "route_flags" in kw:
+        cfg.route_flags = kw["route_flags"]
     with pytest.raises(M.moe.MoeError) as ei:
         M.moe_workspace_size(cfg)
     assert ei.value.status == status
@@ -92,7 +98,7 @@ def test_bad_configs_rejected(M, kw, status):
 def test_null_pointers_rejected_before_launch(M):
     cfg = M.make_config(64, 64, 64, 8, 2)
     lib = M.moe.lib()
-    st = lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None)
+    st = lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, None)
     assert st == M.moe.MOE_ERR_INVALID_ARG
     st = lib.moe_layer_fwd(ctypes.byref(cfg), None, None, None, None, None, None, None, 0, None)
     assert st == M.moe.MOE_ERR_INVALID_ARG

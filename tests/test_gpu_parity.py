@@ -48,6 +48,10 @@ def check_routing(r, sv, stats, x=None):
         assert stats[key] == ref[key], key
     assert abs(stats["drop_rate"] - ref["drop_rate"]) <= 1e-15
     assert abs(stats["balance_stat"] - ref["balance_stat"]) <= 1e-12 * max(1.0, abs(ref["balance_stat"]))
+    # the router entropy (fp32 per token, fp64 mean); moe_dispatch alone leaves NaN
+    if not np.isnan(stats["router_entropy"]):
+        assert abs(stats["router_entropy"] - ref["router_entropy"]) <= 2e-5, (stats["router_entropy"],
+                                                                                ref["router_entropy"])
     if x is not None:
         # every kept slot's row is an exact copy of its token
         pos = sv["pos"].long()
@@ -409,3 +413,34 @@ def test_route_with_workspace(T, d, E, k):
         np.testing.assert_array_equal(counts.cpu().numpy(), O.usage_counts(ridx, E))
     for a, b in zip(outs[0], outs[1]):
         assert torch.equal(a, b)
+
+
+
+@pytest.mark.parametrize("raw,tm,E", [(True, False, 16), (False, True, 16), (True, True, 12), (True, False, 130)])
+def test_routing_variants(raw, tm, E):
+    """Raw softmax weights ([P2] 3.2, [P4] 5.1) and token-major capacity
+    priority, through the tensor-core router (E multiple of 8) and the
+    mma.sync one (E = 12, 130); capacity binds (cf 0.8)."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=700, d=256, h=256, E=E, capacity_factor=0.8, seed=27)
+    t = guarded_inputs(wl, DEV)
+    cfg = M.make_config(wl.T, wl.d, wl.h, wl.E, wl.k, wl.act, wl.dtype, capacity_factor=wl.capacity_factor,
+                        raw_probs=raw, token_major=tm)
+    sv = M.moe.alloc_saved(cfg)
+    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg, 1)
+    M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], None, y, sv, st, ws)
+    assert M.moe_check_error(ws) == 0
+    ocfg = dict(oracle_cfg(wl), raw_probs=raw, token_major=tm)
+    r = O.layer_forward(ocfg, oracle_weights(t), t["x"])
+    stats = M.moe.read_stats(st)
+    check_routing(r, sv, stats, t["x"])
+    assert stats["dropped_slots"] > 0
+    if raw:
+        assert (sv["w"].sum(dim=1) < 0.999).all()  # not renormalised
+    assert_close_bf16(to_np(y), r["y"], "y")
+    if raw:
+        g = M.moe.alloc_grads(cfg)
+        with pytest.raises(M.moe.MoeError) as ei:
+            M.moe_layer_bwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], sv, y, g, M.moe.workspace(cfg, 2))
+        assert ei.value.status == M.moe.MOE_ERR_UNSUPPORTED

@@ -471,3 +471,73 @@ def test_sampled_backward_entries_match_full_backward(act, shared):
             np.testing.assert_allclose(sl["db1"], full["db1"][e][cols], atol=1e-12)
     toks = [0, 3, 11, 29]
     np.testing.assert_allclose(O.token_input_grads(cfg, w, x, dY, r, toks), full["dX"][toks], atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# routing variants
+# ---------------------------------------------------------------------------
+
+
+def test_raw_probability_weights_on_gate_sample():
+    """[P4] 5.1 prints the top-2 probabilities (0.85, 0.08) as the weights it
+    uses; raw_probs returns exactly those, not renormalised."""
+    g = read_golden("top2_gate_sample.txt")
+    p = np.array(g["probs"])
+    idx, w, _ = O.top_k_route(np.log(p)[None, :], 2, raw_probs=True)
+    assert idx[0].tolist() == [1, 2]
+    np.testing.assert_allclose(w[0], g["top2_probs"], rtol=1e-14)
+    # raw weights are the softmax entries: they sum to p1 + p2 < 1
+    rl = _rng(31).normal(size=(50, 9))
+    idx, w, _ = O.top_k_route(rl, 3, raw_probs=True)
+    sm = O.softmax(rl)
+    np.testing.assert_allclose(w, np.take_along_axis(sm, idx, axis=1), rtol=1e-13)
+
+
+def test_router_entropy_closed_forms_and_library():
+    from scipy.stats import entropy
+    E = 16
+    assert abs(O.router_entropy(np.zeros((5, E))) - math.log(E)) < 1e-14
+    one_hot = np.full((3, E), -1e4)
+    one_hot[:, 2] = 0.0
+    assert O.router_entropy(one_hot) < 1e-12
+    l = _rng(33).normal(size=(40, E)) * 2
+    ref = np.mean([entropy(O.softmax(l[t:t + 1])[0]) for t in range(40)])
+    assert abs(O.router_entropy(l) - ref) < 1e-13
+    # tokens with a non-finite logit are left out
+    l2 = l.copy()
+    l2[3, 0] = np.nan
+    ref2 = np.mean([entropy(O.softmax(l[t:t + 1])[0]) for t in range(40) if t != 3])
+    assert abs(O.router_entropy(l2) - ref2) < 1e-13
+
+
+def _dispatch_token_major_by_sorting(idx, E, C):
+    """Independent formulation: each expert keeps its first C slots in
+    (token t, choice j) order."""
+    T, k = idx.shape
+    pos = -np.ones((T, k), dtype=np.int64)
+    base = 0
+    for e in range(E):
+        mine = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e][:C]
+        for r, (t, j) in enumerate(mine):
+            pos[t, j] = base + r
+        base += len(mine)
+    return pos
+
+
+@pytest.mark.parametrize("T,E,k,cf", [(37, 5, 2, 1.0), (50, 8, 3, 0.6)])
+def test_token_major_capacity(T, E, k, cf):
+    rng = _rng(T + 7 * E)
+    l = rng.normal(size=(T, E)) + np.linspace(2, 0, E)[None, :]
+    idx, _, _ = O.top_k_route(l, k)
+    C = O.expert_capacity(T, k, E, cf)
+    rank, fill = O.assign_capacity(idx, E, C, token_major=True)
+    _, pos = O.dispatch_positions(idx, rank, fill)
+    np.testing.assert_array_equal(pos, _dispatch_token_major_by_sorting(idx, E, C))
+    # a kept slot of an expert never follows, in token order, a dropped one
+    for e in range(E):
+        slots = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e]
+        kept = [pos[t, j] >= 0 for t, j in slots]
+        assert kept == sorted(kept, reverse=True)
+    # the two priority orders differ once capacity binds on second choices
+    rank_s, _ = O.assign_capacity(idx, E, C)
+    assert (rank_s != rank).any()
