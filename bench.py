@@ -166,7 +166,7 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     # one step = the layer's C-ABI stages in the order moe_layer_fwd runs them
     stages = [
         ("route", lambda: M.moe_route(cfg, x, weights["Wr"], weights.get("expert_bias"), noise, sv["idx"], sv["w"],
-                                      sv["counts"])),
+                                      sv["counts"], ws)),
         ("dispatch", lambda: M.moe_dispatch(cfg, sv["idx"], x, sv["kept"], sv["offsets"], sv["pos"], sv["Xp"], st,
                                             ws)),
         ("expert_ffn", lambda: M.moe_expert_ffn(cfg, sv["Xp"], sv["offsets"], weights["W1"], weights.get("W3"),
@@ -245,10 +245,11 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
         "ms_per_step": ms_step,
         "layer_fwd_ms": layer_fwd_ms,
         "stage_path_ms": stage_ms_total / steps,
-        # our kernels per step: moe_layer_fwd = router GEMM + top-k, 4 dispatch,
-        # entropy mean, 2 grouped GEMMs, combine (10); the stage path = the
-        # same without the entropy mean (9)
-        "launches_per_step": 19,
+        # our kernels per step: moe_layer_fwd = zeroing, router GEMM + top-k,
+        # 4 dispatch, entropy mean, 2 grouped GEMMs, combine (11); the stage
+        # path = the same without the entropy mean, plus moe_expert_ffn's
+        # zeroing of the error word (11)
+        "launches_per_step": 22,
         "tokens_per_s": tokens / (ms_step * 1e-3),
         "stats": stats,
         "components_ms": comp,

@@ -271,7 +271,6 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr, const
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   void* scratch = ws && route_scratch_bytes(*cfg) ? at(ws, layout(cfg, 1).route_off) : nullptr;
   int* err = ws ? static_cast<int*>(ws) : nullptr;
-  if (err && cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, entropy, scratch, err, st);
 }
 
@@ -311,7 +310,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offs
     return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
-  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_zero(err, sizeof(int), nullptr, 0, st) != MOE_OK) return MOE_ERR_CUDA;
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
   return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, W1, W3, b1, W2, b2, H, Yp, nullptr, err, st);
 }
@@ -330,7 +329,7 @@ moe_status moe_expert_ffn_shared(const moe_config* cfg, const void* Xp, const in
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
-  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_zero(err, sizeof(int), nullptr, 0, st) != MOE_OK) return MOE_ERR_CUDA;
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
   SharedFfn sh{x, wts, Hs, Sx, nullptr};
   return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, H, Yp, nullptr,
@@ -379,8 +378,7 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
     S.Z = S.Hs = S.Zs = nullptr;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int* err = static_cast<int*>(ws);
-  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  int* err = static_cast<int*>(ws);  // zeroed by the router's first launch
 
   float* ent = stats ? static_cast<float*>(at(ws, L.ent)) : nullptr;
   s = launch_route(*cfg, x, wts->Wr, wts->expert_bias, noise, S.idx, S.w, S.counts, ent,
@@ -437,7 +435,8 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
-  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  s = launch_zero(err, sizeof(int), at(ws, L.imp), sizeof(unsigned long long) * cfg->E, st);
+  if (s != MOE_OK) return s;
   void* dYp = at(ws, L.dYp);
   void* dAB = at(ws, L.dAB);
   float* dXp = static_cast<float*>(at(ws, L.dXp));

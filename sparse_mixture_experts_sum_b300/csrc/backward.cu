@@ -156,46 +156,75 @@ __global__ void router_bwd_kernel(const int* __restrict__ idx, const float* __re
     if (j < k) dl[static_cast<size_t>(t) * k + j] = routed ? wt[j] * (G[j] - s) : 0.f;
 }
 
-constexpr int RW_TOK = 1024;  // tokens per block of the router weight gradient
-constexpr int RW_EXP = 32;    // experts per block (32 KB of per-warp accumulators)
-constexpr int RW_WARPS = 8;
+constexpr int RW_TOK = 512;   // tokens per block of the router weight gradient
+constexpr int RW_EXP = 16;    // experts per block
+constexpr int RW_WARPS = 4;
+constexpr int RW_COLS = 256;  // columns per block: 8 per lane, one 16-byte load per token row
 
-// partial[chunk][e][c] = sum over the chunk's tokens t (ascending, per warp
-// t = warp mod 8) of sum_j [idx=e] dl[t,j] x[t][c]; 32 columns per block,
-// one per lane; every warp accumulates privately in shared memory and the
-// warps are summed in a fixed order.
+// partial[chunk][e][c] = sum over the chunk's tokens (each warp takes every
+// RW_WARPS-th token, ascending) of sum_j [idx=e] dl[t,j] x[t][c].  A block
+// covers 256 columns (a lane owns 8 consecutive ones: one 16-byte load of a
+// bf16 row) and 16 experts; every warp accumulates privately in shared
+// memory, laid out acc[warp][e][q][lane] (column lane*8+q) so that a warp's
+// updates hit 32 distinct banks; the warps are summed in a fixed order.
 template <typename Tx>
 __global__ void __launch_bounds__(RW_WARPS * 32)
 router_wgrad_partial_kernel(const Tx* __restrict__ x, const int* __restrict__ idx, const float* __restrict__ dl,
                             int T, int d, int k, int E, float* __restrict__ partial) {
-  __shared__ float acc[RW_WARPS][RW_EXP][32];
+  extern __shared__ float acc_s[];  // [RW_WARPS][RW_EXP][8][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.y * 32 + lane;
+  float* acc = acc_s + warp * (RW_EXP * 8 * 32);
+  const int c0 = blockIdx.y * RW_COLS + lane * 8;
   const int e0 = blockIdx.z * RW_EXP;
   const int t0 = blockIdx.x * RW_TOK;
-  for (int i = lane; i < RW_EXP * 32; i += 32) (&acc[warp][0][0])[i] = 0.f;
+  for (int i = lane; i < RW_EXP * 8 * 32; i += 32) acc[i] = 0.f;
   __syncwarp();
   const int t1 = min(T, t0 + RW_TOK);
-  for (int t = t0 + warp; t < t1; t += RW_WARPS) {
-    float xv = 0.f;
-    if (c < d) {
-      if constexpr (sizeof(Tx) == 2) xv = __bfloat162float(x[static_cast<size_t>(t) * d + c]);
-      else xv = x[static_cast<size_t>(t) * d + c];
+  constexpr int U = 4;  // token rows in flight per warp
+  for (int tb = t0 + warp; tb < t1; tb += U * RW_WARPS) {
+    float xv[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = tb + u * RW_WARPS;
+      if constexpr (sizeof(Tx) == 2) {
+        uint4 q4 = make_uint4(0, 0, 0, 0);
+        if (t < t1 && c0 + 8 <= d) q4 = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + c0);
+        const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          xv[u][2 * i] = bf16lo(wv[i]);
+          xv[u][2 * i + 1] = bf16hi(wv[i]);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          xv[u][q] = (t < t1 && c0 + q < d) ? x[static_cast<size_t>(t) * d + c0 + q] : 0.f;
+      }
     }
-    for (int j = 0; j < k; ++j) {
-      const int e = idx[static_cast<size_t>(t) * k + j] - e0;
-      if (e >= 0 && e < RW_EXP && e0 + e < E)
-        acc[warp][e][lane] = fmaf(dl[static_cast<size_t>(t) * k + j], xv, acc[warp][e][lane]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = tb + u * RW_WARPS;
+      if (t >= t1) break;
+      for (int j = 0; j < k; ++j) {
+        const int e = idx[static_cast<size_t>(t) * k + j] - e0;
+        if (e >= 0 && e < RW_EXP && e0 + e < E) {
+          const float g = dl[static_cast<size_t>(t) * k + j];
+          float* a = acc + e * 256 + lane;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) a[q * 32] = fmaf(g, xv[u][q], a[q * 32]);
+        }
+      }
     }
   }
   __syncthreads();
   const int ne = min(RW_EXP, E - e0);
-  for (int i = threadIdx.x; i < ne * 32; i += blockDim.x) {
-    const int e = i >> 5, l = i & 31;
-    const int cc = blockIdx.y * 32 + l;
+  for (int i = threadIdx.x; i < ne * RW_COLS; i += blockDim.x) {
+    const int e = i / RW_COLS, c = i - e * RW_COLS;
+    const int cc = blockIdx.y * RW_COLS + c;
+    const int off = e * 256 + (c & 7) * 32 + (c >> 3);
     float s = 0.f;
 #pragma unroll
-    for (int w2 = 0; w2 < RW_WARPS; ++w2) s += acc[w2][e][l];
+    for (int w2 = 0; w2 < RW_WARPS; ++w2) s += acc_s[w2 * (RW_EXP * 8 * 32) + off];
     if (cc < d) partial[(static_cast<size_t>(blockIdx.x) * E + e0 + e) * d + cc] = s;
   }
 }
@@ -227,6 +256,7 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
     g[j] = j < k ? dl[static_cast<size_t>(t) * k + j] : 0.f;
   }
   float* out = dX + static_cast<size_t>(t) * d;
+#pragma unroll 4
   for (int c = lane * 4; c < d; c += 128) {
     float4 a = accumulate ? *reinterpret_cast<const float4*>(out + c) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -297,7 +327,6 @@ moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* 
 moe_status launch_router_bwd(const moe_config& cfg, const int* idx, const float* w, const float* dot,
                              unsigned long long* imp, float* coef, float* dl, cudaStream_t st) {
   const long long nslots = static_cast<long long>(cfg.T) * cfg.k;
-  if (cudaMemsetAsync(imp, 0, sizeof(unsigned long long) * cfg.E, st) != cudaSuccess) return MOE_ERR_CUDA;
   long long blocks = (nslots + 255) / 256;
   if (blocks > 1184) blocks = 1184;
   importance_kernel<<<static_cast<unsigned>(blocks), 256, sizeof(unsigned long long) * cfg.E, st>>>(idx, w, nslots,
@@ -310,13 +339,25 @@ moe_status launch_router_bwd(const moe_config& cfg, const int* idx, const float*
 moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl, float* partial,
                                float* dWr, cudaStream_t st) {
   const int nchunks = (cfg.T + RW_TOK - 1) / RW_TOK;
-  dim3 grid(nchunks, (cfg.d + 31) / 32, (cfg.E + RW_EXP - 1) / RW_EXP);
+  dim3 grid(nchunks, (cfg.d + RW_COLS - 1) / RW_COLS, (cfg.E + RW_EXP - 1) / RW_EXP);
+  const size_t smem = sizeof(float) * RW_WARPS * RW_EXP * 8 * 32;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(router_wgrad_partial_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(router_wgrad_partial_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set[dev] = true;
+  }
   if (cfg.dtype == MOE_BF16)
-    router_wgrad_partial_kernel<bf16><<<grid, RW_WARPS * 32, 0, st>>>(static_cast<const bf16*>(x), idx, dl, cfg.T,
-                                                                      cfg.d, cfg.k, cfg.E, partial);
+    router_wgrad_partial_kernel<bf16><<<grid, RW_WARPS * 32, smem, st>>>(static_cast<const bf16*>(x), idx, dl, cfg.T,
+                                                                         cfg.d, cfg.k, cfg.E, partial);
   else
-    router_wgrad_partial_kernel<float><<<grid, RW_WARPS * 32, 0, st>>>(static_cast<const float*>(x), idx, dl, cfg.T,
-                                                                       cfg.d, cfg.k, cfg.E, partial);
+    router_wgrad_partial_kernel<float><<<grid, RW_WARPS * 32, smem, st>>>(static_cast<const float*>(x), idx, dl,
+                                                                          cfg.T, cfg.d, cfg.k, cfg.E, partial);
   const long long Ed = static_cast<long long>(cfg.E) * cfg.d;
   router_wgrad_reduce_kernel<<<static_cast<unsigned>((Ed + 255) / 256), 256, 0, st>>>(partial, nchunks, Ed, dWr);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -11,8 +11,9 @@
 //   pos[t,j] = offsets[e] + rank, or -1 when dropped / unrouted
 //   Xp[pos[t,j]] = x[t]
 // Four launches, all integer and deterministic (no order-visible atomics):
-//   slot_hist   per 4096-slot chunk, per-expert counts (+ unrouted)
-//   scan        per-expert exclusive scan over chunks, kept, offsets, stats
+//   slot_hist   per chunk of 1024 (or 4096) slots, per-expert counts (+ unrouted)
+//   scan        per-expert exclusive scan over chunks (a warp per expert),
+//               kept, offsets, stats
 //   assign      in-chunk ranks (warp match + per-warp counts), pos
 //   permute     one warp per token copies its row to its k destinations
 //
@@ -28,9 +29,13 @@
 namespace moe {
 namespace {
 
-constexpr int CH = 4096;     // slots per chunk
 constexpr int DT = 256;      // threads of the chunk kernels
 constexpr int DW = DT / 32;  // warps of the chunk kernels
+
+// Slots per chunk of the histogram/rank kernels: 1024 for up to 2^18 slots
+// (enough blocks to fill the GPU), 4096 beyond (so that T*k <= 2^20 slots
+// need at most 256 chunks of scratch).
+inline int chunk_slots(long long nslots) { return nslots <= (1LL << 18) ? 1024 : 4096; }
 
 // Slot s in priority order -> (t, j) and its expert.  Slot-major: s = j*T + t;
 // token-major: s = t*k + j (the row-major order of idx).
@@ -47,7 +52,7 @@ __device__ __forceinline__ int slot_expert(const int* idx, int T, int k, bool to
 }
 
 __global__ void __launch_bounds__(DT) slot_hist_kernel(const int* __restrict__ idx, int T, int k, int E,
-                                                       bool token_major, int* __restrict__ blockhist) {
+                                                       bool token_major, int CH, int* __restrict__ blockhist) {
   extern __shared__ int hist[];  // E + 1 (last: unrouted)
   for (int e = threadIdx.x; e <= E; e += DT) hist[e] = 0;
   __syncthreads();
@@ -74,21 +79,31 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
   __shared__ int unrouted;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  int my_kept = 0;
-  if (tid < E) {
-    int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      base[static_cast<size_t>(b) * E + tid] = run;
-      run += blockhist[static_cast<size_t>(b) * (E + 1) + tid];
+  // per expert (one warp each), exclusive scan of its chunk counts across
+  // chunks, 32 chunks a step; expert E is the "unrouted" column
+  const int nwarps = blockDim.x >> 5;
+  for (int e = warp; e <= E; e += nwarps) {
+    int carry = 0;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int b = b0 + lane;
+      const int v = b < nb ? blockhist[static_cast<size_t>(b) * (E + 1) + e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (e < E && b < nb) base[static_cast<size_t>(b) * E + e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    tot[tid] = run;
-    my_kept = run < C ? run : C;
+    if (lane == 0) {
+      if (e < E) tot[e] = carry;
+      else unrouted = carry;
+    }
   }
-  if (tid == 0) {
-    int u = 0;
-    for (int b = 0; b < nb; ++b) u += blockhist[static_cast<size_t>(b) * (E + 1) + E];
-    unrouted = u;
-  }
+  __syncthreads();
+  int my_kept = 0;
+  if (tid < E) my_kept = tot[tid] < C ? tot[tid] : C;
   // exclusive scan of kept over experts (block-wide, experts in index order)
   int incl = my_kept;
 #pragma unroll
@@ -183,7 +198,7 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
 }
 
 __global__ void __launch_bounds__(DT) assign_kernel(const int* __restrict__ idx, int T, int k, int E,
-                                                    bool token_major, const int* __restrict__ base,
+                                                    bool token_major, int CH, const int* __restrict__ base,
                                                     const int* __restrict__ kept,
                                                     const int* __restrict__ offsets, int* __restrict__ pos) {
   extern __shared__ int sm[];
@@ -235,18 +250,24 @@ __global__ void __launch_bounds__(DT) assign_kernel(const int* __restrict__ idx,
   }
 }
 
-// One warp per token: copy row x[t] to its kept destinations in Xp.
+// One warp per (token, column chunk): copy row x[t] to its kept
+// destinations in Xp.  Small batches split each row into `chunks` pieces so
+// that enough warps are in flight.
 template <typename V>
-__global__ void permute_kernel(const V* __restrict__ x, int T, int k, int vec_per_row, const int* __restrict__ pos,
-                               V* __restrict__ Xp) {
-  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+__global__ void permute_kernel(const V* __restrict__ x, int T, int k, int vec_per_row, int chunks,
+                               const int* __restrict__ pos, V* __restrict__ Xp) {
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int t = static_cast<int>(wid / chunks);
+  const int ch = static_cast<int>(wid - static_cast<long long>(t) * chunks);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   int p[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
   const V* src = x + static_cast<size_t>(t) * vec_per_row;
-  for (int v = lane; v < vec_per_row; v += 32) {
+  const int per = (vec_per_row + chunks - 1) / chunks;
+  const int v1 = min(vec_per_row, (ch + 1) * per);
+  for (int v = ch * per + lane; v < v1; v += 32) {
     const V val = src[v];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -254,11 +275,14 @@ __global__ void permute_kernel(const V* __restrict__ x, int T, int k, int vec_pe
   }
 }
 
-// One warp per token: y[t] = sum_j w[t,j] Yp[pos[t,j]] (+ Sx[t]); 8 bf16 per lane step.
+// One warp per (token, column chunk): y[t] = sum_j w[t,j] Yp[pos[t,j]]
+// (+ Sx[t]); 8 bf16 per lane step.
 __global__ void combine_bf16_kernel(const uint4* __restrict__ Yp, const int* __restrict__ pos,
                                     const float* __restrict__ w, const uint4* __restrict__ Sx, int T, int k,
-                                    int vec_per_row, uint4* __restrict__ y) {
-  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+                                    int vec_per_row, int chunks, uint4* __restrict__ y) {
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int t = static_cast<int>(wid / chunks);
+  const int ch = static_cast<int>(wid - static_cast<long long>(t) * chunks);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   int p[8];
@@ -268,7 +292,9 @@ __global__ void combine_bf16_kernel(const uint4* __restrict__ Yp, const int* __r
     p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
     wt[j] = j < k ? w[static_cast<size_t>(t) * k + j] : 0.f;
   }
-  for (int v = lane; v < vec_per_row; v += 32) {
+  const int per = (vec_per_row + chunks - 1) / chunks;
+  const int v1 = min(vec_per_row, (ch + 1) * per);
+  for (int v = ch * per + lane; v < v1; v += 32) {
     float a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = 0.f;
@@ -324,6 +350,7 @@ __global__ void __launch_bounds__(1024) entropy_mean_kernel(const float* __restr
   __shared__ int rc[32];
   double s = 0.0;
   int c = 0;
+#pragma unroll 8
   for (int t = threadIdx.x; t < T; t += blockDim.x) {
     const float v = ent[t];
     if (isfinite(v)) {
@@ -355,10 +382,21 @@ __global__ void __launch_bounds__(1024) entropy_mean_kernel(const float* __restr
 
 inline int n_chunks(const moe_config& cfg) {
   const long long n = static_cast<long long>(cfg.T) * cfg.k;
-  return static_cast<int>((n + CH - 1) / CH);
+  const int ch = chunk_slots(n);
+  return static_cast<int>((n + ch - 1) / ch);
 }
 
-inline unsigned warp_grid(int T) { return static_cast<unsigned>((static_cast<long long>(T) * 32 + 255) / 256); }
+inline unsigned warp_grid(int T, int chunks = 1) {
+  return static_cast<unsigned>((static_cast<long long>(T) * chunks * 32 + 255) / 256);
+}
+
+// Column chunks per row for the per-token copy kernels: enough warps to
+// keep the memory system busy when the batch is small.
+inline int row_chunks(int T, int vec_per_row) {
+  int c = 1;
+  while (c < 8 && static_cast<long long>(T) * c < 4096 && vec_per_row / (2 * c) >= 32) c *= 2;
+  return c;
+}
 
 }  // namespace
 
@@ -374,22 +412,27 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
   int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) +
                                      align_up(static_cast<size_t>(nb) * (cfg.E + 1) * sizeof(int), 256));
   const bool tm = (cfg.route_flags & MOE_ROUTE_TOKEN_MAJOR) != 0;
-  slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, blockhist);
+  const int CH = chunk_slots(static_cast<long long>(cfg.T) * cfg.k);
+  slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
   capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance, base,
                                                kept, offsets, stats);
   const size_t asmem = static_cast<size_t>(cfg.E) * (DW + 1) * sizeof(int);
-  assign_kernel<<<nb, DT, asmem, stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, base, kept, offsets, pos);
+  assign_kernel<<<nb, DT, asmem, stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets, pos);
   if (Xp) {
     const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
     const long long row_bytes = static_cast<long long>(cfg.d) * es;
-    if (row_bytes % 16 == 0)
-      permute_kernel<uint4><<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const uint4*>(x), cfg.T, cfg.k,
-                                                                  static_cast<int>(row_bytes / 16), pos,
-                                                                  static_cast<uint4*>(Xp));
-    else
-      permute_kernel<uint32_t><<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const uint32_t*>(x), cfg.T,
-                                                                     cfg.k, static_cast<int>(row_bytes / 4), pos,
-                                                                     static_cast<uint32_t*>(Xp));
+    if (row_bytes % 16 == 0) {
+      const int vpr = static_cast<int>(row_bytes / 16);
+      const int ch = row_chunks(cfg.T, vpr);
+      permute_kernel<uint4><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(static_cast<const uint4*>(x), cfg.T, cfg.k, vpr,
+                                                                      ch, pos, static_cast<uint4*>(Xp));
+    } else {
+      const int vpr = static_cast<int>(row_bytes / 4);
+      const int ch = row_chunks(cfg.T, vpr);
+      permute_kernel<uint32_t><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(static_cast<const uint32_t*>(x), cfg.T,
+                                                                         cfg.k, vpr, ch, pos,
+                                                                         static_cast<uint32_t*>(Xp));
+    }
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -429,9 +472,10 @@ moe_status launch_entropy_mean(const float* ent, int T, moe_stats* stats, cudaSt
 moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos, const float* w, const void* Sx,
                           void* y, cudaStream_t stream) {
   if (cfg.dtype == MOE_BF16) {
-    combine_bf16_kernel<<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const uint4*>(Yp), pos, w,
-                                                              static_cast<const uint4*>(Sx), cfg.T, cfg.k,
-                                                              cfg.d / 8, static_cast<uint4*>(y));
+    const int ch = row_chunks(cfg.T, cfg.d / 8);
+    combine_bf16_kernel<<<warp_grid(cfg.T, ch), 256, 0, stream>>>(static_cast<const uint4*>(Yp), pos, w,
+                                                                  static_cast<const uint4*>(Sx), cfg.T, cfg.k,
+                                                                  cfg.d / 8, ch, static_cast<uint4*>(y));
   } else {
     combine_f32_kernel<<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const float*>(Yp), pos, w,
                                                              static_cast<const float*>(Sx), cfg.T, cfg.k, cfg.d,

@@ -77,7 +77,7 @@ moe_status launch_grouped_gemm_f32(const GemmParams& p, const void* A, long long
 
 // Router: logits, top-k, weights, routed counts.  scratch (nullable, at
 // least route_scratch_bytes) holds the fp32 logits of the tensor-core path;
-// err: the workspace error word of that path's GEMM (nullable).
+// err: the workspace error word (nullable), zeroed here with counts.
 size_t route_scratch_bytes(const moe_config& cfg);
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
                         const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* err,
@@ -106,6 +106,7 @@ moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos,
 size_t router_wgrad_partial_bytes(const moe_config& cfg);
 moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* Yp, const int* pos, const float* w,
                              void* dYp, float* dot, cudaStream_t st);
+// imp (E words of 8 bytes) must be zero on entry.
 moe_status launch_router_bwd(const moe_config& cfg, const int* idx, const float* w, const float* dot,
                              unsigned long long* imp, float* coef, float* dl, cudaStream_t st);
 moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl, float* partial,
@@ -120,5 +121,8 @@ moe_status launch_group_colsum(const void* src, long long ld, const int* offsets
 bool make_tma_2d_bf16(CUtensorMap* map, const void* base, long long inner, long long rows, int box_inner,
                       int box_rows);
 int device_sm_count(int dev);
+// Zero a_bytes at a and b_bytes at b (multiples of 4; either may be null)
+// with one small kernel on `stream`.
+moe_status launch_zero(void* a, size_t a_bytes, void* b, size_t b_bytes, cudaStream_t stream);
 
 }  // namespace moe

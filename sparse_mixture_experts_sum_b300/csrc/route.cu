@@ -460,7 +460,8 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
                         const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* err,
                         cudaStream_t stream) {
   const int raw = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0;
-  if (cudaMemsetAsync(counts, 0, sizeof(int) * cfg.E, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status zs = launch_zero(counts, sizeof(int) * cfg.E, err, err ? sizeof(int) : 0, stream);
+  if (zs != MOE_OK) return zs;
   if (route_on_tensor_cores(cfg) && scratch) {
     // logits = x . Wr^T on the tcgen05 grouped GEMM (one group of T rows,
     // N = E, fp32 out), then the top-k per token

@@ -42,6 +42,29 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, long long inner, long 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+// Zero two word ranges in one small launch (the error word and a counter
+// array, typically); a kernel on the compute stream rather than a memset.
+__global__ void zero_words_kernel(uint32_t* __restrict__ a, long long na, uint32_t* __restrict__ b, long long nb) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    if (i < na) a[i] = 0u;
+    else b[i - na] = 0u;
+  }
+}
+}  // namespace
+
+moe_status launch_zero(void* a, size_t a_bytes, void* b, size_t b_bytes, cudaStream_t stream) {
+  const long long na = a ? static_cast<long long>(a_bytes / 4) : 0;
+  const long long nb = b ? static_cast<long long>(b_bytes / 4) : 0;
+  if (na + nb == 0) return MOE_OK;
+  long long blocks = (na + nb + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  zero_words_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<uint32_t*>(a), na,
+                                                                        static_cast<uint32_t*>(b), nb);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int device_sm_count(int dev) {
   static int cache[64] = {0};
   if (dev < 0 || dev >= 64) return 0;
