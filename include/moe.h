@@ -78,8 +78,13 @@ enum { MOE_F32 = 0, MOE_BF16 = 1 };
  *    p1*e1 + p2*e2; [P4] 5.1 uses the top-k probabilities as they are).
  *    Forward only: moe_layer_bwd returns MOE_ERR_UNSUPPORTED.
  *  MOE_ROUTE_TOKEN_MAJOR: capacity is granted token by token (all of token
- *    t's choices, in order, before token t+1's) instead of slot-major. */
-enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2 };
+ *    t's choices, in order, before token t+1's) instead of slot-major.
+ *  MOE_ROUTE_LAYERNORM: the router sees LayerNorm(x[t]) = (x[t] - mean) /
+ *    sqrt(biased variance + 1e-5), unit scale and zero shift ([P2] 5.2, a
+ *    LayerNorm in front of the linear router); the experts still see x.
+ *    bf16 needs the workspace path of moe_route (ws != NULL); moe_layer_bwd
+ *    returns its gradient through the normalisation. */
+enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2, MOE_ROUTE_LAYERNORM = 4 };
 
 /* Layer shape and routing rule.  [P2] 4.2 (capacity_factor, min_capacity),
  * [P1] 4.3 (load_balancing_loss_coef 0.01). */
@@ -188,10 +193,11 @@ moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes
  * both nullable.  Outputs idx [T,k] int32, w [T,k] fp32, counts [E] int32,
  * entropy [T] fp32 (nullable): -sum_e p_e ln p_e of each token's softmax
  * over all experts, NaN for a token with a non-finite logit.
- * ws: NULL, or >= moe_workspace_size(cfg, 1) bytes; with it a batch too
- * small to fill the GPU splits the contraction over more CTAs (the
- * partial logits are summed in a fixed order, so results repeat bit for
- * bit either way). */
+ * ws: NULL, or >= moe_workspace_size(cfg, 1) bytes.  bf16 with ws: the
+ * logits run on the tcgen05 tensor cores into the workspace, then a top-k
+ * pass; without ws a fused mma.sync kernel (MOE_ROUTE_LAYERNORM then
+ * returns MOE_ERR_UNSUPPORTED).  Both sum in a fixed order, so results
+ * repeat bit for bit; the two paths may differ in the last bits of l. */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr,
                      const float* expert_bias, const float* noise, int* idx,
                      float* w, int* counts, float* entropy, void* ws,

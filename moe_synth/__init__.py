@@ -38,8 +38,16 @@ place, so a test that feeds the same inputs to both sides generates them once
 and copies them, never regenerates them on the other device.
 
 Tensor ids: x=1, Wr=2, W1=3, W3=4, W2=5, Ws1=6, Ws3=7, Ws2=8, b1=9, b2=10,
-noise=11, dY=12.  A row of x that is redrawn (see ``redraw_rows``) on attempt
-``a`` comes from tensor id ``1 + 256*a`` at the same element counters.
+noise=11, dY=12, x_scale=13, x_shift=14.  A row of x that is redrawn (see
+``redraw_rows``) on attempt ``a`` comes from tensor id ``1 + 256*a`` at the
+same element counters.
+
+Rows of varying offset and scale (``Workload.x_affine``): row t of x is
+``a_t * z + b_t`` before the storage rounding, z the row's normal draws,
+``a_t = 0.5 + 2.5 u`` (u the t-th uniform of tensor id 13) and
+``b_t = 4 (u' - 0.5)`` (u' the t-th uniform of tensor id 14): activations
+whose rows differ in mean and spread, the input a LayerNorm in front of the
+router normalises.
 """
 
 from __future__ import annotations
@@ -56,7 +64,7 @@ MIX1 = 0xBF58476D1CE4E5B9
 MIX2 = 0x94D049BB133111EB
 
 TID = dict(x=1, Wr=2, W1=3, W3=4, W2=5, Ws1=6, Ws3=7, Ws2=8, b1=9, b2=10,
-           noise=11, dY=12)
+           noise=11, dY=12, x_scale=13, x_shift=14)
 
 _CHUNK = 1 << 25  # elements generated per torch pass (bounds temporaries)
 
@@ -172,6 +180,7 @@ class Workload:
     zipf_s: Optional[float]      # per-expert Zipf(s) logit bias
     gumbel: bool                 # Gumbel(0,1) noise on the router logits
     training: bool
+    x_affine: bool = False       # rows of x with their own offset and scale
 
     def std(self, fan_in: int) -> float:
         return self.weight_std if self.weight_std is not None else 1.0 / math.sqrt(fan_in)
@@ -222,7 +231,12 @@ def make_inputs(wl: Workload, device="cpu", parts: Optional[Iterable[str]] = Non
     s, dt = wl.seed, wl.dtype
     out = {}
     if need("x"):
-        out["x"] = tensor("normal", s, TID["x"], (T, d), dt, 1.0, device)
+        if wl.x_affine:
+            a, b = _row_affine(wl, 0, T, device)
+            z = normal(s, TID["x"], 0, T * d, device).reshape(T, d)
+            out["x"] = store(z * a[:, None] + b[:, None], dt)
+        else:
+            out["x"] = tensor("normal", s, TID["x"], (T, d), dt, 1.0, device)
     if need("Wr"):
         out["Wr"] = tensor("normal", s, TID["Wr"], (E, d), dt, wl.std(d), device)
     if need("W1"):
@@ -254,11 +268,22 @@ def make_inputs(wl: Workload, device="cpu", parts: Optional[Iterable[str]] = Non
     return out
 
 
+def _row_affine(wl: Workload, t0: int, n: int, device):
+    """Scale a_t and offset b_t (fp64) of rows t0 .. t0+n-1 (x_affine)."""
+    a = 0.5 + 2.5 * uniform(wl.seed, TID["x_scale"], t0, n, device)
+    b = 4.0 * (uniform(wl.seed, TID["x_shift"], t0, n, device) - 0.5)
+    return a, b
+
+
 def redraw_rows(wl: Workload, x: torch.Tensor, rows: torch.Tensor, attempt: int) -> None:
     """Replace rows ``rows`` of x (in place) by their draw of attempt ``attempt``:
-    the same element counters of tensor id ``1 + 256*attempt``."""
+    the same element counters of tensor id ``1 + 256*attempt`` (a row keeps
+    its offset and scale under x_affine)."""
     d = wl.d
     tid = TID["x"] + 256 * attempt
     for t in rows.tolist():
         v = normal(wl.seed, tid, t * d, d, x.device)
+        if wl.x_affine:
+            a, b = _row_affine(wl, t, 1, x.device)
+            v = v * a[0] + b[0]
         x[t] = store(v, wl.dtype)

@@ -74,14 +74,39 @@ def decode(a) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 
-def router_logits(x, Wr, expert_bias=None, noise=None) -> np.ndarray:
+LN_EPS = 1e-5
+
+
+def layer_norm(x: np.ndarray) -> np.ndarray:
+    """Row-wise (x - mean) / sqrt(var + 1e-5), var the biased (1/n) variance:
+    [P2] 5.2's nn.LayerNorm in front of the router, at its initial identity
+    scale and zero shift."""
+    mu = x.mean(axis=1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=1, keepdims=True)
+    return (x - mu) / np.sqrt(var + LN_EPS)
+
+
+def layer_norm_backward(x: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """Gradient with respect to x of <g, layer_norm(x)> (chain rule of the
+    row normalisation: r (g - mean(g) - n mean(g n)), n = layer_norm(x))."""
+    mu = x.mean(axis=1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=1, keepdims=True)
+    r = 1.0 / np.sqrt(var + LN_EPS)
+    n = (x - mu) * r
+    return r * (g - g.mean(axis=1, keepdims=True) - n * (g * n).mean(axis=1, keepdims=True))
+
+
+def router_logits(x, Wr, expert_bias=None, noise=None, layernorm: bool = False) -> np.ndarray:
     """l[t,e] = sum_i x[t,i] Wr[e,i] (+ bias[e]) (+ G[t,e]).
 
     [P1] 3.1: "logits = h W_r"; [P3] 2.3: Gumbel noise is added to the router
     score before top-k.  The per-expert bias is an explicit input (a workload
-    of skewed load)."""
+    of skewed load).  layernorm: the router sees layer_norm(x) ([P2] 5.2);
+    the experts still see x."""
     x = decode(x)
     Wr = decode(Wr)
+    if layernorm:
+        x = layer_norm(x)
     l = x @ Wr.T
     if expert_bias is not None:
         l = l + decode(expert_bias)[None, :]
@@ -286,7 +311,7 @@ def combine(expert_out: np.ndarray, w: np.ndarray, kept: np.ndarray, shared: Opt
 def route_and_dispatch(cfg: dict, x, Wr, expert_bias=None, noise=None) -> Dict[str, np.ndarray]:
     """Router, top-k, capacity and dispatch of the whole batch (no experts)."""
     T, E, k = cfg["T"], cfg["E"], cfg["k"]
-    l = router_logits(x, Wr, expert_bias, noise)
+    l = router_logits(x, Wr, expert_bias, noise, layernorm=cfg.get("layernorm", False))
     idx, w, finite = top_k_route(l, k, raw_probs=cfg.get("raw_probs", False))
     counts = usage_counts(idx, E)
     C = expert_capacity(T, k, E, cfg.get("capacity_factor", 0.0), cfg.get("min_capacity", 0))
@@ -486,8 +511,12 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
         for j in range(k):
             dl[t, idx[t, j]] += w[t, j] * (G[t, j] - s)
     Wr = decode(weights["Wr"])
-    grads["dWr"] = dl.T @ X
-    dX += dl @ Wr
+    if cfg.get("layernorm"):
+        grads["dWr"] = dl.T @ layer_norm(X)
+        dX += layer_norm_backward(X, dl @ Wr)
+    else:
+        grads["dWr"] = dl.T @ X
+        dX += dl @ Wr
     grads["dX"] = dX
     grads["dlogits"] = dl
     grads["y"] = y
@@ -563,12 +592,14 @@ def token_input_grads(cfg: dict, weights: dict, x, dY, route: dict, tokens) -> n
     _, dcv = importance_cv_grad(idx, w, E, T, cfg.get("lam", 0.01))
     G += dcv[toks]
     Wr = decode(weights["Wr"])
+    g = np.zeros_like(X)
     for i, t in enumerate(toks):
         if idx[t, 0] < 0:
             continue
         s = (w[t] * G[i]).sum()
         for j in range(k):
-            dX[i] += w[t, j] * (G[i, j] - s) * Wr[idx[t, j]]
+            g[i] += w[t, j] * (G[i, j] - s) * Wr[idx[t, j]]
+    dX += layer_norm_backward(X, g) if cfg.get("layernorm") else g
     return dX
 
 

@@ -19,7 +19,8 @@ moe_status validate(const moe_config* cfg) {
   if (cfg->min_capacity < 0 || !(cfg->capacity_factor == cfg->capacity_factor)) return MOE_ERR_INVALID_ARG;
   if (static_cast<long long>(cfg->T) * cfg->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
   if (cfg->dtype == MOE_BF16 && ((cfg->d % 8) || (cfg->h % 8))) return MOE_ERR_UNSUPPORTED;
-  if (cfg->route_flags & ~(MOE_ROUTE_RAW_PROBS | MOE_ROUTE_TOKEN_MAJOR)) return MOE_ERR_INVALID_ARG;
+  if (cfg->route_flags & ~(MOE_ROUTE_RAW_PROBS | MOE_ROUTE_TOKEN_MAJOR | MOE_ROUTE_LAYERNORM))
+    return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -38,11 +39,11 @@ size_t esize(const moe_config* cfg) { return cfg->dtype == MOE_BF16 ? 2 : 4; }
 // Workspace carving.  training 0/1 (forward): [header | dispatch scratch |
 // (inference) intermediates | shared hidden].  training 2 (backward):
 // [header | dYp | dAB | dXp | dot | dl | importance | coef | router partials
-// | shared dAB].
+// | shared dAB | LayerNorm terms].
 struct WsLayout {
   size_t dispatch_off, route_off, ent;
   size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs;
-  size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs;
+  size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs, lnc;
   size_t total;
 };
 
@@ -66,6 +67,7 @@ WsLayout layout(const moe_config* cfg, int training) {
     L.coef = take(E * 4);
     L.rpart = take(router_wgrad_partial_bytes(*cfg));
     L.dABs = cfg->has_shared ? take(T * hz * es) : 0;
+    L.lnc = (cfg->route_flags & MOE_ROUTE_LAYERNORM) ? take(3 * T * 4) : 0;
     L.total = o;
     return L;
   }
@@ -447,10 +449,11 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   // routing-weight gradients and the router
   s = launch_bwd_gather(*cfg, dY, S.Yp, S.pos, S.w, dYp, dot, st);
   if (s != MOE_OK) return s;
-  s = launch_router_bwd(*cfg, S.idx, S.w, dot, static_cast<unsigned long long*>(at(ws, L.imp)),
-                        static_cast<float*>(at(ws, L.coef)), dl, st);
+  float* lnc = (cfg->route_flags & MOE_ROUTE_LAYERNORM) ? static_cast<float*>(at(ws, L.lnc)) : nullptr;
+  s = launch_router_bwd(*cfg, x, wts->Wr, S.idx, S.w, dot, static_cast<unsigned long long*>(at(ws, L.imp)),
+                        static_cast<float*>(at(ws, L.coef)), dl, lnc, st);
   if (s != MOE_OK) return s;
-  s = launch_router_wgrad(*cfg, x, S.idx, dl, static_cast<float*>(at(ws, L.rpart)), g.dWr, st);
+  s = launch_router_wgrad(*cfg, x, S.idx, dl, lnc, static_cast<float*>(at(ws, L.rpart)), g.dWr, st);
   if (s != MOE_OK) return s;
   // routed experts
   s = run_ffn_bwd(cfg, a_rows, S.offsets, cfg->E, 0, dYp, S.Z, S.H, S.Xp, wts->W1, wts->W3, wts->W2, dAB, dXp, g.dW1,
@@ -462,7 +465,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
                     at(ws, L.dABs), g.dX, g.dWs1, g.dWs3, g.dWs2, g.dbs1, g.dbs2, err, st);
     if (s != MOE_OK) return s;
   }
-  return launch_bwd_dx(*cfg, dXp, S.pos, S.idx, dl, wts->Wr, cfg->has_shared ? 1 : 0, g.dX, st);
+  return launch_bwd_dx(*cfg, dXp, S.pos, S.idx, dl, wts->Wr, x, lnc, cfg->has_shared ? 1 : 0, g.dX, st);
 }
 
 moe_status moe_check_error(const void* ws, int* code_out, moe_stream_t stream) {

@@ -16,6 +16,15 @@
 //   dWr[e]  += dl[t,j] x[t];   dX[t] += dl[t,j] Wr[e]
 // Every reduction runs in a fixed order or in integers, so the results are
 // the same bits on every run.
+//
+// LayerNorm before the router ([P2] "Mixture of Experts Explained..." 5.2):
+// the router saw n_t = r_t (x_t - mu_t).  Then dWr[e] += dl[t,j] n_t, and
+// with g_t = sum_j dl[t,j] Wr[e_j] the input gradient is the normalisation's
+// backward r_t (g - mean(g) - n_t mean(g n_t)).  Writing dl' = r_t dl,
+// S_e = sum_i Wr[e,i], D_j = Wr[e_j] . (x_t - mu_t):
+//   dX[t] += sum_j dl'_j Wr[e_j] - A_t - B_t (x_t - mu_t),
+//   A_t = sum_j dl'_j S_{e_j} / d,  B_t = r_t^2 sum_j dl'_j D_j / d,
+//   dWr[e] += dl'[t,j] (x_t - mu_t).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -156,13 +165,97 @@ __global__ void router_bwd_kernel(const int* __restrict__ idx, const float* __re
     if (j < k) dl[static_cast<size_t>(t) * k + j] = routed ? wt[j] * (G[j] - s) : 0.f;
 }
 
+// LayerNorm before the router, one warp per token (after router_bwd_kernel):
+// mu_t, r_t from two passes over x_t (the second also takes D_j and S_j
+// against the k chosen router rows), then dl[t,:] *= r_t and
+// lnc = {mu[T], A[T], B[T]}.
+__global__ void ln_router_bwd_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr,
+                                     const int* __restrict__ idx, int T, int d, int k, int E, float* __restrict__ dl,
+                                     float* __restrict__ lnc) {
+  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const uint4* xv = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
+  const int nv = d >> 3;
+  float s = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 q = xv[i];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) s += bf16lo(u[c]) + bf16hi(u[c]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mu = s / static_cast<float>(d);
+  int e[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    e[j] = j < k ? idx[static_cast<size_t>(t) * k + j] : -1;
+    if (e[j] >= E) e[j] = -1;
+  }
+  float q2 = 0.f, D[8], Sj[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) D[j] = Sj[j] = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 q = xv[i];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    float xc[8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      xc[2 * c] = bf16lo(u[c]) - mu;
+      xc[2 * c + 1] = bf16hi(u[c]) - mu;
+      q2 = fmaf(xc[2 * c], xc[2 * c], fmaf(xc[2 * c + 1], xc[2 * c + 1], q2));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (e[j] < 0) continue;
+      const uint4 wq = reinterpret_cast<const uint4*>(Wr + static_cast<size_t>(e[j]) * d)[i];
+      const uint32_t wu[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float w0 = bf16lo(wu[c]), w1 = bf16hi(wu[c]);
+        D[j] = fmaf(w0, xc[2 * c], fmaf(w1, xc[2 * c + 1], D[j]));
+        Sj[j] += w0 + w1;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    q2 += __shfl_xor_sync(0xffffffffu, q2, o);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      D[j] += __shfl_xor_sync(0xffffffffu, D[j], o);
+      Sj[j] += __shfl_xor_sync(0xffffffffu, Sj[j], o);
+    }
+  }
+  if (lane != 0) return;
+  const float inv_d = 1.0f / static_cast<float>(d);
+  const float r = 1.0f / sqrtf(q2 * inv_d + 1e-5f);
+  float A = 0.f, B = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      const float g = r * dl[static_cast<size_t>(t) * k + j];
+      dl[static_cast<size_t>(t) * k + j] = g;
+      if (e[j] >= 0) {
+        A = fmaf(g, Sj[j], A);
+        B = fmaf(g, D[j], B);
+      }
+    }
+  }
+  lnc[t] = mu;
+  lnc[static_cast<size_t>(T) + t] = A * inv_d;
+  lnc[2 * static_cast<size_t>(T) + t] = B * r * r * inv_d;
+}
+
 constexpr int RW_TOK = 512;   // tokens per block of the router weight gradient
 constexpr int RW_EXP = 16;    // experts per block
 constexpr int RW_WARPS = 4;
 constexpr int RW_COLS = 256;  // columns per block: 8 per lane, one 16-byte load per token row
 
 // partial[chunk][e][c] = sum over the chunk's tokens (each warp takes every
-// RW_WARPS-th token, ascending) of sum_j [idx=e] dl[t,j] x[t][c].  A block
+// RW_WARPS-th token, ascending) of sum_j [idx=e] dl[t,j] (x[t][c] - mu[t])
+// (mu nullable: 0).  A block
 // covers 256 columns (a lane owns 8 consecutive ones: one 16-byte load of a
 // bf16 row) and 16 experts; every warp accumulates privately in shared
 // memory, laid out acc[warp][e][q][lane] (column lane*8+q) so that a warp's
@@ -170,7 +263,8 @@ constexpr int RW_COLS = 256;  // columns per block: 8 per lane, one 16-byte load
 template <typename Tx>
 __global__ void __launch_bounds__(RW_WARPS * 32)
 router_wgrad_partial_kernel(const Tx* __restrict__ x, const int* __restrict__ idx, const float* __restrict__ dl,
-                            int T, int d, int k, int E, float* __restrict__ partial) {
+                            int T, int d, int k, int E, const float* __restrict__ mu,
+                            float* __restrict__ partial) {
   extern __shared__ float acc_s[];  // [RW_WARPS][RW_EXP][8][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* acc = acc_s + warp * (RW_EXP * 8 * 32);
@@ -200,15 +294,32 @@ router_wgrad_partial_kernel(const Tx* __restrict__ x, const int* __restrict__ id
         for (int q = 0; q < 8; ++q)
           xv[u][q] = (t < t1 && c0 + q < d) ? x[static_cast<size_t>(t) * d + c0 + q] : 0.f;
       }
+      if (mu && t < t1) {
+        const float m = mu[t];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xv[u][q] -= m;
+      }
     }
+    // the slots' experts and logit gradients, loaded with the rows (lane j
+    // of the warp fetches slot j of each token and shares it)
+    int eu[U];
+    float gu[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int t = tb + u * RW_WARPS;
-      if (t >= t1) break;
+      eu[u] = -1;
+      gu[u] = 0.f;
+      if (t < t1 && lane < k) {
+        eu[u] = idx[static_cast<size_t>(t) * k + lane] - e0;
+        gu[u] = dl[static_cast<size_t>(t) * k + lane];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
       for (int j = 0; j < k; ++j) {
-        const int e = idx[static_cast<size_t>(t) * k + j] - e0;
+        const int e = __shfl_sync(0xffffffffu, eu[u], j);
+        const float g = __shfl_sync(0xffffffffu, gu[u], j);
         if (e >= 0 && e < RW_EXP && e0 + e < E) {
-          const float g = dl[static_cast<size_t>(t) * k + j];
           float* a = acc + e * 256 + lane;
 #pragma unroll
           for (int q = 0; q < 8; ++q) a[q * 32] = fmaf(g, xv[u][q], a[q * 32]);
@@ -239,11 +350,13 @@ __global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, in
   dWr[i] = s;
 }
 
-// One warp per token: dX[t] (+)= sum_{kept j} dXp[pos] + sum_j dl[t,j] Wr[idx_j] (fp32, j ascending).
+// One warp per token: dX[t] (+)= sum_{kept j} dXp[pos] + sum_j dl[t,j] Wr[idx_j] (fp32, j ascending)
+// (- A_t - B_t (x[t] - mu_t) with LayerNorm before the router: lnc non-null).
 template <typename Tw>
 __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restrict__ pos, const int* __restrict__ idx,
                               const float* __restrict__ dl, const Tw* __restrict__ Wr, int T, int k, int d, int E,
-                              int accumulate, float* __restrict__ dX) {
+                              const Tw* __restrict__ x, const float* __restrict__ lnc, int accumulate,
+                              float* __restrict__ dX) {
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -256,6 +369,12 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
     g[j] = j < k ? dl[static_cast<size_t>(t) * k + j] : 0.f;
   }
   float* out = dX + static_cast<size_t>(t) * d;
+  float lmu = 0.f, lA = 0.f, lB = 0.f;
+  if (lnc) {
+    lmu = lnc[t];
+    lA = lnc[static_cast<size_t>(T) + t];
+    lB = lnc[2 * static_cast<size_t>(T) + t];
+  }
 #pragma unroll 4
   for (int c = lane * 4; c < d; c += 128) {
     float4 a = accumulate ? *reinterpret_cast<const float4*>(out + c) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -291,6 +410,25 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
         a.w = fmaf(g[j], w3, a.w);
       }
     }
+    if (lnc) {
+      const Tw* xr = x + static_cast<size_t>(t) * d + c;
+      float x0, x1, x2, x3;
+      if constexpr (sizeof(Tw) == 2) {
+        x0 = __bfloat162float(xr[0]);
+        x1 = __bfloat162float(xr[1]);
+        x2 = __bfloat162float(xr[2]);
+        x3 = __bfloat162float(xr[3]);
+      } else {
+        x0 = xr[0];
+        x1 = xr[1];
+        x2 = xr[2];
+        x3 = xr[3];
+      }
+      a.x -= fmaf(lB, x0 - lmu, lA);
+      a.y -= fmaf(lB, x1 - lmu, lA);
+      a.z -= fmaf(lB, x2 - lmu, lA);
+      a.w -= fmaf(lB, x3 - lmu, lA);
+    }
     *reinterpret_cast<float4*>(out + c) = a;
   }
 }
@@ -324,8 +462,9 @@ moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* 
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status launch_router_bwd(const moe_config& cfg, const int* idx, const float* w, const float* dot,
-                             unsigned long long* imp, float* coef, float* dl, cudaStream_t st) {
+moe_status launch_router_bwd(const moe_config& cfg, const void* x, const void* Wr, const int* idx, const float* w,
+                             const float* dot, unsigned long long* imp, float* coef, float* dl, float* lnc,
+                             cudaStream_t st) {
   const long long nslots = static_cast<long long>(cfg.T) * cfg.k;
   long long blocks = (nslots + 255) / 256;
   if (blocks > 1184) blocks = 1184;
@@ -333,11 +472,16 @@ moe_status launch_router_bwd(const moe_config& cfg, const int* idx, const float*
                                                                                                     cfg.E, imp);
   balance_coef_kernel<<<1, 1024, 0, st>>>(imp, cfg.E, cfg.T, cfg.lambda_balance, coef);
   router_bwd_kernel<<<(cfg.T + 255) / 256, 256, 0, st>>>(idx, w, dot, coef, cfg.T, cfg.k, cfg.E, dl);
+  if (lnc) {
+    if (cfg.dtype != MOE_BF16 || (cfg.d % 8)) return MOE_ERR_UNSUPPORTED;
+    ln_router_bwd_kernel<<<warp_grid(cfg.T), 256, 0, st>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(Wr),
+                                                           idx, cfg.T, cfg.d, cfg.k, cfg.E, dl, lnc);
+  }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl, float* partial,
-                               float* dWr, cudaStream_t st) {
+moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl,
+                               const float* lnc, float* partial, float* dWr, cudaStream_t st) {
   const int nchunks = (cfg.T + RW_TOK - 1) / RW_TOK;
   dim3 grid(nchunks, (cfg.d + RW_COLS - 1) / RW_COLS, (cfg.E + RW_EXP - 1) / RW_EXP);
   const size_t smem = sizeof(float) * RW_WARPS * RW_EXP * 8 * 32;
@@ -354,23 +498,25 @@ moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* 
   }
   if (cfg.dtype == MOE_BF16)
     router_wgrad_partial_kernel<bf16><<<grid, RW_WARPS * 32, smem, st>>>(static_cast<const bf16*>(x), idx, dl, cfg.T,
-                                                                         cfg.d, cfg.k, cfg.E, partial);
+                                                                         cfg.d, cfg.k, cfg.E, lnc, partial);
   else
     router_wgrad_partial_kernel<float><<<grid, RW_WARPS * 32, smem, st>>>(static_cast<const float*>(x), idx, dl,
-                                                                          cfg.T, cfg.d, cfg.k, cfg.E, partial);
+                                                                          cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
   const long long Ed = static_cast<long long>(cfg.E) * cfg.d;
   router_wgrad_reduce_kernel<<<static_cast<unsigned>((Ed + 255) / 256), 256, 0, st>>>(partial, nchunks, Ed, dWr);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,
-                         const void* Wr, int accumulate, float* dX, cudaStream_t st) {
+                         const void* Wr, const void* x, const float* lnc, int accumulate, float* dX, cudaStream_t st) {
   if (cfg.dtype == MOE_BF16)
     bwd_dx_kernel<bf16><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, static_cast<const bf16*>(Wr), cfg.T,
-                                                          cfg.k, cfg.d, cfg.E, accumulate, dX);
+                                                          cfg.k, cfg.d, cfg.E, static_cast<const bf16*>(x), lnc,
+                                                          accumulate, dX);
   else
     bwd_dx_kernel<float><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, static_cast<const float*>(Wr), cfg.T,
-                                                           cfg.k, cfg.d, cfg.E, accumulate, dX);
+                                                           cfg.k, cfg.d, cfg.E, static_cast<const float*>(x), lnc,
+                                                           accumulate, dX);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

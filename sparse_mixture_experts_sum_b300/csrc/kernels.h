@@ -106,13 +106,17 @@ moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos,
 size_t router_wgrad_partial_bytes(const moe_config& cfg);
 moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* Yp, const int* pos, const float* w,
                              void* dYp, float* dot, cudaStream_t st);
-// imp (E words of 8 bytes) must be zero on entry.
-moe_status launch_router_bwd(const moe_config& cfg, const int* idx, const float* w, const float* dot,
-                             unsigned long long* imp, float* coef, float* dl, cudaStream_t st);
-moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl, float* partial,
-                               float* dWr, cudaStream_t st);
+// imp (E words of 8 bytes) must be zero on entry.  With LayerNorm before
+// the router (lnc = 3T floats: mu, A, B per token, else nullptr) dl leaves
+// scaled by each token's 1/sqrt(var + eps) and lnc holds the per-token terms
+// of the normalisation's backward.
+moe_status launch_router_bwd(const moe_config& cfg, const void* x, const void* Wr, const int* idx, const float* w,
+                             const float* dot, unsigned long long* imp, float* coef, float* dl, float* lnc,
+                             cudaStream_t st);
+moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl,
+                               const float* lnc, float* partial, float* dWr, cudaStream_t st);
 moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,
-                         const void* Wr, int accumulate, float* dX, cudaStream_t st);
+                         const void* Wr, const void* x, const float* lnc, int accumulate, float* dX, cudaStream_t st);
 moe_status launch_group_colsum(const void* src, long long ld, const int* offsets, int G, int rows, int N, float* out,
                                cudaStream_t st);
 

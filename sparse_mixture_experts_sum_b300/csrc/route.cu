@@ -11,15 +11,23 @@
 // (Gumbel noise added to the router score before top-k).  Selecting on the
 // logits equals selecting on softmax(l), which is monotone.
 //
-// bf16 with E a multiple of 8 (and workspace given): the logits x . Wr^T
-// run on the tcgen05 grouped GEMM (one group of T rows, N = E, fp32 out into
-// the workspace; x streams from HBM through TMA), then route_topk_kernel
-// takes each token's top-k with one warp.  Otherwise a CTA owns 64 tokens;
-// 4 warps compute the 64 x 128 logit block of an expert chunk with
-// mma.sync m16n8k16 (fp32 accumulate) from a 3- to 5-stage cp.async ring of
-// x and Wr tiles, then 64 threads merge the chunk into each token's running
-// top-k.
+// bf16 with a workspace: the logits x . Wr^T run on the tcgen05 grouped
+// GEMM (one group of T rows, N = E rounded up to 8 with zero rows past E,
+// fp32 out into the workspace; x streams from HBM through TMA), then
+// route_topk_kernel takes each token's top-k with one warp.  bf16 without a
+// workspace: a CTA owns 64 tokens; 4 warps compute the 64 x 128 logit block
+// of an expert chunk with mma.sync m16n8k16 (fp32 accumulate) from a 3- to
+// 5-stage cp.async ring of x and Wr tiles, then 64 threads merge the chunk
+// into each token's running top-k.
 // fp32: one warp per token on the CUDA cores (tiny workloads).
+//
+// LayerNorm before the router ([P2] "Mixture of Experts Explained..." 5.2:
+// a LayerNorm, then the linear router; identity scale and zero shift, eps
+// 1e-5, biased variance).  With mu_t, r_t = 1/sqrt(var_t + eps) of row t
+// and S_e = sum_i Wr[e,i]:
+//   LN(x_t) . Wr[e] = r_t (x_t . Wr[e] - mu_t S_e),
+// so the GEMM still contracts the stored x and the top-k kernel applies the
+// row statistics (two passes over x_t in fp32) and S (one warp per expert).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -117,6 +125,76 @@ __device__ __forceinline__ void topk_finish(const float (&v)[MAXK], const int (&
     }
   }
   if (ent) ent[t] = st.entropy();
+}
+
+constexpr float kLnEps = 1e-5f;
+
+// mean and 1/sqrt(biased variance + eps) of a bf16 row of d (a multiple of 8)
+// elements, one warp, two passes (the second centred on the mean).
+__device__ __forceinline__ void row_stats_bf16(const bf16* __restrict__ row, int d, float& mu, float& r) {
+  const uint4* v = reinterpret_cast<const uint4*>(row);
+  const int nv = d >> 3;
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 q = v[i];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) s += bf16lo(u[c]) + bf16hi(u[c]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  mu = s / static_cast<float>(d);
+  float q2 = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 q = v[i];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float a = bf16lo(u[c]) - mu, b = bf16hi(u[c]) - mu;
+      q2 = fmaf(a, a, fmaf(b, b, q2));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, o);
+  r = 1.0f / sqrtf(q2 / static_cast<float>(d) + kLnEps);
+}
+
+__device__ __forceinline__ void row_stats_f32(const float* __restrict__ row, int d, float& mu, float& r) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+  for (int i = lane; i < d; i += 32) s += row[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  mu = s / static_cast<float>(d);
+  float q2 = 0.f;
+  for (int i = lane; i < d; i += 32) {
+    const float a = row[i] - mu;
+    q2 = fmaf(a, a, q2);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, o);
+  r = 1.0f / sqrtf(q2 / static_cast<float>(d) + kLnEps);
+}
+
+// S[e] = sum_i Wr[e,i] (fp32), one warp per expert; S[e] = 0 for E <= e < ld.
+__global__ void weight_row_sum_kernel(const bf16* __restrict__ Wr, int E, int d, int ld, float* __restrict__ S) {
+  const int e = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (e >= ld) return;
+  float s = 0.f;
+  if (e < E) {
+    const uint4* v = reinterpret_cast<const uint4*>(Wr + static_cast<size_t>(e) * d);
+    for (int i = lane; i < (d >> 3); i += 32) {
+      const uint4 q = v[i];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s += bf16lo(u[c]) + bf16hi(u[c]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  }
+  if (lane == 0) S[e] = s;
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -304,15 +382,19 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
     if (hist[e]) atomicAdd(&counts[e], hist[e]);
 }
 
-// Top-k of precomputed logits, one warp per token: l[t,e] = logits[t,e]
-// (+ bias[e]) (+ noise[t,e]); each lane keeps the top-k of its experts
-// (e = lane, lane+32, ... in increasing order), then k rounds of a warp
-// argmax by (value desc, index asc) merge the lanes' lists.  Lane 0 writes
-// idx, the renormalised weights and the block histogram.
+// Top-k of precomputed logits (row stride ld), one warp per token:
+// l[t,e] = logits[t,e] (+ bias[e]) (+ noise[t,e]); with S (LayerNorm before
+// the router) the stored value is x_t . Wr[e] and l[t,e] = r_t (logits[t,e]
+// - mu_t S[e]) (+ ...), mu_t and r_t from the row x_t.  Each lane keeps the
+// top-k of its experts (e = lane, lane+32, ... in increasing order), then k
+// rounds of a warp argmax by (value desc, index asc) merge the lanes'
+// lists.  Lane 0 writes idx, the renormalised weights and the block
+// histogram.
 __global__ void __launch_bounds__(256)
-route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ ebias, const float* __restrict__ noise,
-                  int T, int E, int k, int* __restrict__ idx, float* __restrict__ w, int* __restrict__ counts,
-                  int raw, float* __restrict__ ent) {
+route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ ebias,
+                  const float* __restrict__ noise, int T, int E, int k, int* __restrict__ idx, float* __restrict__ w,
+                  int* __restrict__ counts, int raw, float* __restrict__ ent, const bf16* __restrict__ x, int d,
+                  const float* __restrict__ S) {
   extern __shared__ int hist_s[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
   __syncthreads();
@@ -329,10 +411,13 @@ route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ eb
     bool finite = true;
     const bool need_stat = raw || ent;
     SoftStat sst;
-    const float* lr = logits + static_cast<size_t>(t) * E;
+    float mu = 0.f, r = 1.f;
+    if (S) row_stats_bf16(x + static_cast<size_t>(t) * d, d, mu, r);
+    const float* lr = logits + static_cast<size_t>(t) * ld;
     const float* nr = noise ? noise + static_cast<size_t>(t) * E : nullptr;
     for (int e = lane; e < E; e += 32) {
       float v = lr[e];
+      if (S) v = r * fmaf(-mu, S[e], v);
       if (ebias) v += ebias[e];
       if (nr) v += nr[e];
       if (!isfinite(v)) finite = false;
@@ -389,7 +474,7 @@ route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ eb
 __global__ void route_f32_kernel(const float* __restrict__ x, const float* __restrict__ Wr,
                                  const float* __restrict__ ebias, const float* __restrict__ noise, int T, int d,
                                  int E, int k, int* __restrict__ idx, float* __restrict__ w,
-                                 int* __restrict__ counts, int raw, float* __restrict__ ent) {
+                                 int* __restrict__ counts, int raw, float* __restrict__ ent, int layernorm) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -405,12 +490,15 @@ __global__ void route_f32_kernel(const float* __restrict__ x, const float* __res
   const bool need_stat = raw || ent;
   SoftStat sst;
   const float* xr = x + static_cast<size_t>(t) * d;
+  float mu = 0.f, r = 1.f;
+  if (layernorm) row_stats_f32(xr, d, mu, r);
   for (int e = 0; e < E; ++e) {
     const float* wr = Wr + static_cast<size_t>(e) * d;
     float s = 0.f;
-    for (int i = lane; i < d; i += 32) s = fmaf(xr[i], wr[i], s);
+    for (int i = lane; i < d; i += 32) s = fmaf(xr[i] - mu, wr[i], s);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (layernorm) s *= r;
     if (ebias) s += ebias[e];
     if (noise) s += noise[static_cast<size_t>(t) * E + e];
     if (!isfinite(s)) finite = false;
@@ -446,40 +534,54 @@ moe_status launch_route_stages(const moe_config& cfg, const void* x, const void*
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// bf16 logits on the tensor cores need E a multiple of 8 (a TMA and
-// epilogue granule) and scratch for the fp32 logits.
-bool route_on_tensor_cores(const moe_config& cfg) { return cfg.dtype == MOE_BF16 && cfg.E % 8 == 0; }
+// Row stride of the fp32 logits on the tensor-core path: E rounded up to
+// the GEMM's 8-column granule (columns past E hold the logits of zero
+// weight rows and are never read).
+int logit_ld(const moe_config& cfg) { return cfg.E < 8 ? 8 : (cfg.E + 7) / 8 * 8; }
 
 }  // namespace
 
 size_t route_scratch_bytes(const moe_config& cfg) {
-  return route_on_tensor_cores(cfg) ? static_cast<size_t>(cfg.T) * cfg.E * sizeof(float) : 0;
+  if (cfg.dtype != MOE_BF16) return 0;
+  const size_t ld = logit_ld(cfg);
+  const bool ln = (cfg.route_flags & MOE_ROUTE_LAYERNORM) != 0;
+  return (static_cast<size_t>(cfg.T) + (ln ? 1 : 0)) * ld * sizeof(float);
 }
 
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
                         const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* err,
                         cudaStream_t stream) {
   const int raw = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0;
+  const bool ln = (cfg.route_flags & MOE_ROUTE_LAYERNORM) != 0;
+  if (ln && cfg.dtype == MOE_BF16 && !scratch) return MOE_ERR_UNSUPPORTED;  // the fold needs the workspace path
   moe_status zs = launch_zero(counts, sizeof(int) * cfg.E, err, err ? sizeof(int) : 0, stream);
   if (zs != MOE_OK) return zs;
-  if (route_on_tensor_cores(cfg) && scratch) {
+  if (cfg.dtype == MOE_BF16 && scratch) {
     // logits = x . Wr^T on the tcgen05 grouped GEMM (one group of T rows,
-    // N = E, fp32 out), then the top-k per token
+    // N = E rounded up to 8, fp32 out; the TMA box reads zeros past row E),
+    // then the top-k per token
+    const int ld = logit_ld(cfg);
+    float* logits = static_cast<float*>(scratch);
+    float* S = ln ? logits + static_cast<size_t>(cfg.T) * ld : nullptr;
+    if (ln) {
+      weight_row_sum_kernel<<<static_cast<unsigned>((ld * 32 + 255) / 256), 256, 0, stream>>>(
+          static_cast<const bf16*>(Wr), cfg.E, cfg.d, ld, S);
+    }
     GemmParams g{};
     g.G = 1;
     g.rows = cfg.T;
-    g.N = cfg.E;
+    g.N = ld;
     g.K = cfg.d;
     g.mode = kModePlain;
     g.out_f32 = 1;
-    g.out = scratch;
+    g.out = logits;
     g.err = err;
     moe_status s = launch_grouped_gemm_tc(g, kKindFwd, x, cfg.T, Wr, nullptr, cfg.E, stream);
     if (s != MOE_OK) return s;
     const unsigned grid = static_cast<unsigned>((static_cast<long long>(cfg.T) * 32 + 255) / 256);
-    route_topk_kernel<<<grid, 256, sizeof(int) * cfg.E, stream>>>(static_cast<const float*>(scratch), expert_bias,
-                                                                   noise, cfg.T, cfg.E, cfg.k, idx, w, counts, raw,
-                                                                   ent);
+    route_topk_kernel<<<grid, 256, sizeof(int) * cfg.E, stream>>>(logits, ld, expert_bias, noise, cfg.T, cfg.E,
+                                                                   cfg.k, idx, w, counts, raw, ent,
+                                                                   static_cast<const bf16*>(x), cfg.d, S);
   } else if (cfg.dtype == MOE_BF16) {
     const int nep = ((cfg.E < RT_NE ? cfg.E : RT_NE) + 7) / 8 * 8;
     return nep <= 64 ? launch_route_stages<5>(cfg, x, Wr, expert_bias, noise, idx, w, counts, ent, stream)
@@ -489,7 +591,7 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     const long long grid = (static_cast<long long>(cfg.T) * 32 + threads - 1) / threads;
     route_f32_kernel<<<static_cast<unsigned>(grid), threads, 0, stream>>>(
         static_cast<const float*>(x), static_cast<const float*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E,
-        cfg.k, idx, w, counts, raw, ent);
+        cfg.k, idx, w, counts, raw, ent, ln ? 1 : 0);
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

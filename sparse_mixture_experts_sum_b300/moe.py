@@ -116,20 +116,23 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-ROUTE_RAW_PROBS, ROUTE_TOKEN_MAJOR = 1, 2
+ROUTE_RAW_PROBS, ROUTE_TOKEN_MAJOR, ROUTE_LAYERNORM = 1, 2, 4
 
 
 def make_config(T, d, h, E, k, act="swiglu", dtype="bf16", capacity_factor=0.0, min_capacity=0,
-                lambda_balance=0.01, has_shared=False, raw_probs=False, token_major=False) -> MoeConfig:
-    flags = (ROUTE_RAW_PROBS if raw_probs else 0) | (ROUTE_TOKEN_MAJOR if token_major else 0)
+                lambda_balance=0.01, has_shared=False, raw_probs=False, token_major=False,
+                layernorm=False) -> MoeConfig:
+    flags = ((ROUTE_RAW_PROBS if raw_probs else 0) | (ROUTE_TOKEN_MAJOR if token_major else 0)
+             | (ROUTE_LAYERNORM if layernorm else 0))
     return MoeConfig(T, d, h, E, k, ACT[act], DTYPE[dtype], capacity_factor, min_capacity,
                      lambda_balance, int(bool(has_shared)), flags)
 
 
-def config_of(wl) -> MoeConfig:
-    """MoeConfig of a moe_synth.Workload."""
+def config_of(wl, **route) -> MoeConfig:
+    """MoeConfig of a moe_synth.Workload (route: raw_probs, token_major,
+    layernorm flags)."""
     return make_config(wl.T, wl.d, wl.h, wl.E, wl.k, wl.act, wl.dtype, wl.capacity_factor,
-                       wl.min_capacity, wl.lam, wl.has_shared)
+                       wl.min_capacity, wl.lam, wl.has_shared, **route)
 
 
 def moe_capacity(cfg: MoeConfig) -> int:

@@ -12,12 +12,13 @@ from oracle import moe_oracle as O
 MARGIN = 1e-3
 
 
-def oracle_cfg(wl) -> dict:
+def oracle_cfg(wl, **route) -> dict:
     # the C ABI carries lambda and the capacity factor as fp32 values; the
-    # oracle gets those same values
+    # oracle gets those same values; route: raw_probs, token_major, layernorm
     return dict(T=wl.T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act,
                 capacity_factor=float(np.float32(wl.capacity_factor)),
-                min_capacity=wl.min_capacity, lam=float(np.float32(wl.lam)), has_shared=wl.has_shared)
+                min_capacity=wl.min_capacity, lam=float(np.float32(wl.lam)), has_shared=wl.has_shared,
+                **route)
 
 
 def small_gaps(l: np.ndarray, k: int, margin: float = MARGIN) -> np.ndarray:
@@ -29,11 +30,12 @@ def small_gaps(l: np.ndarray, k: int, margin: float = MARGIN) -> np.ndarray:
     return np.nonzero((gaps < margin).any(axis=1))[0]
 
 
-def guard(wl, t: dict, max_attempts=50) -> dict:
+def guard(wl, t: dict, max_attempts=50, layernorm=False) -> dict:
     """Redraw (in place) every row of t['x'] whose top-k margins are below
-    1e-3, from counter attempt a = 1, 2, ..., until none is left."""
+    1e-3, from counter attempt a = 1, 2, ..., until none is left (margins of
+    the router that sees LayerNorm(x) when layernorm)."""
     for a in range(1, max_attempts + 1):
-        l = O.router_logits(t["x"], t["Wr"], t.get("expert_bias"), t.get("noise"))
+        l = O.router_logits(t["x"], t["Wr"], t.get("expert_bias"), t.get("noise"), layernorm=layernorm)
         bad = small_gaps(l, wl.k)
         if bad.size == 0:
             return t
@@ -41,9 +43,9 @@ def guard(wl, t: dict, max_attempts=50) -> dict:
     raise RuntimeError("margin guard did not converge")
 
 
-def guarded_inputs(wl, device="cpu", parts=None):
+def guarded_inputs(wl, device="cpu", parts=None, layernorm=False):
     """Inputs of workload `wl` with every token's top-k margin >= 1e-3."""
-    return guard(wl, S.make_inputs(wl, device, parts))
+    return guard(wl, S.make_inputs(wl, device, parts), layernorm=layernorm)
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
@@ -62,6 +64,21 @@ def max_abs(a: np.ndarray, b: np.ndarray) -> float:
 def assert_close_bf16(got: np.ndarray, ref: np.ndarray, what: str, rel=1e-2, mabs=2e-2):
     rf, ma = rel_frob(got, ref), max_abs(got, ref)
     assert rf <= rel and ma <= mabs, f"{what}: rel-Frobenius {rf:.3e} (<= {rel}), max-abs {ma:.3e} (<= {mabs})"
+
+
+def assert_close_bf16_scaled(got: np.ndarray, ref: np.ndarray, what: str, rel=1e-2, frac=3e-2):
+    """assert_close_bf16 for rows of any scale: relative-Frobenius <= rel and
+    |err| <= frac * max(1, RMS of the element's reference row, |ref|).  The
+    bf16 stores of a row (its hidden units, expert outputs and the output
+    itself) err by a fixed fraction of the row's scale (sums of products)
+    and of the element (the final rounding: half an ulp, up to 2^-8 of
+    |ref|).  A fp64 model of those stores on rows with offsets up to +-2 and
+    scales up to 3 reaches 1.3e-2 of that scale, so 3e-2 leaves over 2x."""
+    rf = rel_frob(got, ref)
+    rms = np.sqrt(np.mean(ref ** 2, axis=-1, keepdims=True))
+    scale = np.maximum(np.maximum(1.0, rms), np.abs(ref))
+    worst = float((np.abs(got - ref) / scale).max()) if ref.size else 0.0
+    assert rf <= rel and worst <= frac, f"{what}: rel-Frobenius {rf:.3e} (<= {rel}), max |err|/scale {worst:.3e} (<= {frac})"
 
 
 def round_bf16(a: np.ndarray) -> np.ndarray:

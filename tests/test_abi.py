@@ -81,7 +81,7 @@ def test_capacity_matches_oracle(M, T, k, E, cf, minc):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(k=5, E=4), 1), (dict(k=9, E=16), 1), (dict(E=1025), 1), (dict(T=0), 1),
-    (dict(d=100), 2), (dict(h=36), 2), (dict(act=7), 1), (dict(route_flags=4), 1)])
+    (dict(d=100), 2), (dict(h=36), 2), (dict(act=7), 1), (dict(route_flags=8), 1)])
 def test_bad_configs_rejected(M, kw, status):
     base = dict(T=64, d=64, h=64, E=8, k=2)
     base.update({k: v for k, v in kw.items() if k in base})

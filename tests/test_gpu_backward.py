@@ -2,7 +2,14 @@
 fp64 oracle's gradients of L = <dY, y> + lambda * CV(I/T).
 
 Tolerances (bf16 storage, fp32 accumulation): dX within relative-Frobenius
-1e-2 and max-abs 2e-2; weight gradients within relative-Frobenius 1e-2 and,
+1e-2 and, token by token, max-abs 5e-2 * max(1, RMS of the token's
+reference row).  Two stores set that error: each element sums 2h products
+of a bf16-stored dA/dB with a weight (a fixed fraction, ~2e-3 std, of the
+row's own scale), and the logit gradient dl takes <dY, Yp> from the
+bf16-stored expert outputs, which the router term dl . Wr carries into the
+row.  Reproducing both stores in fp64 on rows of varying offset and scale
+(the LayerNorm-router test) gives up to 2.3e-2 of the row RMS, so the
+bound leaves about 2x; weight gradients within relative-Frobenius 1e-2 and,
 entry by entry, |err| <= 5e-2 * max(RMS, |ref|) with RMS that of the
 expert's (or tensor's) reference gradient.  Each weight-gradient entry sums,
 over the expert's rows, products whose factors went through up to three
@@ -38,8 +45,8 @@ def assert_grad_close(got, ref, what, rel=1e-2, rms_frac=5e-2):
         f"{what}: rel-Frobenius {rf:.3e} (<= {rel}), max |err|/max(rms,|ref|) {scaled:.3e} (<= {rms_frac})"
 
 
-def run_fwd_bwd(wl, t, dY):
-    cfg = M.config_of(wl)
+def run_fwd_bwd(wl, t, dY, **route):
+    cfg = M.config_of(wl, **route)
     weights = {n: t.get(n) for n in WEIGHT_NAMES}
     sv = M.moe.alloc_saved(cfg, DEV, backward=True)
     y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=DEV)
@@ -56,9 +63,9 @@ def run_fwd_bwd(wl, t, dY):
     return y, sv, g
 
 
-def oracle_backward(wl, t, dY):
+def oracle_backward(wl, t, dY, **route):
     w = {n: t[n] for n in WEIGHT_NAMES if t.get(n) is not None and n != "expert_bias"}
-    return O.layer_backward(oracle_cfg(wl), w, t["x"], dY, t.get("expert_bias"), t.get("noise"))
+    return O.layer_backward(oracle_cfg(wl, **route), w, t["x"], dY, t.get("expert_bias"), t.get("noise"))
 
 
 PER_EXPERT = ("dW1", "dW3", "dW2", "db1", "db2")
@@ -66,8 +73,12 @@ PER_EXPERT = ("dW1", "dW3", "dW2", "db1", "db2")
 
 def check_all(wl, t, dY, g, ref):
     dX = g["dX"].cpu().numpy().astype(np.float64)
-    rf, ma = rel_frob(dX, ref["dX"]), max_abs(dX, ref["dX"])
-    assert rf <= 1e-2 and ma <= 2e-2, f"dX: rel-Frobenius {rf:.3e}, max-abs {ma:.3e}"
+    rf = rel_frob(dX, ref["dX"])
+    row_rms = np.sqrt(np.mean(ref["dX"] ** 2, axis=1))
+    row_err = np.abs(dX - ref["dX"]).max(axis=1)
+    worst = int(np.argmax(row_err / np.maximum(1.0, row_rms)))
+    assert rf <= 1e-2 and row_err[worst] <= 5e-2 * max(1.0, row_rms[worst]), \
+        f"dX: rel-Frobenius {rf:.3e}; token {worst}: max-abs {row_err[worst]:.3e}, row RMS {row_rms[worst]:.3e}"
     for name in ("dWr", "dW1", "dW3", "dW2", "db1", "db2", "dWs1", "dWs3", "dWs2", "dbs1", "dbs2"):
         if name not in g:
             continue
@@ -141,6 +152,27 @@ def test_backward_ragged_and_empty_experts():
         for name in ("dW1", "dW3", "dW2"):
             assert (g[name][e] == 0).all(), (name, e)
     check_all(wl, t, dY, g, ref)
+
+
+@pytest.mark.parametrize("shared,cf", [(False, 0.0), (True, 1.0)])
+def test_backward_with_router_layernorm(shared, cf):
+    """LayerNorm in front of the router ([P2] 5.2) on rows of varying offset
+    and scale: dWr is the logit gradient against the normalised rows, and dX
+    carries the normalisation's backward (its mean and projection terms)."""
+    wl = _workload(has_shared=shared, gumbel=True, capacity_factor=cf, x_affine=True, seed=67)
+    t = guarded_inputs(wl, "cpu", layernorm=True)
+    dY = t.pop("dY")
+    td = {n: v.to(DEV) for n, v in t.items()}
+    _, sv, g = run_fwd_bwd(wl, td, dY.to(DEV), layernorm=True)
+    ref = oracle_backward(wl, t, dY, layernorm=True)
+    np.testing.assert_array_equal(sv["idx"].cpu().numpy(), ref["route"]["idx"])
+    np.testing.assert_array_equal(sv["pos"].cpu().numpy(), ref["route"]["pos"])
+    check_all(wl, t, dY, g, ref)
+    # the normalisation matters on these rows: the router gradient without
+    # it is a different tensor
+    plain = O.layer_backward(oracle_cfg(wl), {n: t[n] for n in WEIGHT_NAMES if t.get(n) is not None},
+                             t["x"], dY, None, t.get("noise"))
+    assert rel_frob(plain["dWr"], ref["dWr"]) > 0.1
 
 
 def test_backward_is_deterministic():

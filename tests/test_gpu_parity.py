@@ -14,7 +14,7 @@ import torch
 
 import moe_synth as S
 import sparse_mixture_experts_sum_b300 as M
-from moe_testlib import assert_close_bf16, guard, guarded_inputs, max_abs, oracle_cfg, to_np
+from moe_testlib import assert_close_bf16, assert_close_bf16_scaled, guard, guarded_inputs, max_abs, oracle_cfg, to_np
 from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -384,11 +384,11 @@ def test_expert_ffn_shared_matches_oracle(act):
 
 
 @pytest.mark.parametrize("T,d,E,k", [(64, 4096, 128, 2), (200, 1024, 130, 4), (1000, 512, 384, 6),
-                                     (4500, 1024, 64, 2)])
+                                     (4500, 1024, 64, 2), (300, 256, 5, 3)])
 def test_route_with_workspace(T, d, E, k):
-    """With a workspace and E a multiple of 8 the logits run on the tcgen05
-    GEMM and a warp per token takes the top-k (E = 130 keeps the mma.sync
-    kernel): same routing as the oracle, and the same bits on a second run."""
+    """With a workspace the logits run on the tcgen05 GEMM (E = 130 and 5
+    pad the logit rows to 136 and 8 columns) and a warp per token takes the
+    top-k: same routing as the oracle, and the same bits on a second run."""
     wl = S.WORKLOADS["small_prefill"].replace(T=T, d=d, E=E, k=k, seed=19)
     t = guarded_inputs(wl, "cpu", parts=["x", "Wr"])
     cfg = M.config_of(wl)
@@ -443,4 +443,41 @@ def test_routing_variants(raw, tm, E):
         g = M.moe.alloc_grads(cfg)
         with pytest.raises(M.moe.MoeError) as ei:
             M.moe_layer_bwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], sv, y, g, M.moe.workspace(cfg, 2))
+        assert ei.value.status == M.moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("E,dtype", [(16, "bf16"), (12, "bf16"), (4, "f32")])
+def test_layernorm_router(E, dtype):
+    """LayerNorm in front of the router ([P2] 5.2) on rows of varying offset
+    and scale: routing, statistics and output match the oracle's; the plain
+    router would route these rows differently.  bf16 folds the row
+    statistics into the tcgen05 logits (E = 12 pads them to 16); fp32
+    normalises on the CUDA cores; bf16 moe_route without a workspace
+    refuses the flag."""
+    if dtype == "f32":
+        wl = S.WORKLOADS["tiny_fp32"].replace(T=300, E=E, capacity_factor=1.0, x_affine=True, seed=29)
+    else:
+        wl = S.WORKLOADS["small_prefill"].replace(T=700, d=256, h=256, E=E, capacity_factor=1.0,
+                                                  x_affine=True, seed=29)
+    t = guarded_inputs(wl, DEV, layernorm=True)
+    cfg = M.config_of(wl, layernorm=True)
+    sv = M.moe.alloc_saved(cfg)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    y = torch.empty(wl.T, wl.d, dtype=tdt, device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg, 1)
+    M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], None, y, sv, st, ws)
+    assert M.moe_check_error(ws) == 0
+    ocfg = oracle_cfg(wl, layernorm=True)
+    r = O.layer_forward(ocfg, oracle_weights(t), t["x"])
+    check_routing(r, sv, M.moe.read_stats(st), t["x"])
+    assert_close_bf16_scaled(to_np(y), r["y"], "y")
+    plain = O.route_and_dispatch(oracle_cfg(wl), t["x"], t["Wr"])
+    assert (plain["idx"] != r["idx"]).any()
+    if dtype == "bf16":
+        idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device=DEV)
+        w = torch.empty(wl.T, wl.k, device=DEV)
+        counts = torch.empty(wl.E, dtype=torch.int32, device=DEV)
+        with pytest.raises(M.moe.MoeError) as ei:
+            M.moe_route(cfg, t["x"], t["Wr"], None, None, idx, w, counts)
         assert ei.value.status == M.moe.MOE_ERR_UNSUPPORTED

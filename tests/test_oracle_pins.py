@@ -541,3 +541,71 @@ def test_token_major_capacity(T, E, k, cf):
     # the two priority orders differ once capacity binds on second choices
     rank_s, _ = O.assign_capacity(idx, E, C)
     assert (rank_s != rank).any()
+
+
+def test_layer_norm_against_torch_and_backward_by_finite_differences():
+    """[P2] 5.2's LayerNorm before the router: layer_norm equals torch's
+    F.layer_norm (no affine, eps 1e-5); layer_norm_backward equals central
+    differences of <g, layer_norm(x)>."""
+    rng = _rng(81)
+    x = rng.normal(size=(6, 11)) * 3 + 5.5
+    ref = torch.nn.functional.layer_norm(torch.tensor(x), (11,), eps=1e-5).numpy()
+    np.testing.assert_allclose(O.layer_norm(x), ref, rtol=1e-12, atol=1e-12)
+    g = rng.normal(size=x.shape)
+    an = O.layer_norm_backward(x, g)
+    h = 1e-6
+    num = np.zeros_like(x)
+    for i in range(x.shape[0]):
+        for j in range(x.shape[1]):
+            xp, xm = x.copy(), x.copy()
+            xp[i, j] += h
+            xm[i, j] -= h
+            num[i, j] = ((g * O.layer_norm(xp)).sum() - (g * O.layer_norm(xm)).sum()) / (2 * h)
+    np.testing.assert_allclose(an, num, rtol=1e-6, atol=1e-8)
+
+
+def test_backward_with_router_layernorm_finite_differences():
+    """The layer's gradients with the router's LayerNorm against central
+    differences of L (routing fixed, away from ties)."""
+    rng = _rng(83)
+    T, d, h, E, k = 12, 5, 6, 4, 2
+    w = dict(Wr=rng.normal(size=(E, d)), W1=rng.normal(size=(E, h, d)) / 2, W3=rng.normal(size=(E, h, d)) / 2,
+             W2=rng.normal(size=(E, d, h)) / 3)
+    cfg = dict(T=T, d=d, h=h, E=E, k=k, act="swiglu", capacity_factor=0.0, lam=0.05, layernorm=True)
+    x = rng.normal(size=(T, d)) + 2.0
+    dY = rng.normal(size=(T, d))
+    g = O.layer_backward(cfg, w, x, dY)
+
+    def loss(xx, ww):
+        return O.layer_backward(cfg, ww, xx, dY)["loss"]
+
+    hh = 1e-6
+    for (t, i) in [(0, 0), (3, 2), (11, 4)]:
+        xp, xm = x.copy(), x.copy()
+        xp[t, i] += hh
+        xm[t, i] -= hh
+        num = (loss(xp, w) - loss(xm, w)) / (2 * hh)
+        assert abs(num - g["dX"][t, i]) <= 1e-6 * max(1.0, abs(num)), (t, i, num, g["dX"][t, i])
+    for (e, i) in [(0, 1), (2, 3), (3, 0)]:
+        wp = dict(w, Wr=w["Wr"].copy())
+        wm = dict(w, Wr=w["Wr"].copy())
+        wp["Wr"][e, i] += hh
+        wm["Wr"][e, i] -= hh
+        num = (loss(x, wp) - loss(x, wm)) / (2 * hh)
+        assert abs(num - g["dWr"][e, i]) <= 1e-6 * max(1.0, abs(num)), (e, i, num, g["dWr"][e, i])
+
+
+def test_layernorm_router_ignores_row_offset_and_scale():
+    """With the LayerNorm in front of the router ([P2] 5.2) the logits of a
+    row do not change when the row is shifted and scaled (up to the 1e-5 in
+    the variance), while the plain router's do."""
+    rng = _rng(85)
+    x = rng.normal(size=(5, 64))
+    Wr = rng.normal(size=(8, 64)) / 8
+    a = np.array([0.5, 1.0, 2.0, 3.0, 7.0])[:, None]
+    b = np.array([-2.0, 0.0, 1.5, 4.0, -9.0])[:, None]
+    l0 = O.router_logits(x, Wr, layernorm=True)
+    l1 = O.router_logits(a * x + b, Wr, layernorm=True)
+    # the eps moves a row's scale by a relative eps/2 * |1/var - 1/(a^2 var)| < 3e-5 here
+    np.testing.assert_allclose(l1, l0, rtol=3e-5, atol=1e-9)
+    assert np.abs(O.router_logits(a * x + b, Wr) - O.router_logits(x, Wr)).max() > 0.5

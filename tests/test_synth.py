@@ -2,6 +2,8 @@
 
 import math
 
+import numpy as np
+
 import torch
 
 import moe_synth as S
@@ -59,3 +61,19 @@ def test_workload_shapes_small():
     assert abs(x["W1"].std().item() - 0.02) < 0.002
     again = S.make_inputs(wl)
     assert all(torch.equal(x[k], again[k]) for k in x)
+
+
+def test_affine_rows_and_their_redraws():
+    """x_affine: row t has mean ~b_t and spread ~a_t; a redrawn row keeps
+    its offset and scale."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=16, d=4096, x_affine=True, dtype="f32")
+    x = S.make_inputs(wl, parts=["x"])["x"].double()
+    a, b = S._row_affine(wl, 0, wl.T, "cpu")
+    assert (a >= 0.5).all() and (a <= 3.0).all() and (b.abs() <= 2.0).all()
+    np.testing.assert_allclose(x.mean(1).numpy(), b.numpy(), atol=0.12)
+    np.testing.assert_allclose(x.std(1).numpy(), a.numpy(), rtol=0.05)
+    x2 = x.clone().float()
+    S.redraw_rows(wl, x2, torch.tensor([3, 7]), 1)
+    assert not torch.equal(x2[3], x[3].float()) and torch.equal(x2[4], x[4].float())
+    assert abs(x2[3].double().mean().item() - b[3].item()) < 0.12
+    assert abs(x2[7].double().std().item() - a[7].item()) < 0.05 * a[7].item()
