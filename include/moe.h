@@ -86,6 +86,21 @@ enum { MOE_F32 = 0, MOE_BF16 = 1 };
  *    returns its gradient through the normalisation. */
 enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2, MOE_ROUTE_LAYERNORM = 4 };
 
+/* Load-balance term (moe_config.balance).  f[e] = counts[e]/T (pre-capacity
+ * usage), g[e] = I[e]/T with I[e] the sum of the routing weights of the
+ * slots routed to e (the importance of [P4] 2.2).  moe_stats.balance_stat
+ * is the form on f; the backward differentiates the form on g (the counts
+ * are piecewise constant).
+ *  MOE_BALANCE_CV (0): lambda * std_{n-1}(f) / (mean(f) + 1e-8)  ([P1] 3.1).
+ *  MOE_BALANCE_STD_MAX (1): lambda * (std_{n-1}(f) + gamma * max(f)), gamma =
+ *    balance_gamma ([P2] 3.2: gamma = 100); the max's gradient goes to the
+ *    lowest-index expert among the largest g.
+ *  MOE_BALANCE_SWITCH (2): lambda * sum_e f[e] * g[e] ([P3] 2.3's product of
+ *    two per-expert batch sums, read as usage fraction times mean routing
+ *    weight); the backward holds f constant.  moe_dispatch alone cannot
+ *    form it (it has no weights) and reports NaN; moe_layer_fwd fills it. */
+enum { MOE_BALANCE_CV = 0, MOE_BALANCE_STD_MAX = 1, MOE_BALANCE_SWITCH = 2 };
+
 /* Layer shape and routing rule.  [P2] 4.2 (capacity_factor, min_capacity),
  * [P1] 4.3 (load_balancing_loss_coef 0.01). */
 typedef struct {
@@ -101,6 +116,8 @@ typedef struct {
   float lambda_balance;  /* lambda of the usage statistic (0.01)               */
   int has_shared;        /* 1: add the always-on shared expert                 */
   int route_flags;       /* MOE_ROUTE_* bits, 0 = renormalised, slot-major     */
+  int balance;           /* MOE_BALANCE_*, 0 = the CV form                     */
+  float balance_gamma;   /* gamma of MOE_BALANCE_STD_MAX (100 in [P2] 3.2)     */
 } moe_config;
 
 typedef struct {
@@ -163,7 +180,7 @@ typedef struct {
   int capacity;            /* C                                             */
   int numeric_error;       /* tokens with a non-finite logit                */
   double drop_rate;        /* dropped_slots / (T*k)                         */
-  double balance_stat;     /* lambda * std_{n-1}(counts/T) / (mean + 1e-8)  */
+  double balance_stat;     /* cfg->balance's form on counts/T (MOE_BALANCE_*) */
   double router_entropy;   /* mean over tokens with finite logits of
                               -sum_e p_e ln p_e, p = softmax over all E
                               ([P3] monitoring: alert below 0.3); written by

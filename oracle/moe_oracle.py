@@ -16,7 +16,8 @@ Sources (page title -- section):
        quietly activated inside a large model" (mlqm.cn) -- 3.1 Router,
        3.3 Gate, 4.2 model definition, 4.3 training configuration.
   [P2] "MoE mixture-of-experts architecture: principles and engineering
-       practice" (cnnetsun.cn) -- 3.2 router, 4.2 building an MoE model.
+       practice" (cnnetsun.cn) -- 3.2 router, 4.2 building an MoE model,
+       5.2 normalising the router's input.
   [P3] "MoE architecture revealed: why total parameters != active
        parameters" (rkmt.cn) -- 2.3 router design, 3.3 TinyMoE.
   [P4] "GPT-4 has 1.8 trillion parameters and uses 2% of them per token"
@@ -228,19 +229,56 @@ def dispatch_positions(idx: np.ndarray, rank: np.ndarray, fill: np.ndarray):
     return offsets, pos
 
 
-def balance_stat(counts: np.ndarray, T: int, lam: float) -> float:
-    """lambda * std(f) / (mean(f) + 1e-8), f = counts / T, std with n-1.
+BALANCE_VARIANTS = ("cv", "std_max", "switch")
 
-    [P1] 3.1: L_balance = lambda * std(usage)/mean(usage); [P1] 4.2's code
-    averages the one-hot selection over tokens and adds 1e-8 to the mean;
-    torch.std there is the n-1 form."""
-    f = counts.astype(np.float64) / T
+
+def _std_n1(f: np.ndarray) -> float:
+    """Standard deviation with the n-1 divisor (torch.std's default); 0 for
+    a single value."""
     E = f.shape[0]
     if E < 2:
-        return 0.0  # one expert: nothing to balance (n-1 = 0)
+        return 0.0
     mean = f.sum() / E
-    var = ((f - mean) ** 2).sum() / (E - 1)
-    return lam * math.sqrt(var) / (mean + 1e-8)
+    return math.sqrt(((f - mean) ** 2).sum() / (E - 1))
+
+
+def importance(idx: np.ndarray, w: np.ndarray, E: int) -> np.ndarray:
+    """I[e] = sum of the routing weights of the slots routed to e (before
+    capacity): the importance of [P4] 2.2."""
+    I = np.zeros(E, dtype=np.float64)
+    for t in range(idx.shape[0]):
+        for j in range(idx.shape[1]):
+            if idx[t, j] >= 0:
+                I[idx[t, j]] += w[t, j]
+    return I
+
+
+def balance_stat(counts: np.ndarray, T: int, lam: float, variant: str = "cv", gamma: float = 100.0,
+                 imp: np.ndarray = None) -> float:
+    """The load statistic on pre-capacity usage f = counts / T.
+
+    cv (default): lambda * std(f) / (mean(f) + 1e-8), std with n-1 --
+      [P1] 3.1: L_balance = lambda * std(usage)/mean(usage); [P1] 4.2's code
+      averages the one-hot selection over tokens and adds 1e-8 to the mean;
+      torch.std there is the n-1 form.
+    std_max: lambda * (std(f) + gamma * max(f)) -- [P2] 3.2's auxiliary loss
+      on the experts' usage frequency, gamma = 100 in its DeepSeek-R1 setting.
+    switch: lambda * sum_e f_e * P_e with P = imp / T, the mean routing
+      weight each expert receives -- [P3] 2.3's product of two per-expert
+      sums over the batch, read as usage fraction times mean weight (the
+      page prints both factors alike)."""
+    f = counts.astype(np.float64) / T
+    E = f.shape[0]
+    if variant == "cv":
+        if E < 2:
+            return 0.0  # one expert: nothing to balance (n-1 = 0)
+        mean = f.sum() / E
+        return lam * _std_n1(f) / (mean + 1e-8)
+    if variant == "std_max":
+        return lam * (_std_n1(f) + gamma * f.max())
+    if variant == "switch":
+        return lam * float((f * (np.asarray(imp, dtype=np.float64) / T)).sum())
+    raise ValueError(variant)
 
 
 # ----------------------------------------------------------------------------
@@ -325,7 +363,8 @@ def route_and_dispatch(cfg: dict, x, Wr, expert_bias=None, noise=None) -> Dict[s
         dropped_slots=T * k - kept_total,
         capacity=C,
         drop_rate=(T * k - kept_total) / (T * k),
-        balance_stat=balance_stat(counts, T, cfg.get("lam", 0.01)),
+        balance_stat=balance_stat(counts, T, cfg.get("lam", 0.01), cfg.get("balance", "cv"),
+                                  cfg.get("gamma", 100.0), importance(idx, w, E)),
         numeric_error=int((~finite).sum()),
         router_entropy=router_entropy(l),
     )
@@ -449,10 +488,42 @@ def importance_cv_grad(idx: np.ndarray, w: np.ndarray, E: int, T: int, lam: floa
     return val, dval_dw
 
 
-def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None) -> Dict[str, np.ndarray]:
-    """Gradients of L = <dY, y> + lambda*CV(I/T) for the whole (small) batch.
+def balance_term_grad(idx: np.ndarray, w: np.ndarray, E: int, T: int, lam: float, variant: str = "cv",
+                      gamma: float = 100.0):
+    """Value and per-slot weight gradient of the differentiable balance term
+    on g = I/T (I = importance): the form of balance_stat with the counts
+    replaced by the importance where the gradient flows.
 
-    Per slot: G[t,j] = [kept] <dY[t], FFN_e(x[t])> + d(lambda CV)/dw[t,j];
+    cv: lambda * CV(g) (importance_cv_grad).
+    std_max: lambda * (std_{n-1}(g) + gamma * max(g)); the max's gradient goes
+      to the lowest-index expert among the largest.
+    switch: lambda * sum_e f_e g_e with f = counts / T, the usage fraction, a
+      constant (it counts discrete choices)."""
+    if variant == "cv":
+        return importance_cv_grad(idx, w, E, T, lam)
+    g = importance(idx, w, E) / T
+    if variant == "std_max":
+        sd = _std_n1(g)
+        val = lam * (sd + gamma * g.max())
+        dval = np.zeros(E)
+        if E > 1 and sd > 0:
+            dval += (g - g.sum() / E) / ((E - 1) * sd)
+        dval[int(np.argmax(g))] += gamma  # argmax returns the first largest
+        dval *= lam
+    elif variant == "switch":
+        f = usage_counts(idx, E).astype(np.float64) / T
+        val = lam * float((f * g).sum())
+        dval = lam * f
+    else:
+        raise ValueError(variant)
+    return val, np.where(idx >= 0, dval[np.maximum(idx, 0)] / T, 0.0)
+
+
+def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None) -> Dict[str, np.ndarray]:
+    """Gradients of L = <dY, y> + B(I/T) for the whole (small) batch, B the
+    balance term of cfg["balance"] (balance_term_grad; lambda*CV by default).
+
+    Per slot: G[t,j] = [kept] <dY[t], FFN_e(x[t])> + dB/dw[t,j];
     logit gradient dl[t, idx_j] = w_j (G_j - sum_j' w_j' G_j') (softmax over
     the selected logits), other logits 0; dWr = dl^T x; dX = dl Wr + the
     experts' input gradients (routed rows scaled by w) + the shared expert's."""
@@ -501,7 +572,7 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
         else:
             grads["dbs1"] = g["db1"]
             grads["dbs2"] = g["db2"]
-    val, dcv = importance_cv_grad(idx, w, E, T, lam)
+    val, dcv = balance_term_grad(idx, w, E, T, lam, cfg.get("balance", "cv"), cfg.get("gamma", 100.0))
     G += dcv
     dl = np.zeros((T, E))
     for t in range(T):
@@ -589,7 +660,8 @@ def token_input_grads(cfg: dict, weights: dict, x, dY, route: dict, tokens) -> n
     if cfg.get("has_shared"):
         g = _input_grad_rows(X, Y, act, shared_params(weights, act))
         dX += g["dv"]
-    _, dcv = importance_cv_grad(idx, w, E, T, cfg.get("lam", 0.01))
+    _, dcv = balance_term_grad(idx, w, E, T, cfg.get("lam", 0.01), cfg.get("balance", "cv"),
+                               cfg.get("gamma", 100.0))
     G += dcv[toks]
     Wr = decode(weights["Wr"])
     g = np.zeros_like(X)

@@ -21,6 +21,8 @@ moe_status validate(const moe_config* cfg) {
   if (cfg->dtype == MOE_BF16 && ((cfg->d % 8) || (cfg->h % 8))) return MOE_ERR_UNSUPPORTED;
   if (cfg->route_flags & ~(MOE_ROUTE_RAW_PROBS | MOE_ROUTE_TOKEN_MAJOR | MOE_ROUTE_LAYERNORM))
     return MOE_ERR_INVALID_ARG;
+  if (cfg->balance < MOE_BALANCE_CV || cfg->balance > MOE_BALANCE_SWITCH) return MOE_ERR_INVALID_ARG;
+  if (!(cfg->balance_gamma == cfg->balance_gamma) || isinf(cfg->balance_gamma)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -74,6 +76,7 @@ WsLayout layout(const moe_config* cfg, int training) {
   L.dispatch_off = take(dispatch_scratch_bytes(*cfg));
   L.route_off = take(route_scratch_bytes(*cfg));
   L.ent = take(T * 4);
+  L.imp = cfg->balance == MOE_BALANCE_SWITCH ? take(E * 8) : 0;
   if (!training) {
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
@@ -392,6 +395,11 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
   if (stats) {
     s = launch_entropy_mean(ent, cfg->T, stats, st);
     if (s != MOE_OK) return s;
+    if (cfg->balance == MOE_BALANCE_SWITCH) {
+      s = launch_balance_stat_switch(*cfg, S.idx, S.w, S.counts, static_cast<unsigned long long*>(at(ws, L.imp)),
+                                     stats, st);
+      if (s != MOE_OK) return s;
+    }
   }
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
   if (cfg->has_shared && cfg->dtype == MOE_BF16) {
@@ -450,8 +458,10 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   s = launch_bwd_gather(*cfg, dY, S.Yp, S.pos, S.w, dYp, dot, st);
   if (s != MOE_OK) return s;
   float* lnc = (cfg->route_flags & MOE_ROUTE_LAYERNORM) ? static_cast<float*>(at(ws, L.lnc)) : nullptr;
-  s = launch_router_bwd(*cfg, x, wts->Wr, S.idx, S.w, dot, static_cast<unsigned long long*>(at(ws, L.imp)),
-                        static_cast<float*>(at(ws, L.coef)), dl, lnc, st);
+  if (cfg->balance == MOE_BALANCE_SWITCH && !S.counts) return MOE_ERR_INVALID_ARG;
+  s = launch_router_bwd(*cfg, x, wts->Wr, S.idx, S.w, S.counts, dot,
+                        static_cast<unsigned long long*>(at(ws, L.imp)), static_cast<float*>(at(ws, L.coef)), dl,
+                        lnc, st);
   if (s != MOE_OK) return s;
   s = launch_router_wgrad(*cfg, x, S.idx, dl, lnc, static_cast<float*>(at(ws, L.rpart)), g.dWr, st);
   if (s != MOE_OK) return s;

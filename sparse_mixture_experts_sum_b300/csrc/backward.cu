@@ -17,7 +17,8 @@
 // Every reduction runs in a fixed order or in integers, so the results are
 // the same bits on every run.
 //
-// LayerNorm before the router ([P2] "Mixture of Experts Explained..." 5.2):
+// LayerNorm before the router ([P2] "MoE mixture-of-experts architecture:
+// principles and engineering practice" 5.2):
 // the router saw n_t = r_t (x_t - mu_t).  Then dWr[e] += dl[t,j] n_t, and
 // with g_t = sum_j dl[t,j] Wr[e_j] the input gradient is the normalisation's
 // backward r_t (g - mean(g) - n_t mean(g n_t)).  Writing dl' = r_t dl,
@@ -95,32 +96,64 @@ __global__ void importance_kernel(const int* __restrict__ idx, const float* __re
     if (simp[e]) atomicAdd(&imp[e], simp[e]);
 }
 
-// coef[e] = d(lambda CV(f))/d f_e / T with f = I/T, CV = std_{n-1}(f)/(mean(f) + 1e-8).
-// One block of 1024 threads, one expert per thread (E <= 1024); fp64 sums
-// in a fixed order (warp shuffles, then the warp partials in warp order).
-__global__ void __launch_bounds__(1024) balance_coef_kernel(const unsigned long long* __restrict__ imp, int E,
-                                                            int T, float lam, float* __restrict__ coef) {
+// coef[e] = dB/dI[e] of the balance term B on g = I/T (fp64, fixed-order
+// reductions; one block of 1024 threads, thread e owns expert e):
+//   CV:      lambda * (dstd_e / (m + 1e-8) - std / (m + 1e-8)^2 / E) / T
+//   STD_MAX: lambda * (dstd_e + gamma [e = lowest-index argmax of I]) / T
+//   SWITCH:  lambda * (counts[e] / T) / T
+// with m the mean of g and dstd_e = (g_e - m) / ((E - 1) std).
+__global__ void __launch_bounds__(1024) balance_coef_kernel(const unsigned long long* __restrict__ imp,
+                                                            const int* __restrict__ counts, int E, int T, float lam,
+                                                            int variant, float gamma, float* __restrict__ coef) {
   __shared__ double red[32];
+  __shared__ unsigned long long rmax[32];
+  __shared__ int rarg[32];
   __shared__ double mean_s, std_s;
+  __shared__ int amax_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
   const double scale = 1.0 / (kImpScale * static_cast<double>(T));
-  const double fe = tid < E ? static_cast<double>(imp[tid]) * scale : 0.0;
+  const unsigned long long my = tid < E ? imp[tid] : 0ull;
+  const double fe = static_cast<double>(my) * scale;
   double v = fe;
+  unsigned long long mx = my;
+  int arg = tid < E ? tid : 0x7fffffff;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) red[warp] = v;
+  for (int o = 16; o > 0; o >>= 1) {
+    v += __shfl_xor_sync(0xffffffffu, v, o);
+    const unsigned long long omx = __shfl_xor_sync(0xffffffffu, mx, o);
+    const int oarg = __shfl_xor_sync(0xffffffffu, arg, o);
+    if (omx > mx || (omx == mx && oarg < arg)) {
+      mx = omx;
+      arg = oarg;
+    }
+  }
+  if (lane == 0) {
+    red[warp] = v;
+    rmax[warp] = mx;
+    rarg[warp] = arg;
+  }
   __syncthreads();
   if (tid == 0) {
     double m = 0.0;
-    for (int w2 = 0; w2 < nwarps; ++w2) m += red[w2];
+    unsigned long long bm = 0ull;
+    int ba = 0x7fffffff;
+    for (int w2 = 0; w2 < nwarps; ++w2) {
+      m += red[w2];
+      if (rmax[w2] > bm || (rmax[w2] == bm && rarg[w2] < ba)) {
+        bm = rmax[w2];
+        ba = rarg[w2];
+      }
+    }
     mean_s = m / E;
+    amax_s = ba;
   }
   __syncthreads();
   const double m = mean_s;
   double dv2 = tid < E ? (fe - m) * (fe - m) : 0.0;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) dv2 += __shfl_xor_sync(0xffffffffu, dv2, o);
+  __syncthreads();
   if (lane == 0) red[warp] = dv2;
   __syncthreads();
   if (tid == 0) {
@@ -129,14 +162,39 @@ __global__ void __launch_bounds__(1024) balance_coef_kernel(const unsigned long 
     std_s = E > 1 ? sqrt(var / (E - 1)) : 0.0;
   }
   __syncthreads();
-  const double sd = std_s, den = m + 1e-8;
   if (tid < E) {
+    const double sd = std_s, den = m + 1e-8;
+    const double dstd = (E > 1 && sd > 0.0) ? (fe - m) / ((E - 1) * sd) : 0.0;
     double g = 0.0;
-    if (E > 1 && sd > 0.0) {
-      const double dstd = (fe - m) / ((E - 1) * sd);
+    if (variant == MOE_BALANCE_STD_MAX) {
+      g = static_cast<double>(lam) * (dstd + (tid == amax_s ? static_cast<double>(gamma) : 0.0));
+    } else if (variant == MOE_BALANCE_SWITCH) {
+      g = static_cast<double>(lam) * static_cast<double>(counts[tid]) / T;
+    } else if (E > 1 && sd > 0.0) {
       g = static_cast<double>(lam) * (dstd / den - sd / (den * den) / E);
     }
     coef[tid] = static_cast<float>(g / T);
+  }
+}
+
+// stats->balance_stat = lambda * sum_e (counts[e] / T) (I[e] / T), fp64, warps
+// in order (one block of 1024 threads).
+__global__ void __launch_bounds__(1024) balance_switch_stat_kernel(const unsigned long long* __restrict__ imp,
+                                                                   const int* __restrict__ counts, int E, int T,
+                                                                   float lam, moe_stats* __restrict__ stats) {
+  __shared__ double red[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const double invT = 1.0 / static_cast<double>(T);
+  double v = tid < E ? static_cast<double>(counts[tid]) * invT * (static_cast<double>(imp[tid]) / kImpScale * invT)
+                     : 0.0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (tid == 0) {
+    double s = 0.0;
+    for (int w2 = 0; w2 < (blockDim.x >> 5); ++w2) s += red[w2];
+    stats->balance_stat = static_cast<double>(lam) * s;
   }
 }
 
@@ -463,20 +521,34 @@ moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* 
 }
 
 moe_status launch_router_bwd(const moe_config& cfg, const void* x, const void* Wr, const int* idx, const float* w,
-                             const float* dot, unsigned long long* imp, float* coef, float* dl, float* lnc,
-                             cudaStream_t st) {
+                             const int* counts, const float* dot, unsigned long long* imp, float* coef, float* dl,
+                             float* lnc, cudaStream_t st) {
   const long long nslots = static_cast<long long>(cfg.T) * cfg.k;
   long long blocks = (nslots + 255) / 256;
   if (blocks > 1184) blocks = 1184;
   importance_kernel<<<static_cast<unsigned>(blocks), 256, sizeof(unsigned long long) * cfg.E, st>>>(idx, w, nslots,
                                                                                                     cfg.E, imp);
-  balance_coef_kernel<<<1, 1024, 0, st>>>(imp, cfg.E, cfg.T, cfg.lambda_balance, coef);
+  balance_coef_kernel<<<1, 1024, 0, st>>>(imp, counts, cfg.E, cfg.T, cfg.lambda_balance, cfg.balance,
+                                          cfg.balance_gamma, coef);
   router_bwd_kernel<<<(cfg.T + 255) / 256, 256, 0, st>>>(idx, w, dot, coef, cfg.T, cfg.k, cfg.E, dl);
   if (lnc) {
     if (cfg.dtype != MOE_BF16 || (cfg.d % 8)) return MOE_ERR_UNSUPPORTED;
     ln_router_bwd_kernel<<<warp_grid(cfg.T), 256, 0, st>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(Wr),
                                                            idx, cfg.T, cfg.d, cfg.k, cfg.E, dl, lnc);
   }
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_balance_stat_switch(const moe_config& cfg, const int* idx, const float* w, const int* counts,
+                                      unsigned long long* imp, moe_stats* stats, cudaStream_t st) {
+  moe_status s = launch_zero(imp, sizeof(unsigned long long) * cfg.E, nullptr, 0, st);
+  if (s != MOE_OK) return s;
+  const long long nslots = static_cast<long long>(cfg.T) * cfg.k;
+  long long blocks = (nslots + 255) / 256;
+  if (blocks > 1184) blocks = 1184;
+  importance_kernel<<<static_cast<unsigned>(blocks), 256, sizeof(unsigned long long) * cfg.E, st>>>(idx, w, nslots,
+                                                                                                    cfg.E, imp);
+  balance_switch_stat_kernel<<<1, 1024, 0, st>>>(imp, counts, cfg.E, cfg.T, cfg.lambda_balance, stats);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

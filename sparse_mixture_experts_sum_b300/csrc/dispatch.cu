@@ -71,8 +71,9 @@ __global__ void __launch_bounds__(DT) slot_hist_kernel(const int* __restrict__ i
 }
 
 __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restrict__ blockhist, int nb, int T,
-                                                             int k, int E, int C, float lam,
-                                                             int* __restrict__ base, int* __restrict__ kept,
+                                                             int k, int E, int C, float lam, int balance,
+                                                             float gamma, int* __restrict__ base,
+                                                             int* __restrict__ kept,
                                                              int* __restrict__ offsets, moe_stats* stats) {
   __shared__ int tot[1024];
   __shared__ int warp_sums[32];
@@ -136,36 +137,44 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
     // the warp partials in warp order)
     __shared__ double red[32];
     __shared__ long long redl[32][2];
+    __shared__ int redmax[32];
     const long long nslots = static_cast<long long>(T) * k;
     const double invT = 1.0 / static_cast<double>(T);
     const int nwarps = (blockDim.x + 31) >> 5;
     long long r_cnt = tid < E ? tot[tid] : 0, k_cnt = tid < E ? my_kept : 0;
+    int cmax = tid < E ? tot[tid] : 0;
     double fsum = tid < E ? static_cast<double>(tot[tid]) * invT : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       r_cnt += __shfl_xor_sync(0xffffffffu, r_cnt, o);
       k_cnt += __shfl_xor_sync(0xffffffffu, k_cnt, o);
+      cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
       fsum += __shfl_xor_sync(0xffffffffu, fsum, o);
     }
     if (lane == 0) {
       red[warp] = fsum;
       redl[warp][0] = r_cnt;
       redl[warp][1] = k_cnt;
+      redmax[warp] = cmax;
     }
     __syncthreads();
     __shared__ double mean_s;
     __shared__ long long routed_s, kept_s;
+    __shared__ int max_s;
     if (tid == 0) {
       double fs = 0.0;
       long long rc = 0, kc = 0;
+      int mx = 0;
       for (int w2 = 0; w2 < nwarps; ++w2) {
         fs += red[w2];
         rc += redl[w2][0];
         kc += redl[w2][1];
+        mx = max(mx, redmax[w2]);
       }
       mean_s = fs / E;
       routed_s = rc;
       kept_s = kc;
+      max_s = mx;
     }
     __syncthreads();
     const double mean = mean_s;
@@ -190,7 +199,12 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
       st.capacity = C;
       st.numeric_error = unrouted / k;
       st.drop_rate = static_cast<double>(nslots - kept_s) / static_cast<double>(nslots);
-      st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
+      if (balance == MOE_BALANCE_STD_MAX)
+        st.balance_stat = static_cast<double>(lam) * (sd + static_cast<double>(gamma) * (max_s * invT));
+      else if (balance == MOE_BALANCE_SWITCH)
+        st.balance_stat = __longlong_as_double(0x7ff8000000000000LL);  // needs the weights: set by the layer
+      else
+        st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
       st.router_entropy = __longlong_as_double(0x7ff8000000000000LL);  // set by the layer forward
       *stats = st;
     }
@@ -414,8 +428,8 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
   const bool tm = (cfg.route_flags & MOE_ROUTE_TOKEN_MAJOR) != 0;
   const int CH = chunk_slots(static_cast<long long>(cfg.T) * cfg.k);
   slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
-  capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance, base,
-                                               kept, offsets, stats);
+  capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance,
+                                               cfg.balance, cfg.balance_gamma, base, kept, offsets, stats);
   const size_t asmem = static_cast<size_t>(cfg.E) * (DW + 1) * sizeof(int);
   assign_kernel<<<nb, DT, asmem, stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets, pos);
   if (Xp) {

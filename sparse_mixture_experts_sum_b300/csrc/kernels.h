@@ -111,8 +111,12 @@ moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* 
 // scaled by each token's 1/sqrt(var + eps) and lnc holds the per-token terms
 // of the normalisation's backward.
 moe_status launch_router_bwd(const moe_config& cfg, const void* x, const void* Wr, const int* idx, const float* w,
-                             const float* dot, unsigned long long* imp, float* coef, float* dl, float* lnc,
-                             cudaStream_t st);
+                             const int* counts, const float* dot, unsigned long long* imp, float* coef, float* dl,
+                             float* lnc, cudaStream_t st);
+// stats->balance_stat of MOE_BALANCE_SWITCH: lambda * sum_e (counts[e]/T) (I[e]/T)
+// (imp: E scratch words, zeroed here).
+moe_status launch_balance_stat_switch(const moe_config& cfg, const int* idx, const float* w, const int* counts,
+                                      unsigned long long* imp, moe_stats* stats, cudaStream_t st);
 moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* idx, const float* dl,
                                const float* lnc, float* partial, float* dWr, cudaStream_t st);
 moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,

@@ -21,7 +21,8 @@
 // into each token's running top-k.
 // fp32: one warp per token on the CUDA cores (tiny workloads).
 //
-// LayerNorm before the router ([P2] "Mixture of Experts Explained..." 5.2:
+// LayerNorm before the router ([P2] "MoE mixture-of-experts architecture:
+// principles and engineering practice" 5.2:
 // a LayerNorm, then the linear router; identity scale and zero shift, eps
 // 1e-5, biased variance).  With mu_t, r_t = 1/sqrt(var_t + eps) of row t
 // and S_e = sum_i Wr[e,i]:

@@ -27,7 +27,8 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("h", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("act", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int),
-                ("lambda_balance", ctypes.c_float), ("has_shared", ctypes.c_int), ("route_flags", ctypes.c_int)]
+                ("lambda_balance", ctypes.c_float), ("has_shared", ctypes.c_int), ("route_flags", ctypes.c_int),
+                ("balance", ctypes.c_int), ("balance_gamma", ctypes.c_float)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -117,20 +118,21 @@ def _stream(stream=None):
 
 
 ROUTE_RAW_PROBS, ROUTE_TOKEN_MAJOR, ROUTE_LAYERNORM = 1, 2, 4
+BALANCE = {"cv": 0, "std_max": 1, "switch": 2}
 
 
 def make_config(T, d, h, E, k, act="swiglu", dtype="bf16", capacity_factor=0.0, min_capacity=0,
                 lambda_balance=0.01, has_shared=False, raw_probs=False, token_major=False,
-                layernorm=False) -> MoeConfig:
+                layernorm=False, balance="cv", balance_gamma=100.0) -> MoeConfig:
     flags = ((ROUTE_RAW_PROBS if raw_probs else 0) | (ROUTE_TOKEN_MAJOR if token_major else 0)
              | (ROUTE_LAYERNORM if layernorm else 0))
     return MoeConfig(T, d, h, E, k, ACT[act], DTYPE[dtype], capacity_factor, min_capacity,
-                     lambda_balance, int(bool(has_shared)), flags)
+                     lambda_balance, int(bool(has_shared)), flags, BALANCE[balance], balance_gamma)
 
 
 def config_of(wl, **route) -> MoeConfig:
     """MoeConfig of a moe_synth.Workload (route: raw_probs, token_major,
-    layernorm flags)."""
+    layernorm, balance, balance_gamma)."""
     return make_config(wl.T, wl.d, wl.h, wl.E, wl.k, wl.act, wl.dtype, wl.capacity_factor,
                        wl.min_capacity, wl.lam, wl.has_shared, **route)
 

@@ -13,8 +13,12 @@ MARGIN = 1e-3
 
 
 def oracle_cfg(wl, **route) -> dict:
-    # the C ABI carries lambda and the capacity factor as fp32 values; the
-    # oracle gets those same values; route: raw_probs, token_major, layernorm
+    # the C ABI carries lambda, gamma and the capacity factor as fp32 values;
+    # the oracle gets those same values; route: raw_probs, token_major,
+    # layernorm, balance, balance_gamma (the oracle's gamma)
+    route = dict(route)
+    if "balance_gamma" in route:
+        route["gamma"] = float(np.float32(route.pop("balance_gamma")))
     return dict(T=wl.T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act,
                 capacity_factor=float(np.float32(wl.capacity_factor)),
                 min_capacity=wl.min_capacity, lam=float(np.float32(wl.lam)), has_shared=wl.has_shared,

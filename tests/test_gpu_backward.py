@@ -175,6 +175,23 @@ def test_backward_with_router_layernorm(shared, cf):
     assert rel_frob(plain["dWr"], ref["dWr"]) > 0.1
 
 
+@pytest.mark.parametrize("variant,lam", [("std_max", 20.0), ("switch", 500.0)])
+def test_backward_balance_variants(variant, lam):
+    """The balance term as [P2] 3.2's lambda*(std + gamma*max) (gamma = 100)
+    or [P3] 2.3's product lambda*sum f*g, differentiated on the importance:
+    dWr and dX against the oracle.  lambda is large enough that the term
+    moves the oracle's dWr by over 5% from the default form's."""
+    wl = _workload(has_shared=False, gumbel=True, capacity_factor=1.0, lam=lam, seed=71)
+    t = guarded_inputs(wl, "cpu")
+    dY = t.pop("dY")
+    td = {n: v.to(DEV) for n, v in t.items()}
+    _, sv, g = run_fwd_bwd(wl, td, dY.to(DEV), balance=variant, balance_gamma=100.0)
+    ref = oracle_backward(wl, t, dY, balance=variant, balance_gamma=100.0)
+    assert rel_frob(ref["dWr"], oracle_backward(wl, t, dY)["dWr"]) > 0.05
+    np.testing.assert_array_equal(sv["pos"].cpu().numpy(), ref["route"]["pos"])
+    check_all(wl, t, dY, g, ref)
+
+
 def test_backward_is_deterministic():
     wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, seed=53)
     t = guarded_inputs(wl, DEV)

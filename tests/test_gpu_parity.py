@@ -36,7 +36,7 @@ def run_layer(wl, t):
     return y, sv, M.moe.read_stats(st)
 
 
-def check_routing(r, sv, stats, x=None):
+def check_routing(r, sv, stats, x=None, bal_rtol=1e-12):
     np.testing.assert_array_equal(sv["idx"].cpu().numpy(), r["idx"])
     np.testing.assert_allclose(sv["w"].cpu().numpy(), r["w"], atol=W_TOL, rtol=0)
     np.testing.assert_array_equal(sv["counts"].cpu().numpy(), r["counts"])
@@ -47,7 +47,7 @@ def check_routing(r, sv, stats, x=None):
     for key in ("routed_slots", "kept_slots", "dropped_slots", "capacity", "numeric_error"):
         assert stats[key] == ref[key], key
     assert abs(stats["drop_rate"] - ref["drop_rate"]) <= 1e-15
-    assert abs(stats["balance_stat"] - ref["balance_stat"]) <= 1e-12 * max(1.0, abs(ref["balance_stat"]))
+    assert abs(stats["balance_stat"] - ref["balance_stat"]) <= bal_rtol * max(1.0, abs(ref["balance_stat"]))
     # the router entropy (fp32 per token, fp64 mean); moe_dispatch alone leaves NaN
     if not np.isnan(stats["router_entropy"]):
         assert abs(stats["router_entropy"] - ref["router_entropy"]) <= 2e-5, (stats["router_entropy"],
@@ -481,3 +481,36 @@ def test_layernorm_router(E, dtype):
         with pytest.raises(M.moe.MoeError) as ei:
             M.moe_route(cfg, t["x"], t["Wr"], None, None, idx, w, counts)
         assert ei.value.status == M.moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("variant", ["std_max", "switch"])
+def test_balance_statistic_variants(variant):
+    """[P2] 3.2's lambda*(std + gamma*max(f)) with gamma = 100 (from the
+    counts alone: as exact as the default form) and [P3] 2.3's product
+    lambda*sum f*g (g the mean routing weight, from fp32 weights: relative
+    2e-6).  moe_dispatch alone has no weights, so the product reads NaN
+    there while the counts-only form is complete."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=700, d=256, h=256, E=16, capacity_factor=1.0, seed=31,
+                                              zipf_s=1.1)
+    t = guarded_inputs(wl, DEV)
+    cfg = M.config_of(wl, balance=variant, balance_gamma=100.0)
+    sv = M.moe.alloc_saved(cfg)
+    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg, 1)
+    M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], None, y, sv, st, ws)
+    assert M.moe_check_error(ws) == 0
+    r = O.layer_forward(oracle_cfg(wl, balance=variant, balance_gamma=100.0), oracle_weights(t), t["x"],
+                        t.get("expert_bias"))
+    stats = M.moe.read_stats(st)
+    check_routing(r, sv, stats, t["x"], bal_rtol=1e-12 if variant == "std_max" else 2e-6)
+    assert_close_bf16(to_np(y), r["y"], "y")
+    st2 = M.moe.stats_buffer()
+    Xp = torch.empty_like(sv["Xp"])
+    M.moe_dispatch(cfg, sv["idx"], t["x"], torch.empty_like(sv["kept"]), torch.empty_like(sv["offsets"]),
+                   torch.empty_like(sv["pos"]), Xp, st2, ws)
+    s2 = M.moe.read_stats(st2)
+    if variant == "switch":
+        assert np.isnan(s2["balance_stat"])
+    else:
+        assert s2["balance_stat"] == stats["balance_stat"]

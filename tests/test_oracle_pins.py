@@ -609,3 +609,87 @@ def test_layernorm_router_ignores_row_offset_and_scale():
     # the eps moves a row's scale by a relative eps/2 * |1/var - 1/(a^2 var)| < 3e-5 here
     np.testing.assert_allclose(l1, l0, rtol=3e-5, atol=1e-9)
     assert np.abs(O.router_logits(a * x + b, Wr) - O.router_logits(x, Wr)).max() > 0.5
+
+
+def test_balance_variants_closed_forms():
+    """[P2] 3.2's lambda*(std + gamma*max) and [P3] 2.3's product form, on
+    hand-worked cases and against torch.std (the n-1 form)."""
+    counts = np.array([3, 1, 0, 0])
+    f = counts / 2.0
+    ref = 0.01 * (torch.tensor(f).std().item() + 100 * 1.5)
+    assert abs(O.balance_stat(counts, 2, 0.01, "std_max", 100.0) - ref) < 1e-12
+    assert abs(O.balance_stat(counts, 2, 0.01, "std_max", 100.0) - 0.01 * (math.sqrt(0.5) + 150)) < 1e-12
+    # one expert: the n-1 std is 0, the max term remains
+    assert O.balance_stat(np.array([7]), 7, 0.5, "std_max", 3.0) == 0.5 * 3.0
+    # product form: token 0 -> experts 0, 1 (0.75, 0.25); token 1 -> 0, 2 (0.6, 0.4)
+    idx = np.array([[0, 1], [0, 2]])
+    w = np.array([[0.75, 0.25], [0.6, 0.4]])
+    imp = O.importance(idx, w, 4)
+    np.testing.assert_allclose(imp, [1.35, 0.25, 0.4, 0.0], rtol=0, atol=1e-15)
+    v = O.balance_stat(O.usage_counts(idx, 4), 2, 0.01, "switch", imp=imp)
+    assert abs(v - 0.01 * (1.0 * 0.675 + 0.5 * 0.125 + 0.5 * 0.2)) < 1e-15
+    # perfectly uniform routing: f = k/E, mean weight 1/E -> lambda*k/E
+    E, k, T = 8, 2, 64
+    idx = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)])
+    w = np.full((T, k), 0.5)
+    v = O.balance_stat(O.usage_counts(idx, E), T, 0.01, "switch", imp=O.importance(idx, w, E))
+    assert abs(v - 0.01 * k / E) < 1e-15
+    assert O.balance_stat(O.usage_counts(idx, E), T, 0.01, "std_max", 100.0) == pytest.approx(0.01 * 100 * k / E)
+
+
+@pytest.mark.parametrize("variant", ["std_max", "switch"])
+def test_balance_variant_gradients_finite_differences(variant):
+    """Each slot's gradient of the balance term against central differences
+    in that slot's weight (routing fixed, a unique largest importance)."""
+    rng = _rng(87)
+    T, E, k = 40, 6, 2
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    idx[3, :] = -1  # a token routed nowhere
+    w = rng.uniform(0.1, 0.9, size=(T, k))
+    val, g = O.balance_term_grad(idx, w, E, T, 0.05, variant, 7.0)
+    imp = O.importance(idx, w, E)
+    assert np.sort(imp)[-1] - np.sort(imp)[-2] > 1e-3
+    h = 1e-6
+    for (t, j) in [(0, 0), (5, 1), (17, 0), (39, 1), (3, 0)]:
+        wp, wm = w.copy(), w.copy()
+        wp[t, j] += h
+        wm[t, j] -= h
+        num = (O.balance_term_grad(idx, wp, E, T, 0.05, variant, 7.0)[0]
+               - O.balance_term_grad(idx, wm, E, T, 0.05, variant, 7.0)[0]) / (2 * h)
+        assert abs(num - g[t, j]) <= 1e-7 * max(1.0, abs(num)), (t, j, num, g[t, j])
+
+
+@pytest.mark.parametrize("variant", ["cv", "std_max", "switch"])
+def test_layer_backward_balance_variants_finite_differences(variant):
+    """The whole layer's dX and dWr under each balance term against central
+    differences of L = <dY, y> + B (routing fixed, away from ties)."""
+    rng = _rng(89)
+    T, d, h, E, k = 14, 5, 6, 4, 2
+    w = dict(Wr=rng.normal(size=(E, d)), W1=rng.normal(size=(E, h, d)) / 2, W3=rng.normal(size=(E, h, d)) / 2,
+             W2=rng.normal(size=(E, d, h)) / 3)
+    cfg = dict(T=T, d=d, h=h, E=E, k=k, act="swiglu", capacity_factor=1.0, lam=0.3, balance=variant,
+               gamma=2.0)
+    x = rng.normal(size=(T, d))
+    dY = rng.normal(size=(T, d))
+    g = O.layer_backward(cfg, w, x, dY)
+    if variant != "cv":
+        cv = O.layer_backward(dict(cfg, balance="cv"), w, x, dY)
+        assert np.abs(cv["dWr"] - g["dWr"]).max() > 1e-3  # the term reaches the router
+
+    def loss(xx, ww):
+        return O.layer_backward(cfg, ww, xx, dY)["loss"]
+
+    hh = 1e-6
+    for (t, i) in [(0, 0), (6, 2), (13, 4)]:
+        xp, xm = x.copy(), x.copy()
+        xp[t, i] += hh
+        xm[t, i] -= hh
+        num = (loss(xp, w) - loss(xm, w)) / (2 * hh)
+        assert abs(num - g["dX"][t, i]) <= 1e-6 * max(1.0, abs(num)), (t, i, num, g["dX"][t, i])
+    for (e, i) in [(0, 1), (2, 3), (3, 0)]:
+        wp = dict(w, Wr=w["Wr"].copy())
+        wm = dict(w, Wr=w["Wr"].copy())
+        wp["Wr"][e, i] += hh
+        wm["Wr"][e, i] -= hh
+        num = (loss(x, wp) - loss(x, wm)) / (2 * hh)
+        assert abs(num - g["dWr"][e, i]) <= 1e-6 * max(1.0, abs(num)), (e, i, num, g["dWr"][e, i])
