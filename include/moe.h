@@ -83,8 +83,19 @@ enum { MOE_F32 = 0, MOE_BF16 = 1 };
  *    sqrt(biased variance + 1e-5), unit scale and zero shift ([P2] 5.2, a
  *    LayerNorm in front of the linear router); the experts still see x.
  *    bf16 needs the workspace path of moe_route (ws != NULL); moe_layer_bwd
- *    returns its gradient through the normalisation. */
-enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2, MOE_ROUTE_LAYERNORM = 4 };
+ *    returns its gradient through the normalisation.
+ *  MOE_ROUTE_REROUTE: a slot over capacity tries its token's next-best
+ *    expert before it is dropped ([P3] 2.3).  The router also records each
+ *    token's experts ranked k .. 2k-1 (its backups).  After the usual pass,
+ *    the r-th dropped slot of token t (r in slot order) is offered
+ *    backup r, in the same priority order.  It is kept if that expert has
+ *    room left, and is placed after the expert's first-pass rows.  The
+ *    slot keeps its weight w[t,j] and idx keeps the router's choice; pos
+ *    and offsets show the serving expert.  Needs k <= 4 and a workspace:
+ *    moe_route writes the backups into ws, moe_dispatch reads them from
+ *    the same ws.  moe_dispatch_static and moe_layer_bwd return
+ *    MOE_ERR_UNSUPPORTED. */
+enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2, MOE_ROUTE_LAYERNORM = 4, MOE_ROUTE_REROUTE = 8 };
 
 /* Load-balance term (moe_config.balance).  f[e] = counts[e]/T (pre-capacity
  * usage), g[e] = I[e]/T with I[e] the sum of the routing weights of the
@@ -185,6 +196,8 @@ typedef struct {
                               -sum_e p_e ln p_e, p = softmax over all E
                               ([P3] monitoring: alert below 0.3); written by
                               moe_layer_fwd; moe_dispatch alone leaves NaN  */
+  long long rerouted_slots; /* slots kept by a backup expert
+                               (MOE_ROUTE_REROUTE; counted in kept_slots)  */
 } moe_stats;
 
 /* C = max(min_capacity, ceil(cf*T*k/E)) or T when cf <= 0 ([P3] 2.3:

@@ -217,6 +217,64 @@ def assign_capacity(idx: np.ndarray, E: int, C: int, token_major: bool = False):
     return rank, fill
 
 
+def backup_experts(l: np.ndarray, k: int) -> np.ndarray:
+    """Each token's experts ranked k .. 2k-1 by (logit descending, index
+    ascending): its next-best experts, which the slots that overflow can be
+    rerouted to ([P3] 2.3).  -1 where fewer than 2k experts exist or the
+    token's logits are not all finite.  Returns [T,k] int64."""
+    T, E = l.shape
+    b = np.full((T, k), -1, dtype=np.int64)
+    nb = max(0, min(k, E - k))
+    experts = np.arange(E)
+    for t in range(T):
+        if not np.all(np.isfinite(l[t])):
+            continue
+        order = np.lexsort((experts, -l[t]))
+        b[t, :nb] = order[k:k + nb]
+    return b
+
+
+def reroute_overflow(idx: np.ndarray, backup: np.ndarray, rank: np.ndarray, fill: np.ndarray, C: int,
+                     token_major: bool = False):
+    """Second capacity pass: the slots the first pass dropped try their
+    token's next-best experts ([P3] 2.3: tokens beyond capacity are dropped
+    or routed to the next-best expert).
+
+    The r-th dropped slot of token t (r counted in slot order j) tries
+    backup[t, r] once.  Slots are visited in the first pass's priority order.
+    A slot is kept if that expert has room left after the first pass and
+    the slots rerouted to it before; it then takes that expert's next place
+    after its first-pass rows.  Otherwise it stays dropped.
+    Returns served [T,k] (the expert serving each slot, -1 for none), rank2
+    [T,k] (place among the expert's rerouted rows, -1 if not rerouted) and
+    fill2 [E] (rerouted rows per expert)."""
+    T, k = idx.shape
+    E = fill.shape[0]
+    nth = np.full((T, k), -1, dtype=np.int64)
+    for t in range(T):
+        r = 0
+        for j in range(k):
+            if idx[t, j] >= 0 and rank[t, j] < 0:
+                nth[t, j] = r
+                r += 1
+    served = np.where(rank >= 0, idx, -1)
+    rank2 = np.full((T, k), -1, dtype=np.int64)
+    fill2 = np.zeros(E, dtype=np.int64)
+    order = [(t, j) for t in range(T) for j in range(k)] if token_major else \
+        [(t, j) for j in range(k) for t in range(T)]
+    for t, j in order:
+        if nth[t, j] < 0:
+            continue
+        b = backup[t, nth[t, j]]
+        if b < 0:
+            continue
+        if fill[b] + fill2[b] < C:
+            rank2[t, j] = fill2[b]
+            fill2[b] += 1
+            served[t, j] = b
+    return served, rank2, fill2
+
+
 def dispatch_positions(idx: np.ndarray, rank: np.ndarray, fill: np.ndarray):
     """offsets = exclusive prefix sum of the kept counts (experts in index
     order); a kept slot's row in the expert-contiguous buffer is
@@ -354,7 +412,21 @@ def route_and_dispatch(cfg: dict, x, Wr, expert_bias=None, noise=None) -> Dict[s
     counts = usage_counts(idx, E)
     C = expert_capacity(T, k, E, cfg.get("capacity_factor", 0.0), cfg.get("min_capacity", 0))
     rank, fill = assign_capacity(idx, E, C, token_major=cfg.get("token_major", False))
-    offsets, pos = dispatch_positions(idx, rank, fill)
+    served = np.where(rank >= 0, idx, -1)
+    backup = None
+    rerouted = 0
+    if cfg.get("reroute"):
+        backup = backup_experts(l, k)
+        served, rank2, fill2 = reroute_overflow(idx, backup, rank, fill, C, cfg.get("token_major", False))
+        offsets, _ = dispatch_positions(idx, rank, fill + fill2)
+        # first-pass rows first, then the rerouted rows, in each expert
+        pos = np.where(rank >= 0, offsets[np.maximum(idx, 0)] + rank,
+                       np.where(rank2 >= 0, offsets[np.maximum(served, 0)] + fill[np.maximum(served, 0)] + rank2,
+                                -1))
+        fill = fill + fill2
+        rerouted = int(fill2.sum())
+    else:
+        offsets, pos = dispatch_positions(idx, rank, fill)
     routed = int(counts.sum())
     kept_total = int(fill.sum())
     stats = dict(
@@ -367,9 +439,10 @@ def route_and_dispatch(cfg: dict, x, Wr, expert_bias=None, noise=None) -> Dict[s
                                   cfg.get("gamma", 100.0), importance(idx, w, E)),
         numeric_error=int((~finite).sum()),
         router_entropy=router_entropy(l),
+        rerouted_slots=rerouted,
     )
     return dict(logits=l, idx=idx, w=w, counts=counts, kept=fill, capacity=C,
-                rank=rank, offsets=offsets, pos=pos, stats=stats)
+                rank=rank, offsets=offsets, pos=pos, stats=stats, served=served, backup=backup)
 
 
 def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None,
@@ -384,7 +457,7 @@ def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None,
     act = cfg["act"]
     out = np.zeros((len(toks), k, d), dtype=np.float64)
     kept = r["pos"][toks] >= 0
-    idx = r["idx"][toks]
+    idx = r["served"][toks]  # the expert serving each slot (a rerouted slot's backup)
     touched = np.zeros(len(toks), dtype=np.int64)
     for e in range(cfg["E"]):
         rows, slots = np.nonzero((idx == e) & kept)
@@ -532,6 +605,8 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
     lam = cfg.get("lam", 0.01)
     if cfg.get("raw_probs"):
         raise NotImplementedError("the backward covers renormalised top-k weights only")
+    if cfg.get("reroute"):
+        raise NotImplementedError("the backward covers slots served by their chosen experts only")
     r = route_and_dispatch(cfg, x, weights["Wr"], expert_bias, noise)
     X = decode(x)
     DY = decode(dY)

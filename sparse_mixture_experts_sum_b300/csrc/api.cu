@@ -19,8 +19,9 @@ moe_status validate(const moe_config* cfg) {
   if (cfg->min_capacity < 0 || !(cfg->capacity_factor == cfg->capacity_factor)) return MOE_ERR_INVALID_ARG;
   if (static_cast<long long>(cfg->T) * cfg->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
   if (cfg->dtype == MOE_BF16 && ((cfg->d % 8) || (cfg->h % 8))) return MOE_ERR_UNSUPPORTED;
-  if (cfg->route_flags & ~(MOE_ROUTE_RAW_PROBS | MOE_ROUTE_TOKEN_MAJOR | MOE_ROUTE_LAYERNORM))
+  if (cfg->route_flags & ~(MOE_ROUTE_RAW_PROBS | MOE_ROUTE_TOKEN_MAJOR | MOE_ROUTE_LAYERNORM | MOE_ROUTE_REROUTE))
     return MOE_ERR_INVALID_ARG;
+  if ((cfg->route_flags & MOE_ROUTE_REROUTE) && cfg->k > 4) return MOE_ERR_UNSUPPORTED;
   if (cfg->balance < MOE_BALANCE_CV || cfg->balance > MOE_BALANCE_SWITCH) return MOE_ERR_INVALID_ARG;
   if (!(cfg->balance_gamma == cfg->balance_gamma) || isinf(cfg->balance_gamma)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -43,7 +44,7 @@ size_t esize(const moe_config* cfg) { return cfg->dtype == MOE_BF16 ? 2 : 4; }
 // [header | dYp | dAB | dXp | dot | dl | importance | coef | router partials
 // | shared dAB | LayerNorm terms].
 struct WsLayout {
-  size_t dispatch_off, route_off, ent;
+  size_t dispatch_off, route_off, ent, backup;
   size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs;
   size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs, lnc;
   size_t total;
@@ -77,6 +78,7 @@ WsLayout layout(const moe_config* cfg, int training) {
   L.route_off = take(route_scratch_bytes(*cfg));
   L.ent = take(T * 4);
   L.imp = cfg->balance == MOE_BALANCE_SWITCH ? take(E * 8) : 0;
+  L.backup = (cfg->route_flags & MOE_ROUTE_REROUTE) ? take(T * k * 4) : 0;
   if (!training) {
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
@@ -274,9 +276,11 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr, const
   if (!x || !Wr || !idx || !w || !counts) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wr) || (ws && !aligned16(ws))) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  void* scratch = ws && route_scratch_bytes(*cfg) ? at(ws, layout(cfg, 1).route_off) : nullptr;
+  const WsLayout L = layout(cfg, 1);
+  void* scratch = ws && route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr;
+  int* backup = ws && (cfg->route_flags & MOE_ROUTE_REROUTE) ? static_cast<int*>(at(ws, L.backup)) : nullptr;
   int* err = ws ? static_cast<int*>(ws) : nullptr;
-  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, entropy, scratch, err, st);
+  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, entropy, scratch, backup, err, st);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x, int* kept, int* offsets, int* pos,
@@ -286,7 +290,9 @@ moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x, in
   if (!idx || !x || !kept || !offsets || !pos || !Xp || !ws) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Xp) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = layout(cfg, 1);
+  const int* backup = (cfg->route_flags & MOE_ROUTE_REROUTE) ? static_cast<const int*>(at(ws, L.backup)) : nullptr;
   return launch_dispatch(*cfg, capacity_of(cfg), idx, x, kept, offsets, pos, Xp, stats, at(ws, L.dispatch_off),
+                         backup,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -296,10 +302,11 @@ moe_status moe_dispatch_static(const moe_config* cfg, const int* idx, const void
   if (s != MOE_OK) return s;
   if (!idx || !x || !kept || !offsets || !pos || !Xp) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Xp)) return MOE_ERR_INVALID_ARG;
+  if (cfg->route_flags & MOE_ROUTE_REROUTE) return MOE_ERR_UNSUPPORTED;  // the backups live in a workspace
   void* scratch = nullptr;
   s = static_dispatch_scratch(dispatch_scratch_bytes(*cfg), &scratch);
   if (s != MOE_OK) return s;
-  return launch_dispatch(*cfg, capacity_of(cfg), idx, x, kept, offsets, pos, Xp, stats, scratch,
+  return launch_dispatch(*cfg, capacity_of(cfg), idx, x, kept, offsets, pos, Xp, stats, scratch, nullptr,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -386,11 +393,12 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
   int* err = static_cast<int*>(ws);  // zeroed by the router's first launch
 
   float* ent = stats ? static_cast<float*>(at(ws, L.ent)) : nullptr;
+  int* backup = (cfg->route_flags & MOE_ROUTE_REROUTE) ? static_cast<int*>(at(ws, L.backup)) : nullptr;
   s = launch_route(*cfg, x, wts->Wr, wts->expert_bias, noise, S.idx, S.w, S.counts, ent,
-                   route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr, err, st);
+                   route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr, backup, err, st);
   if (s != MOE_OK) return s;
   s = launch_dispatch(*cfg, capacity_of(cfg), S.idx, x, S.kept, S.offsets, S.pos, S.Xp, stats,
-                      at(ws, L.dispatch_off), st);
+                      at(ws, L.dispatch_off), backup, st);
   if (s != MOE_OK) return s;
   if (stats) {
     s = launch_entropy_mean(ent, cfg->T, stats, st);
@@ -430,7 +438,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
   if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if ((cfg->d % 64) || (cfg->h % 64)) return MOE_ERR_UNSUPPORTED;
-  if (cfg->route_flags & MOE_ROUTE_RAW_PROBS) return MOE_ERR_UNSUPPORTED;
+  if (cfg->route_flags & (MOE_ROUTE_RAW_PROBS | MOE_ROUTE_REROUTE)) return MOE_ERR_UNSUPPORTED;
   if (!wts->Wr || !wts->W1 || !wts->W2 || (swiglu && !wts->W3)) return MOE_ERR_INVALID_ARG;
   if (cfg->has_shared && (!wts->Ws1 || !wts->Ws2 || (swiglu && !wts->Ws3))) return MOE_ERR_INVALID_ARG;
   const moe_saved& S = *saved;

@@ -51,8 +51,32 @@ __device__ __forceinline__ int slot_expert(const int* idx, int T, int k, bool to
   return idx[static_cast<size_t>(t) * k + j];
 }
 
-__global__ void __launch_bounds__(DT) slot_hist_kernel(const int* __restrict__ idx, int T, int k, int E,
-                                                       bool token_major, int CH, int* __restrict__ blockhist) {
+// The slots of one capacity pass.  Pass 1 (rank1 == nullptr): each slot
+// asks for its chosen expert.  Pass 2 (rerouting on overflow): a slot the
+// first pass dropped asks for backup[t, r], r = the number of the token's
+// earlier slots (j' < j) that were dropped too; every other slot asks for
+// none (-1).  rank1 holds the first pass's ranks (-1 = not kept).
+struct SlotSrc {
+  const int* idx;
+  const int* rank1;
+  const int* backup;
+};
+
+// Expert slot s asks for in this pass; e0 receives its chosen expert.
+__device__ __forceinline__ int pass_expert(const SlotSrc& S, int T, int k, bool token_major, long long s, int& t,
+                                           int& j, int& e0) {
+  e0 = slot_expert(S.idx, T, k, token_major, s, t, j);
+  if (!S.rank1) return e0;
+  const size_t row = static_cast<size_t>(t) * k;
+  if (e0 < 0 || S.rank1[row + j] >= 0) return -1;
+  int r = 0;
+  for (int q = 0; q < j; ++q)
+    if (S.idx[row + q] >= 0 && S.rank1[row + q] < 0) ++r;
+  return S.backup[row + r];
+}
+
+__global__ void __launch_bounds__(DT) slot_hist_kernel(SlotSrc S, int T, int k, int E, bool token_major, int CH,
+                                                       int* __restrict__ blockhist) {
   extern __shared__ int hist[];  // E + 1 (last: unrouted)
   for (int e = threadIdx.x; e <= E; e += DT) hist[e] = 0;
   __syncthreads();
@@ -61,8 +85,8 @@ __global__ void __launch_bounds__(DT) slot_hist_kernel(const int* __restrict__ i
   for (int i = threadIdx.x; i < CH; i += DT) {
     const long long s = s0 + i;
     if (s >= nslots) break;
-    int t, j;
-    const int e = slot_expert(idx, T, k, token_major, s, t, j);
+    int t, j, e0;
+    const int e = pass_expert(S, T, k, token_major, s, t, j, e0);
     atomicAdd(&hist[(e >= 0 && e < E) ? e : E], 1);
   }
   __syncthreads();
@@ -72,8 +96,8 @@ __global__ void __launch_bounds__(DT) slot_hist_kernel(const int* __restrict__ i
 
 __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restrict__ blockhist, int nb, int T,
                                                              int k, int E, int C, float lam, int balance,
-                                                             float gamma, int* __restrict__ base,
-                                                             int* __restrict__ kept,
+                                                             float gamma, const int* __restrict__ used,
+                                                             int* __restrict__ base, int* __restrict__ kept,
                                                              int* __restrict__ offsets, moe_stats* stats) {
   __shared__ int tot[1024];
   __shared__ int warp_sums[32];
@@ -103,8 +127,14 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
     }
   }
   __syncthreads();
-  int my_kept = 0;
-  if (tid < E) my_kept = tot[tid] < C ? tot[tid] : C;
+  // pass 2 (used != nullptr): the room left after the first pass's rows,
+  // and kept[e] counts both passes
+  int my_kept = 0, my_new = 0;
+  if (tid < E) {
+    const int u = used ? used[tid] : 0;
+    my_new = tot[tid] < C - u ? tot[tid] : C - u;
+    my_kept = u + my_new;
+  }
   // exclusive scan of kept over experts (block-wide, experts in index order)
   int incl = my_kept;
 #pragma unroll
@@ -131,7 +161,24 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
     offsets[tid] = excl;
     if (tid == E - 1) offsets[E] = excl + my_kept;
   }
-  if (stats) {
+  if (stats && used) {
+    // pass 2: the rerouted rows move from dropped to kept
+    __shared__ long long rer_s[32];
+    long long v = my_new;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) rer_s[warp] = v;
+    __syncthreads();
+    if (tid == 0) {
+      long long rer = 0;
+      for (int w2 = 0; w2 < ((blockDim.x + 31) >> 5); ++w2) rer += rer_s[w2];
+      const long long nslots = static_cast<long long>(T) * k;
+      stats->kept_slots += rer;
+      stats->dropped_slots -= rer;
+      stats->drop_rate = static_cast<double>(stats->dropped_slots) / static_cast<double>(nslots);
+      stats->rerouted_slots = rer;
+    }
+  } else if (stats) {
     // load statistics: fp64, one division, fixed-order reductions (each
     // thread owns one expert; warps reduce by shuffles, then warp 0 sums
     // the warp partials in warp order)
@@ -206,15 +253,21 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
       else
         st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
       st.router_entropy = __longlong_as_double(0x7ff8000000000000LL);  // set by the layer forward
+      st.rerouted_slots = 0;
       *stats = st;
     }
   }
 }
 
-__global__ void __launch_bounds__(DT) assign_kernel(const int* __restrict__ idx, int T, int k, int E,
-                                                    bool token_major, int CH, const int* __restrict__ base,
-                                                    const int* __restrict__ kept,
-                                                    const int* __restrict__ offsets, int* __restrict__ pos) {
+// Ranks of one pass and the slots' places.  Pass 1: p = offsets[e] + rank
+// (offsets == nullptr: the bare rank, kept for a second pass).  Pass 2
+// (used = the first pass's kept rows): a rerouted slot lands after its new
+// expert's first-pass rows, p = offsets[e] + used[e] + rank; a slot the
+// first pass kept gets p = offsets[e0] + rank1.
+__global__ void __launch_bounds__(DT) assign_kernel(SlotSrc S, int T, int k, int E, bool token_major, int CH,
+                                                    const int* __restrict__ base, const int* __restrict__ kept,
+                                                    const int* __restrict__ offsets, const int* __restrict__ used,
+                                                    int* __restrict__ pos) {
   extern __shared__ int sm[];
   int* runcnt = sm;       // [E]
   int* warpcnt = sm + E;  // [DW][E]
@@ -228,10 +281,10 @@ __global__ void __launch_bounds__(DT) assign_kernel(const int* __restrict__ idx,
   for (int r = 0; r < CH / DT; ++r) {
     if (s0 + static_cast<long long>(r) * DT >= nslots) break;  // uniform across the block
     const long long s = s0 + static_cast<long long>(r) * DT + threadIdx.x;
-    int t = 0, j = 0, e = -1;
+    int t = 0, j = 0, e = -1, e0 = -1;
     const bool in = s < nslots;
     if (in) {
-      e = slot_expert(idx, T, k, token_major, s, t, j);
+      e = pass_expert(S, T, k, token_major, s, t, j, e0);
       if (e >= E) e = -1;
     }
     const int key = in ? e : -2;
@@ -245,9 +298,14 @@ __global__ void __launch_bounds__(DT) assign_kernel(const int* __restrict__ idx,
         int prefix = 0;
         for (int w2 = 0; w2 < warp; ++w2) prefix += warpcnt[w2 * E + e];
         const int rank = bbase[e] + runcnt[e] + prefix + lrank;
-        // kept[e] = min(routed[e], C): a slot is kept iff its rank is below it,
-        // which also keeps every position inside [offsets[e], offsets[e+1])
-        if (rank < kept[e]) p = offsets[e] + rank;
+        // kept[e] = min(routed[e], C) (+ the first pass's rows): a slot is
+        // kept iff its rank is below its pass's share, which also keeps every
+        // position inside [offsets[e], offsets[e+1])
+        const int u = used ? used[e] : 0;
+        if (rank < kept[e] - u) p = (offsets ? offsets[e] : 0) + u + rank;
+      } else if (used && e0 >= 0 && e0 < E) {
+        const int r1 = S.rank1[static_cast<size_t>(t) * k + j];
+        if (r1 >= 0) p = offsets[e0] + r1;
       }
       pos[static_cast<size_t>(t) * k + j] = p;
     }
@@ -416,22 +474,52 @@ inline int row_chunks(int T, int vec_per_row) {
 
 size_t dispatch_scratch_bytes(const moe_config& cfg) {
   const size_t nb = n_chunks(cfg);
-  return align_up(nb * (cfg.E + 1) * sizeof(int), 256) + align_up(nb * cfg.E * sizeof(int), 256);
+  size_t b = align_up(nb * (cfg.E + 1) * sizeof(int), 256) + align_up(nb * cfg.E * sizeof(int), 256);
+  if (cfg.route_flags & MOE_ROUTE_REROUTE)
+    b += align_up(static_cast<size_t>(cfg.E) * sizeof(int), 256) +
+         align_up(static_cast<size_t>(cfg.T) * cfg.k * sizeof(int), 256);
+  return b;
 }
 
 moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const void* x, int* kept, int* offsets,
-                           int* pos, void* Xp, moe_stats* stats, void* scratch, cudaStream_t stream) {
+                           int* pos, void* Xp, moe_stats* stats, void* scratch, const int* backup,
+                           cudaStream_t stream) {
   const int nb = n_chunks(cfg);
-  int* blockhist = static_cast<int*>(scratch);
-  int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) +
-                                     align_up(static_cast<size_t>(nb) * (cfg.E + 1) * sizeof(int), 256));
+  uint8_t* sp = static_cast<uint8_t*>(scratch);
+  int* blockhist = reinterpret_cast<int*>(sp);
+  sp += align_up(static_cast<size_t>(nb) * (cfg.E + 1) * sizeof(int), 256);
+  int* base = reinterpret_cast<int*>(sp);
+  sp += align_up(static_cast<size_t>(nb) * cfg.E * sizeof(int), 256);
   const bool tm = (cfg.route_flags & MOE_ROUTE_TOKEN_MAJOR) != 0;
+  const bool reroute = (cfg.route_flags & MOE_ROUTE_REROUTE) != 0;
+  if (reroute && !backup) return MOE_ERR_UNSUPPORTED;
   const int CH = chunk_slots(static_cast<long long>(cfg.T) * cfg.k);
-  slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
-  capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance,
-                                               cfg.balance, cfg.balance_gamma, base, kept, offsets, stats);
   const size_t asmem = static_cast<size_t>(cfg.E) * (DW + 1) * sizeof(int);
-  assign_kernel<<<nb, DT, asmem, stream>>>(idx, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets, pos);
+  const SlotSrc S1{idx, nullptr, nullptr};
+  if (!reroute) {
+    slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(S1, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
+    capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance,
+                                                 cfg.balance, cfg.balance_gamma, nullptr, base, kept, offsets,
+                                                 stats);
+    assign_kernel<<<nb, DT, asmem, stream>>>(S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets, nullptr, pos);
+  } else {
+    // pass 1 keeps its ranks; pass 2 offers the dropped slots their backups
+    // in the same priority order, then places every slot
+    int* kept1 = reinterpret_cast<int*>(sp);
+    sp += align_up(static_cast<size_t>(cfg.E) * sizeof(int), 256);
+    int* rank1 = reinterpret_cast<int*>(sp);
+    slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(S1, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
+    capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance,
+                                                 cfg.balance, cfg.balance_gamma, nullptr, base, kept1, offsets,
+                                                 stats);
+    assign_kernel<<<nb, DT, asmem, stream>>>(S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept1, nullptr, nullptr,
+                                             rank1);
+    const SlotSrc S2{idx, rank1, backup};
+    slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(S2, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
+    capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance,
+                                                 cfg.balance, cfg.balance_gamma, kept1, base, kept, offsets, stats);
+    assign_kernel<<<nb, DT, asmem, stream>>>(S2, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets, kept1, pos);
+  }
   if (Xp) {
     const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
     const long long row_bytes = static_cast<long long>(cfg.d) * es;

@@ -128,6 +128,13 @@ __device__ __forceinline__ void topk_finish(const float (&v)[MAXK], const int (&
   if (ent) ent[t] = st.entropy();
 }
 
+// Backup experts of a token for rerouting on overflow: its entries k .. kk-1
+// of the sorted list (kk <= 2k), -1 past kk or for a non-finite token.
+__device__ __forceinline__ void write_backup(const int (&ix)[MAXK], int k, int kk, bool finite, int t,
+                                             int* backup) {
+  for (int r = 0; r < k; ++r) backup[static_cast<size_t>(t) * k + r] = (finite && k + r < kk) ? ix[k + r] : -1;
+}
+
 constexpr float kLnEps = 1e-5f;
 
 // mean and 1/sqrt(biased variance + eps) of a bf16 row of d (a multiple of 8)
@@ -395,7 +402,9 @@ __global__ void __launch_bounds__(256)
 route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ ebias,
                   const float* __restrict__ noise, int T, int E, int k, int* __restrict__ idx, float* __restrict__ w,
                   int* __restrict__ counts, int raw, float* __restrict__ ent, const bf16* __restrict__ x, int d,
-                  const float* __restrict__ S) {
+                  const float* __restrict__ S, int* __restrict__ backup) {
+  // with backup: the 2k best (at most E), the last k of them the backups
+  const int kk = backup ? min(2 * k, E) : k;
   extern __shared__ int hist_s[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
   __syncthreads();
@@ -422,7 +431,7 @@ route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restr
       if (ebias) v += ebias[e];
       if (nr) v += nr[e];
       if (!isfinite(v)) finite = false;
-      topk_insert(tv, tix, k, v, e);
+      topk_insert(tv, tix, kk, v, e);
       if (need_stat && finite) sst.add(v);
     }
     finite = __all_sync(0xffffffffu, finite);
@@ -440,7 +449,7 @@ route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restr
     int head = 0;  // next unconsumed entry of this lane's list
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
-      if (j < k) {
+      if (j < kk) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
 #pragma unroll
@@ -464,7 +473,10 @@ route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restr
         if (head < MAXK && tix[head] == bi) ++head;
       }
     }
-    if (lane == 0) topk_finish(sel_v, sel_i, k, finite, t, idx, w, hist_s, raw, sst, ent);
+    if (lane == 0) {
+      topk_finish(sel_v, sel_i, k, finite, t, idx, w, hist_s, raw, sst, ent);
+      if (backup) write_backup(sel_i, k, kk, finite, t, backup);
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -475,7 +487,9 @@ route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restr
 __global__ void route_f32_kernel(const float* __restrict__ x, const float* __restrict__ Wr,
                                  const float* __restrict__ ebias, const float* __restrict__ noise, int T, int d,
                                  int E, int k, int* __restrict__ idx, float* __restrict__ w,
-                                 int* __restrict__ counts, int raw, float* __restrict__ ent, int layernorm) {
+                                 int* __restrict__ counts, int raw, float* __restrict__ ent, int layernorm,
+                                 int* __restrict__ backup) {
+  const int kk = backup ? min(2 * k, E) : k;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -503,10 +517,13 @@ __global__ void route_f32_kernel(const float* __restrict__ x, const float* __res
     if (ebias) s += ebias[e];
     if (noise) s += noise[static_cast<size_t>(t) * E + e];
     if (!isfinite(s)) finite = false;
-    topk_insert(tv, tix, k, s, e);
+    topk_insert(tv, tix, kk, s, e);
     if (need_stat && finite) sst.add(s);
   }
-  if (lane == 0) topk_finish(tv, tix, k, finite, t, idx, w, counts, raw, sst, ent);
+  if (lane == 0) {
+    topk_finish(tv, tix, k, finite, t, idx, w, counts, raw, sst, ent);
+    if (backup) write_backup(tix, k, kk, finite, t, backup);
+  }
 }
 
 }  // namespace
@@ -550,11 +567,13 @@ size_t route_scratch_bytes(const moe_config& cfg) {
 }
 
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
-                        const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* err,
-                        cudaStream_t stream) {
+                        const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* backup,
+                        int* err, cudaStream_t stream) {
   const int raw = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0;
   const bool ln = (cfg.route_flags & MOE_ROUTE_LAYERNORM) != 0;
   if (ln && cfg.dtype == MOE_BF16 && !scratch) return MOE_ERR_UNSUPPORTED;  // the fold needs the workspace path
+  if ((cfg.route_flags & MOE_ROUTE_REROUTE) && (!backup || (cfg.dtype == MOE_BF16 && !scratch)))
+    return MOE_ERR_UNSUPPORTED;  // the backups live in the workspace
   moe_status zs = launch_zero(counts, sizeof(int) * cfg.E, err, err ? sizeof(int) : 0, stream);
   if (zs != MOE_OK) return zs;
   if (cfg.dtype == MOE_BF16 && scratch) {
@@ -582,7 +601,7 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     const unsigned grid = static_cast<unsigned>((static_cast<long long>(cfg.T) * 32 + 255) / 256);
     route_topk_kernel<<<grid, 256, sizeof(int) * cfg.E, stream>>>(logits, ld, expert_bias, noise, cfg.T, cfg.E,
                                                                    cfg.k, idx, w, counts, raw, ent,
-                                                                   static_cast<const bf16*>(x), cfg.d, S);
+                                                                   static_cast<const bf16*>(x), cfg.d, S, backup);
   } else if (cfg.dtype == MOE_BF16) {
     const int nep = ((cfg.E < RT_NE ? cfg.E : RT_NE) + 7) / 8 * 8;
     return nep <= 64 ? launch_route_stages<5>(cfg, x, Wr, expert_bias, noise, idx, w, counts, ent, stream)
@@ -592,7 +611,7 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     const long long grid = (static_cast<long long>(cfg.T) * 32 + threads - 1) / threads;
     route_f32_kernel<<<static_cast<unsigned>(grid), threads, 0, stream>>>(
         static_cast<const float*>(x), static_cast<const float*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E,
-        cfg.k, idx, w, counts, raw, ent, ln ? 1 : 0);
+        cfg.k, idx, w, counts, raw, ent, ln ? 1 : 0, backup);
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -50,7 +50,8 @@ class MoeStats(ctypes.Structure):
     _fields_ = [("routed_slots", ctypes.c_longlong), ("kept_slots", ctypes.c_longlong),
                 ("dropped_slots", ctypes.c_longlong), ("capacity", ctypes.c_int),
                 ("numeric_error", ctypes.c_int), ("drop_rate", ctypes.c_double),
-                ("balance_stat", ctypes.c_double), ("router_entropy", ctypes.c_double)]
+                ("balance_stat", ctypes.c_double), ("router_entropy", ctypes.c_double),
+                ("rerouted_slots", ctypes.c_longlong)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -117,22 +118,22 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-ROUTE_RAW_PROBS, ROUTE_TOKEN_MAJOR, ROUTE_LAYERNORM = 1, 2, 4
+ROUTE_RAW_PROBS, ROUTE_TOKEN_MAJOR, ROUTE_LAYERNORM, ROUTE_REROUTE = 1, 2, 4, 8
 BALANCE = {"cv": 0, "std_max": 1, "switch": 2}
 
 
 def make_config(T, d, h, E, k, act="swiglu", dtype="bf16", capacity_factor=0.0, min_capacity=0,
                 lambda_balance=0.01, has_shared=False, raw_probs=False, token_major=False,
-                layernorm=False, balance="cv", balance_gamma=100.0) -> MoeConfig:
+                layernorm=False, balance="cv", balance_gamma=100.0, reroute=False) -> MoeConfig:
     flags = ((ROUTE_RAW_PROBS if raw_probs else 0) | (ROUTE_TOKEN_MAJOR if token_major else 0)
-             | (ROUTE_LAYERNORM if layernorm else 0))
+             | (ROUTE_LAYERNORM if layernorm else 0) | (ROUTE_REROUTE if reroute else 0))
     return MoeConfig(T, d, h, E, k, ACT[act], DTYPE[dtype], capacity_factor, min_capacity,
                      lambda_balance, int(bool(has_shared)), flags, BALANCE[balance], balance_gamma)
 
 
 def config_of(wl, **route) -> MoeConfig:
     """MoeConfig of a moe_synth.Workload (route: raw_probs, token_major,
-    layernorm, balance, balance_gamma)."""
+    layernorm, balance, balance_gamma, reroute)."""
     return make_config(wl.T, wl.d, wl.h, wl.E, wl.k, wl.act, wl.dtype, wl.capacity_factor,
                        wl.min_capacity, wl.lam, wl.has_shared, **route)
 

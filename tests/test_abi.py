@@ -54,7 +54,8 @@ int main(void) {
          offsetof(moe_stats, balance_stat), offsetof(moe_weights, expert_bias));
   printf("%zu %zu %zu %zu\n", offsetof(moe_config, route_flags), offsetof(moe_stats, router_entropy),
          offsetof(moe_saved, Zs), sizeof(moe_grads));
-  printf("%zu %zu\n", offsetof(moe_config, balance), offsetof(moe_config, balance_gamma));
+  printf("%zu %zu %zu\n", offsetof(moe_config, balance), offsetof(moe_config, balance_gamma),
+         offsetof(moe_stats, rerouted_slots));
   return 0;
 }'''
     with tempfile.TemporaryDirectory() as d:
@@ -68,7 +69,8 @@ int main(void) {
            ctypes.sizeof(m.MoeStats), m.MoeConfig.has_shared.offset, m.MoeStats.drop_rate.offset,
            m.MoeStats.balance_stat.offset, m.MoeWeights.expert_bias.offset,
            m.MoeConfig.route_flags.offset, m.MoeStats.router_entropy.offset, m.MoeSaved.Zs.offset,
-           ctypes.sizeof(m.MoeGrads), m.MoeConfig.balance.offset, m.MoeConfig.balance_gamma.offset]
+           ctypes.sizeof(m.MoeGrads), m.MoeConfig.balance.offset, m.MoeConfig.balance_gamma.offset,
+           m.MoeStats.rerouted_slots.offset]
     assert [int(v) for v in out] == got
 
 
@@ -82,7 +84,8 @@ def test_capacity_matches_oracle(M, T, k, E, cf, minc):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(k=5, E=4), 1), (dict(k=9, E=16), 1), (dict(E=1025), 1), (dict(T=0), 1),
-    (dict(d=100), 2), (dict(h=36), 2), (dict(act=7), 1), (dict(route_flags=8), 1), (dict(balance=3), 1),
+    (dict(d=100), 2), (dict(h=36), 2), (dict(act=7), 1), (dict(route_flags=16), 1), (dict(balance=3), 1),
+    (dict(route_flags=8, k=5, E=16), 2),
     (dict(balance_gamma=float("nan")), 1)])
 def test_bad_configs_rejected(M, kw, status):
     base = dict(T=64, d=64, h=64, E=8, k=2)

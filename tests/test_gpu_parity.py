@@ -44,7 +44,7 @@ def check_routing(r, sv, stats, x=None, bal_rtol=1e-12):
     np.testing.assert_array_equal(sv["offsets"].cpu().numpy(), r["offsets"])
     np.testing.assert_array_equal(sv["pos"].cpu().numpy(), r["pos"])
     ref = r["stats"]
-    for key in ("routed_slots", "kept_slots", "dropped_slots", "capacity", "numeric_error"):
+    for key in ("routed_slots", "kept_slots", "dropped_slots", "capacity", "numeric_error", "rerouted_slots"):
         assert stats[key] == ref[key], key
     assert abs(stats["drop_rate"] - ref["drop_rate"]) <= 1e-15
     assert abs(stats["balance_stat"] - ref["balance_stat"]) <= bal_rtol * max(1.0, abs(ref["balance_stat"]))
@@ -514,3 +514,52 @@ def test_balance_statistic_variants(variant):
         assert np.isnan(s2["balance_stat"])
     else:
         assert s2["balance_stat"] == stats["balance_stat"]
+
+
+@pytest.mark.parametrize("tm,k,E,dtype", [(False, 2, 16, "bf16"), (True, 2, 12, "bf16"), (False, 4, 8, "bf16"),
+                                          (False, 2, 4, "f32")])
+def test_reroute_on_overflow(tm, k, E, dtype):
+    """[P3] 2.3's rerouting of the overflow to the next-best expert: with a
+    skewed router and cf 0.8, slots dropped by the first pass try their
+    token's backups; positions, per-expert rows, statistics (with the
+    rerouted count) and the output match the oracle.  moe_route followed by
+    moe_dispatch on the same workspace gives the same placement; the
+    backward refuses the flag."""
+    if dtype == "f32":
+        wl = S.WORKLOADS["tiny_fp32"].replace(T=300, E=E, k=k, capacity_factor=0.8, seed=33)
+    else:
+        wl = S.WORKLOADS["small_prefill"].replace(T=700, d=256, h=256, E=E, k=k, capacity_factor=0.8, seed=33)
+    t = S.make_inputs(wl, DEV)
+    # a router bias that loads the low-index experts, so that the others have room
+    t["expert_bias"] = torch.linspace(1.0, 0.0, E, dtype=torch.float32, device=DEV)
+    # the backups are ranks k .. 2k-1: guard the order of the top 2k+1
+    t = guard(wl.replace(k=2 * k), t)
+    cfg = M.config_of(wl, reroute=True, token_major=tm)
+    sv = M.moe.alloc_saved(cfg)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    y = torch.empty(wl.T, wl.d, dtype=tdt, device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg, 1)
+    weights = {n: t.get(n) for n in WEIGHT_NAMES}
+    M.moe_layer_fwd(cfg, weights, t["x"], None, y, sv, st, ws)
+    assert M.moe_check_error(ws) == 0
+    ocfg = oracle_cfg(wl, reroute=True, token_major=tm)
+    r = O.layer_forward(ocfg, oracle_weights(t), t["x"], t.get("expert_bias"))
+    stats = M.moe.read_stats(st)
+    check_routing(r, sv, stats, t["x"])
+    assert stats["rerouted_slots"] > 0
+    r0 = O.route_and_dispatch(oracle_cfg(wl, token_major=tm), t["x"], t["Wr"], t.get("expert_bias"))
+    assert stats["kept_slots"] == r0["stats"]["kept_slots"] + stats["rerouted_slots"]
+    assert_close_bf16(to_np(y), r["y"], "y")
+    # the standalone calls on one workspace place the slots the same way
+    idx = torch.empty_like(sv["idx"])
+    w = torch.empty_like(sv["w"])
+    counts = torch.empty_like(sv["counts"])
+    M.moe_route(cfg, t["x"], t["Wr"], t.get("expert_bias"), None, idx, w, counts, ws)
+    kept, offs, pos = torch.empty_like(sv["kept"]), torch.empty_like(sv["offsets"]), torch.empty_like(sv["pos"])
+    M.moe_dispatch(cfg, idx, t["x"], kept, offs, pos, torch.empty_like(sv["Xp"]), None, ws)
+    assert torch.equal(pos, sv["pos"]) and torch.equal(kept, sv["kept"]) and torch.equal(offs, sv["offsets"])
+    if dtype == "bf16":
+        with pytest.raises(M.moe.MoeError) as ei:
+            M.moe_layer_bwd(cfg, weights, t["x"], sv, y, M.moe.alloc_grads(cfg), M.moe.workspace(cfg, 2))
+        assert ei.value.status == M.moe.MOE_ERR_UNSUPPORTED

@@ -693,3 +693,75 @@ def test_layer_backward_balance_variants_finite_differences(variant):
         wm["Wr"][e, i] -= hh
         num = (loss(x, wp) - loss(x, wm)) / (2 * hh)
         assert abs(num - g["dWr"][e, i]) <= 1e-6 * max(1.0, abs(num)), (e, i, num, g["dWr"][e, i])
+
+
+def test_reroute_overflow_worked_example():
+    """[P3] 2.3's alternative to dropping: route the overflow to the next-best
+    expert.  T=4, E=3, top-1, C=1: tokens 0-2 all prefer expert 0 (backups
+    1, 1, 2), token 3 prefers expert 1.  Token 0 keeps expert 0; token 1's
+    backup (expert 1) is taken by token 3 in the first pass, so it stays
+    dropped; token 2 moves to expert 2."""
+    l = np.array([[3.0, 2.0, 1.0], [3.0, 2.0, 1.0], [3.0, 1.0, 2.0], [0.0, 3.0, 1.0]])
+    idx, w, _ = O.top_k_route(l, 1)
+    np.testing.assert_array_equal(O.backup_experts(l, 1), [[1], [1], [2], [2]])
+    C = O.expert_capacity(4, 1, 3, 0.75, 0)
+    assert C == 1
+    rank, fill = O.assign_capacity(idx, 3, C)
+    served, rank2, fill2 = O.reroute_overflow(idx, O.backup_experts(l, 1), rank, fill, C)
+    np.testing.assert_array_equal(served[:, 0], [0, -1, 2, 1])
+    np.testing.assert_array_equal(fill2, [0, 0, 1])
+    cfg = dict(T=4, E=3, k=1, capacity_factor=0.75, reroute=True)
+    r = O.route_and_dispatch(cfg, l, np.eye(3))
+    np.testing.assert_array_equal(r["pos"][:, 0], [0, -1, 2, 1])
+    np.testing.assert_array_equal(r["kept"], [1, 1, 1])
+    assert r["stats"]["rerouted_slots"] == 1 and r["stats"]["kept_slots"] == 3
+    # without the flag token 2 is dropped too
+    r0 = O.route_and_dispatch(dict(cfg, reroute=False), l, np.eye(3))
+    np.testing.assert_array_equal(r0["pos"][:, 0], [0, -1, -1, 1])
+
+
+@pytest.mark.parametrize("T,E,k,cf,tm", [(300, 8, 2, 0.8, False), (200, 6, 3, 0.6, True), (150, 5, 2, 1.0, False),
+                                         (64, 3, 2, 0.5, False)])
+def test_reroute_properties(T, E, k, cf, tm):
+    """On random skewed logits: the first pass is untouched (every slot kept
+    without rerouting keeps its expert and place order); no expert exceeds
+    C; a rerouted slot is served by the token's backup of its drop order,
+    never by an expert the token already uses; for each expert the rerouted
+    slots are exactly the first (C - first-pass rows) candidates aimed at it
+    in priority order (greedy); rerouting never lowers the kept count."""
+    rng = _rng(91 + T)
+    l = rng.normal(size=(T, E)) + np.linspace(2.0, 0.0, E)[None, :]
+    cfg = dict(T=T, E=E, k=k, capacity_factor=cf, token_major=tm)
+    r0 = O.route_and_dispatch(cfg, l, np.eye(E))
+    r1 = O.route_and_dispatch(dict(cfg, reroute=True), l, np.eye(E))
+    C = r0["capacity"]
+    idx, b = r1["idx"], r1["backup"]
+    assert (r1["kept"] <= C).all() and r1["kept"].sum() >= r0["kept"].sum()
+    assert r1["stats"]["rerouted_slots"] == r1["kept"].sum() - r0["kept"].sum()
+    first = r0["pos"] >= 0
+    np.testing.assert_array_equal(r1["served"][first], idx[first])
+    # each expert's rows: first-pass rows in their order, then rerouted rows
+    for e in range(E):
+        o0, o1 = r1["offsets"][e], r1["offsets"][e + 1]
+        mine = np.nonzero((r1["served"] == e) & (r1["pos"] >= 0))
+        got = np.sort(r1["pos"][mine])
+        np.testing.assert_array_equal(got, np.arange(o0, o1))
+    order = [(t, j) for t in range(T) for j in range(k)] if tm else [(t, j) for j in range(k) for t in range(T)]
+    cand = {e: [] for e in range(E)}
+    for t in range(T):
+        r = 0
+        for j in range(k):
+            if not first[t, j]:
+                if b[t, r] >= 0:
+                    assert b[t, r] not in idx[t]
+                    cand[b[t, r]].append((t, j))
+                if r1["pos"][t, j] >= 0:
+                    assert r1["served"][t, j] == b[t, r]
+                r += 1
+    for e in range(E):
+        room = C - int(first[idx == e].sum())
+        ranked = sorted(cand[e], key=order.index)
+        taken = {(t, j) for (t, j) in ranked[:max(room, 0)]}
+        got = {(t, j) for t, j in zip(*np.nonzero((r1["served"] == e) & ~first))}
+        assert got == taken, e
+    assert r1["stats"]["rerouted_slots"] > 0
