@@ -473,6 +473,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-training", action="store_true")
+    ap.add_argument("--no-fine-grained", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
@@ -568,6 +569,38 @@ def main():
                           "components_ms": {k: round(v, 4) for k, v in d["components_ms"].items()},
                           "clocks": d["clocks"]}
         del d["tensors"]
+    if not args.no_fine_grained:
+        # fine-grained routing: E=384 top-6 + shared, ~128 rows per expert;
+        # its expert weights (9.7 GB) take longer to stream than its FLOPs
+        # take on the tensor cores, so both fractions are reported
+        fargs = argparse.Namespace(**vars(args))
+        fargs.steps = max(args.steps, 40)
+        f = run_gpu(fargs, "fine_grained", world, rank, local)
+        fwl = f["wl"]
+        ffn_ms = f["components_ms"]["expert_ffn"]
+        fflops = expert_ffn_flops(fwl, f["stats"]["kept_slots"]) + shared_flops(fwl)
+        # algorithmic bytes of the two grouped GEMMs: the touched weights once,
+        # plus per row (kept slots and the shared expert's T rows) its input
+        # row read, its hidden row written and read back, its output row written
+        rows = f["stats"]["kept_slots"] + (fwl.T if fwl.has_shared else 0)
+        act_bytes = rows * 2 * (2 * fwl.d + 2 * fwl.h)
+        fbytes = f["touched_weight_bytes"] + act_bytes
+        gbs = fbytes / (ffn_ms * 1e-3) / 1e9
+        t_roof = max(fflops / (peak * 1e12), fbytes / (peaks["hbm_gbs"] * 1e9))
+        line["fine_grained"] = {
+            "workload": f"fine_grained: T={fwl.T} d={fwl.d} h={fwl.h} E={fwl.E}+1 shared top-{fwl.k} "
+                        f"cf={fwl.capacity_factor} {fwl.dtype}",
+            "ms_per_step": f["ms_per_step"], "tokens_per_s": f["tokens_per_s"], "e2e": f["e2e"],
+            "kept_slots": f["stats"]["kept_slots"], "touched_experts": f["n_touched"] + 1,
+            "touched_weight_gb": f["touched_weight_bytes"] / 1e9, "activation_gb": act_bytes / 1e9,
+            "expert_ffn_ms": ffn_ms,
+            "gemm_tflops": fflops / (ffn_ms * 1e-3) / 1e12,
+            "gemm_frac_of_sustained": fflops / (ffn_ms * 1e-3) / 1e12 / peak,
+            "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+            "expert_ffn_roofline_frac": t_roof / (ffn_ms * 1e-3),
+            "components_ms": {k: round(v, 4) for k, v in f["components_ms"].items()},
+            "clocks": f["clocks"]}
+        del f["tensors"]
     if not args.no_training:
         tr = run_training(args, world, rank, local)
         tr["frac_of_sustained"] = tr["tflops"] / peaks["bf16_sus"]

@@ -563,3 +563,36 @@ def test_reroute_on_overflow(tm, k, E, dtype):
         with pytest.raises(M.moe.MoeError) as ei:
             M.moe_layer_bwd(cfg, weights, t["x"], sv, y, M.moe.alloc_grads(cfg), M.moe.workspace(cfg, 2))
         assert ei.value.status == M.moe.MOE_ERR_UNSUPPORTED
+
+
+def test_top1_routing_forward_and_backward():
+    """k = 1, the baseline [P3] 5.3 says to run first: every routed token's
+    weight is exactly 1; routing, dispatch, statistics and output match the
+    oracle, and so do the backward's gradients (the logit gradient of a
+    one-expert softmax is 0, so no gradient reaches the router: dWr = 0)."""
+    wl = S.WORKLOADS["training"].replace(T=512, d=256, h=384, E=8, k=1, capacity_factor=1.0, gumbel=False,
+                                        has_shared=False, lam=0.5, seed=37)
+    t = guarded_inputs(wl, "cpu")
+    dY = t.pop("dY")
+    td = {n: v.to(DEV) for n, v in t.items()}
+    cfg = M.config_of(wl)
+    weights = {n: td.get(n) for n in WEIGHT_NAMES}
+    sv = M.moe.alloc_saved(cfg, DEV, backward=True)
+    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg, 1)
+    M.moe_layer_fwd(cfg, weights, td["x"], None, y, sv, st, ws)
+    assert M.moe_check_error(ws) == 0
+    r = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"])
+    check_routing(r, sv, M.moe.read_stats(st), td["x"])
+    assert (sv["w"] == 1.0).all()
+    assert_close_bf16(to_np(y), r["y"], "y")
+    g = M.moe.alloc_grads(cfg)
+    M.moe_layer_bwd(cfg, weights, td["x"], sv, dY.to(DEV), g, M.moe.workspace(cfg, 2))
+    ref = O.layer_backward(oracle_cfg(wl), {n: t[n] for n in ("Wr", "W1", "W3", "W2")}, t["x"], dY)
+    assert not g["dWr"].any() and not ref["dWr"].any()
+    dX = g["dX"].cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(dX - ref["dX"]) <= 1e-2 * np.linalg.norm(ref["dX"])
+    for name in ("dW1", "dW3", "dW2"):
+        got = g[name].cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(got - ref[name]) <= 1e-2 * np.linalg.norm(ref[name]), name
