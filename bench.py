@@ -49,7 +49,7 @@ WEIGHTS = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2"
 # figure is reported only while the source is unchanged)
 GEMM_TRAFFIC = {
     # profiles/grouped_gemm_large_prefill_slice.md
-    "2f60f6a57b7cf033b9dd5891b6d4469f81674a649458e68b98fcb4559d98cf53": 12.37e9,
+    "cb7f072115f3683c88d5aea8778b9784200810094c8f76cbbd97eca4f34114eb": 12.37e9,
 }
 
 

@@ -208,6 +208,11 @@ WORKLOADS: Dict[str, Workload] = {
     # cf=1.25 (C=160)
     "fine_grained": Workload("fine_grained", 8192, 4096, 1024, 384, 6, "swiglu", "bf16", 1.25, 0,
                              0.01, True, 5, None, None, False, False),
+    # 96 experts of the fine-grained layer at its rows per expert (~128) plus
+    # the shared expert: the same GEMM tile shapes at a quarter of the
+    # weights (profiling case)
+    "fine_grained_slice": Workload("fine_grained_slice", 2048, 4096, 1024, 96, 6, "swiglu", "bf16", 1.25, 0,
+                                   0.01, True, 5, None, None, False, False),
     # T=64, d=4096, E=128 routed + 1 shared, SwiGLU h=8192, no capacity limit
     "decode": Workload("decode", 64, 4096, 8192, 128, 2, "swiglu", "bf16", 0.0, 0, 0.01,
                        True, 3, None, None, False, False),

@@ -104,24 +104,31 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
   __shared__ int unrouted;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  // per expert (one warp each), exclusive scan of its chunk counts across
-  // chunks, 32 chunks a step; expert E is the "unrouted" column
+  // per expert, exclusive scan of its chunk counts across chunks; expert E
+  // is the "unrouted" column.  L lanes per expert (as many as fit all E+1
+  // columns into the block at once, at most a warp) take L chunks a step;
+  // the loops are uniform per warp, lanes past column E carry zeros.
+  int L = 32;
+  while (L > 1 && (E + 1) * L > static_cast<int>(blockDim.x)) L >>= 1;
+  const int gpw = 32 / L;  // experts per warp
+  const int sub = lane / L, gl = lane - (lane / L) * L;
   const int nwarps = blockDim.x >> 5;
-  for (int e = warp; e <= E; e += nwarps) {
+  for (int e0 = warp * gpw; e0 <= E; e0 += nwarps * gpw) {
+    const int e = e0 + sub;
+    const bool ev = e <= E;
     int carry = 0;
-    for (int b0 = 0; b0 < nb; b0 += 32) {
-      const int b = b0 + lane;
-      const int v = b < nb ? blockhist[static_cast<size_t>(b) * (E + 1) + e] : 0;
+    for (int b0 = 0; b0 < nb; b0 += L) {
+      const int b = b0 + gl;
+      const int v = (ev && b < nb) ? blockhist[static_cast<size_t>(b) * (E + 1) + e] : 0;
       int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
+      for (int o = 1; o < L; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o, L);
+        if (gl >= o) incl += u;
       }
-      if (e < E && b < nb) base[static_cast<size_t>(b) * E + e] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+      if (ev && e < E && b < nb) base[static_cast<size_t>(b) * E + e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, L - 1, L);
     }
-    if (lane == 0) {
+    if (ev && gl == 0) {
       if (e < E) tot[e] = carry;
       else unrouted = carry;
     }
@@ -349,6 +356,7 @@ __global__ void permute_kernel(const V* __restrict__ x, int T, int k, int vec_pe
 
 // One warp per (token, column chunk): y[t] = sum_j w[t,j] Yp[pos[t,j]]
 // (+ Sx[t]); 8 bf16 per lane step.
+template <int KM>  // slots per token rounded up to 2, 4 or 8 (register arrays)
 __global__ void combine_bf16_kernel(const uint4* __restrict__ Yp, const int* __restrict__ pos,
                                     const float* __restrict__ w, const uint4* __restrict__ Sx, int T, int k,
                                     int vec_per_row, int chunks, uint4* __restrict__ y) {
@@ -357,24 +365,29 @@ __global__ void combine_bf16_kernel(const uint4* __restrict__ Yp, const int* __r
   const int ch = static_cast<int>(wid - static_cast<long long>(t) * chunks);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  int p[8];
-  float wt[8];
+  int p[KM];
+  float wt[KM];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < KM; ++j) {
     p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
     wt[j] = j < k ? w[static_cast<size_t>(t) * k + j] : 0.f;
   }
   const int per = (vec_per_row + chunks - 1) / chunks;
   const int v1 = min(vec_per_row, (ch + 1) * per);
   for (int v = ch * per + lane; v < v1; v += 32) {
+    // every row's 16 bytes are requested before the first is used
+    uint4 q[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      q[j] = p[j] >= 0 ? Yp[static_cast<size_t>(p[j]) * vec_per_row + v] : make_uint4(0, 0, 0, 0);
+    const uint4 qs = Sx ? Sx[static_cast<size_t>(t) * vec_per_row + v] : make_uint4(0, 0, 0, 0);
     float a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KM; ++j) {
       if (p[j] >= 0) {
-        const uint4 q = Yp[static_cast<size_t>(p[j]) * vec_per_row + v];
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+        const uint32_t u[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           a[2 * i] = fmaf(wt[j], bf16lo(u[i]), a[2 * i]);
@@ -383,8 +396,7 @@ __global__ void combine_bf16_kernel(const uint4* __restrict__ Yp, const int* __r
       }
     }
     if (Sx) {
-      const uint4 q = Sx[static_cast<size_t>(t) * vec_per_row + v];
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+      const uint32_t u[4] = {qs.x, qs.y, qs.z, qs.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         a[2 * i] += bf16lo(u[i]);
@@ -575,9 +587,15 @@ moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos,
                           void* y, cudaStream_t stream) {
   if (cfg.dtype == MOE_BF16) {
     const int ch = row_chunks(cfg.T, cfg.d / 8);
-    combine_bf16_kernel<<<warp_grid(cfg.T, ch), 256, 0, stream>>>(static_cast<const uint4*>(Yp), pos, w,
-                                                                  static_cast<const uint4*>(Sx), cfg.T, cfg.k,
-                                                                  cfg.d / 8, ch, static_cast<uint4*>(y));
+    const uint4* yp = static_cast<const uint4*>(Yp);
+    const uint4* sx = static_cast<const uint4*>(Sx);
+    uint4* yo = static_cast<uint4*>(y);
+    if (cfg.k <= 2)
+      combine_bf16_kernel<2><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(yp, pos, w, sx, cfg.T, cfg.k, cfg.d / 8, ch, yo);
+    else if (cfg.k <= 4)
+      combine_bf16_kernel<4><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(yp, pos, w, sx, cfg.T, cfg.k, cfg.d / 8, ch, yo);
+    else
+      combine_bf16_kernel<8><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(yp, pos, w, sx, cfg.T, cfg.k, cfg.d / 8, ch, yo);
   } else {
     combine_f32_kernel<<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const float*>(Yp), pos, w,
                                                              static_cast<const float*>(Sx), cfg.T, cfg.k, cfg.d,

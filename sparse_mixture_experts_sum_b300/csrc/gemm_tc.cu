@@ -98,19 +98,27 @@ struct Tile {
 
 // Tile index -> (group, n-tile, m-tile).  Fwd/Dgrad: a group has
 // ceil(rows/BM) m-tiles per n-tile, m fastest.  Wgrad: every group has
-// m_tiles x n_tiles tiles, n fastest when n_fast.
+// m_tiles x n_tiles tiles, n fastest when n_fast.  The extra group's X
+// tiles (the shared expert: many rows on one weight set, so bound by the
+// tensor cores where the routed groups stream weights) are spread evenly
+// through the schedule of N tiles: slot s holds extra tile floor(s X / N)
+// when that count steps at s, else routed tile s - floor(s X / N).
 template <int KIND, int BM, typename C>
 __device__ __forceinline__ Tile tile_coords(const C& c, int G, int n_tiles, int m_tiles, bool n_fast, int tile,
                                             int xrows) {
-  if (KIND == kKindFwd && tile >= c.x_tile0) {
-    // the extra group (g = G): ceil(xrows/BM) m-tiles per n-tile, m fastest
-    const int local = tile - c.x_tile0;
-    const int mt = (xrows + BM - 1) / BM;
-    Tile t;
-    t.g = G;
-    t.n = local / mt;
-    t.m = local - t.n * mt;
-    return t;
+  if (KIND == kKindFwd && c.total_tiles > c.x_tile0) {
+    const long long NT = c.total_tiles, XT = NT - c.x_tile0;
+    const long long before = static_cast<long long>(tile) * XT / NT;
+    if ((static_cast<long long>(tile) + 1) * XT / NT > before) {
+      const int local = static_cast<int>(before);
+      const int mt = (xrows + BM - 1) / BM;
+      Tile t;
+      t.g = G;
+      t.n = local / mt;
+      t.m = local - t.n * mt;
+      return t;
+    }
+    tile -= static_cast<int>(before);
   }
   int lo = 0, hi = G;  // largest g with tile_start[g] <= tile (a group with tiles)
   while (hi - lo > 1) {
