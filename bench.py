@@ -129,6 +129,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(ms, world, device):
+    """The job's time for a region every rank times between two barriers:
+    the slowest rank's (replicas do no collective in their own steps)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_max):
+    """Whole-job rate: the units all ranks processed over the slowest
+    rank's time (units per second)."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
@@ -231,16 +248,12 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
         for j, (name, _) in enumerate(stages):
             comp[name] += prev.elapsed_time(evs[i][j]) / steps
             prev = evs[i][j]
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / steps
     layer_fwd_ms = ms_step
     assert M.moe_check_error(ws) == 0, "a kernel gave up a bounded wait"
 
     peaks = load_peaks()
-    tokens = wl.T * world
     out = {
         "ms_per_step": ms_step,
         "layer_fwd_ms": layer_fwd_ms,
@@ -250,7 +263,7 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
         # path = the same without the entropy mean, plus moe_expert_ffn's
         # zeroing of the error word (11)
         "launches_per_step": 22,
-        "tokens_per_s": tokens / (ms_step * 1e-3),
+        "tokens_per_s": job_throughput(wl.T, world, ms_step),
         "stats": stats,
         "components_ms": comp,
         "clocks": clocks,
@@ -317,13 +330,10 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     e2e1.record(cstream)
     barrier()
     e2e_ms = e2e0.elapsed_time(e2e1) / n_e2e
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     yh = yh[0]
     h2d = xh.numel() * xh.element_size() + (nh.numel() * nh.element_size() if nh is not None else 0)
-    out["e2e"] = {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    out["e2e"] = {"value": job_throughput(wl.T, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                   "d2h_bytes_per_step": yh.numel() * yh.element_size()}
     out["peaks"] = peaks
     out["tensors"] = dict(t=t, saved=saved)
@@ -367,8 +377,13 @@ def run_training(args, world, rank, local):
     steps = max(3, min(args.steps, 10))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     sampler = ClockSampler(local)
-    with sampler:
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
         torch.cuda.synchronize(dev)
+
+    with sampler:
+        barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(steps):
@@ -376,7 +391,7 @@ def run_training(args, world, rank, local):
             ev[i][0].record(stream)
             bwd()
             ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
+        barrier()
     assert M.moe_check_error(ws_b) == 0
     f_ms = b_ms = 0.0
     prev = e0
@@ -384,15 +399,17 @@ def run_training(args, world, rank, local):
         f_ms += prev.elapsed_time(a) / steps
         b_ms += a.elapsed_time(b) / steps
         prev = b
+    # the job's step is the slowest rank's; the halves are reported as this rank measured them
+    step_ms = max_over_ranks(f_ms + b_ms, world, dev)
     kept = stats["kept_slots"]
     per = 2.0 * wl.d * wl.h * (3 if wl.act == "swiglu" else 2)
     fwd_flops = per * (kept + (wl.T if wl.has_shared else 0)) + 2.0 * wl.T * wl.d * wl.E
     bwd_flops = 2.0 * per * (kept + (wl.T if wl.has_shared else 0)) + 4.0 * wl.T * wl.d * wl.E
     return {"workload": f"training: T={wl.T} d={wl.d} h={wl.h} E={wl.E}+1 shared top-{wl.k} {wl.act} "
                         f"cf={wl.capacity_factor} gumbel bf16, fp32 grads",
-            "steps": steps, "ms_per_step": f_ms + b_ms, "fwd_ms": f_ms, "bwd_ms": b_ms,
-            "tokens_per_s": wl.T / ((f_ms + b_ms) * 1e-3),
-            "tflops": (fwd_flops + bwd_flops) / ((f_ms + b_ms) * 1e-3) / 1e12,
+            "steps": steps, "ms_per_step": step_ms, "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "tokens_per_s": job_throughput(wl.T, world, step_ms),
+            "tflops": (fwd_flops + bwd_flops) * world / (step_ms * 1e-3) / 1e12,
             "bwd_tflops": bwd_flops / (b_ms * 1e-3) / 1e12, "kept_slots": kept,
             "clocks": sampler.summary()}
 
@@ -603,7 +620,7 @@ def main():
         del f["tensors"]
     if not args.no_training:
         tr = run_training(args, world, rank, local)
-        tr["frac_of_sustained"] = tr["tflops"] / peaks["bf16_sus"]
+        tr["frac_of_sustained"] = tr["tflops"] / (peaks["bf16_sus"] * world)  # per GPU
         line["training"] = tr
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import moe_synth as S
