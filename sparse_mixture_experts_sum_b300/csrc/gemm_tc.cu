@@ -638,12 +638,26 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
                            long long b_rows, long long avg_rows, const GemmExtra* extra, cudaStream_t stream) {
   // BM = 256 feeds the tensor cores with 2/3 of the shared-memory traffic
   // per MAC but has a single accumulator, so its epilogue does not overlap
-  // the next tile's MMAs: take it for the light (plain) epilogues only.
-  const bool tall = avg_rows >= 256 && p.mode == kModePlain;
+  // the next tile's MMAs: take it for the light (plain) epilogues only, and
+  // only when it still gives every SM a tile (a single-group launch such as
+  // the router's logits would otherwise leave most SMs idle).
+  const long long n_tiles = (KIND == kKindFwd && p.mode == kModeSwiGLU) ? (p.N + 127) / 128 : (p.N + BN - 1) / BN;
+  auto tiles_for = [&](int bm) -> long long {
+    if (KIND == kKindWgrad) return static_cast<long long>(p.G) * ((p.M + bm - 1) / bm) * n_tiles;
+    const long long rows_bound = p.offsets ? a_rows : p.rows;
+    long long tl = ((rows_bound + bm - 1) / bm + (p.offsets ? p.G : 0)) * n_tiles;
+    if (KIND == kKindFwd && p.xrows > 0) tl += ((p.xrows + bm - 1) / bm) * n_tiles;
+    return tl;
+  };
+  bool tall = avg_rows >= 256 && p.mode == kModePlain;
+  if (tall) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (tiles_for(256) < device_sm_count(dev)) tall = false;
+  }
   const int BMv = tall ? 256 : 128;
   CUtensorMap mA, mB0, mB1, mXA, mXB0, mXB1;
-  const long long n_tiles = (KIND == kKindFwd && p.mode == kModeSwiGLU) ? (p.N + 127) / 128 : (p.N + BN - 1) / BN;
-  long long tiles = 0;
+  const long long tiles = tiles_for(BMv);
   if (KIND == kKindFwd) {
     if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BMv)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mB0, B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
@@ -666,13 +680,6 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
     mXA = mA;
     mXB0 = mB0;
     mXB1 = mB1;
-  }
-  if (KIND == kKindWgrad) {
-    tiles = static_cast<long long>(p.G) * ((p.M + BMv - 1) / BMv) * n_tiles;
-  } else {
-    const long long rows_bound = p.offsets ? a_rows : p.rows;
-    tiles = ((rows_bound + BMv - 1) / BMv + (p.offsets ? p.G : 0)) * n_tiles;
-    if (KIND == kKindFwd && p.xrows > 0) tiles += ((p.xrows + BMv - 1) / BMv) * n_tiles;
   }
   return tall ? launch_kind<KIND, 256>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream)
               : launch_kind<KIND, 128>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream);

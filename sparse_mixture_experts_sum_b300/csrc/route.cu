@@ -132,7 +132,9 @@ __device__ __forceinline__ void topk_finish(const float (&v)[MAXK], const int (&
 // of the sorted list (kk <= 2k), -1 past kk or for a non-finite token.
 __device__ __forceinline__ void write_backup(const int (&ix)[MAXK], int k, int kk, bool finite, int t,
                                              int* backup) {
-  for (int r = 0; r < k; ++r) backup[static_cast<size_t>(t) * k + r] = (finite && k + r < kk) ? ix[k + r] : -1;
+#pragma unroll
+  for (int q = 0; q < MAXK; ++q)  // static indices keep ix in registers
+    if (q >= k && q < 2 * k) backup[static_cast<size_t>(t) * k + (q - k)] = (finite && q < kk) ? ix[q] : -1;
 }
 
 constexpr float kLnEps = 1e-5f;
@@ -393,84 +395,109 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
 // Top-k of precomputed logits (row stride ld), one warp per token:
 // l[t,e] = logits[t,e] (+ bias[e]) (+ noise[t,e]); with S (LayerNorm before
 // the router) the stored value is x_t . Wr[e] and l[t,e] = r_t (logits[t,e]
-// - mu_t S[e]) (+ ...), mu_t and r_t from the row x_t.  Each lane keeps the
-// top-k of its experts (e = lane, lane+32, ... in increasing order), then k
-// rounds of a warp argmax by (value desc, index asc) merge the lanes'
-// lists.  Lane 0 writes idx, the renormalised weights and the block
+// - mu_t S[e]) (+ ...), mu_t and r_t from the row x_t.  Lane i holds the
+// logits of experts i, i+32, ... (NV per lane, -inf past E).  The softmax
+// statistics come from one warp max m and then sums of exp(l - m); the
+// top-k from k rounds of a warp argmax by (value desc, index asc), each
+// round retiring its winner.  Lane 0 writes idx, the weights and the block
 // histogram.
+template <int NV>
 __global__ void __launch_bounds__(256)
 route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ ebias,
                   const float* __restrict__ noise, int T, int E, int k, int* __restrict__ idx, float* __restrict__ w,
                   int* __restrict__ counts, int raw, float* __restrict__ ent, const bf16* __restrict__ x, int d,
                   const float* __restrict__ S, int* __restrict__ backup) {
-  // with backup: the 2k best (at most E), the last k of them the backups
-  const int kk = backup ? min(2 * k, E) : k;
   extern __shared__ int hist_s[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
   __syncthreads();
+  // with backup: the 2k best (at most E), the last k of them the backups
+  const int kk = backup ? min(2 * k, E) : k;
   const int lane = threadIdx.x & 31;
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   if (t < T) {
-    float tv[MAXK];
-    int tix[MAXK];
-#pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
-      tv[j] = -INFINITY;
-      tix[j] = -1;
-    }
-    bool finite = true;
-    const bool need_stat = raw || ent;
-    SoftStat sst;
     float mu = 0.f, r = 1.f;
     if (S) row_stats_bf16(x + static_cast<size_t>(t) * d, d, mu, r);
     const float* lr = logits + static_cast<size_t>(t) * ld;
     const float* nr = noise ? noise + static_cast<size_t>(t) * E : nullptr;
-    for (int e = lane; e < E; e += 32) {
-      float v = lr[e];
-      if (S) v = r * fmaf(-mu, S[e], v);
-      if (ebias) v += ebias[e];
-      if (nr) v += nr[e];
-      if (!isfinite(v)) finite = false;
-      topk_insert(tv, tix, kk, v, e);
-      if (need_stat && finite) sst.add(v);
-    }
-    finite = __all_sync(0xffffffffu, finite);
-    if (need_stat && finite) {
+    float v[NV];
+    bool finite = true;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, sst.m, o);
-        const float Z2 = __shfl_xor_sync(0xffffffffu, sst.Z, o);
-        const float S2 = __shfl_xor_sync(0xffffffffu, sst.S, o);
-        sst.merge(m2, Z2, S2);
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = -INFINITY;
+      if (e < E) {
+        float a = lr[e];
+        if (S) a = r * fmaf(-mu, S[e], a);
+        if (ebias) a += ebias[e];
+        if (nr) a += nr[e];
+        if (!isfinite(a)) finite = false;
+        v[i] = a;
       }
     }
+    finite = __all_sync(0xffffffffu, finite);
+    SoftStat sst;
     float sel_v[MAXK];
     int sel_i[MAXK];
-    int head = 0;  // next unconsumed entry of this lane's list
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
-      if (j < kk) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+      sel_v[j] = -INFINITY;
+      sel_i[j] = -1;
+    }
+    if (finite) {
+      if (raw || ent) {
+        float m = v[0];
 #pragma unroll
-        for (int q = 0; q < MAXK; ++q)
-          if (q == head && tix[q] >= 0) {
-            bv = tv[q];
-            bi = tix[q];
-          }
+        for (int i = 1; i < NV; ++i) m = fmaxf(m, v[i]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float z = 0.f, sz = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          if (lane + 32 * i < E) {
+            const float dv = v[i] - m;
+            const float ex = expf(dv);
+            z += ex;
+            sz = fmaf(ex, dv, sz);
           }
         }
-        sel_v[j] = bv;
-        sel_i[j] = bi;
-        // the lane that held the winner advances its list
-        if (head < MAXK && tix[head] == bi) ++head;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          z += __shfl_xor_sync(0xffffffffu, z, o);
+          sz += __shfl_xor_sync(0xffffffffu, sz, o);
+        }
+        sst.m = m;
+        sst.Z = z;
+        sst.S = sz;
+      }
+#pragma unroll
+      for (int j = 0; j < MAXK; ++j) {
+        if (j < kk) {
+          // this lane's best remaining (the first of equal values: lower expert)
+          float bv = v[0];
+          int bi = lane;
+#pragma unroll
+          for (int i = 1; i < NV; ++i)
+            if (v[i] > bv) {
+              bv = v[i];
+              bi = lane + 32 * i;
+            }
+          if (bv == -INFINITY) bi = 0x7fffffff;  // nothing left in this lane
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+              bv = ov;
+              bi = oi;
+            }
+          }
+          sel_v[j] = bv;
+          sel_i[j] = bi;
+          // the lane that held the winner retires it
+#pragma unroll
+          for (int i = 0; i < NV; ++i)
+            if (lane + 32 * i == bi) v[i] = -INFINITY;
+        }
       }
     }
     if (lane == 0) {
@@ -599,9 +626,19 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     moe_status s = launch_grouped_gemm_tc(g, kKindFwd, x, cfg.T, Wr, nullptr, cfg.E, stream);
     if (s != MOE_OK) return s;
     const unsigned grid = static_cast<unsigned>((static_cast<long long>(cfg.T) * 32 + 255) / 256);
-    route_topk_kernel<<<grid, 256, sizeof(int) * cfg.E, stream>>>(logits, ld, expert_bias, noise, cfg.T, cfg.E,
-                                                                   cfg.k, idx, w, counts, raw, ent,
-                                                                   static_cast<const bf16*>(x), cfg.d, S, backup);
+    const bf16* xb = static_cast<const bf16*>(x);
+    const size_t hs = sizeof(int) * cfg.E;
+    const int nv = (cfg.E + 31) / 32;
+#define MOE_TOPK(NVv)                                                                                        \
+  route_topk_kernel<NVv><<<grid, 256, hs, stream>>>(logits, ld, expert_bias, noise, cfg.T, cfg.E, cfg.k, idx, w, \
+                                                     counts, raw, ent, xb, cfg.d, S, backup)
+    if (nv <= 1) MOE_TOPK(1);
+    else if (nv <= 2) MOE_TOPK(2);
+    else if (nv <= 4) MOE_TOPK(4);
+    else if (nv <= 8) MOE_TOPK(8);
+    else if (nv <= 16) MOE_TOPK(16);
+    else MOE_TOPK(32);
+#undef MOE_TOPK
   } else if (cfg.dtype == MOE_BF16) {
     const int nep = ((cfg.E < RT_NE ? cfg.E : RT_NE) + 7) / 8 * 8;
     return nep <= 64 ? launch_route_stages<5>(cfg, x, Wr, expert_bias, noise, idx, w, counts, ent, stream)
