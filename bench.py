@@ -49,7 +49,7 @@ WEIGHTS = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2"
 # figure is reported only while the source is unchanged)
 GEMM_TRAFFIC = {
     # profiles/grouped_gemm_large_prefill_slice.md
-    "cb7f072115f3683c88d5aea8778b9784200810094c8f76cbbd97eca4f34114eb": 12.37e9,
+    "60216de4f5163834f35f4ef06dc060962625ca2a65f0a5176ac42066576cbf9f": 12.35e9,
 }
 
 

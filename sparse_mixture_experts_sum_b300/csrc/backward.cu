@@ -35,16 +35,18 @@ namespace {
 constexpr double kImpScale = 4294967296.0;  // routing weights accumulate as 2^-32 fixed point
 
 // One warp per token: dot[t,j] = <dY[t], Yp[pos]>, dYp[pos] = w[t,j] dY[t].
+// KM = k rounded up to 2, 4 or 8 sizes the per-slot register arrays.
+template <int KM>
 __global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ Yp,
                                   const int* __restrict__ pos, const float* __restrict__ w, int T, int k,
                                   int vec_per_row, uint4* __restrict__ dYp, float* __restrict__ dot) {
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  int p[8];
-  float wt[8], acc[8];
+  int p[KM];
+  float wt[KM], acc[KM];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < KM; ++j) {
     p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
     wt[j] = j < k ? w[static_cast<size_t>(t) * k + j] : 0.f;
     acc[j] = 0.f;
@@ -53,7 +55,7 @@ __global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __r
     const uint4 q = dY[static_cast<size_t>(t) * vec_per_row + v];
     const uint32_t g[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KM; ++j) {
       if (p[j] < 0) continue;
       const uint4 yq = Yp[static_cast<size_t>(p[j]) * vec_per_row + v];
       const uint32_t y[4] = {yq.x, yq.y, yq.z, yq.w};
@@ -68,7 +70,7 @@ __global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __r
     }
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < KM; ++j) {
     float s = acc[j];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -409,8 +411,9 @@ __global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, in
 }
 
 // One warp per token: dX[t] (+)= sum_{kept j} dXp[pos] + sum_j dl[t,j] Wr[idx_j] (fp32, j ascending)
-// (- A_t - B_t (x[t] - mu_t) with LayerNorm before the router: lnc non-null).
-template <typename Tw>
+// (- A_t - B_t (x[t] - mu_t) with LayerNorm before the router: LN, lnc).
+// KM = k rounded up to 2, 4 or 8 sizes the per-slot register arrays.
+template <typename Tw, int KM, bool LN>
 __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restrict__ pos, const int* __restrict__ idx,
                               const float* __restrict__ dl, const Tw* __restrict__ Wr, int T, int k, int d, int E,
                               const Tw* __restrict__ x, const float* __restrict__ lnc, int accumulate,
@@ -418,17 +421,17 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  int p[8], e[8];
-  float g[8];
+  int p[KM], e[KM];
+  float g[KM];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < KM; ++j) {
     p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
     e[j] = j < k ? idx[static_cast<size_t>(t) * k + j] : -1;
     g[j] = j < k ? dl[static_cast<size_t>(t) * k + j] : 0.f;
   }
   float* out = dX + static_cast<size_t>(t) * d;
   float lmu = 0.f, lA = 0.f, lB = 0.f;
-  if (lnc) {
+  if (LN) {
     lmu = lnc[t];
     lA = lnc[static_cast<size_t>(T) + t];
     lB = lnc[2 * static_cast<size_t>(T) + t];
@@ -437,7 +440,7 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
   for (int c = lane * 4; c < d; c += 128) {
     float4 a = accumulate ? *reinterpret_cast<const float4*>(out + c) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KM; ++j) {
       if (p[j] >= 0) {
         const float4 v = *reinterpret_cast<const float4*>(dXp + static_cast<size_t>(p[j]) * d + c);
         a.x += v.x;
@@ -447,7 +450,7 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
       }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KM; ++j) {
       if (e[j] >= 0 && e[j] < E) {
         const Tw* wr = Wr + static_cast<size_t>(e[j]) * d + c;
         float w0, w1, w2, w3;
@@ -468,7 +471,7 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
         a.w = fmaf(g[j], w3, a.w);
       }
     }
-    if (lnc) {
+    if (LN) {
       const Tw* xr = x + static_cast<size_t>(t) * d + c;
       float x0, x1, x2, x3;
       if constexpr (sizeof(Tw) == 2) {
@@ -515,8 +518,15 @@ size_t router_wgrad_partial_bytes(const moe_config& cfg) {
 
 moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* Yp, const int* pos, const float* w,
                              void* dYp, float* dot, cudaStream_t st) {
-  bwd_gather_kernel<<<warp_grid(cfg.T), 256, 0, st>>>(static_cast<const uint4*>(dY), static_cast<const uint4*>(Yp),
-                                                       pos, w, cfg.T, cfg.k, cfg.d / 8, static_cast<uint4*>(dYp), dot);
+  const uint4* dy = static_cast<const uint4*>(dY);
+  const uint4* yp = static_cast<const uint4*>(Yp);
+  uint4* dyp = static_cast<uint4*>(dYp);
+  if (cfg.k <= 2)
+    bwd_gather_kernel<2><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, cfg.d / 8, dyp, dot);
+  else if (cfg.k <= 4)
+    bwd_gather_kernel<4><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, cfg.d / 8, dyp, dot);
+  else
+    bwd_gather_kernel<8><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, cfg.d / 8, dyp, dot);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -579,16 +589,36 @@ moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* 
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+template <typename Tw, int KM>
+void launch_bwd_dx_t(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,
+                     const void* Wr, const void* x, const float* lnc, int accumulate, float* dX, cudaStream_t st) {
+  const Tw* w = static_cast<const Tw*>(Wr);
+  const Tw* xx = static_cast<const Tw*>(x);
+  if (lnc)
+    bwd_dx_kernel<Tw, KM, true><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k, cfg.d, cfg.E,
+                                                                  xx, lnc, accumulate, dX);
+  else
+    bwd_dx_kernel<Tw, KM, false><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k, cfg.d, cfg.E,
+                                                                   xx, lnc, accumulate, dX);
+}
+
+template <typename Tw>
+void launch_bwd_dx_k(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,
+                     const void* Wr, const void* x, const float* lnc, int accumulate, float* dX, cudaStream_t st) {
+  if (cfg.k <= 2)
+    launch_bwd_dx_t<Tw, 2>(cfg, dXp, pos, idx, dl, Wr, x, lnc, accumulate, dX, st);
+  else if (cfg.k <= 4)
+    launch_bwd_dx_t<Tw, 4>(cfg, dXp, pos, idx, dl, Wr, x, lnc, accumulate, dX, st);
+  else
+    launch_bwd_dx_t<Tw, 8>(cfg, dXp, pos, idx, dl, Wr, x, lnc, accumulate, dX, st);
+}
+
 moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,
                          const void* Wr, const void* x, const float* lnc, int accumulate, float* dX, cudaStream_t st) {
   if (cfg.dtype == MOE_BF16)
-    bwd_dx_kernel<bf16><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, static_cast<const bf16*>(Wr), cfg.T,
-                                                          cfg.k, cfg.d, cfg.E, static_cast<const bf16*>(x), lnc,
-                                                          accumulate, dX);
+    launch_bwd_dx_k<bf16>(cfg, dXp, pos, idx, dl, Wr, x, lnc, accumulate, dX, st);
   else
-    bwd_dx_kernel<float><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, static_cast<const float*>(Wr), cfg.T,
-                                                           cfg.k, cfg.d, cfg.E, static_cast<const float*>(x), lnc,
-                                                           accumulate, dX);
+    launch_bwd_dx_k<float>(cfg, dXp, pos, idx, dl, Wr, x, lnc, accumulate, dX, st);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -186,75 +186,59 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
       stats->rerouted_slots = rer;
     }
   } else if (stats) {
-    // load statistics: fp64, one division, fixed-order reductions (each
-    // thread owns one expert; warps reduce by shuffles, then warp 0 sums
-    // the warp partials in warp order)
-    __shared__ double red[32];
-    __shared__ long long redl[32][2];
+    // load statistics from integer sums (exact in any order): routed and
+    // kept slots, sum and max of the counts c_e, and sum of c_e^2; one
+    // thread then forms, with f = c/T,
+    //   sum_e (f_e - mean f)^2 = (E sum c^2 - (sum c)^2) / (E T^2)
+    // from an exact 128-bit numerator, so the fp64 work is a handful of
+    // operations on one thread
+    __shared__ long long redl[32][3];
     __shared__ int redmax[32];
     const long long nslots = static_cast<long long>(T) * k;
-    const double invT = 1.0 / static_cast<double>(T);
     const int nwarps = (blockDim.x + 31) >> 5;
     long long r_cnt = tid < E ? tot[tid] : 0, k_cnt = tid < E ? my_kept : 0;
+    long long sq = tid < E ? static_cast<long long>(tot[tid]) * tot[tid] : 0;
     int cmax = tid < E ? tot[tid] : 0;
-    double fsum = tid < E ? static_cast<double>(tot[tid]) * invT : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       r_cnt += __shfl_xor_sync(0xffffffffu, r_cnt, o);
       k_cnt += __shfl_xor_sync(0xffffffffu, k_cnt, o);
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
       cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-      fsum += __shfl_xor_sync(0xffffffffu, fsum, o);
     }
     if (lane == 0) {
-      red[warp] = fsum;
       redl[warp][0] = r_cnt;
       redl[warp][1] = k_cnt;
+      redl[warp][2] = sq;
       redmax[warp] = cmax;
     }
     __syncthreads();
-    __shared__ double mean_s;
-    __shared__ long long routed_s, kept_s;
-    __shared__ int max_s;
     if (tid == 0) {
-      double fs = 0.0;
-      long long rc = 0, kc = 0;
+      long long rc = 0, kc = 0, s2 = 0;
       int mx = 0;
       for (int w2 = 0; w2 < nwarps; ++w2) {
-        fs += red[w2];
         rc += redl[w2][0];
         kc += redl[w2][1];
+        s2 += redl[w2][2];
         mx = max(mx, redmax[w2]);
       }
-      mean_s = fs / E;
-      routed_s = rc;
-      kept_s = kc;
-      max_s = mx;
-    }
-    __syncthreads();
-    const double mean = mean_s;
-    double dv2 = 0.0;
-    if (tid < E) {
-      const double dv = static_cast<double>(tot[tid]) * invT - mean;
-      dv2 = dv * dv;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dv2 += __shfl_xor_sync(0xffffffffu, dv2, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = dv2;
-    __syncthreads();
-    if (tid == 0) {
-      double var = 0.0;
-      for (int w2 = 0; w2 < nwarps; ++w2) var += red[w2];
-      const double sd = E > 1 ? sqrt(var / (E - 1)) : 0.0;
+      // rc = sum c <= T k <= 2^30, so s2 <= rc^2 <= 2^60 and E s2 < 2^71
+      const unsigned __int128 num = static_cast<unsigned __int128>(E) * static_cast<unsigned long long>(s2) -
+                                    static_cast<unsigned __int128>(rc) * static_cast<unsigned long long>(rc);
+      const double numd = static_cast<double>(static_cast<unsigned long long>(num >> 64)) * 18446744073709551616.0 +
+                          static_cast<double>(static_cast<unsigned long long>(num));
+      const double Td = static_cast<double>(T);
+      const double mean = static_cast<double>(rc) / (static_cast<double>(E) * Td);
+      const double sd = E > 1 ? sqrt(numd / (static_cast<double>(E) * (E - 1)) / (Td * Td)) : 0.0;
       moe_stats st;
-      st.routed_slots = routed_s;
-      st.kept_slots = kept_s;
-      st.dropped_slots = nslots - kept_s;
+      st.routed_slots = rc;
+      st.kept_slots = kc;
+      st.dropped_slots = nslots - kc;
       st.capacity = C;
       st.numeric_error = unrouted / k;
-      st.drop_rate = static_cast<double>(nslots - kept_s) / static_cast<double>(nslots);
+      st.drop_rate = static_cast<double>(nslots - kc) / static_cast<double>(nslots);
       if (balance == MOE_BALANCE_STD_MAX)
-        st.balance_stat = static_cast<double>(lam) * (sd + static_cast<double>(gamma) * (max_s * invT));
+        st.balance_stat = static_cast<double>(lam) * (sd + static_cast<double>(gamma) * (mx / Td));
       else if (balance == MOE_BALANCE_SWITCH)
         st.balance_stat = __longlong_as_double(0x7ff8000000000000LL);  // needs the weights: set by the layer
       else
