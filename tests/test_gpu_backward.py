@@ -192,6 +192,21 @@ def test_backward_balance_variants(variant, lam):
     check_all(wl, t, dY, g, ref)
 
 
+def test_backward_layernorm_router_with_product_balance():
+    """LayerNorm before the router together with the product balance term
+    (lambda 500, so the term moves dWr): the normalisation's backward
+    carries the balance gradient as well."""
+    wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, lam=500.0, x_affine=True, seed=73)
+    t = guarded_inputs(wl, "cpu", layernorm=True)
+    dY = t.pop("dY")
+    td = {n: v.to(DEV) for n, v in t.items()}
+    route = dict(layernorm=True, balance="switch")
+    _, sv, g = run_fwd_bwd(wl, td, dY.to(DEV), **route)
+    ref = oracle_backward(wl, t, dY, **route)
+    np.testing.assert_array_equal(sv["pos"].cpu().numpy(), ref["route"]["pos"])
+    check_all(wl, t, dY, g, ref)
+
+
 def test_backward_is_deterministic():
     wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, seed=53)
     t = guarded_inputs(wl, DEV)

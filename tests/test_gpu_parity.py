@@ -596,3 +596,28 @@ def test_top1_routing_forward_and_backward():
     for name in ("dW1", "dW3", "dW2"):
         got = g[name].cpu().numpy().astype(np.float64)
         assert np.linalg.norm(got - ref[name]) <= 1e-2 * np.linalg.norm(ref[name]), name
+
+
+def test_routing_and_balance_variants_combined():
+    """Every routing flag that composes at once: LayerNorm before the router,
+    token-major priority, rerouting of the overflow and the std + gamma*max
+    statistic, on rows of varying offset and scale with a biased router
+    (E = 12 pads the tensor-core logits to 16)."""
+    wl = S.WORKLOADS["small_prefill"].replace(T=600, d=256, h=256, E=12, k=2, capacity_factor=0.8, seed=35,
+                                              x_affine=True)
+    t = S.make_inputs(wl, DEV)
+    t["expert_bias"] = torch.linspace(1.0, 0.0, wl.E, dtype=torch.float32, device=DEV)
+    t = guard(wl.replace(k=2 * wl.k), t, layernorm=True)
+    route = dict(layernorm=True, token_major=True, reroute=True, balance="std_max", balance_gamma=100.0)
+    cfg = M.config_of(wl, **route)
+    sv = M.moe.alloc_saved(cfg)
+    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg, 1)
+    M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], None, y, sv, st, ws)
+    assert M.moe_check_error(ws) == 0
+    r = O.layer_forward(oracle_cfg(wl, **route), oracle_weights(t), t["x"], t["expert_bias"])
+    stats = M.moe.read_stats(st)
+    check_routing(r, sv, stats, t["x"])
+    assert stats["rerouted_slots"] > 0 and stats["dropped_slots"] > 0
+    assert_close_bf16_scaled(to_np(y), r["y"], "y")
