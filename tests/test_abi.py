@@ -128,3 +128,26 @@ def test_workspace_sizes(M):
     # inference keeps Xp, H, Yp in the workspace: at least T*k*(2d + h) bf16
     assert inf >= 16384 * 2 * (2 * 4096 + 14336) * 2
     assert tr < inf
+
+
+def test_workspace_grows_with_the_variants_that_need_scratch(M):
+    """The host-side workspace layout makes room for each variant's
+    scratch: LayerNorm's weight-row sums (forward) and per-token terms
+    (backward), the reroute backups and second-pass ranks, and the product
+    balance term's importance words."""
+    T, d, h, E, k = 4096, 1024, 2816, 12, 2
+    base = M.make_config(T, d, h, E, k, capacity_factor=1.0)
+    ln = M.make_config(T, d, h, E, k, capacity_factor=1.0, layernorm=True)
+    rr = M.make_config(T, d, h, E, k, capacity_factor=1.0, reroute=True)
+    sw = M.make_config(T, d, h, E, k, capacity_factor=1.0, balance="switch")
+    for training in (0, 1):
+        b = M.moe_workspace_size(base, training)
+        assert M.moe_workspace_size(ln, training) >= b + 16 * 4  # E rounded up to 16 sums
+        assert M.moe_workspace_size(rr, training) >= b + T * k * 4 * 2  # backups + first-pass ranks
+        assert M.moe_workspace_size(sw, training) >= b + E * 8
+    assert M.moe_workspace_size(ln, 2) >= M.moe_workspace_size(base, 2) + 3 * T * 4
+    # the router scratch pads the logit rows to the 8-column GEMM granule
+    e5 = M.make_config(T, d, h, 5, k, capacity_factor=1.0)
+    e8 = M.make_config(T, d, h, 8, k, capacity_factor=1.0)
+    assert M.moe_workspace_size(e5, 1) >= T * 8 * 4
+    assert M.moe_workspace_size(e5, 1) <= M.moe_workspace_size(e8, 1)
