@@ -342,6 +342,15 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
  * a bounded wait (code_out receives the raw word, nullable). */
 moe_status moe_check_error(const void* ws, int* code_out, moe_stream_t stream);
 
+/* Self-test of the failure-detection path; the pages have no counterpart.
+ * Enqueues one kernel whose single thread waits on a shared-memory barrier
+ * that nothing completes.  The wait gives up after its bound (1 s), records
+ * code 0x1ff in the workspace error word and returns, so the context stays
+ * usable and moe_check_error(ws) then reports MOE_ERR_TIMEOUT.  The kernel
+ * holds one SM for about a second.  ws: >= 256 bytes of device memory (the
+ * error word is its first int, zeroed by this call). */
+moe_status moe_selftest_wait_timeout(void* ws, moe_stream_t stream);
+
 const char* moe_status_string(moe_status s);
 
 #ifdef __cplusplus

@@ -496,6 +496,11 @@ moe_status moe_check_error(const void* ws, int* code_out, moe_stream_t stream) {
   return code ? MOE_ERR_TIMEOUT : MOE_OK;
 }
 
+moe_status moe_selftest_wait_timeout(void* ws, moe_stream_t stream) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  return launch_selftest_wait(static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char* moe_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "ok";

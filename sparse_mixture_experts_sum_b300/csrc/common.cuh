@@ -27,6 +27,7 @@ enum : int {
   kErrWaitMma = 0x102,       // MMA issuer waited too long for data / accumulator
   kErrWaitEpilogue = 0x103,  // epilogue waited too long for an accumulator
   kErrWaitDrain = 0x104,     // teardown could not drain in-flight copies / MMAs
+  kErrSelfTest = 0x1ff,      // the self-test's wait on a barrier that nothing completes
 };
 
 // 1 second: every legitimate wait in these kernels is microseconds long

@@ -133,6 +133,8 @@ moe_status launch_group_colsum(const void* src, long long ld, const int* offsets
 bool make_tma_2d_bf16(CUtensorMap* map, const void* base, long long inner, long long rows, int box_inner,
                       int box_rows);
 int device_sm_count(int dev);
+// One kernel whose bounded wait runs out (~1 s): kErrSelfTest lands in *err.
+moe_status launch_selftest_wait(int* err, cudaStream_t stream);
 // Zero a_bytes at a and b_bytes at b (multiples of 4; either may be null)
 // with one small kernel on `stream`.
 moe_status launch_zero(void* a, size_t a_bytes, void* b, size_t b_bytes, cudaStream_t stream);

@@ -76,4 +76,23 @@ int device_sm_count(int dev) {
   return cache[dev];
 }
 
+// Self-test of the bounded-wait path: one thread waits on a shared-memory
+// barrier that expects one arrival and gets none.  The wait gives up after
+// kWaitLimitNs and records kErrSelfTest in the error word; the kernel then
+// returns normally, so the context stays usable.
+__global__ void selftest_wait_kernel(int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (!mbar_wait(&bar, 0)) record_error(err, kErrSelfTest);
+}
+
+moe_status launch_selftest_wait(int* err, cudaStream_t stream) {
+  moe_status s = launch_zero(err, sizeof(int), nullptr, 0, stream);
+  if (s != MOE_OK) return s;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(err);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace moe

@@ -59,7 +59,8 @@ class MoeStats(ctypes.Structure):
 
 EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_static",
            "moe_expert_ffn", "moe_expert_ffn_shared",
-           "moe_combine", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error", "moe_status_string")
+           "moe_combine", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error", "moe_status_string",
+           "moe_selftest_wait_timeout")
 
 _lib = None
 
@@ -89,6 +90,7 @@ def lib() -> ctypes.CDLL:
                               ctypes.POINTER(MoeGrads), vp, sz, vp],
             "moe_check_error": [vp, ctypes.POINTER(i), vp],
             "moe_status_string": [i],
+            "moe_selftest_wait_timeout": [vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -256,6 +258,12 @@ def moe_check_error(ws, stream=None) -> int:
     if st not in (MOE_OK, MOE_ERR_TIMEOUT):
         raise MoeError("moe_check_error", st)
     return code.value
+
+
+def moe_selftest_wait_timeout(ws, stream=None):
+    """Enqueue the failure-detection self-test: a kernel whose bounded wait
+    runs out (~1 s) and records its code in ws's error word."""
+    _check("moe_selftest_wait_timeout", lib().moe_selftest_wait_timeout(_p(ws), _stream(stream)))
 
 
 def alloc_saved(cfg: MoeConfig, device="cuda", backward=False) -> dict:
