@@ -242,16 +242,14 @@ struct RouteLayout {
   }
 };
 
-// Logits of 64 tokens against all experts (chunks of 128), over the K
-// blocks of this CTA's split (blockIdx.y of gridDim.y); cp.async ring of
-// STAGES stages.  partial == nullptr: add bias and noise, take the top-k and
-// count.  Otherwise write the raw partial logits partial[split][t][e].
+// Logits of 64 tokens against all experts (chunks of 128) from a cp.async
+// ring of STAGES stages, plus bias and noise; then each token's top-k and
+// the block histogram.
 template <int STAGES>
 __global__ void __launch_bounds__(128)
 route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const float* __restrict__ ebias,
                   const float* __restrict__ noise, int T, int d, int E, int k, int* __restrict__ idx,
-                  float* __restrict__ w, int* __restrict__ counts, int kb_per_split, float* __restrict__ partial,
-                  int raw, float* __restrict__ ent) {
+                  float* __restrict__ w, int* __restrict__ counts, int raw, float* __restrict__ ent) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const RouteLayout Lay(E, STAGES);
   const int nep = Lay.nep;
@@ -264,10 +262,7 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
   const int warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c4 = lane & 3;
   const int t0 = blockIdx.x * RT_TM;
-  const int nk_all = (d + RT_BK - 1) / RT_BK;
-  const int kb0 = blockIdx.y * kb_per_split;
-  const int kb1 = min(nk_all, kb0 + kb_per_split);
-  const int nk = kb1 - kb0;
+  const int nk = (d + RT_BK - 1) / RT_BK;
 
   for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
 
@@ -290,7 +285,7 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
     for (int f = 0; f < RT_NE / 8; ++f) acc[f][0] = acc[f][1] = acc[f][2] = acc[f][3] = 0.f;
 
     auto load_stage = [&](int stage, int kb) {
-      const int k0 = (kb0 + kb) * RT_BK;
+      const int k0 = kb * RT_BK;
       bf16* xd = xs(stage);
       bf16* wd = wsm(stage);
       // x tile: 64 rows x 8 chunks of 16 B; out-of-range chunks are zero-filled
@@ -345,7 +340,7 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
     cp_async_wait<0>();
     __syncthreads();  // the ring becomes L
 
-    // logits of this chunk (+ bias, + noise unless partial) -> L
+    // logits of this chunk (+ bias, + noise) -> L
     {
       const int r0 = warp * 16;
 #pragma unroll
@@ -358,7 +353,7 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
             const int e = e0 + col;
             const int t = t0 + r;
             float v = acc[f][q];
-            if (!partial && e < E && t < T) {
+            if (e < E && t < T) {
               if (ebias) v += ebias[e];
               if (noise) v += noise[static_cast<size_t>(t) * E + e];
             }
@@ -368,13 +363,7 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
       }
     }
     __syncthreads();
-    if (partial) {
-      float* pp = partial + static_cast<size_t>(blockIdx.y) * T * E;
-      for (int q = tid; q < RT_TM * ne; q += blockDim.x) {
-        const int r = q / ne, col = q - r * ne;
-        if (t0 + r < T) pp[static_cast<size_t>(t0 + r) * E + e0 + col] = L[r * (nep + 1) + col];
-      }
-    } else if (tid < RT_TM && t0 + tid < T) {
+    if (tid < RT_TM && t0 + tid < T) {
       for (int col = 0; col < ne; ++col) {
         const float v = L[tid * (nep + 1) + col];
         if (!isfinite(v)) finite = false;
@@ -385,7 +374,6 @@ route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const
     __syncthreads();  // L is the ring again for the next expert chunk
   }
 
-  if (partial) return;
   if (tid < RT_TM && t0 + tid < T) topk_finish(tv, tix, k, finite, t0 + tid, idx, w, hist, raw, sst, ent);
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x)
@@ -571,11 +559,10 @@ moe_status launch_route_stages(const moe_config& cfg, const void* x, const void*
       return MOE_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int nk = (cfg.d + RT_BK - 1) / RT_BK;
   dim3 grid((cfg.T + RT_TM - 1) / RT_TM, 1);
   route_bf16_kernel<STAGES><<<grid, 128, Lay.total, stream>>>(
       static_cast<const bf16*>(x), static_cast<const bf16*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E, cfg.k,
-      idx, w, counts, nk, nullptr, (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0, ent);
+      idx, w, counts, (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0, ent);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -419,8 +419,8 @@ def test_route_with_workspace(T, d, E, k):
 @pytest.mark.parametrize("raw,tm,E", [(True, False, 16), (False, True, 16), (True, True, 12), (True, False, 130)])
 def test_routing_variants(raw, tm, E):
     """Raw softmax weights ([P2] 3.2, [P4] 5.1) and token-major capacity
-    priority, through the tensor-core router (E multiple of 8) and the
-    mma.sync one (E = 12, 130); capacity binds (cf 0.8)."""
+    priority through the tensor-core router (E = 12 and 130 pad its logit
+    rows to 16 and 136); capacity binds (cf 0.8)."""
     wl = S.WORKLOADS["small_prefill"].replace(T=700, d=256, h=256, E=E, capacity_factor=0.8, seed=27)
     t = guarded_inputs(wl, DEV)
     cfg = M.make_config(wl.T, wl.d, wl.h, wl.E, wl.k, wl.act, wl.dtype, capacity_factor=wl.capacity_factor,
