@@ -10,10 +10,13 @@
  *        quietly activated inside a large model" (mlqm.cn) -- 3.1 Router,
  *        3.3 Gate, 4.2 model definition, 4.3 training configuration.
  *   [P2] "MoE mixture-of-experts architecture: principles and engineering
- *        practice" (cnnetsun.cn) -- 3.2 router, 4.1 expert fusion, 4.2
- *        building an MoE model.
+ *        practice" (cnnetsun.cn) -- 3.2 router (and its auxiliary loss), 4.1
+ *        expert fusion, 4.2 building an MoE model, 5.2 normalising the
+ *        router's input.
  *   [P3] "MoE architecture revealed: why total parameters != active
- *        parameters" (rkmt.cn) -- 2.3 router design, 3.3 TinyMoE.
+ *        parameters" (rkmt.cn) -- 2.3 router design (noise, capacity,
+ *        dropping or rerouting, the balance loss), 3.3 TinyMoE, 5.3 (k = 1
+ *        first).
  *   [P4] "GPT-4 has 1.8 trillion parameters and uses 2% of them per token"
  *        (wmrh.cn) -- 2.2 dynamic routing, 5.1 MVP.
  *   [P5] "Training a 200B LLM from scratch 5/25: how does MoE compute with
@@ -43,10 +46,11 @@
  *    workspace error word (read it with moe_check_error).
  *  - Fixed rules: top-k ties go to the lower expert index; capacity is
  *    granted in slot-major priority (every token's first choice in token
- *    order, then every second choice, ...).
+ *    order, then every second choice, ...) unless MOE_ROUTE_TOKEN_MAJOR.
  *  - Limits: 1 <= k <= min(E, 8); 1 <= E <= 1024; T >= 1; T*k <= 2^30; for
  *    bf16, d and h multiples of 8 (16-byte rows); moe_layer_bwd: bf16 with
- *    d and h multiples of 64.
+ *    d and h multiples of 64, not with MOE_ROUTE_RAW_PROBS or
+ *    MOE_ROUTE_REROUTE; MOE_ROUTE_REROUTE: k <= 4.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -223,11 +227,15 @@ moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes
  * both nullable.  Outputs idx [T,k] int32, w [T,k] fp32, counts [E] int32,
  * entropy [T] fp32 (nullable): -sum_e p_e ln p_e of each token's softmax
  * over all experts, NaN for a token with a non-finite logit.
+ * (MOE_ROUTE_LAYERNORM: l uses LayerNorm(x[t]) in place of x[t];
+ * MOE_ROUTE_REROUTE: each token's experts ranked k .. 2k-1 are also left in
+ * ws for moe_dispatch.)
  * ws: NULL, or >= moe_workspace_size(cfg, 1) bytes.  bf16 with ws: the
  * logits run on the tcgen05 tensor cores into the workspace, then a top-k
- * pass; without ws a fused mma.sync kernel (MOE_ROUTE_LAYERNORM then
- * returns MOE_ERR_UNSUPPORTED).  Both sum in a fixed order, so results
- * repeat bit for bit; the two paths may differ in the last bits of l. */
+ * pass; without ws a fused mma.sync kernel (MOE_ROUTE_LAYERNORM and
+ * MOE_ROUTE_REROUTE then return MOE_ERR_UNSUPPORTED).  Both sum in a fixed
+ * order, so results repeat bit for bit; the two paths may differ in the
+ * last bits of l. */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr,
                      const float* expert_bias, const float* noise, int* idx,
                      float* w, int* counts, float* entropy, void* ws,
@@ -239,7 +247,11 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr,
  *   scan of kept, pos[t,j] = offsets[e] + rank or -1, Xp[pos[t,j]] = x[t].
  * idx [T,k] int32 from moe_route; x [T,d].  Outputs kept [E], offsets [E+1],
  * pos [T,k] int32; Xp [T*k, d] (rows >= offsets[E] untouched); stats:
- * device moe_stats*, nullable.  ws: >= moe_workspace_size(cfg, 1) bytes. */
+ * device moe_stats*, nullable (balance_stat in cfg->balance's form; NaN for
+ * MOE_BALANCE_SWITCH, which needs the weights).  ws: >= moe_workspace_size(
+ * cfg, 1) bytes; with MOE_ROUTE_REROUTE it must hold the backups moe_route
+ * left there, and a second pass offers the dropped slots to them (kept[e]
+ * then counts both passes). */
 moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x,
                         int* kept, int* offsets, int* pos, void* Xp,
                         moe_stats* stats, void* ws, moe_stream_t stream);
