@@ -49,8 +49,8 @@
  *    order, then every second choice, ...) unless MOE_ROUTE_TOKEN_MAJOR.
  *  - Limits: 1 <= k <= min(E, 8); 1 <= E <= 1024; T >= 1; T*k <= 2^30; for
  *    bf16, d and h multiples of 8 (16-byte rows); moe_layer_bwd: bf16 with
- *    d and h multiples of 64, not with MOE_ROUTE_RAW_PROBS or
- *    MOE_ROUTE_REROUTE; MOE_ROUTE_REROUTE: k <= 4.
+ *    d and h multiples of 64, not with MOE_ROUTE_RAW_PROBS;
+ *    MOE_ROUTE_REROUTE: k <= 4.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -97,8 +97,9 @@ enum { MOE_F32 = 0, MOE_BF16 = 1 };
  *    slot keeps its weight w[t,j] and idx keeps the router's choice; pos
  *    and offsets show the serving expert.  Needs k <= 4 and a workspace:
  *    moe_route writes the backups into ws, moe_dispatch reads them from
- *    the same ws.  moe_dispatch_static and moe_layer_bwd return
- *    MOE_ERR_UNSUPPORTED. */
+ *    the same ws.  moe_dispatch_static returns MOE_ERR_UNSUPPORTED.  In
+ *    moe_layer_bwd a rerouted slot's logit gradient goes to idx[t,j] and
+ *    its expert gradients to the backup that served it. */
 enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2, MOE_ROUTE_LAYERNORM = 4, MOE_ROUTE_REROUTE = 8 };
 
 /* Load-balance term (moe_config.balance).  f[e] = counts[e]/T (pre-capacity

@@ -605,13 +605,14 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
     lam = cfg.get("lam", 0.01)
     if cfg.get("raw_probs"):
         raise NotImplementedError("the backward covers renormalised top-k weights only")
-    if cfg.get("reroute"):
-        raise NotImplementedError("the backward covers slots served by their chosen experts only")
     r = route_and_dispatch(cfg, x, weights["Wr"], expert_bias, noise)
     X = decode(x)
     DY = decode(dY)
     idx, w, pos = r["idx"], r["w"], r["pos"]
-    kept = pos >= 0
+    # the expert that serves each kept slot: the router's choice, or with
+    # rerouting a backup (whose output still carries the slot's weight w_j,
+    # so the logit gradient stays on idx_j)
+    served = r["served"]
     dX = np.zeros((T, d))
     G = np.zeros((T, k))
     grads = {}
@@ -623,7 +624,7 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
         grads["db2"] = np.zeros((E, d))
     y = np.zeros((T, d))
     for e in range(E):
-        rows, slots = np.nonzero((idx == e) & kept)
+        rows, slots = np.nonzero(served == e)
         if rows.size == 0:
             continue
         We = expert_params(weights, e, act)

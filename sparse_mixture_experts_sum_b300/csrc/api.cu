@@ -438,7 +438,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
   if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if ((cfg->d % 64) || (cfg->h % 64)) return MOE_ERR_UNSUPPORTED;
-  if (cfg->route_flags & (MOE_ROUTE_RAW_PROBS | MOE_ROUTE_REROUTE)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->route_flags & MOE_ROUTE_RAW_PROBS) return MOE_ERR_UNSUPPORTED;
   if (!wts->Wr || !wts->W1 || !wts->W2 || (swiglu && !wts->W3)) return MOE_ERR_INVALID_ARG;
   if (cfg->has_shared && (!wts->Ws1 || !wts->Ws2 || (swiglu && !wts->Ws3))) return MOE_ERR_INVALID_ARG;
   const moe_saved& S = *saved;

@@ -207,6 +207,27 @@ def test_backward_layernorm_router_with_product_balance():
     check_all(wl, t, dY, g, ref)
 
 
+def test_backward_with_reroute():
+    """Rerouting of the overflow ([P3] 2.3): a moved slot's expert gradients
+    go to the backup that served it, its logit gradient to the router's
+    choice; everything matches the oracle.  A biased router and cf 0.9 make
+    the first pass drop slots that the second pass places (91 of 512x2)."""
+    from moe_testlib import guard
+    wl = _workload(has_shared=True, gumbel=True, capacity_factor=0.9, seed=79)
+    t = S.make_inputs(wl, "cpu")
+    t["expert_bias"] = torch.linspace(2.0, 0.0, wl.E, dtype=torch.float32)
+    t = guard(wl.replace(k=2 * wl.k), t)
+    dY = t.pop("dY")
+    td = {n: v.to(DEV) for n, v in t.items()}
+    _, sv, g = run_fwd_bwd(wl, td, dY.to(DEV), reroute=True)
+    ref = oracle_backward(wl, t, dY, reroute=True)
+    r = ref["route"] if "route" in ref else O.route_and_dispatch(oracle_cfg(wl, reroute=True), t["x"], t["Wr"],
+                                                                   t["expert_bias"], t["noise"])
+    assert ((r["served"] >= 0) & (r["served"] != r["idx"])).any()
+    np.testing.assert_array_equal(sv["pos"].cpu().numpy(), r["pos"])
+    check_all(wl, t, dY, g, ref)
+
+
 def test_backward_is_deterministic():
     wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, seed=53)
     t = guarded_inputs(wl, DEV)

@@ -765,3 +765,42 @@ def test_reroute_properties(T, E, k, cf, tm):
         got = {(t, j) for t, j in zip(*np.nonzero((r1["served"] == e) & ~first))}
         assert got == taken, e
     assert r1["stats"]["rerouted_slots"] > 0
+
+
+def test_backward_with_reroute_finite_differences():
+    """With rerouting ([P3] 2.3), a moved slot's output comes from its backup
+    expert but keeps the weight of the router's choice: dX, dWr and the
+    backup expert's weights match central differences of L (routing fixed,
+    away from ties), and the run does reroute."""
+    rng = _rng(93)
+    T, d, h, E, k = 16, 5, 6, 4, 2
+    w = dict(Wr=rng.normal(size=(E, d)), W1=rng.normal(size=(E, h, d)) / 2, W3=rng.normal(size=(E, h, d)) / 2,
+             W2=rng.normal(size=(E, d, h)) / 3)
+    bias = np.array([1.5, 1.0, 0.0, -0.5])
+    cfg = dict(T=T, d=d, h=h, E=E, k=k, act="swiglu", capacity_factor=0.5, lam=0.2, reroute=True)
+    x = rng.normal(size=(T, d))
+    dY = rng.normal(size=(T, d))
+    g = O.layer_backward(cfg, w, x, dY, bias)
+    r = g["route"] if "route" in g else O.route_and_dispatch(cfg, x, w["Wr"], bias)
+    moved = (r["served"] >= 0) & (r["served"] != r["idx"])
+    assert moved.any()
+    b = int(r["served"][moved][0])
+
+    def loss(xx, ww):
+        return O.layer_backward(cfg, ww, xx, dY, bias)["loss"]
+
+    hh = 1e-6
+    for (t, i) in [(0, 0), (7, 3), (15, 4)]:
+        xp, xm = x.copy(), x.copy()
+        xp[t, i] += hh
+        xm[t, i] -= hh
+        num = (loss(xp, w) - loss(xm, w)) / (2 * hh)
+        assert abs(num - g["dX"][t, i]) <= 1e-6 * max(1.0, abs(num)), (t, i, num, g["dX"][t, i])
+    for name, ix in [("Wr", (0, 1)), ("Wr", (3, 2)), ("W1", (b, 2, 1)), ("W2", (b, 3, 4))]:
+        wp = dict(w, **{name: w[name].copy()})
+        wm = dict(w, **{name: w[name].copy()})
+        wp[name][ix] += hh
+        wm[name][ix] -= hh
+        num = (loss(x, wp) - loss(x, wm)) / (2 * hh)
+        got = g["d" + name][ix]
+        assert abs(num - got) <= 1e-6 * max(1.0, abs(num)), (name, ix, num, got)
