@@ -49,8 +49,8 @@
  *    order, then every second choice, ...) unless MOE_ROUTE_TOKEN_MAJOR.
  *  - Limits: 1 <= k <= min(E, 8); 1 <= E <= 1024; T >= 1; T*k <= 2^30; for
  *    bf16, d and h multiples of 8 (16-byte rows); moe_layer_bwd: bf16 with
- *    d and h multiples of 64, not with MOE_ROUTE_RAW_PROBS;
- *    MOE_ROUTE_REROUTE: k <= 4.
+ *    d and h multiples of 64, not with MOE_ROUTE_RAW_PROBS and
+ *    MOE_ROUTE_LAYERNORM together; MOE_ROUTE_REROUTE: k <= 4.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -80,7 +80,9 @@ enum { MOE_F32 = 0, MOE_BF16 = 1 };
  *  MOE_ROUTE_RAW_PROBS: the weights are the selected entries of the softmax
  *    over all E experts, not renormalised over the k ([P2] 3.2: output =
  *    p1*e1 + p2*e2; [P4] 5.1 uses the top-k probabilities as they are).
- *    Forward only: moe_layer_bwd returns MOE_ERR_UNSUPPORTED.
+ *    moe_layer_bwd then gives every logit a gradient (the softmax's
+ *    denominator) and needs the forward's saved logits (moe_saved.logits);
+ *    not combined with MOE_ROUTE_LAYERNORM in the backward.
  *  MOE_ROUTE_TOKEN_MAJOR: capacity is granted token by token (all of token
  *    t's choices, in order, before token t+1's) instead of slot-major.
  *  MOE_ROUTE_LAYERNORM: the router sees LayerNorm(x[t]) = (x[t] - mean) /
@@ -168,6 +170,10 @@ typedef struct {
   void* Z;       /* [T*k, 2h] SwiGLU gate | up  (GeLU: [T*k, h], W1 v + b1) */
   void* Hs;      /* [T, h]   shared expert's activated hidden rows          */
   void* Zs;      /* [T, 2h]  shared expert's pre-activations (GeLU [T, h])  */
+  float* logits; /* [T, E]   the router's final logits (bias, noise and the
+                              LayerNorm applied), fp32: written by a bf16
+                              forward when non-NULL; moe_layer_bwd reads them
+                              with MOE_ROUTE_RAW_PROBS                       */
 } moe_saved;
 
 /* Gradients written by moe_layer_bwd (device, fp32, caller-owned).  Every

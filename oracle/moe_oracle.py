@@ -598,13 +598,13 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
 
     Per slot: G[t,j] = [kept] <dY[t], FFN_e(x[t])> + dB/dw[t,j];
     logit gradient dl[t, idx_j] = w_j (G_j - sum_j' w_j' G_j') (softmax over
-    the selected logits), other logits 0; dWr = dl^T x; dX = dl Wr + the
-    experts' input gradients (routed rows scaled by w) + the shared expert's."""
+    the selected logits), other logits 0 -- or, with raw_probs (w_j = p_{idx_j}
+    of the softmax over all E), dl[t, e] = p_e ([e selected] G_e - sum_j w_j
+    G_j) for every e; dWr = dl^T x; dX = dl Wr + the experts' input
+    gradients (routed rows scaled by w) + the shared expert's."""
     T, d, E, k = cfg["T"], cfg["d"], cfg["E"], cfg["k"]
     act = cfg["act"]
     lam = cfg.get("lam", 0.01)
-    if cfg.get("raw_probs"):
-        raise NotImplementedError("the backward covers renormalised top-k weights only")
     r = route_and_dispatch(cfg, x, weights["Wr"], expert_bias, noise)
     X = decode(x)
     DY = decode(dY)
@@ -651,12 +651,21 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
     val, dcv = balance_term_grad(idx, w, E, T, lam, cfg.get("balance", "cv"), cfg.get("gamma", 100.0))
     G += dcv
     dl = np.zeros((T, E))
+    if cfg.get("raw_probs"):
+        # w_j = p_{idx_j}, p the softmax over all E: every logit e gets
+        # p_e ([e selected] G_e - sum_j w_j G_j)
+        P = softmax(np.where(np.isfinite(r["logits"]), r["logits"], 0.0))
     for t in range(T):
         if idx[t, 0] < 0:
             continue
         s = (w[t] * G[t]).sum()
-        for j in range(k):
-            dl[t, idx[t, j]] += w[t, j] * (G[t, j] - s)
+        if cfg.get("raw_probs"):
+            dl[t] = -P[t] * s
+            for j in range(k):
+                dl[t, idx[t, j]] += P[t, idx[t, j]] * G[t, j]
+        else:
+            for j in range(k):
+                dl[t, idx[t, j]] += w[t, j] * (G[t, j] - s)
     Wr = decode(weights["Wr"])
     if cfg.get("layernorm"):
         grads["dWr"] = dl.T @ layer_norm(X)

@@ -46,7 +46,7 @@ size_t esize(const moe_config* cfg) { return cfg->dtype == MOE_BF16 ? 2 : 4; }
 struct WsLayout {
   size_t dispatch_off, route_off, ent, backup;
   size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs;
-  size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs, lnc;
+  size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs, lnc, dld;
   size_t total;
 };
 
@@ -71,6 +71,7 @@ WsLayout layout(const moe_config* cfg, int training) {
     L.rpart = take(router_wgrad_partial_bytes(*cfg));
     L.dABs = cfg->has_shared ? take(T * hz * es) : 0;
     L.lnc = (cfg->route_flags & MOE_ROUTE_LAYERNORM) ? take(3 * T * 4) : 0;
+    L.dld = (cfg->route_flags & MOE_ROUTE_RAW_PROBS) ? take(T * E * 4) : 0;
     L.total = o;
     return L;
   }
@@ -280,7 +281,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr, const
   void* scratch = ws && route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr;
   int* backup = ws && (cfg->route_flags & MOE_ROUTE_REROUTE) ? static_cast<int*>(at(ws, L.backup)) : nullptr;
   int* err = ws ? static_cast<int*>(ws) : nullptr;
-  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, entropy, scratch, backup, err, st);
+  return launch_route(*cfg, x, Wr, expert_bias, noise, idx, w, counts, entropy, scratch, backup, nullptr, err, st);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x, int* kept, int* offsets, int* pos,
@@ -388,14 +389,16 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
     S.Yp = at(ws, L.Yp);
     S.Sx = cfg->has_shared ? at(ws, L.Sx) : nullptr;
     S.Z = S.Hs = S.Zs = nullptr;
+    S.logits = nullptr;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);  // zeroed by the router's first launch
 
   float* ent = stats ? static_cast<float*>(at(ws, L.ent)) : nullptr;
   int* backup = (cfg->route_flags & MOE_ROUTE_REROUTE) ? static_cast<int*>(at(ws, L.backup)) : nullptr;
+  float* out_logits = training && cfg->dtype == MOE_BF16 ? S.logits : nullptr;
   s = launch_route(*cfg, x, wts->Wr, wts->expert_bias, noise, S.idx, S.w, S.counts, ent,
-                   route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr, backup, err, st);
+                   route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr, backup, out_logits, err, st);
   if (s != MOE_OK) return s;
   s = launch_dispatch(*cfg, capacity_of(cfg), S.idx, x, S.kept, S.offsets, S.pos, S.Xp, stats,
                       at(ws, L.dispatch_off), backup, st);
@@ -438,11 +441,13 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
   if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if ((cfg->d % 64) || (cfg->h % 64)) return MOE_ERR_UNSUPPORTED;
-  if (cfg->route_flags & MOE_ROUTE_RAW_PROBS) return MOE_ERR_UNSUPPORTED;
+  const bool raw = (cfg->route_flags & MOE_ROUTE_RAW_PROBS) != 0;
+  if (raw && (cfg->route_flags & MOE_ROUTE_LAYERNORM)) return MOE_ERR_UNSUPPORTED;
   if (!wts->Wr || !wts->W1 || !wts->W2 || (swiglu && !wts->W3)) return MOE_ERR_INVALID_ARG;
   if (cfg->has_shared && (!wts->Ws1 || !wts->Ws2 || (swiglu && !wts->Ws3))) return MOE_ERR_INVALID_ARG;
   const moe_saved& S = *saved;
   if (!S.idx || !S.w || !S.offsets || !S.pos || !S.Xp || !S.H || !S.Yp || !S.Z) return MOE_ERR_INVALID_ARG;
+  if (raw && !S.logits) return MOE_ERR_INVALID_ARG;
   if (cfg->has_shared && (!S.Hs || !S.Zs)) return MOE_ERR_INVALID_ARG;
   const moe_grads& g = *grads;
   if (!g.dX || !g.dWr || !g.dW1 || !g.dW2 || (swiglu && !g.dW3)) return MOE_ERR_INVALID_ARG;
@@ -471,6 +476,13 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
                         static_cast<unsigned long long*>(at(ws, L.imp)), static_cast<float*>(at(ws, L.coef)), dl,
                         lnc, st);
   if (s != MOE_OK) return s;
+  if (raw) {
+    // every logit has a gradient: dl becomes the dense [T, E] matrix
+    float* dld = static_cast<float*>(at(ws, L.dld));
+    s = launch_router_bwd_raw(*cfg, S.logits, S.idx, S.w, dot, static_cast<float*>(at(ws, L.coef)), dld, st);
+    if (s != MOE_OK) return s;
+    dl = dld;
+  }
   s = launch_router_wgrad(*cfg, x, S.idx, dl, lnc, static_cast<float*>(at(ws, L.rpart)), g.dWr, st);
   if (s != MOE_OK) return s;
   // routed experts

@@ -33,6 +33,7 @@ namespace moe {
 namespace {
 
 constexpr double kImpScale = 4294967296.0;  // routing weights accumulate as 2^-32 fixed point
+constexpr int MAXK_BWD = 8;                  // largest k
 
 // One warp per token: dot[t,j] = <dY[t], Yp[pos]>, dYp[pos] = w[t,j] dY[t].
 // KM = k rounded up to 2, 4 or 8 sizes the per-slot register arrays.
@@ -308,6 +309,70 @@ __global__ void ln_router_bwd_kernel(const bf16* __restrict__ x, const bf16* __r
   lnc[2 * static_cast<size_t>(T) + t] = B * r * r * inv_d;
 }
 
+// Raw softmax weights (w_j = p_{idx_j}, p the softmax over all E experts):
+// every logit gets a gradient, dlD[t,e] = p_e ([e selected] G_e - s), with
+// G_j = dot[t,j] + coef[idx_j] and s = sum_j w_j G_j.  One warp per token;
+// p from the forward's saved logits (one warp max, then exp(l - m) / Z).
+template <int NV>
+__global__ void router_bwd_raw_kernel(const float* __restrict__ logits, const int* __restrict__ idx,
+                                      const float* __restrict__ w, const float* __restrict__ dot,
+                                      const float* __restrict__ coef, int T, int k, int E, float* __restrict__ dlD) {
+  const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  float* out = dlD + static_cast<size_t>(t) * E;
+  if (idx[static_cast<size_t>(t) * k] < 0) {  // routed nowhere: no gradient
+    for (int e = lane; e < E; e += 32) out[e] = 0.f;
+    return;
+  }
+  int ej = -1;
+  float gj = 0.f, sp = 0.f;
+  if (lane < k) {
+    ej = idx[static_cast<size_t>(t) * k + lane];
+    gj = dot[static_cast<size_t>(t) * k + lane] + (ej >= 0 && ej < E ? coef[ej] : 0.f);
+    sp = w[static_cast<size_t>(t) * k + lane] * gj;
+  }
+  // s = sum_j w_j G_j in slot order (every lane forms the same sum)
+  float s = 0.f;
+  int es[MAXK_BWD];
+  float gs[MAXK_BWD];
+#pragma unroll
+  for (int j = 0; j < MAXK_BWD; ++j) {
+    es[j] = __shfl_sync(0xffffffffu, ej, j);
+    gs[j] = __shfl_sync(0xffffffffu, gj, j);
+    const float pj = __shfl_sync(0xffffffffu, sp, j);
+    if (j < k) s += pj;
+  }
+  float v[NV];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? logits[static_cast<size_t>(t) * E + e] : -INFINITY;
+    m = fmaxf(m, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    if (lane + 32 * i < E) z += expf(v[i] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  const float inv = 1.0f / z;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      float g = -s;
+#pragma unroll
+      for (int j = 0; j < MAXK_BWD; ++j)
+        if (j < k && es[j] == e) g += gs[j];
+      out[e] = expf(v[i] - m) * inv * g;
+    }
+  }
+}
+
 constexpr int RW_TOK = 512;   // tokens per block of the router weight gradient
 constexpr int RW_EXP = 16;    // experts per block
 constexpr int RW_WARPS = 4;
@@ -315,12 +380,12 @@ constexpr int RW_COLS = 256;  // columns per block: 8 per lane, one 16-byte load
 
 // partial[chunk][e][c] = sum over the chunk's tokens (each warp takes every
 // RW_WARPS-th token, ascending) of sum_j [idx=e] dl[t,j] (x[t][c] - mu[t])
-// (mu nullable: 0).  A block
+// (mu nullable: 0); DENSE: of dlD[t][e] x[t][c] for every expert e.  A block
 // covers 256 columns (a lane owns 8 consecutive ones: one 16-byte load of a
 // bf16 row) and 16 experts; every warp accumulates privately in shared
 // memory, laid out acc[warp][e][q][lane] (column lane*8+q) so that a warp's
 // updates hit 32 distinct banks; the warps are summed in a fixed order.
-template <typename Tx>
+template <typename Tx, bool DENSE>
 __global__ void __launch_bounds__(RW_WARPS * 32)
 router_wgrad_partial_kernel(const Tx* __restrict__ x, const int* __restrict__ idx, const float* __restrict__ dl,
                             int T, int d, int k, int E, const float* __restrict__ mu,
@@ -360,29 +425,51 @@ router_wgrad_partial_kernel(const Tx* __restrict__ x, const int* __restrict__ id
         for (int q = 0; q < 8; ++q) xv[u][q] -= m;
       }
     }
-    // the slots' experts and logit gradients, loaded with the rows (lane j
-    // of the warp fetches slot j of each token and shares it)
-    int eu[U];
-    float gu[U];
+    if constexpr (DENSE) {
+      // dl is [T, E]: lane e < RW_EXP fetches the chunk's expert e of each token
+      float gu[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int t = tb + u * RW_WARPS;
-      eu[u] = -1;
-      gu[u] = 0.f;
-      if (t < t1 && lane < k) {
-        eu[u] = idx[static_cast<size_t>(t) * k + lane] - e0;
-        gu[u] = dl[static_cast<size_t>(t) * k + lane];
+      for (int u = 0; u < U; ++u) {
+        const int t = tb + u * RW_WARPS;
+        gu[u] = (t < t1 && lane < RW_EXP && e0 + lane < E) ? dl[static_cast<size_t>(t) * E + e0 + lane] : 0.f;
       }
-    }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      for (int j = 0; j < k; ++j) {
-        const int e = __shfl_sync(0xffffffffu, eu[u], j);
-        const float g = __shfl_sync(0xffffffffu, gu[u], j);
-        if (e >= 0 && e < RW_EXP && e0 + e < E) {
-          float* a = acc + e * 256 + lane;
+      for (int u = 0; u < U; ++u) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) a[q * 32] = fmaf(g, xv[u][q], a[q * 32]);
+        for (int e = 0; e < RW_EXP; ++e) {
+          const float g = __shfl_sync(0xffffffffu, gu[u], e);
+          if (e0 + e < E) {
+            float* a = acc + e * 256 + lane;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) a[q * 32] = fmaf(g, xv[u][q], a[q * 32]);
+          }
+        }
+      }
+    } else {
+      // the slots' experts and logit gradients, loaded with the rows (lane j
+      // of the warp fetches slot j of each token and shares it)
+      int eu[U];
+      float gu[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int t = tb + u * RW_WARPS;
+        eu[u] = -1;
+        gu[u] = 0.f;
+        if (t < t1 && lane < k) {
+          eu[u] = idx[static_cast<size_t>(t) * k + lane] - e0;
+          gu[u] = dl[static_cast<size_t>(t) * k + lane];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        for (int j = 0; j < k; ++j) {
+          const int e = __shfl_sync(0xffffffffu, eu[u], j);
+          const float g = __shfl_sync(0xffffffffu, gu[u], j);
+          if (e >= 0 && e < RW_EXP && e0 + e < E) {
+            float* a = acc + e * 256 + lane;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) a[q * 32] = fmaf(g, xv[u][q], a[q * 32]);
+          }
         }
       }
     }
@@ -412,8 +499,10 @@ __global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, in
 
 // One warp per token: dX[t] (+)= sum_{kept j} dXp[pos] + sum_j dl[t,j] Wr[idx_j] (fp32, j ascending)
 // (- A_t - B_t (x[t] - mu_t) with LayerNorm before the router: LN, lnc).
-// KM = k rounded up to 2, 4 or 8 sizes the per-slot register arrays.
-template <typename Tw, int KM, bool LN>
+// DENSE (raw softmax weights): dl is [T, E] and the router term is
+// sum_e dl[t,e] Wr[e], e ascending.  KM = k rounded up to 2, 4 or 8 sizes
+// the per-slot register arrays.
+template <typename Tw, int KM, bool LN, bool DENSE>
 __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restrict__ pos, const int* __restrict__ idx,
                               const float* __restrict__ dl, const Tw* __restrict__ Wr, int T, int k, int d, int E,
                               const Tw* __restrict__ x, const float* __restrict__ lnc, int accumulate,
@@ -426,8 +515,8 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
 #pragma unroll
   for (int j = 0; j < KM; ++j) {
     p[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
-    e[j] = j < k ? idx[static_cast<size_t>(t) * k + j] : -1;
-    g[j] = j < k ? dl[static_cast<size_t>(t) * k + j] : 0.f;
+    e[j] = (!DENSE && j < k) ? idx[static_cast<size_t>(t) * k + j] : -1;
+    g[j] = (!DENSE && j < k) ? dl[static_cast<size_t>(t) * k + j] : 0.f;
   }
   float* out = dX + static_cast<size_t>(t) * d;
   float lmu = 0.f, lA = 0.f, lB = 0.f;
@@ -469,6 +558,29 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
         a.y = fmaf(g[j], w1, a.y);
         a.z = fmaf(g[j], w2, a.z);
         a.w = fmaf(g[j], w3, a.w);
+      }
+    }
+    if (DENSE) {
+      const float* gl = dl + static_cast<size_t>(t) * E;
+      for (int ee = 0; ee < E; ++ee) {
+        const float gg = gl[ee];
+        const Tw* wr = Wr + static_cast<size_t>(ee) * d + c;
+        float w0, w1, w2, w3;
+        if constexpr (sizeof(Tw) == 2) {
+          w0 = __bfloat162float(wr[0]);
+          w1 = __bfloat162float(wr[1]);
+          w2 = __bfloat162float(wr[2]);
+          w3 = __bfloat162float(wr[3]);
+        } else {
+          w0 = wr[0];
+          w1 = wr[1];
+          w2 = wr[2];
+          w3 = wr[3];
+        }
+        a.x = fmaf(gg, w0, a.x);
+        a.y = fmaf(gg, w1, a.y);
+        a.z = fmaf(gg, w2, a.z);
+        a.w = fmaf(gg, w3, a.w);
       }
     }
     if (LN) {
@@ -549,6 +661,22 @@ moe_status launch_router_bwd(const moe_config& cfg, const void* x, const void* W
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status launch_router_bwd_raw(const moe_config& cfg, const float* logits, const int* idx, const float* w,
+                                 const float* dot, const float* coef, float* dlD, cudaStream_t st) {
+  const int nv = (cfg.E + 31) / 32;
+  const unsigned grid = warp_grid(cfg.T);
+#define MOE_RAWBWD(NVv) \
+  router_bwd_raw_kernel<NVv><<<grid, 256, 0, st>>>(logits, idx, w, dot, coef, cfg.T, cfg.k, cfg.E, dlD)
+  if (nv <= 1) MOE_RAWBWD(1);
+  else if (nv <= 2) MOE_RAWBWD(2);
+  else if (nv <= 4) MOE_RAWBWD(4);
+  else if (nv <= 8) MOE_RAWBWD(8);
+  else if (nv <= 16) MOE_RAWBWD(16);
+  else MOE_RAWBWD(32);
+#undef MOE_RAWBWD
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status launch_balance_stat_switch(const moe_config& cfg, const int* idx, const float* w, const int* counts,
                                       unsigned long long* imp, moe_stats* stats, cudaStream_t st) {
   moe_status s = launch_zero(imp, sizeof(unsigned long long) * cfg.E, nullptr, 0, st);
@@ -571,19 +699,28 @@ moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(router_wgrad_partial_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(router_wgrad_partial_kernel<bf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(router_wgrad_partial_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(router_wgrad_partial_kernel<bf16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(router_wgrad_partial_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr_set[dev] = true;
   }
-  if (cfg.dtype == MOE_BF16)
-    router_wgrad_partial_kernel<bf16><<<grid, RW_WARPS * 32, smem, st>>>(static_cast<const bf16*>(x), idx, dl, cfg.T,
-                                                                         cfg.d, cfg.k, cfg.E, lnc, partial);
+  // raw softmax weights: dl is the dense [T, E] logit gradient
+  const bool dense = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) != 0;
+  if (cfg.dtype == MOE_BF16 && dense)
+    router_wgrad_partial_kernel<bf16, true><<<grid, RW_WARPS * 32, smem, st>>>(
+        static_cast<const bf16*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
+  else if (cfg.dtype == MOE_BF16)
+    router_wgrad_partial_kernel<bf16, false><<<grid, RW_WARPS * 32, smem, st>>>(
+        static_cast<const bf16*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
+  else if (!dense)
+    router_wgrad_partial_kernel<float, false><<<grid, RW_WARPS * 32, smem, st>>>(
+        static_cast<const float*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
   else
-    router_wgrad_partial_kernel<float><<<grid, RW_WARPS * 32, smem, st>>>(static_cast<const float*>(x), idx, dl,
-                                                                          cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
+    return MOE_ERR_UNSUPPORTED;
   const long long Ed = static_cast<long long>(cfg.E) * cfg.d;
   router_wgrad_reduce_kernel<<<static_cast<unsigned>((Ed + 255) / 256), 256, 0, st>>>(partial, nchunks, Ed, dWr);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -594,12 +731,16 @@ void launch_bwd_dx_t(const moe_config& cfg, const float* dXp, const int* pos, co
                      const void* Wr, const void* x, const float* lnc, int accumulate, float* dX, cudaStream_t st) {
   const Tw* w = static_cast<const Tw*>(Wr);
   const Tw* xx = static_cast<const Tw*>(x);
-  if (lnc)
-    bwd_dx_kernel<Tw, KM, true><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k, cfg.d, cfg.E,
-                                                                  xx, lnc, accumulate, dX);
+  const bool dense = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) != 0;
+  if (dense)
+    bwd_dx_kernel<Tw, KM, false, true><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k, cfg.d,
+                                                                         cfg.E, xx, lnc, accumulate, dX);
+  else if (lnc)
+    bwd_dx_kernel<Tw, KM, true, false><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k, cfg.d,
+                                                                         cfg.E, xx, lnc, accumulate, dX);
   else
-    bwd_dx_kernel<Tw, KM, false><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k, cfg.d, cfg.E,
-                                                                   xx, lnc, accumulate, dX);
+    bwd_dx_kernel<Tw, KM, false, false><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k,
+                                                                          cfg.d, cfg.E, xx, lnc, accumulate, dX);
 }
 
 template <typename Tw>

@@ -79,11 +79,12 @@ moe_status launch_grouped_gemm_f32(const GemmParams& p, const void* A, long long
 // least route_scratch_bytes) holds the fp32 logits of the tensor-core path;
 // err: the workspace error word (nullable), zeroed here with counts.
 // backup [T,k] (MOE_ROUTE_REROUTE, else nullable): each token's next-best
-// experts, ranks k .. 2k-1, -1 where none.
+// experts, ranks k .. 2k-1, -1 where none.  out_logits [T,E] (nullable; bf16
+// with scratch only): the final logits the top-k saw.
 size_t route_scratch_bytes(const moe_config& cfg);
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
                         const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* backup,
-                        int* err, cudaStream_t stream);
+                        float* out_logits, int* err, cudaStream_t stream);
 // stats->router_entropy = mean of the finite ent[0..T) (fixed-order fp64 sum).
 moe_status launch_entropy_mean(const float* ent, int T, moe_stats* stats, cudaStream_t stream);
 
@@ -117,6 +118,10 @@ moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* 
 moe_status launch_router_bwd(const moe_config& cfg, const void* x, const void* Wr, const int* idx, const float* w,
                              const int* counts, const float* dot, unsigned long long* imp, float* coef, float* dl,
                              float* lnc, cudaStream_t st);
+// Raw softmax weights: the dense logit gradient dlD [T, E] from the forward's
+// logits, the saved weights, the dots and the balance coefficients.
+moe_status launch_router_bwd_raw(const moe_config& cfg, const float* logits, const int* idx, const float* w,
+                                 const float* dot, const float* coef, float* dlD, cudaStream_t st);
 // stats->balance_stat of MOE_BALANCE_SWITCH: lambda * sum_e (counts[e]/T) (I[e]/T)
 // (imp: E scratch words, zeroed here).
 moe_status launch_balance_stat_switch(const moe_config& cfg, const int* idx, const float* w, const int* counts,

@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(256)
 route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ ebias,
                   const float* __restrict__ noise, int T, int E, int k, int* __restrict__ idx, float* __restrict__ w,
                   int* __restrict__ counts, int raw, float* __restrict__ ent, const bf16* __restrict__ x, int d,
-                  const float* __restrict__ S, int* __restrict__ backup) {
+                  const float* __restrict__ S, int* __restrict__ backup, float* __restrict__ out_logits) {
   extern __shared__ int hist_s[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
   __syncthreads();
@@ -423,6 +423,11 @@ route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restr
       }
     }
     finite = __all_sync(0xffffffffu, finite);
+    if (out_logits) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i < E) out_logits[static_cast<size_t>(t) * E + lane + 32 * i] = v[i];
+    }
     SoftStat sst;
     float sel_v[MAXK];
     int sel_i[MAXK];
@@ -582,12 +587,13 @@ size_t route_scratch_bytes(const moe_config& cfg) {
 
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
                         const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* backup,
-                        int* err, cudaStream_t stream) {
+                        float* out_logits, int* err, cudaStream_t stream) {
   const int raw = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0;
   const bool ln = (cfg.route_flags & MOE_ROUTE_LAYERNORM) != 0;
   if (ln && cfg.dtype == MOE_BF16 && !scratch) return MOE_ERR_UNSUPPORTED;  // the fold needs the workspace path
   if ((cfg.route_flags & MOE_ROUTE_REROUTE) && (!backup || (cfg.dtype == MOE_BF16 && !scratch)))
     return MOE_ERR_UNSUPPORTED;  // the backups live in the workspace
+  if (out_logits && !(cfg.dtype == MOE_BF16 && scratch)) return MOE_ERR_UNSUPPORTED;  // top-k kernel path only
   moe_status zs = launch_zero(counts, sizeof(int) * cfg.E, err, err ? sizeof(int) : 0, stream);
   if (zs != MOE_OK) return zs;
   if (cfg.dtype == MOE_BF16 && scratch) {
@@ -618,7 +624,7 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     const int nv = (cfg.E + 31) / 32;
 #define MOE_TOPK(NVv)                                                                                        \
   route_topk_kernel<NVv><<<grid, 256, hs, stream>>>(logits, ld, expert_bias, noise, cfg.T, cfg.E, cfg.k, idx, w, \
-                                                     counts, raw, ent, xb, cfg.d, S, backup)
+                                                     counts, raw, ent, xb, cfg.d, S, backup, out_logits)
     if (nv <= 1) MOE_TOPK(1);
     else if (nv <= 2) MOE_TOPK(2);
     else if (nv <= 4) MOE_TOPK(4);

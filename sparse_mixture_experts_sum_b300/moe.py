@@ -38,7 +38,7 @@ class MoeWeights(ctypes.Structure):
 
 class MoeSaved(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("idx", "w", "counts", "kept", "offsets", "pos", "Xp", "H", "Yp", "Sx", "Z", "Hs", "Zs")]
+                ("idx", "w", "counts", "kept", "offsets", "pos", "Xp", "H", "Yp", "Sx", "Z", "Hs", "Zs", "logits")]
 
 
 class MoeGrads(ctypes.Structure):
@@ -269,7 +269,7 @@ def moe_selftest_wait_timeout(ws, stream=None):
 def alloc_saved(cfg: MoeConfig, device="cuda", backward=False) -> dict:
     """Caller-owned buffers of one forward (the moe_saved set); with
     backward=True also the pre-activations and shared hidden rows that
-    moe_layer_bwd reads."""
+    moe_layer_bwd reads (and, with raw softmax weights, the logits)."""
     T, k, E, d, h = cfg.T, cfg.k, cfg.E, cfg.d, cfg.h
     dt = torch.bfloat16 if cfg.dtype == DTYPE["bf16"] else torch.float32
     out = dict(idx=torch.empty(T, k, dtype=torch.int32, device=device),
@@ -289,4 +289,6 @@ def alloc_saved(cfg: MoeConfig, device="cuda", backward=False) -> dict:
         if cfg.has_shared:
             out["Hs"] = torch.empty(T, h, dtype=dt, device=device)
             out["Zs"] = torch.empty(T, hz, dtype=dt, device=device)
+        if cfg.route_flags & ROUTE_RAW_PROBS:
+            out["logits"] = torch.empty(T, E, dtype=torch.float32, device=device)
     return out

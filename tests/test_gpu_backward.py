@@ -228,6 +228,26 @@ def test_backward_with_reroute():
     check_all(wl, t, dY, g, ref)
 
 
+@pytest.mark.parametrize("balance", ["cv", "switch"])
+def test_backward_raw_probs(balance):
+    """Raw softmax weights ([P2] 3.2, [P4] 5.1): every logit reaches the loss
+    through the softmax's denominator, so the router gradient is dense over
+    the experts (rows of dWr for experts a token did not pick); the backward
+    reads the forward's saved logits.  Matches the oracle."""
+    wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, seed=83,
+                   lam=500.0 if balance == "switch" else 0.01)
+    t = guarded_inputs(wl, "cpu")
+    dY = t.pop("dY")
+    td = {n: v.to(DEV) for n, v in t.items()}
+    route = dict(raw_probs=True, balance=balance)
+    _, sv, g = run_fwd_bwd(wl, td, dY.to(DEV), **route)
+    ref = oracle_backward(wl, t, dY, **route)
+    np.testing.assert_array_equal(sv["idx"].cpu().numpy(), ref["route"]["idx"])
+    # the saved logits are the ones the oracle routed on
+    np.testing.assert_allclose(sv["logits"].cpu().numpy(), ref["route"]["logits"], rtol=0, atol=2e-4)
+    check_all(wl, t, dY, g, ref)
+
+
 def test_backward_is_deterministic():
     wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, seed=53)
     t = guarded_inputs(wl, DEV)

@@ -804,3 +804,42 @@ def test_backward_with_reroute_finite_differences():
         num = (loss(x, wp) - loss(x, wm)) / (2 * hh)
         got = g["d" + name][ix]
         assert abs(num - got) <= 1e-6 * max(1.0, abs(num)), (name, ix, num, got)
+
+
+@pytest.mark.parametrize("balance", ["cv", "switch"])
+def test_backward_raw_probs_finite_differences(balance):
+    """With raw softmax weights ([P2] 3.2: output = p1*e1 + p2*e2) every
+    logit reaches the loss through the softmax's denominator, so dWr gets
+    rows for unselected experts too: dX and dWr against central
+    differences of L (routing fixed, away from ties)."""
+    rng = _rng(95)
+    T, d, h, E, k = 12, 5, 6, 5, 2
+    w = dict(Wr=rng.normal(size=(E, d)), W1=rng.normal(size=(E, h, d)) / 2, W3=rng.normal(size=(E, h, d)) / 2,
+             W2=rng.normal(size=(E, d, h)) / 3)
+    cfg = dict(T=T, d=d, h=h, E=E, k=k, act="swiglu", capacity_factor=1.0, lam=0.3, raw_probs=True,
+               balance=balance)
+    x = rng.normal(size=(T, d))
+    dY = rng.normal(size=(T, d))
+    g = O.layer_backward(cfg, w, x, dY)
+    # an expert no token selects still gets a router gradient
+    sel = np.zeros(E, bool)
+    sel[np.unique(g["route"]["idx"])] = True
+    assert (np.abs(g["dlogits"]) > 0).sum() > T * k
+
+    def loss(xx, ww):
+        return O.layer_backward(cfg, ww, xx, dY)["loss"]
+
+    hh = 1e-6
+    for (t, i) in [(0, 0), (5, 2), (11, 4)]:
+        xp, xm = x.copy(), x.copy()
+        xp[t, i] += hh
+        xm[t, i] -= hh
+        num = (loss(xp, w) - loss(xm, w)) / (2 * hh)
+        assert abs(num - g["dX"][t, i]) <= 1e-6 * max(1.0, abs(num)), (t, i, num, g["dX"][t, i])
+    for (e, i) in [(0, 1), (2, 3), (4, 0)]:
+        wp = dict(w, Wr=w["Wr"].copy())
+        wm = dict(w, Wr=w["Wr"].copy())
+        wp["Wr"][e, i] += hh
+        wm["Wr"][e, i] -= hh
+        num = (loss(x, wp) - loss(x, wm)) / (2 * hh)
+        assert abs(num - g["dWr"][e, i]) <= 1e-6 * max(1.0, abs(num)), (e, i, num, g["dWr"][e, i])
