@@ -3,17 +3,22 @@
 // gradients (with the load-balance term), the router weight gradient, the
 // GeLU bias gradients, and the assembly of dX.
 //
-// Loss: L = <dY, y> + lambda * CV(I / T), I[e] = the sum of the routing
-// weights of the slots routed to e -- the importance of [P4] "GPT-4 has 1.8
-// trillion parameters..." 2.2, in the std/mean form of [P1] "'More
-// parameters is better' is not the story..." 3.1 (std with n-1, +1e-8 on the
-// mean).  Gradients flow back to the router and to the chosen experts
-// ([P1] 3.3).  Per slot (t, j) routed to e:
+// Loss: L = <dY, y> + B(I / T), I[e] = the sum of the routing weights of
+// the slots routed to e -- the importance of [P4] "GPT-4 has 1.8 trillion
+// parameters..." 2.2 -- and B the balance term: lambda * CV in the std/mean
+// form of [P1] "'More parameters is better' is not the story..." 3.1 (std
+// with n-1, +1e-8 on the mean), or lambda * (std + gamma * max) ([P2] 3.2),
+// or lambda * sum_e (counts_e / T) g_e ([P3] 2.3).  Gradients flow back to
+// the router and to the experts that served the slots ([P1] 3.3).  Per slot
+// (t, j) routed to e:
 //   dot[t,j] = <dY[t], Yp[pos[t,j]]>          (kept slots; 0 when dropped)
-//   G[t,j]   = dot[t,j] + d(lambda CV)/dw[t,j]
+//   G[t,j]   = dot[t,j] + dB/dw[t,j]
 //   dl[t,j]  = w[t,j] (G[t,j] - sum_j' w[t,j'] G[t,j'])   (softmax over the
 //              selected logits, [P1] 3.3; the other logits get no gradient)
 //   dWr[e]  += dl[t,j] x[t];   dX[t] += dl[t,j] Wr[e]
+// With raw softmax weights (w_j = p_{idx_j} over all E) every logit gets
+// p_e ([e selected] G_e - sum_j w_j G_j), and dWr, dX take that dense
+// [T, E] gradient.
 // Every reduction runs in a fixed order or in integers, so the results are
 // the same bits on every run.
 //

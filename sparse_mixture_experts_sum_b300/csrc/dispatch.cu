@@ -12,10 +12,14 @@
 //   Xp[pos[t,j]] = x[t]
 // Four launches, all integer and deterministic (no order-visible atomics):
 //   slot_hist   per chunk of 1024 (or 4096) slots, per-expert counts (+ unrouted)
-//   scan        per-expert exclusive scan over chunks (a warp per expert),
-//               kept, offsets, stats
+//   scan        per-expert exclusive scan over chunks (several lanes per
+//               expert), kept, offsets, stats from integer sums
 //   assign      in-chunk ranks (warp match + per-warp counts), pos
 //   permute     one warp per token copies its row to its k destinations
+// Token-major priority orders the slots s = t*k + j instead.  Rerouting on
+// overflow ([P3] 2.3: the next-best expert) runs slot_hist, scan and assign
+// a second time over the slots the first pass dropped, each asking for its
+// token's backup expert against the room left.
 //
 // Combine ([P5] "Training a 200B LLM from scratch 5/25", "Who decides which
 // experts to call?": y = 0.75*E1(x) + 0.25*E3(x); "Shared experts": the
