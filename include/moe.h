@@ -166,10 +166,12 @@ typedef struct {
   void* Yp;      /* [T*k, d] expert outputs, permuted order                */
   void* Sx;      /* [T, d]   shared-expert output (has_shared)             */
   /* Pre-activations and the shared hidden rows, written by a training
-   * forward when non-NULL and read by moe_layer_bwd (bf16 only):          */
-  void* Z;       /* [T*k, 2h] SwiGLU gate | up  (GeLU: [T*k, h], W1 v + b1) */
+   * forward when non-NULL and read by moe_layer_bwd (bf16 layers only).
+   * Z and Zs are fp32, whatever the storage type: the backward evaluates
+   * silu'/gelu' on them, and a bf16 copy would put a 2^-9 rounding there. */
+  float* Z;      /* [T*k, 2h] SwiGLU gate | up  (GeLU: [T*k, h], W1 v + b1) */
   void* Hs;      /* [T, h]   shared expert's activated hidden rows          */
-  void* Zs;      /* [T, 2h]  shared expert's pre-activations (GeLU [T, h])  */
+  float* Zs;     /* [T, 2h]  shared expert's pre-activations (GeLU [T, h])  */
   float* logits; /* [T, E]   the router's final logits (bias, noise and the
                               LayerNorm applied), fp32: written by a bf16
                               forward when non-NULL; moe_layer_bwd reads them
@@ -275,9 +277,11 @@ moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x,
  *   call whose scratch need exceeds it returns MOE_ERR_UNSUPPORTED before
  *   any launch; every T*k <= 2^20 (1,048,576 slots) fits at any E <= 1024.
  *   Allocation: none -- no cudaMalloc, cudaFree or allocating library call.
- *   Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, device current); make that first call before
- *   any stream capture.
+ *   Set-up: every call looks up the array's device address on the current
+ *   device (cudaGetSymbolAddress, which allocates nothing) instead of
+ *   keeping it from an earlier call, so an address cannot go stale across a
+ *   cudaDeviceReset.  The first call on a device also loads the library's
+ *   module there: make that first call before any stream capture.
  *   Sharing: all calls on a device share the one array and it keeps the
  *   last call's contents; nothing in it has to start at zero (each call
  *   writes every word it later reads).  Calls whose work overlaps on the
@@ -349,9 +353,12 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
  *   silu'(z) = s (1 + z (1 - s)) and gelu'(z) = Phi(z) + z phi(z).
  * Noise and the expert bias are additive constants of the logits and get no
  * gradient.  x, wts: the forward's inputs; saved: the forward's moe_saved
- * with Z (and Hs, Zs with a shared expert) filled; dY [T,d] bf16.  Sums run
- * in a fixed order (integers for the importance), so repeated calls give
- * the same bits.  ws_bytes >= moe_workspace_size(cfg, 2). */
+ * with Z (and Zs with a shared expert) filled -- H and Hs are not read:
+ * the backward forms w * act(z) again from the fp32 pre-activations, in
+ * bf16 plus its bf16 residual, for the W2 gradients; dY [T,d] bf16.  The
+ * expert GEMMs contract dY as stored and apply the routing weight in fp32.
+ * Sums run in a fixed order (integers for the importance), so repeated
+ * calls give the same bits.  ws_bytes >= moe_workspace_size(cfg, 2). */
 moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const void* x,
                          const moe_saved* saved, const void* dY, const moe_grads* grads,
                          void* ws, size_t ws_bytes, moe_stream_t stream);

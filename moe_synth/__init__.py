@@ -181,6 +181,7 @@ class Workload:
     gumbel: bool                 # Gumbel(0,1) noise on the router logits
     training: bool
     x_affine: bool = False       # rows of x with their own offset and scale
+    zipf_log: bool = False       # the Zipf bias as ln(pmf) instead of the pmf itself
 
     def std(self, fan_in: int) -> float:
         return self.weight_std if self.weight_std is not None else 1.0 / math.sqrt(fan_in)
@@ -199,6 +200,12 @@ WORKLOADS: Dict[str, Workload] = {
     # T=16384, d=4096, E=64, SwiGLU h=14336, cf=1.25 (C=640), Zipf(1.1) logit bias
     "large_prefill": Workload("large_prefill", 16384, 4096, 14336, 64, 2, "swiglu", "bf16",
                               1.25, 0, 0.01, False, 2, None, 1.1, False, False),
+    # stress variant of the large prefill: the Zipf(1.1) bias taken as ln(pmf)
+    # (a logit spread of 4.6 between the first and last expert), so that the
+    # popular experts overflow their capacity (~75% of slots dropped) and
+    # most experts receive fewer than one 128-row tile
+    "large_prefill_3z": Workload("large_prefill_3z", 16384, 4096, 14336, 64, 2, "swiglu", "bf16",
+                                 1.25, 0, 0.01, False, 2, None, 1.1, False, False, zipf_log=True),
     # four experts of the large prefill layer at its rows per expert (~512):
     # the same GEMM tile shapes at 1/16 of the device memory (profiling case)
     "large_prefill_slice": Workload("large_prefill_slice", 1024, 4096, 14336, 4, 2, "swiglu", "bf16",
@@ -265,7 +272,8 @@ def make_inputs(wl: Workload, device="cpu", parts: Optional[Iterable[str]] = Non
         if need("Ws2"):
             out["Ws2"] = tensor("normal", s, TID["Ws2"], (d, h), dt, wl.std(h), device)
     if wl.zipf_s is not None and need("expert_bias"):
-        out["expert_bias"] = zipf_pmf(E, wl.zipf_s).to(torch.float32).to(device)
+        pmf = zipf_pmf(E, wl.zipf_s)
+        out["expert_bias"] = (torch.log(pmf) if wl.zipf_log else pmf).to(torch.float32).to(device)
     if wl.gumbel and need("noise"):
         out["noise"] = tensor("gumbel", s, TID["noise"], (T, E), "f32", 1.0, device)
     if wl.training and need("dY"):

@@ -48,6 +48,7 @@ P1's balance term; its forward statistic stays the count-based one.
 from __future__ import annotations
 
 import math
+from fractions import Fraction
 from typing import Dict, Optional
 
 import numpy as np
@@ -178,10 +179,13 @@ def softmax(l: np.ndarray) -> np.ndarray:
 def expert_capacity(T: int, k: int, E: int, capacity_factor: float, min_capacity: int = 0) -> int:
     """C = max(min_capacity, ceil(cf * T * k / E)); no limit (C = T) if cf <= 0.
 
-    [P3] 2.3's worked case: batch 1024, k=2, 16 experts -> (1024*2)/16 = 128."""
+    [P3] 2.3's worked case: batch 1024, k=2, 16 experts -> (1024*2)/16 = 128.
+    The ceiling is taken of the exact value of cf*T*k/E, cf being the binary
+    number the caller passed (a rational), so no rounding of the product can
+    move C by one."""
     if capacity_factor <= 0:
         return T
-    c = math.ceil(capacity_factor * T * k / E - 1e-9)
+    c = math.ceil(Fraction(capacity_factor) * T * k / E)
     return max(int(min_capacity), int(c))
 
 
@@ -687,18 +691,71 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
 # ----------------------------------------------------------------------------
 
 
+def _served(route: dict) -> np.ndarray:
+    """The expert that serves each slot: the route's own map when it has one
+    (with rerouting a dropped slot may be served by a backup), else the
+    router's choice where the slot was kept and -1 where it was dropped."""
+    if route.get("served") is not None:
+        return route["served"]
+    return np.where(route["pos"] >= 0, route["idx"], -1)
+
+
+def _slot_dots(cfg: dict, weights: dict, X: np.ndarray, Y: np.ndarray, served: np.ndarray) -> np.ndarray:
+    """G[i,j] = <Y[i], FFN_e(X[i])> for the expert e = served[i,j] of each
+    kept slot (0 for a dropped slot): the upstream term of the routing
+    weight's gradient."""
+    act = cfg["act"]
+    G = np.zeros(served.shape)
+    for e in sorted(set(served[served >= 0].tolist())):
+        rr, ss = np.nonzero(served == e)
+        out = expert_ffn(X[rr], act, **expert_params(weights, e, act))
+        G[rr, ss] = np.einsum("nd,nd->n", Y[rr], out)
+    return G
+
+
+def _logit_grads(cfg: dict, route: dict, toks: np.ndarray, G: np.ndarray) -> np.ndarray:
+    """dl[i, e] for the listed tokens, layer_backward's rule: renormalised
+    weights give w_j (G_j - sum_j' w_j' G_j') at the selected experts and 0
+    elsewhere; raw softmax weights give p_e ([e selected] G_e - sum_j w_j G_j)
+    at every expert (p the softmax of the route's logits)."""
+    E, k = cfg["E"], cfg["k"]
+    idx, w = route["idx"], route["w"]
+    dl = np.zeros((len(toks), E))
+    if cfg.get("raw_probs"):
+        L = route["logits"][toks]
+        P = softmax(np.where(np.isfinite(L), L, 0.0))
+    for i, t in enumerate(toks):
+        if idx[t, 0] < 0:
+            continue
+        s = (w[t] * G[i]).sum()
+        if cfg.get("raw_probs"):
+            dl[i] = -P[i] * s
+            for j in range(k):
+                dl[i, idx[t, j]] += P[i, idx[t, j]] * G[i, j]
+        else:
+            for j in range(k):
+                dl[i, idx[t, j]] += w[t, j] * (G[i, j] - s)
+    return dl
+
+
+def _rows(a, ix) -> np.ndarray:
+    """Rows ix of a stored tensor (numpy or torch, any device), decoded."""
+    return decode(a[_as_index(a, ix)]) if hasattr(a, "index_select") else decode(a)[np.asarray(ix)]
+
+
 def expert_grad_slices(cfg: dict, weights: dict, x, dY, route: dict, e: int, cols) -> Dict[str, np.ndarray]:
     """Weight gradients of expert e restricted to hidden units `cols`, summed
-    over all of the expert's kept rows: dW1[e][cols,:], dW3[e][cols,:] (or
+    over all of the rows the expert serves (with rerouting, a backup's rows
+    include the slots moved to it): dW1[e][cols,:], dW3[e][cols,:] (or
     db1[e][cols] for GeLU) and dW2[e][:,cols].  The chain rule of
-    expert_ffn_backward with the upstream gradient w[t,j] dY[t] of each kept
-    slot; a hidden unit's gradients depend only on that unit's row of W1/W3
-    and column of W2, so the slice is exact."""
+    expert_ffn_backward with the upstream gradient w[t,j] dY[t] of each
+    served slot; a hidden unit's gradients depend only on that unit's row of
+    W1/W3 and column of W2, so the slice is exact."""
     act = cfg["act"]
     cols = np.asarray(cols)
-    rows, slots = np.nonzero((route["idx"] == e) & (route["pos"] >= 0))
-    X = decode(x)[rows] if not hasattr(x, "index_select") else decode(x[_as_index(x, rows)])
-    Y = decode(dY)[rows] if not hasattr(dY, "index_select") else decode(dY[_as_index(dY, rows)])
+    rows, slots = np.nonzero(_served(route) == e)
+    X = _rows(x, rows)
+    Y = _rows(dY, rows)
     g_out = route["w"][rows, slots][:, None] * Y
     W1 = decode(weights["W1"][e][_as_index(weights["W1"], cols)])
     W2 = decode(weights["W2"][e][:, _as_index(weights["W2"], cols)])
@@ -724,40 +781,60 @@ def expert_grad_slices(cfg: dict, weights: dict, x, dY, route: dict, e: int, col
 
 
 def token_input_grads(cfg: dict, weights: dict, x, dY, route: dict, tokens) -> np.ndarray:
-    """dX[t] for the listed tokens: the router term sum_j dl[t,j] Wr[idx_j]
-    (dl from layer_backward's rule, with the balance term over the whole
-    batch), plus each kept slot's expert input gradient for w[t,j] dY[t],
-    plus the shared expert's for dY[t]."""
-    T, k, E = cfg["T"], cfg["k"], cfg["E"]
+    """dX[t] for the listed tokens: the router term sum_e dl[t,e] Wr[e] (dl
+    from layer_backward's rule, with the balance term over the whole batch;
+    through the LayerNorm's backward when the router normalises), plus each
+    served slot's expert input gradient for w[t,j] dY[t], plus the shared
+    expert's for dY[t]."""
+    T, E = cfg["T"], cfg["E"]
     act = cfg["act"]
     toks = np.asarray(tokens)
-    idx, w, pos = route["idx"], route["w"], route["pos"]
-    X = decode(x[_as_index(x, toks)]) if hasattr(x, "index_select") else decode(x)[toks]
-    Y = decode(dY[_as_index(dY, toks)]) if hasattr(dY, "index_select") else decode(dY)[toks]
+    idx, w = route["idx"], route["w"]
+    served = _served(route)[toks]
+    X = _rows(x, toks)
+    Y = _rows(dY, toks)
     dX = np.zeros_like(X)
-    G = np.zeros((len(toks), k))
-    for e in sorted(set(idx[toks][pos[toks] >= 0].tolist())):
-        rr, ss = np.nonzero((idx[toks] == e) & (pos[toks] >= 0))
-        We = expert_params(weights, e, act)
-        g = _input_grad_rows(X[rr], w[toks[rr], ss][:, None] * Y[rr], act, We)
+    G = np.zeros(served.shape)
+    for e in sorted(set(served[served >= 0].tolist())):
+        rr, ss = np.nonzero(served == e)
+        g = _input_grad_rows(X[rr], w[toks[rr], ss][:, None] * Y[rr], act, expert_params(weights, e, act))
         np.add.at(dX, rr, g["dv"])
-        G[rr, ss] += np.einsum("nd,nd->n", Y[rr], g["out"])
+        G[rr, ss] = np.einsum("nd,nd->n", Y[rr], g["out"])
     if cfg.get("has_shared"):
         g = _input_grad_rows(X, Y, act, shared_params(weights, act))
         dX += g["dv"]
     _, dcv = balance_term_grad(idx, w, E, T, cfg.get("lam", 0.01), cfg.get("balance", "cv"),
                                cfg.get("gamma", 100.0))
     G += dcv[toks]
-    Wr = decode(weights["Wr"])
-    g = np.zeros_like(X)
-    for i, t in enumerate(toks):
-        if idx[t, 0] < 0:
-            continue
-        s = (w[t] * G[i]).sum()
-        for j in range(k):
-            g[i] += w[t, j] * (G[i, j] - s) * Wr[idx[t, j]]
+    g = _logit_grads(cfg, route, toks, G) @ decode(weights["Wr"])
     dX += layer_norm_backward(X, g) if cfg.get("layernorm") else g
     return dX
+
+
+def router_grad_rows(cfg: dict, weights: dict, x, dY, route: dict, experts) -> np.ndarray:
+    """Rows `experts` of the router weight gradient dWr over the whole
+    batch: sum over tokens t of dl[t,e] x[t] (LayerNorm(x[t]) when the router
+    normalises), dl by layer_backward's rule.  With renormalised weights
+    dl[t,e] is 0 unless e is one of t's selected experts, so only the tokens
+    routed to one of `experts` contribute, and only their slots' expert
+    outputs are computed -- every served slot of each such token, since
+    dl[t,e] involves the token's sum_j w_j G_j.  Raw softmax weights reach
+    every row from every token; use layer_backward there."""
+    if cfg.get("raw_probs"):
+        raise ValueError("router_grad_rows: with raw softmax weights every token reaches every row")
+    T, E = cfg["T"], cfg["E"]
+    experts = np.asarray(experts)
+    idx, w = route["idx"], route["w"]
+    toks = np.nonzero(np.isin(idx, experts).any(axis=1))[0]
+    X = _rows(x, toks)
+    Y = _rows(dY, toks)
+    G = _slot_dots(cfg, weights, X, Y, _served(route)[toks])
+    _, dcv = balance_term_grad(idx, w, E, T, cfg.get("lam", 0.01), cfg.get("balance", "cv"),
+                               cfg.get("gamma", 100.0))
+    G += dcv[toks]
+    dl = _logit_grads(cfg, route, toks, G)
+    Xr = layer_norm(X) if cfg.get("layernorm") else X
+    return dl[:, experts].T @ Xr
 
 
 def _input_grad_rows(v, g_out, act, p):

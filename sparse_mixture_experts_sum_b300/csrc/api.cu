@@ -28,12 +28,30 @@ moe_status validate(const moe_config* cfg) {
 }
 
 int capacity_of(const moe_config* cfg) {
-  if (cfg->capacity_factor <= 0.f) return cfg->T;
-  // ceil(cf*T*k/E) in double, guarded against representation noise
-  const double v = static_cast<double>(cfg->capacity_factor) * cfg->T * cfg->k / cfg->E;
-  long long c = static_cast<long long>(ceil(v - 1e-9));
+  const float cf = cfg->capacity_factor;
+  if (cf <= 0.f) return cfg->T;
+  // ceil(cf*T*k/E) of the exact value: cf = m * 2^e with m a 24-bit
+  // integer, so the quotient is a ratio of integers and the ceiling is
+  // taken in 128-bit integer arithmetic, free of rounding.
+  long long c;
+  if (static_cast<double>(cf) * cfg->T * cfg->k / cfg->E >= 2147483647.0) {
+    c = 2147483647LL;
+  } else {
+    int e2 = 0;
+    const float fr = frexpf(cf, &e2);  // cf = fr * 2^e2, fr in [0.5, 1)
+    const long long m = static_cast<long long>(ldexpf(fr, 24));
+    const int e = e2 - 24;              // cf = m * 2^e exactly
+    if (e < -100) {
+      c = 1;  // 0 < cf*T*k/E < 2^30 * 2^24 * 2^-100 < 1
+    } else {
+      __int128 num = static_cast<__int128>(m) * cfg->T * cfg->k;
+      __int128 den = cfg->E;
+      if (e >= 0) num <<= e;
+      else den <<= -e;
+      c = static_cast<long long>((num + den - 1) / den);
+    }
+  }
   if (c < cfg->min_capacity) c = cfg->min_capacity;
-  if (c > 2147483647LL) c = 2147483647LL;
   return static_cast<int>(c);
 }
 
@@ -41,12 +59,13 @@ size_t esize(const moe_config* cfg) { return cfg->dtype == MOE_BF16 ? 2 : 4; }
 
 // Workspace carving.  training 0/1 (forward): [header | dispatch scratch |
 // (inference) intermediates | shared hidden].  training 2 (backward):
-// [header | dYp | dAB | dXp | dot | dl | importance | coef | router partials
-// | shared dAB | LayerNorm terms].
+// [header | dYg | slot weights | weighted hidden rows (hi, lo) | dAB | dXp |
+// dot | dl | importance | coef | router partials | shared dAB | LayerNorm
+// terms | dense logit gradient].
 struct WsLayout {
   size_t dispatch_off, route_off, ent, backup;
   size_t idx, w, counts, kept, offsets, pos, Xp, H, Yp, Sx, Hs;
-  size_t dYp, dAB, dXp, dot, dl, imp, coef, rpart, dABs, lnc, dld;
+  size_t dYg, wp, Hw, Hw_lo, dAB, dXp, dot, dl, imp, coef, rpart, dABs, lnc, dld;
   size_t total;
 };
 
@@ -61,7 +80,10 @@ WsLayout layout(const moe_config* cfg, int training) {
     return at;
   };
   if (training == 2) {
-    L.dYp = take(T * k * d * es);
+    L.dYg = take(T * k * d * es);
+    L.wp = take(T * k * 4);
+    L.Hw = take(T * k * h * es);
+    L.Hw_lo = take(T * k * h * es);
     L.dAB = take(T * k * hz * es);
     L.dXp = take(T * k * d * 4);
     L.dot = take(T * k * 4);
@@ -166,18 +188,23 @@ moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, cons
 }
 
 // Backward of one expert group set (routed: G experts over offsets; shared:
-// G = 1 over `rows` rows).  dYp [a_rows, d] is the upstream gradient in
-// expert order, Z the saved pre-activations, H the saved hidden rows, Xin
-// the forward input rows.  Writes dAB (scratch), dXin (fp32, [a_rows, d]),
+// G = 1 over `rows` rows).  dYg [a_rows, d] holds the upstream gradient
+// rows in expert order as stored, and wp [a_rows] each row's routing weight
+// (nullable: 1), so the expert's upstream gradient is wp[r] * dYg[r].  Z:
+// the saved fp32 pre-activations; Xin: the forward input rows.  The Dgrad
+// epilogue leaves wp[r] * act(z[r]) in Hw + Hw_lo (scratch [a_rows, h] each:
+// its bf16 rounding and the bf16 residual), and the W2 gradient contracts
+// dYg with both, so that gradient carries no rounding of its operands
+// beyond 2^-16.  Writes dAB (scratch), dXin (fp32, [a_rows, d]),
 // dW1/dW3/dW2 (fp32) and, for GeLU, db1/db2.
 moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offsets, int G, int rows,
-                       const void* dYp, const void* Z, const void* H, const void* Xin, const void* W1,
-                       const void* W3, const void* W2, void* dAB, float* dXin, float* dW1, float* dW3, float* dW2,
-                       float* db1, float* db2, int* err, cudaStream_t st) {
+                       const void* dYg, const float* wp, const float* Z, void* Hw, void* Hw_lo, const void* Xin,
+                       const void* W1, const void* W3, const void* W2, void* dAB, float* dXin, float* dW1,
+                       float* dW3, float* dW2, float* db1, float* db2, int* err, cudaStream_t st) {
   const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
   const int h = cfg->h, d = cfg->d;
   const long long hz = swiglu ? 2LL * h : h;
-  // dH = dYp . W2_g -> activation backward -> dAB = [dA | dB] (or dZ)
+  // dH = wp * (dYg . W2_g) -> activation backward -> dAB = [dA | dB] (or dZ)
   GemmParams a{};
   a.offsets = offsets;
   a.G = G;
@@ -189,8 +216,11 @@ moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offse
   a.ldo = hz;
   a.zin = Z;
   a.ldz = hz;
+  a.row_scale = wp;
+  a.hout = Hw;
+  a.hout_lo = Hw_lo;
   a.err = err;
-  moe_status s = launch_grouped_gemm_tc(a, kKindDgrad, dYp, a_rows, W2, nullptr, static_cast<long long>(G) * d, st);
+  moe_status s = launch_grouped_gemm_tc(a, kKindDgrad, dYg, a_rows, W2, nullptr, static_cast<long long>(G) * d, st);
   if (s != MOE_OK) return s;
   // dXin = dA . W1_g + dB . W3_g  (fp32)
   GemmParams b{};
@@ -207,7 +237,7 @@ moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offse
   s = launch_grouped_gemm_tc(b, kKindDgrad, dAB, a_rows, W1, swiglu ? W3 : nullptr, static_cast<long long>(G) * h,
                              st);
   if (s != MOE_OK) return s;
-  // dW2_g = dYp_g^T . H_g
+  // dW2_g = dYg_g^T . (Hw + Hw_lo)_g, Hw + Hw_lo = wp * act(Z)
   GemmParams c{};
   c.offsets = offsets;
   c.G = G;
@@ -217,8 +247,9 @@ moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offse
   c.mode = kModePlain;
   c.out_f32 = 1;
   c.out = dW2;
+  c.b_lo = 1;
   c.err = err;
-  s = launch_grouped_gemm_tc(c, kKindWgrad, dYp, a_rows, H, nullptr, a_rows, st);
+  s = launch_grouped_gemm_tc(c, kKindWgrad, dYg, a_rows, Hw, Hw_lo, a_rows, st);
   if (s != MOE_OK) return s;
   // [dW1; dW3]_g = [dA | dB]_g^T . Xin_g
   GemmParams w{};
@@ -237,11 +268,11 @@ moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offse
   if (s != MOE_OK) return s;
   if (!swiglu) {
     if (db1) {
-      s = launch_group_colsum(dAB, hz, offsets, G, rows, h, db1, st);
+      s = launch_group_colsum(dAB, hz, offsets, G, rows, h, nullptr, db1, st);
       if (s != MOE_OK) return s;
     }
     if (db2) {
-      s = launch_group_colsum(dYp, d, offsets, G, rows, d, db2, st);
+      s = launch_group_colsum(dYg, d, offsets, G, rows, d, wp, db2, st);
       if (s != MOE_OK) return s;
     }
   }
@@ -388,7 +419,9 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
     S.H = at(ws, L.H);
     S.Yp = at(ws, L.Yp);
     S.Sx = cfg->has_shared ? at(ws, L.Sx) : nullptr;
-    S.Z = S.Hs = S.Zs = nullptr;
+    S.Z = nullptr;
+    S.Hs = nullptr;
+    S.Zs = nullptr;
     S.logits = nullptr;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -446,9 +479,9 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   if (!wts->Wr || !wts->W1 || !wts->W2 || (swiglu && !wts->W3)) return MOE_ERR_INVALID_ARG;
   if (cfg->has_shared && (!wts->Ws1 || !wts->Ws2 || (swiglu && !wts->Ws3))) return MOE_ERR_INVALID_ARG;
   const moe_saved& S = *saved;
-  if (!S.idx || !S.w || !S.offsets || !S.pos || !S.Xp || !S.H || !S.Yp || !S.Z) return MOE_ERR_INVALID_ARG;
+  if (!S.idx || !S.w || !S.offsets || !S.pos || !S.Xp || !S.Yp || !S.Z) return MOE_ERR_INVALID_ARG;
   if (raw && !S.logits) return MOE_ERR_INVALID_ARG;
-  if (cfg->has_shared && (!S.Hs || !S.Zs)) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_shared && !S.Zs) return MOE_ERR_INVALID_ARG;
   const moe_grads& g = *grads;
   if (!g.dX || !g.dWr || !g.dW1 || !g.dW2 || (swiglu && !g.dW3)) return MOE_ERR_INVALID_ARG;
   if (cfg->has_shared && (!g.dWs1 || !g.dWs2 || (swiglu && !g.dWs3))) return MOE_ERR_INVALID_ARG;
@@ -460,7 +493,8 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   int* err = static_cast<int*>(ws);
   s = launch_zero(err, sizeof(int), at(ws, L.imp), sizeof(unsigned long long) * cfg->E, st);
   if (s != MOE_OK) return s;
-  void* dYp = at(ws, L.dYp);
+  void* dYg = at(ws, L.dYg);
+  float* wp = static_cast<float*>(at(ws, L.wp));
   void* dAB = at(ws, L.dAB);
   float* dXp = static_cast<float*>(at(ws, L.dXp));
   float* dot = static_cast<float*>(at(ws, L.dot));
@@ -468,7 +502,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
 
   // routing-weight gradients and the router
-  s = launch_bwd_gather(*cfg, dY, S.Yp, S.pos, S.w, dYp, dot, st);
+  s = launch_bwd_gather(*cfg, dY, S.Yp, S.pos, S.w, dYg, wp, dot, st);
   if (s != MOE_OK) return s;
   float* lnc = (cfg->route_flags & MOE_ROUTE_LAYERNORM) ? static_cast<float*>(at(ws, L.lnc)) : nullptr;
   if (cfg->balance == MOE_BALANCE_SWITCH && !S.counts) return MOE_ERR_INVALID_ARG;
@@ -486,13 +520,15 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
   s = launch_router_wgrad(*cfg, x, S.idx, dl, lnc, static_cast<float*>(at(ws, L.rpart)), g.dWr, st);
   if (s != MOE_OK) return s;
   // routed experts
-  s = run_ffn_bwd(cfg, a_rows, S.offsets, cfg->E, 0, dYp, S.Z, S.H, S.Xp, wts->W1, wts->W3, wts->W2, dAB, dXp, g.dW1,
-                  g.dW3, g.dW2, g.db1, g.db2, err, st);
+  s = run_ffn_bwd(cfg, a_rows, S.offsets, cfg->E, 0, dYg, wp, S.Z, at(ws, L.Hw), at(ws, L.Hw_lo), S.Xp, wts->W1,
+                  wts->W3, wts->W2, dAB, dXp, g.dW1, g.dW3, g.dW2, g.db1, g.db2, err, st);
   if (s != MOE_OK) return s;
-  // shared expert: its input gradient lands in dX directly
+  // shared expert: its input gradient lands in dX directly (its weighted
+  // hidden rows reuse the routed experts' scratch, T <= T*k rows, after the
+  // routed launches on the same stream)
   if (cfg->has_shared) {
-    s = run_ffn_bwd(cfg, cfg->T, nullptr, 1, cfg->T, dY, S.Zs, S.Hs, x, wts->Ws1, wts->Ws3, wts->Ws2,
-                    at(ws, L.dABs), g.dX, g.dWs1, g.dWs3, g.dWs2, g.dbs1, g.dbs2, err, st);
+    s = run_ffn_bwd(cfg, cfg->T, nullptr, 1, cfg->T, dY, nullptr, S.Zs, at(ws, L.Hw), at(ws, L.Hw_lo), x, wts->Ws1,
+                    wts->Ws3, wts->Ws2, at(ws, L.dABs), g.dX, g.dWs1, g.dWs3, g.dWs2, g.dbs1, g.dbs2, err, st);
     if (s != MOE_OK) return s;
   }
   return launch_bwd_dx(*cfg, dXp, S.pos, S.idx, dl, wts->Wr, x, lnc, cfg->has_shared ? 1 : 0, g.dX, st);

@@ -40,12 +40,15 @@ namespace {
 constexpr double kImpScale = 4294967296.0;  // routing weights accumulate as 2^-32 fixed point
 constexpr int MAXK_BWD = 8;                  // largest k
 
-// One warp per token: dot[t,j] = <dY[t], Yp[pos]>, dYp[pos] = w[t,j] dY[t].
-// KM = k rounded up to 2, 4 or 8 sizes the per-slot register arrays.
+// One warp per token: dot[t,j] = <dY[t], Yp[pos]>, dYg[pos] = dY[t] (the
+// stored bits: the routing weight is applied in fp32 by the expert GEMMs'
+// epilogue, not folded into a rounded copy), wp[pos] = w[t,j].  KM = k
+// rounded up to 2, 4 or 8 sizes the per-slot register arrays.
 template <int KM>
 __global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ Yp,
                                   const int* __restrict__ pos, const float* __restrict__ w, int T, int k,
-                                  int vec_per_row, uint4* __restrict__ dYp, float* __restrict__ dot) {
+                                  int vec_per_row, uint4* __restrict__ dYg, float* __restrict__ wp,
+                                  float* __restrict__ dot) {
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -65,14 +68,12 @@ __global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __r
       if (p[j] < 0) continue;
       const uint4 yq = Yp[static_cast<size_t>(p[j]) * vec_per_row + v];
       const uint32_t y[4] = {yq.x, yq.y, yq.z, yq.w};
-      uint32_t o[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc[j] = fmaf(bf16lo(g[i]), bf16lo(y[i]), acc[j]);
         acc[j] = fmaf(bf16hi(g[i]), bf16hi(y[i]), acc[j]);
-        o[i] = pack_bf16(wt[j] * bf16lo(g[i]), wt[j] * bf16hi(g[i]));
       }
-      dYp[static_cast<size_t>(p[j]) * vec_per_row + v] = make_uint4(o[0], o[1], o[2], o[3]);
+      dYg[static_cast<size_t>(p[j]) * vec_per_row + v] = q;
     }
   }
 #pragma unroll
@@ -80,7 +81,10 @@ __global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __r
     float s = acc[j];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0 && j < k) dot[static_cast<size_t>(t) * k + j] = p[j] >= 0 ? s : 0.f;
+    if (lane == 0 && j < k) {
+      dot[static_cast<size_t>(t) * k + j] = p[j] >= 0 ? s : 0.f;
+      if (p[j] >= 0) wp[p[j]] = wt[j];
+    }
   }
 }
 
@@ -611,16 +615,20 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
   }
 }
 
-// out[g][n] = sum of src[r][n] over the rows r of group g (ascending).
+// out[g][n] = sum of scale[r] src[r][n] over the rows r of group g
+// (ascending; scale nullable: 1).
 __global__ void group_colsum_kernel(const bf16* __restrict__ src, long long ld, const int* __restrict__ offsets,
-                                    int rows, int N, float* __restrict__ out) {
+                                    int rows, int N, const float* __restrict__ scale, float* __restrict__ out) {
   const int g = blockIdx.y;
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= N) return;
   const int r0 = offsets ? offsets[g] : 0;
   const int r1 = offsets ? offsets[g + 1] : rows;
   float s = 0.f;
-  for (int r = r0; r < r1; ++r) s += __bfloat162float(src[static_cast<size_t>(r) * ld + n]);
+  for (int r = r0; r < r1; ++r) {
+    const float v = __bfloat162float(src[static_cast<size_t>(r) * ld + n]);
+    s = scale ? fmaf(scale[r], v, s) : s + v;
+  }
   out[static_cast<size_t>(g) * N + n] = s;
 }
 
@@ -634,16 +642,17 @@ size_t router_wgrad_partial_bytes(const moe_config& cfg) {
 }
 
 moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* Yp, const int* pos, const float* w,
-                             void* dYp, float* dot, cudaStream_t st) {
+                             void* dYg, float* wp, float* dot, cudaStream_t st) {
   const uint4* dy = static_cast<const uint4*>(dY);
   const uint4* yp = static_cast<const uint4*>(Yp);
-  uint4* dyp = static_cast<uint4*>(dYp);
+  uint4* dyg = static_cast<uint4*>(dYg);
+  const int nv = cfg.d / 8;
   if (cfg.k <= 2)
-    bwd_gather_kernel<2><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, cfg.d / 8, dyp, dot);
+    bwd_gather_kernel<2><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, nv, dyg, wp, dot);
   else if (cfg.k <= 4)
-    bwd_gather_kernel<4><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, cfg.d / 8, dyp, dot);
+    bwd_gather_kernel<4><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, nv, dyg, wp, dot);
   else
-    bwd_gather_kernel<8><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, cfg.d / 8, dyp, dot);
+    bwd_gather_kernel<8><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, nv, dyg, wp, dot);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -700,19 +709,19 @@ moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* 
   const int nchunks = (cfg.T + RW_TOK - 1) / RW_TOK;
   dim3 grid(nchunks, (cfg.d + RW_COLS - 1) / RW_COLS, (cfg.E + RW_EXP - 1) / RW_EXP);
   const size_t smem = sizeof(float) * RW_WARPS * RW_EXP * 8 * 32;
-  static bool attr_set[64] = {false};
+  static DeviceOnce attr;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(router_wgrad_partial_kernel<bf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(router_wgrad_partial_kernel<bf16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(router_wgrad_partial_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const moe_status sa = attr.run(dev, [&] {
+    const int b = static_cast<int>(smem);
+    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    return cudaFuncSetAttribute(router_wgrad_partial_kernel<bf16, false>, a, b) == cudaSuccess &&
+                   cudaFuncSetAttribute(router_wgrad_partial_kernel<bf16, true>, a, b) == cudaSuccess &&
+                   cudaFuncSetAttribute(router_wgrad_partial_kernel<float, false>, a, b) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+  });
+  if (sa != MOE_OK) return sa;
   // raw softmax weights: dl is the dense [T, E] logit gradient
   const bool dense = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) != 0;
   if (cfg.dtype == MOE_BF16 && dense)
@@ -768,10 +777,10 @@ moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status launch_group_colsum(const void* src, long long ld, const int* offsets, int G, int rows, int N, float* out,
-                               cudaStream_t st) {
+moe_status launch_group_colsum(const void* src, long long ld, const int* offsets, int G, int rows, int N,
+                               const float* scale, float* out, cudaStream_t st) {
   dim3 grid((N + 255) / 256, G);
-  group_colsum_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(src), ld, offsets, rows, N, out);
+  group_colsum_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(src), ld, offsets, rows, N, scale, out);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

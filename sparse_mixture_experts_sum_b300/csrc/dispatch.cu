@@ -550,19 +550,14 @@ static __device__ __align__(256) uint8_t g_dispatch_scratch[kStaticDispatchScrat
 
 moe_status static_dispatch_scratch(size_t need, void** ptr) {
   if (need > kStaticDispatchScratchBytes) return MOE_ERR_UNSUPPORTED;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  // the array's name is a host-side stand-in in host code; its device
-  // address is looked up once per device, with that device current
-  static void* addr[64] = {nullptr};
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    addr[dev] = p;
-  }
-  *ptr = addr[dev];
+  // The array's name is a host-side stand-in in host code; its device
+  // address on the current device is looked up on every call (the lookup
+  // allocates nothing).  No address is cached, so a cudaDeviceReset that
+  // reloads the module -- and may place the array elsewhere -- cannot leave
+  // a stale pointer behind.
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+  *ptr = p;
   return MOE_OK;
 }
 

@@ -35,8 +35,11 @@
 //
 // Epilogue modes (GemmMode): plain (+bias), SwiGLU (B rows [0,128) from W1
 // and [128,256) from W3 at the same 128 output columns: silu(gate) * up),
-// GeLU (gelu(acc + bias)), and the backward of both activations, which read
-// the pre-activations the forward saved.
+// GeLU (gelu(acc + bias)), and the backward of both activations.  The
+// forward saves the pre-activations in fp32; the backward reads them, scales
+// the accumulator by the row's routing weight (so the GEMM contracts the
+// upstream gradient rows as stored, not a rounded weighted copy) and can
+// write the weighted activation s * act(z) for the W2 gradient.
 //
 // Every wait on a barrier is bounded (1 s); on expiry the kernel records an
 // error code in the workspace error word, drains its in-flight copies and
@@ -97,25 +100,26 @@ struct Tile {
 };
 
 // Tile index -> (group, n-tile, m-tile).  Fwd/Dgrad: a group has
-// ceil(rows/BM) m-tiles per n-tile, m fastest.  Wgrad: every group has
-// m_tiles x n_tiles tiles, n fastest when n_fast.  The extra group's X
-// tiles (the shared expert: many rows on one weight set, so bound by the
-// tensor cores where the routed groups stream weights) are spread evenly
-// through the schedule of N tiles: slot s holds extra tile floor(s X / N)
-// when that count steps at s, else routed tile s - floor(s X / N).
+// ceil(rows/BM) m-tiles per n-tile, m fastest, so the CTAs running together
+// share each weight tile through L2.  Wgrad: every group has m_tiles x
+// n_tiles tiles, n fastest when n_fast.  The extra group's X tiles (the
+// shared expert: many rows on one weight set, so bound by the tensor cores
+// where the routed groups stream weights) are spread evenly through the
+// schedule of N tiles: slot s holds extra tile floor(s X / N) when that
+// count steps at s, else routed tile s - floor(s X / N).  They run n
+// fastest: the shared weights are small enough to stay in L2, while its T
+// input rows are not, so each block of rows is read once for all n-tiles.
 template <int KIND, int BM, typename C>
-__device__ __forceinline__ Tile tile_coords(const C& c, int G, int n_tiles, int m_tiles, bool n_fast, int tile,
-                                            int xrows) {
+__device__ __forceinline__ Tile tile_coords(const C& c, int G, int n_tiles, int m_tiles, bool n_fast, int tile) {
   if (KIND == kKindFwd && c.total_tiles > c.x_tile0) {
     const long long NT = c.total_tiles, XT = NT - c.x_tile0;
     const long long before = static_cast<long long>(tile) * XT / NT;
     if ((static_cast<long long>(tile) + 1) * XT / NT > before) {
       const int local = static_cast<int>(before);
-      const int mt = (xrows + BM - 1) / BM;
       Tile t;
       t.g = G;
-      t.n = local / mt;
-      t.m = local - t.n * mt;
+      t.m = local / n_tiles;
+      t.n = local - t.m * n_tiles;
       return t;
     }
     tile -= static_cast<int>(before);
@@ -160,18 +164,16 @@ __device__ __forceinline__ void store_f32x32(float* dst, int col, int N, const f
   }
 }
 
-// 32 consecutive bf16 (16-byte aligned) -> fp32; groups of 8 past N read as 0.
-__device__ __forceinline__ void load_bf16x32(const bf16* src, int col, int N, float (&v)[32]) {
+// 32 consecutive fp32 (16-byte aligned); groups of 4 past N read as 0.
+__device__ __forceinline__ void load_f32x32(const float* src, int col, int N, float (&v)[32]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (col + q * 8 + 8 <= N) u = *reinterpret_cast<const uint4*>(src + col + q * 8);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[q * 8 + 2 * i] = bf16lo(w[i]);
-      v[q * 8 + 2 * i + 1] = bf16hi(w[i]);
-    }
+  for (int q = 0; q < 8; ++q) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col + q * 4 + 4 <= N) f = *reinterpret_cast<const float4*>(src + col + q * 4);
+    v[4 * q] = f.x;
+    v[4 * q + 1] = f.y;
+    v[4 * q + 2] = f.z;
+    v[4 * q + 3] = f.w;
   }
 }
 
@@ -269,10 +271,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     if (lane == 0) {
       uint32_t it = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile, p.xrows);
+        const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
         const bool xg = KIND == kKindFwd && t.g == G;  // the extra group
         const int grow = xg ? 0 : c.grp_row[t.g];
-        const int nk = KIND == kKindWgrad ? (c.grp_row[t.g + 1] - grow + BK - 1) / BK : nk_fixed;
+        // Wgrad: k-blocks of the group's rows (twice over with a hi/lo B pair)
+        const int nk1 = KIND == kKindWgrad ? (c.grp_row[t.g + 1] - grow + BK - 1) / BK : nk_fixed;
+        const int nk = KIND == kKindWgrad && p.b_lo ? 2 * nk1 : nk1;
         // every box of k-block kb, handed to emit(dst offset in the stage, map, x, y)
         auto boxes = [&](int kb, auto&& emit) {
           if (KIND == kKindFwd) {
@@ -303,11 +307,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
 #pragma unroll
             for (int i = 0; i < 4; ++i) emit(A_TILE_BYTES + i * MN_BLOCK_BYTES, mb, t.n * BN + 64 * i, y);
           } else {
-            const int y = grow + kb * BK;
+            const bool lo = kb >= nk1;  // second pass: the B1 (lo) rows
+            const int y = grow + (lo ? kb - nk1 : kb) * BK;
+            const CUtensorMap* mb = lo ? &mapB1 : &mapB0;
 #pragma unroll
             for (int i = 0; i < BM / 64; ++i) emit(i * MN_BLOCK_BYTES, &mapA, t.m * BM + 64 * i, y);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) emit(A_TILE_BYTES + i * MN_BLOCK_BYTES, &mapB0, t.n * BN + 64 * i, y);
+            for (int i = 0; i < 4; ++i) emit(A_TILE_BYTES + i * MN_BLOCK_BYTES, mb, t.n * BN + 64 * i, y);
           }
         };
         for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -344,9 +350,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       // one read of the abort flag for the whole warp keeps its lanes together
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile, p.xrows);
+      const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
       const int grows = KIND == kKindWgrad ? c.grp_row[t.g + 1] - c.grp_row[t.g] : 0;
-      const int nk = KIND == kKindWgrad ? (grows + BK - 1) / BK : nk_fixed;
+      const int nk1 = KIND == kKindWgrad ? (grows + BK - 1) / BK : nk_fixed;
+      const int nk = KIND == kKindWgrad && p.b_lo ? 2 * nk1 : nk1;
       const uint32_t acc = local % NACC;
       const uint32_t aph = (local / NACC) & 1u;
       bool ok = lane == 0 ? mbar_wait(&c.tmem_empty[acc], aph ^ 1u) : true;
@@ -372,7 +379,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         uint8_t* sa = tiles + s * STAGE_BYTES;
         uint8_t* sb = sa + A_TILE_BYTES;
         if (KIND == kKindWgrad) {
-          const int valid = grows - kb * BK;  // in (0, BK]
+          const int valid = grows - (kb >= nk1 ? kb - nk1 : kb) * BK;  // in (0, BK]
           if (valid < BK) {
             // rows [valid, BK) of this k-block belong to the next group (or
             // lie past the tensor): clear them in all six 64-row MN blocks.
@@ -432,7 +439,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       // tcgen05.ld is warp-collective: the warp decides to stop as one
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile, p.xrows);
+      const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
       const bool xg = KIND == kKindFwd && t.g == G;  // the extra group
       const int grow = xg ? 0 : c.grp_row[t.g];
       const int gend = xg ? p.xrows : c.grp_row[t.g + 1];
@@ -478,7 +485,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         const bool valid = row < row_end;
         if (swiglu_fwd) {
           bf16* orow = static_cast<bf16*>(out_p) + static_cast<size_t>(row) * p.ldo;
-          bf16* zrow = zsave_p ? static_cast<bf16*>(zsave_p) + static_cast<size_t>(row) * p.ldz : nullptr;
+          // the pre-activations are kept in fp32 for the backward: a bf16
+          // copy would put a 2^-9 rounding inside silu'(gate) and up there
+          float* zrow = zsave_p ? static_cast<float*>(zsave_p) + static_cast<size_t>(row) * p.ldz : nullptr;
           const int col0 = t.n * 128;
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
@@ -497,14 +506,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             if (valid) {
               store_bf16x32(orow, col, p.N, pk);
               if (zrow) {
-                uint32_t zg[16], zu[16];
+                float zv[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  zg[i] = pack_bf16(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
-                  zu[i] = pack_bf16(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
-                }
-                store_bf16x32(zrow, col, p.N, zg);
-                store_bf16x32(zrow + p.N, col, p.N, zu);
+                for (int i = 0; i < 32; ++i) zv[i] = __uint_as_float(gr[i]);
+                store_f32x32(zrow, col, p.N, zv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) zv[i] = __uint_as_float(ur[i]);
+                store_f32x32(zrow + p.N, col, p.N, zv);
               }
             }
           }
@@ -513,12 +521,19 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
           const int mode = p.mode;
           const bf16* brow = xg ? static_cast<const bf16*>(p.xbias)
                                 : (p.bias ? static_cast<const bf16*>(p.bias) + static_cast<size_t>(t.g) * p.N : nullptr);
-          const bf16* zin = (mode == kModeSwiGLUBwd || mode == kModeGeLUBwd) && valid
-                                ? static_cast<const bf16*>(p.zin) + static_cast<size_t>(row) * p.ldz
-                                : nullptr;
-          bf16* zrow = zsave_p && mode == kModeGeLU && valid
-                           ? static_cast<bf16*>(zsave_p) + static_cast<size_t>(row) * p.ldz
-                           : nullptr;
+          const bool bwd_mode = mode == kModeSwiGLUBwd || mode == kModeGeLUBwd;
+          const float* zin = bwd_mode && valid ? static_cast<const float*>(p.zin) + static_cast<size_t>(row) * p.ldz
+                                               : nullptr;
+          // backward: dH = s * acc with s the row's routing weight, and the
+          // weighted activation s * act(z) for the W2 gradient
+          const float rs = bwd_mode && valid && p.row_scale ? p.row_scale[row] : 1.0f;
+          bf16* hrow = bwd_mode && valid && p.hout ? static_cast<bf16*>(p.hout) + static_cast<size_t>(row) * p.N
+                                                   : nullptr;
+          bf16* lrow = hrow && p.hout_lo ? static_cast<bf16*>(p.hout_lo) + static_cast<size_t>(row) * p.N
+                                         : nullptr;
+          float* zrow = zsave_p && mode == kModeGeLU && valid
+                            ? static_cast<float*>(zsave_p) + static_cast<size_t>(row) * p.ldz
+                            : nullptr;
 #pragma unroll 1
           for (int cc = 0; cc < BN / 32; ++cc) {
             uint32_t r[32];
@@ -530,35 +545,52 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
             if (!valid) continue;
             if (mode == kModeSwiGLUBwd) {
-              // dH = acc; gate g, up u: dA = dH u silu'(g), dB = dH silu(g)
+              // dH = s acc; gate g, up u: dA = dH u silu'(g), dB = dH silu(g), H' = s silu(g) u
               float g[32], u[32];
-              load_bf16x32(zin, col, p.N, g);
-              load_bf16x32(zin + p.N, col, p.N, u);
-              uint32_t pa[16], pb[16];
+              load_f32x32(zin, col, p.N, g);
+              load_f32x32(zin + p.N, col, p.N, u);
+              uint32_t pa[16], pb[16], ph[16], pl[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                float da[2], db[2];
+                float da[2], db[2], hh[2];
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                   const int e = 2 * i + h2;
                   const float sg = sigmoid_fast(g[e]);
                   const float sl = g[e] * sg;
-                  da[h2] = v[e] * u[e] * (sg * (1.0f + g[e] * (1.0f - sg)));
-                  db[h2] = v[e] * sl;
+                  const float dh = rs * v[e];
+                  da[h2] = dh * u[e] * (sg * (1.0f + g[e] * (1.0f - sg)));
+                  db[h2] = dh * sl;
+                  hh[h2] = rs * sl * u[e];
                 }
                 pa[i] = pack_bf16(da[0], da[1]);
                 pb[i] = pack_bf16(db[0], db[1]);
+                ph[i] = pack_bf16(hh[0], hh[1]);
+                pl[i] = pack_bf16(hh[0] - bf16lo(ph[i]), hh[1] - bf16hi(ph[i]));
               }
               bf16* orow = static_cast<bf16*>(p.out) + static_cast<size_t>(row) * p.ldo;
               store_bf16x32(orow, col, p.N, pa);
               store_bf16x32(orow + p.N, col, p.N, pb);
+              if (hrow) store_bf16x32(hrow, col, p.N, ph);
+              if (lrow) store_bf16x32(lrow, col, p.N, pl);
               continue;
             }
             if (mode == kModeGeLUBwd) {
               float z[32];
-              load_bf16x32(zin, col, p.N, z);
+              load_f32x32(zin, col, p.N, z);
+              if (hrow) {
+                uint32_t ph[16], pl[16];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(z[i]);
+                for (int i = 0; i < 16; ++i) {
+                  const float h0 = rs * gelu_f(z[2 * i]), h1 = rs * gelu_f(z[2 * i + 1]);
+                  ph[i] = pack_bf16(h0, h1);
+                  pl[i] = pack_bf16(h0 - bf16lo(ph[i]), h1 - bf16hi(ph[i]));
+                }
+                store_bf16x32(hrow, col, p.N, ph);
+                if (lrow) store_bf16x32(lrow, col, p.N, pl);
+              }
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= rs * gelu_grad_f(z[i]);
             } else {
               if (brow) {
 #pragma unroll
@@ -566,12 +598,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
                   if (col + i < p.N) v[i] += __bfloat162float(brow[col + i]);
               }
               if (mode == kModeGeLU) {
-                if (zrow) {
-                  uint32_t zp[16];
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) zp[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-                  store_bf16x32(zrow, col, p.N, zp);
-                }
+                if (zrow) store_f32x32(zrow, col, p.N, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
               }
@@ -609,13 +636,14 @@ moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtenso
   const int sms = device_sm_count(dev);
   if (sms <= 0) return MOE_ERR_CUDA;
   constexpr size_t smem = smem_bytes<BM_>();
-  static bool attr_set[64] = {false};
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<KIND, BM_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  static DeviceOnce attr;
+  const moe_status sa = attr.run(dev, [&] {
+    return cudaFuncSetAttribute(grouped_gemm_tc_kernel<KIND, BM_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem)) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+  });
+  if (sa != MOE_OK) return sa;
   long long grid = tiles_bound;
   if (grid > sms) grid = sms;
   if (grid < 1) grid = 1;
@@ -669,7 +697,11 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
   } else {
     if (!make_tma_2d_bf16(&mA, A, p.M, a_rows, 64, BK)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mB0, B0, p.N, a_rows, 64, BK)) return MOE_ERR_CUDA;
-    mB1 = mB0;
+    if (p.b_lo) {
+      if (!make_tma_2d_bf16(&mB1, B1, p.N, a_rows, 64, BK)) return MOE_ERR_CUDA;
+    } else {
+      mB1 = mB0;
+    }
   }
   if (KIND == kKindFwd && p.xrows > 0) {
     const long long n_rows = p.N;  // rows of the extra group's weights [N, K]
@@ -716,6 +748,7 @@ moe_status launch_grouped_gemm_tc(const GemmParams& p_in, int kind, const void* 
   if (kind == kKindWgrad) {
     if (p.M < 8 || (p.M % 8) || !p.out_f32 || p.mode != kModePlain) return MOE_ERR_UNSUPPORTED;
     if (p.m_split && (p.m_split % 8 || p.m_split >= p.M || !p.out2)) return MOE_ERR_UNSUPPORTED;
+    if (p.b_lo && !B1) return MOE_ERR_INVALID_ARG;
     return launch_geometry<kKindWgrad>(p, A, a_rows, B0, B1, b_rows, avg_rows, nullptr, stream);
   }
   return MOE_ERR_INVALID_ARG;

@@ -5,17 +5,43 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "moe.h"
 
 namespace moe {
+
+// A per-device set-up step (a kernel attribute, a cached device property)
+// that must succeed once per device: the first call for a device runs fn
+// and, on MOE_OK, records it.  One lock covers the flags, so first calls from
+// several host threads do not race.
+class DeviceOnce {
+ public:
+  template <typename F>
+  moe_status run(int dev, F&& fn) {
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev]) return MOE_OK;
+    const moe_status s = fn();
+    if (s == MOE_OK) done_[dev] = true;
+    return s;
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+};
 
 // Epilogue of a grouped GEMM (acc = the fp32 accumulator of one output element).
 enum GemmMode : int {
   kModePlain = 0,      // out = acc (+ bias)
   kModeSwiGLU = 1,     // out = silu(gate) * up (B tile pairs W1 and W3 rows); zsave: gate | up
   kModeGeLU = 2,       // out = gelu(acc + bias); zsave: acc + bias
-  kModeSwiGLUBwd = 3,  // g = zin[r,n], u = zin[r,N+n]: out[r,n] = acc*u*silu'(g), out[r,N+n] = acc*silu(g)
-  kModeGeLUBwd = 4,    // out = acc * gelu'(zin[r,n])
+  // Backward modes; s = row_scale[r] (1 when null), dH = s * acc:
+  kModeSwiGLUBwd = 3,  // g = zin[r,n], u = zin[r,N+n]: out[r,n] = dH*u*silu'(g), out[r,N+n] = dH*silu(g);
+                       // hout + hout_lo = s*silu(g)*u
+  kModeGeLUBwd = 4,    // out = dH * gelu'(zin[r,n]); hout + hout_lo = s*gelu(zin[r,n])
 };
 
 // Operand geometry of a grouped GEMM launch.
@@ -43,9 +69,14 @@ struct GemmParams {
   void* out;             // Fwd/Dgrad: [rows, ldo]; Wgrad: [G, M or m_split, N]
   void* out2;            // Wgrad second output [G, M - m_split, N]
   long long ldo;         // Fwd/Dgrad row stride of out (elements); 0: N
-  void* zsave;           // Fwd SwiGLU/GeLU: pre-activations out (bf16), nullable
-  const void* zin;       // *Bwd modes: saved pre-activations (bf16)
+  void* zsave;           // Fwd SwiGLU/GeLU: pre-activations out (fp32), nullable
+  const void* zin;       // *Bwd modes: saved pre-activations (fp32)
   long long ldz;         // row stride of zsave / zin (elements)
+  const float* row_scale;  // *Bwd modes: per output row factor of the accumulator, nullable (1)
+  void* hout;            // *Bwd modes: s * act(z) per row, rounded to bf16 ([rows, N]), nullable
+  void* hout_lo;         // *Bwd modes: the bf16 residual s * act(z) - hout ([rows, N]), nullable
+  int b_lo;              // Wgrad: out_g = A_g^T . (B0_g + B1_g) -- the contraction runs over the
+                         // group's rows twice, with B0 then with B1 (a hi/lo pair)
   const void* bias;      // [G, N] nullable (GeLU / plain)
   int* err;              // workspace error word
   // Fwd only: one more group with its own operands (the shared expert):
@@ -109,8 +140,10 @@ moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos,
 
 // Backward pieces outside the expert GEMMs (backward.cu).
 size_t router_wgrad_partial_bytes(const moe_config& cfg);
+// Per kept slot (t,j): dYg[pos] = dY[t] (the rows as stored), wp[pos] =
+// w[t,j], dot[t,j] = <dY[t], Yp[pos]> (0 when dropped).
 moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* Yp, const int* pos, const float* w,
-                             void* dYp, float* dot, cudaStream_t st);
+                             void* dYg, float* wp, float* dot, cudaStream_t st);
 // imp (E words of 8 bytes) must be zero on entry.  With LayerNorm before
 // the router (lnc = 3T floats: mu, A, B per token, else nullptr) dl leaves
 // scaled by each token's 1/sqrt(var + eps) and lnc holds the per-token terms
@@ -130,8 +163,9 @@ moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* 
                                const float* lnc, float* partial, float* dWr, cudaStream_t st);
 moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos, const int* idx, const float* dl,
                          const void* Wr, const void* x, const float* lnc, int accumulate, float* dX, cudaStream_t st);
-moe_status launch_group_colsum(const void* src, long long ld, const int* offsets, int G, int rows, int N, float* out,
-                               cudaStream_t st);
+// out[g][n] = sum over group g's rows r of scale[r] * src[r][n] (scale nullable: 1).
+moe_status launch_group_colsum(const void* src, long long ld, const int* offsets, int G, int rows, int N,
+                               const float* scale, float* out, cudaStream_t st);
 
 // TMA descriptor of a row-major bf16 matrix [rows, inner] with a
 // (box_inner x box_rows) box and 128-byte swizzling.

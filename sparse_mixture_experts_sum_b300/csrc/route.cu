@@ -554,16 +554,17 @@ template <int STAGES>
 moe_status launch_route_stages(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
                                const float* noise, int* idx, float* w, int* counts, float* ent, cudaStream_t stream) {
   const RouteLayout Lay(cfg.E, STAGES);
-  static bool attr_set[64] = {false};
+  static DeviceOnce attr;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  if (!attr_set[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const moe_status sa = attr.run(dev, [&] {
     const RouteLayout Lmax(1024, STAGES);
-    if (cudaFuncSetAttribute(route_bf16_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Lmax.total)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+    return cudaFuncSetAttribute(route_bf16_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(Lmax.total)) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+  });
+  if (sa != MOE_OK) return sa;
   dim3 grid((cfg.T + RT_TM - 1) / RT_TM, 1);
   route_bf16_kernel<STAGES><<<grid, 128, Lay.total, stream>>>(
       static_cast<const bf16*>(x), static_cast<const bf16*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E, cfg.k,

@@ -66,14 +66,16 @@ moe_status launch_zero(void* a, size_t a_bytes, void* b, size_t b_bytes, cudaStr
 }
 
 int device_sm_count(int dev) {
+  static DeviceOnce once;
   static int cache[64] = {0};
-  if (dev < 0 || dev >= 64) return 0;
-  if (cache[dev] == 0) {
+  const moe_status s = once.run(dev, [&] {
     int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return MOE_ERR_CUDA;
     cache[dev] = v;
-  }
-  return cache[dev];
+    return MOE_OK;
+  });
+  return s == MOE_OK ? cache[dev] : 0;
 }
 
 // Self-test of the bounded-wait path: one thread waits on a shared-memory

@@ -285,10 +285,11 @@ def alloc_saved(cfg: MoeConfig, device="cuda", backward=False) -> dict:
         out["Sx"] = torch.empty(T, d, dtype=dt, device=device)
     if backward:
         hz = 2 * h if cfg.act == ACT["swiglu"] else h
-        out["Z"] = torch.empty(T * k, hz, dtype=dt, device=device)
+        # pre-activations are fp32 (the backward's activation derivative reads them)
+        out["Z"] = torch.empty(T * k, hz, dtype=torch.float32, device=device)
         if cfg.has_shared:
             out["Hs"] = torch.empty(T, h, dtype=dt, device=device)
-            out["Zs"] = torch.empty(T, hz, dtype=dt, device=device)
+            out["Zs"] = torch.empty(T, hz, dtype=torch.float32, device=device)
         if cfg.route_flags & ROUTE_RAW_PROBS:
             out["logits"] = torch.empty(T, E, dtype=torch.float32, device=device)
     return out

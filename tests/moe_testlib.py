@@ -92,21 +92,24 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
 
 def bf16_storage_model_expert_grads(t: dict, route: dict, dY, e: int) -> dict:
     """Expert e's SwiGLU weight gradients computed in fp64 but with the
-    values rounded to bf16 wherever the layer stores them in bf16 between
-    kernels: the saved gate/up pre-activations, the hidden rows H, the
-    scaled upstream rows w*dY, and dA/dB.  A model of the storage
-    arithmetic (not the oracle): it explains the layer's deviation from the
-    fp64 oracle, so the GPU must match it much more tightly."""
+    values rounded wherever the layer stores them between kernels: the
+    pre-activations g, u in fp32; dA and dB (the tensor-core operands of the
+    W1/W3 gradients) in bf16; the weighted hidden rows w*silu(g)*u (the
+    operand of the W2 gradient) as a bf16 value plus its bf16 residual.  The
+    upstream rows dY enter as stored and the routing weight w (fp32) scales
+    the W2 product in fp32.  A model of the storage arithmetic (not the
+    oracle): it explains the layer's deviation from the fp64 oracle, so the
+    GPU must match it much more tightly."""
     rows, slots = np.nonzero((route["idx"] == e) & (route["pos"] >= 0))
     v = O.decode(t["x"])[rows]
     W1, W3, W2 = (O.decode(t[n][e]) for n in ("W1", "W3", "W2"))
-    a = v @ W1.T
-    b = v @ W3.T
-    g, u = round_bf16(a), round_bf16(b)
-    H = round_bf16(O.silu(a) * b)
-    w32 = route["w"][rows, slots].astype(np.float32).astype(np.float64)
-    dYp = round_bf16(w32[:, None] * O.decode(dY)[rows])
-    dH = dYp @ W2
+    f32 = lambda a: np.asarray(a, dtype=np.float32).astype(np.float64)
+    g, u = f32(v @ W1.T), f32(v @ W3.T)
+    w32 = f32(route["w"][rows, slots])[:, None]
+    dy = O.decode(dY)[rows]
+    dH = w32 * (dy @ W2)
     dA = round_bf16(dH * u * O.silu_grad(g))
     dB = round_bf16(dH * O.silu(g))
-    return dict(dW1=dA.T @ v, dW3=dB.T @ v, dW2=dYp.T @ H)
+    Hw = w32 * O.silu(g) * u
+    hi = round_bf16(Hw)
+    return dict(dW1=dA.T @ v, dW3=dB.T @ v, dW2=dy.T @ (hi + round_bf16(Hw - hi)))

@@ -76,7 +76,12 @@ int main(void) {
 
 @pytest.mark.parametrize("T,k,E,cf,minc", [(1024, 2, 16, 1.0, 0), (4096, 2, 16, 1.0, 0), (16384, 2, 64, 1.25, 0),
                                            (32768, 2, 16, 1.25, 0), (64, 2, 4, 0.0, 0), (10, 2, 16, 1.0, 4),
-                                           (1000, 3, 7, 1.1, 0), (333, 6, 384, 1.0, 0)])
+                                           (1000, 3, 7, 1.1, 0), (333, 6, 384, 1.0, 0),
+                                           # fp32 cf a hair above the decimal: the exact product sits
+                                           # just above an integer, and the ceiling takes the next one
+                                           (1000, 2, 16, 0.8, 0), (5, 1, 2, 0.4, 0), (700, 2, 16, 0.8, 0),
+                                           # exact integer products, large and tiny factors
+                                           (1 << 20, 8, 1024, 0.5, 0), (64, 2, 4, 3e7, 0), (3, 1, 3, 1e-30, 0)])
 def test_capacity_matches_oracle(M, T, k, E, cf, minc):
     cfg = M.make_config(T, 64, 64, E, k, capacity_factor=cf, min_capacity=minc)
     assert M.moe_capacity(cfg) == O.expert_capacity(T, k, E, float(np.float32(cf)), minc)

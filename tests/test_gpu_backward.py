@@ -1,27 +1,24 @@
 """Parity of the layer backward (moe_layer_bwd through the C ABI) with the
 fp64 oracle's gradients of L = <dY, y> + lambda * CV(I/T).
 
-Tolerances (bf16 storage, fp32 accumulation): dX within relative-Frobenius
-1e-2 and, token by token, max-abs 5e-2 * max(1, RMS of the token's
-reference row).  Two stores set that error: each element sums 2h products
-of a bf16-stored dA/dB with a weight (a fixed fraction, ~2e-3 std, of the
-row's own scale), and the logit gradient dl takes <dY, Yp> from the
-bf16-stored expert outputs, which the router term dl . Wr carries into the
-row.  Reproducing both stores in fp64 on rows of varying offset and scale
-(the LayerNorm-router test) gives up to 2.3e-2 of the row RMS, so the
-bound leaves about 2x; weight gradients within relative-Frobenius 1e-2 and,
-entry by entry, |err| <= 5e-2 * max(RMS, |ref|) with RMS that of the
-expert's (or tensor's) reference gradient.  Each weight-gradient entry sums,
-over the expert's rows, products whose factors went through up to three
-bf16 stores (the saved pre-activations, w*dY, and dA/dB, which are
-tensor-core operands); each store errs by up to 2^-9 relative.  Over many
-rows that leaves ~3e-3 of the RMS as near-Gaussian noise whose largest of N
-values is ~sqrt(2 ln N) = 5..6.5 times that for N = 1e5..1e9 entries; over
-few rows the error stays relative to the entry itself, hence the max(RMS,
-|ref|) scale.  A test below reproduces those roundings in fp64 and requires
-the GPU to match that model far more tightly, so the looser bound against
-the oracle hides no kernel error.  Routing inputs keep every token's top-k
-margin >= 1e-3."""
+Tolerances (bf16 storage, fp32 accumulation), the stated bf16 bounds:
+- dX: relative-Frobenius 1e-2 and max-abs 2e-2 (rows of unit scale).  The
+  LayerNorm-router tests draw rows with their own offset (up to +-2) and
+  scale (up to 3); there the max-abs bound is taken relative to the row,
+  5e-2 * max(1, RMS of the token's reference row): the bf16 stores of a row
+  (dA/dB, the expert outputs behind the logit gradient) err by a fixed
+  fraction of the row's own scale.
+- weight gradients: relative-Frobenius 1e-2 and, entry by entry, |err| <=
+  2e-2 * max(RMS, |ref|), RMS that of the expert's (or tensor's) reference
+  gradient: an entry is a sum over the expert's rows, so the absolute 2e-2
+  is read against the gradient's own scale.  The saved pre-activations are
+  fp32 and the upstream rows enter the GEMMs as stored, with the routing
+  weight applied in fp32; dW1/dW3 products carry one bf16 rounding (the
+  tensor-core operands dA/dB), and dW2 contracts the weighted hidden rows
+  w*act(z) as a bf16 value plus its bf16 residual (no rounding beyond 2^-16).
+A test below reproduces those roundings in fp64 and requires the GPU to
+match that model far more tightly, so the bound hides no kernel error.
+Routing inputs keep every token's top-k margin >= 1e-3."""
 
 import numpy as np
 import pytest
@@ -37,7 +34,7 @@ DEV = "cuda"
 WEIGHT_NAMES = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2", "expert_bias")
 
 
-def assert_grad_close(got, ref, what, rel=1e-2, rms_frac=5e-2):
+def assert_grad_close(got, ref, what, rel=1e-2, rms_frac=2e-2):
     rf = rel_frob(got, ref)
     rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
     scaled = float((np.abs(got - ref) / np.maximum(max(rms, 1e-30), np.abs(ref))).max()) if ref.size else 0.0
@@ -71,14 +68,22 @@ def oracle_backward(wl, t, dY, **route):
 PER_EXPERT = ("dW1", "dW3", "dW2", "db1", "db2")
 
 
-def check_all(wl, t, dY, g, ref):
+def check_all(wl, t, dY, g, ref, dx_row_scaled=False):
+    """Every gradient against the oracle.  dx_row_scaled: rows of x with
+    their own offset and scale (the LayerNorm-router inputs), where dX's
+    max-abs bound is 5e-2 of max(1, the row's RMS); else max-abs 2e-2."""
     dX = g["dX"].cpu().numpy().astype(np.float64)
     rf = rel_frob(dX, ref["dX"])
-    row_rms = np.sqrt(np.mean(ref["dX"] ** 2, axis=1))
     row_err = np.abs(dX - ref["dX"]).max(axis=1)
-    worst = int(np.argmax(row_err / np.maximum(1.0, row_rms)))
-    assert rf <= 1e-2 and row_err[worst] <= 5e-2 * max(1.0, row_rms[worst]), \
-        f"dX: rel-Frobenius {rf:.3e}; token {worst}: max-abs {row_err[worst]:.3e}, row RMS {row_rms[worst]:.3e}"
+    if dx_row_scaled:
+        row_rms = np.sqrt(np.mean(ref["dX"] ** 2, axis=1))
+        worst = int(np.argmax(row_err / np.maximum(1.0, row_rms)))
+        assert rf <= 1e-2 and row_err[worst] <= 5e-2 * max(1.0, row_rms[worst]), \
+            f"dX: rel-Frobenius {rf:.3e}; token {worst}: max-abs {row_err[worst]:.3e}, row RMS {row_rms[worst]:.3e}"
+    else:
+        worst = int(np.argmax(row_err))
+        assert rf <= 1e-2 and row_err[worst] <= 2e-2, \
+            f"dX: rel-Frobenius {rf:.3e}; token {worst}: max-abs {row_err[worst]:.3e} (<= 2e-2)"
     for name in ("dWr", "dW1", "dW3", "dW2", "db1", "db2", "dWs1", "dWs3", "dWs2", "dbs1", "dbs2"):
         if name not in g:
             continue
@@ -167,7 +172,7 @@ def test_backward_with_router_layernorm(shared, cf):
     ref = oracle_backward(wl, t, dY, layernorm=True)
     np.testing.assert_array_equal(sv["idx"].cpu().numpy(), ref["route"]["idx"])
     np.testing.assert_array_equal(sv["pos"].cpu().numpy(), ref["route"]["pos"])
-    check_all(wl, t, dY, g, ref)
+    check_all(wl, t, dY, g, ref, dx_row_scaled=True)
     # the normalisation matters on these rows: the router gradient without
     # it is a different tensor
     plain = O.layer_backward(oracle_cfg(wl), {n: t[n] for n in WEIGHT_NAMES if t.get(n) is not None},
@@ -204,7 +209,7 @@ def test_backward_layernorm_router_with_product_balance():
     _, sv, g = run_fwd_bwd(wl, td, dY.to(DEV), **route)
     ref = oracle_backward(wl, t, dY, **route)
     np.testing.assert_array_equal(sv["pos"].cpu().numpy(), ref["route"]["pos"])
-    check_all(wl, t, dY, g, ref)
+    check_all(wl, t, dY, g, ref, dx_row_scaled=True)
 
 
 def test_backward_with_reroute():
@@ -277,7 +282,7 @@ def test_balance_term_reaches_router_only():
 
 def test_weight_grads_match_bf16_storage_model():
     """Against a model of the bf16 stores (moe_testlib), the expert weight
-    gradients agree to rel-Frobenius 5e-4 (against ~3e-3 for the oracle) --
+    gradients agree to rel-Frobenius 5e-4 (against ~2e-3 for the oracle) --
     the remaining deviation from the fp64 oracle is the storage rounding.
     What is left is fp32-vs-fp64 values that fall on different sides of a
     bf16 rounding boundary (one bf16 ulp on an element), so max-abs is held
@@ -303,9 +308,10 @@ def test_training_full_size_sampled():
     shared, Gumbel noise, cf 1.25): routing and dispatch bit-exact; dX on
     sampled tokens; rows/columns of dW1, dW3, dW2 of two routed experts and
     of the shared expert, each summed by the oracle over all of that
-    expert's tokens; and, for dWr (which needs every token's expert output),
-    the identity sum_e dWr[e] = 0 -- each token's logit gradient is a
-    softmax gradient over its selected experts and sums to zero."""
+    expert's tokens; and the router weight gradient's rows of the two
+    experts with the fewest routed tokens, which the oracle sums over every
+    token routed to them (the expert outputs of both of each such token's
+    slots, the balance term over the whole batch)."""
     wl = S.WORKLOADS["training"]
     t = guarded_inputs(wl, DEV)
     dY = t.pop("dY")
@@ -347,7 +353,8 @@ def test_training_full_size_sampled():
     assert_grad_close(g["dWs3"][ci].cpu().numpy().astype(np.float64), sl["dW3"], "dWs3 rows")
     assert_grad_close(g["dWs2"][:, ci].cpu().numpy().astype(np.float64), sl["dW2"], "dWs2 cols")
 
-    dWr = g["dWr"].double()
-    assert torch.isfinite(dWr).all()
-    colsum = dWr.sum(dim=0).abs().max().item()
-    assert colsum <= 1e-4 * dWr.abs().max().item(), colsum
+    ex = [int(e) for e in np.argsort(r["counts"], kind="stable")[:2]]
+    ref_wr = O.router_grad_rows(cfg, w, t["x"], dY, r, ex)
+    got_wr = g["dWr"][torch.as_tensor(ex, device=DEV)].cpu().numpy().astype(np.float64)
+    assert_grad_close(got_wr, ref_wr, f"dWr rows {ex}")
+    assert torch.isfinite(g["dWr"]).all()

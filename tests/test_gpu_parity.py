@@ -130,6 +130,19 @@ def test_large_prefill_layer_sampled():
 
 
 @pytest.mark.slow
+def test_large_prefill_stress_sampled():
+    """The large prefill with the Zipf bias taken as ln(pmf): ~75% of slots
+    dropped, most experts under one 128-row tile and some with no rows, so
+    the capacity scan, the ragged grouped GEMM and the combine meet their
+    extremes at full size.  Routing and dispatch bit-exact; y on sampled
+    tokens of popular, rare and empty experts."""
+    wl = S.WORKLOADS["large_prefill_3z"]
+    r, st = _sampled_layer_check(wl, experts=[0, 1, 9, 30, 47, 60, 63], seed=12)
+    assert st["capacity"] == 640 and st["drop_rate"] > 0.7
+    assert (r["kept"] < 128).sum() >= 40 and (r["kept"] == 0).any()
+
+
+@pytest.mark.slow
 def test_decode_layer_sampled():
     wl = S.WORKLOADS["decode"]
     t = guarded_inputs(wl, DEV)
@@ -389,11 +402,15 @@ def test_route_with_workspace(T, d, E, k):
     """With a workspace the logits run on the tcgen05 GEMM (E = 130 and 5
     pad the logit rows to 136 and 8 columns) and a warp per token takes the
     top-k: same routing as the oracle, and the same bits on a second run."""
+    from moe_testlib import guard
     wl = S.WORKLOADS["small_prefill"].replace(T=T, d=d, E=E, k=k, seed=19)
-    t = guarded_inputs(wl, "cpu", parts=["x", "Wr"])
+    t = S.make_inputs(wl, "cpu", parts=["x", "Wr"])
+    # the margins are guarded on the logits the router sees, bias included
+    eb = torch.linspace(0.3, 0.0, E, dtype=torch.float32)
+    t["expert_bias"] = eb
+    t = guard(wl, t)
     cfg = M.config_of(wl)
     x, Wr = t["x"].to(DEV), t["Wr"].to(DEV)
-    eb = torch.linspace(0.3, 0.0, E, dtype=torch.float32)
     ws = M.moe.workspace(cfg, 1)
     outs = []
     for _ in range(2):
@@ -404,13 +421,10 @@ def test_route_with_workspace(T, d, E, k):
         outs.append((idx, w, counts))
     l = O.router_logits(t["x"], t["Wr"], eb)
     ridx, rw, _ = O.top_k_route(l, k)
-    from moe_testlib import small_gaps
-    safe = np.setdiff1d(np.arange(T), small_gaps(l, k))
     idx, w, counts = outs[0]
-    np.testing.assert_array_equal(idx.cpu().numpy()[safe], ridx[safe])
-    np.testing.assert_allclose(w.cpu().numpy()[safe], rw[safe], atol=W_TOL, rtol=0)
-    if len(safe) == T:
-        np.testing.assert_array_equal(counts.cpu().numpy(), O.usage_counts(ridx, E))
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, atol=W_TOL, rtol=0)
+    np.testing.assert_array_equal(counts.cpu().numpy(), O.usage_counts(ridx, E))
     for a, b in zip(outs[0], outs[1]):
         assert torch.equal(a, b)
 
@@ -518,8 +532,7 @@ def test_reroute_on_overflow(tm, k, E, dtype):
     skewed router and cf 0.8, slots dropped by the first pass try their
     token's backups; positions, per-expert rows, statistics (with the
     rerouted count) and the output match the oracle.  moe_route followed by
-    moe_dispatch on the same workspace gives the same placement; the
-    backward refuses the flag."""
+    moe_dispatch on the same workspace gives the same placement."""
     if dtype == "f32":
         wl = S.WORKLOADS["tiny_fp32"].replace(T=300, E=E, k=k, capacity_factor=0.8, seed=33)
     else:

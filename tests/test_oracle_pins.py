@@ -440,10 +440,19 @@ def test_backward_balance_term_isolated():
     np.testing.assert_allclose(gz["dWr"], g1["dWr"] - g0["dWr"], atol=1e-12)
 
 
-@pytest.mark.parametrize("act,shared", [("swiglu", True), ("gelu", False)])
-def test_sampled_backward_entries_match_full_backward(act, shared):
-    """The sampled-entry functions used at full size agree with the
-    finite-difference-pinned layer_backward on a tiny batch."""
+SAMPLED_VARIANTS = [("swiglu", True, {}), ("gelu", False, {}), ("swiglu", True, {"reroute": True}),
+                    ("swiglu", False, {"raw_probs": True}), ("swiglu", True, {"layernorm": True}),
+                    ("gelu", True, {"balance": "std_max"}), ("swiglu", False, {"balance": "switch", "raw_probs": True})]
+
+
+@pytest.mark.parametrize("act,shared,route", SAMPLED_VARIANTS)
+def test_sampled_backward_entries_match_full_backward(act, shared, route):
+    """The sampled-entry functions used at full size (expert_grad_slices,
+    token_input_grads, router_grad_rows) agree with the
+    finite-difference-pinned layer_backward on a tiny batch, under the
+    routing and balance variants: rerouted slots are served by their backup,
+    raw softmax weights give every logit a gradient, the LayerNorm router
+    carries its backward."""
     rng = _rng(71)
     T, d, h, E, k = 30, 6, 10, 4, 2
     w = dict(Wr=rng.normal(size=(E, d)), W1=rng.normal(size=(E, h, d)) / 2, W2=rng.normal(size=(E, d, h)) / 3)
@@ -454,12 +463,17 @@ def test_sampled_backward_entries_match_full_backward(act, shared):
         w["b2"] = rng.normal(size=(E, d)) * 0.1
     if shared:
         w.update(Ws1=rng.normal(size=(h, d)) / 2, Ws3=rng.normal(size=(h, d)) / 2, Ws2=rng.normal(size=(d, h)) / 3)
-    cfg = dict(T=T, d=d, h=h, E=E, k=k, act=act, capacity_factor=0.75, has_shared=shared, lam=0.05)
-    x = rng.normal(size=(T, d))
+        if act == "gelu":
+            w.update(bs1=rng.normal(size=h) * 0.1, bs2=rng.normal(size=d) * 0.1)
+    cfg = dict(T=T, d=d, h=h, E=E, k=k, act=act, capacity_factor=0.75, has_shared=shared, lam=0.05, **route)
+    x = rng.normal(size=(T, d)) * 1.5 + 0.3
     dY = rng.normal(size=(T, d))
-    full = O.layer_backward(cfg, w, x, dY)
+    bias = np.array([1.0, 0.5, 0.0, -0.5])
+    full = O.layer_backward(cfg, w, x, dY, bias)
     r = full["route"]
-    assert (r["pos"] < 0).any()
+    assert (r["pos"] < 0).any() or route.get("reroute")
+    if route.get("reroute"):
+        assert ((r["served"] >= 0) & (r["served"] != r["idx"])).any()
     for e in range(E):
         cols = [1, 4, 7]
         sl = O.expert_grad_slices(cfg, w, x, dY, r, e, cols)
@@ -471,6 +485,12 @@ def test_sampled_backward_entries_match_full_backward(act, shared):
             np.testing.assert_allclose(sl["db1"], full["db1"][e][cols], atol=1e-12)
     toks = [0, 3, 11, 29]
     np.testing.assert_allclose(O.token_input_grads(cfg, w, x, dY, r, toks), full["dX"][toks], atol=1e-12)
+    if route.get("raw_probs"):
+        with pytest.raises(ValueError):
+            O.router_grad_rows(cfg, w, x, dY, r, [1])
+    else:
+        for ex in ([1], [0, 3], [2, 1]):
+            np.testing.assert_allclose(O.router_grad_rows(cfg, w, x, dY, r, ex), full["dWr"][ex], atol=1e-12)
 
 
 # ---------------------------------------------------------------------------

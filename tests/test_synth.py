@@ -53,6 +53,26 @@ def test_zipf_bias():
     assert (p[:-1] > p[1:]).all()
 
 
+def test_stress_workload_bias_is_log_pmf_and_overflows():
+    """The large-prefill stress variant takes the Zipf(1.1) bias as ln(pmf):
+    ln(1/H) for the first expert, ln(64^-1.1/H) for the last (H = the
+    generalised harmonic number over 64 ranks).  Routed by the oracle it
+    drops about 3/4 of the slots and leaves most experts below one 128-row
+    tile, some with none."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    wl = S.WORKLOADS["large_prefill_3z"]
+    t = S.make_inputs(wl, "cpu", parts=["x", "Wr", "expert_bias"])
+    H = sum(i ** -1.1 for i in range(1, 65))
+    b = t["expert_bias"].double()
+    assert abs(b[0].item() + np.log(H)) < 1e-6 and abs(b[63].item() - (-1.1 * np.log(64) - np.log(H))) < 1e-6
+    cfg = dict(T=wl.T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act, capacity_factor=1.25, min_capacity=0,
+               lam=0.01, has_shared=False)
+    r = O.route_and_dispatch(cfg, t["x"], t["Wr"], t["expert_bias"])
+    assert 0.70 < r["stats"]["drop_rate"] < 0.80
+    assert (r["kept"] < 128).sum() >= 40 and (r["kept"] == 0).any() and (r["kept"] == 640).sum() >= 8
+
+
 def test_workload_shapes_small():
     wl = S.WORKLOADS["tiny_fp32"]
     x = S.make_inputs(wl)

@@ -31,9 +31,8 @@ def _routing(T, E, k, seed):
     """Seeded top-k indices with a skewed expert popularity (capacity binds)
     and a few tokens routed nowhere (-1), as moe_route leaves them."""
     g = torch.Generator().manual_seed(seed)
-    p = torch.linspace(3.0, 1.0, E)
-    idx = torch.stack([torch.multinomial(p, k, replacement=False, generator=g) for _ in range(T)])
-    idx = idx.to(torch.int32)
+    p = torch.linspace(3.0, 1.0, E).expand(T, E)
+    idx = torch.multinomial(p, k, replacement=False, generator=g).to(torch.int32)
     idx[torch.randperm(T, generator=g)[: max(1, T // 97)]] = -1
     return idx
 
@@ -60,9 +59,13 @@ def _dispatch_both(M, T, d, E, k, cf, seed):
 
 
 def test_static_dispatch_matches_workspace_dispatch_twice(M):
-    # first call: 12 chunks of 4096 slots, 300 experts; second call: fewer
-    # chunks and experts, so it runs over scratch the first call left behind
-    for T, d, E, k, cf, seed in [(24000, 256, 300, 2, 1.0, 31), (5000, 128, 16, 2, 0.8, 32)]:
+    # The dispatch cuts the slots into chunks of 1024 (T*k <= 2^18) or 4096.
+    # First call: 300,000 slots, 74 chunks of 4096, 64 experts; second: 48,000
+    # slots, 47 chunks of 1024, 300 experts; third: 10,000 slots, 10 chunks,
+    # 16 experts -- each later call runs over the scratch the earlier ones
+    # left behind.
+    for T, d, E, k, cf, seed in [(150000, 128, 64, 2, 1.0, 30), (24000, 256, 300, 2, 1.0, 31),
+                                 (5000, 128, 16, 2, 0.8, 32)]:
         ref, got = _dispatch_both(M, T, d, E, k, cf, seed)
         for key in ("kept", "offsets", "pos", "stats"):
             assert torch.equal(got[key], ref[key]), key
