@@ -43,14 +43,12 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s at E=64 top-2 bf16; grouped-GEMM % peak; decode % HBM BW"
 WEIGHTS = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2", "expert_bias")
-# dram bytes (read + write) per grouped_gemm_tc_kernel launch at the large
-# prefill shapes, from an ncu capture of the four-expert slice scaled by the
-# kept rows, keyed by the sha256 of the kernel source it was taken on (the
-# figure is reported only while the source is unchanged)
-GEMM_TRAFFIC = {
-    # profiles/grouped_gemm_large_prefill_slice.md
-    "60216de4f5163834f35f4ef06dc060962625ca2a65f0a5176ac42066576cbf9f": 12.35e9,
-}
+# DRAM bytes (read + write) of one moe_expert_ffn call -- its GEMM-1 and
+# GEMM-2 launches together -- at the large-prefill shapes, from an ncu
+# capture of the four-expert slice scaled to the 64 experts by the kept
+# rows, keyed by the sha256 of the kernel source it was taken on (the figure
+# is reported only while that source is unchanged)
+GEMM_TRAFFIC = {}
 
 
 def load_peaks():
@@ -65,7 +63,8 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 100 ms while running."""
+    """nvidia-smi clock / throttle samples every 100 ms while running, each
+    stamped with the host time, so a summary can cover one timed region."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -91,7 +90,7 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) == 7:
-                self.rows.append(parts)
+                self.rows.append((time.time(), parts))
 
     def __exit__(self, *a):
         if self.proc:
@@ -101,15 +100,33 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        if not self.rows:
+    def summary(self, t_from=None, t_to=None):
+        """Median SM clock, max clock and the throttle reasons seen, over the
+        samples taken between host times t_from and t_to (all if None)."""
+        rows = [r for ts, r in self.rows if (t_from is None or ts >= t_from) and (t_to is None or ts <= t_to)]
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(rows)}
+
+
+def percentiles(ms):
+    """Median and the p10-p90 range of per-step times (ms)."""
+    import numpy as np
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90))}
+
+
+def gemm_bytes(r):
+    """Algorithmic DRAM bytes of one moe_expert_ffn call: the touched expert
+    weights once, and per kept row its input row read, its hidden row written
+    by GEMM-1 and read by GEMM-2, its output row written (bf16)."""
+    wl = r["wl"]
+    return r["touched_weight_bytes"] + r["stats"]["kept_slots"] * 2 * (2 * wl.d + 2 * wl.h)
 
 
 def gemm_traffic():
@@ -171,13 +188,14 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     cfg = M.config_of(wl)
     weights = {n: t.get(n) for n in WEIGHTS}
     x, noise = t["x"], t.get("noise")
-    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=dev)
+    sdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    y = torch.empty(wl.T, wl.d, dtype=sdt, device=dev)
     st = M.moe.stats_buffer(dev)
     saved = M.moe.alloc_saved(cfg, dev)
     ws = M.moe.workspace(cfg, training=True, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    Hs = torch.empty(wl.T, wl.h, dtype=torch.bfloat16, device=dev) if wl.has_shared else None
+    Hs = torch.empty(wl.T, wl.h, dtype=sdt, device=dev) if wl.has_shared else None
     sv = saved
 
     # one step = the layer's C-ABI stages in the order moe_layer_fwd runs them
@@ -215,14 +233,17 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     steps = args.steps
     sampler = ClockSampler(local)
     with sampler:
-        # --- timed region 1: K forwards through the single moe_layer_fwd call (the value) ---
+        # --- timed region 1: K forwards through the single moe_layer_fwd call
+        # (the value), an event after each step for the per-step spread ---
         barrier()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(steps):
+        h0 = time.time()
+        fe = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        fe[0].record(stream)
+        for i in range(steps):
             M.moe_layer_fwd(cfg, weights, x, noise, y, saved, st, ws)
-        f1.record(stream)
+            fe[i + 1].record(stream)
         barrier()
+        h1 = time.time()
         # --- timed region 2: the same steps through the stage entry points, an
         # event before each step and after every stage (the per-kernel times;
         # a step-start event that fires late marks the GPU waiting on the host) ---
@@ -236,9 +257,15 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
                 fn()
                 evs[i][j].record(stream)
         barrier()
-    clocks = sampler.summary()
-    ms_total = f0.elapsed_time(f1)
+        h2 = time.time()
+    # the clocks of each region side by side: the stage path's kernel times
+    # (the GEMM figure of the roofline) come from region 2
+    clocks = sampler.summary(h0, h1)
+    stage_clocks = sampler.summary(h1, h2)
+    ms_total = fe[0].elapsed_time(fe[-1])
+    step_ms = [fe[i].elapsed_time(fe[i + 1]) for i in range(steps)]
     stage_ms_total = e0.elapsed_time(evs[-1][-1])
+    stage_step_ms = [(pre[i].elapsed_time(evs[i][-1])) for i in range(steps)]
     comp = {name: 0.0 for name, _ in stages}
     comp["host_gap"] = 0.0
     prev = e0
@@ -256,8 +283,11 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     peaks = load_peaks()
     out = {
         "ms_per_step": ms_step,
+        "step_ms": percentiles(step_ms),
         "layer_fwd_ms": layer_fwd_ms,
         "stage_path_ms": stage_ms_total / steps,
+        "stage_step_ms": percentiles(stage_step_ms),
+        "stage_clocks": stage_clocks,
         # our kernels per step: moe_layer_fwd = zeroing, router GEMM + top-k,
         # 4 dispatch, entropy mean, 2 grouped GEMMs, combine (11); the stage
         # path = the same without the entropy mean, plus moe_expert_ffn's
@@ -287,7 +317,7 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     # neighbours' compute (events order each buffer's reuse).
     xh = x.cpu().pin_memory()
     nh = noise.cpu().pin_memory() if noise is not None else None
-    yh = [torch.empty(wl.T, wl.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    yh = [torch.empty(wl.T, wl.d, dtype=sdt).pin_memory() for _ in range(2)]
     xd = [torch.empty_like(x) for _ in range(2)]
     nd = [torch.empty_like(noise) if noise is not None else None for _ in range(2)]
     yd = [torch.empty_like(y) for _ in range(2)]
@@ -414,70 +444,167 @@ def run_training(args, world, rank, local):
             "clocks": sampler.summary()}
 
 
-def cpu_baseline(wl_name, gpu_tensors=None, max_rows=None, budget_s=20.0):
-    """fp64 oracle on the host cores, on a bounded sample of the workload:
-    router, top-k, capacity and dispatch of the whole batch, then the expert
-    FFN of the kept rows of the two busiest experts (at most `max_rows` rows,
-    stopping after `budget_s`).  Whole-layer tokens/s is extrapolated per
-    token: routing share + (expert rows per token) x (measured cost per row).
-    Inputs come from the GPU run when given (the oracle copies only the
-    expert slices it reads); otherwise a 2048-token batch and the two
-    experts' weight slices are drawn on the host."""
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# How the oracle is timed per workload: the whole layer where it runs in
+# seconds to a minute; else router, top-k, capacity and dispatch of the whole
+# batch plus the expert rows of the two busiest experts, extrapolated per
+# token by the measured cost of an expert row (forward and backward for the
+# training step).
+CPU_PLAN = {"tiny_fp32": ("whole", None), "small_prefill": ("whole", None), "decode": ("whole", None),
+            "large_prefill": ("experts", None), "training": ("train", 192)}
+
+
+def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None):
+    """The fp64 oracle as it stands, on ONE host core (its BLAS held to one
+    thread), on the workload's inputs (from the GPU run when given, else
+    drawn on the host at T <= 2048 for the expert-sampling modes):
+      whole   -- layer_forward over the whole batch;
+      experts -- route_and_dispatch of the whole batch, then expert_ffn on the
+                 kept rows of the two busiest experts (at most max_rows each);
+                 tokens/s extrapolated: routing share + expert rows per token
+                 (kept slots / T, + 1 with a shared expert) x cost per row;
+      train   -- the same with expert_ffn_backward (forward and backward of
+                 the rows) for the training step."""
     import numpy as np
     import torch
     import moe_synth as S
     from oracle import moe_oracle as O
 
     wl = S.WORKLOADS[wl_name]
+    plan, rows_cap = CPU_PLAN.get(wl_name, ("experts", None))
+    mode = mode or plan
+    max_rows = max_rows if max_rows is not None else rows_cap
     if gpu_tensors is not None:
-        t = gpu_tensors
+        t, T = gpu_tensors, wl.T
+    elif mode == "whole":
         T = wl.T
+        t = S.make_inputs(wl, "cpu")
     else:
+        # a 2048-token batch on the host; expert weights are drawn below for
+        # the two experts that are timed only
         T = min(wl.T, 2048)
-        t = S.make_inputs(wl.replace(T=T), "cpu", parts=["x", "Wr", "expert_bias", "noise"])
+        t = S.make_inputs(wl.replace(T=T), "cpu", parts=["x", "Wr", "expert_bias", "noise", "dY"])
     cfg = dict(T=T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act,
                capacity_factor=float(np.float32(wl.capacity_factor)), min_capacity=wl.min_capacity,
                lam=float(np.float32(wl.lam)), has_shared=wl.has_shared)
+    host = os.cpu_count() or 1
+    cores = blas_threads()
+    common = {"unit": "tokens/s", "cores": cores, "kind": "oracle", "host_cores": host, "cpu_model": _cpu_model(),
+              "threads": f"{cores} core{'s' if cores != 1 else ''} of {host}"}
+    if mode == "whole":
+        t0 = time.perf_counter()
+        O.layer_forward(cfg, t, t["x"], t.get("expert_bias"), t.get("noise"))
+        dt = time.perf_counter() - t0
+        return dict(common, value=T / dt, seconds=dt, extrapolated=False,
+                    sample=f"fp64 oracle layer_forward of the whole batch ({T} tokens) in {dt:.2f} s")
     t0 = time.perf_counter()
     r = O.route_and_dispatch(cfg, t["x"], t["Wr"], t.get("expert_bias"), t.get("noise"))
     t_route = time.perf_counter() - t0
     experts = [int(e) for e in np.argsort(-r["kept"], kind="stable")[:2]]
-    if gpu_tensors is not None:
-        weights = {n: t[n] for n in ("W1", "W3", "W2", "b1", "b2") if t.get(n) is not None}
-    else:
-        weights = {}
-        dt, d, h = wl.dtype, wl.d, wl.h
-        for name, (rows, cols, fan) in dict(W1=(h, d, d), W3=(h, d, d), W2=(d, h, h)).items():
+    if "W1" not in t:
+        t = dict(t)
+        for name, (rows_, cols, fan) in dict(W1=(wl.h, wl.d, wl.d), W3=(wl.h, wl.d, wl.d),
+                                             W2=(wl.d, wl.h, wl.h)).items():
             if name == "W3" and wl.act != "swiglu":
                 continue
-            weights[name] = {e: S.tensor("normal", wl.seed, S.TID[name], (rows, cols), dt, wl.std(fan),
-                                         "cpu", start=e * rows * cols) for e in experts}
-    X = None
+            t[name] = {e: S.tensor("normal", wl.seed, S.TID[name], (rows_, cols), wl.dtype, wl.std(fan), "cpu",
+                                   start=e * rows_ * cols) for e in experts}
     slots = 0
     t1 = time.perf_counter()
     for e in experts:
-        rows, _ = np.nonzero((r["idx"] == e) & (r["pos"] >= 0))
+        rows, sl = np.nonzero((r["idx"] == e) & (r["pos"] >= 0))
         if max_rows is not None:
-            rows = rows[:max_rows]
-        src = t["x"][torch.as_tensor(rows, device=t["x"].device)] if rows.size else t["x"][:0]
-        p = O.expert_params(weights, e, wl.act)
-        O.expert_ffn(O.decode(src), wl.act, **p)
+            rows, sl = rows[:max_rows], sl[:max_rows]
+        src = O.decode(t["x"][torch.as_tensor(rows, device=t["x"].device)]) if rows.size else None
+        p = O.expert_params(t, e, wl.act)
+        if src is not None:
+            if mode == "train":
+                dy = O.decode(t["dY"][torch.as_tensor(rows, device=t["dY"].device)])
+                O.expert_ffn_backward(src, r["w"][rows, sl][:, None] * dy, wl.act, **p)
+            else:
+                O.expert_ffn(src, wl.act, **p)
         slots += rows.size
-        if time.perf_counter() - t1 > budget_s:
-            break
     t_ffn = time.perf_counter() - t1
     per_row = t_ffn / max(slots, 1)
     rows_per_token = float(r["kept"].sum()) / T + (1 if wl.has_shared else 0)
     per_token = t_route / T + per_row * rows_per_token
+    what = "forward and backward of" if mode == "train" else "expert FFN of"
+    return dict(common, value=1.0 / per_token, seconds=t_route + t_ffn, extrapolated=True,
+                sample=f"fp64 oracle: router+top-k+capacity+dispatch of all {T} tokens ({t_route:.2f} s), "
+                       f"{what} {slots} kept rows of experts {experts} ({t_ffn:.2f} s); whole-layer tokens/s "
+                       f"extrapolated per token at {rows_per_token:.3f} expert rows/token")
+
+
+ONE_THREAD = {v: "1" for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")}
+
+
+def blas_threads():
+    """Threads numpy's BLAS runs with: from threadpoolctl when it is
+    installed, else from the thread-count variables the BLAS read at load."""
     try:
         from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:
-        cores = os.cpu_count() or 1
-    return {"value": 1.0 / per_token, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"fp64 numpy oracle: router+top-k+capacity+dispatch of all {T} tokens ({t_route:.2f} s), "
-                      f"expert FFN of {slots} kept rows of experts {experts} ({t_ffn:.2f} s); whole-layer "
-                      f"tokens/s extrapolated per token at {rows_per_token:.3f} expert rows/token"}
+        for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(v, "").isdigit():
+                return int(os.environ[v])
+        return os.cpu_count() or 1
+
+
+def cpu_baselines(local):
+    """cpu_baseline of every workload of the plan, each in a child process
+    whose BLAS is held to one thread by the thread-count variables (set
+    before numpy loads); the child draws its inputs on the GPU."""
+    out = {}
+    for name in ("tiny_fp32", "small_prefill", "decode", "large_prefill", "training"):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", name,
+                            "--local-rank", str(local)], env=dict(os.environ, **ONE_THREAD),
+                           capture_output=True, text=True, timeout=900)
+        lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+        out[name] = json.loads(lines[-1]) if r.returncode == 0 and lines else {
+            "unavailable": (r.stderr.strip().splitlines() or ["no output"])[-1]}
+    return out
+
+
+def layer_section(r, peaks, peak):
+    """Throughput and roofline of one workload's layer forward (run_gpu's
+    result): tokens/s, the per-step spread, algorithmic FLOPs (expert rows,
+    the shared expert's T rows, the router's 2*T*d*E) and bytes (the touched
+    weights once, x read, y written), and the roofline fraction
+    max(FLOPs / tensor peak, bytes / HBM) / measured step time."""
+    wl = r["wl"]
+    es = 2 if wl.dtype == "bf16" else 4
+    flops = r["gemm"]["flops"] + shared_flops(wl) + 2.0 * wl.T * wl.d * wl.E
+    bytes_ = r["touched_weight_bytes"] * es // 2 + 2 * wl.T * wl.d * es
+    t_tensor, t_hbm = flops / (peak * 1e12), bytes_ / (peaks["hbm_gbs"] * 1e9)
+    ms = r["ms_per_step"]
+    bias = "" if wl.zipf_s is None else f" zipf_bias={'ln pmf ' if wl.zipf_log else ''}{wl.zipf_s}"
+    out = {"workload": f"{wl.name}: T={wl.T} d={wl.d} h={wl.h} E={wl.E}{'+1 shared' if wl.has_shared else ''} "
+                       f"top-{wl.k} {wl.act} cf={wl.capacity_factor}{bias} {wl.dtype}",
+           "ms_per_step": ms, "step_ms": r["step_ms"], "tokens_per_s": r["tokens_per_s"],
+           "tflops": flops / (ms * 1e-3) / 1e12, "algorithmic_flops": flops, "algorithmic_bytes": bytes_,
+           "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+           "roofline_ms": max(t_tensor, t_hbm) * 1e3, "roofline_frac": max(t_tensor, t_hbm) / (ms * 1e-3),
+           "kept_slots": r["stats"]["kept_slots"], "drop_rate": r["stats"]["drop_rate"],
+           "balance_stat": r["stats"]["balance_stat"], "e2e": r["e2e"],
+           "components_ms": {k: round(v, 4) for k, v in r["components_ms"].items()}, "clocks": r["clocks"]}
+    if wl.dtype != "bf16":
+        # fp32 runs on the CUDA cores, not the bf16 tensor path; at this size
+        # the layer is launch-latency bound and the fraction is only a figure
+        out["bound"] = "latency"
+        out["launches_per_step"] = r["launches_per_step"] // 2
+        out["us_per_launch"] = ms * 1e3 / out["launches_per_step"]
+    return out
 
 
 def main():
@@ -491,13 +618,30 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-training", action="store_true")
     ap.add_argument("--no-fine-grained", action="store_true")
+    ap.add_argument("--no-small-prefill", action="store_true")
+    ap.add_argument("--no-tiny-fp32", action="store_true")
+    ap.add_argument("--no-large-prefill-3z", action="store_true")
+    ap.add_argument("--cpu-baseline-child", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--local-rank", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
 
+    if args.cpu_baseline_child:
+        # one workload's oracle timing (run by cpu_baselines with one BLAS thread)
+        import torch
+        import moe_synth as S
+        dev = torch.device("cuda", args.local_rank)
+        torch.cuda.set_device(dev)
+        t = S.make_inputs(S.WORKLOADS[args.cpu_baseline_child], dev)
+        print(json.dumps(cpu_baseline(args.cpu_baseline_child, t)))
+        return 0
+
     if args.impl == "reference":
         if rank != 0:
             return 0
+        # the oracle on one host core: the BLAS reads these before numpy loads
+        os.environ.update(ONE_THREAD)
         import torch
         dev_ok = torch.cuda.is_available()
         t0 = time.time()
@@ -509,7 +653,10 @@ def main():
             torch.cuda.set_device(local)
             gt = S.make_inputs(S.WORKLOADS[args.workload], torch.device("cuda", local))
         for i in range(args.warmup + args.steps):
-            cb = cpu_baseline(args.workload, gt, max_rows=128, budget_s=max(1.0, 60.0 / (args.steps + args.warmup)))
+            # each step: the whole routing plus up to 48 rows of each of the
+            # two busiest experts, on one core
+            cb = cpu_baseline(args.workload, gt, mode="train" if args.workload == "training" else None,
+                              max_rows=48)
             if i >= args.warmup:
                 vals.append(cb["value"])
         v = statistics.median(vals)
@@ -552,10 +699,16 @@ def main():
                          f"x {wl.T * wl.d * 2 / 1e6:.0f} MB vs 126 MB L2), no flush"},
         "roofline": {"bound": "tensor", "achieved": gemm["tflops"], "peak": peak, "unit": "TFLOP/s",
                      "frac": gemm["tflops"] / peak, "traffic": gemm_traffic(),
+                     "traffic_per": "one moe_expert_ffn call (its GEMM-1 and GEMM-2 launches), DRAM bytes",
+                     "algorithmic_bytes": gemm_bytes(r),
                      "kernel": "grouped_gemm_tc_kernel (GEMM-1 SwiGLU + GEMM-2, one moe_expert_ffn call)",
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
-                     "frac_of_burst": gemm["tflops"] / peaks["bf16"]},
+                     "frac_of_burst": gemm["tflops"] / peaks["bf16"],
+                     "gemm_ms": gemm["ms"], "gemm_ms_from": "stage-path region (clocks: stage_clocks)"},
+        "step_ms": r["step_ms"],
         "clocks": r["clocks"],
+        "stage_clocks": r["stage_clocks"],
+        "stage_step_ms": r["stage_step_ms"],
         "e2e": r["e2e"],
         "gpu_launches": r["launches_per_step"] * args.steps,
         "components_ms": {k: round(v, 4) for k, v in r["components_ms"].items()},
@@ -569,6 +722,15 @@ def main():
     line["layer_roofline_frac"] = t_roof / (r["ms_per_step"] * 1e-3)
 
     del r["tensors"]
+    # the small prefill and the tiny fp32 layer: throughput and roofline
+    for name, n_min in (("small_prefill", 100), ("tiny_fp32", 200), ("large_prefill_3z", 40)):
+        if getattr(args, "no_" + name):
+            continue
+        sargs = argparse.Namespace(**vars(args))
+        sargs.steps = max(args.steps, n_min)  # >= 0.25 s timed for the clock sampler (small prefill)
+        sr = run_gpu(sargs, name, world, rank, local)
+        line[name] = layer_section(sr, peaks, peak)
+        del sr["tensors"]
     if not args.no_decode:
         dargs = argparse.Namespace(**vars(args))
         dargs.steps = max(args.steps, 100)  # >= 0.25 s timed, so the clock sampler sees it
@@ -623,9 +785,9 @@ def main():
         tr["frac_of_sustained"] = tr["tflops"] / (peaks["bf16_sus"] * world)  # per GPU
         line["training"] = tr
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import moe_synth as S
-        gt = S.make_inputs(S.WORKLOADS[args.workload], torch.device("cuda", local))
-        line["cpu_baseline"] = cpu_baseline(args.workload, gt)
+        cb = cpu_baselines(local)
+        line["cpu_baseline"] = cb[args.workload] if args.workload in cb else None
+        line["cpu_baselines"] = cb
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
