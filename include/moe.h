@@ -104,6 +104,16 @@ enum { MOE_F32 = 0, MOE_BF16 = 1 };
  *    its expert gradients to the backup that served it. */
 enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2, MOE_ROUTE_LAYERNORM = 4, MOE_ROUTE_REROUTE = 8 };
 
+/* Tile choices of the forward expert GEMMs (moe_config.gemm_flags; no effect
+ * on any result bit, only on speed; the pages have no counterpart).
+ *  MOE_GEMM_CTA_PAIRS: groups averaging >= 256 rows run 256-row tiles on
+ *    clusters of two CTAs on two SMs, one tcgen05 M=256 MMA (cta_group::2)
+ *    per K step, each CTA staging half of the rows and half of the weight
+ *    tile.  It raises tensor-pipe activity per cycle (GEMM-1 of the large
+ *    prefill: 66% -> 73%) but, on a power-capped part, draws the clock down
+ *    by as much, so it is off by default. */
+enum { MOE_GEMM_CTA_PAIRS = 1 };
+
 /* Load-balance term (moe_config.balance).  f[e] = counts[e]/T (pre-capacity
  * usage), g[e] = I[e]/T with I[e] the sum of the routing weights of the
  * slots routed to e (the importance of [P4] 2.2).  moe_stats.balance_stat
@@ -136,6 +146,7 @@ typedef struct {
   int route_flags;       /* MOE_ROUTE_* bits, 0 = renormalised, slot-major     */
   int balance;           /* MOE_BALANCE_*, 0 = the CV form                     */
   float balance_gamma;   /* gamma of MOE_BALANCE_STD_MAX (100 in [P2] 3.2)     */
+  int gemm_flags;        /* MOE_GEMM_* bits, 0 = the default tiles             */
 } moe_config;
 
 typedef struct {
@@ -290,6 +301,47 @@ moe_status moe_dispatch(const moe_config* cfg, const int* idx, const void* x,
 moe_status moe_dispatch_static(const moe_config* cfg, const int* idx, const void* x,
                                int* kept, int* offsets, int* pos, void* Xp,
                                moe_stats* stats, moe_stream_t stream);
+
+/* Expert parallelism ([P1] 4.2-4.3 and [P2] 4.1: experts on different GPUs,
+ * tokens sent to them and back with all-to-all; [P5] "Experts on different
+ * GPUs: a new kind of waiting").  R ranks each hold their own tokens and the
+ * weights of a contiguous block of experts.  The layer keeps the one-GPU
+ * result on the ranks' batches concatenated in rank order: the capacity C
+ * is the global one, and slot-major priority runs over all ranks' first
+ * choices (rank 0's tokens, then rank 1's, ...) before any second choice.
+ * The ranks exchange their per-(slot, expert) counts (moe_slot_counts); from
+ * all of them every rank derives the same plan -- for each of its slots
+ * (j, e), the earlier slots of the other ranks routed to e (rank_adjust)
+ * and the row where the slot's run starts in its send buffer (send_adjust);
+ * the host computes the plan (the binding's ep module).  Rows then travel
+ * by all-to-all: the send buffer holds each owner's rows, expert by expert,
+ * each expert's rows in slot-major order. */
+
+/* counts[j*E + e] = #{t : idx[t,j] = e}, int32 [k, E] (zeroed by this
+ * call); idx [T,k] from moe_route. */
+moe_status moe_slot_counts(const moe_config* cfg, const int* idx, int* counts, moe_stream_t stream);
+
+/* moe_dispatch for one rank of an expert-parallel layer (slot-major
+ * priority only; MOE_ROUTE_TOKEN_MAJOR and MOE_ROUTE_REROUTE return
+ * MOE_ERR_UNSUPPORTED).  A slot (t,j) routed to e with local slot-major
+ * rank L (the number of this rank's earlier slots routed to e) is kept iff
+ * L + rank_adjust[j*E + e] < capacity, the global capacity; then pos[t,j] =
+ * L + send_adjust[j*E + e] and Xsend[pos[t,j]] = x[t]; else pos[t,j] = -1.
+ * rank_adjust, send_adjust: device int32 [k, E] from the plan.  Xsend: the
+ * send buffer, as many rows as the plan sends (nullable: positions only).
+ * ws: >= moe_workspace_size(cfg, 1) bytes. */
+moe_status moe_dispatch_ep(const moe_config* cfg, const int* idx, const void* x, const int* rank_adjust,
+                           const int* send_adjust, int capacity, int* pos, void* Xsend, void* ws,
+                           moe_stream_t stream);
+
+/* Row permutation on the device, rows of row_bytes (a multiple of 16):
+ * scatter != 0: dst[map[i]] = src[i]; scatter == 0: dst[i] = src[map[i]];
+ * for i < n, skipping map[i] < 0.  An expert-parallel owner scatters the
+ * rows it received into expert-contiguous order (map: each row's place from
+ * the plan), runs moe_expert_ffn there, and gathers the outputs back into
+ * the received order for the return all-to-all. */
+moe_status moe_permute_rows(const void* src, const int* map, long long n, long long row_bytes, int scatter,
+                            void* dst, moe_stream_t stream);
 
 /* Grouped expert FFN over expert-contiguous rows ([P2] 4.2 and [P3] 3.3:
  * Linear -> GELU -> Linear; SwiGLU gate/up; [P2] 4.1 all experts' weights

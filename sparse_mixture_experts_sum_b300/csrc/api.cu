@@ -24,6 +24,7 @@ moe_status validate(const moe_config* cfg) {
   if ((cfg->route_flags & MOE_ROUTE_REROUTE) && cfg->k > 4) return MOE_ERR_UNSUPPORTED;
   if (cfg->balance < MOE_BALANCE_CV || cfg->balance > MOE_BALANCE_SWITCH) return MOE_ERR_INVALID_ARG;
   if (!(cfg->balance_gamma == cfg->balance_gamma) || isinf(cfg->balance_gamma)) return MOE_ERR_INVALID_ARG;
+  if (cfg->gemm_flags & ~MOE_GEMM_CTA_PAIRS) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -97,7 +98,7 @@ WsLayout layout(const moe_config* cfg, int training) {
     L.total = o;
     return L;
   }
-  L.dispatch_off = take(dispatch_scratch_bytes(*cfg));
+  L.dispatch_off = take(dispatch_ep_scratch_bytes(*cfg));  // also serves moe_dispatch_ep
   L.route_off = take(route_scratch_bytes(*cfg));
   L.ent = take(T * 4);
   L.imp = cfg->balance == MOE_BALANCE_SWITCH ? take(E * 8) : 0;
@@ -149,6 +150,7 @@ moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, cons
   g1.ldz = swiglu ? 2LL * cfg->h : cfg->h;
   g1.bias = swiglu ? nullptr : b1;
   g1.err = err;
+  g1.cta_pairs = (cfg->gemm_flags & MOE_GEMM_CTA_PAIRS) != 0;
   GemmParams g2 = g1;
   g2.N = cfg->d;
   g2.K = cfg->h;
@@ -340,6 +342,33 @@ moe_status moe_dispatch_static(const moe_config* cfg, const int* idx, const void
   if (s != MOE_OK) return s;
   return launch_dispatch(*cfg, capacity_of(cfg), idx, x, kept, offsets, pos, Xp, stats, scratch, nullptr,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_slot_counts(const moe_config* cfg, const int* idx, int* counts, moe_stream_t stream) {
+  const moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!idx || !counts) return MOE_ERR_INVALID_ARG;
+  return launch_slot_counts(*cfg, idx, counts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_dispatch_ep(const moe_config* cfg, const int* idx, const void* x, const int* rank_adjust,
+                           const int* send_adjust, int capacity, int* pos, void* Xsend, void* ws,
+                           moe_stream_t stream) {
+  const moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!idx || !x || !rank_adjust || !send_adjust || !pos || !ws || capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->route_flags & (MOE_ROUTE_TOKEN_MAJOR | MOE_ROUTE_REROUTE)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(ws) || (Xsend && !aligned16(Xsend))) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(cfg, 1);
+  return launch_dispatch_ep(*cfg, idx, x, rank_adjust, send_adjust, capacity, pos, Xsend, at(ws, L.dispatch_off),
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute_rows(const void* src, const int* map, long long n, long long row_bytes, int scatter,
+                            void* dst, moe_stream_t stream) {
+  if (n < 0 || (n > 0 && (!src || !map || !dst))) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (!aligned16(src) || !aligned16(dst))) return MOE_ERR_INVALID_ARG;
+  return launch_permute_rows(src, map, n, row_bytes, scatter, dst, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offsets, const void* W1,

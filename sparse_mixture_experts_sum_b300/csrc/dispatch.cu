@@ -254,15 +254,28 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
   }
 }
 
+// Expert-parallel placement of a rank's slots (adj == nullptr: none).  With
+// experts split over ranks, a slot's rank among all ranks' slots routed to
+// its expert is its local slot-major rank plus adj[j*E + e] (the earlier
+// slots of the other ranks, from the exchanged counts); it is kept iff that
+// global rank is below C, and then goes to row rank + send[j*E + e] of the
+// rank's send buffer (rows grouped by owner rank, expert, slot, token).
+struct EpMap {
+  const int* adj;
+  const int* send;
+  int C;
+};
+
 // Ranks of one pass and the slots' places.  Pass 1: p = offsets[e] + rank
 // (offsets == nullptr: the bare rank, kept for a second pass).  Pass 2
 // (used = the first pass's kept rows): a rerouted slot lands after its new
 // expert's first-pass rows, p = offsets[e] + used[e] + rank; a slot the
-// first pass kept gets p = offsets[e0] + rank1.
+// first pass kept gets p = offsets[e0] + rank1.  Expert parallel (ep.adj):
+// p = rank + ep.send[j*E + e] when rank + ep.adj[j*E + e] < ep.C.
 __global__ void __launch_bounds__(DT) assign_kernel(SlotSrc S, int T, int k, int E, bool token_major, int CH,
                                                     const int* __restrict__ base, const int* __restrict__ kept,
                                                     const int* __restrict__ offsets, const int* __restrict__ used,
-                                                    int* __restrict__ pos) {
+                                                    int* __restrict__ pos, EpMap ep = EpMap{nullptr, nullptr, 0}) {
   extern __shared__ int sm[];
   int* runcnt = sm;       // [E]
   int* warpcnt = sm + E;  // [DW][E]
@@ -293,11 +306,16 @@ __global__ void __launch_bounds__(DT) assign_kernel(SlotSrc S, int T, int k, int
         int prefix = 0;
         for (int w2 = 0; w2 < warp; ++w2) prefix += warpcnt[w2 * E + e];
         const int rank = bbase[e] + runcnt[e] + prefix + lrank;
-        // kept[e] = min(routed[e], C) (+ the first pass's rows): a slot is
-        // kept iff its rank is below its pass's share, which also keeps every
-        // position inside [offsets[e], offsets[e+1])
-        const int u = used ? used[e] : 0;
-        if (rank < kept[e] - u) p = (offsets ? offsets[e] : 0) + u + rank;
+        if (ep.adj) {
+          const int je = j * E + e;
+          if (rank + ep.adj[je] < ep.C) p = rank + ep.send[je];
+        } else {
+          // kept[e] = min(routed[e], C) (+ the first pass's rows): a slot is
+          // kept iff its rank is below its pass's share, which also keeps
+          // every position inside [offsets[e], offsets[e+1])
+          const int u = used ? used[e] : 0;
+          if (rank < kept[e] - u) p = (offsets ? offsets[e] : 0) + u + rank;
+        }
       } else if (used && e0 >= 0 && e0 < E) {
         const int r1 = S.rank1[static_cast<size_t>(t) * k + j];
         if (r1 >= 0) p = offsets[e0] + r1;
@@ -452,6 +470,38 @@ __global__ void __launch_bounds__(1024) entropy_mean_kernel(const float* __restr
   }
 }
 
+// counts[j*E + e] = the slots (t, j) routed to expert e: the per-slot
+// histogram that expert-parallel ranks exchange.  Integer atomics, so the
+// result does not depend on their order.
+__global__ void slot_counts_kernel(const int* __restrict__ idx, int T, int k, int E, int* __restrict__ counts) {
+  extern __shared__ int hc[];  // k * E
+  for (int i = threadIdx.x; i < k * E; i += blockDim.x) hc[i] = 0;
+  __syncthreads();
+  const long long n = static_cast<long long>(T) * k;
+  for (long long s = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; s < n;
+       s += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int e = idx[s];
+    if (e >= 0 && e < E) atomicAdd(&hc[static_cast<int>(s % k) * E + e], 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < k * E; i += blockDim.x)
+    if (hc[i]) atomicAdd(&counts[i], hc[i]);
+}
+
+// One warp per row: dst[map[i]] = src[i] (scatter) or dst[i] = src[map[i]]
+// (gather), rows of vec_per_row 16-byte vectors; map[i] < 0 skips row i.
+__global__ void permute_rows_kernel(const uint4* __restrict__ src, const int* __restrict__ map, long long n,
+                                    int vec_per_row, int scatter, uint4* __restrict__ dst) {
+  const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (i >= n) return;
+  const int m = map[i];
+  if (m < 0) return;
+  const uint4* s = src + (scatter ? i : static_cast<long long>(m)) * vec_per_row;
+  uint4* d = dst + (scatter ? static_cast<long long>(m) : i) * vec_per_row;
+  for (int v = lane; v < vec_per_row; v += 32) d[v] = s[v];
+}
+
 inline int n_chunks(const moe_config& cfg) {
   const long long n = static_cast<long long>(cfg.T) * cfg.k;
   const int ch = chunk_slots(n);
@@ -559,6 +609,63 @@ moe_status static_dispatch_scratch(size_t need, void** ptr) {
   if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
   *ptr = p;
   return MOE_OK;
+}
+
+moe_status launch_slot_counts(const moe_config& cfg, const int* idx, int* counts, cudaStream_t stream) {
+  moe_status s = launch_zero(counts, static_cast<size_t>(cfg.k) * cfg.E * sizeof(int), nullptr, 0, stream);
+  if (s != MOE_OK) return s;
+  const long long n = static_cast<long long>(cfg.T) * cfg.k;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 1184) blocks = 1184;
+  slot_counts_kernel<<<static_cast<unsigned>(blocks), 256, static_cast<size_t>(cfg.k) * cfg.E * sizeof(int),
+                       stream>>>(idx, cfg.T, cfg.k, cfg.E, counts);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t dispatch_ep_scratch_bytes(const moe_config& cfg) {
+  return dispatch_scratch_bytes(cfg) + align_up(static_cast<size_t>(2 * cfg.E + 1) * sizeof(int), 256);
+}
+
+moe_status launch_dispatch_ep(const moe_config& cfg, const int* idx, const void* x, const int* adj, const int* send,
+                              int C, int* pos, void* Xsend, void* scratch, cudaStream_t stream) {
+  const int nb = n_chunks(cfg);
+  uint8_t* sp = static_cast<uint8_t*>(scratch);
+  int* blockhist = reinterpret_cast<int*>(sp);
+  sp += align_up(static_cast<size_t>(nb) * (cfg.E + 1) * sizeof(int), 256);
+  int* base = reinterpret_cast<int*>(sp);
+  sp += align_up(static_cast<size_t>(nb) * cfg.E * sizeof(int), 256);
+  int* kept = reinterpret_cast<int*>(sp);  // E local counts (no local capacity), then E+1 offsets: unused
+  int* offsets = kept + cfg.E;
+  const int CH = chunk_slots(static_cast<long long>(cfg.T) * cfg.k);
+  const size_t asmem = static_cast<size_t>(cfg.E) * (DW + 1) * sizeof(int);
+  const SlotSrc S1{idx, nullptr, nullptr};
+  slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(S1, cfg.T, cfg.k, cfg.E, false, CH, blockhist);
+  // local slot-major ranks only: the capacity test is on the global rank
+  capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, 0x7fffffff, 0.f, 0, 0.f,
+                                               nullptr, base, kept, offsets, nullptr);
+  assign_kernel<<<nb, DT, asmem, stream>>>(S1, cfg.T, cfg.k, cfg.E, false, CH, base, kept, offsets, nullptr, pos,
+                                           EpMap{adj, send, C});
+  if (Xsend) {
+    const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
+    const long long row_bytes = static_cast<long long>(cfg.d) * es;
+    if (row_bytes % 16) return MOE_ERR_UNSUPPORTED;
+    const int vpr = static_cast<int>(row_bytes / 16);
+    const int ch = row_chunks(cfg.T, vpr);
+    permute_kernel<uint4><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(static_cast<const uint4*>(x), cfg.T, cfg.k, vpr,
+                                                                    ch, pos, static_cast<uint4*>(Xsend));
+  }
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_permute_rows(const void* src, const int* map, long long n, long long row_bytes, int scatter,
+                               void* dst, cudaStream_t stream) {
+  if (n <= 0) return MOE_OK;
+  if (row_bytes <= 0 || row_bytes % 16) return MOE_ERR_UNSUPPORTED;
+  const long long blocks = (n * 32 + 255) / 256;
+  if (blocks > 2147483647LL) return MOE_ERR_UNSUPPORTED;
+  permute_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint4*>(src), map, n, static_cast<int>(row_bytes / 16), scatter, static_cast<uint4*>(dst));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status launch_entropy_mean(const float* ent, int T, moe_stats* stats, cudaStream_t stream) {

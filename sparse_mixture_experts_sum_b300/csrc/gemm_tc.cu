@@ -57,21 +57,31 @@ constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN block of 64 K row
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_GROUPS = 1024;
 
-// Tile shape per BM (output rows per tile):
+// Tile shape per BM (output rows per CTA) and PAIR:
 //   BM = 128: 4-stage ring of 48 KB, two 128x256 accumulators (the epilogue
 //             of one tile overlaps the MMAs of the next), 4 epilogue warps;
 //   BM = 256: 3-stage ring of 64 KB, one 256x256 accumulator (two M=128
 //             MMAs per K step share the B tile: 2x the MACs per byte of
-//             shared memory filled), 8 epilogue warps.
-template <int BM_>
+//             shared memory filled), 8 epilogue warps;
+//   PAIR (BM = 128 per CTA, Fwd): a cluster of two CTAs on two SMs runs
+//             256-row tiles with one M=256 tcgen05 MMA per K step
+//             (cta_group::2).  Each CTA stages its own 128 A rows and half of
+//             the 256 B rows (32 KB per stage, 6 stages), and keeps two
+//             128x256 accumulators for its rows: the B bytes staged per MAC
+//             halve against BM = 128, and the epilogue still overlaps.  Both
+//             CTAs' copies of a stage complete on the even CTA's barrier.
+template <int BM_, bool PAIR = false>
 struct TileCfg {
-  static constexpr int BM = BM_;
+  static constexpr int BM = BM_;                        // output rows per CTA
+  static constexpr int TILE_M = PAIR ? 2 * BM_ : BM_;   // output rows per tile
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + 2 * B_HALF_BYTES;
-  static constexpr int STAGES = BM == 128 ? 4 : 3;
+  static constexpr int B_BYTES = PAIR ? B_HALF_BYTES : 2 * B_HALF_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = PAIR ? 6 : (BM == 128 ? 4 : 3);
   static constexpr int NACC = BM == 128 ? 2 : 1;
   static constexpr int EPI_WARPS = BM / 32;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static_assert(!PAIR || BM_ == 128, "pair tiles are two 128-row halves");
 };
 
 template <int STAGES>
@@ -89,10 +99,10 @@ struct __align__(8) Ctl {
   int tile_start[MAX_GROUPS + 1];  // first tile of each group (+ total)
 };
 
-template <int BM_>
+template <int BM_, bool PAIR = false>
 constexpr size_t smem_bytes() {
-  return 1024 + static_cast<size_t>(TileCfg<BM_>::STAGES) * TileCfg<BM_>::STAGE_BYTES +
-         sizeof(Ctl<TileCfg<BM_>::STAGES>);
+  return 1024 + static_cast<size_t>(TileCfg<BM_, PAIR>::STAGES) * TileCfg<BM_, PAIR>::STAGE_BYTES +
+         sizeof(Ctl<TileCfg<BM_, PAIR>::STAGES>);
 }
 
 struct Tile {
@@ -177,14 +187,16 @@ __device__ __forceinline__ void load_f32x32(const float* src, int col, int N, fl
   }
 }
 
-template <int KIND, int BM_>
-__global__ void __launch_bounds__(TileCfg<BM_>::THREADS, 1)
+template <int KIND, int BM_, bool PAIR>
+__global__ void __launch_bounds__(TileCfg<BM_, PAIR>::THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
                        const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapXA,
                        const __grid_constant__ CUtensorMap mapXB0, const __grid_constant__ CUtensorMap mapXB1,
                        const GemmParams p) {
-  using TC = TileCfg<BM_>;
+  static_assert(!PAIR || KIND == kKindFwd, "pair tiles are for the forward geometry");
+  using TC = TileCfg<BM_, PAIR>;
   constexpr int BM = TC::BM;
+  constexpr int TM = TC::TILE_M;
   constexpr int STAGES = TC::STAGES;
   constexpr int STAGE_BYTES = TC::STAGE_BYTES;
   constexpr int A_TILE_BYTES = TC::A_BYTES;
@@ -202,6 +214,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
   const int m_tiles_w = KIND == kKindWgrad ? (p.M + BM - 1) / BM : 1;
   const bool n_fast = KIND == kKindWgrad && p.M > p.N;
   const int nk_fixed = (p.K + BK - 1) / BK;
+  // PAIR: this CTA's rank in its cluster (0 issues the MMAs) and the tile
+  // stream of the cluster; otherwise one CTA per tile stream
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   // ---------------- set-up ----------------
   if (threadIdx.x == 0) {
@@ -211,7 +228,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&c.tmem_full[a], 1);
-      mbar_init(&c.tmem_empty[a], 32 * TC::EPI_WARPS);
+      // PAIR: one arrival per epilogue warp of both CTAs; else every thread
+      mbar_init(&c.tmem_empty[a], PAIR ? 2 * TC::EPI_WARPS : 32 * TC::EPI_WARPS);
     }
     mbar_init(&c.drain, 1);
     c.abort = 0;
@@ -222,8 +240,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     tma_prefetch_desc(&mapB1);
   }
   if (warp == 1) {
-    tmem_alloc(&c.tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&c.tmem_base, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&c.tmem_base, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == 2) {
     // per-group tile counts -> exclusive prefix (one warp, 32 groups a step)
@@ -239,7 +262,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         } else {
           const int r1 = p.offsets ? p.offsets[g + 1] : p.rows;
           const int rows = r1 - row;
-          tiles_g = rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+          tiles_g = rows > 0 ? ((rows + TM - 1) / TM) * n_tiles : 0;
         }
       }
       int incl = tiles_g;
@@ -256,11 +279,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     }
     if (lane == 0) {
       c.x_tile0 = carry;
-      c.total_tiles = carry + (KIND == kKindFwd && p.xrows > 0 ? ((p.xrows + BM - 1) / BM) * n_tiles : 0);
+      c.total_tiles = carry + (KIND == kKindFwd && p.xrows > 0 ? ((p.xrows + TM - 1) / TM) * n_tiles : 0);
     }
   }
   tc_fence_before();
   __syncthreads();
+  // PAIR: both CTAs' barriers are initialised before either signals the other's
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
 
   const int total = c.total_tiles;
@@ -270,8 +295,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       uint32_t it = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
+      for (int tile = tile0; tile < total && !*abort_flag; tile += tstep) {
+        const Tile t = tile_coords<KIND, TM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
         const bool xg = KIND == kKindFwd && t.g == G;  // the extra group
         const int grow = xg ? 0 : c.grp_row[t.g];
         // Wgrad: k-blocks of the group's rows (twice over with a hi/lo B pair)
@@ -284,8 +309,17 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             const CUtensorMap* mb0 = xg ? &mapXB0 : &mapB0;
             const CUtensorMap* mb1 = xg ? &mapXB1 : &mapB1;
             const int g_row = xg ? 0 : t.g * p.N;
-            emit(0, ma, kb * BK, grow + t.m * BM);
-            if (swiglu_fwd) {
+            // this CTA's 128 rows of the tile (PAIR: the odd CTA the upper half)
+            emit(0, ma, kb * BK, grow + t.m * TM + static_cast<int>(crank) * BM);
+            if constexpr (PAIR) {
+              // this CTA's half of the 256 B rows: SwiGLU W1 (even) or W3
+              // (odd) rows of the tile's 128 hidden units; plain rows
+              // [128 crank, 128 crank + 128) of the tile's 256 columns
+              if (swiglu_fwd)
+                emit(A_TILE_BYTES, crank ? mb1 : mb0, kb * BK, g_row + t.n * 128);
+              else
+                emit(A_TILE_BYTES, mb0, kb * BK, g_row + t.n * BN + static_cast<int>(crank) * 128);
+            } else if (swiglu_fwd) {
               const int b_row = g_row + t.n * 128;
               emit(A_TILE_BYTES, mb0, kb * BK, b_row);
               emit(A_TILE_BYTES + B_HALF_BYTES, mb1, kb * BK, b_row);
@@ -319,23 +353,92 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
+          // (PAIR: the even CTA's commit frees the stage on both SMs)
           if (!mbar_wait(&c.empty[s], ph ^ 1u)) {
             record_error(p.err, kErrWaitProducer);
             *abort_flag = 1;
             break;
           }
           uint8_t* st_base = tiles + s * STAGE_BYTES;
-          mbar_arrive_expect_tx(&c.full[s], STAGE_BYTES);
-          boxes(kb, [&](int off, const CUtensorMap* m, int x, int y) { tma_load_2d(st_base + off, m, &c.full[s], x, y); });
+          if (PAIR && crank == 1) {
+            // the odd CTA's half of the stage counts on the even CTA's
+            // barrier, which expects both halves
+            const uint32_t bar0 = mapa_shared(&c.full[s], 0);
+            boxes(kb, [&](int off, const CUtensorMap* m, int x, int y) {
+              tma_load_2d_to_peer_bar(st_base + off, m, bar0, x, y);
+            });
+          } else {
+            mbar_arrive_expect_tx(&c.full[s], PAIR ? 2 * STAGE_BYTES : STAGE_BYTES);
+            boxes(kb, [&](int off, const CUtensorMap* m, int x, int y) { tma_load_2d(st_base + off, m, &c.full[s], x, y); });
+          }
         }
       }
-      if (*abort_flag) {
+      if (*abort_flag && PAIR && crank == 1) {
+        // the copies already issued count on the other CTA's barriers, which
+        // this CTA cannot wait on: give them a bounded grace period to land
+        spin_ns(100000);
+      } else if (*abort_flag) {
         // let the copies already issued land before the CTA goes away
         const uint32_t n = it < STAGES ? it : STAGES;
         for (uint32_t q = it - n; q < it; ++q) {
           if (!mbar_wait(&c.full[q % STAGES], (q / STAGES) & 1u)) record_error(p.err, kErrWaitDrain);
         }
       }
+    }
+  } else if (warp == 1 && PAIR) {
+    // ---------------- PAIR: MMA issuer (even CTA only) ----------------
+    // The even CTA waits until both CTAs' halves of a stage have landed (one
+    // barrier counts both), issues one M=256 x N=256 x K=16 MMA per K step
+    // over both, and commits with a multicast so that both CTAs see the
+    // stage freed and the accumulator full.
+    const uint32_t IDESC2 = idesc_bf16_f32(256, BN, 0, 0);
+    uint32_t it = 0, local = 0;
+    bool issued = false;
+    for (int tile = tile0; tile < total && crank == 0; tile += tstep, ++local) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const uint32_t acc = local % NACC;
+      const uint32_t aph = (local / NACC) & 1u;
+      // both CTAs' epilogues have drained this accumulator
+      bool ok = lane == 0 ? mbar_wait(&c.tmem_empty[acc], aph ^ 1u) : true;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) record_error(p.err, kErrWaitMma);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < nk_fixed; ++kb, ++it) {
+        const uint32_t s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1u;
+        bool okf = lane == 0 ? mbar_wait(&c.full[s], ph) : true;
+        okf = __shfl_sync(0xffffffffu, okf, 0);
+        if (!okf) {
+          if (lane == 0) record_error(p.err, kErrWaitMma);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(tiles + s * STAGE_BYTES);
+          const uint32_t b_base = a_base + A_TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16_pair(d_tmem, sw128_kmajor_desc(a_base + kk * 32), sw128_kmajor_desc(b_base + kk * 32),
+                             IDESC2, (kb | kk) != 0 ? 1u : 0u);
+          tc_commit_pair_mc(&c.empty[s], 0x3);
+        }
+        __syncwarp();
+        issued = true;
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit_pair_mc(&c.tmem_full[acc], 0x3);
+      __syncwarp();
+    }
+    if (*abort_flag && issued && crank == 0 && lane == 0) {
+      tc_commit_pair_mc(&c.drain, 0x1);
+      if (!mbar_wait(&c.drain, 0)) record_error(p.err, kErrWaitDrain);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (lane 0 issues; the warp clears Wgrad tails) ----------------
@@ -347,10 +450,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     const uint32_t IDESC = idesc_bf16_f32(128, n_mma, KIND == kKindWgrad ? 1 : 0, KIND == kKindFwd ? 0 : 1);
     uint32_t it = 0, local = 0;
     bool issued = false;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+    for (int tile = tile0; tile < total; tile += tstep, ++local) {
       // one read of the abort flag for the whole warp keeps its lanes together
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
+      const Tile t = tile_coords<KIND, TM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
       const int grows = KIND == kKindWgrad ? c.grp_row[t.g + 1] - c.grp_row[t.g] : 0;
       const int nk1 = KIND == kKindWgrad ? (grows + BK - 1) / BK : nk_fixed;
       const int nk = KIND == kKindWgrad && p.b_lo ? 2 * nk1 : nk1;
@@ -436,10 +539,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     const int quarter = warp & 3;          // TMEM lanes [32*quarter, 32*quarter+32)
     const int half = (warp - 2) >> 2;      // BM = 256: accumulator rows 128*half.. (columns 256*half..)
     uint32_t local = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+    for (int tile = tile0; tile < total; tile += tstep, ++local) {
       // tcgen05.ld is warp-collective: the warp decides to stop as one
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = tile_coords<KIND, BM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
+      const Tile t = tile_coords<KIND, TM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
       const bool xg = KIND == kKindFwd && t.g == G;  // the extra group
       const int grow = xg ? 0 : c.grp_row[t.g];
       const int gend = xg ? p.xrows : c.grp_row[t.g + 1];
@@ -447,6 +550,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
       void* const zsave_p = xg ? p.xzsave : p.zsave;
       const uint32_t acc = local % NACC;
       const uint32_t aph = (local / NACC) & 1u;
+      // (PAIR: the even CTA's commit arrives here on both SMs)
       if (!__all_sync(0xffffffffu, mbar_wait(&c.tmem_full[acc], aph))) {
         if (lane == 0) record_error(p.err, kErrWaitEpilogue);
         *abort_flag = 1;
@@ -481,7 +585,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         }
       } else {
         const long long row_end = xg ? static_cast<long long>(gend) : min(static_cast<long long>(gend), p.rows_alloc);
-        const int row = grow + t.m * BM + rt;
+        const int row = grow + t.m * TM + static_cast<int>(crank) * BM + rt;
         const bool valid = row < row_end;
         if (swiglu_fwd) {
           bf16* orow = static_cast<bf16*>(out_p) + static_cast<size_t>(row) * p.ldo;
@@ -615,19 +719,33 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         }
       }
       tc_fence_before();
-      mbar_arrive(&c.tmem_empty[acc]);
+      if constexpr (PAIR) {
+        // one arrival per warp, on the even CTA's barrier (it reuses the
+        // accumulator of both CTAs)
+        __syncwarp();
+        if (lane == 0) {
+          if (crank == 0) mbar_arrive(&c.tmem_empty[acc]);
+          else mbar_arrive_cluster(mapa_shared(&c.tmem_empty[acc], 0));
+        }
+      } else {
+        mbar_arrive(&c.tmem_empty[acc]);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // PAIR: neither CTA leaves (or frees its TMEM) while the other may still
+  // signal its barriers or the MMAs may still read its shared memory
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-template <int KIND, int BM_>
+template <int KIND, int BM_, bool PAIR>
 moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
                        const CUtensorMap& mXA, const CUtensorMap& mXB0, const CUtensorMap& mXB1, long long tiles_bound,
                        cudaStream_t stream) {
@@ -635,20 +753,53 @@ moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtenso
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return MOE_ERR_CUDA;
-  constexpr size_t smem = smem_bytes<BM_>();
+  constexpr size_t smem = smem_bytes<BM_, PAIR>();
+  constexpr int threads = TileCfg<BM_, PAIR>::THREADS;
+  auto kern = grouped_gemm_tc_kernel<KIND, BM_, PAIR>;
+  // pair launches: clusters of two CTAs; the kernel is persistent, so the
+  // grid is no larger than the clusters that can be resident at once
+  cudaLaunchAttribute cluster_attr[1];
+  cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
+  cluster_attr[0].val.clusterDim.x = 2;
+  cluster_attr[0].val.clusterDim.y = 1;
+  cluster_attr[0].val.clusterDim.z = 1;
   static DeviceOnce attr;
+  static int max_clusters[64] = {0};
   const moe_status sa = attr.run(dev, [&] {
-    return cudaFuncSetAttribute(grouped_gemm_tc_kernel<KIND, BM_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem)) == cudaSuccess
-               ? MOE_OK
-               : MOE_ERR_CUDA;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (PAIR) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(2, 1, 1);
+      q.blockDim = dim3(threads, 1, 1);
+      q.dynamicSmemBytes = smem;
+      q.attrs = cluster_attr;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
+      max_clusters[dev] = n;
+    }
+    return MOE_OK;
   });
   if (sa != MOE_OK) return sa;
   long long grid = tiles_bound;
-  if (grid > sms) grid = sms;
-  if (grid < 1) grid = 1;
-  grouped_gemm_tc_kernel<KIND, BM_>
-      <<<static_cast<unsigned>(grid), TileCfg<BM_>::THREADS, smem, stream>>>(mA, mB0, mB1, mXA, mXB0, mXB1, p);
+  if (PAIR) {
+    if (grid > max_clusters[dev]) grid = max_clusters[dev];
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * grid), 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = cluster_attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, mXA, mXB0, mXB1, p) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
+    kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(mA, mB0, mB1, mXA, mXB0, mXB1, p);
+  }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -659,16 +810,20 @@ moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtenso
 // ---------------------------------------------------------------------------
 namespace {
 
-// Tile height for a launch: 256 when the groups average at least 256 output
-// rows and the epilogue is plain, else 128.
+// Tile shape for a launch: 256-row single-CTA tiles for plain epilogues when
+// the groups average at least 256 output rows and such tiles still give every
+// SM one, else 128-row tiles; a forward launch asked for CTA pairs
+// (p.cta_pairs) runs 256-row tiles on pairs under the same rule, any epilogue.
 template <int KIND>
 moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows, const void* B0, const void* B1,
                            long long b_rows, long long avg_rows, const GemmExtra* extra, cudaStream_t stream) {
-  // BM = 256 feeds the tensor cores with 2/3 of the shared-memory traffic
-  // per MAC but has a single accumulator, so its epilogue does not overlap
-  // the next tile's MMAs: take it for the light (plain) epilogues only, and
-  // only when it still gives every SM a tile (a single-group launch such as
-  // the router's logits would otherwise leave most SMs idle).
+  // BM = 256 on one CTA feeds the tensor cores with 2/3 of the shared-memory
+  // traffic per MAC but has a single accumulator, so its epilogue does not
+  // overlap the next tile's MMAs: take it for the light (plain) epilogues
+  // only.  A CTA pair halves the B bytes staged per MAC and keeps two
+  // accumulators per CTA, so it serves every forward epilogue.  Either only
+  // when it still gives every SM a tile (a single-group launch such as the
+  // router's logits would otherwise leave most SMs idle).
   const long long n_tiles = (KIND == kKindFwd && p.mode == kModeSwiGLU) ? (p.N + 127) / 128 : (p.N + BN - 1) / BN;
   auto tiles_for = [&](int bm) -> long long {
     if (KIND == kKindWgrad) return static_cast<long long>(p.G) * ((p.M + bm - 1) / bm) * n_tiles;
@@ -677,15 +832,15 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
     if (KIND == kKindFwd && p.xrows > 0) tl += ((p.xrows + bm - 1) / bm) * n_tiles;
     return tl;
   };
-  bool tall = avg_rows >= 256 && p.mode == kModePlain;
-  if (tall) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    if (tiles_for(256) < device_sm_count(dev)) tall = false;
-  }
-  const int BMv = tall ? 256 : 128;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  const bool pair = KIND == kKindFwd && p.cta_pairs && avg_rows >= 256 && (p.mode == kModeSwiGLU || p.N >= BN) &&
+                    2 * tiles_for(256) >= sms;
+  const bool tall = !pair && avg_rows >= 256 && p.mode == kModePlain && tiles_for(256) >= sms;
+  const int BMv = tall ? 256 : 128;  // A rows a CTA stages per tile
   CUtensorMap mA, mB0, mB1, mXA, mXB0, mXB1;
-  const long long tiles = tiles_for(BMv);
+  const long long tiles = tiles_for(pair || tall ? 256 : 128);
   if (KIND == kKindFwd) {
     if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BMv)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mB0, B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
@@ -713,8 +868,11 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
     mXB0 = mB0;
     mXB1 = mB1;
   }
-  return tall ? launch_kind<KIND, 256>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream)
-              : launch_kind<KIND, 128>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream);
+  if constexpr (KIND == kKindFwd) {
+    if (pair) return launch_kind<KIND, 128, true>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream);
+  }
+  return tall ? launch_kind<KIND, 256, false>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream)
+              : launch_kind<KIND, 128, false>(p, mA, mB0, mB1, mXA, mXB0, mXB1, tiles, stream);
 }
 
 }  // namespace

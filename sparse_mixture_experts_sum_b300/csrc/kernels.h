@@ -77,6 +77,7 @@ struct GemmParams {
   void* hout_lo;         // *Bwd modes: the bf16 residual s * act(z) - hout ([rows, N]), nullable
   int b_lo;              // Wgrad: out_g = A_g^T . (B0_g + B1_g) -- the contraction runs over the
                          // group's rows twice, with B0 then with B1 (a hi/lo pair)
+  int cta_pairs;         // Fwd: 256-row tiles on CTA pairs where the groups average >= 256 rows
   const void* bias;      // [G, N] nullable (GeLU / plain)
   int* err;              // workspace error word
   // Fwd only: one more group with its own operands (the shared expert):
@@ -133,6 +134,18 @@ constexpr size_t kStaticDispatchScratchBytes = 256u * 1025u * 4u + 256u * 1024u 
 // Device address of that scratch on the current device (looked up on the
 // first call per device); MOE_ERR_UNSUPPORTED if `need` bytes do not fit.
 moe_status static_dispatch_scratch(size_t need, void** ptr);
+
+// Expert parallelism: per-(slot, expert) routed counts [k, E] (zeroed here);
+// the dispatch of one rank's slots with global ranks (adj) and send-buffer
+// rows (send), both [k, E], and the global capacity C (slot-major priority;
+// scratch >= dispatch_ep_scratch_bytes); and a row permutation (scatter:
+// dst[map[i]] = src[i]; gather: dst[i] = src[map[i]]; map[i] < 0 skips).
+moe_status launch_slot_counts(const moe_config& cfg, const int* idx, int* counts, cudaStream_t stream);
+size_t dispatch_ep_scratch_bytes(const moe_config& cfg);
+moe_status launch_dispatch_ep(const moe_config& cfg, const int* idx, const void* x, const int* adj, const int* send,
+                              int C, int* pos, void* Xsend, void* scratch, cudaStream_t stream);
+moe_status launch_permute_rows(const void* src, const int* map, long long n, long long row_bytes, int scatter,
+                               void* dst, cudaStream_t stream);
 
 // Combine / un-permute.
 moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos, const float* w,

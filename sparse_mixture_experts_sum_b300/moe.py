@@ -28,7 +28,7 @@ class MoeConfig(ctypes.Structure):
                 ("k", ctypes.c_int), ("act", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int),
                 ("lambda_balance", ctypes.c_float), ("has_shared", ctypes.c_int), ("route_flags", ctypes.c_int),
-                ("balance", ctypes.c_int), ("balance_gamma", ctypes.c_float)]
+                ("balance", ctypes.c_int), ("balance_gamma", ctypes.c_float), ("gemm_flags", ctypes.c_int)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -58,6 +58,7 @@ class MoeStats(ctypes.Structure):
 
 
 EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_static",
+           "moe_slot_counts", "moe_dispatch_ep", "moe_permute_rows",
            "moe_expert_ffn", "moe_expert_ffn_shared",
            "moe_combine", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error", "moe_status_string",
            "moe_selftest_wait_timeout")
@@ -81,6 +82,9 @@ def lib() -> ctypes.CDLL:
             "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_dispatch_static": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_slot_counts": [cfgp, vp, vp, vp],
+            "moe_dispatch_ep": [cfgp, vp, vp, vp, vp, i, vp, vp, vp, vp],
+            "moe_permute_rows": [vp, vp, ctypes.c_longlong, ctypes.c_longlong, i, vp, vp],
             "moe_expert_ffn": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "moe_expert_ffn_shared": [cfgp, vp, vp, ctypes.POINTER(MoeWeights), vp, vp, vp, vp, vp, vp, vp],
             "moe_combine": [cfgp, vp, vp, vp, vp, vp, vp],
@@ -121,16 +125,18 @@ def _stream(stream=None):
 
 
 ROUTE_RAW_PROBS, ROUTE_TOKEN_MAJOR, ROUTE_LAYERNORM, ROUTE_REROUTE = 1, 2, 4, 8
+GEMM_CTA_PAIRS = 1
 BALANCE = {"cv": 0, "std_max": 1, "switch": 2}
 
 
 def make_config(T, d, h, E, k, act="swiglu", dtype="bf16", capacity_factor=0.0, min_capacity=0,
                 lambda_balance=0.01, has_shared=False, raw_probs=False, token_major=False,
-                layernorm=False, balance="cv", balance_gamma=100.0, reroute=False) -> MoeConfig:
+                layernorm=False, balance="cv", balance_gamma=100.0, reroute=False, cta_pairs=False) -> MoeConfig:
     flags = ((ROUTE_RAW_PROBS if raw_probs else 0) | (ROUTE_TOKEN_MAJOR if token_major else 0)
              | (ROUTE_LAYERNORM if layernorm else 0) | (ROUTE_REROUTE if reroute else 0))
     return MoeConfig(T, d, h, E, k, ACT[act], DTYPE[dtype], capacity_factor, min_capacity,
-                     lambda_balance, int(bool(has_shared)), flags, BALANCE[balance], balance_gamma)
+                     lambda_balance, int(bool(has_shared)), flags, BALANCE[balance], balance_gamma,
+                     GEMM_CTA_PAIRS if cta_pairs else 0)
 
 
 def config_of(wl, **route) -> MoeConfig:
@@ -181,6 +187,24 @@ def moe_dispatch_static(cfg, idx, x, kept, offsets, pos, Xp, stats, stream=None)
     _check("moe_dispatch_static", lib().moe_dispatch_static(ctypes.byref(cfg), _p(idx), _p(x), _p(kept),
                                                             _p(offsets), _p(pos), _p(Xp), _p(stats),
                                                             _stream(stream)))
+
+
+def moe_slot_counts(cfg, idx, counts, stream=None):
+    _check("moe_slot_counts", lib().moe_slot_counts(ctypes.byref(cfg), _p(idx), _p(counts), _stream(stream)))
+
+
+def moe_dispatch_ep(cfg, idx, x, rank_adjust, send_adjust, capacity, pos, Xsend, ws, stream=None):
+    _check("moe_dispatch_ep", lib().moe_dispatch_ep(ctypes.byref(cfg), _p(idx), _p(x), _p(rank_adjust),
+                                                    _p(send_adjust), int(capacity), _p(pos), _p(Xsend), _p(ws),
+                                                    _stream(stream)))
+
+
+def moe_permute_rows(src, index, n, scatter, dst, stream=None):
+    """Rows of src/dst (2-D tensors with the same row size): scatter
+    dst[index[i]] = src[i], or gather dst[i] = src[index[i]], i < n."""
+    row_bytes = src.stride(0) * src.element_size()
+    _check("moe_permute_rows", lib().moe_permute_rows(_p(src), _p(index), int(n), int(row_bytes),
+                                                      1 if scatter else 0, _p(dst), _stream(stream)))
 
 
 def moe_expert_ffn(cfg, Xp, offsets, W1, W3, b1, W2, b2, H, Yp, ws, stream=None):

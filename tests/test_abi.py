@@ -54,6 +54,7 @@ int main(void) {
          offsetof(moe_stats, balance_stat), offsetof(moe_weights, expert_bias));
   printf("%zu %zu %zu %zu\n", offsetof(moe_config, route_flags), offsetof(moe_stats, router_entropy),
          offsetof(moe_saved, Zs), sizeof(moe_grads));
+  printf("%zu\n", offsetof(moe_config, gemm_flags));
   printf("%zu %zu %zu\n", offsetof(moe_config, balance), offsetof(moe_config, balance_gamma),
          offsetof(moe_stats, rerouted_slots));
   return 0;
@@ -69,7 +70,8 @@ int main(void) {
            ctypes.sizeof(m.MoeStats), m.MoeConfig.has_shared.offset, m.MoeStats.drop_rate.offset,
            m.MoeStats.balance_stat.offset, m.MoeWeights.expert_bias.offset,
            m.MoeConfig.route_flags.offset, m.MoeStats.router_entropy.offset, m.MoeSaved.Zs.offset,
-           ctypes.sizeof(m.MoeGrads), m.MoeConfig.balance.offset, m.MoeConfig.balance_gamma.offset,
+           ctypes.sizeof(m.MoeGrads), m.MoeConfig.gemm_flags.offset,
+           m.MoeConfig.balance.offset, m.MoeConfig.balance_gamma.offset,
            m.MoeStats.rerouted_slots.offset]
     assert [int(v) for v in out] == got
 

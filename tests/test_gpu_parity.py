@@ -208,6 +208,77 @@ def test_expert_ffn_ragged_tiles(act):
     assert (Hn[off[-1]:] == 7.0).all() and (Yn[off[-1]:] == 7.0).all()
 
 
+@pytest.mark.parametrize("act,shared", [("swiglu", False), ("gelu", False), ("swiglu", True)])
+def test_expert_ffn_pair_tiles(act, shared):
+    """With MOE_GEMM_CTA_PAIRS, groups averaging >= 256 rows run as 256-row
+    tiles on CTA pairs (one M=256 MMA over two SMs, each holding half of the
+    rows and half of B); the outputs are the same bits as the default tiles'.
+    Per-expert rows 0, 1, 255, 256, 257, 600, 37, 1000 put the pair's row
+    split and the group ends everywhere (empty group, one row, a tile one
+    row short, exact, one over, several tiles, a single short tile); d = h =
+    1024 keeps both GEMMs on pairs; with the shared expert, its T = 1300
+    rows ride in the same launches.  Every row matches the oracle's expert
+    FFN and rows past offsets[E] are never written."""
+    T, k, E, d, h = 1300, 2, 8, 1024, 1024
+    rows = [0, 1, 255, 256, 257, 600, 37, 1000]
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    cfg = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared, cta_pairs=True)
+    cfg1 = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared)
+    g = torch.Generator().manual_seed(15)
+    bf = torch.bfloat16
+    # input projections at std 0.5/sqrt(d) keep the hidden values O(1), where
+    # the bf16 bound max-abs 2e-2 applies (over 1e5 values per expert at unit
+    # std, |H| reaches ~10 and one bf16 half-ulp alone is 3e-2 there)
+    s1 = 0.5 / d ** 0.5
+    W = dict(W1=(torch.randn(E, h, d, generator=g) * s1), W2=(torch.randn(E, d, h, generator=g) / h ** 0.5),
+             Ws1=(torch.randn(h, d, generator=g) * s1), Ws2=(torch.randn(d, h, generator=g) / h ** 0.5))
+    if act == "swiglu":
+        W["W3"] = torch.randn(E, h, d, generator=g) * s1
+        W["Ws3"] = torch.randn(h, d, generator=g) * s1
+    else:
+        W.update(b1=torch.randn(E, h, generator=g) * 0.2, b2=torch.randn(E, d, generator=g) * 0.2,
+                 bs1=torch.randn(h, generator=g) * 0.2, bs2=torch.randn(d, generator=g) * 0.2)
+    W = {n: v.to(bf).to(DEV) for n, v in W.items()}
+    x = torch.randn(T, d, generator=g).to(bf).to(DEV)
+    Xp = torch.randn(T * k, d, generator=g).to(bf).to(DEV)
+    H = torch.full((T * k, h), 7.0, dtype=bf, device=DEV)
+    Yp = torch.full((T * k, d), 7.0, dtype=bf, device=DEV)
+    offs = torch.as_tensor(off, device=DEV)
+    ws = M.moe.workspace(cfg, 1)
+
+    def run(c, H, Yp, Hs=None, Sx=None):
+        if shared:
+            M.moe.moe_expert_ffn_shared(c, Xp, offs, W, H, Yp, x, Hs, Sx, ws)
+        else:
+            M.moe_expert_ffn(c, Xp, offs, W["W1"], W.get("W3"), W.get("b1"), W["W2"], W.get("b2"), H, Yp, ws)
+        assert M.moe_check_error(ws) == 0
+
+    Hs = torch.empty(T, h, dtype=bf, device=DEV) if shared else None
+    Sx = torch.empty(T, d, dtype=bf, device=DEV) if shared else None
+    run(cfg, H, Yp, Hs, Sx)
+    # the default tiles give the same bits
+    H1, Y1 = torch.full_like(H, 7.0), torch.full_like(Yp, 7.0)
+    Sx1 = torch.empty_like(Sx) if shared else None
+    run(cfg1, H1, Y1, torch.empty_like(Hs) if shared else None, Sx1)
+    assert torch.equal(H1, H) and torch.equal(Y1, Yp) and (not shared or torch.equal(Sx1, Sx))
+    Wn = {n: to_np(v) for n, v in W.items()}
+    Xn, Hn, Yn = to_np(Xp), to_np(H), to_np(Yp)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b == a:
+            continue
+        p = O.expert_params(Wn, e, act)
+        if act == "swiglu":
+            Href = O.silu(Xn[a:b] @ p["W1"].T) * (Xn[a:b] @ p["W3"].T)
+        else:
+            Href = O.gelu(Xn[a:b] @ p["W1"].T + p["b1"])
+        assert_close_bf16(Hn[a:b], Href, f"H expert {e}")
+        assert_close_bf16(Yn[a:b], O.expert_ffn(Xn[a:b], act, **p), f"Yp expert {e}")
+    assert (Hn[off[-1]:] == 7.0).all() and (Yn[off[-1]:] == 7.0).all()
+    if shared:
+        assert_close_bf16(to_np(Sx), O.expert_ffn(to_np(x), act, **O.shared_params(Wn, act)), "Sx (shared expert)")
+
+
 def test_combine_worked_example_on_gpu():
     """[P5] worked example: 0.75*[0.8,0.2,-0.4] + 0.25*[0.4,0.6,0.8] = [0.7,0.3,-0.1]."""
     cfg = M.make_config(1, 4, 8, 4, 2, "gelu", "f32")
