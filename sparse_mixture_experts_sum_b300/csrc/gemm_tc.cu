@@ -302,6 +302,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         // Wgrad: k-blocks of the group's rows (twice over with a hi/lo B pair)
         const int nk1 = KIND == kKindWgrad ? (c.grp_row[t.g + 1] - grow + BK - 1) / BK : nk_fixed;
         const int nk = KIND == kKindWgrad && p.b_lo ? 2 * nk1 : nk1;
+        // a 256-row tile holding at most 128 of its group's rows stages and
+        // multiplies only its first half
+        const int gend_p = xg ? p.xrows : c.grp_row[t.g + 1];
+        const bool half_tile = KIND != kKindWgrad && !PAIR && BM == 256 && gend_p - (grow + t.m * TM) <= 128;
         // every box of k-block kb, handed to emit(dst offset in the stage, map, x, y)
         auto boxes = [&](int kb, auto&& emit) {
           if (KIND == kKindFwd) {
@@ -309,8 +313,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             const CUtensorMap* mb0 = xg ? &mapXB0 : &mapB0;
             const CUtensorMap* mb1 = xg ? &mapXB1 : &mapB1;
             const int g_row = xg ? 0 : t.g * p.N;
-            // this CTA's 128 rows of the tile (PAIR: the odd CTA the upper half)
-            emit(0, ma, kb * BK, grow + t.m * TM + static_cast<int>(crank) * BM);
+            // this CTA's rows of the tile, 128-row boxes (PAIR: the odd CTA
+            // stages the upper half; BM = 256: two boxes, one for a half tile)
+            const int a_row = grow + t.m * TM + static_cast<int>(crank) * (PAIR ? BM : 0);
+            emit(0, ma, kb * BK, a_row);
+            if (BM == 256 && !half_tile) emit(16384, ma, kb * BK, a_row + 128);
             if constexpr (PAIR) {
               // this CTA's half of the 256 B rows: SwiGLU W1 (even) or W3
               // (odd) rows of the tile's 128 hidden units; plain rows
@@ -330,6 +337,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             }
           } else if (KIND == kKindDgrad) {
             emit(0, &mapA, kb * BK, grow + t.m * BM);
+            if (BM == 256 && !half_tile) emit(16384, &mapA, kb * BK, grow + t.m * BM + 128);
             int k0 = kb * BK;
             const CUtensorMap* mb = &mapB0;
             const int kb_rows = p.k_split ? p.k_split : p.K;
@@ -368,7 +376,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
               tma_load_2d_to_peer_bar(st_base + off, m, bar0, x, y);
             });
           } else {
-            mbar_arrive_expect_tx(&c.full[s], PAIR ? 2 * STAGE_BYTES : STAGE_BYTES);
+            mbar_arrive_expect_tx(&c.full[s], PAIR ? 2 * STAGE_BYTES : STAGE_BYTES - (half_tile ? 16384 : 0));
             boxes(kb, [&](int off, const CUtensorMap* m, int x, int y) { tma_load_2d(st_base + off, m, &c.full[s], x, y); });
           }
         }
@@ -457,6 +465,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
       const int grows = KIND == kKindWgrad ? c.grp_row[t.g + 1] - c.grp_row[t.g] : 0;
       const int nk1 = KIND == kKindWgrad ? (grows + BK - 1) / BK : nk_fixed;
       const int nk = KIND == kKindWgrad && p.b_lo ? 2 * nk1 : nk1;
+      int n_half = BM / 128;  // M=128 MMAs per K step
+      if (KIND != kKindWgrad && BM == 256) {
+        const bool xt = KIND == kKindFwd && t.g == G;
+        const int g0 = xt ? 0 : c.grp_row[t.g], g1 = xt ? p.xrows : c.grp_row[t.g + 1];
+        if (g1 - (g0 + t.m * TM) <= 128) n_half = 1;
+      }
       const uint32_t acc = local % NACC;
       const uint32_t aph = (local / NACC) & 1u;
       bool ok = lane == 0 ? mbar_wait(&c.tmem_empty[acc], aph ^ 1u) : true;
@@ -516,6 +530,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             // 128 B K-major, or two 64-wide MN blocks)
 #pragma unroll
             for (int hh = 0; hh < BM / 128; ++hh) {
+              if (hh >= n_half) break;
               const uint64_t ad = KIND == kKindWgrad ? sw128_mnmajor_desc(a_k + hh * 16384)
                                                      : sw128_kmajor_desc(a_k + hh * 16384);
               tc_mma_bf16(d_tmem + hh * BN, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
@@ -559,6 +574,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
       tc_fence_after();
       const int rt = half * 128 + quarter * 32 + lane;  // tile row of this thread
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + (acc + half) * BN;
+      // the upper half of a half tile holds no rows and was not multiplied
+      const bool idle_half = KIND != kKindWgrad && BM == 256 && half == 1 && gend - (grow + t.m * TM) <= 128;
 
       if (KIND == kKindWgrad) {
         // out_g[m, n] fp32; a group with no rows has a zero gradient
@@ -583,7 +600,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
           for (int i = 0; i < 32; ++i) v[i] = empty ? 0.f : __uint_as_float(r[i]);
           if (valid) store_f32x32(orow, t.n * BN + cc * 32, p.N, v);
         }
-      } else {
+      } else if (!idle_half) {
         const long long row_end = xg ? static_cast<long long>(gend) : min(static_cast<long long>(gend), p.rows_alloc);
         const int row = grow + t.m * TM + static_cast<int>(crank) * BM + rt;
         const bool valid = row < row_end;
@@ -838,15 +855,14 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
   const bool pair = KIND == kKindFwd && p.cta_pairs && avg_rows >= 256 && (p.mode == kModeSwiGLU || p.N >= BN) &&
                     2 * tiles_for(256) >= sms;
   const bool tall = !pair && avg_rows >= 256 && p.mode == kModePlain && tiles_for(256) >= sms;
-  const int BMv = tall ? 256 : 128;  // A rows a CTA stages per tile
-  CUtensorMap mA, mB0, mB1, mXA, mXB0, mXB1;
+  CUtensorMap mA, mB0, mB1, mXA, mXB0, mXB1;  // Fwd/Dgrad A boxes: 128 rows (two per 256-row tile)
   const long long tiles = tiles_for(pair || tall ? 256 : 128);
   if (KIND == kKindFwd) {
-    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BMv)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, 128)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mB0, B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.K, b_rows, BK, 128)) return MOE_ERR_CUDA;
   } else if (KIND == kKindDgrad) {
-    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, BMv)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mA, A, p.K, a_rows, BK, 128)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mB0, B0, p.N, b_rows, 64, BK)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mB1, B1 ? B1 : B0, p.N, b_rows, 64, BK)) return MOE_ERR_CUDA;
   } else {
@@ -860,7 +876,7 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
   }
   if (KIND == kKindFwd && p.xrows > 0) {
     const long long n_rows = p.N;  // rows of the extra group's weights [N, K]
-    if (!make_tma_2d_bf16(&mXA, extra->A, p.K, p.xrows, BK, BMv)) return MOE_ERR_CUDA;
+    if (!make_tma_2d_bf16(&mXA, extra->A, p.K, p.xrows, BK, 128)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mXB0, extra->B0, p.K, n_rows, BK, 128)) return MOE_ERR_CUDA;
     if (!make_tma_2d_bf16(&mXB1, extra->B1 ? extra->B1 : extra->B0, p.K, n_rows, BK, 128)) return MOE_ERR_CUDA;
   } else {
