@@ -49,8 +49,8 @@ WEIGHTS = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2"
 # rows, keyed by the sha256 of the kernel source it was taken on (the figure
 # is reported only while that source is unchanged)
 GEMM_TRAFFIC = {
-    # 1.5555 GB (GEMM-1 1.0229 GB + GEMM-2 0.5326 GB) x 32607 / 2048 kept rows
-    "bb608e81de0dd17e11ecd51f5282baeb05dc83adc7ba2adce8d66577890fbdc1": 24.77e9,
+    # 1.5741 GB (GEMM-1 1.0414 GB + GEMM-2 0.5326 GB) x 32607 / 2048 kept rows
+    "9efcd79313345f1161a9f87f496a9425ba69a5055688a7190586f6fd0bd00be9": 25.06e9,
 }
 
 
@@ -66,7 +66,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 100 ms while running, each
+    """nvidia-smi clock / throttle samples every 50 ms while running, each
     stamped with the host time, so a summary can cover one timed region."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -82,7 +82,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
