@@ -49,6 +49,7 @@ __global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __r
                                   const int* __restrict__ pos, const float* __restrict__ w, int T, int k,
                                   int vec_per_row, uint4* __restrict__ dYg, float* __restrict__ wp,
                                   float* __restrict__ dot) {
+  pdl_entry();
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -92,6 +93,7 @@ __global__ void bwd_gather_kernel(const uint4* __restrict__ dY, const uint4* __r
 // sums are exact, so the order of the atomics does not show).
 __global__ void importance_kernel(const int* __restrict__ idx, const float* __restrict__ w, long long nslots, int E,
                                   unsigned long long* __restrict__ imp) {
+  pdl_entry();
   extern __shared__ unsigned long long simp[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) simp[e] = 0ull;
   __syncthreads();
@@ -117,6 +119,7 @@ __global__ void importance_kernel(const int* __restrict__ idx, const float* __re
 __global__ void __launch_bounds__(1024) balance_coef_kernel(const unsigned long long* __restrict__ imp,
                                                             const int* __restrict__ counts, int E, int T, float lam,
                                                             int variant, float gamma, float* __restrict__ coef) {
+  pdl_entry();
   __shared__ double red[32];
   __shared__ unsigned long long rmax[32];
   __shared__ int rarg[32];
@@ -194,6 +197,7 @@ __global__ void __launch_bounds__(1024) balance_coef_kernel(const unsigned long 
 __global__ void __launch_bounds__(1024) balance_switch_stat_kernel(const unsigned long long* __restrict__ imp,
                                                                    const int* __restrict__ counts, int E, int T,
                                                                    float lam, moe_stats* __restrict__ stats) {
+  pdl_entry();
   __shared__ double red[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const double invT = 1.0 / static_cast<double>(T);
@@ -214,6 +218,7 @@ __global__ void __launch_bounds__(1024) balance_switch_stat_kernel(const unsigne
 __global__ void router_bwd_kernel(const int* __restrict__ idx, const float* __restrict__ w,
                                   const float* __restrict__ dot, const float* __restrict__ coef, int T, int k, int E,
                                   float* __restrict__ dl) {
+  pdl_entry();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float G[8], wt[8];
@@ -242,6 +247,7 @@ __global__ void router_bwd_kernel(const int* __restrict__ idx, const float* __re
 __global__ void ln_router_bwd_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr,
                                      const int* __restrict__ idx, int T, int d, int k, int E, float* __restrict__ dl,
                                      float* __restrict__ lnc) {
+  pdl_entry();
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -326,6 +332,7 @@ template <int NV>
 __global__ void router_bwd_raw_kernel(const float* __restrict__ logits, const int* __restrict__ idx,
                                       const float* __restrict__ w, const float* __restrict__ dot,
                                       const float* __restrict__ coef, int T, int k, int E, float* __restrict__ dlD) {
+  pdl_entry();
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -399,6 +406,7 @@ __global__ void __launch_bounds__(RW_WARPS * 32)
 router_wgrad_partial_kernel(const Tx* __restrict__ x, const int* __restrict__ idx, const float* __restrict__ dl,
                             int T, int d, int k, int E, const float* __restrict__ mu,
                             float* __restrict__ partial) {
+  pdl_entry();
   extern __shared__ float acc_s[];  // [RW_WARPS][RW_EXP][8][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* acc = acc_s + warp * (RW_EXP * 8 * 32);
@@ -499,6 +507,7 @@ router_wgrad_partial_kernel(const Tx* __restrict__ x, const int* __restrict__ id
 // dWr[e][c] = sum over chunks (ascending) of partial[chunk][e][c].
 __global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, int nchunks, long long Ed,
                                            float* __restrict__ dWr) {
+  pdl_entry();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= Ed) return;
   float s = 0.f;
@@ -516,6 +525,7 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
                               const float* __restrict__ dl, const Tw* __restrict__ Wr, int T, int k, int d, int E,
                               const Tw* __restrict__ x, const float* __restrict__ lnc, int accumulate,
                               float* __restrict__ dX) {
+  pdl_entry();
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -619,6 +629,7 @@ __global__ void bwd_dx_kernel(const float* __restrict__ dXp, const int* __restri
 // (ascending; scale nullable: 1).
 __global__ void group_colsum_kernel(const bf16* __restrict__ src, long long ld, const int* __restrict__ offsets,
                                     int rows, int N, const float* __restrict__ scale, float* __restrict__ out) {
+  pdl_entry();
   const int g = blockIdx.y;
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= N) return;
@@ -648,11 +659,14 @@ moe_status launch_bwd_gather(const moe_config& cfg, const void* dY, const void* 
   uint4* dyg = static_cast<uint4*>(dYg);
   const int nv = cfg.d / 8;
   if (cfg.k <= 2)
-    bwd_gather_kernel<2><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, nv, dyg, wp, dot);
+    launch_pdl(bwd_gather_kernel<2>, dim3(warp_grid(cfg.T)), dim3(256), 0, st, dy, yp, pos, w, cfg.T, cfg.k, nv, dyg,
+               wp, dot);
   else if (cfg.k <= 4)
-    bwd_gather_kernel<4><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, nv, dyg, wp, dot);
+    launch_pdl(bwd_gather_kernel<4>, dim3(warp_grid(cfg.T)), dim3(256), 0, st, dy, yp, pos, w, cfg.T, cfg.k, nv, dyg,
+               wp, dot);
   else
-    bwd_gather_kernel<8><<<warp_grid(cfg.T), 256, 0, st>>>(dy, yp, pos, w, cfg.T, cfg.k, nv, dyg, wp, dot);
+    launch_pdl(bwd_gather_kernel<8>, dim3(warp_grid(cfg.T)), dim3(256), 0, st, dy, yp, pos, w, cfg.T, cfg.k, nv, dyg,
+               wp, dot);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -662,15 +676,16 @@ moe_status launch_router_bwd(const moe_config& cfg, const void* x, const void* W
   const long long nslots = static_cast<long long>(cfg.T) * cfg.k;
   long long blocks = (nslots + 255) / 256;
   if (blocks > 1184) blocks = 1184;
-  importance_kernel<<<static_cast<unsigned>(blocks), 256, sizeof(unsigned long long) * cfg.E, st>>>(idx, w, nslots,
-                                                                                                    cfg.E, imp);
-  balance_coef_kernel<<<1, 1024, 0, st>>>(imp, counts, cfg.E, cfg.T, cfg.lambda_balance, cfg.balance,
-                                          cfg.balance_gamma, coef);
-  router_bwd_kernel<<<(cfg.T + 255) / 256, 256, 0, st>>>(idx, w, dot, coef, cfg.T, cfg.k, cfg.E, dl);
+  launch_pdl(importance_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), sizeof(unsigned long long) * cfg.E, st,
+             idx, w, nslots, cfg.E, imp);
+  launch_pdl(balance_coef_kernel, dim3(1), dim3(1024), 0, st, imp, counts, cfg.E, cfg.T, cfg.lambda_balance,
+             cfg.balance, cfg.balance_gamma, coef);
+  launch_pdl(router_bwd_kernel, dim3((cfg.T + 255) / 256), dim3(256), 0, st, idx, w, dot, coef, cfg.T, cfg.k, cfg.E,
+             dl);
   if (lnc) {
     if (cfg.dtype != MOE_BF16 || (cfg.d % 8)) return MOE_ERR_UNSUPPORTED;
-    ln_router_bwd_kernel<<<warp_grid(cfg.T), 256, 0, st>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(Wr),
-                                                           idx, cfg.T, cfg.d, cfg.k, cfg.E, dl, lnc);
+    launch_pdl(ln_router_bwd_kernel, dim3(warp_grid(cfg.T)), dim3(256), 0, st, static_cast<const bf16*>(x),
+               static_cast<const bf16*>(Wr), idx, cfg.T, cfg.d, cfg.k, cfg.E, dl, lnc);
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -679,8 +694,9 @@ moe_status launch_router_bwd_raw(const moe_config& cfg, const float* logits, con
                                  const float* dot, const float* coef, float* dlD, cudaStream_t st) {
   const int nv = (cfg.E + 31) / 32;
   const unsigned grid = warp_grid(cfg.T);
-#define MOE_RAWBWD(NVv) \
-  router_bwd_raw_kernel<NVv><<<grid, 256, 0, st>>>(logits, idx, w, dot, coef, cfg.T, cfg.k, cfg.E, dlD)
+#define MOE_RAWBWD(NVv)                                                                                          \
+  launch_pdl(router_bwd_raw_kernel<NVv>, dim3(grid), dim3(256), 0, st, logits, idx, w, dot, coef, cfg.T, cfg.k, \
+             cfg.E, dlD)
   if (nv <= 1) MOE_RAWBWD(1);
   else if (nv <= 2) MOE_RAWBWD(2);
   else if (nv <= 4) MOE_RAWBWD(4);
@@ -698,9 +714,10 @@ moe_status launch_balance_stat_switch(const moe_config& cfg, const int* idx, con
   const long long nslots = static_cast<long long>(cfg.T) * cfg.k;
   long long blocks = (nslots + 255) / 256;
   if (blocks > 1184) blocks = 1184;
-  importance_kernel<<<static_cast<unsigned>(blocks), 256, sizeof(unsigned long long) * cfg.E, st>>>(idx, w, nslots,
-                                                                                                    cfg.E, imp);
-  balance_switch_stat_kernel<<<1, 1024, 0, st>>>(imp, counts, cfg.E, cfg.T, cfg.lambda_balance, stats);
+  launch_pdl(importance_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), sizeof(unsigned long long) * cfg.E, st,
+             idx, w, nslots, cfg.E, imp);
+  launch_pdl(balance_switch_stat_kernel, dim3(1), dim3(1024), 0, st, imp, counts, cfg.E, cfg.T, cfg.lambda_balance,
+             stats);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -725,18 +742,19 @@ moe_status launch_router_wgrad(const moe_config& cfg, const void* x, const int* 
   // raw softmax weights: dl is the dense [T, E] logit gradient
   const bool dense = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) != 0;
   if (cfg.dtype == MOE_BF16 && dense)
-    router_wgrad_partial_kernel<bf16, true><<<grid, RW_WARPS * 32, smem, st>>>(
-        static_cast<const bf16*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
+    launch_pdl(router_wgrad_partial_kernel<bf16, true>, dim3(grid), dim3(RW_WARPS * 32), smem, st,
+               static_cast<const bf16*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
   else if (cfg.dtype == MOE_BF16)
-    router_wgrad_partial_kernel<bf16, false><<<grid, RW_WARPS * 32, smem, st>>>(
-        static_cast<const bf16*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
+    launch_pdl(router_wgrad_partial_kernel<bf16, false>, dim3(grid), dim3(RW_WARPS * 32), smem, st,
+               static_cast<const bf16*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
   else if (!dense)
-    router_wgrad_partial_kernel<float, false><<<grid, RW_WARPS * 32, smem, st>>>(
-        static_cast<const float*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
+    launch_pdl(router_wgrad_partial_kernel<float, false>, dim3(grid), dim3(RW_WARPS * 32), smem, st,
+               static_cast<const float*>(x), idx, dl, cfg.T, cfg.d, cfg.k, cfg.E, lnc, partial);
   else
     return MOE_ERR_UNSUPPORTED;
   const long long Ed = static_cast<long long>(cfg.E) * cfg.d;
-  router_wgrad_reduce_kernel<<<static_cast<unsigned>((Ed + 255) / 256), 256, 0, st>>>(partial, nchunks, Ed, dWr);
+  launch_pdl(router_wgrad_reduce_kernel, dim3(static_cast<unsigned>((Ed + 255) / 256)), dim3(256), 0, st, partial,
+             nchunks, Ed, dWr);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -747,14 +765,14 @@ void launch_bwd_dx_t(const moe_config& cfg, const float* dXp, const int* pos, co
   const Tw* xx = static_cast<const Tw*>(x);
   const bool dense = (cfg.route_flags & MOE_ROUTE_RAW_PROBS) != 0;
   if (dense)
-    bwd_dx_kernel<Tw, KM, false, true><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k, cfg.d,
-                                                                         cfg.E, xx, lnc, accumulate, dX);
+    launch_pdl(bwd_dx_kernel<Tw, KM, false, true>, dim3(warp_grid(cfg.T)), dim3(256), 0, st, dXp, pos, idx, dl, w,
+               cfg.T, cfg.k, cfg.d, cfg.E, xx, lnc, accumulate, dX);
   else if (lnc)
-    bwd_dx_kernel<Tw, KM, true, false><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k, cfg.d,
-                                                                         cfg.E, xx, lnc, accumulate, dX);
+    launch_pdl(bwd_dx_kernel<Tw, KM, true, false>, dim3(warp_grid(cfg.T)), dim3(256), 0, st, dXp, pos, idx, dl, w,
+               cfg.T, cfg.k, cfg.d, cfg.E, xx, lnc, accumulate, dX);
   else
-    bwd_dx_kernel<Tw, KM, false, false><<<warp_grid(cfg.T), 256, 0, st>>>(dXp, pos, idx, dl, w, cfg.T, cfg.k,
-                                                                          cfg.d, cfg.E, xx, lnc, accumulate, dX);
+    launch_pdl(bwd_dx_kernel<Tw, KM, false, false>, dim3(warp_grid(cfg.T)), dim3(256), 0, st, dXp, pos, idx, dl, w,
+               cfg.T, cfg.k, cfg.d, cfg.E, xx, lnc, accumulate, dX);
 }
 
 template <typename Tw>
@@ -780,7 +798,8 @@ moe_status launch_bwd_dx(const moe_config& cfg, const float* dXp, const int* pos
 moe_status launch_group_colsum(const void* src, long long ld, const int* offsets, int G, int rows, int N,
                                const float* scale, float* out, cudaStream_t st) {
   dim3 grid((N + 255) / 256, G);
-  group_colsum_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(src), ld, offsets, rows, N, scale, out);
+  launch_pdl(group_colsum_kernel, dim3(grid), dim3(256), 0, st, static_cast<const bf16*>(src), ld, offsets, rows, N,
+             scale, out);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -60,6 +60,28 @@ __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f,
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch (kernels launched by launch_pdl)
+// ---------------------------------------------------------------------------
+// Lets the next kernel in the stream be scheduled now; it still waits for
+// this one in its own pdl_wait().
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Returns once the preceding kernel in the stream has completed and its
+// memory operations are visible (at once for a kernel launched without
+// programmatic serialization).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The first statement of every kernel but the GEMM: before any global
+// memory access and before any thread can return.  A grid of at most one
+// CTA per SM runs in one wave, so it lets the next kernel be scheduled at
+// once; a larger grid does not (the next kernel's CTAs would take SM room
+// from its later waves while they wait) and triggers as its CTAs exit.
+__device__ __forceinline__ void pdl_entry() {
+  uint32_t nsm;
+  asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+  if (static_cast<unsigned long long>(gridDim.x) * gridDim.y * gridDim.z <= nsm) pdl_trigger();
+  pdl_wait();
+}
+
+// ---------------------------------------------------------------------------
 // shared-memory addresses, mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

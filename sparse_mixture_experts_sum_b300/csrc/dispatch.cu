@@ -81,6 +81,7 @@ __device__ __forceinline__ int pass_expert(const SlotSrc& S, int T, int k, bool 
 
 __global__ void __launch_bounds__(DT) slot_hist_kernel(SlotSrc S, int T, int k, int E, bool token_major, int CH,
                                                        int* __restrict__ blockhist) {
+  pdl_entry();
   extern __shared__ int hist[];  // E + 1 (last: unrouted)
   for (int e = threadIdx.x; e <= E; e += DT) hist[e] = 0;
   __syncthreads();
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
                                                              float gamma, const int* __restrict__ used,
                                                              int* __restrict__ base, int* __restrict__ kept,
                                                              int* __restrict__ offsets, moe_stats* stats) {
+  pdl_entry();
   __shared__ int tot[1024];
   __shared__ int warp_sums[32];
   __shared__ int unrouted;
@@ -275,7 +277,8 @@ struct EpMap {
 __global__ void __launch_bounds__(DT) assign_kernel(SlotSrc S, int T, int k, int E, bool token_major, int CH,
                                                     const int* __restrict__ base, const int* __restrict__ kept,
                                                     const int* __restrict__ offsets, const int* __restrict__ used,
-                                                    int* __restrict__ pos, EpMap ep = EpMap{nullptr, nullptr, 0}) {
+                                                    int* __restrict__ pos, EpMap ep) {
+  pdl_entry();
   extern __shared__ int sm[];
   int* runcnt = sm;       // [E]
   int* warpcnt = sm + E;  // [DW][E]
@@ -341,6 +344,7 @@ __global__ void __launch_bounds__(DT) assign_kernel(SlotSrc S, int T, int k, int
 template <typename V>
 __global__ void permute_kernel(const V* __restrict__ x, int T, int k, int vec_per_row, int chunks,
                                const int* __restrict__ pos, V* __restrict__ Xp) {
+  pdl_entry();
   const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int t = static_cast<int>(wid / chunks);
   const int ch = static_cast<int>(wid - static_cast<long long>(t) * chunks);
@@ -366,6 +370,7 @@ template <int KM>  // slots per token rounded up to 2, 4 or 8 (register arrays)
 __global__ void combine_bf16_kernel(const uint4* __restrict__ Yp, const int* __restrict__ pos,
                                     const float* __restrict__ w, const uint4* __restrict__ Sx, int T, int k,
                                     int vec_per_row, int chunks, uint4* __restrict__ y) {
+  pdl_entry();
   const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int t = static_cast<int>(wid / chunks);
   const int ch = static_cast<int>(wid - static_cast<long long>(t) * chunks);
@@ -417,6 +422,7 @@ __global__ void combine_bf16_kernel(const uint4* __restrict__ Yp, const int* __r
 __global__ void combine_f32_kernel(const float* __restrict__ Yp, const int* __restrict__ pos,
                                    const float* __restrict__ w, const float* __restrict__ Sx, int T, int k, int d,
                                    float* __restrict__ y) {
+  pdl_entry();
   const int t = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -436,6 +442,7 @@ __global__ void combine_f32_kernel(const float* __restrict__ Yp, const int* __re
 // reduce in a fixed order (NaN when no token is finite).
 __global__ void __launch_bounds__(1024) entropy_mean_kernel(const float* __restrict__ ent, int T,
                                                             moe_stats* stats) {
+  pdl_entry();
   __shared__ double rs[32];
   __shared__ int rc[32];
   double s = 0.0;
@@ -474,6 +481,7 @@ __global__ void __launch_bounds__(1024) entropy_mean_kernel(const float* __restr
 // histogram that expert-parallel ranks exchange.  Integer atomics, so the
 // result does not depend on their order.
 __global__ void slot_counts_kernel(const int* __restrict__ idx, int T, int k, int E, int* __restrict__ counts) {
+  pdl_entry();
   extern __shared__ int hc[];  // k * E
   for (int i = threadIdx.x; i < k * E; i += blockDim.x) hc[i] = 0;
   __syncthreads();
@@ -492,6 +500,7 @@ __global__ void slot_counts_kernel(const int* __restrict__ idx, int T, int k, in
 // (gather), rows of vec_per_row 16-byte vectors; map[i] < 0 skips row i.
 __global__ void permute_rows_kernel(const uint4* __restrict__ src, const int* __restrict__ map, long long n,
                                     int vec_per_row, int scatter, uint4* __restrict__ dst) {
+  pdl_entry();
   const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (i >= n) return;
@@ -547,28 +556,31 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
   const size_t asmem = static_cast<size_t>(cfg.E) * (DW + 1) * sizeof(int);
   const SlotSrc S1{idx, nullptr, nullptr};
   if (!reroute) {
-    slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(S1, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
-    capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance,
-                                                 cfg.balance, cfg.balance_gamma, nullptr, base, kept, offsets,
-                                                 stats);
-    assign_kernel<<<nb, DT, asmem, stream>>>(S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets, nullptr, pos);
+    launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S1, cfg.T, cfg.k, cfg.E, tm, CH,
+               blockhist);
+    launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept, offsets, stats);
+    launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets,
+               nullptr, pos, EpMap{nullptr, nullptr, 0});
   } else {
     // pass 1 keeps its ranks; pass 2 offers the dropped slots their backups
     // in the same priority order, then places every slot
     int* kept1 = reinterpret_cast<int*>(sp);
     sp += align_up(static_cast<size_t>(cfg.E) * sizeof(int), 256);
     int* rank1 = reinterpret_cast<int*>(sp);
-    slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(S1, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
-    capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance,
-                                                 cfg.balance, cfg.balance_gamma, nullptr, base, kept1, offsets,
-                                                 stats);
-    assign_kernel<<<nb, DT, asmem, stream>>>(S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept1, nullptr, nullptr,
-                                             rank1);
+    launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S1, cfg.T, cfg.k, cfg.E, tm, CH,
+               blockhist);
+    launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept1, offsets, stats);
+    launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept1, nullptr,
+               nullptr, rank1, EpMap{nullptr, nullptr, 0});
     const SlotSrc S2{idx, rank1, backup};
-    slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(S2, cfg.T, cfg.k, cfg.E, tm, CH, blockhist);
-    capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, C, cfg.lambda_balance,
-                                                 cfg.balance, cfg.balance_gamma, kept1, base, kept, offsets, stats);
-    assign_kernel<<<nb, DT, asmem, stream>>>(S2, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets, kept1, pos);
+    launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S2, cfg.T, cfg.k, cfg.E, tm, CH,
+               blockhist);
+    launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, kept1, base, kept, offsets, stats);
+    launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S2, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets,
+               kept1, pos, EpMap{nullptr, nullptr, 0});
   }
   if (Xp) {
     const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
@@ -576,14 +588,13 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
     if (row_bytes % 16 == 0) {
       const int vpr = static_cast<int>(row_bytes / 16);
       const int ch = row_chunks(cfg.T, vpr);
-      permute_kernel<uint4><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(static_cast<const uint4*>(x), cfg.T, cfg.k, vpr,
-                                                                      ch, pos, static_cast<uint4*>(Xp));
+      launch_pdl(permute_kernel<uint4>, dim3(warp_grid(cfg.T, ch)), dim3(256), 0, stream, static_cast<const uint4*>(x),
+                 cfg.T, cfg.k, vpr, ch, pos, static_cast<uint4*>(Xp));
     } else {
       const int vpr = static_cast<int>(row_bytes / 4);
       const int ch = row_chunks(cfg.T, vpr);
-      permute_kernel<uint32_t><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(static_cast<const uint32_t*>(x), cfg.T,
-                                                                         cfg.k, vpr, ch, pos,
-                                                                         static_cast<uint32_t*>(Xp));
+      launch_pdl(permute_kernel<uint32_t>, dim3(warp_grid(cfg.T, ch)), dim3(256), 0, stream,
+                 static_cast<const uint32_t*>(x), cfg.T, cfg.k, vpr, ch, pos, static_cast<uint32_t*>(Xp));
     }
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -617,8 +628,8 @@ moe_status launch_slot_counts(const moe_config& cfg, const int* idx, int* counts
   const long long n = static_cast<long long>(cfg.T) * cfg.k;
   long long blocks = (n + 255) / 256;
   if (blocks > 1184) blocks = 1184;
-  slot_counts_kernel<<<static_cast<unsigned>(blocks), 256, static_cast<size_t>(cfg.k) * cfg.E * sizeof(int),
-                       stream>>>(idx, cfg.T, cfg.k, cfg.E, counts);
+  launch_pdl(slot_counts_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256),
+             static_cast<size_t>(cfg.k) * cfg.E * sizeof(int), stream, idx, cfg.T, cfg.k, cfg.E, counts);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -639,20 +650,21 @@ moe_status launch_dispatch_ep(const moe_config& cfg, const int* idx, const void*
   const int CH = chunk_slots(static_cast<long long>(cfg.T) * cfg.k);
   const size_t asmem = static_cast<size_t>(cfg.E) * (DW + 1) * sizeof(int);
   const SlotSrc S1{idx, nullptr, nullptr};
-  slot_hist_kernel<<<nb, DT, (cfg.E + 1) * sizeof(int), stream>>>(S1, cfg.T, cfg.k, cfg.E, false, CH, blockhist);
+  launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S1, cfg.T, cfg.k, cfg.E, false,
+             CH, blockhist);
   // local slot-major ranks only: the capacity test is on the global rank
-  capacity_scan_kernel<<<1, 1024, 0, stream>>>(blockhist, nb, cfg.T, cfg.k, cfg.E, 0x7fffffff, 0.f, 0, 0.f,
-                                               nullptr, base, kept, offsets, nullptr);
-  assign_kernel<<<nb, DT, asmem, stream>>>(S1, cfg.T, cfg.k, cfg.E, false, CH, base, kept, offsets, nullptr, pos,
-                                           EpMap{adj, send, C});
+  launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, 0x7fffffff, 0.f,
+             0, 0.f, nullptr, base, kept, offsets, nullptr);
+  launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, false, CH, base, kept, offsets,
+             nullptr, pos, EpMap{adj, send, C});
   if (Xsend) {
     const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
     const long long row_bytes = static_cast<long long>(cfg.d) * es;
     if (row_bytes % 16) return MOE_ERR_UNSUPPORTED;
     const int vpr = static_cast<int>(row_bytes / 16);
     const int ch = row_chunks(cfg.T, vpr);
-    permute_kernel<uint4><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(static_cast<const uint4*>(x), cfg.T, cfg.k, vpr,
-                                                                    ch, pos, static_cast<uint4*>(Xsend));
+    launch_pdl(permute_kernel<uint4>, dim3(warp_grid(cfg.T, ch)), dim3(256), 0, stream, static_cast<const uint4*>(x),
+               cfg.T, cfg.k, vpr, ch, pos, static_cast<uint4*>(Xsend));
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -663,13 +675,14 @@ moe_status launch_permute_rows(const void* src, const int* map, long long n, lon
   if (row_bytes <= 0 || row_bytes % 16) return MOE_ERR_UNSUPPORTED;
   const long long blocks = (n * 32 + 255) / 256;
   if (blocks > 2147483647LL) return MOE_ERR_UNSUPPORTED;
-  permute_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const uint4*>(src), map, n, static_cast<int>(row_bytes / 16), scatter, static_cast<uint4*>(dst));
+  launch_pdl(permute_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+             static_cast<const uint4*>(src), map, n, static_cast<int>(row_bytes / 16), scatter,
+             static_cast<uint4*>(dst));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status launch_entropy_mean(const float* ent, int T, moe_stats* stats, cudaStream_t stream) {
-  entropy_mean_kernel<<<1, 1024, 0, stream>>>(ent, T, stats);
+  launch_pdl(entropy_mean_kernel, dim3(1), dim3(1024), 0, stream, ent, T, stats);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -681,15 +694,17 @@ moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos,
     const uint4* sx = static_cast<const uint4*>(Sx);
     uint4* yo = static_cast<uint4*>(y);
     if (cfg.k <= 2)
-      combine_bf16_kernel<2><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(yp, pos, w, sx, cfg.T, cfg.k, cfg.d / 8, ch, yo);
+      launch_pdl(combine_bf16_kernel<2>, dim3(warp_grid(cfg.T, ch)), dim3(256), 0, stream, yp, pos, w, sx, cfg.T, cfg.k,
+                 cfg.d / 8, ch, yo);
     else if (cfg.k <= 4)
-      combine_bf16_kernel<4><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(yp, pos, w, sx, cfg.T, cfg.k, cfg.d / 8, ch, yo);
+      launch_pdl(combine_bf16_kernel<4>, dim3(warp_grid(cfg.T, ch)), dim3(256), 0, stream, yp, pos, w, sx, cfg.T, cfg.k,
+                 cfg.d / 8, ch, yo);
     else
-      combine_bf16_kernel<8><<<warp_grid(cfg.T, ch), 256, 0, stream>>>(yp, pos, w, sx, cfg.T, cfg.k, cfg.d / 8, ch, yo);
+      launch_pdl(combine_bf16_kernel<8>, dim3(warp_grid(cfg.T, ch)), dim3(256), 0, stream, yp, pos, w, sx, cfg.T, cfg.k,
+                 cfg.d / 8, ch, yo);
   } else {
-    combine_f32_kernel<<<warp_grid(cfg.T), 256, 0, stream>>>(static_cast<const float*>(Yp), pos, w,
-                                                             static_cast<const float*>(Sx), cfg.T, cfg.k, cfg.d,
-                                                             static_cast<float*>(y));
+    launch_pdl(combine_f32_kernel, dim3(warp_grid(cfg.T)), dim3(256), 0, stream, static_cast<const float*>(Yp), pos, w,
+               static_cast<const float*>(Sx), cfg.T, cfg.k, cfg.d, static_cast<float*>(y));
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -14,6 +14,7 @@ namespace {
 
 __global__ void grouped_gemm_f32_kernel(const GemmParams p, const float* __restrict__ A,
                                         const float* __restrict__ B0, const float* __restrict__ B1) {
+  pdl_entry();
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   const int r = blockIdx.y;
   const int rows_total = p.offsets ? p.offsets[p.G] : p.rows;
@@ -54,9 +55,8 @@ moe_status launch_grouped_gemm_f32(const GemmParams& p_in, const void* A, long l
   if (rows > 2147483647LL) return MOE_ERR_UNSUPPORTED;
   dim3 block(128);
   dim3 grid((p.N + 127) / 128, static_cast<unsigned>(rows));
-  grouped_gemm_f32_kernel<<<grid, block, 0, stream>>>(p, static_cast<const float*>(A),
-                                                      static_cast<const float*>(B0),
-                                                      static_cast<const float*>(B1));
+  launch_pdl(grouped_gemm_f32_kernel, dim3(grid), dim3(block), 0, stream, p, static_cast<const float*>(A),
+             static_cast<const float*>(B0), static_cast<const float*>(B1));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

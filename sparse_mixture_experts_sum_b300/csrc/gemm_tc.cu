@@ -221,6 +221,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
   const int tstep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   // ---------------- set-up ----------------
+  // the barriers, TMEM and descriptor prefetches below touch no global
+  // memory, so they overlap the preceding kernel's tail; pdl_wait() comes
+  // before the first read
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&c.full[s], 1);
@@ -248,6 +251,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
       tmem_relinquish();
     }
   }
+  pdl_wait();
   if (warp == 2) {
     // per-group tile counts -> exclusive prefix (one warp, 32 groups a step)
     int carry = 0;
@@ -381,6 +385,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
           }
         }
       }
+      // every load of this CTA is issued: the next kernel in the stream may
+      // be scheduled (its CTAs wait in pdl_wait() until this grid completes)
+      pdl_trigger();
       if (*abort_flag && PAIR && crank == 1) {
         // the copies already issued count on the other CTA's barriers, which
         // this CTA cannot wait on: give them a bounded grace period to land
@@ -775,11 +782,14 @@ moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtenso
   auto kern = grouped_gemm_tc_kernel<KIND, BM_, PAIR>;
   // pair launches: clusters of two CTAs; the kernel is persistent, so the
   // grid is no larger than the clusters that can be resident at once
-  cudaLaunchAttribute cluster_attr[1];
+  cudaLaunchAttribute cluster_attr[2];
   cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
   cluster_attr[0].val.clusterDim.x = 2;
   cluster_attr[0].val.clusterDim.y = 1;
   cluster_attr[0].val.clusterDim.z = 1;
+  // programmatic stream serialization, as launch_pdl gives every other launch
+  cluster_attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  cluster_attr[1].val.programmaticStreamSerializationAllowed = 1;
   static DeviceOnce attr;
   static int max_clusters[64] = {0};
   const moe_status sa = attr.run(dev, [&] {
@@ -810,12 +820,13 @@ moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtenso
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = cluster_attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, mXA, mXB0, mXB1, p) != cudaSuccess) return MOE_ERR_CUDA;
   } else {
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
-    kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(mA, mB0, mB1, mXA, mXB0, mXB1, p);
+    launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, mA, mB0, mB1, mXA, mXB0, mXB1,
+               p);
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

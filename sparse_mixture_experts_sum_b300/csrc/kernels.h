@@ -33,6 +33,32 @@ class DeviceOnce {
   bool done_[kMaxDevices] = {};
 };
 
+// Launches kern<<<grid, block, smem, st>>>(args...) with programmatic
+// stream serialization: the kernel may be scheduled while its predecessor in
+// the stream is still running, once the predecessor's CTAs have all
+// triggered (pdl_trigger) or exited.  Every kernel of this library starts
+// with pdl_entry() (the GEMM: its shared-memory and TMEM set-up, then
+// pdl_wait()), so no thread reads or writes global memory before the
+// predecessor has completed and its writes are visible; since every kernel
+// waits so, a kernel also runs after all earlier ones in the stream.  What
+// overlaps is the launch and, in the GEMM, the set-up.  Launch errors are
+// also reported by cudaGetLastError().
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Epilogue of a grouped GEMM (acc = the fp32 accumulator of one output element).
 enum GemmMode : int {
   kModePlain = 0,      // out = acc (+ bias)

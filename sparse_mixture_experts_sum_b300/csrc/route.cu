@@ -189,6 +189,7 @@ __device__ __forceinline__ void row_stats_f32(const float* __restrict__ row, int
 
 // S[e] = sum_i Wr[e,i] (fp32), one warp per expert; S[e] = 0 for E <= e < ld.
 __global__ void weight_row_sum_kernel(const bf16* __restrict__ Wr, int E, int d, int ld, float* __restrict__ S) {
+  pdl_entry();
   const int e = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (e >= ld) return;
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(128)
 route_bf16_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wr, const float* __restrict__ ebias,
                   const float* __restrict__ noise, int T, int d, int E, int k, int* __restrict__ idx,
                   float* __restrict__ w, int* __restrict__ counts, int raw, float* __restrict__ ent) {
+  pdl_entry();
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const RouteLayout Lay(E, STAGES);
   const int nep = Lay.nep;
@@ -395,6 +397,7 @@ route_topk_kernel(const float* __restrict__ logits, int ld, const float* __restr
                   const float* __restrict__ noise, int T, int E, int k, int* __restrict__ idx, float* __restrict__ w,
                   int* __restrict__ counts, int raw, float* __restrict__ ent, const bf16* __restrict__ x, int d,
                   const float* __restrict__ S, int* __restrict__ backup, float* __restrict__ out_logits) {
+  pdl_entry();
   extern __shared__ int hist_s[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
   __syncthreads();
@@ -509,6 +512,7 @@ __global__ void route_f32_kernel(const float* __restrict__ x, const float* __res
                                  int E, int k, int* __restrict__ idx, float* __restrict__ w,
                                  int* __restrict__ counts, int raw, float* __restrict__ ent, int layernorm,
                                  int* __restrict__ backup) {
+  pdl_entry();
   const int kk = backup ? min(2 * k, E) : k;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -566,9 +570,9 @@ moe_status launch_route_stages(const moe_config& cfg, const void* x, const void*
   });
   if (sa != MOE_OK) return sa;
   dim3 grid((cfg.T + RT_TM - 1) / RT_TM, 1);
-  route_bf16_kernel<STAGES><<<grid, 128, Lay.total, stream>>>(
-      static_cast<const bf16*>(x), static_cast<const bf16*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E, cfg.k,
-      idx, w, counts, (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0, ent);
+  launch_pdl(route_bf16_kernel<STAGES>, dim3(grid), dim3(128), Lay.total, stream, static_cast<const bf16*>(x),
+             static_cast<const bf16*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E, cfg.k, idx, w, counts,
+             (cfg.route_flags & MOE_ROUTE_RAW_PROBS) ? 1 : 0, ent);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -605,8 +609,8 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     float* logits = static_cast<float*>(scratch);
     float* S = ln ? logits + static_cast<size_t>(cfg.T) * ld : nullptr;
     if (ln) {
-      weight_row_sum_kernel<<<static_cast<unsigned>((ld * 32 + 255) / 256), 256, 0, stream>>>(
-          static_cast<const bf16*>(Wr), cfg.E, cfg.d, ld, S);
+      launch_pdl(weight_row_sum_kernel, dim3(static_cast<unsigned>((ld * 32 + 255) / 256)), dim3(256), 0, stream,
+                 static_cast<const bf16*>(Wr), cfg.E, cfg.d, ld, S);
     }
     GemmParams g{};
     g.G = 1;
@@ -623,9 +627,9 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     const bf16* xb = static_cast<const bf16*>(x);
     const size_t hs = sizeof(int) * cfg.E;
     const int nv = (cfg.E + 31) / 32;
-#define MOE_TOPK(NVv)                                                                                        \
-  route_topk_kernel<NVv><<<grid, 256, hs, stream>>>(logits, ld, expert_bias, noise, cfg.T, cfg.E, cfg.k, idx, w, \
-                                                     counts, raw, ent, xb, cfg.d, S, backup, out_logits)
+#define MOE_TOPK(NVv)                                                                                          \
+  launch_pdl(route_topk_kernel<NVv>, dim3(grid), dim3(256), hs, stream, logits, ld, expert_bias, noise, cfg.T, \
+             cfg.E, cfg.k, idx, w, counts, raw, ent, xb, cfg.d, S, backup, out_logits)
     if (nv <= 1) MOE_TOPK(1);
     else if (nv <= 2) MOE_TOPK(2);
     else if (nv <= 4) MOE_TOPK(4);
@@ -640,9 +644,9 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
   } else {
     const int threads = 256;
     const long long grid = (static_cast<long long>(cfg.T) * 32 + threads - 1) / threads;
-    route_f32_kernel<<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-        static_cast<const float*>(x), static_cast<const float*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E,
-        cfg.k, idx, w, counts, raw, ent, ln ? 1 : 0, backup);
+    launch_pdl(route_f32_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, stream,
+               static_cast<const float*>(x), static_cast<const float*>(Wr), expert_bias, noise, cfg.T, cfg.d, cfg.E,
+               cfg.k, idx, w, counts, raw, ent, ln ? 1 : 0, backup);
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -46,6 +46,7 @@ namespace {
 // Zero two word ranges in one small launch (the error word and a counter
 // array, typically); a kernel on the compute stream rather than a memset.
 __global__ void zero_words_kernel(uint32_t* __restrict__ a, long long na, uint32_t* __restrict__ b, long long nb) {
+  pdl_entry();
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     if (i < na) a[i] = 0u;
@@ -60,8 +61,8 @@ moe_status launch_zero(void* a, size_t a_bytes, void* b, size_t b_bytes, cudaStr
   if (na + nb == 0) return MOE_OK;
   long long blocks = (na + nb + 255) / 256;
   if (blocks > 1024) blocks = 1024;
-  zero_words_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<uint32_t*>(a), na,
-                                                                        static_cast<uint32_t*>(b), nb);
+  launch_pdl(zero_words_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, static_cast<uint32_t*>(a),
+             na, static_cast<uint32_t*>(b), nb);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -83,6 +84,7 @@ int device_sm_count(int dev) {
 // kWaitLimitNs and records kErrSelfTest in the error word; the kernel then
 // returns normally, so the context stays usable.
 __global__ void selftest_wait_kernel(int* err) {
+  pdl_entry();
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x != 0) return;
   mbar_init(&bar, 1);
@@ -93,7 +95,7 @@ __global__ void selftest_wait_kernel(int* err) {
 moe_status launch_selftest_wait(int* err, cudaStream_t stream) {
   moe_status s = launch_zero(err, sizeof(int), nullptr, 0, stream);
   if (s != MOE_OK) return s;
-  selftest_wait_kernel<<<1, 32, 0, stream>>>(err);
+  launch_pdl(selftest_wait_kernel, dim3(1), dim3(32), 0, stream, err);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -263,6 +263,51 @@ def test_backward_is_deterministic():
         assert torch.equal(g1[name], g2[name]), name
 
 
+def test_back_to_back_steps_match_isolated_steps():
+    """Every launch lets the next kernel in the stream be scheduled before
+    the current one ends (programmatic dependent launch), and each kernel
+    waits for its predecessor before it touches memory.  Six training steps
+    (forward and backward) alternate between two inputs whose routings
+    differ, issued back to back on one stream with shared workspaces and no
+    host synchronisation.  Each step's output, saved routing and gradients
+    must be the same bits as the same step run on its own."""
+    wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, seed=67)
+    ta = guarded_inputs(wl, DEV)
+    tb = dict(ta)
+    other = guarded_inputs(wl.replace(seed=71), DEV)
+    for n in ("x", "noise", "dY"):
+        tb[n] = other[n]
+    dY = {0: ta.pop("dY"), 1: tb.pop("dY")}
+    inp = {0: ta, 1: tb}
+    ref = {i: run_fwd_bwd(wl, inp[i], dY[i]) for i in (0, 1)}
+    assert not torch.equal(ref[0][1]["idx"], ref[1][1]["idx"])
+    cfg = M.config_of(wl)
+    weights = {n: ta.get(n) for n in WEIGHT_NAMES}
+    ws, wsb, st = M.moe.workspace(cfg, 1), M.moe.workspace(cfg, 2), M.moe.stats_buffer()
+    outs = []
+    for i in range(6):
+        sv = M.moe.alloc_saved(cfg, DEV, backward=True)
+        y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=DEV)
+        g = M.moe.alloc_grads(cfg)
+        for v in g.values():
+            v.fill_(float("nan"))
+        outs.append((y, sv, g))
+    torch.cuda.synchronize()
+    for i, (y, sv, g) in enumerate(outs):
+        t = inp[i % 2]
+        M.moe_layer_fwd(cfg, weights, t["x"], t.get("noise"), y, sv, st, ws)
+        M.moe_layer_bwd(cfg, weights, t["x"], sv, dY[i % 2], g, wsb)
+    torch.cuda.synchronize()
+    assert M.moe_check_error(ws) == 0 and M.moe_check_error(wsb) == 0
+    for i, (y, sv, g) in enumerate(outs):
+        y0, sv0, g0 = ref[i % 2]
+        assert torch.equal(y, y0), i
+        for n in ("idx", "pos", "offsets"):
+            assert torch.equal(sv[n], sv0[n]), (i, n)
+        for n in g0:
+            assert torch.equal(g[n], g0[n]), (i, n)
+
+
 def test_balance_term_reaches_router_only():
     """lambda changes dWr and dX only (the balance term depends on the
     routing weights alone); expert gradients are the same bits."""

@@ -208,6 +208,70 @@ def test_expert_ffn_ragged_tiles(act):
     assert (Hn[off[-1]:] == 7.0).all() and (Yn[off[-1]:] == 7.0).all()
 
 
+@pytest.mark.parametrize("act,tall,shared", [("swiglu", False, False), ("gelu", False, True),
+                                              ("swiglu", True, True), ("gelu", True, False)])
+def test_expert_ffn_tile_tails(act, tall, shared):
+    """Ragged group ends on both tile heights.  128-row tiles (groups
+    averaging under 256 rows): groups of 0, 1, 15, 16, 17, 112, 113, 127,
+    128, 129, 240 and 300 rows.  256-row tiles (groups averaging >= 256 rows,
+    enough tiles for every SM): last tiles of 1, 37, 88, 112, 113, 128 (half
+    tiles), 129, 188, 232, 240 and 241 rows.  The shared expert's T = 1300
+    rows end in a 20-row tile.  GeLU runs with biases.  Every row matches the
+    oracle's expert FFN, and rows past offsets[E] are never written."""
+    if tall:
+        # 256-row tiles need T k / E >= 256 and, per GEMM, at least one tile per SM
+        T, k, d, h = 2000, 2, 2048, 1536
+        rows = [1000, 37, 600, 257, 1, 700, 128, 112, 113, 240, 241, 496]
+    else:
+        T, k, d, h = 1300, 2, 256, 384
+        rows = [0, 1, 15, 16, 17, 112, 113, 127, 128, 129, 240, 300]
+    E = len(rows)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    assert (sum(rows) / E >= 256) == tall
+    cfg = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared)
+    g = torch.Generator().manual_seed(17)
+    bf = torch.bfloat16
+    s1 = 0.5 / d ** 0.5
+    W = dict(W1=(torch.randn(E, h, d, generator=g) * s1), W2=(torch.randn(E, d, h, generator=g) / h ** 0.5),
+             Ws1=(torch.randn(h, d, generator=g) * s1), Ws2=(torch.randn(d, h, generator=g) / h ** 0.5))
+    if act == "swiglu":
+        W["W3"] = torch.randn(E, h, d, generator=g) * s1
+        W["Ws3"] = torch.randn(h, d, generator=g) * s1
+    else:
+        W.update(b1=torch.randn(E, h, generator=g) * 0.2, b2=torch.randn(E, d, generator=g) * 0.2,
+                 bs1=torch.randn(h, generator=g) * 0.2, bs2=torch.randn(d, generator=g) * 0.2)
+    W = {n: v.to(bf).to(DEV) for n, v in W.items()}
+    x = torch.randn(T, d, generator=g).to(bf).to(DEV)
+    Xp = torch.randn(T * k, d, generator=g).to(bf).to(DEV)
+    H = torch.full((T * k, h), 7.0, dtype=bf, device=DEV)
+    Yp = torch.full((T * k, d), 7.0, dtype=bf, device=DEV)
+    offs = torch.as_tensor(off, device=DEV)
+    ws = M.moe.workspace(cfg, 1)
+    Hs = torch.empty(T, h, dtype=bf, device=DEV) if shared else None
+    Sx = torch.empty(T, d, dtype=bf, device=DEV) if shared else None
+    if shared:
+        M.moe.moe_expert_ffn_shared(cfg, Xp, offs, W, H, Yp, x, Hs, Sx, ws)
+    else:
+        M.moe_expert_ffn(cfg, Xp, offs, W["W1"], W.get("W3"), W.get("b1"), W["W2"], W.get("b2"), H, Yp, ws)
+    assert M.moe_check_error(ws) == 0
+    Wn = {n: to_np(v) for n, v in W.items()}
+    Xn, Hn, Yn = to_np(Xp), to_np(H), to_np(Yp)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b == a:
+            continue
+        p = O.expert_params(Wn, e, act)
+        if act == "swiglu":
+            Href = O.silu(Xn[a:b] @ p["W1"].T) * (Xn[a:b] @ p["W3"].T)
+        else:
+            Href = O.gelu(Xn[a:b] @ p["W1"].T + p["b1"])
+        assert_close_bf16(Hn[a:b], Href, f"H expert {e} ({rows[e]} rows)")
+        assert_close_bf16(Yn[a:b], O.expert_ffn(Xn[a:b], act, **p), f"Yp expert {e} ({rows[e]} rows)")
+    assert (Hn[off[-1]:] == 7.0).all() and (Yn[off[-1]:] == 7.0).all()
+    if shared:
+        assert_close_bf16(to_np(Sx), O.expert_ffn(to_np(x), act, **O.shared_params(Wn, act)), "Sx (shared expert)")
+
+
 @pytest.mark.parametrize("act,shared", [("swiglu", False), ("gelu", False), ("swiglu", True)])
 def test_expert_ffn_pair_tiles(act, shared):
     """With MOE_GEMM_CTA_PAIRS, groups averaging >= 256 rows run as 256-row
