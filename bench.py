@@ -29,6 +29,7 @@ on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -49,8 +50,8 @@ WEIGHTS = ("Wr", "W1", "W3", "W2", "b1", "b2", "Ws1", "Ws3", "Ws2", "bs1", "bs2"
 # rows, keyed by the sha256 of the kernel source it was taken on (the figure
 # is reported only while that source is unchanged)
 GEMM_TRAFFIC = {
-    # 1.5741 GB (GEMM-1 1.0414 GB + GEMM-2 0.5326 GB) x 32607 / 2048 kept rows
-    "9efcd79313345f1161a9f87f496a9425ba69a5055688a7190586f6fd0bd00be9": 25.06e9,
+    # 1.5743 GB (GEMM-1 1.0417 GB + GEMM-2 0.5326 GB) x 32607 / 2048 kept rows
+    "275ec474d689f64c3b1343efdd97715d0a01b52226e356b836145c9ca221d7e1": 25.065e9,
 }
 
 
@@ -66,8 +67,10 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 50 ms while running, each
-    stamped with the host time, so a summary can cover one timed region."""
+    """SM clock / throttle-reason samples while running, each stamped with
+    the host time, so a summary can cover one timed region.  NVML is read
+    every 5 ms from a thread (read-only queries); without NVML, nvidia-smi
+    every 50 ms."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -77,17 +80,63 @@ class ClockSampler:
         self.index = index
         self.rows = []
         self.proc = None
+        self.stop = threading.Event()
+        self.thread = None
+        self.source = None
 
     def __enter__(self):
+        try:
+            self.thread = threading.Thread(target=self._nvml, args=(self._nvml_open(),), daemon=True)
+            self.thread.start()
+            self.source = "nvml"
+            return self
+        except Exception as e:
+            self.nvml_error = repr(e)[:120]
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
         return self
+
+    def _nvml_open(self):
+        """The driver's NVML library through ctypes (read-only queries):
+        (lib, device handle, max SM clock, the clock-event reasons call)."""
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByIndex_v2")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) != 0:
+            raise RuntimeError("nvmlDeviceGetMaxClockInfo")
+        try:
+            reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, mx.value, reasons
+
+    # NVML_CLOCK_SM, and the clock-event reason bits in the order of FIELDS[3:]:
+    # hardware slowdown, hardware thermal, software thermal, software power cap
+    NVML_CLOCK_SM = 1
+    NVML_REASONS = (0x8, 0x40, 0x20, 0x4)
+
+    def _nvml(self, opened):
+        lib, h, mx, get_reasons = opened
+        sm, mw, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(sm)) != 0 or
+                    lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) != 0 or get_reasons(h, ctypes.byref(bits)) != 0):
+                break
+            act = ["Active" if bits.value & b else "Not Active" for b in self.NVML_REASONS]
+            self.rows.append((time.time(), [str(sm.value), str(mx), f"{mw.value / 1000.0:.1f}", *act]))
+            self.stop.wait(0.005)
+        lib.nvmlShutdown()
 
     def _read(self):
         for line in self.proc.stdout:
@@ -96,12 +145,15 @@ class ClockSampler:
                 self.rows.append((time.time(), parts))
 
     def __exit__(self, *a):
+        self.stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        elif self.thread:
+            self.thread.join(timeout=5)
 
     def summary(self, t_from=None, t_to=None):
         """Median SM clock, max clock and the throttle reasons seen, over the
@@ -114,7 +166,7 @@ class ClockSampler:
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": self.source}
 
 
 def percentiles(ms):
@@ -284,6 +336,7 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     assert M.moe_check_error(ws) == 0, "a kernel gave up a bounded wait"
 
     peaks = load_peaks()
+    layer_launches = 1 + (2 if wl.dtype == "bf16" else 1) + 4 + 2 + 1
     out = {
         "ms_per_step": ms_step,
         "step_ms": percentiles(step_ms),
@@ -291,11 +344,13 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
         "stage_path_ms": stage_ms_total / steps,
         "stage_step_ms": percentiles(stage_step_ms),
         "stage_clocks": stage_clocks,
-        # our kernels per step: moe_layer_fwd = zeroing, router GEMM + top-k,
-        # 4 dispatch, entropy mean, 2 grouped GEMMs, combine (11); the stage
-        # path = the same without the entropy mean, plus moe_expert_ffn's
-        # zeroing of the error word (11)
-        "launches_per_step": 22,
+        # our kernels per step of both regions: moe_layer_fwd = zeroing,
+        # router (bf16: logits GEMM + top-k; fp32: one kernel), 4 dispatch
+        # (the entropy mean rides in the capacity scan), 2 grouped GEMMs,
+        # combine; the stage path = the same plus moe_expert_ffn's zeroing of
+        # the error word
+        "layer_launches": layer_launches,
+        "launches_per_step": 2 * layer_launches + 1,
         "tokens_per_s": job_throughput(wl.T, world, ms_step),
         "stats": stats,
         "components_ms": comp,
@@ -605,7 +660,7 @@ def layer_section(r, peaks, peak):
         # fp32 runs on the CUDA cores, not the bf16 tensor path; at this size
         # the layer is launch-latency bound and the fraction is only a figure
         out["bound"] = "latency"
-        out["launches_per_step"] = r["launches_per_step"] // 2
+        out["launches_per_step"] = r["layer_launches"]
         out["us_per_launch"] = ms * 1e3 / out["launches_per_step"]
     return out
 
@@ -713,7 +768,11 @@ def main():
         "stage_clocks": r["stage_clocks"],
         "stage_step_ms": r["stage_step_ms"],
         "e2e": r["e2e"],
-        "gpu_launches": r["launches_per_step"] * args.steps,
+        # our kernels in the value's timed region (K moe_layer_fwd calls); the
+        # stage-path region that times the kernels one by one launches
+        # gpu_launches_stage_path more
+        "gpu_launches": r["layer_launches"] * args.steps,
+        "gpu_launches_stage_path": (r["launches_per_step"] - r["layer_launches"]) * args.steps,
         "components_ms": {k: round(v, 4) for k, v in r["components_ms"].items()},
         "layer_stats": {k: r["stats"][k] for k in ("kept_slots", "dropped_slots", "capacity", "drop_rate",
                                                     "balance_stat")},

@@ -463,11 +463,9 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* wts, const vo
                    route_scratch_bytes(*cfg) ? at(ws, L.route_off) : nullptr, backup, out_logits, err, st);
   if (s != MOE_OK) return s;
   s = launch_dispatch(*cfg, capacity_of(cfg), S.idx, x, S.kept, S.offsets, S.pos, S.Xp, stats,
-                      at(ws, L.dispatch_off), backup, st);
+                      at(ws, L.dispatch_off), backup, st, ent);
   if (s != MOE_OK) return s;
   if (stats) {
-    s = launch_entropy_mean(ent, cfg->T, stats, st);
-    if (s != MOE_OK) return s;
     if (cfg->balance == MOE_BALANCE_SWITCH) {
       s = launch_balance_stat_switch(*cfg, S.idx, S.w, S.counts, static_cast<unsigned long long*>(at(ws, L.imp)),
                                      stats, st);

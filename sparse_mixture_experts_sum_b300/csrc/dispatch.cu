@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
                                                              int k, int E, int C, float lam, int balance,
                                                              float gamma, const int* __restrict__ used,
                                                              int* __restrict__ base, int* __restrict__ kept,
-                                                             int* __restrict__ offsets, moe_stats* stats) {
+                                                             int* __restrict__ offsets, moe_stats* stats,
+                                                             const float* __restrict__ ent) {
   pdl_entry();
   __shared__ int tot[1024];
   __shared__ int warp_sums[32];
@@ -198,10 +199,28 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
     //   sum_e (f_e - mean f)^2 = (E sum c^2 - (sum c)^2) / (E T^2)
     // from an exact 128-bit numerator, so the fp64 work is a handful of
     // operations on one thread
+    //
+    // With ent (the layer forward): router_entropy = the mean of the finite
+    // entries of ent[0..T), each thread summing a strided subset in fp64,
+    // then warps and the block in a fixed order (NaN when none is finite).
     __shared__ long long redl[32][3];
     __shared__ int redmax[32];
+    __shared__ double rede[32];
+    __shared__ int redec[32];
     const long long nslots = static_cast<long long>(T) * k;
     const int nwarps = (blockDim.x + 31) >> 5;
+    double es = 0.0;
+    int ec = 0;
+    if (ent) {
+#pragma unroll 8
+      for (int t = tid; t < T; t += blockDim.x) {
+        const float v = ent[t];
+        if (isfinite(v)) {
+          es += v;
+          ++ec;
+        }
+      }
+    }
     long long r_cnt = tid < E ? tot[tid] : 0, k_cnt = tid < E ? my_kept : 0;
     long long sq = tid < E ? static_cast<long long>(tot[tid]) * tot[tid] : 0;
     int cmax = tid < E ? tot[tid] : 0;
@@ -211,12 +230,16 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
       k_cnt += __shfl_xor_sync(0xffffffffu, k_cnt, o);
       sq += __shfl_xor_sync(0xffffffffu, sq, o);
       cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+      es += __shfl_xor_sync(0xffffffffu, es, o);
+      ec += __shfl_xor_sync(0xffffffffu, ec, o);
     }
     if (lane == 0) {
       redl[warp][0] = r_cnt;
       redl[warp][1] = k_cnt;
       redl[warp][2] = sq;
       redmax[warp] = cmax;
+      rede[warp] = es;
+      redec[warp] = ec;
     }
     __syncthreads();
     if (tid == 0) {
@@ -249,7 +272,13 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
         st.balance_stat = __longlong_as_double(0x7ff8000000000000LL);  // needs the weights: set by the layer
       else
         st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
-      st.router_entropy = __longlong_as_double(0x7ff8000000000000LL);  // set by the layer forward
+      double ts = 0.0;
+      long long tc = 0;
+      for (int w2 = 0; w2 < nwarps; ++w2) {
+        ts += rede[w2];
+        tc += redec[w2];
+      }
+      st.router_entropy = tc > 0 ? ts / tc : __longlong_as_double(0x7ff8000000000000LL);
       st.rerouted_slots = 0;
       *stats = st;
     }
@@ -437,46 +466,6 @@ __global__ void combine_f32_kernel(const float* __restrict__ Yp, const int* __re
   }
 }
 
-// stats->router_entropy = the mean of the finite entries of ent[0..T):
-// each thread sums a strided subset in fp64, then warps and the block
-// reduce in a fixed order (NaN when no token is finite).
-__global__ void __launch_bounds__(1024) entropy_mean_kernel(const float* __restrict__ ent, int T,
-                                                            moe_stats* stats) {
-  pdl_entry();
-  __shared__ double rs[32];
-  __shared__ int rc[32];
-  double s = 0.0;
-  int c = 0;
-#pragma unroll 8
-  for (int t = threadIdx.x; t < T; t += blockDim.x) {
-    const float v = ent[t];
-    if (isfinite(v)) {
-      s += v;
-      ++c;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    s += __shfl_xor_sync(0xffffffffu, s, o);
-    c += __shfl_xor_sync(0xffffffffu, c, o);
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) {
-    rs[warp] = s;
-    rc[warp] = c;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double ts = 0.0;
-    long long tc = 0;
-    for (int w2 = 0; w2 < (blockDim.x >> 5); ++w2) {
-      ts += rs[w2];
-      tc += rc[w2];
-    }
-    stats->router_entropy = tc > 0 ? ts / tc : __longlong_as_double(0x7ff8000000000000LL);
-  }
-}
-
 // counts[j*E + e] = the slots (t, j) routed to expert e: the per-slot
 // histogram that expert-parallel ranks exchange.  Integer atomics, so the
 // result does not depend on their order.
@@ -542,7 +531,7 @@ size_t dispatch_scratch_bytes(const moe_config& cfg) {
 
 moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const void* x, int* kept, int* offsets,
                            int* pos, void* Xp, moe_stats* stats, void* scratch, const int* backup,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const float* ent) {
   const int nb = n_chunks(cfg);
   uint8_t* sp = static_cast<uint8_t*>(scratch);
   int* blockhist = reinterpret_cast<int*>(sp);
@@ -559,7 +548,7 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
     launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S1, cfg.T, cfg.k, cfg.E, tm, CH,
                blockhist);
     launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
-               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept, offsets, stats);
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept, offsets, stats, ent);
     launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets,
                nullptr, pos, EpMap{nullptr, nullptr, 0});
   } else {
@@ -571,14 +560,14 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
     launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S1, cfg.T, cfg.k, cfg.E, tm, CH,
                blockhist);
     launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
-               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept1, offsets, stats);
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept1, offsets, stats, ent);
     launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept1, nullptr,
                nullptr, rank1, EpMap{nullptr, nullptr, 0});
     const SlotSrc S2{idx, rank1, backup};
     launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S2, cfg.T, cfg.k, cfg.E, tm, CH,
                blockhist);
     launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
-               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, kept1, base, kept, offsets, stats);
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, kept1, base, kept, offsets, stats, nullptr);
     launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S2, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets,
                kept1, pos, EpMap{nullptr, nullptr, 0});
   }
@@ -654,7 +643,7 @@ moe_status launch_dispatch_ep(const moe_config& cfg, const int* idx, const void*
              CH, blockhist);
   // local slot-major ranks only: the capacity test is on the global rank
   launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, 0x7fffffff, 0.f,
-             0, 0.f, nullptr, base, kept, offsets, nullptr);
+             0, 0.f, nullptr, base, kept, offsets, nullptr, nullptr);
   launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, false, CH, base, kept, offsets,
              nullptr, pos, EpMap{adj, send, C});
   if (Xsend) {
@@ -681,10 +670,6 @@ moe_status launch_permute_rows(const void* src, const int* map, long long n, lon
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status launch_entropy_mean(const float* ent, int T, moe_stats* stats, cudaStream_t stream) {
-  launch_pdl(entropy_mean_kernel, dim3(1), dim3(1024), 0, stream, ent, T, stats);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
 
 moe_status launch_combine(const moe_config& cfg, const void* Yp, const int* pos, const float* w, const void* Sx,
                           void* y, cudaStream_t stream) {

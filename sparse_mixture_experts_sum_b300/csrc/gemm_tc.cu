@@ -840,22 +840,23 @@ namespace {
 
 // Tile shape for a launch: 256-row single-CTA tiles when the groups average
 // at least 256 output rows, such tiles still give every SM one, and the
-// epilogue is light -- plain, or a forward activation that saves no
-// pre-activations -- else 128-row tiles; a forward launch asked for CTA pairs
-// (p.cta_pairs) runs 256-row tiles on pairs under the same rule, any epilogue.
+// epilogue is light -- plain, or any forward activation -- else 128-row
+// tiles; a forward launch asked for CTA pairs (p.cta_pairs) runs 256-row
+// tiles on pairs under the same rule.
 template <int KIND>
 moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows, const void* B0, const void* B1,
                            long long b_rows, long long avg_rows, const GemmExtra* extra, cudaStream_t stream) {
   // BM = 256 on one CTA feeds the tensor cores with 2/3 of the shared-memory
   // traffic per MAC but has a single accumulator, so its epilogue does not
-  // overlap the next tile's MMAs: take it for the light epilogues only.  On
-  // the power-capped part the saved traffic outweighs the lost overlap for
-  // an activation epilogue too (the large prefill's SwiGLU GEMM-1: 3% faster
-  // live, though 9% slower at uncapped clocks), but not once it also stores
-  // fp32 pre-activations for a backward.  A CTA pair halves the B bytes staged per MAC and keeps two
-  // accumulators per CTA, so it serves every forward epilogue.  Either only
-  // when it still gives every SM a tile (a single-group launch such as the
-  // router's logits would otherwise leave most SMs idle).
+  // overlap the next tile's MMAs.  On the power-capped part the saved
+  // traffic outweighs the lost overlap for every forward epilogue: the large
+  // prefill's SwiGLU GEMM-1 is 3% faster live (though 9% slower at uncapped
+  // clocks), and the training forward's, which also stores the fp32
+  // pre-activations, 6%.  The backward's activation epilogue (it reads those
+  // pre-activations and writes four outputs) keeps 128-row tiles.  A CTA
+  // pair halves the B bytes staged per MAC and keeps two accumulators per
+  // CTA.  Either only when it still gives every SM a tile (a single-group
+  // launch such as the router's logits would otherwise leave most SMs idle).
   const long long n_tiles = (KIND == kKindFwd && p.mode == kModeSwiGLU) ? (p.N + 127) / 128 : (p.N + BN - 1) / BN;
   auto tiles_for = [&](int bm) -> long long {
     if (KIND == kKindWgrad) return static_cast<long long>(p.G) * ((p.M + bm - 1) / bm) * n_tiles;
@@ -869,8 +870,7 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
   const int sms = device_sm_count(dev);
   const bool pair = KIND == kKindFwd && p.cta_pairs && avg_rows >= 256 && (p.mode == kModeSwiGLU || p.N >= BN) &&
                     2 * tiles_for(256) >= sms;
-  const bool light = p.mode == kModePlain ||
-                     (KIND == kKindFwd && !p.zsave && (p.xrows == 0 || !p.xzsave));
+  const bool light = p.mode == kModePlain || KIND == kKindFwd;
   const bool tall = !pair && avg_rows >= 256 && light && tiles_for(256) >= sms;
   CUtensorMap mA, mB0, mB1, mXA, mXB0, mXB1;  // Fwd/Dgrad A boxes: 128 rows (two per 256-row tile)
   const long long tiles = tiles_for(pair || tall ? 256 : 128);

@@ -143,16 +143,16 @@ size_t route_scratch_bytes(const moe_config& cfg);
 moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, const float* expert_bias,
                         const float* noise, int* idx, float* w, int* counts, float* ent, void* scratch, int* backup,
                         float* out_logits, int* err, cudaStream_t stream);
-// stats->router_entropy = mean of the finite ent[0..T) (fixed-order fp64 sum).
-moe_status launch_entropy_mean(const float* ent, int T, moe_stats* stats, cudaStream_t stream);
 
 // Dispatch: slot-major capacity ranks, offsets, positions, statistics, permute.
 size_t dispatch_scratch_bytes(const moe_config& cfg);
 // backup: the router's backup experts (MOE_ROUTE_REROUTE: a second pass
-// offers the dropped slots to them), else nullptr.
+// offers the dropped slots to them), else nullptr.  ent (with stats): the
+// router's per-token entropies; stats->router_entropy = the mean of their
+// finite entries (fixed-order fp64 sum), else NaN.
 moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const void* x, int* kept,
                            int* offsets, int* pos, void* Xp, moe_stats* stats, void* scratch,
-                           const int* backup, cudaStream_t stream);
+                           const int* backup, cudaStream_t stream, const float* ent = nullptr);
 
 // Size of the library's own dispatch scratch (moe_dispatch_static): enough
 // for T*k <= 2^20 slots (256 chunks of 4096) at any E <= 1024.

@@ -253,6 +253,48 @@ def test_backward_raw_probs(balance):
     check_all(wl, t, dY, g, ref)
 
 
+@pytest.mark.parametrize("tall", [False, True])
+def test_saved_preactivations(tall):
+    """The training forward saves GEMM-1's pre-activations in fp32: Z[r] =
+    [Xp[r] W1_e^T | Xp[r] W3_e^T] for the rows of expert e, and Zs = [x Ws1^T |
+    x Ws3^T] for the shared expert.  They are fp32 sums of exact bf16
+    products, so against fp64 products of the stored bf16 operands they hold
+    max-abs 2e-4 of max(1, the row's RMS).  tall: groups averaging 512 rows
+    with enough tiles for every SM, so GEMM-1 runs on 256-row tiles; else
+    128-row tiles."""
+    if tall:
+        wl = S.WORKLOADS["training"].replace(T=2048, d=1024, h=2048, E=8, seed=73)
+    else:
+        wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, seed=79)
+    t = guarded_inputs(wl, DEV)
+    t.pop("dY")
+    cfg = M.config_of(wl)
+    sv = M.moe.alloc_saved(cfg, DEV, backward=True)
+    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=DEV)
+    ws = M.moe.workspace(cfg, 1)
+    M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], t.get("noise"), y, sv, None, ws)
+    assert M.moe_check_error(ws) == 0
+    h = wl.h
+
+    def check(Z, X, W1, W3, what):
+        ref = np.concatenate([X @ W1.T, X @ W3.T], axis=1)
+        rms = np.sqrt(np.mean(ref ** 2, axis=1, keepdims=True))
+        worst = float((np.abs(Z - ref) / np.maximum(1.0, rms)).max())
+        assert worst <= 2e-4, f"{what}: max |err| / max(1, row RMS) {worst:.3e}"
+
+    off = sv["offsets"].cpu().numpy()
+    n = int(off[-1])  # rows past the kept ones are never written
+    Xp = to_np(sv["Xp"][:n])
+    Z = sv["Z"][:n].cpu().numpy().astype(np.float64)
+    assert Z.shape[1] == 2 * h
+    for e in range(wl.E):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            check(Z[a:b], Xp[a:b], to_np(t["W1"][e]), to_np(t["W3"][e]), f"Z expert {e}")
+    if wl.has_shared:
+        check(sv["Zs"].cpu().numpy().astype(np.float64), to_np(t["x"]), to_np(t["Ws1"]), to_np(t["Ws3"]), "Zs")
+
+
 def test_backward_is_deterministic():
     wl = _workload(has_shared=True, gumbel=True, capacity_factor=1.0, seed=53)
     t = guarded_inputs(wl, DEV)
