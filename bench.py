@@ -513,30 +513,35 @@ def _cpu_model():
     return "unknown"
 
 
-# How the oracle is timed per workload: the whole layer where it runs in
-# seconds to a minute; else router, top-k, capacity and dispatch of the whole
-# batch plus the expert rows of the two busiest experts, extrapolated per
-# token by the measured cost of an expert row (forward and backward for the
-# training step).
-CPU_PLAN = {"tiny_fp32": ("whole", None), "small_prefill": ("whole", None), "decode": ("whole", None),
-            "large_prefill": ("experts", None), "training": ("train", 192)}
+# How the oracle is timed per workload.  The forward runs on the C++ fp64
+# oracle (oracle/moe_oracle.cpp: plain single-threaded loops, inputs read as
+# the stored bf16/fp32 bits): the whole layer where that takes seconds;
+# else the router, top-k, capacity and dispatch of the whole batch plus the
+# expert rows of the two busiest experts (at most the given rows each),
+# extrapolated per token by the measured cost of an expert row.  The
+# training step runs on the numpy fp64 oracle, which holds the backward:
+# the same routing plus forward and backward of the sampled rows.
+CPU_PLAN = {"tiny_fp32": ("whole", None), "small_prefill": ("experts", 256), "decode": ("experts", None),
+            "large_prefill": ("experts", 32), "training": ("train", 192)}
 
 
-def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None):
-    """The fp64 oracle as it stands, on ONE host core (its BLAS held to one
-    thread), on the workload's inputs (from the GPU run when given, else
-    drawn on the host at T <= 2048 for the expert-sampling modes):
-      whole   -- layer_forward over the whole batch;
-      experts -- route_and_dispatch of the whole batch, then expert_ffn on the
-                 kept rows of the two busiest experts (at most max_rows each);
-                 tokens/s extrapolated: routing share + expert rows per token
-                 (kept slots / T, + 1 with a shared expert) x cost per row;
-      train   -- the same with expert_ffn_backward (forward and backward of
-                 the rows) for the training step."""
+def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None, tokens=None):
+    """The oracle as it stands, on ONE host core, on the workload's inputs
+    (from the GPU run when given, else drawn on the host at T <= 2048 for
+    the expert-sampling modes):
+      whole   -- the C++ oracle's layer forward over the whole batch;
+      experts -- the C++ oracle's router, top-k, capacity and dispatch of the
+                 whole batch, then its expert FFN on the kept rows of the two
+                 busiest experts (at most max_rows each); tokens/s
+                 extrapolated: routing share + expert rows per token (kept
+                 slots / T, + 1 with a shared expert) x cost per row;
+      train   -- the numpy oracle's routing, then forward and backward of the
+                 sampled rows (expert_ffn_backward), extrapolated alike.
+    tokens: route only the batch's first `tokens` tokens (a bounded sample
+    per step for the reference arm); the rates are per token either way."""
     import numpy as np
     import torch
     import moe_synth as S
-    from oracle import moe_oracle as O
 
     wl = S.WORKLOADS[wl_name]
     plan, rows_cap = CPU_PLAN.get(wl_name, ("experts", None))
@@ -552,23 +557,47 @@ def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None):
         # the two experts that are timed only
         T = min(wl.T, 2048)
         t = S.make_inputs(wl.replace(T=T), "cpu", parts=["x", "Wr", "expert_bias", "noise", "dY"])
+    if tokens is not None and tokens < T:
+        T = tokens
+        t = dict(t, x=t["x"][:T], **({"noise": t["noise"][:T]} if t.get("noise") is not None else {}),
+                 **({"dY": t["dY"][:T]} if t.get("dY") is not None else {}))
     cfg = dict(T=T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act,
                capacity_factor=float(np.float32(wl.capacity_factor)), min_capacity=wl.min_capacity,
                lam=float(np.float32(wl.lam)), has_shared=wl.has_shared)
     host = os.cpu_count() or 1
-    cores = blas_threads()
+    cores = 1 if mode != "train" else blas_threads()
     common = {"unit": "tokens/s", "cores": cores, "kind": "oracle", "host_cores": host, "cpu_model": _cpu_model(),
               "threads": f"{cores} core{'s' if cores != 1 else ''} of {host}"}
+    cpu = lambda a: None if a is None else a.detach().to("cpu")
     if mode == "whole":
+        from oracle import cpp
+        hw = {n: cpu(v) for n, v in t.items()}
         t0 = time.perf_counter()
-        O.layer_forward(cfg, t, t["x"], t.get("expert_bias"), t.get("noise"))
+        cpp.layer_forward(cfg, hw, hw["x"], hw.get("expert_bias"), hw.get("noise"))
         dt = time.perf_counter() - t0
-        return dict(common, value=T / dt, seconds=dt, extrapolated=False,
-                    sample=f"fp64 oracle layer_forward of the whole batch ({T} tokens) in {dt:.2f} s")
-    t0 = time.perf_counter()
-    r = O.route_and_dispatch(cfg, t["x"], t["Wr"], t.get("expert_bias"), t.get("noise"))
-    t_route = time.perf_counter() - t0
-    experts = [int(e) for e in np.argsort(-r["kept"], kind="stable")[:2]]
+        return dict(common, value=T / dt, seconds=dt, extrapolated=False, impl="C++ fp64 oracle, single thread",
+                    sample=f"C++ fp64 oracle layer forward of the whole batch ({T} tokens) in {dt:.2f} s")
+    x, Wr = cpu(t["x"]), cpu(t["Wr"])
+    bias, noise = cpu(t.get("expert_bias")), cpu(t.get("noise"))
+    if mode == "train":
+        from oracle import moe_oracle as O
+        t0 = time.perf_counter()
+        r = O.route_and_dispatch(cfg, x, Wr, bias, noise)
+        t_route = time.perf_counter() - t0
+        idx, pos, kept_e = r["idx"], r["pos"], r["kept"]
+        impl = "numpy fp64 oracle, BLAS on one thread"
+    else:
+        from oracle import cpp
+        t0 = time.perf_counter()
+        l = cpp.router_logits(x, Wr, bias, noise)
+        idx, w_, _ = cpp.top_k(l, wl.k)
+        cpp.usage_counts(idx, wl.E)
+        C = cpp.capacity(T, wl.k, wl.E, cfg["capacity_factor"], wl.min_capacity)
+        rank, kept_e = cpp.assign_capacity(idx, wl.E, C)
+        _, pos = cpp.dispatch_positions(idx, rank, kept_e)
+        t_route = time.perf_counter() - t0
+        impl = "C++ fp64 oracle, single thread"
+    experts = [int(e) for e in np.argsort(-kept_e, kind="stable")[:2]]
     if "W1" not in t:
         t = dict(t)
         for name, (rows_, cols, fan) in dict(W1=(wl.h, wl.d, wl.d), W3=(wl.h, wl.d, wl.d),
@@ -577,28 +606,34 @@ def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None):
                 continue
             t[name] = {e: S.tensor("normal", wl.seed, S.TID[name], (rows_, cols), wl.dtype, wl.std(fan), "cpu",
                                    start=e * rows_ * cols) for e in experts}
-    slots = 0
-    t1 = time.perf_counter()
+    slots, t_ffn = 0, 0.0
     for e in experts:
-        rows, sl = np.nonzero((r["idx"] == e) & (r["pos"] >= 0))
+        rows, sl = np.nonzero((idx == e) & (pos >= 0))
         if max_rows is not None:
             rows, sl = rows[:max_rows], sl[:max_rows]
-        src = O.decode(t["x"][torch.as_tensor(rows, device=t["x"].device)]) if rows.size else None
-        p = O.expert_params(t, e, wl.act)
-        if src is not None:
-            if mode == "train":
-                dy = O.decode(t["dY"][torch.as_tensor(rows, device=t["dY"].device)])
-                O.expert_ffn_backward(src, r["w"][rows, sl][:, None] * dy, wl.act, **p)
-            else:
-                O.expert_ffn(src, wl.act, **p)
+        if rows.size == 0:
+            continue
+        v = x[torch.as_tensor(rows)]
+        p = {n: cpu(t[n][e]) if t.get(n) is not None else None for n in ("W1", "W3", "W2", "b1", "b2")}
+        if wl.act != "swiglu":
+            p["W3"] = None
+        if mode == "train":
+            from oracle import moe_oracle as O
+            src = O.decode(v)
+            dy = O.decode(cpu(t["dY"])[torch.as_tensor(rows)])
+            t1 = time.perf_counter()
+            O.expert_ffn_backward(src, r["w"][rows, sl][:, None] * dy, wl.act, **O.expert_params(t, e, wl.act))
+        else:
+            t1 = time.perf_counter()
+            cpp.expert_ffn(v, wl.act, p["W1"], p["W2"], W3=p["W3"], b1=p["b1"], b2=p["b2"])
+        t_ffn += time.perf_counter() - t1
         slots += rows.size
-    t_ffn = time.perf_counter() - t1
     per_row = t_ffn / max(slots, 1)
-    rows_per_token = float(r["kept"].sum()) / T + (1 if wl.has_shared else 0)
+    rows_per_token = float(kept_e.sum()) / T + (1 if wl.has_shared else 0)
     per_token = t_route / T + per_row * rows_per_token
     what = "forward and backward of" if mode == "train" else "expert FFN of"
-    return dict(common, value=1.0 / per_token, seconds=t_route + t_ffn, extrapolated=True,
-                sample=f"fp64 oracle: router+top-k+capacity+dispatch of all {T} tokens ({t_route:.2f} s), "
+    return dict(common, value=1.0 / per_token, seconds=t_route + t_ffn, extrapolated=True, impl=impl,
+                sample=f"{impl}: router+top-k+capacity+dispatch of all {T} tokens ({t_route:.2f} s), "
                        f"{what} {slots} kept rows of experts {experts} ({t_ffn:.2f} s); whole-layer tokens/s "
                        f"extrapolated per token at {rows_per_token:.3f} expert rows/token")
 
@@ -711,10 +746,11 @@ def main():
             torch.cuda.set_device(local)
             gt = S.make_inputs(S.WORKLOADS[args.workload], torch.device("cuda", local))
         for i in range(args.warmup + args.steps):
-            # each step: the whole routing plus up to 48 rows of each of the
-            # two busiest experts, on one core
+            # each step a bounded sample on one core: the routing of the
+            # batch's first 512 tokens plus up to 8 rows of each of the two
+            # busiest experts among them
             cb = cpu_baseline(args.workload, gt, mode="train" if args.workload == "training" else None,
-                              max_rows=48)
+                              max_rows=8, tokens=512)
             if i >= args.warmup:
                 vals.append(cb["value"])
         v = statistics.median(vals)

@@ -1,0 +1,413 @@
+// Plain fp64 CPU oracle of the sparse Mixture-of-Experts FFN layer's
+// forward pass, in single-threaded C++.
+//
+// TEST INFRASTRUCTURE ONLY.  This is a checker: the tests, the smoke check
+// and the benchmark's CPU-baseline leg may call it; the CUDA library never
+// does, and it shares no code with the CUDA path.  It restates the same
+// definitions as moe_oracle.py, in plain loops written in the order the
+// pages state the method, and the tests hold the two oracles to each other
+// and to the pages' worked examples.
+//
+// Inputs are the stored bits the GPU reads: fp32 or bf16 elements, decoded
+// exactly to fp64 on every read (bf16 is the upper half of an fp32 word),
+// so both sides start from identical values.  Every sum runs in index
+// order in fp64; there is no blocking, threading or reordering.
+//
+// Sources (page title -- section):
+//   [P1] "'More parameters is better' is not the story: the expert group
+//        quietly activated inside a large model" -- 3.1 Router, 3.3 Gate,
+//        4.2 model definition.
+//   [P2] "MoE mixture-of-experts architecture: principles and engineering
+//        practice" -- 4.2 building an MoE model.
+//   [P3] "MoE architecture revealed: why total parameters != active
+//        parameters" -- 2.3 router design, 3.3 TinyMoE.
+//   [P5] "Training a 200B LLM from scratch 5/25: how does MoE compute with
+//        part of its parameters?" -- "Who decides which experts to call?",
+//        "Shared experts".
+//
+// Readings (the same as the numpy oracle's): selection on the logits with
+// ties to the lower expert index; weights = the softmax of the selected
+// logits; capacity C = max(min_capacity, ceil(cf*T*k/E)) with the ceiling
+// of the exact rational value of the caller's fp32 cf, no limit when
+// cf <= 0; overflow in slot-major priority (every token's first choice in
+// token order, then every second choice); a dropped slot adds nothing; GeLU
+// is the exact erf form; SwiGLU is W2 (silu(W1 v) * (W3 v)); the shared
+// expert is added with weight 1; usage statistic lambda * std_{n-1}(f) /
+// (mean(f) + 1e-8) on pre-capacity counts f = counts / T; a token with a
+// non-finite logit is routed to no expert.  The routing variants (raw
+// probabilities, token-major priority, rerouting, a LayerNorm in front,
+// other balance statistics) are checked by the numpy oracle only.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <algorithm>
+#include <vector>
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// stored inputs
+// ---------------------------------------------------------------------------
+enum { MO_F32 = 0, MO_BF16 = 1 };
+
+// Element i of a stored tensor, exactly, as fp64.
+inline double rd(const void* p, int dtype, long long i) {
+  if (dtype == MO_BF16) {
+    const uint32_t u = static_cast<uint32_t>(static_cast<const uint16_t*>(p)[i]) << 16;
+    float f;
+    std::memcpy(&f, &u, sizeof f);
+    return f;
+  }
+  return static_cast<const float*>(p)[i];
+}
+
+inline bool all_finite(const double* v, int n) {
+  for (int i = 0; i < n; ++i)
+    if (!std::isfinite(v[i])) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+// router ([P1] 3.1, 3.3, 4.2; [P3] 2.3)
+// ---------------------------------------------------------------------------
+
+// l[t,e] = sum_i x[t,i] Wr[e,i] (+ bias[e]) (+ noise[t,e]).  x [T,d] and Wr
+// [E,d] in `dtype`; bias [E] and noise [T,E] fp32, either may be null.
+// [P1] 3.1: the logits are h W_r; [P3] 2.3: Gumbel noise is added to the
+// router's scores before the top-k.
+void mo_router_logits(int T, int d, int E, int dtype, const void* x, const void* Wr, const float* bias,
+                      const float* noise, double* l) {
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int i = 0; i < d; ++i)
+        s += rd(x, dtype, static_cast<long long>(t) * d + i) * rd(Wr, dtype, static_cast<long long>(e) * d + i);
+      if (bias) s += bias[e];
+      if (noise) s += noise[static_cast<long long>(t) * E + e];
+      l[static_cast<long long>(t) * E + e] = s;
+    }
+  }
+}
+
+// Top-k experts per token by (logit descending, index ascending) -- softmax
+// is monotone, so this is [P1] 4.2's top-k of the probabilities -- and their
+// weights w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0), the softmax of the
+// selected logits ([P1] 3.3: p_i / (p_i + p_j); [P3] 3.3).  A token with a
+// non-finite logit gets idx = -1 and w = 0 in every slot.  Returns the
+// number of such tokens.
+int mo_top_k(int T, int E, int k, const double* l, int* idx, double* w) {
+  int nonfinite = 0;
+  std::vector<char> taken(E);
+  for (int t = 0; t < T; ++t) {
+    const double* lt = l + static_cast<long long>(t) * E;
+    int* it = idx + static_cast<long long>(t) * k;
+    double* wt = w + static_cast<long long>(t) * k;
+    if (!all_finite(lt, E)) {
+      ++nonfinite;
+      for (int j = 0; j < k; ++j) {
+        it[j] = -1;
+        wt[j] = 0.0;
+      }
+      continue;
+    }
+    // k rounds: the largest logit not yet taken; the first index wins a tie
+    std::fill(taken.begin(), taken.end(), 0);
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e)
+        if (!taken[e] && (best < 0 || lt[e] > lt[best])) best = e;
+      taken[best] = 1;
+      it[j] = best;
+    }
+    double z = 0.0;
+    for (int j = 0; j < k; ++j) z += std::exp(lt[it[j]] - lt[it[0]]);
+    for (int j = 0; j < k; ++j) wt[j] = std::exp(lt[it[j]] - lt[it[0]]) / z;
+  }
+  return nonfinite;
+}
+
+// Mean over the tokens with finite logits of H_t = -sum_e p_te ln p_te,
+// p_t = the softmax over all E experts ([P3]'s monitoring of the router
+// entropy).  NaN when no token has finite logits.
+double mo_router_entropy(int T, int E, const double* l) {
+  double sum = 0.0;
+  long long n = 0;
+  std::vector<double> p(E);
+  for (int t = 0; t < T; ++t) {
+    const double* lt = l + static_cast<long long>(t) * E;
+    if (!all_finite(lt, E)) continue;
+    double m = lt[0];
+    for (int e = 1; e < E; ++e) m = lt[e] > m ? lt[e] : m;
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) z += (p[e] = std::exp(lt[e] - m));
+    double h = 0.0;
+    for (int e = 0; e < E; ++e) {
+      const double pe = p[e] / z;
+      if (pe > 0.0) h -= pe * std::log(pe);
+    }
+    sum += h;
+    ++n;
+  }
+  return n ? sum / static_cast<double>(n) : std::nan("");
+}
+
+// ---------------------------------------------------------------------------
+// capacity and dispatch ([P3] 2.3; [P1] 4.2 step 2)
+// ---------------------------------------------------------------------------
+
+// C = max(min_capacity, ceil(cf * T * k / E)), or T when cf <= 0 (no
+// limit).  [P3] 2.3: batch 1024, top-2, 16 experts -> 1024 * 2 / 16 = 128.
+// The ceiling is taken of the exact rational value of the fp32 cf the
+// caller passed: cf = m * 2^p with an integer m, so ceil(m T k 2^p / E) is
+// an integer division (128-bit numerator), never a rounded product.  A
+// capacity above 2^31 - 1 is returned as 2^31 - 1.
+int mo_capacity(int T, int k, int E, float capacity_factor, int min_capacity) {
+  if (!(capacity_factor > 0.0f)) return T;
+  int p = 0;
+  const float frac = std::frexp(capacity_factor, &p);           // cf = frac * 2^p, frac in [0.5, 1)
+  const long long m = static_cast<long long>(std::ldexp(frac, 24));  // cf = m * 2^(p - 24), exactly
+  p -= 24;
+  // m < 2^24, T k < 2^35, E < 2^31: the numerator is below 2^59, so a
+  // value with p <= -59 lies in (0, 1) and one with p >= 40 is above 2^31
+  long long cap;
+  if (p <= -59) {
+    cap = 1;
+  } else if (p >= 40) {
+    cap = 0x7fffffffLL;
+  } else {
+    unsigned __int128 num = static_cast<unsigned __int128>(m) * static_cast<unsigned long long>(T) *
+                            static_cast<unsigned long long>(k);
+    unsigned __int128 den = static_cast<unsigned __int128>(E);
+    if (p >= 0) num <<= p;
+    else den <<= -p;
+    const unsigned __int128 c = (num + den - 1) / den;
+    cap = c > 0x7fffffff ? 0x7fffffffLL : static_cast<long long>(c);
+  }
+  return static_cast<int>(cap > min_capacity ? cap : min_capacity);
+}
+
+// counts[e] = the (t, j) slots routed to expert e, before capacity.
+void mo_usage_counts(int T, int k, int E, const int* idx, long long* counts) {
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (long long s = 0; s < static_cast<long long>(T) * k; ++s)
+    if (idx[s] >= 0) ++counts[idx[s]];
+}
+
+// Capacity in slot-major priority: for j = 0..k-1, for t = 0..T-1, the slot
+// (t, j) takes the next free place of its expert if one of C is left, else
+// it is dropped (rank -1).  fill[e] = the slots kept by expert e.
+void mo_assign_capacity(int T, int k, int E, int C, const int* idx, int* rank, long long* fill) {
+  for (int e = 0; e < E; ++e) fill[e] = 0;
+  for (int j = 0; j < k; ++j) {
+    for (int t = 0; t < T; ++t) {
+      const long long s = static_cast<long long>(t) * k + j;
+      const int e = idx[s];
+      if (e >= 0 && fill[e] < C) rank[s] = static_cast<int>(fill[e]++);
+      else rank[s] = -1;
+    }
+  }
+}
+
+// offsets = the exclusive scan of fill (expert e's rows are [offsets[e],
+// offsets[e+1]) of the expert-contiguous matrix); pos[t,j] = offsets[e] +
+// rank for a kept slot, else -1.
+void mo_dispatch_positions(int T, int k, int E, const int* idx, const int* rank, const long long* fill,
+                           long long* offsets, long long* pos) {
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + fill[e];
+  for (long long s = 0; s < static_cast<long long>(T) * k; ++s)
+    pos[s] = rank[s] >= 0 ? offsets[idx[s]] + rank[s] : -1;
+}
+
+// ---------------------------------------------------------------------------
+// experts and combine ([P2] 4.2; [P3] 3.3; [P5])
+// ---------------------------------------------------------------------------
+
+// One expert FFN on n rows v [n,d] (stored in `dtype`, row stride d) ->
+// out [n,d] fp64.  act 0, GeLU: W2 gelu(W1 v + b1) + b2, gelu(z) = z (1 +
+// erf(z / sqrt 2)) / 2 ([P2] 4.2, [P3] 3.3: Linear, GELU, Linear).  act 1,
+// SwiGLU: W2 (silu(W1 v) * (W3 v)), silu(z) = z / (1 + e^-z).  W1, W3 [h,d],
+// W2 [d,h] and the biases b1 [h], b2 [d] (null: none) in `dtype`.  Each
+// weight row is read once for all n rows; every output element is its own
+// sum in index order.
+void mo_expert_ffn(int n, int d, int h, int act, int dtype, const void* v, const void* W1, const void* W3,
+                   const void* b1, const void* W2, const void* b2, double* out) {
+  std::vector<double> vr(static_cast<size_t>(n) * d), hid(static_cast<size_t>(n) * h), wrow(d), grow(d), orow(h);
+  for (long long i = 0; i < static_cast<long long>(n) * d; ++i) vr[i] = rd(v, dtype, i);
+  for (int u = 0; u < h; ++u) {
+    for (int i = 0; i < d; ++i) wrow[i] = rd(W1, dtype, static_cast<long long>(u) * d + i);
+    if (act == 1)
+      for (int i = 0; i < d; ++i) grow[i] = rd(W3, dtype, static_cast<long long>(u) * d + i);
+    for (int r = 0; r < n; ++r) {
+      const double* vrow = vr.data() + static_cast<long long>(r) * d;
+      double z = 0.0;
+      for (int i = 0; i < d; ++i) z += wrow[i] * vrow[i];
+      if (act == 0) {
+        if (b1) z += rd(b1, dtype, u);
+        hid[static_cast<long long>(r) * h + u] = z * 0.5 * (1.0 + std::erf(z / std::sqrt(2.0)));
+      } else {
+        double g = 0.0;
+        for (int i = 0; i < d; ++i) g += grow[i] * vrow[i];
+        hid[static_cast<long long>(r) * h + u] = z / (1.0 + std::exp(-z)) * g;
+      }
+    }
+  }
+  for (int col = 0; col < d; ++col) {
+    for (int u = 0; u < h; ++u) orow[u] = rd(W2, dtype, static_cast<long long>(col) * h + u);
+    const double bias = (act == 0 && b2) ? rd(b2, dtype, col) : 0.0;
+    for (int r = 0; r < n; ++r) {
+      const double* hr = hid.data() + static_cast<long long>(r) * h;
+      double o = 0.0;
+      for (int u = 0; u < h; ++u) o += orow[u] * hr[u];
+      out[static_cast<long long>(r) * d + col] = o + bias;
+    }
+  }
+}
+
+// y[t] = sum over the kept slots j (ascending) of w[t,j] * out[t,j,:], plus
+// shared[t] when given.  [P5] "Who decides which experts to call?": the two
+// chosen experts' outputs mixed in the routing proportions, 0.75 E1(x) +
+// 0.25 E3(x); "Shared experts": the always-on expert's output is added.
+// out [T,k,d], w [T,k], kept [T,k] (nonzero = kept), shared [T,d] or null.
+void mo_combine(int T, int k, int d, const double* out, const double* w, const int* kept, const double* shared,
+                double* y) {
+  for (int t = 0; t < T; ++t) {
+    double* yt = y + static_cast<long long>(t) * d;
+    for (int c = 0; c < d; ++c) yt[c] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const long long s = static_cast<long long>(t) * k + j;
+      if (!kept[s]) continue;
+      for (int c = 0; c < d; ++c) yt[c] += w[s] * out[s * d + c];
+    }
+    if (shared)
+      for (int c = 0; c < d; ++c) yt[c] += shared[static_cast<long long>(t) * d + c];
+  }
+}
+
+// lambda * std_{n-1}(f) / (mean(f) + 1e-8) on f = counts / T ([P1] 3.1:
+// L_balance = lambda * std(usage) / mean(usage); [P1] 4.2 averages the
+// one-hot selection over the tokens, adds 1e-8 to the mean and uses the n-1
+// standard deviation).  0 for a single expert.
+double mo_balance_stat(int E, int T, const long long* counts, double lam) {
+  if (E < 2) return 0.0;
+  double mean = 0.0;
+  for (int e = 0; e < E; ++e) mean += static_cast<double>(counts[e]) / T;
+  mean /= E;
+  double ss = 0.0;
+  for (int e = 0; e < E; ++e) {
+    const double f = static_cast<double>(counts[e]) / T - mean;
+    ss += f * f;
+  }
+  return lam * std::sqrt(ss / (E - 1)) / (mean + 1e-8);
+}
+
+// ---------------------------------------------------------------------------
+// the layer
+// ---------------------------------------------------------------------------
+
+struct mo_config {
+  int T, d, h, E, k;
+  int act;    // 0 GeLU, 1 SwiGLU
+  int dtype;  // storage of x and the weights: 0 fp32, 1 bf16
+  int min_capacity;
+  int has_shared;
+  float capacity_factor;  // <= 0: no limit
+  double lam;
+};
+
+// Stored inputs (pointers in the config's dtype unless noted; null where
+// absent).  W1/W3 [E,h,d], W2 [E,d,h], b1 [E,h], b2 [E,d]; the shared
+// expert's Ws1/Ws3 [h,d], Ws2 [d,h], bs1 [h], bs2 [d]; bias [E] and noise
+// [T,E] fp32.
+struct mo_inputs {
+  const void *x, *Wr, *W1, *W3, *b1, *W2, *b2, *Ws1, *Ws3, *bs1, *Ws2, *bs2;
+  const float *bias, *noise;
+};
+
+// Outputs: y [T,d], idx/pos [T,k], w [T,k], counts/kept [E], offsets
+// [E+1]; stats[0..7] = routed, kept and dropped slots, capacity, drop rate,
+// balance statistic, tokens with a non-finite logit, mean router entropy.
+struct mo_outputs {
+  double* y;
+  int* idx;
+  double* w;
+  long long *counts, *kept, *offsets, *pos;
+  double* stats;
+};
+
+// The whole forward pass, steps in the pages' order: logits, top-k and
+// weights, usage counts, capacity, dispatch positions, each kept slot
+// through its expert, the shared expert, the combine, the statistics.
+// Returns 0, or -1 on an invalid configuration.
+int mo_layer_forward(const mo_config* c, const mo_inputs* in, mo_outputs* out) {
+  const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
+  if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
+      (dt != MO_F32 && dt != MO_BF16))
+    return -1;
+  const long long S = static_cast<long long>(T) * k;
+  const int es = dt == MO_BF16 ? 2 : 4;
+  std::vector<double> l(static_cast<size_t>(T) * E);
+  mo_router_logits(T, d, E, dt, in->x, in->Wr, in->bias, in->noise, l.data());
+  const int nonfinite = mo_top_k(T, E, k, l.data(), out->idx, out->w);
+  mo_usage_counts(T, k, E, out->idx, out->counts);
+  const int C = mo_capacity(T, k, E, c->capacity_factor, c->min_capacity);
+  std::vector<int> rank(S);
+  mo_assign_capacity(T, k, E, C, out->idx, rank.data(), out->kept);
+  mo_dispatch_positions(T, k, E, out->idx, rank.data(), out->kept, out->offsets, out->pos);
+
+  // dispatch ([P1] 4.2 step 2: the tokens bound for the same expert grouped
+  // together): the stored row of x[t] copied to row pos[t,j] of Xp; then
+  // each expert once over its rows; slot (t,j)'s output is Yp[pos[t,j]]
+  const long long rows = out->offsets[E];
+  std::vector<char> Xp(static_cast<size_t>(rows) * d * es);
+  for (long long s = 0; s < S; ++s)
+    if (out->pos[s] >= 0)
+      std::memcpy(Xp.data() + out->pos[s] * d * es, static_cast<const char*>(in->x) + (s / k) * d * es,
+                  static_cast<size_t>(d) * es);
+  std::vector<double> Yp(static_cast<size_t>(rows) * d);
+  const auto at = [&](const void* base, long long elems) -> const void* {
+    return base ? static_cast<const char*>(base) + elems * es : nullptr;
+  };
+  for (int e = 0; e < E; ++e) {
+    const long long r0 = out->offsets[e], n = out->offsets[e + 1] - r0;
+    if (n == 0) continue;
+    mo_expert_ffn(static_cast<int>(n), d, h, c->act, dt, Xp.data() + r0 * d * es,
+                  at(in->W1, static_cast<long long>(e) * h * d), at(in->W3, static_cast<long long>(e) * h * d),
+                  at(in->b1, static_cast<long long>(e) * h), at(in->W2, static_cast<long long>(e) * d * h),
+                  at(in->b2, static_cast<long long>(e) * d), Yp.data() + r0 * d);
+  }
+  std::vector<double> yslot(static_cast<size_t>(S) * d, 0.0);
+  std::vector<int> keep(S);
+  for (long long s = 0; s < S; ++s) {
+    keep[s] = out->pos[s] >= 0;
+    if (keep[s]) std::memcpy(&yslot[s * d], &Yp[out->pos[s] * d], sizeof(double) * d);
+  }
+  std::vector<double> shared;
+  if (c->has_shared) {
+    shared.resize(static_cast<size_t>(T) * d);
+    mo_expert_ffn(T, d, h, c->act, dt, in->x, in->Ws1, in->Ws3, in->bs1, in->Ws2, in->bs2, shared.data());
+  }
+  mo_combine(T, k, d, yslot.data(), out->w, keep.data(), c->has_shared ? shared.data() : nullptr, out->y);
+
+  long long routed = 0, kept = 0;
+  for (int e = 0; e < E; ++e) {
+    routed += out->counts[e];
+    kept += out->kept[e];
+  }
+  out->stats[0] = static_cast<double>(routed);
+  out->stats[1] = static_cast<double>(kept);
+  out->stats[2] = static_cast<double>(S - kept);
+  out->stats[3] = C;
+  out->stats[4] = static_cast<double>(S - kept) / static_cast<double>(S);
+  out->stats[5] = mo_balance_stat(E, T, out->counts, c->lam);
+  out->stats[6] = nonfinite;
+  out->stats[7] = mo_router_entropy(T, E, l.data());
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,203 @@
+"""Pins of the C++ fp64 oracle (oracle/moe_oracle.cpp), on the CPU.
+
+Each step is held to what the pages or the mathematics fix, independently
+of the oracle's own code: the pages' worked examples (the combine of
+"Training a 200B LLM from scratch 5/25", the capacity of "MoE architecture
+revealed" 2.3), brute force on tiny inputs, closed forms, torch and scipy
+routines.  The whole forward is then held to the numpy oracle, itself pinned
+in test_oracle_pins.py: integers bit for bit, floating point to 1e-12.
+"""
+
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import moe_synth as S
+from oracle import cpp
+from oracle import moe_oracle as O
+
+
+def test_capacity_rule():
+    # "MoE architecture revealed" 2.3: batch 1024, top-2, 16 experts -> 128
+    assert cpp.capacity(1024, 2, 16, 1.0) == 128
+    # the workloads' capacities
+    assert cpp.capacity(4096, 2, 16, 1.0) == 512
+    assert cpp.capacity(16384, 2, 64, 1.25) == 640
+    assert cpp.capacity(32768, 2, 16, 1.25) == 5120
+    # no limit, and the floor
+    assert cpp.capacity(300, 2, 7, 0.0) == 300
+    assert cpp.capacity(300, 2, 7, -1.0) == 300
+    assert cpp.capacity(100, 2, 16, 0.1, min_capacity=40) == 40
+    # the exact ceiling of the fp32 factor's rational value
+    rng = np.random.default_rng(3)
+    for _ in range(2000):
+        T, k, E = int(rng.integers(1, 1 << 20)), int(rng.integers(1, 9)), int(rng.integers(1, 1025))
+        cf = np.float32(rng.uniform(0.01, 4.0))
+        ref = math.ceil(Fraction(float(cf)) * T * k / E)
+        assert cpp.capacity(T, k, E, float(cf)) == ref, (T, k, E, float(cf))
+    # a factor whose product lands exactly on an integer, and the extremes
+    assert cpp.capacity(1000, 2, 8, 1.25) == 313  # 312.5 -> 313
+    assert cpp.capacity(640, 2, 5, 1.0) == 256
+    assert cpp.capacity(64, 2, 4, 1e-30) == 1
+    assert cpp.capacity(64, 2, 4, 1e30) == 2 ** 31 - 1
+
+
+def test_combine_worked_example():
+    """0.75 * [0.8, 0.2, -0.4] + 0.25 * [0.4, 0.6, 0.8] = [0.7, 0.3, -0.1]."""
+    out = np.array([[[0.8, 0.2, -0.4], [0.4, 0.6, 0.8]]])
+    y = cpp.combine(out, np.array([[0.75, 0.25]]), np.array([[True, True]]))
+    np.testing.assert_allclose(y, [[0.7, 0.3, -0.1]], rtol=0, atol=1e-15)
+    # a dropped slot adds nothing; the shared expert adds with weight 1
+    y = cpp.combine(out, np.array([[0.75, 0.25]]), np.array([[True, False]]), shared=np.array([[1.0, 2.0, 3.0]]))
+    np.testing.assert_allclose(y, [[1.6, 2.15, 2.7]], rtol=0, atol=1e-15)
+
+
+def _beats(l, a, b):
+    """Expert a precedes b: larger logit, or equal logit and lower index."""
+    return l[a] > l[b] or (l[a] == l[b] and a < b)
+
+
+def test_top_k_brute_force():
+    rng = np.random.default_rng(5)
+    for E, k in ((5, 2), (6, 3), (4, 1), (4, 4)):
+        l = rng.normal(size=(300, E))
+        l[::7, 1] = l[::7, 3]  # exact ties
+        idx, w, nf = cpp.top_k(l, k)
+        assert nf == 0
+        for t in range(l.shape[0]):
+            sel = list(idx[t])
+            # brute force over all k-subsets: the chosen one is the only set
+            # whose every member precedes every other expert
+            ok = [s for s in itertools.combinations(range(E), k)
+                  if all(_beats(l[t], a, b) for a in s for b in range(E) if b not in s)]
+            assert ok == [tuple(sorted(sel))]
+            assert all(_beats(l[t], sel[j], sel[j + 1]) for j in range(k - 1))
+            ref = [math.exp(l[t, e]) for e in sel]
+            np.testing.assert_allclose(w[t], np.array(ref) / sum(ref), rtol=1e-13, atol=0)
+            assert abs(w[t].sum() - 1.0) < 1e-14
+
+
+def test_top_k_ties_and_nonfinite():
+    l = np.array([[1.0, 1.0, 1.0, 1.0], [1.0, 3.0, 3.0, 2.0], [0.0, np.nan, 1.0, 2.0], [np.inf, 0.0, 0.0, 0.0]])
+    idx, w, nf = cpp.top_k(l, 2)
+    assert idx[0].tolist() == [0, 1] and idx[1].tolist() == [1, 2]
+    np.testing.assert_allclose(w[0], [0.5, 0.5], rtol=0, atol=1e-15)
+    assert idx[2].tolist() == [-1, -1] and idx[3].tolist() == [-1, -1] and nf == 2
+    assert not w[2].any() and not w[3].any()
+
+
+def test_router_logits_definition():
+    rng = np.random.default_rng(7)
+    x = torch.tensor(rng.normal(size=(9, 24)), dtype=torch.bfloat16)
+    Wr = torch.tensor(rng.normal(size=(5, 24)), dtype=torch.bfloat16)
+    bias = rng.normal(size=5).astype(np.float32)
+    noise = rng.gumbel(size=(9, 5)).astype(np.float32)
+    l = cpp.router_logits(x, Wr, bias, noise)
+    ref = x.double().numpy() @ Wr.double().numpy().T + bias.astype(np.float64) + noise.astype(np.float64)
+    np.testing.assert_allclose(l, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_capacity_queue_and_positions():
+    """Slot-major queue against a direct simulation: all first choices in
+    token order, then all second choices; each expert takes up to C."""
+    rng = np.random.default_rng(11)
+    T, k, E, C = 500, 3, 7, 160
+    idx = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    idx[rng.random(T) < 0.05] = -1  # unrouted tokens
+    counts = cpp.usage_counts(idx, E)
+    np.testing.assert_array_equal(counts, np.bincount(idx[idx >= 0], minlength=E))
+    rank, fill = cpp.assign_capacity(idx, E, C)
+    queue = {e: [] for e in range(E)}
+    for j in range(k):
+        for t in range(T):
+            if idx[t, j] >= 0:
+                queue[idx[t, j]].append((t, j))
+    for e in range(E):
+        assert fill[e] == min(len(queue[e]), C)
+        for r, (t, j) in enumerate(queue[e]):
+            assert rank[t, j] == (r if r < C else -1)
+    assert (rank[idx < 0] == -1).all()
+    offsets, pos = cpp.dispatch_positions(idx, rank, fill)
+    assert offsets[0] == 0 and (np.diff(offsets) == fill).all()
+    kept = pos >= 0
+    # every kept slot has one row of its expert's block, and rows follow the queue
+    assert sorted(pos[kept].tolist()) == list(range(int(fill.sum())))
+    for e in range(E):
+        rows = [pos[t, j] for t, j in queue[e][:C]]
+        assert rows == list(range(offsets[e], offsets[e + 1]))
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_expert_ffn_against_torch(act):
+    """One expert as torch's fp64 dense FFN (exact-erf GeLU with biases, or
+    SwiGLU), on rows and weights stored in bf16."""
+    g = torch.Generator().manual_seed(13)
+    n, d, h = 11, 40, 56
+    v = torch.randn(n, d, generator=g).to(torch.bfloat16)
+    W1 = (torch.randn(h, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    W3 = (torch.randn(h, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    W2 = (torch.randn(d, h, generator=g) / h ** 0.5).to(torch.bfloat16)
+    b1 = (torch.randn(h, generator=g) * 0.3).to(torch.bfloat16)
+    b2 = (torch.randn(d, generator=g) * 0.3).to(torch.bfloat16)
+    vd, W1d, W3d, W2d, b1d, b2d = (a.double() for a in (v, W1, W3, W2, b1, b2))
+    if act == "gelu":
+        got = cpp.expert_ffn(v, "gelu", W1, W2, b1=b1, b2=b2)
+        ref = torch.nn.functional.gelu(vd @ W1d.T + b1d) @ W2d.T + b2d
+    else:
+        got = cpp.expert_ffn(v, "swiglu", W1, W2, W3=W3)
+        ref = (torch.nn.functional.silu(vd @ W1d.T) * (vd @ W3d.T)) @ W2d.T
+    np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_balance_statistic_and_entropy():
+    from scipy.stats import entropy
+    counts = np.array([30, 10, 0, 24, 16], dtype=np.int64)
+    T, lam = 40, 0.01
+    f = torch.tensor(counts / T, dtype=torch.float64)
+    ref = lam * float(f.std(unbiased=True)) / (float(f.mean()) + 1e-8)
+    assert abs(cpp.balance_stat(counts, T, lam) - ref) <= 1e-15
+    assert cpp.balance_stat(np.array([7], dtype=np.int64), T, lam) == 0.0
+    assert cpp.balance_stat(np.full(4, 9, dtype=np.int64), T, lam) == 0.0
+    rng = np.random.default_rng(17)
+    l = rng.normal(size=(50, 6)) * 2
+    p = np.exp(l - l.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    assert abs(cpp.router_entropy(l) - float(np.mean([entropy(r) for r in p]))) <= 1e-13
+    assert abs(cpp.router_entropy(np.zeros((3, 6))) - math.log(6)) <= 1e-14
+    l[0, 2] = np.nan  # a non-finite token is left out of the mean
+    assert abs(cpp.router_entropy(l) - float(np.mean([entropy(r) for r in p[1:]]))) <= 1e-13
+    assert math.isnan(cpp.router_entropy(np.full((2, 3), np.nan)))
+
+
+LAYERS = [
+    # GeLU in fp32 with biases, no capacity limit
+    S.WORKLOADS["tiny_fp32"].replace(T=40, seed=21),
+    # SwiGLU in bf16 with the shared expert, Gumbel noise and a binding capacity
+    S.WORKLOADS["training"].replace(T=160, d=48, h=64, E=6, capacity_factor=0.7, seed=23),
+    # a skewed router bias and k = 3
+    S.WORKLOADS["small_prefill"].replace(T=150, d=32, h=40, E=5, k=3, capacity_factor=0.9, zipf_s=1.1, seed=29),
+]
+
+
+@pytest.mark.parametrize("wl", LAYERS, ids=lambda w: w.name)
+def test_layer_forward_matches_numpy_oracle(wl):
+    t = S.make_inputs(wl, "cpu")
+    cfg = dict(T=wl.T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act, capacity_factor=float(np.float32(wl.capacity_factor)),
+               min_capacity=wl.min_capacity, lam=0.01, has_shared=wl.has_shared)
+    c = cpp.layer_forward(cfg, t, t["x"], t.get("expert_bias"), t.get("noise"))
+    n = O.layer_forward(cfg, t, t["x"], t.get("expert_bias"), t.get("noise"))
+    for key in ("idx", "counts", "kept", "offsets", "pos"):
+        np.testing.assert_array_equal(c[key], n[key], err_msg=key)
+    np.testing.assert_allclose(c["w"], n["w"], rtol=0, atol=1e-14)
+    scale = max(1.0, float(np.abs(n["y"]).max()))
+    np.testing.assert_allclose(c["y"], n["y"], rtol=0, atol=1e-12 * scale)
+    for key in ("routed_slots", "kept_slots", "dropped_slots", "capacity", "numeric_error"):
+        assert c["stats"][key] == n["stats"][key], key
+    for key in ("drop_rate", "balance_stat", "router_entropy"):
+        assert abs(c["stats"][key] - n["stats"][key]) <= 1e-12 * max(1.0, abs(n["stats"][key])), key
+    if wl.capacity_factor > 0:
+        assert c["stats"]["dropped_slots"] > 0  # capacity binds
