@@ -15,6 +15,7 @@ import torch
 import moe_synth as S
 import sparse_mixture_experts_sum_b300 as M
 from moe_testlib import assert_close_bf16, assert_close_bf16_scaled, guard, guarded_inputs, max_abs, oracle_cfg, to_np
+from oracle import cpp
 from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -78,6 +79,41 @@ def test_tiny_fp32_layer():
     r = O.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"])
     check_routing(r, sv, st, t["x"])
     assert max_abs(to_np(y), r["y"]) <= 1e-4
+    # the C++ oracle, whole layer: routing bit for bit, y to the fp32 bound
+    c = cpp.layer_forward(oracle_cfg(wl), oracle_weights(t), t["x"])
+    for key in ("idx", "counts", "kept", "offsets", "pos"):
+        np.testing.assert_array_equal(sv[key].cpu().numpy(), c[key], err_msg=key)
+    assert max_abs(to_np(y), c["y"]) <= 1e-4
+
+
+def test_small_prefill_against_cpp_oracle():
+    """The small prefill against the single-threaded C++ oracle: its router,
+    top-k, capacity and dispatch bit for bit, and its expert FFN on the
+    first and last 4 rows of every expert (Yp, bf16 bound)."""
+    wl = S.WORKLOADS["small_prefill"]
+    t = guarded_inputs(wl, DEV)
+    y, sv, st = run_layer(wl, t)
+    l = cpp.router_logits(t["x"], t["Wr"], t.get("expert_bias"), t.get("noise"))
+    idx, w, nf = cpp.top_k(l, wl.k)
+    C = cpp.capacity(wl.T, wl.k, wl.E, wl.capacity_factor, wl.min_capacity)
+    rank, kept = cpp.assign_capacity(idx, wl.E, C)
+    offsets, pos = cpp.dispatch_positions(idx, rank, kept)
+    assert nf == 0 and C == st["capacity"] == 512
+    np.testing.assert_array_equal(sv["idx"].cpu().numpy(), idx)
+    np.testing.assert_allclose(sv["w"].cpu().numpy(), w, atol=W_TOL, rtol=0)
+    np.testing.assert_array_equal(sv["counts"].cpu().numpy(), cpp.usage_counts(idx, wl.E))
+    np.testing.assert_array_equal(sv["kept"].cpu().numpy(), kept)
+    np.testing.assert_array_equal(sv["offsets"].cpu().numpy(), offsets)
+    np.testing.assert_array_equal(sv["pos"].cpu().numpy(), pos)
+    assert st["dropped_slots"] > 0  # capacity binds
+    for e in range(wl.E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        rows = sorted(set(range(a, min(a + 4, b))) | set(range(max(a, b - 4), b)))
+        if not rows:
+            continue
+        ix = torch.as_tensor(rows, device=DEV)
+        ref = cpp.expert_ffn(sv["Xp"][ix], wl.act, t["W1"][e], t["W2"][e], W3=t["W3"][e])
+        assert_close_bf16(to_np(sv["Yp"][ix]), ref, f"Yp expert {e}")
 
 
 def test_small_prefill_layer():
