@@ -336,7 +336,9 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
     assert M.moe_check_error(ws) == 0, "a kernel gave up a bounded wait"
 
     peaks = load_peaks()
-    layer_launches = 1 + (2 if wl.dtype == "bf16" else 1) + 4 + 2 + 1
+    # router: one launch (fp32, or the bf16 logits GEMM with its top-k
+    # epilogue up to 64 experts), else the logits GEMM and a top-k kernel
+    layer_launches = 1 + (2 if wl.dtype == "bf16" and wl.E > 64 else 1) + 4 + 2 + 1
     out = {
         "ms_per_step": ms_step,
         "step_ms": percentiles(step_ms),
@@ -345,7 +347,7 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
         "stage_step_ms": percentiles(stage_step_ms),
         "stage_clocks": stage_clocks,
         # our kernels per step of both regions: moe_layer_fwd = zeroing,
-        # router (bf16: logits GEMM + top-k; fp32: one kernel), 4 dispatch
+        # router (one or two launches, above), 4 dispatch
         # (the entropy mean rides in the capacity scan), 2 grouped GEMMs,
         # combine; the stage path = the same plus moe_expert_ffn's zeroing of
         # the error word

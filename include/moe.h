@@ -251,11 +251,13 @@ moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes
  * MOE_ROUTE_REROUTE: each token's experts ranked k .. 2k-1 are also left in
  * ws for moe_dispatch.)
  * ws: NULL, or >= moe_workspace_size(cfg, 1) bytes.  bf16 with ws: the
- * logits run on the tcgen05 tensor cores into the workspace, then a top-k
- * pass; without ws a fused mma.sync kernel (MOE_ROUTE_LAYERNORM and
- * MOE_ROUTE_REROUTE then return MOE_ERR_UNSUPPORTED).  Both sum in a fixed
- * order, so results repeat bit for bit; the two paths may differ in the
- * last bits of l. */
+ * logits run on the tcgen05 tensor cores; up to 64 experts the top-k is
+ * taken in the same kernel's epilogue, else (or with MOE_ROUTE_LAYERNORM or
+ * MOE_ROUTE_REROUTE) the logits go through the workspace to a top-k pass.
+ * Without ws a fused mma.sync kernel (MOE_ROUTE_LAYERNORM and
+ * MOE_ROUTE_REROUTE then return MOE_ERR_UNSUPPORTED).  All sum in a fixed
+ * order, so results repeat bit for bit; the paths may differ in the last
+ * bits of l (and of w and the entropy). */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* Wr,
                      const float* expert_bias, const float* noise, int* idx,
                      float* w, int* counts, float* entropy, void* ws,

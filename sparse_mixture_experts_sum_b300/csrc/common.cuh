@@ -60,6 +60,98 @@ __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f,
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // ---------------------------------------------------------------------------
+// router top-k, shared by the router kernels and the GEMM's top-k epilogue
+// ---------------------------------------------------------------------------
+constexpr int MAXK = 8;  // the largest k
+
+// Insert (val, e) into a descending top-k list; equal values keep the
+// earlier (lower) index first because experts arrive in increasing order.
+__device__ __forceinline__ void topk_insert(float (&v)[MAXK], int (&ix)[MAXK], int k, float val, int e) {
+#pragma unroll
+  for (int p = MAXK - 1; p > 0; --p) {
+    if (p < k) {
+      if (val > v[p - 1]) {
+        v[p] = v[p - 1];
+        ix[p] = ix[p - 1];
+      } else if (val > v[p]) {
+        v[p] = val;
+        ix[p] = e;
+      }
+    }
+  }
+  if (val > v[0]) {
+    v[0] = val;
+    ix[0] = e;
+  }
+}
+
+// Running softmax statistics over a token's logits (any order):
+//   m = max l,  Z = sum exp(l - m),  S = sum exp(l - m) (l - m),
+// so that p_e = exp(l_e - m) / Z and the entropy -sum p ln p = ln Z - S/Z.
+struct SoftStat {
+  float m, Z, S;
+  __device__ __forceinline__ SoftStat() : m(-INFINITY), Z(0.f), S(0.f) {}
+  __device__ __forceinline__ void add(float v) { merge(v, 1.f, 0.f); }
+  __device__ __forceinline__ void merge(float m2, float Z2, float S2) {
+    if (Z2 == 0.f) return;
+    if (Z == 0.f) {
+      m = m2;
+      Z = Z2;
+      S = S2;
+      return;
+    }
+    if (m2 > m) {
+      const float sc = expf(m - m2);
+      S = sc * (S + (m - m2) * Z) + S2;
+      Z = sc * Z + Z2;
+      m = m2;
+    } else {
+      const float sc = expf(m2 - m);
+      S += sc * (S2 + (m2 - m) * Z2);
+      Z += sc * Z2;
+    }
+  }
+  __device__ __forceinline__ float entropy() const { return logf(Z) - S / Z; }
+};
+
+// Weights, indices, entropy and histogram of one token from its sorted
+// top-k (v descending, ix).  raw: w_j = p_{ix_j} from the softmax over all
+// experts (st holds its statistics); otherwise the softmax over the k
+// selected logits.  ent (nullable) receives the token's router entropy (NaN
+// for a token with a non-finite logit, which is routed nowhere).
+__device__ __forceinline__ void topk_finish(const float (&v)[MAXK], const int (&ix)[MAXK], int k, bool finite,
+                                            int t, int* idx, float* w, int* hist, bool raw, const SoftStat& st,
+                                            float* ent) {
+  if (!finite) {
+    for (int j = 0; j < k; ++j) {
+      idx[static_cast<size_t>(t) * k + j] = -1;
+      w[static_cast<size_t>(t) * k + j] = 0.f;
+    }
+    if (ent) ent[t] = __int_as_float(0x7fc00000);
+    return;
+  }
+  float ex[MAXK];
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXK; ++j) {
+    if (j < k) {
+      ex[j] = expf(v[j] - (raw ? st.m : v[0]));
+      s += ex[j];
+    }
+  }
+  const float inv = 1.0f / (raw ? st.Z : s);
+#pragma unroll
+  for (int j = 0; j < MAXK; ++j) {
+    if (j < k) {
+      idx[static_cast<size_t>(t) * k + j] = ix[j];
+      w[static_cast<size_t>(t) * k + j] = ex[j] * inv;
+      atomicAdd(&hist[ix[j]], 1);
+    }
+  }
+  if (ent) ent[t] = st.entropy();
+}
+
+// ---------------------------------------------------------------------------
 // programmatic dependent launch (kernels launched by launch_pdl)
 // ---------------------------------------------------------------------------
 // Lets the next kernel in the stream be scheduled now; it still waits for
@@ -191,6 +283,13 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// 32 lanes x 4 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).

@@ -97,6 +97,7 @@ struct __align__(8) Ctl {
   int x_tile0;  // first tile of the extra group (= tiles of the routed groups)
   int grp_row[MAX_GROUPS + 1];     // first row of each group (+ end)
   int tile_start[MAX_GROUPS + 1];  // first tile of each group (+ total)
+  int hist[256];                   // kModeRouteTopK: this CTA's selections per expert
 };
 
 template <int BM_, bool PAIR = false>
@@ -242,6 +243,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     tma_prefetch_desc(&mapB0);
     tma_prefetch_desc(&mapB1);
   }
+  if (KIND == kKindFwd && p.mode == kModeRouteTopK)
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) c.hist[i] = 0;
   if (warp == 1) {
     if constexpr (PAIR) {
       tmem_alloc_pair(&c.tmem_base, TMEM_COLS);
@@ -611,7 +614,80 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         const long long row_end = xg ? static_cast<long long>(gend) : min(static_cast<long long>(gend), p.rows_alloc);
         const int row = grow + t.m * TM + static_cast<int>(crank) * BM + rt;
         const bool valid = row < row_end;
-        if (swiglu_fwd) {
+        if (KIND == kKindFwd && BM == 128 && !PAIR && p.mode == kModeRouteTopK) {
+          // (the launcher runs this mode on single-CTA 128-row tiles only)
+          // the router: this thread's token's E logits, 4 columns at a time
+          // (a small loop body: the thread walks all E alone).  Pass 1 adds
+          // bias and noise, checks finiteness and keeps a descending top-k
+          // (experts in increasing order, so an equal value keeps the lower
+          // index) and the max m; pass 2 (raw weights or the entropy) sums
+          // exp(l - m) and exp(l - m) (l - m).
+          const RouteEpilogue& R = p.route;
+          float sv[MAXK];
+          int si[MAXK];
+#pragma unroll
+          for (int j = 0; j < MAXK; ++j) {
+            sv[j] = -INFINITY;
+            si[j] = -1;
+          }
+          bool finite = true;
+          float m = -INFINITY;
+          const float* nrow = R.noise && valid ? R.noise + static_cast<size_t>(row) * R.E : nullptr;
+          float* lrow = R.logits && valid ? R.logits + static_cast<size_t>(row) * R.E : nullptr;
+          auto logit = [&](uint32_t raw_bits, int e) {
+            float a = __uint_as_float(raw_bits);
+            if (R.bias) a += R.bias[e];
+            if (nrow) a += nrow[e];
+            return a;
+          };
+          const int nq = (R.E + 3) / 4;
+#pragma unroll 1
+          for (int q = 0; q < nq; ++q) {
+            uint32_t r[4];
+            tmem_ld_32x32b_x4(taddr + q * 4, r);
+            tmem_ld_wait();
+            if (!valid) continue;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int e = q * 4 + i;
+              if (e < R.E) {
+                const float a = logit(r[i], e);
+                if (!isfinite(a)) finite = false;
+                if (lrow) lrow[e] = a;
+                topk_insert(sv, si, R.k, a, e);
+                m = fmaxf(m, a);
+              }
+            }
+          }
+          SoftStat st;
+          // tcgen05.ld is warp-collective: the whole warp runs this pass
+          // (the condition is the same for every lane); a row that is past
+          // the end or not finite only skips the sums
+          if (R.raw || R.ent) {
+            float z = 0.f, sz = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < nq; ++q) {
+              uint32_t r[4];
+              tmem_ld_32x32b_x4(taddr + q * 4, r);
+              tmem_ld_wait();
+              if (!valid || !finite) continue;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int e = q * 4 + i;
+                if (e < R.E) {
+                  const float dv = logit(r[i], e) - m;
+                  const float ex = expf(dv);
+                  z += ex;
+                  sz = fmaf(ex, dv, sz);
+                }
+              }
+            }
+            st.m = m;
+            st.Z = z;
+            st.S = sz;
+          }
+          if (valid) topk_finish(sv, si, R.k, finite, row, R.idx, R.w, c.hist, R.raw != 0, st, R.ent);
+        } else if (swiglu_fwd) {
           bf16* orow = static_cast<bf16*>(out_p) + static_cast<size_t>(row) * p.ldo;
           // the pre-activations are kept in fp32 for the backward: a bf16
           // copy would put a 2^-9 rounding inside silu'(gate) and up there
@@ -759,6 +835,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
 
   tc_fence_before();
   __syncthreads();
+  if (KIND == kKindFwd && p.mode == kModeRouteTopK)
+    for (int e = threadIdx.x; e < p.route.E; e += blockDim.x)
+      if (c.hist[e]) atomicAdd(&p.route.counts[e], c.hist[e]);
   // PAIR: neither CTA leaves (or frees its TMEM) while the other may still
   // signal its barriers or the MMAs may still read its shared memory
   if constexpr (PAIR) cluster_sync();
@@ -870,7 +949,7 @@ moe_status launch_geometry(const GemmParams& p, const void* A, long long a_rows,
   const int sms = device_sm_count(dev);
   const bool pair = KIND == kKindFwd && p.cta_pairs && avg_rows >= 256 && (p.mode == kModeSwiGLU || p.N >= BN) &&
                     2 * tiles_for(256) >= sms;
-  const bool light = p.mode == kModePlain || KIND == kKindFwd;
+  const bool light = p.mode == kModePlain || (KIND == kKindFwd && p.mode != kModeRouteTopK);
   const bool tall = !pair && avg_rows >= 256 && light && tiles_for(256) >= sms;
   CUtensorMap mA, mB0, mB1, mXA, mXB0, mXB1;  // Fwd/Dgrad A boxes: 128 rows (two per 256-row tile)
   const long long tiles = tiles_for(pair || tall ? 256 : 128);
@@ -918,7 +997,8 @@ moe_status launch_grouped_gemm_tc(const GemmParams& p_in, int kind, const void* 
   if (p.xrows == 0) extra = nullptr;
   p.rows_alloc = a_rows;
   if (p.ldo == 0) p.ldo = p.N;
-  if (p.G < 1 || p.G > MAX_GROUPS || p.N < 8 || (p.N % 8) || !p.out) return MOE_ERR_UNSUPPORTED;
+  if (p.G < 1 || p.G > MAX_GROUPS || p.N < 8 || (p.N % 8) || (!p.out && p.mode != kModeRouteTopK))
+    return MOE_ERR_UNSUPPORTED;
   if (a_rows <= 0) return MOE_OK;
   if (a_rows > 2147483647LL || b_rows > 2147483647LL) return MOE_ERR_UNSUPPORTED;
   // output rows per group on average (Wgrad: M, the same for every group)
@@ -926,6 +1006,13 @@ moe_status launch_grouped_gemm_tc(const GemmParams& p_in, int kind, const void* 
   if (kind == kKindFwd) {
     if (p.K < 8 || (p.K % 8)) return MOE_ERR_UNSUPPORTED;
     if (p.mode == kModeSwiGLUBwd || p.mode == kModeGeLUBwd) return MOE_ERR_UNSUPPORTED;
+    if (p.mode == kModeRouteTopK) {
+      // one group of T rows, all E logits in one 256-column tile
+      const RouteEpilogue& R = p.route;
+      if (p.offsets || p.G != 1 || p.xrows || p.cta_pairs || p.N > BN || R.E < 1 || R.E > p.N || R.k < 1 ||
+          R.k > MAXK || R.k > R.E || !R.idx || !R.w || !R.counts)
+        return MOE_ERR_INVALID_ARG;
+    }
     return launch_geometry<kKindFwd>(p, A, a_rows, B0, B1, b_rows, avg_rows, extra, stream);
   }
   if (kind == kKindDgrad) {

@@ -68,6 +68,27 @@ enum GemmMode : int {
   kModeSwiGLUBwd = 3,  // g = zin[r,n], u = zin[r,N+n]: out[r,n] = dH*u*silu'(g), out[r,N+n] = dH*silu(g);
                        // hout + hout_lo = s*silu(g)*u
   kModeGeLUBwd = 4,    // out = dH * gelu'(zin[r,n]); hout + hout_lo = s*gelu(zin[r,n])
+  // Fwd, one group of T rows, N = E (<= 256): the router.  Row t's logits
+  // l = acc (+ r_bias) (+ r_noise[t]) go through the top-k in the epilogue
+  // (value desc, index asc); out is not written
+  kModeRouteTopK = 5,
+};
+
+// The router's top-k epilogue (kModeRouteTopK): idx/w [T, k]; counts [E]
+// gets each expert's selections added (atomics); ent [T] the entropy of the
+// softmax over all E (nullable); logits [T, E] the final logits (nullable);
+// raw: w = the selected entries of that softmax instead of the softmax over
+// the k selected logits.  A token with a non-finite logit gets idx -1, w 0,
+// entropy NaN.
+struct RouteEpilogue {
+  const float* bias;   // [E] nullable
+  const float* noise;  // [T, E] nullable
+  int* idx;
+  float* w;
+  int* counts;
+  float* ent;
+  float* logits;
+  int E, k, raw;
 };
 
 // Operand geometry of a grouped GEMM launch.
@@ -113,6 +134,7 @@ struct GemmParams {
   void* xout;
   void* xzsave;
   const void* xbias;
+  RouteEpilogue route;  // kModeRouteTopK
 };
 
 // Operands of the extra group of a Fwd launch.

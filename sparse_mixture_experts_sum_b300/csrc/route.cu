@@ -35,98 +35,10 @@
 namespace moe {
 namespace {
 
-constexpr int MAXK = 8;
 constexpr int RT_TM = 64;         // tokens per CTA
 constexpr int RT_NE = 128;        // experts per chunk
 constexpr int RT_BK = 64;         // k per stage
 constexpr int RT_LD = RT_BK + 8;  // padded smem row (bf16): conflict-free fragment loads
-
-// Insert (val, e) into a descending top-k list; equal values keep the
-// earlier (lower) index first because experts arrive in increasing order.
-__device__ __forceinline__ void topk_insert(float (&v)[MAXK], int (&ix)[MAXK], int k, float val, int e) {
-#pragma unroll
-  for (int p = MAXK - 1; p > 0; --p) {
-    if (p < k) {
-      if (val > v[p - 1]) {
-        v[p] = v[p - 1];
-        ix[p] = ix[p - 1];
-      } else if (val > v[p]) {
-        v[p] = val;
-        ix[p] = e;
-      }
-    }
-  }
-  if (val > v[0]) {
-    v[0] = val;
-    ix[0] = e;
-  }
-}
-
-// Running softmax statistics over a token's logits (any order):
-//   m = max l,  Z = sum exp(l - m),  S = sum exp(l - m) (l - m),
-// so that p_e = exp(l_e - m) / Z and the entropy -sum p ln p = ln Z - S/Z.
-struct SoftStat {
-  float m, Z, S;
-  __device__ __forceinline__ SoftStat() : m(-INFINITY), Z(0.f), S(0.f) {}
-  __device__ __forceinline__ void add(float v) { merge(v, 1.f, 0.f); }
-  __device__ __forceinline__ void merge(float m2, float Z2, float S2) {
-    if (Z2 == 0.f) return;
-    if (Z == 0.f) {
-      m = m2;
-      Z = Z2;
-      S = S2;
-      return;
-    }
-    if (m2 > m) {
-      const float sc = expf(m - m2);
-      S = sc * (S + (m - m2) * Z) + S2;
-      Z = sc * Z + Z2;
-      m = m2;
-    } else {
-      const float sc = expf(m2 - m);
-      S += sc * (S2 + (m2 - m) * Z2);
-      Z += sc * Z2;
-    }
-  }
-  __device__ __forceinline__ float entropy() const { return logf(Z) - S / Z; }
-};
-
-// Weights, indices, entropy and histogram of one token from its sorted
-// top-k (v descending, ix).  raw: w_j = p_{ix_j} from the softmax over all
-// experts (st holds its statistics); otherwise the softmax over the k
-// selected logits.  ent (nullable) receives the token's router entropy (NaN
-// for a token with a non-finite logit, which is routed nowhere).
-__device__ __forceinline__ void topk_finish(const float (&v)[MAXK], const int (&ix)[MAXK], int k, bool finite,
-                                            int t, int* idx, float* w, int* hist, bool raw, const SoftStat& st,
-                                            float* ent) {
-  if (!finite) {
-    for (int j = 0; j < k; ++j) {
-      idx[static_cast<size_t>(t) * k + j] = -1;
-      w[static_cast<size_t>(t) * k + j] = 0.f;
-    }
-    if (ent) ent[t] = __int_as_float(0x7fc00000);
-    return;
-  }
-  float ex[MAXK];
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < MAXK; ++j) {
-    if (j < k) {
-      ex[j] = expf(v[j] - (raw ? st.m : v[0]));
-      s += ex[j];
-    }
-  }
-  const float inv = 1.0f / (raw ? st.Z : s);
-#pragma unroll
-  for (int j = 0; j < MAXK; ++j) {
-    if (j < k) {
-      idx[static_cast<size_t>(t) * k + j] = ix[j];
-      w[static_cast<size_t>(t) * k + j] = ex[j] * inv;
-      atomicAdd(&hist[ix[j]], 1);
-    }
-  }
-  if (ent) ent[t] = st.entropy();
-}
 
 // Backup experts of a token for rerouting on overflow: its entries k .. kk-1
 // of the sorted list (kk <= 2k), -1 past kk or for a non-finite token.
@@ -579,6 +491,14 @@ moe_status launch_route_stages(const moe_config& cfg, const void* x, const void*
 // Row stride of the fp32 logits on the tensor-core path: E rounded up to
 // the GEMM's 8-column granule (columns past E hold the logits of zero
 // weight rows and are never read).
+// The largest E whose top-k runs in the logits GEMM's epilogue.  There one
+// thread walks its token's E logits alone, against a warp per token in
+// route_topk_kernel: measured per router call, the epilogue wins at E = 16
+// (small prefill 23.4 -> 21.0 us, training 79.9 -> 66.0 us) and ties at
+// E = 64 (large prefill 52.2 -> 51.5 us), but loses at E = 128 (decode, 64
+// tokens: 34.0 -> 55.5 us).
+constexpr int kRouteFuseMaxE = 64;
+
 int logit_ld(const moe_config& cfg) { return cfg.E < 8 ? 8 : (cfg.E + 7) / 8 * 8; }
 
 }  // namespace
@@ -601,10 +521,26 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
   if (out_logits && !(cfg.dtype == MOE_BF16 && scratch)) return MOE_ERR_UNSUPPORTED;  // top-k kernel path only
   moe_status zs = launch_zero(counts, sizeof(int) * cfg.E, err, err ? sizeof(int) : 0, stream);
   if (zs != MOE_OK) return zs;
+  if (cfg.dtype == MOE_BF16 && scratch && !ln && !backup && cfg.E <= kRouteFuseMaxE && cfg.k <= MAXK) {
+    // logits = x . Wr^T on the tcgen05 grouped GEMM (one group of T rows,
+    // N = E rounded up to 8; the TMA box reads zeros past row E), and the
+    // top-k in its epilogue: each thread holds one token's logits in TMEM,
+    // so no logit goes through HBM
+    GemmParams g{};
+    g.G = 1;
+    g.rows = cfg.T;
+    g.N = logit_ld(cfg);
+    g.K = cfg.d;
+    g.mode = kModeRouteTopK;
+    g.err = err;
+    g.route = RouteEpilogue{expert_bias, noise, idx, w, counts, ent, out_logits, cfg.E, cfg.k, raw};
+    return launch_grouped_gemm_tc(g, kKindFwd, x, cfg.T, Wr, nullptr, cfg.E, stream);
+  }
   if (cfg.dtype == MOE_BF16 && scratch) {
     // logits = x . Wr^T on the tcgen05 grouped GEMM (one group of T rows,
     // N = E rounded up to 8, fp32 out; the TMA box reads zeros past row E),
-    // then the top-k per token
+    // then the top-k per token (a LayerNorm in front, backups for rerouting,
+    // or more than kRouteFuseMaxE experts)
     const int ld = logit_ld(cfg);
     float* logits = static_cast<float*>(scratch);
     float* S = ln ? logits + static_cast<size_t>(cfg.T) * ld : nullptr;

@@ -571,11 +571,15 @@ def test_expert_ffn_shared_matches_oracle(act):
 
 
 @pytest.mark.parametrize("T,d,E,k", [(64, 4096, 128, 2), (200, 1024, 130, 4), (1000, 512, 384, 6),
-                                     (4500, 1024, 64, 2), (300, 256, 5, 3)])
+                                     (4500, 1024, 64, 2), (300, 256, 5, 3), (1000, 256, 64, 8),
+                                     (600, 128, 65, 4)])
 def test_route_with_workspace(T, d, E, k):
     """With a workspace the logits run on the tcgen05 GEMM (E = 130 and 5
-    pad the logit rows to 136 and 8 columns) and a warp per token takes the
-    top-k: same routing as the oracle, and the same bits on a second run."""
+    pad the logit rows to 136 and 8 columns).  Up to 64 experts the GEMM's
+    epilogue takes the top-k of each token's row in TMEM (E = 5, and E = 64
+    with k = 2 and 8); beyond, a warp per token takes it from the logits in
+    the workspace (E = 65, 128, 130, 384).  Same routing as the oracle
+    either way, and the same bits on a second run."""
     from moe_testlib import guard
     wl = S.WORKLOADS["small_prefill"].replace(T=T, d=d, E=E, k=k, seed=19)
     t = S.make_inputs(wl, "cpu", parts=["x", "Wr"])
