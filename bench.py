@@ -337,8 +337,11 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
 
     peaks = load_peaks()
     # router: one launch (fp32, or the bf16 logits GEMM with its top-k
-    # epilogue up to 64 experts), else the logits GEMM and a top-k kernel
-    layer_launches = 1 + (2 if wl.dtype == "bf16" and wl.E > 64 else 1) + 4 + 2 + 1
+    # epilogue up to 64 experts), else the logits GEMM and a top-k kernel;
+    # dispatch: one fused kernel + the permute for up to 4096 slots and 128
+    # experts, else histogram, scan, assignment + the permute
+    small = wl.T * wl.k <= 4096 and wl.E <= 128
+    layer_launches = 1 + (2 if wl.dtype == "bf16" and wl.E > 64 else 1) + (2 if small else 4) + 2 + 1
     out = {
         "ms_per_step": ms_step,
         "step_ms": percentiles(step_ms),
@@ -347,7 +350,7 @@ def run_gpu(args, wl_name, world, rank, local, main=True):
         "stage_step_ms": percentiles(stage_step_ms),
         "stage_clocks": stage_clocks,
         # our kernels per step of both regions: moe_layer_fwd = zeroing,
-        # router (one or two launches, above), 4 dispatch
+        # router and dispatch (above)
         # (the entropy mean rides in the capacity scan), 2 grouped GEMMs,
         # combine; the stage path = the same plus moe_expert_ffn's zeroing of
         # the error word

@@ -434,10 +434,14 @@ def test_route_shapes(T, d, E, k):
     np.testing.assert_array_equal(counts.cpu().numpy(), O.usage_counts(ridx, E))
 
 
-@pytest.mark.parametrize("T,E,k,cf,minc", [(3000, 6, 3, 0.5, 0), (513, 5, 2, 0.1, 40), (9000, 16, 2, 1.0, 0)])
+@pytest.mark.parametrize("T,E,k,cf,minc", [(3000, 6, 3, 0.5, 0), (513, 5, 2, 0.1, 40), (9000, 16, 2, 1.0, 0),
+                                            (2048, 128, 2, 0.7, 0)])
 def test_dispatch_capacity_exact(T, E, k, cf, minc):
     """Capacity binds hard (skewed router bias); positions must equal the
-    oracle's slot-major queue exactly, across several 4096-slot chunks."""
+    oracle's slot-major queue exactly.  Up to 4096 slots and 128 experts the
+    histogram, scan and placement run in one CTA (1026 slots; 4096 slots in
+    exactly four chunks with E = 128); larger batches use the three chunk
+    kernels (9000 and 18000 slots)."""
     wl = S.WORKLOADS["small_prefill"].replace(T=T, d=64, h=64, E=E, k=k, capacity_factor=cf,
                                               min_capacity=minc, seed=13)
     t = S.make_inputs(wl, "cpu", parts=["x", "Wr"])
