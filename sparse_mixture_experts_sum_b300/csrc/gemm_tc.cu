@@ -17,7 +17,8 @@
 // no transposed copy of any weight is made.  Its K range may be split
 // between two weight tensors (dXp = dA.W1 + dB.W3 with A = [dA | dB]).
 //
-// Design (one persistent CTA per SM, 192 threads):
+// Design (one persistent CTA per SM; the 128-row tile shown, TileCfg below
+// has the 256-row and CTA-pair forms):
 //   warp 0  : TMA producer -- A tile 128x64 and B tile 256x64 (bf16, 128-byte
 //             swizzle) per k-block into a 4-stage shared-memory ring;
 //   warp 1  : owns 512 TMEM columns; one lane issues tcgen05.mma
@@ -27,7 +28,10 @@
 //   warps 2-5: epilogue -- tcgen05.ld the accumulator, apply the epilogue
 //             mode, store the rows / columns inside the output.
 // Accumulators are double-buffered so the epilogue of tile i overlaps the
-// MMAs of tile i+1.  The tile list is derived on the device from offsets[],
+// MMAs of tile i+1.  Every launch is a programmatic dependent launch: the
+// barrier and TMEM set-up runs before griddepcontrol.wait, and the producer
+// lets the next kernel be scheduled once its last load is issued.  The tile
+// list is derived on the device from offsets[],
 // so no host round-trip is needed for the data-dependent per-expert row
 // counts.  Fwd/Dgrad tiles run m fastest, so the CTAs running together share
 // each weight tile through L2; Wgrad tiles run along the smaller of M and N
@@ -35,7 +39,8 @@
 //
 // Epilogue modes (GemmMode): plain (+bias), SwiGLU (B rows [0,128) from W1
 // and [128,256) from W3 at the same 128 output columns: silu(gate) * up),
-// GeLU (gelu(acc + bias)), and the backward of both activations.  The
+// GeLU (gelu(acc + bias)), the backward of both activations, and the
+// router's top-k (each thread takes its token's logits from TMEM).  The
 // forward saves the pre-activations in fp32; the backward reads them, scales
 // the accumulator by the row's routing weight (so the GEMM contracts the
 // upstream gradient rows as stored, not a rounded weighted copy) and can
