@@ -150,6 +150,7 @@ moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, cons
   g1.ldz = swiglu ? 2LL * cfg->h : cfg->h;
   g1.bias = swiglu ? nullptr : b1;
   g1.err = err;
+  g1.sched = err ? err + 1 : nullptr;
   g1.cta_pairs = (cfg->gemm_flags & MOE_GEMM_CTA_PAIRS) != 0;
   GemmParams g2 = g1;
   g2.N = cfg->d;
@@ -222,6 +223,7 @@ moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offse
   a.hout = Hw;
   a.hout_lo = Hw_lo;
   a.err = err;
+  a.sched = err ? err + 1 : nullptr;
   moe_status s = launch_grouped_gemm_tc(a, kKindDgrad, dYg, a_rows, W2, nullptr, static_cast<long long>(G) * d, st);
   if (s != MOE_OK) return s;
   // dXin = dA . W1_g + dB . W3_g  (fp32)
@@ -236,6 +238,7 @@ moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offse
   b.out_f32 = 1;
   b.out = dXin;
   b.err = err;
+  b.sched = err ? err + 1 : nullptr;
   s = launch_grouped_gemm_tc(b, kKindDgrad, dAB, a_rows, W1, swiglu ? W3 : nullptr, static_cast<long long>(G) * h,
                              st);
   if (s != MOE_OK) return s;
@@ -251,6 +254,7 @@ moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offse
   c.out = dW2;
   c.b_lo = 1;
   c.err = err;
+  c.sched = err ? err + 1 : nullptr;
   s = launch_grouped_gemm_tc(c, kKindWgrad, dYg, a_rows, Hw, Hw_lo, a_rows, st);
   if (s != MOE_OK) return s;
   // [dW1; dW3]_g = [dA | dB]_g^T . Xin_g
@@ -266,6 +270,7 @@ moe_status run_ffn_bwd(const moe_config* cfg, long long a_rows, const int* offse
   w.out = dW1;
   w.out2 = swiglu ? dW3 : nullptr;
   w.err = err;
+  w.sched = err ? err + 1 : nullptr;
   s = launch_grouped_gemm_tc(w, kKindWgrad, dAB, a_rows, Xin, nullptr, a_rows, st);
   if (s != MOE_OK) return s;
   if (!swiglu) {
@@ -383,7 +388,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* Xp, const int* offs
     return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
-  if (launch_zero(err, sizeof(int), nullptr, 0, st) != MOE_OK) return MOE_ERR_CUDA;
+  if (launch_zero(err, kWsZeroBytes, nullptr, 0, st) != MOE_OK) return MOE_ERR_CUDA;
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
   return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, W1, W3, b1, W2, b2, H, Yp, nullptr, err, st);
 }
@@ -402,7 +407,7 @@ moe_status moe_expert_ffn_shared(const moe_config* cfg, const void* Xp, const in
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
-  if (launch_zero(err, sizeof(int), nullptr, 0, st) != MOE_OK) return MOE_ERR_CUDA;
+  if (launch_zero(err, kWsZeroBytes, nullptr, 0, st) != MOE_OK) return MOE_ERR_CUDA;
   const long long a_rows = static_cast<long long>(cfg->T) * cfg->k;
   SharedFfn sh{x, wts, Hs, Sx, nullptr};
   return run_ffn(cfg, Xp, a_rows, offsets, cfg->E, 0, wts->W1, wts->W3, wts->b1, wts->W2, wts->b2, H, Yp, nullptr,
@@ -518,7 +523,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* wts, const vo
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
-  s = launch_zero(err, sizeof(int), at(ws, L.imp), sizeof(unsigned long long) * cfg->E, st);
+  s = launch_zero(err, kWsZeroBytes, at(ws, L.imp), sizeof(unsigned long long) * cfg->E, st);
   if (s != MOE_OK) return s;
   void* dYg = at(ws, L.dYg);
   float* wp = static_cast<float*>(at(ws, L.wp));

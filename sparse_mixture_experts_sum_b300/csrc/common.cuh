@@ -16,9 +16,13 @@ namespace moe {
 typedef __nv_bfloat16 bf16;
 
 // ---------------------------------------------------------------------------
-// workspace layout: the first 256 bytes hold the error word
+// workspace layout: the first 256 bytes are a header.  Word 0 is the error
+// word; words 1-2 are the grouped GEMM's dynamic tile scheduler (the next
+// tile to hand out, the CTAs finished), which every launch leaves at zero.
+// Each entry point zeroes the first kWsZeroBytes before its first launch.
 // ---------------------------------------------------------------------------
 constexpr size_t kWsHeader = 256;
+constexpr size_t kWsZeroBytes = 3 * sizeof(int);
 
 // error codes written by bounded waits (nonzero = a wait gave up)
 enum : int {

@@ -61,6 +61,7 @@ constexpr int B_HALF_BYTES = 128 * BK * 2;   // 16 KB
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN block of 64 K rows: 8 KB
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_GROUPS = 1024;
+constexpr int SCHED_DEPTH = 8;  // tiles the producer may hand out ahead of the last epilogue warp
 
 // Tile shape per BM (output rows per CTA) and PAIR:
 //   BM = 128: 4-stage ring of 48 KB, two 128x256 accumulators (the epilogue
@@ -96,6 +97,12 @@ struct __align__(8) Ctl {
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
+  // dynamic schedule: the producer writes the tile of its j-th turn to
+  // sched_tile[j % SCHED_DEPTH] and arrives on sched_full; the MMA warp and
+  // each epilogue warp read it and arrive on sched_empty
+  uint64_t sched_full[SCHED_DEPTH];
+  uint64_t sched_empty[SCHED_DEPTH];
+  int sched_tile[SCHED_DEPTH];
   uint32_t tmem_base;
   int abort;
   int total_tiles;
@@ -241,6 +248,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
       mbar_init(&c.tmem_empty[a], PAIR ? 2 * TC::EPI_WARPS : 32 * TC::EPI_WARPS);
     }
     mbar_init(&c.drain, 1);
+    for (int q = 0; q < SCHED_DEPTH; ++q) {
+      mbar_init(&c.sched_full[q], 1);
+      mbar_init(&c.sched_empty[q], 1 + TC::EPI_WARPS);
+    }
     c.abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -302,12 +313,57 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
 
   const int total = c.total_tiles;
   const uint32_t tmem_base = c.tmem_base;
+  // Dynamic schedule, for the launches whose tiles differ in cost (256-row
+  // tiles, where a group's last tile may be a half tile; Wgrad, where a
+  // tile's k-blocks are its group's rows), given the scheduler words: a
+  // CTA's first tile is its block index, and each further one comes from a
+  // counter in the workspace (tiles gridDim.x, gridDim.x + 1, ... in order).
+  // A CTA whose tiles ran short takes more of them, while the tiles in
+  // flight at any time stay neighbours in the order above and share their
+  // weight tiles through L2.  Otherwise CTA b runs tiles b, b + tstep, ...
+  // (equal tiles gain nothing from the counter's round trips).
+  const bool dyn = !PAIR && (BM == 256 || KIND == kKindWgrad) && p.sched != nullptr;
+  // a consumer warp's tile for its j-th turn (warp-uniform); total once the
+  // schedule has ended, or when the wait gave up (the abort flag is then set)
+  auto take_tile = [&](uint32_t j, int err_code) -> int {
+    if (!dyn) return tile0 + static_cast<int>(j) * tstep;
+    const uint32_t q = j % SCHED_DEPTH;
+    int tile = total;
+    if (lane == 0) {
+      if (mbar_wait(&c.sched_full[q], (j / SCHED_DEPTH) & 1u)) {
+        tile = c.sched_tile[q];
+        mbar_arrive(&c.sched_empty[q]);
+      } else {
+        record_error(p.err, err_code);
+        *abort_flag = 1;
+      }
+    }
+    return __shfl_sync(0xffffffffu, tile, 0);
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       uint32_t it = 0;
-      for (int tile = tile0; tile < total && !*abort_flag; tile += tstep) {
+      int next = tile0;
+      for (uint32_t j = 0; !*abort_flag; ++j) {
+        const int tile = next < total ? next : total;
+        if (dyn) {
+          // fetch the tile after this one now, so that its latency hides
+          // behind this tile's loads; then hand this one to the consumers
+          if (tile < total) next = static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
+          const uint32_t q = j % SCHED_DEPTH;
+          if (!mbar_wait(&c.sched_empty[q], ((j / SCHED_DEPTH) & 1u) ^ 1u)) {
+            record_error(p.err, kErrWaitProducer);
+            *abort_flag = 1;
+            break;
+          }
+          c.sched_tile[q] = tile;
+          mbar_arrive(&c.sched_full[q]);
+        } else {
+          next = tile + tstep;
+        }
+        if (tile >= total) break;
         const Tile t = tile_coords<KIND, TM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
         const bool xg = KIND == kKindFwd && t.g == G;  // the extra group
         const int grow = xg ? 0 : c.grp_row[t.g];
@@ -393,6 +449,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
           }
         }
       }
+      if (dyn) {
+        // this CTA fetches no more tiles (on every way out of the loop): the
+        // last CTA to get here leaves the scheduler words at zero for the
+        // next launch, while its MMAs and epilogue still run
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+          atomicExch(p.sched, 0);
+          atomicExch(p.sched + 1, 0);
+        }
+      }
       // every load of this CTA is issued: the next kernel in the stream may
       // be scheduled (its CTAs wait in pdl_wait() until this grid completes)
       pdl_trigger();
@@ -471,11 +537,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     // that are never stored
     const int n_mma = (p.N < BN && !swiglu_fwd) ? ((p.N + 15) / 16) * 16 : BN;
     const uint32_t IDESC = idesc_bf16_f32(128, n_mma, KIND == kKindWgrad ? 1 : 0, KIND == kKindFwd ? 0 : 1);
-    uint32_t it = 0, local = 0;
+    uint32_t it = 0;
     bool issued = false;
-    for (int tile = tile0; tile < total; tile += tstep, ++local) {
+    for (uint32_t local = 0;; ++local) {
       // one read of the abort flag for the whole warp keeps its lanes together
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const int tile = take_tile(local, kErrWaitMma);
+      if (tile >= total) break;
       const Tile t = tile_coords<KIND, TM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
       const int grows = KIND == kKindWgrad ? c.grp_row[t.g + 1] - c.grp_row[t.g] : 0;
       const int nk1 = KIND == kKindWgrad ? (grows + BK - 1) / BK : nk_fixed;
@@ -568,10 +636,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;          // TMEM lanes [32*quarter, 32*quarter+32)
     const int half = (warp - 2) >> 2;      // BM = 256: accumulator rows 128*half.. (columns 256*half..)
-    uint32_t local = 0;
-    for (int tile = tile0; tile < total; tile += tstep, ++local) {
+    for (uint32_t local = 0;; ++local) {
       // tcgen05.ld is warp-collective: the warp decides to stop as one
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const int tile = take_tile(local, kErrWaitEpilogue);
+      if (tile >= total) break;
       const Tile t = tile_coords<KIND, TM>(c, G, n_tiles, m_tiles_w, n_fast, tile);
       const bool xg = KIND == kKindFwd && t.g == G;  // the extra group
       const int grow = xg ? 0 : c.grp_row[t.g];

@@ -127,6 +127,8 @@ struct GemmParams {
   int cta_pairs;         // Fwd: 256-row tiles on CTA pairs where the groups average >= 256 rows
   const void* bias;      // [G, N] nullable (GeLU / plain)
   int* err;              // workspace error word
+  int* sched;            // [2] the workspace's tile scheduler words, zero at the launch (it leaves them
+                         // zero); nullptr: a static round-robin schedule
   // Fwd only: one more group with its own operands (the shared expert):
   // xrows rows of its own A, its own weights, output xout [xrows, ldo],
   // pre-activations xzsave, bias xbias [N].  xrows = 0: none.

@@ -519,7 +519,7 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
   if ((cfg.route_flags & MOE_ROUTE_REROUTE) && (!backup || (cfg.dtype == MOE_BF16 && !scratch)))
     return MOE_ERR_UNSUPPORTED;  // the backups live in the workspace
   if (out_logits && !(cfg.dtype == MOE_BF16 && scratch)) return MOE_ERR_UNSUPPORTED;  // top-k kernel path only
-  moe_status zs = launch_zero(counts, sizeof(int) * cfg.E, err, err ? sizeof(int) : 0, stream);
+  moe_status zs = launch_zero(counts, sizeof(int) * cfg.E, err, err ? kWsZeroBytes : 0, stream);
   if (zs != MOE_OK) return zs;
   if (cfg.dtype == MOE_BF16 && scratch && !ln && !backup && cfg.E <= kRouteFuseMaxE && cfg.k <= MAXK) {
     // logits = x . Wr^T on the tcgen05 grouped GEMM (one group of T rows,
@@ -533,6 +533,7 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     g.K = cfg.d;
     g.mode = kModeRouteTopK;
     g.err = err;
+    g.sched = err ? err + 1 : nullptr;
     g.route = RouteEpilogue{expert_bias, noise, idx, w, counts, ent, out_logits, cfg.E, cfg.k, raw};
     return launch_grouped_gemm_tc(g, kKindFwd, x, cfg.T, Wr, nullptr, cfg.E, stream);
   }
@@ -557,6 +558,7 @@ moe_status launch_route(const moe_config& cfg, const void* x, const void* Wr, co
     g.out_f32 = 1;
     g.out = logits;
     g.err = err;
+    g.sched = err ? err + 1 : nullptr;
     moe_status s = launch_grouped_gemm_tc(g, kKindFwd, x, cfg.T, Wr, nullptr, cfg.E, stream);
     if (s != MOE_OK) return s;
     const unsigned grid = static_cast<unsigned>((static_cast<long long>(cfg.T) * 32 + 255) / 256);

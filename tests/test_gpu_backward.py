@@ -341,6 +341,8 @@ def test_back_to_back_steps_match_isolated_steps():
         M.moe_layer_bwd(cfg, weights, t["x"], sv, dY[i % 2], g, wsb)
     torch.cuda.synchronize()
     assert M.moe_check_error(ws) == 0 and M.moe_check_error(wsb) == 0
+    # the weight-gradient launches' tile counter is left at zero
+    assert wsb[:12].view(torch.int32)[1:].tolist() == [0, 0]
     for i, (y, sv, g) in enumerate(outs):
         y0, sv0, g0 = ref[i % 2]
         assert torch.equal(y, y0), i

@@ -256,7 +256,12 @@ def test_expert_ffn_tile_tails(act, tall, shared):
     enough tiles for every SM): last tiles of 1, 37, 88, 112, 113, 128 (half
     tiles), 129, 188, 232, 240 and 241 rows.  The shared expert's T = 1300
     rows end in a 20-row tile.  GeLU runs with biases.  Every row matches the
-    oracle's expert FFN, and rows past offsets[E] are never written."""
+    oracle's expert FFN, and rows past offsets[E] are never written.
+
+    256-row launches hand out tiles from a counter in the workspace header:
+    the workspace starts as 0xff bytes (the entry point zeroes the counter),
+    the launches leave the counter at zero, and a second call on the same
+    workspace gives the same bits."""
     if tall:
         # 256-row tiles need T k / E >= 256 and, per GEMM, at least one tile per SM
         T, k, d, h = 2000, 2, 2048, 1536
@@ -286,13 +291,25 @@ def test_expert_ffn_tile_tails(act, tall, shared):
     Yp = torch.full((T * k, d), 7.0, dtype=bf, device=DEV)
     offs = torch.as_tensor(off, device=DEV)
     ws = M.moe.workspace(cfg, 1)
+    ws.fill_(0xFF)
+
+    def ffn(H, Yp, Hs, Sx):
+        if shared:
+            M.moe.moe_expert_ffn_shared(cfg, Xp, offs, W, H, Yp, x, Hs, Sx, ws)
+        else:
+            M.moe_expert_ffn(cfg, Xp, offs, W["W1"], W.get("W3"), W.get("b1"), W["W2"], W.get("b2"), H, Yp, ws)
+        assert M.moe_check_error(ws) == 0
+        assert ws[:12].view(torch.int32)[1:].tolist() == [0, 0]
+
     Hs = torch.empty(T, h, dtype=bf, device=DEV) if shared else None
     Sx = torch.empty(T, d, dtype=bf, device=DEV) if shared else None
+    ffn(H, Yp, Hs, Sx)
+    H2, Yp2 = torch.full_like(H, 7.0), torch.full_like(Yp, 7.0)
+    Sx2 = torch.empty_like(Sx) if shared else None
+    ffn(H2, Yp2, torch.empty_like(Hs) if shared else None, Sx2)
+    assert torch.equal(H2, H) and torch.equal(Yp2, Yp)
     if shared:
-        M.moe.moe_expert_ffn_shared(cfg, Xp, offs, W, H, Yp, x, Hs, Sx, ws)
-    else:
-        M.moe_expert_ffn(cfg, Xp, offs, W["W1"], W.get("W3"), W.get("b1"), W["W2"], W.get("b2"), H, Yp, ws)
-    assert M.moe_check_error(ws) == 0
+        assert torch.equal(Sx2, Sx)
     Wn = {n: to_np(v) for n, v in W.items()}
     Xn, Hn, Yn = to_np(Xp), to_np(H), to_np(Yp)
     for e in range(E):
