@@ -112,10 +112,15 @@ struct __align__(8) Ctl {
   int hist[256];                   // kModeRouteTopK: this CTA's selections per expert
 };
 
-template <int BM_, bool PAIR = false>
+// A Wgrad epilogue warp stages 32 rows x 64 bytes of output here (see
+// warp_store_rows64), after the control block.
+constexpr int STAGE_OUT_BYTES = 32 * 64;
+
+template <int KIND, int BM_, bool PAIR = false>
 constexpr size_t smem_bytes() {
   return 1024 + static_cast<size_t>(TileCfg<BM_, PAIR>::STAGES) * TileCfg<BM_, PAIR>::STAGE_BYTES +
-         sizeof(Ctl<TileCfg<BM_, PAIR>::STAGES>);
+         (sizeof(Ctl<TileCfg<BM_, PAIR>::STAGES>) + 15) / 16 * 16 +
+         (KIND == kKindWgrad ? static_cast<size_t>(TileCfg<BM_, PAIR>::EPI_WARPS) * STAGE_OUT_BYTES : 0);
 }
 
 struct Tile {
@@ -187,6 +192,45 @@ __device__ __forceinline__ void store_f32x32(float* dst, int col, int N, const f
   }
 }
 
+// The warp's 32 rows (one per lane) each hand 64 bytes (words w(0..15)) to dst, this
+// lane's destination (nullptr: the row is not stored); the first `bytes` of
+// them (a multiple of 16, the same in every lane) are stored.  The rows go
+// through the warp's 2 KB of shared memory, so that each store instruction
+// writes 8 rows of 64 contiguous bytes rather than 16 bytes in each of 32
+// rows: a quarter of the L1 wavefronts, and whole 32-byte sectors.  Used for
+// the weight gradients (fp32).  In the forward kernels the same staging
+// raised register use past the 256-row tile's ceiling (spills), and the
+// small prefill's layer went from 0.176 to 0.182-0.184 ms.  Granule
+// q of row r sits in slot q ^ ((r >> 1) & 3), so neither the row-wise
+// writes nor the column-wise reads conflict on banks.  Warp-collective.
+template <typename W>
+__device__ __forceinline__ void warp_store_rows64(uint4* stage, const W& w, void* dst, int bytes, int lane) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    stage[lane * 4 + (q ^ ((lane >> 1) & 3))] = make_uint4(w(4 * q), w(4 * q + 1), w(4 * q + 2), w(4 * q + 3));
+  __syncwarp();
+  const int q = lane & 3;
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2);
+    uint8_t* d = reinterpret_cast<uint8_t*>(
+        __shfl_sync(0xffffffffu, static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(dst)), r));
+    if (d && q * 16 < bytes) *reinterpret_cast<uint4*>(d + q * 16) = stage[r * 4 + (q ^ ((r >> 1) & 3))];
+  }
+  __syncwarp();
+}
+
+// 32 fp32 of this lane's row, in two 16-column halves; warp-collective
+__device__ __forceinline__ void warp_store_f32x32(uint4* stage, float* rowp, int col, int N, const float (&v)[32],
+                                                  int lane) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int c = col + 16 * hf;
+    warp_store_rows64(stage, [&](int i) { return __float_as_uint(v[16 * hf + i]); }, rowp ? rowp + c : nullptr,
+                      min(64, (N - c) * 4), lane);
+  }
+}
+
 // 32 consecutive fp32 (16-byte aligned); groups of 4 past N read as 0.
 __device__ __forceinline__ void load_f32x32(const float* src, int col, int N, float (&v)[32]) {
 #pragma unroll
@@ -217,6 +261,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl<STAGES>& c = *reinterpret_cast<Ctl<STAGES>*>(tiles + static_cast<size_t>(STAGES) * STAGE_BYTES);
+  uint4* const stage_out = reinterpret_cast<uint4*>(tiles + static_cast<size_t>(STAGES) * STAGE_BYTES +
+                                                    (sizeof(Ctl<STAGES>) + 15) / 16 * 16);
   volatile int* abort_flag = &c.abort;
 
   const int warp = threadIdx.x >> 5;
@@ -636,6 +682,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;          // TMEM lanes [32*quarter, 32*quarter+32)
     const int half = (warp - 2) >> 2;      // BM = 256: accumulator rows 128*half.. (columns 256*half..)
+    uint4* const stg = stage_out + (warp - 2) * (STAGE_OUT_BYTES / 16);  // this warp's output staging
     for (uint32_t local = 0;; ++local) {
       // tcgen05.ld is warp-collective: the warp decides to stop as one
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
@@ -656,6 +703,26 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         break;
       }
       tc_fence_after();
+      // hand the accumulator back to the MMA warp.  The branches below call
+      // this as soon as their last TMEM load of the tile has completed, so
+      // that the next tile's MMAs overlap the last chunk's arithmetic and
+      // stores; otherwise it runs at the end of the tile.  Warp-uniform.
+      bool released = false;
+      auto release = [&]() {
+        tc_fence_before();
+        if constexpr (PAIR) {
+          // one arrival per warp, on the even CTA's barrier (it reuses the
+          // accumulator of both CTAs)
+          __syncwarp();
+          if (lane == 0) {
+            if (crank == 0) mbar_arrive(&c.tmem_empty[acc]);
+            else mbar_arrive_cluster(mapa_shared(&c.tmem_empty[acc], 0));
+          }
+        } else {
+          mbar_arrive(&c.tmem_empty[acc]);
+        }
+        released = true;
+      };
       const int rt = half * 128 + quarter * 32 + lane;  // tile row of this thread
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + (acc + half) * BN;
       // the upper half of a half tile holds no rows and was not multiplied
@@ -679,10 +746,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + cc * 32, r);
           tmem_ld_wait();
+          if (cc == BN / 32 - 1) release();
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = empty ? 0.f : __uint_as_float(r[i]);
-          if (valid) store_f32x32(orow, t.n * BN + cc * 32, p.N, v);
+          warp_store_f32x32(stg, orow, t.n * BN + cc * 32, p.N, v, lane);
         }
       } else if (!idle_half) {
         const long long row_end = xg ? static_cast<long long>(gend) : min(static_cast<long long>(gend), p.rows_alloc);
@@ -773,6 +841,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             tmem_ld_32x32b_x32(taddr + cc * 32, gr);
             tmem_ld_32x32b_x32(taddr + 128 + cc * 32, ur);
             tmem_ld_wait();
+            if (cc == 3) release();
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -817,6 +886,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             uint32_t r[32];
             tmem_ld_32x32b_x32(taddr + cc * 32, r);
             tmem_ld_wait();
+            if (cc == BN / 32 - 1) release();
             const int col = col0 + cc * 32;
             float v[32];
 #pragma unroll
@@ -892,18 +962,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
           }
         }
       }
-      tc_fence_before();
-      if constexpr (PAIR) {
-        // one arrival per warp, on the even CTA's barrier (it reuses the
-        // accumulator of both CTAs)
-        __syncwarp();
-        if (lane == 0) {
-          if (crank == 0) mbar_arrive(&c.tmem_empty[acc]);
-          else mbar_arrive_cluster(mapa_shared(&c.tmem_empty[acc], 0));
-        }
-      } else {
-        mbar_arrive(&c.tmem_empty[acc]);
-      }
+      if (!released) release();
     }
   }
 
@@ -930,7 +989,7 @@ moe_status launch_kind(const GemmParams& p, const CUtensorMap& mA, const CUtenso
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return MOE_ERR_CUDA;
-  constexpr size_t smem = smem_bytes<BM_, PAIR>();
+  constexpr size_t smem = smem_bytes<KIND, BM_, PAIR>();
   constexpr int threads = TileCfg<BM_, PAIR>::THREADS;
   auto kern = grouped_gemm_tc_kernel<KIND, BM_, PAIR>;
   // pair launches: clusters of two CTAs; the kernel is persistent, so the
