@@ -105,14 +105,21 @@ enum { MOE_F32 = 0, MOE_BF16 = 1 };
 enum { MOE_ROUTE_RAW_PROBS = 1, MOE_ROUTE_TOKEN_MAJOR = 2, MOE_ROUTE_LAYERNORM = 4, MOE_ROUTE_REROUTE = 8 };
 
 /* Tile choices of the forward expert GEMMs (moe_config.gemm_flags; no effect
- * on any result bit, only on speed; the pages have no counterpart).
- *  MOE_GEMM_CTA_PAIRS: groups averaging >= 256 rows run 256-row tiles on
- *    clusters of two CTAs on two SMs, one tcgen05 M=256 MMA (cta_group::2)
- *    per K step, each CTA staging half of the rows and half of the weight
- *    tile.  It raises tensor-pipe activity per cycle (GEMM-1 of the large
- *    prefill: 66% -> 73%) but, on a power-capped part, draws the clock down
- *    by as much, so it is off by default. */
-enum { MOE_GEMM_CTA_PAIRS = 1 };
+ * on any result bit, only on speed; the pages have no counterpart).  CTA
+ * pair tiles: groups averaging >= 256 rows run 256-row tiles on clusters of
+ * two CTAs on two SMs, one tcgen05 M=256 MMA (cta_group::2) per K step,
+ * each CTA staging half of the rows and half of the weight tile.  They raise
+ * tensor-pipe activity per cycle, which pays in a short launch (the small
+ * prefill, T=4096 d=1024 h=2816 E=16: 0.176 -> 0.169 ms per layer) but, in
+ * a long one held at the power cap, draws the clock down by more (the
+ * large prefill: ~10% slower).
+ *  0 (default): pair tiles for an expert GEMM of under 2e11 FLOPs (counted
+ *    over the T k routed rows and the shared expert's T rows), single-CTA
+ *    tiles above;
+ *  MOE_GEMM_CTA_PAIRS: pair tiles for every expert GEMM;
+ *  MOE_GEMM_SINGLE_CTA: single-CTA tiles for every expert GEMM.
+ * Setting both is MOE_ERR_INVALID_ARG. */
+enum { MOE_GEMM_CTA_PAIRS = 1, MOE_GEMM_SINGLE_CTA = 2 };
 
 /* Load-balance term (moe_config.balance).  f[e] = counts[e]/T (pre-capacity
  * usage), g[e] = I[e]/T with I[e] the sum of the routing weights of the

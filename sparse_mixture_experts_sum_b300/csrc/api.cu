@@ -24,7 +24,9 @@ moe_status validate(const moe_config* cfg) {
   if ((cfg->route_flags & MOE_ROUTE_REROUTE) && cfg->k > 4) return MOE_ERR_UNSUPPORTED;
   if (cfg->balance < MOE_BALANCE_CV || cfg->balance > MOE_BALANCE_SWITCH) return MOE_ERR_INVALID_ARG;
   if (!(cfg->balance_gamma == cfg->balance_gamma) || isinf(cfg->balance_gamma)) return MOE_ERR_INVALID_ARG;
-  if (cfg->gemm_flags & ~MOE_GEMM_CTA_PAIRS) return MOE_ERR_INVALID_ARG;
+  if ((cfg->gemm_flags & ~(MOE_GEMM_CTA_PAIRS | MOE_GEMM_SINGLE_CTA)) ||
+      ((cfg->gemm_flags & MOE_GEMM_CTA_PAIRS) && (cfg->gemm_flags & MOE_GEMM_SINGLE_CTA)))
+    return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -134,6 +136,12 @@ struct SharedFfn {
   void* Zs;       // pre-activations, nullable
 };
 
+// Expert GEMM launches under this many FLOPs take CTA pair tiles by
+// default: the small prefill's (9.5e10 and 4.7e10) gained 4%, the large
+// prefill's (7.7e12 and 3.9e12) lost 10% (the four-expert profiling slice of
+// the large prefill, 4.8e11 and 2.4e11, keeps the large prefill's tiles).
+constexpr double kPairAutoFlops = 2e11;
+
 moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, const int* offsets, int G, int rows,
                    const void* W1, const void* W3, const void* b1, const void* W2, const void* b2, void* H,
                    void* Yp, void* Z, int* err, cudaStream_t st, const SharedFfn* sh = nullptr) {
@@ -151,8 +159,20 @@ moe_status run_ffn(const moe_config* cfg, const void* Xp, long long a_rows, cons
   g1.bias = swiglu ? nullptr : b1;
   g1.err = err;
   g1.sched = err ? err + 1 : nullptr;
-  g1.cta_pairs = (cfg->gemm_flags & MOE_GEMM_CTA_PAIRS) != 0;
+  // CTA pair tiles as gemm_flags asks, else for a launch short enough to
+  // gain from them (see MOE_GEMM_CTA_PAIRS); each launch's FLOPs are counted
+  // over every row it may run (the T k routed bound and the shared expert)
+  const double launch_rows = static_cast<double>(a_rows) + (sh ? static_cast<double>(cfg->T) : 0.0);
+  const double flops1 = 2.0 * launch_rows * cfg->d * (swiglu ? 2.0 * cfg->h : cfg->h);
+  const double flops2 = 2.0 * launch_rows * cfg->d * cfg->h;
+  auto pairs_for = [&](double flops) {
+    if (cfg->gemm_flags & MOE_GEMM_CTA_PAIRS) return 1;
+    if (cfg->gemm_flags & MOE_GEMM_SINGLE_CTA) return 0;
+    return flops < kPairAutoFlops ? 1 : 0;
+  };
+  g1.cta_pairs = pairs_for(flops1);
   GemmParams g2 = g1;
+  g2.cta_pairs = pairs_for(flops2);
   g2.N = cfg->d;
   g2.K = cfg->h;
   g2.mode = kModePlain;

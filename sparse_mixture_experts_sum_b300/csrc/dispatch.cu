@@ -99,6 +99,20 @@ __global__ void __launch_bounds__(DT) slot_hist_kernel(SlotSrc S, int T, int k, 
   for (int e = threadIdx.x; e <= E; e += DT) out[e] = hist[e];
 }
 
+// v 2^40 truncated toward zero, as an integer, for a finite |v| < 2^23 (an
+// entropy is at most ln E); integer operations only.  v = m 2^(e - 150) for
+// the 24-bit significand m and biased exponent e, so v 2^40 = m 2^(e - 110);
+// subnormals (|v| < 2^-126) count as 0.
+__device__ __forceinline__ long long fixed40(float v) {
+  const uint32_t u = __float_as_uint(v);
+  const int e = static_cast<int>((u >> 23) & 0xFFu);
+  if (e == 0) return 0;
+  const long long m = static_cast<long long>((u & 0x7FFFFFu) | 0x800000u);
+  const int sh = min(e - 110, 39);
+  const long long mag = sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0);
+  return (u >> 31) ? -mag : mag;
+}
+
 // The capacity scan of a whole block of 1024 threads (every thread calls
 // it; it synchronises the block): per-expert bases across chunks, kept,
 // offsets and the statistics.  blockhist [nb][E+1] may be in global or
@@ -196,29 +210,34 @@ __device__ __forceinline__ void capacity_scan_block(const int* __restrict__ bloc
     }
   } else if (stats) {
     // load statistics from integer sums (exact in any order): routed and
-    // kept slots, sum and max of the counts c_e, and sum of c_e^2; one
-    // thread then forms, with f = c/T,
+    // kept slots, sum and max of the counts c_e, and sum of c_e^2.  With f =
+    // c/T,
     //   sum_e (f_e - mean f)^2 = (E sum c^2 - (sum c)^2) / (E T^2)
-    // from an exact 128-bit numerator, so the fp64 work is a handful of
-    // operations on one thread
+    // from an exact 128-bit numerator.
     //
     // With ent (the layer forward): router_entropy = the mean of the finite
-    // entries of ent[0..T), each thread summing a strided subset in fp64,
-    // then warps and the block in a fixed order (NaN when none is finite).
-    __shared__ long long redl[32][3];
+    // entries of ent[0..T), summed exactly in fixed point (units of 2^-40,
+    // each entry truncated by less than 2^-40, so the mean is within 2^-40
+    // of the fp32 entries' exact mean).
+    //
+    // This part's floating point is fp64, whose rate on this part is a small
+    // fraction of fp32's: the sums run in the integer pipes, and the five
+    // independent quotients on five lanes of one warp at once, so that the
+    // longest dependent fp64 chain is a division, a square root and a
+    // division.
+    __shared__ long long redl[32][4];
     __shared__ int redmax[32];
-    __shared__ double rede[32];
     __shared__ int redec[32];
     const long long nslots = static_cast<long long>(T) * k;
     const int nwarps = (blockDim.x + 31) >> 5;
-    double es = 0.0;
+    long long es = 0;
     int ec = 0;
     if (ent) {
 #pragma unroll 8
       for (int t = tid; t < T; t += blockDim.x) {
         const float v = ent[t];
         if (isfinite(v)) {
-          es += v;
+          es += fixed40(v);
           ++ec;
         }
       }
@@ -239,50 +258,73 @@ __device__ __forceinline__ void capacity_scan_block(const int* __restrict__ bloc
       redl[warp][0] = r_cnt;
       redl[warp][1] = k_cnt;
       redl[warp][2] = sq;
+      redl[warp][3] = es;
       redmax[warp] = cmax;
-      rede[warp] = es;
       redec[warp] = ec;
     }
     __syncthreads();
-    if (tid == 0) {
-      long long rc = 0, kc = 0, s2 = 0;
-      int mx = 0;
-      for (int w2 = 0; w2 < nwarps; ++w2) {
-        rc += redl[w2][0];
-        kc += redl[w2][1];
-        s2 += redl[w2][2];
-        mx = max(mx, redmax[w2]);
+    if (warp == 0) {
+      // block totals on every lane of warp 0 (lane w holds warp w's partials)
+      long long rc = lane < nwarps ? redl[lane][0] : 0, kc = lane < nwarps ? redl[lane][1] : 0;
+      long long s2 = lane < nwarps ? redl[lane][2] : 0, ts = lane < nwarps ? redl[lane][3] : 0;
+      int mx = lane < nwarps ? redmax[lane] : 0, tc = lane < nwarps ? redec[lane] : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        rc += __shfl_xor_sync(0xffffffffu, rc, o);
+        kc += __shfl_xor_sync(0xffffffffu, kc, o);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        ts += __shfl_xor_sync(0xffffffffu, ts, o);
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        tc += __shfl_xor_sync(0xffffffffu, tc, o);
       }
       // rc = sum c <= T k <= 2^30, so s2 <= rc^2 <= 2^60 and E s2 < 2^71
       const unsigned __int128 num = static_cast<unsigned __int128>(E) * static_cast<unsigned long long>(s2) -
                                     static_cast<unsigned __int128>(rc) * static_cast<unsigned long long>(rc);
-      const double numd = static_cast<double>(static_cast<unsigned long long>(num >> 64)) * 18446744073709551616.0 +
-                          static_cast<double>(static_cast<unsigned long long>(num));
       const double Td = static_cast<double>(T);
-      const double mean = static_cast<double>(rc) / (static_cast<double>(E) * Td);
-      const double sd = E > 1 ? sqrt(numd / (static_cast<double>(E) * (E - 1)) / (Td * Td)) : 0.0;
-      moe_stats st;
-      st.routed_slots = rc;
-      st.kept_slots = kc;
-      st.dropped_slots = nslots - kc;
-      st.capacity = C;
-      st.numeric_error = unrouted / k;
-      st.drop_rate = static_cast<double>(nslots - kc) / static_cast<double>(nslots);
-      if (balance == MOE_BALANCE_STD_MAX)
-        st.balance_stat = static_cast<double>(lam) * (sd + static_cast<double>(gamma) * (mx / Td));
-      else if (balance == MOE_BALANCE_SWITCH)
-        st.balance_stat = __longlong_as_double(0x7ff8000000000000LL);  // needs the weights: set by the layer
-      else
-        st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
-      double ts = 0.0;
-      long long tc = 0;
-      for (int w2 = 0; w2 < nwarps; ++w2) {
-        ts += rede[w2];
-        tc += redec[w2];
+      // lane 0: the variance sum (E sum c^2 - (sum c)^2) / (E (E-1) T^2);
+      // 1: mean f = sum c / (E T); 2: the drop rate; 3: the mean entropy;
+      // 4: max f = max c / T
+      double a = 0.0, b = 1.0;
+      if (lane == 0) {
+        a = static_cast<double>(static_cast<unsigned long long>(num >> 64)) * 18446744073709551616.0 +
+            static_cast<double>(static_cast<unsigned long long>(num));
+        b = E > 1 ? static_cast<double>(E) * static_cast<double>(E - 1) * (Td * Td) : 1.0;
+      } else if (lane == 1) {
+        a = static_cast<double>(rc);
+        b = static_cast<double>(E) * Td;
+      } else if (lane == 2) {
+        a = static_cast<double>(nslots - kc);
+        b = static_cast<double>(nslots);
+      } else if (lane == 3) {
+        a = static_cast<double>(ts) * 0x1p-40;
+        b = static_cast<double>(tc > 0 ? tc : 1);
+      } else if (lane == 4) {
+        a = static_cast<double>(mx);
+        b = Td;
       }
-      st.router_entropy = tc > 0 ? ts / tc : __longlong_as_double(0x7ff8000000000000LL);
-      st.rerouted_slots = 0;
-      *stats = st;
+      const double q = a / b;
+      const double var = __shfl_sync(0xffffffffu, q, 0), mean = __shfl_sync(0xffffffffu, q, 1);
+      const double drop = __shfl_sync(0xffffffffu, q, 2), emean = __shfl_sync(0xffffffffu, q, 3);
+      const double fmax = __shfl_sync(0xffffffffu, q, 4);
+      if (lane == 0) {
+        const double sd = E > 1 ? sqrt(var) : 0.0;
+        moe_stats st;
+        st.routed_slots = rc;
+        st.kept_slots = kc;
+        st.dropped_slots = nslots - kc;
+        st.capacity = C;
+        st.numeric_error = unrouted / k;
+        st.drop_rate = drop;
+        if (balance == MOE_BALANCE_STD_MAX)
+          st.balance_stat = static_cast<double>(lam) * (sd + static_cast<double>(gamma) * fmax);
+        else if (balance == MOE_BALANCE_SWITCH)
+          st.balance_stat = __longlong_as_double(0x7ff8000000000000LL);  // needs the weights: set by the layer
+        else
+          st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
+        st.router_entropy = tc > 0 ? emean : __longlong_as_double(0x7ff8000000000000LL);
+        st.rerouted_slots = 0;
+        *stats = st;
+      }
     }
   }
 }

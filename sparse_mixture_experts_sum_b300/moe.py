@@ -125,18 +125,21 @@ def _stream(stream=None):
 
 
 ROUTE_RAW_PROBS, ROUTE_TOKEN_MAJOR, ROUTE_LAYERNORM, ROUTE_REROUTE = 1, 2, 4, 8
-GEMM_CTA_PAIRS = 1
+GEMM_CTA_PAIRS, GEMM_SINGLE_CTA = 1, 2
 BALANCE = {"cv": 0, "std_max": 1, "switch": 2}
 
 
 def make_config(T, d, h, E, k, act="swiglu", dtype="bf16", capacity_factor=0.0, min_capacity=0,
                 lambda_balance=0.01, has_shared=False, raw_probs=False, token_major=False,
-                layernorm=False, balance="cv", balance_gamma=100.0, reroute=False, cta_pairs=False) -> MoeConfig:
+                layernorm=False, balance="cv", balance_gamma=100.0, reroute=False,
+                cta_pairs: Optional[bool] = None) -> MoeConfig:
+    """cta_pairs: None = the library's choice per launch, True = CTA pair
+    tiles, False = single-CTA tiles (moe_config.gemm_flags)."""
     flags = ((ROUTE_RAW_PROBS if raw_probs else 0) | (ROUTE_TOKEN_MAJOR if token_major else 0)
              | (ROUTE_LAYERNORM if layernorm else 0) | (ROUTE_REROUTE if reroute else 0))
     return MoeConfig(T, d, h, E, k, ACT[act], DTYPE[dtype], capacity_factor, min_capacity,
                      lambda_balance, int(bool(has_shared)), flags, BALANCE[balance], balance_gamma,
-                     GEMM_CTA_PAIRS if cta_pairs else 0)
+                     0 if cta_pairs is None else (GEMM_CTA_PAIRS if cta_pairs else GEMM_SINGLE_CTA))
 
 
 def config_of(wl, **route) -> MoeConfig:

@@ -93,19 +93,28 @@ def test_capacity_matches_oracle(M, T, k, E, cf, minc):
     (dict(k=5, E=4), 1), (dict(k=9, E=16), 1), (dict(E=1025), 1), (dict(T=0), 1),
     (dict(d=100), 2), (dict(h=36), 2), (dict(act=7), 1), (dict(route_flags=16), 1), (dict(balance=3), 1),
     (dict(route_flags=8, k=5, E=16), 2),
-    (dict(balance_gamma=float("nan")), 1)])
+    (dict(balance_gamma=float("nan")), 1), (dict(gemm_flags=3), 1), (dict(gemm_flags=4), 1)])
 def test_bad_configs_rejected(M, kw, status):
     base = dict(T=64, d=64, h=64, E=8, k=2)
     base.update({k: v for k, v in kw.items() if k in base})
     cfg = M.make_config(**base)
     if "act" in kw:
         cfg.act = kw["act"]
-    for name in ("route_flags", "balance", "balance_gamma"):
+    for name in ("route_flags", "balance", "balance_gamma", "gemm_flags"):
         if name in kw:
             setattr(cfg, name, kw[name])
     with pytest.raises(M.moe.MoeError) as ei:
         M.moe_workspace_size(cfg)
     assert ei.value.status == status
+
+
+def test_tile_choice_flags(M):
+    """cta_pairs None leaves the choice to the library (0); True and False
+    set MOE_GEMM_CTA_PAIRS and MOE_GEMM_SINGLE_CTA, which validate alone."""
+    for arg, flags in ((None, 0), (True, M.moe.GEMM_CTA_PAIRS), (False, M.moe.GEMM_SINGLE_CTA)):
+        cfg = M.make_config(64, 64, 64, 8, 2, cta_pairs=arg)
+        assert cfg.gemm_flags == flags
+        assert M.moe_workspace_size(cfg) > 0
 
 
 def test_null_pointers_rejected_before_launch(M):

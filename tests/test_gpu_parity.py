@@ -272,7 +272,9 @@ def test_expert_ffn_tile_tails(act, tall, shared):
     E = len(rows)
     off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
     assert (sum(rows) / E >= 256) == tall
-    cfg = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared)
+    # single-CTA tiles asked for: at these sizes the library would pick CTA
+    # pairs for the 256-row tiles (test_expert_ffn_pair_tiles covers those)
+    cfg = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared, cta_pairs=False)
     g = torch.Generator().manual_seed(17)
     bf = torch.bfloat16
     s1 = 0.5 / d ** 0.5
@@ -332,7 +334,9 @@ def test_expert_ffn_tile_tails(act, tall, shared):
 def test_expert_ffn_pair_tiles(act, shared):
     """With MOE_GEMM_CTA_PAIRS, groups averaging >= 256 rows run as 256-row
     tiles on CTA pairs (one M=256 MMA over two SMs, each holding half of the
-    rows and half of B); the outputs are the same bits as the default tiles'.
+    rows and half of B); the outputs are the same bits as the single-CTA
+    tiles' (MOE_GEMM_SINGLE_CTA).  Launches this short take pairs by default
+    too: the default config gives the same bits again.
     Per-expert rows 0, 1, 255, 256, 257, 600, 37, 1000 put the pair's row
     split and the group ends everywhere (empty group, one row, a tile one
     row short, exact, one over, several tiles, a single short tile); d = h =
@@ -343,7 +347,8 @@ def test_expert_ffn_pair_tiles(act, shared):
     rows = [0, 1, 255, 256, 257, 600, 37, 1000]
     off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
     cfg = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared, cta_pairs=True)
-    cfg1 = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared)
+    cfg1 = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared, cta_pairs=False)
+    cfg0 = M.make_config(T, d, h, E, k, act, "bf16", has_shared=shared)
     g = torch.Generator().manual_seed(15)
     bf = torch.bfloat16
     # input projections at std 0.5/sqrt(d) keep the hidden values O(1), where
@@ -376,11 +381,12 @@ def test_expert_ffn_pair_tiles(act, shared):
     Hs = torch.empty(T, h, dtype=bf, device=DEV) if shared else None
     Sx = torch.empty(T, d, dtype=bf, device=DEV) if shared else None
     run(cfg, H, Yp, Hs, Sx)
-    # the default tiles give the same bits
-    H1, Y1 = torch.full_like(H, 7.0), torch.full_like(Yp, 7.0)
-    Sx1 = torch.empty_like(Sx) if shared else None
-    run(cfg1, H1, Y1, torch.empty_like(Hs) if shared else None, Sx1)
-    assert torch.equal(H1, H) and torch.equal(Y1, Yp) and (not shared or torch.equal(Sx1, Sx))
+    # single-CTA tiles, and the default choice, give the same bits
+    for c in (cfg1, cfg0):
+        H1, Y1 = torch.full_like(H, 7.0), torch.full_like(Yp, 7.0)
+        Sx1 = torch.empty_like(Sx) if shared else None
+        run(c, H1, Y1, torch.empty_like(Hs) if shared else None, Sx1)
+        assert torch.equal(H1, H) and torch.equal(Y1, Yp) and (not shared or torch.equal(Sx1, Sx))
     Wn = {n: to_np(v) for n, v in W.items()}
     Xn, Hn, Yn = to_np(Xp), to_np(H), to_np(Yp)
     for e in range(E):
