@@ -173,7 +173,7 @@ size_t dispatch_scratch_bytes(const moe_config& cfg);
 // backup: the router's backup experts (MOE_ROUTE_REROUTE: a second pass
 // offers the dropped slots to them), else nullptr.  ent (with stats): the
 // router's per-token entropies; stats->router_entropy = the mean of their
-// finite entries (fixed-order fp64 sum), else NaN.
+// finite entries (an exact sum in 2^-40 fixed point), else NaN.
 moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const void* x, int* kept,
                            int* offsets, int* pos, void* Xp, moe_stats* stats, void* scratch,
                            const int* backup, cudaStream_t stream, const float* ent = nullptr);
