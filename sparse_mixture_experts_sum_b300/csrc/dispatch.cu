@@ -113,6 +113,81 @@ __device__ __forceinline__ long long fixed40(float v) {
   return (u >> 31) ? -mag : mag;
 }
 
+// Integer totals of the load statistics: routed and kept slots, sum of
+// c_e^2, the entropy sum in units of 2^-40, max c_e, finite entropies,
+// unrouted slots.
+struct StatSums {
+  long long rc, kc, s2, ts;
+  int mx, tc, unrouted, pad;
+};
+
+// Parameters of the statistics' fp64 finish.
+struct StatsFinish {
+  const StatSums* sums;  // nullptr: none to finish
+  moe_stats* stats;
+  int T, k, E, C, balance;
+  float lam, gamma;
+};
+
+// The statistics from their integer totals, by one whole warp.  With f =
+// c/T,
+//   sum_e (f_e - mean f)^2 = (E sum c^2 - (sum c)^2) / (E T^2)
+// from an exact 128-bit numerator.  fp64 runs at a small fraction of fp32's
+// rate on this part, so the five independent quotients run on five lanes at
+// once: the longest dependent fp64 chain is a division, a square root and a
+// division.
+__device__ __forceinline__ void stats_finish_warp(const StatSums& S, const StatsFinish& F, int lane) {
+  const long long nslots = static_cast<long long>(F.T) * F.k;
+  const int E = F.E;
+  // rc = sum c <= T k <= 2^30, so s2 <= rc^2 <= 2^60 and E s2 < 2^71
+  const unsigned __int128 num = static_cast<unsigned __int128>(E) * static_cast<unsigned long long>(S.s2) -
+                                static_cast<unsigned __int128>(S.rc) * static_cast<unsigned long long>(S.rc);
+  const double Td = static_cast<double>(F.T);
+  // lane 0: the variance sum / (E (E-1) T^2); 1: mean f = sum c / (E T);
+  // 2: the drop rate; 3: the mean entropy; 4: max f = max c / T
+  double a = 0.0, b = 1.0;
+  if (lane == 0) {
+    a = static_cast<double>(static_cast<unsigned long long>(num >> 64)) * 18446744073709551616.0 +
+        static_cast<double>(static_cast<unsigned long long>(num));
+    b = E > 1 ? static_cast<double>(E) * static_cast<double>(E - 1) * (Td * Td) : 1.0;
+  } else if (lane == 1) {
+    a = static_cast<double>(S.rc);
+    b = static_cast<double>(E) * Td;
+  } else if (lane == 2) {
+    a = static_cast<double>(nslots - S.kc);
+    b = static_cast<double>(nslots);
+  } else if (lane == 3) {
+    a = static_cast<double>(S.ts) * 0x1p-40;
+    b = static_cast<double>(S.tc > 0 ? S.tc : 1);
+  } else if (lane == 4) {
+    a = static_cast<double>(S.mx);
+    b = Td;
+  }
+  const double q = a / b;
+  const double var = __shfl_sync(0xffffffffu, q, 0), mean = __shfl_sync(0xffffffffu, q, 1);
+  const double drop = __shfl_sync(0xffffffffu, q, 2), emean = __shfl_sync(0xffffffffu, q, 3);
+  const double fmax = __shfl_sync(0xffffffffu, q, 4);
+  if (lane == 0) {
+    const double sd = E > 1 ? sqrt(var) : 0.0;
+    moe_stats st;
+    st.routed_slots = S.rc;
+    st.kept_slots = S.kc;
+    st.dropped_slots = nslots - S.kc;
+    st.capacity = F.C;
+    st.numeric_error = S.unrouted / F.k;
+    st.drop_rate = drop;
+    if (F.balance == MOE_BALANCE_STD_MAX)
+      st.balance_stat = static_cast<double>(F.lam) * (sd + static_cast<double>(F.gamma) * fmax);
+    else if (F.balance == MOE_BALANCE_SWITCH)
+      st.balance_stat = __longlong_as_double(0x7ff8000000000000LL);  // needs the weights: set by the layer
+    else
+      st.balance_stat = E > 1 ? static_cast<double>(F.lam) * sd / (mean + 1e-8) : 0.0;
+    st.router_entropy = S.tc > 0 ? emean : __longlong_as_double(0x7ff8000000000000LL);
+    st.rerouted_slots = 0;
+    *F.stats = st;
+  }
+}
+
 // The capacity scan of a whole block of 1024 threads (every thread calls
 // it; it synchronises the block): per-expert bases across chunks, kept,
 // offsets and the statistics.  blockhist [nb][E+1] may be in global or
@@ -121,7 +196,8 @@ __device__ __forceinline__ void capacity_scan_block(const int* __restrict__ bloc
                                                     int C, float lam, int balance, float gamma,
                                                     const int* __restrict__ used, int* __restrict__ base,
                                                     int* __restrict__ kept, int* __restrict__ offsets,
-                                                    moe_stats* stats, const float* __restrict__ ent) {
+                                                    moe_stats* stats, const float* __restrict__ ent,
+                                                    StatSums* defer) {
   __shared__ int tot[1024];
   __shared__ int warp_sums[32];
   __shared__ int unrouted;
@@ -210,25 +286,20 @@ __device__ __forceinline__ void capacity_scan_block(const int* __restrict__ bloc
     }
   } else if (stats) {
     // load statistics from integer sums (exact in any order): routed and
-    // kept slots, sum and max of the counts c_e, and sum of c_e^2.  With f =
-    // c/T,
-    //   sum_e (f_e - mean f)^2 = (E sum c^2 - (sum c)^2) / (E T^2)
-    // from an exact 128-bit numerator.
+    // kept slots, sum and max of the counts c_e, and sum of c_e^2.
     //
     // With ent (the layer forward): router_entropy = the mean of the finite
     // entries of ent[0..T), summed exactly in fixed point (units of 2^-40,
     // each entry truncated by less than 2^-40, so the mean is within 2^-40
     // of the fp32 entries' exact mean).
     //
-    // This part's floating point is fp64, whose rate on this part is a small
-    // fraction of fp32's: the sums run in the integer pipes, and the five
-    // independent quotients on five lanes of one warp at once, so that the
-    // longest dependent fp64 chain is a division, a square root and a
-    // division.
+    // The sums run in the integer pipes; stats_finish_warp forms the fp64
+    // statistics from them, here or (defer) in an extra block of the
+    // assignment kernel, where it runs beside the placement instead of
+    // between the scan and it.
     __shared__ long long redl[32][4];
     __shared__ int redmax[32];
     __shared__ int redec[32];
-    const long long nslots = static_cast<long long>(T) * k;
     const int nwarps = (blockDim.x + 31) >> 5;
     long long es = 0;
     int ec = 0;
@@ -277,53 +348,12 @@ __device__ __forceinline__ void capacity_scan_block(const int* __restrict__ bloc
         mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         tc += __shfl_xor_sync(0xffffffffu, tc, o);
       }
-      // rc = sum c <= T k <= 2^30, so s2 <= rc^2 <= 2^60 and E s2 < 2^71
-      const unsigned __int128 num = static_cast<unsigned __int128>(E) * static_cast<unsigned long long>(s2) -
-                                    static_cast<unsigned __int128>(rc) * static_cast<unsigned long long>(rc);
-      const double Td = static_cast<double>(T);
-      // lane 0: the variance sum (E sum c^2 - (sum c)^2) / (E (E-1) T^2);
-      // 1: mean f = sum c / (E T); 2: the drop rate; 3: the mean entropy;
-      // 4: max f = max c / T
-      double a = 0.0, b = 1.0;
-      if (lane == 0) {
-        a = static_cast<double>(static_cast<unsigned long long>(num >> 64)) * 18446744073709551616.0 +
-            static_cast<double>(static_cast<unsigned long long>(num));
-        b = E > 1 ? static_cast<double>(E) * static_cast<double>(E - 1) * (Td * Td) : 1.0;
-      } else if (lane == 1) {
-        a = static_cast<double>(rc);
-        b = static_cast<double>(E) * Td;
-      } else if (lane == 2) {
-        a = static_cast<double>(nslots - kc);
-        b = static_cast<double>(nslots);
-      } else if (lane == 3) {
-        a = static_cast<double>(ts) * 0x1p-40;
-        b = static_cast<double>(tc > 0 ? tc : 1);
-      } else if (lane == 4) {
-        a = static_cast<double>(mx);
-        b = Td;
-      }
-      const double q = a / b;
-      const double var = __shfl_sync(0xffffffffu, q, 0), mean = __shfl_sync(0xffffffffu, q, 1);
-      const double drop = __shfl_sync(0xffffffffu, q, 2), emean = __shfl_sync(0xffffffffu, q, 3);
-      const double fmax = __shfl_sync(0xffffffffu, q, 4);
-      if (lane == 0) {
-        const double sd = E > 1 ? sqrt(var) : 0.0;
-        moe_stats st;
-        st.routed_slots = rc;
-        st.kept_slots = kc;
-        st.dropped_slots = nslots - kc;
-        st.capacity = C;
-        st.numeric_error = unrouted / k;
-        st.drop_rate = drop;
-        if (balance == MOE_BALANCE_STD_MAX)
-          st.balance_stat = static_cast<double>(lam) * (sd + static_cast<double>(gamma) * fmax);
-        else if (balance == MOE_BALANCE_SWITCH)
-          st.balance_stat = __longlong_as_double(0x7ff8000000000000LL);  // needs the weights: set by the layer
-        else
-          st.balance_stat = E > 1 ? static_cast<double>(lam) * sd / (mean + 1e-8) : 0.0;
-        st.router_entropy = tc > 0 ? emean : __longlong_as_double(0x7ff8000000000000LL);
-        st.rerouted_slots = 0;
-        *stats = st;
+      const StatSums S{rc, kc, s2, ts, mx, tc, unrouted, 0};
+      if (defer) {
+        // an extra block of the assignment kernel that follows finishes them
+        if (lane == 0) *defer = S;
+      } else {
+        stats_finish_warp(S, StatsFinish{nullptr, stats, T, k, E, C, balance, lam, gamma}, lane);
       }
     }
   }
@@ -334,9 +364,9 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(const int* __restri
                                                              float gamma, const int* __restrict__ used,
                                                              int* __restrict__ base, int* __restrict__ kept,
                                                              int* __restrict__ offsets, moe_stats* stats,
-                                                             const float* __restrict__ ent) {
+                                                             const float* __restrict__ ent, StatSums* defer) {
   pdl_entry();
-  capacity_scan_block(blockhist, nb, T, k, E, C, lam, balance, gamma, used, base, kept, offsets, stats, ent);
+  capacity_scan_block(blockhist, nb, T, k, E, C, lam, balance, gamma, used, base, kept, offsets, stats, ent, defer);
 }
 
 // Expert-parallel placement of a rank's slots (adj == nullptr: none).  With
@@ -437,8 +467,13 @@ __device__ __forceinline__ void assign_chunk(const SlotSrc& S, int T, int k, int
 __global__ void __launch_bounds__(DT) assign_kernel(SlotSrc S, int T, int k, int E, bool token_major, int CH,
                                                     const int* __restrict__ base, const int* __restrict__ kept,
                                                     const int* __restrict__ offsets, const int* __restrict__ used,
-                                                    int* __restrict__ pos, EpMap ep) {
+                                                    int* __restrict__ pos, EpMap ep, StatsFinish fin) {
   pdl_entry();
+  if (fin.sums && blockIdx.x == gridDim.x - 1) {
+    // the extra block: the statistics' fp64 finish, beside the placement
+    if (threadIdx.x < 32) stats_finish_warp(*fin.sums, fin, static_cast<int>(threadIdx.x));
+    return;
+  }
   extern __shared__ int sm[];
   assign_chunk(S, T, k, E, token_major, CH, blockIdx.x, threadIdx.x, sm, base, kept, offsets, used, pos, ep,
                BlockSync{});
@@ -474,7 +509,7 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(SlotSrc S, int T, 
     atomicAdd(&hist[static_cast<int>(s / CH) * (E + 1) + ((e >= 0 && e < E) ? e : E)], 1);
   }
   __syncthreads();
-  capacity_scan_block(hist, nb, T, k, E, C, lam, balance, gamma, nullptr, base, kept, offsets, stats, ent);
+  capacity_scan_block(hist, nb, T, k, E, C, lam, balance, gamma, nullptr, base, kept, offsets, stats, ent, nullptr);
   __syncthreads();  // the bases, kept and offsets it wrote are visible to the block
   const int g = threadIdx.x / DT;
   int* scratch = sm + nb * (E + 1) + g * E * (DW + 1);
@@ -639,6 +674,7 @@ inline int row_chunks(int T, int vec_per_row) {
 size_t dispatch_scratch_bytes(const moe_config& cfg) {
   const size_t nb = n_chunks(cfg);
   size_t b = align_up(nb * (cfg.E + 1) * sizeof(int), 256) + align_up(nb * cfg.E * sizeof(int), 256);
+  b += align_up(sizeof(StatSums), 256);  // the statistics' integer totals (no rerouting)
   if (cfg.route_flags & MOE_ROUTE_REROUTE)
     b += align_up(static_cast<size_t>(cfg.E) * sizeof(int), 256) +
          align_up(static_cast<size_t>(cfg.T) * cfg.k * sizeof(int), 256);
@@ -671,10 +707,16 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
   } else if (!reroute) {
     launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S1, cfg.T, cfg.k, cfg.E, tm, CH,
                blockhist);
+    // with statistics the scan hands their integer totals to an extra block
+    // of the assignment kernel, which forms the fp64 figures beside the
+    // placement (13.1 -> 10.0 us of scan on the small prefill went to
+    // integer sums; the rest of the fp64 leaves the chain here)
+    StatSums* sums = stats ? reinterpret_cast<StatSums*>(sp) : nullptr;
+    const StatsFinish fin{sums, stats, cfg.T, cfg.k, cfg.E, C, cfg.balance, cfg.lambda_balance, cfg.balance_gamma};
     launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
-               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept, offsets, stats, ent);
-    launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets,
-               nullptr, pos, EpMap{nullptr, nullptr, 0});
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept, offsets, stats, ent, sums);
+    launch_pdl(assign_kernel, dim3(nb + (sums ? 1 : 0)), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, tm, CH,
+               base, kept, offsets, nullptr, pos, EpMap{nullptr, nullptr, 0}, fin);
   } else {
     // pass 1 keeps its ranks; pass 2 offers the dropped slots their backups
     // in the same priority order, then places every slot
@@ -684,16 +726,18 @@ moe_status launch_dispatch(const moe_config& cfg, int C, const int* idx, const v
     launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S1, cfg.T, cfg.k, cfg.E, tm, CH,
                blockhist);
     launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
-               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept1, offsets, stats, ent);
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, nullptr, base, kept1, offsets, stats, ent,
+               nullptr);
     launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, tm, CH, base, kept1, nullptr,
-               nullptr, rank1, EpMap{nullptr, nullptr, 0});
+               nullptr, rank1, EpMap{nullptr, nullptr, 0}, StatsFinish{nullptr, nullptr, 0, 0, 0, 0, 0, 0.f, 0.f});
     const SlotSrc S2{idx, rank1, backup};
     launch_pdl(slot_hist_kernel, dim3(nb), dim3(DT), (cfg.E + 1) * sizeof(int), stream, S2, cfg.T, cfg.k, cfg.E, tm, CH,
                blockhist);
     launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, C,
-               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, kept1, base, kept, offsets, stats, nullptr);
+               cfg.lambda_balance, cfg.balance, cfg.balance_gamma, kept1, base, kept, offsets, stats, nullptr,
+               nullptr);
     launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S2, cfg.T, cfg.k, cfg.E, tm, CH, base, kept, offsets,
-               kept1, pos, EpMap{nullptr, nullptr, 0});
+               kept1, pos, EpMap{nullptr, nullptr, 0}, StatsFinish{nullptr, nullptr, 0, 0, 0, 0, 0, 0.f, 0.f});
   }
   if (Xp) {
     const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
@@ -767,9 +811,9 @@ moe_status launch_dispatch_ep(const moe_config& cfg, const int* idx, const void*
              CH, blockhist);
   // local slot-major ranks only: the capacity test is on the global rank
   launch_pdl(capacity_scan_kernel, dim3(1), dim3(1024), 0, stream, blockhist, nb, cfg.T, cfg.k, cfg.E, 0x7fffffff, 0.f,
-             0, 0.f, nullptr, base, kept, offsets, nullptr, nullptr);
+             0, 0.f, nullptr, base, kept, offsets, nullptr, nullptr, nullptr);
   launch_pdl(assign_kernel, dim3(nb), dim3(DT), asmem, stream, S1, cfg.T, cfg.k, cfg.E, false, CH, base, kept, offsets,
-             nullptr, pos, EpMap{adj, send, C});
+             nullptr, pos, EpMap{adj, send, C}, StatsFinish{nullptr, nullptr, 0, 0, 0, 0, 0, 0.f, 0.f});
   if (Xsend) {
     const int es = cfg.dtype == MOE_BF16 ? 2 : 4;
     const long long row_bytes = static_cast<long long>(cfg.d) * es;
