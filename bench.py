@@ -524,10 +524,10 @@ def _cpu_model():
 # else the router, top-k, capacity and dispatch of the whole batch plus the
 # expert rows of the two busiest experts (at most the given rows each),
 # extrapolated per token by the measured cost of an expert row.  The
-# training step runs on the numpy fp64 oracle, which holds the backward:
-# the same routing plus forward and backward of the sampled rows.
+# training step runs the same routing plus the C++ oracle's forward and
+# backward of the sampled rows.
 CPU_PLAN = {"tiny_fp32": ("whole", None), "small_prefill": ("experts", 256), "decode": ("experts", None),
-            "large_prefill": ("experts", 32), "training": ("train", 192)}
+            "large_prefill": ("experts", 32), "training": ("train", 4)}
 
 
 def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None, tokens=None):
@@ -540,8 +540,9 @@ def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None, tokens=Non
                  busiest experts (at most max_rows each); tokens/s
                  extrapolated: routing share + expert rows per token (kept
                  slots / T, + 1 with a shared expert) x cost per row;
-      train   -- the numpy oracle's routing, then forward and backward of the
-                 sampled rows (expert_ffn_backward), extrapolated alike.
+      train   -- the same routing, then the C++ oracle's forward and
+                 backward of the sampled rows (expert_ffn_backward),
+                 extrapolated alike.
     tokens: route only the batch's first `tokens` tokens (a bounded sample
     per step for the reference arm); the rates are per token either way."""
     import numpy as np
@@ -570,7 +571,7 @@ def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None, tokens=Non
                capacity_factor=float(np.float32(wl.capacity_factor)), min_capacity=wl.min_capacity,
                lam=float(np.float32(wl.lam)), has_shared=wl.has_shared)
     host = os.cpu_count() or 1
-    cores = 1 if mode != "train" else blas_threads()
+    cores = 1
     common = {"unit": "tokens/s", "cores": cores, "kind": "oracle", "host_cores": host, "cpu_model": _cpu_model(),
               "threads": f"{cores} core{'s' if cores != 1 else ''} of {host}"}
     cpu = lambda a: None if a is None else a.detach().to("cpu")
@@ -584,24 +585,16 @@ def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None, tokens=Non
                     sample=f"C++ fp64 oracle layer forward of the whole batch ({T} tokens) in {dt:.2f} s")
     x, Wr = cpu(t["x"]), cpu(t["Wr"])
     bias, noise = cpu(t.get("expert_bias")), cpu(t.get("noise"))
-    if mode == "train":
-        from oracle import moe_oracle as O
-        t0 = time.perf_counter()
-        r = O.route_and_dispatch(cfg, x, Wr, bias, noise)
-        t_route = time.perf_counter() - t0
-        idx, pos, kept_e = r["idx"], r["pos"], r["kept"]
-        impl = "numpy fp64 oracle, BLAS on one thread"
-    else:
-        from oracle import cpp
-        t0 = time.perf_counter()
-        l = cpp.router_logits(x, Wr, bias, noise)
-        idx, w_, _ = cpp.top_k(l, wl.k)
-        cpp.usage_counts(idx, wl.E)
-        C = cpp.capacity(T, wl.k, wl.E, cfg["capacity_factor"], wl.min_capacity)
-        rank, kept_e = cpp.assign_capacity(idx, wl.E, C)
-        _, pos = cpp.dispatch_positions(idx, rank, kept_e)
-        t_route = time.perf_counter() - t0
-        impl = "C++ fp64 oracle, single thread"
+    from oracle import cpp
+    t0 = time.perf_counter()
+    l = cpp.router_logits(x, Wr, bias, noise)
+    idx, w_, _ = cpp.top_k(l, wl.k)
+    cpp.usage_counts(idx, wl.E)
+    C = cpp.capacity(T, wl.k, wl.E, cfg["capacity_factor"], wl.min_capacity)
+    rank, kept_e = cpp.assign_capacity(idx, wl.E, C)
+    _, pos = cpp.dispatch_positions(idx, rank, kept_e)
+    t_route = time.perf_counter() - t0
+    impl = "C++ fp64 oracle, single thread"
     experts = [int(e) for e in np.argsort(-kept_e, kind="stable")[:2]]
     if "W1" not in t:
         t = dict(t)
@@ -623,11 +616,10 @@ def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None, tokens=Non
         if wl.act != "swiglu":
             p["W3"] = None
         if mode == "train":
-            from oracle import moe_oracle as O
-            src = O.decode(v)
-            dy = O.decode(cpu(t["dY"])[torch.as_tensor(rows)])
+            dy = cpu(t["dY"])[torch.as_tensor(rows)].double().numpy()
             t1 = time.perf_counter()
-            O.expert_ffn_backward(src, r["w"][rows, sl][:, None] * dy, wl.act, **O.expert_params(t, e, wl.act))
+            cpp.expert_ffn_backward(v, w_[rows, sl][:, None] * dy, wl.act, p["W1"], p["W2"], W3=p["W3"], b1=p["b1"],
+                                    b2=p["b2"])
         else:
             t1 = time.perf_counter()
             cpp.expert_ffn(v, wl.act, p["W1"], p["W2"], W3=p["W3"], b1=p["b1"], b2=p["b2"])
@@ -644,19 +636,6 @@ def cpu_baseline(wl_name, gpu_tensors=None, mode=None, max_rows=None, tokens=Non
 
 
 ONE_THREAD = {v: "1" for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")}
-
-
-def blas_threads():
-    """Threads numpy's BLAS runs with: from threadpoolctl when it is
-    installed, else from the thread-count variables the BLAS read at load."""
-    try:
-        from threadpoolctl import threadpool_info
-        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-    except Exception:
-        for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-            if os.environ.get(v, "").isdigit():
-                return int(os.environ[v])
-        return os.cpu_count() or 1
 
 
 def cpu_baselines(local):
@@ -752,10 +731,12 @@ def main():
             gt = S.make_inputs(S.WORKLOADS[args.workload], torch.device("cuda", local))
         for i in range(args.warmup + args.steps):
             # each step a bounded sample on one core: the routing of the
-            # batch's first 512 tokens plus up to 8 rows of each of the two
+            # batch's first 512 tokens plus up to 8 rows (the training
+            # step's forward and backward: 1 row, ~0.8 s) of each of the two
             # busiest experts among them
-            cb = cpu_baseline(args.workload, gt, mode="train" if args.workload == "training" else None,
-                              max_rows=8, tokens=512)
+            train = args.workload == "training"
+            cb = cpu_baseline(args.workload, gt, mode="train" if train else None, max_rows=1 if train else 8,
+                              tokens=512)
             if i >= args.warmup:
                 vals.append(cb["value"])
         v = statistics.median(vals)

@@ -57,6 +57,12 @@ class _Outputs(ctypes.Structure):
                 ("pos", ctypes.c_void_p), ("stats", ctypes.c_void_p)]
 
 
+class _Grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dX", "dWr", "dW1", "dW3", "dW2", "db1", "db2", "dWs1", "dWs3",
+                                               "dWs2", "dbs1", "dbs2", "dl", "y")] + \
+               [("loss", ctypes.c_double), ("balance", ctypes.c_double)]
+
+
 _lib = None
 
 
@@ -77,6 +83,10 @@ def lib() -> ctypes.CDLL:
             "mo_combine": ([i, i, i, vp, vp, vp, vp, vp], None),
             "mo_balance_stat": ([i, i, vp, d], d),
             "mo_layer_forward": ([ctypes.POINTER(_Config), ctypes.POINTER(_Inputs), ctypes.POINTER(_Outputs)], i),
+            "mo_expert_ffn_backward": ([i, i, i, i, i] + [vp] * 14, None),
+            "mo_balance_term_grad": ([i, i, i, vp, vp, d, vp], d),
+            "mo_layer_backward": ([ctypes.POINTER(_Config), ctypes.POINTER(_Inputs), vp, ctypes.POINTER(_Grads)],
+                                  i),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -252,4 +262,88 @@ def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None) -> 
     for n in ("routed_slots", "kept_slots", "dropped_slots", "capacity", "numeric_error"):
         st[n] = int(st[n])
     r["stats"] = st
+    return r
+
+
+def expert_ffn_backward(v, g_out: np.ndarray, act: str, W1, W2, W3=None, b1=None, b2=None) -> dict:
+    """Chain rule through one expert for the stored rows v [n,d] with the
+    fp64 upstream gradient g_out [n,d]: dv, the forward output out, dW1,
+    dW2 and dW3 (SwiGLU) or db1, db2 (GeLU), all fp64."""
+    pv, dt, kv = _stored(v)
+    n, d = kv.shape
+    args = [_stored(a) for a in (W1, W3, b1, W2, b2)]
+    h = args[0][2].shape[0]
+    for p_, dta, _ in args:
+        assert p_ is None or dta == dt, "the weights share the rows' storage type"
+    go = np.ascontiguousarray(g_out, dtype=np.float64)
+    assert go.shape == (n, d)
+    r = dict(dv=np.empty((n, d)), out=np.empty((n, d)), dW1=np.zeros((h, d)), dW2=np.zeros((d, h)))
+    if act == "swiglu":
+        r["dW3"] = np.zeros((h, d))
+    else:
+        r["db1"], r["db2"] = np.zeros(h), np.zeros(d)
+    lib().mo_expert_ffn_backward(n, d, h, ACT[act], dt, pv, go.ctypes.data, *[a[0] for a in args],
+                                 r["dv"].ctypes.data, r["out"].ctypes.data, r["dW1"].ctypes.data,
+                                 _p(r.get("dW3")), r["dW2"].ctypes.data, _p(r.get("db1")), _p(r.get("db2")))
+    return r
+
+
+def balance_term_grad(idx: np.ndarray, w: np.ndarray, E: int, T: int, lam: float):
+    """(B, dB/dw [T,k]) of the CV balance term on the importance I/T."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    dw = np.empty(idx.shape, dtype=np.float64)
+    val = lib().mo_balance_term_grad(T, idx.shape[1], E, idx.ctypes.data, w.ctypes.data, float(lam), dw.ctypes.data)
+    return val, dw
+
+
+def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None) -> dict:
+    """Gradients of L = <dY, y> + B(I/T) with the default routing and the CV
+    balance term (cfg and weights as for layer_forward; dY [T,d] stored like
+    x).  Keys as moe_oracle.layer_backward's: dX, dWr, dW1, dW2, dW3 or
+    db1/db2, the shared expert's dWs1, dWs2, dWs3 or dbs1/dbs2, dlogits, y,
+    loss, balance_term."""
+    for flag in ("raw_probs", "token_major", "layernorm", "reroute"):
+        if cfg.get(flag):
+            raise ValueError(f"the C++ oracle's backward has the default routing only (not {flag})")
+    if cfg.get("balance", "cv") != "cv":
+        raise ValueError("the C++ oracle's backward has the CV balance term only")
+    T, d, h, E, k = cfg["T"], cfg["d"], cfg["h"], cfg["E"], cfg["k"]
+    act = cfg["act"]
+    px, dt, kx = _stored(x)
+    pd, dtd, kd = _stored(dY)
+    assert dtd == dt, "dY shares x's storage type"
+    keep = [kx, kd]
+    inp = _Inputs()
+    inp.x = px
+    for n in ("Wr", "W1", "W3", "b1", "W2", "b2", "Ws1", "Ws3", "bs1", "Ws2", "bs2"):
+        p_, dta, ka = _stored(weights.get(n))
+        assert p_ is None or dta == dt, f"{n} shares x's storage type"
+        setattr(inp, n, p_)
+        keep.append(ka)
+    b, nz = _f32(expert_bias), _f32(noise)
+    inp.bias, inp.noise = _p(b), _p(nz)
+    c = _Config(T=T, d=d, h=h, E=E, k=k, act=ACT[act], dtype=dt,
+                min_capacity=int(cfg.get("min_capacity", 0)), has_shared=int(bool(cfg.get("has_shared"))),
+                capacity_factor=float(np.float32(cfg.get("capacity_factor", 0.0))),
+                lam=float(cfg.get("lam", 0.01)))
+    r = dict(dX=np.empty((T, d)), dWr=np.empty((E, d)), dW1=np.empty((E, h, d)), dW2=np.empty((E, d, h)),
+             dlogits=np.empty((T, E)), y=np.empty((T, d)))
+    if act == "swiglu":
+        r["dW3"] = np.empty((E, h, d))
+    else:
+        r["db1"], r["db2"] = np.empty((E, h)), np.empty((E, d))
+    if cfg.get("has_shared"):
+        r["dWs1"], r["dWs2"] = np.empty((h, d)), np.empty((d, h))
+        if act == "swiglu":
+            r["dWs3"] = np.empty((h, d))
+        else:
+            r["dbs1"], r["dbs2"] = np.empty(h), np.empty(d)
+    g = _Grads(dX=_p(r["dX"]), dWr=_p(r["dWr"]), dW1=_p(r["dW1"]), dW3=_p(r.get("dW3")), dW2=_p(r["dW2"]),
+               db1=_p(r.get("db1")), db2=_p(r.get("db2")), dWs1=_p(r.get("dWs1")), dWs3=_p(r.get("dWs3")),
+               dWs2=_p(r.get("dWs2")), dbs1=_p(r.get("dbs1")), dbs2=_p(r.get("dbs2")), dl=_p(r["dlogits"]),
+               y=_p(r["y"]))
+    if lib().mo_layer_backward(ctypes.byref(c), ctypes.byref(inp), pd, ctypes.byref(g)) != 0:
+        raise ValueError("invalid configuration for the C++ oracle")
+    r["loss"], r["balance_term"] = g.loss, g.balance
     return r

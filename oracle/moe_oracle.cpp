@@ -1,5 +1,6 @@
 // Plain fp64 CPU oracle of the sparse Mixture-of-Experts FFN layer's
-// forward pass, in single-threaded C++.
+// forward pass and, with the default routing and the CV balance term, its
+// backward, in single-threaded C++.
 //
 // TEST INFRASTRUCTURE ONLY.  This is a checker: the tests, the smoke check
 // and the benchmark's CPU-baseline leg may call it; the CUDA library never
@@ -407,6 +408,274 @@ int mo_layer_forward(const mo_config* c, const mo_inputs* in, mo_outputs* out) {
   out->stats[5] = mo_balance_stat(E, T, out->counts, c->lam);
   out->stats[6] = nonfinite;
   out->stats[7] = mo_router_entropy(T, E, l.data());
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// backward (the training step): gradients of L = <dY, y> + B(I/T)
+// ---------------------------------------------------------------------------
+
+// Chain rule through one expert for n rows v [n,d] (stored in `dtype`) with
+// upstream gradient g_out [n,d] (fp64): dv [n,d] and the forward output out
+// [n,d] are written; the weight gradients are ADDED to dW1/dW3 [h,d], dW2
+// [d,h], db1 [h], db2 [d] (null where the activation has none), so that a
+// caller may sum several calls.  SwiGLU, hid = silu(a) b with a = W1 v and
+// b = W3 v: dhid = W2^T g, da = dhid b silu'(a) with silu'(a) = s (1 + a (1 -
+// s)), s = sigmoid(a), db = dhid silu(a).  GeLU, hid = gelu(z) with z = W1 v
+// + b1: dz = dhid gelu'(z), gelu'(z) = Phi(z) + z phi(z).  Then dW2 += g
+// hid^T, dW1 += da v^T (dz v^T), dW3 += db v^T, db1 += sum dz, db2 += sum g,
+// dv = W1^T da + W3^T db (W1^T dz).  Sums in index order.
+void mo_expert_ffn_backward(int n, int d, int h, int act, int dtype, const void* v, const double* g_out,
+                            const void* W1, const void* W3, const void* b1, const void* W2, const void* b2,
+                            double* dv, double* out, double* dW1, double* dW3, double* dW2, double* db1,
+                            double* db2) {
+  const long long nd = static_cast<long long>(n) * d, nh = static_cast<long long>(n) * h;
+  std::vector<double> vr(nd), pre(nh), up(nh), hid(nh), dhid(nh, 0.0), w(static_cast<size_t>(d));
+  for (long long i = 0; i < nd; ++i) vr[i] = rd(v, dtype, i);
+  // forward: the pre-activations and hidden values of every row
+  for (int u = 0; u < h; ++u) {
+    for (int i = 0; i < d; ++i) w[i] = rd(W1, dtype, static_cast<long long>(u) * d + i);
+    std::vector<double> w3(act == 1 ? d : 0);
+    if (act == 1)
+      for (int i = 0; i < d; ++i) w3[i] = rd(W3, dtype, static_cast<long long>(u) * d + i);
+    for (int r = 0; r < n; ++r) {
+      const double* vrow = vr.data() + static_cast<long long>(r) * d;
+      double z = 0.0;
+      for (int i = 0; i < d; ++i) z += w[i] * vrow[i];
+      const long long o = static_cast<long long>(r) * h + u;
+      if (act == 0) {
+        if (b1) z += rd(b1, dtype, u);
+        pre[o] = z;
+        hid[o] = z * 0.5 * (1.0 + std::erf(z / std::sqrt(2.0)));
+      } else {
+        double g = 0.0;
+        for (int i = 0; i < d; ++i) g += w3[i] * vrow[i];
+        pre[o] = z;
+        up[o] = g;
+        hid[o] = z / (1.0 + std::exp(-z)) * g;
+      }
+    }
+  }
+  // the output, dW2 (db2) and the hidden gradient, one output column at a time
+  for (int c = 0; c < d; ++c) {
+    std::vector<double> w2(h);
+    for (int u = 0; u < h; ++u) w2[u] = rd(W2, dtype, static_cast<long long>(c) * h + u);
+    const double bias = (act == 0 && b2) ? rd(b2, dtype, c) : 0.0;
+    for (int r = 0; r < n; ++r) {
+      const double* hr = hid.data() + static_cast<long long>(r) * h;
+      double o = 0.0;
+      for (int u = 0; u < h; ++u) o += w2[u] * hr[u];
+      out[static_cast<long long>(r) * d + c] = o + bias;
+      const double g = g_out[static_cast<long long>(r) * d + c];
+      double* dh = dhid.data() + static_cast<long long>(r) * h;
+      for (int u = 0; u < h; ++u) {
+        dW2[static_cast<long long>(c) * h + u] += g * hr[u];
+        dh[u] += g * w2[u];
+      }
+      if (act == 0 && db2) db2[c] += g;
+    }
+  }
+  // the pre-activation gradients, then dW1, dW3 (db1) and dv
+  std::vector<double> da(nh), db(act == 1 ? nh : 0);
+  for (long long o = 0; o < nh; ++o) {
+    const double z = pre[o];
+    if (act == 0) {
+      const double pdf = std::exp(-0.5 * z * z) / std::sqrt(2.0 * std::acos(-1.0));
+      da[o] = dhid[o] * (0.5 * (1.0 + std::erf(z / std::sqrt(2.0))) + z * pdf);
+    } else {
+      const double s = 1.0 / (1.0 + std::exp(-z));
+      da[o] = dhid[o] * up[o] * s * (1.0 + z * (1.0 - s));
+      db[o] = dhid[o] * z * s;
+    }
+  }
+  for (long long i = 0; i < nd; ++i) dv[i] = 0.0;
+  for (int u = 0; u < h; ++u) {
+    for (int i = 0; i < d; ++i) w[i] = rd(W1, dtype, static_cast<long long>(u) * d + i);
+    std::vector<double> w3(act == 1 ? d : 0);
+    if (act == 1)
+      for (int i = 0; i < d; ++i) w3[i] = rd(W3, dtype, static_cast<long long>(u) * d + i);
+    for (int r = 0; r < n; ++r) {
+      const long long o = static_cast<long long>(r) * h + u;
+      const double* vrow = vr.data() + static_cast<long long>(r) * d;
+      double* dvr = dv + static_cast<long long>(r) * d;
+      for (int i = 0; i < d; ++i) {
+        dW1[static_cast<long long>(u) * d + i] += da[o] * vrow[i];
+        dvr[i] += da[o] * w[i];
+      }
+      if (act == 1) {
+        for (int i = 0; i < d; ++i) {
+          dW3[static_cast<long long>(u) * d + i] += db[o] * vrow[i];
+          dvr[i] += db[o] * w3[i];
+        }
+      } else if (db1) {
+        db1[u] += da[o];
+      }
+    }
+  }
+}
+
+// The differentiable balance term on g = I/T, I[e] the sum of the routing
+// weights of the slots routed to e before capacity (the importance of [P4]
+// 2.2), in the CV form of [P1] 3.1 / 4.2: B = lambda * std_{n-1}(g) /
+// (mean(g) + 1e-8).  Returns B and writes dB/dw for every slot into dw
+// [T,k] (0 for an unrouted slot).  With dev = g - mean,
+//   dB/dg_e = lambda (dev_e / ((E-1) std) / (mean + 1e-8)
+//             - std / (mean + 1e-8)^2 / E),
+// the first term 0 when std = 0, and dg_e/dw = 1/T.
+double mo_balance_term_grad(int T, int k, int E, const int* idx, const double* w, double lam, double* dw) {
+  std::vector<double> g(static_cast<size_t>(E), 0.0), dB(static_cast<size_t>(E), 0.0);
+  const long long S = static_cast<long long>(T) * k;
+  for (long long s = 0; s < S; ++s)
+    if (idx[s] >= 0) g[idx[s]] += w[s];
+  for (int e = 0; e < E; ++e) g[e] /= T;
+  double val = 0.0;
+  if (E > 1) {
+    double mean = 0.0;
+    for (int e = 0; e < E; ++e) mean += g[e];
+    mean /= E;
+    double ss = 0.0;
+    for (int e = 0; e < E; ++e) ss += (g[e] - mean) * (g[e] - mean);
+    const double sd = std::sqrt(ss / (E - 1)), m = mean + 1e-8;
+    val = lam * sd / m;
+    for (int e = 0; e < E; ++e)
+      dB[e] = lam * ((sd > 0.0 ? (g[e] - mean) / ((E - 1) * sd) : 0.0) / m - sd / (m * m) / E);
+  }
+  for (long long s = 0; s < S; ++s) dw[s] = idx[s] >= 0 ? dB[idx[s]] / T : 0.0;
+  return val;
+}
+
+// Gradients of one layer, fp64.  dY [T,d] is stored in the config's dtype.
+// Every pointer is caller-owned and fully written (zeroed first): dX [T,d],
+// dWr [E,d], dW1/dW3 [E,h,d], dW2 [E,d,h], db1 [E,h], db2 [E,d] (GeLU), the
+// shared expert's dWs1/dWs3 [h,d], dWs2 [d,h], dbs1 [h], dbs2 [d]; the
+// logit gradient dl [T,E], y [T,d]; loss = <dY, y> + B and B.  Pointers for
+// parts the configuration does not have may be null.
+struct mo_grads {
+  double *dX, *dWr, *dW1, *dW3, *dW2, *db1, *db2, *dWs1, *dWs3, *dWs2, *dbs1, *dbs2, *dl, *y;
+  double loss, balance;
+};
+
+// The training step's backward with the default routing (softmax over the
+// selected logits, slot-major capacity) and the CV balance term:
+//   per slot, G[t,j] = [kept] <dY[t], FFN_e(x[t])> + dB/dw[t,j];
+//   dl[t, idx_j] = w_j (G_j - sum_j' w_j' G_j') (the softmax over the
+//   selected logits), other logits 0;
+//   dWr = dl^T x; dX = dl Wr + the experts' input gradients (a routed row's
+//   upstream gradient is w_j dY[t]) + the shared expert's (upstream dY).
+// Returns 0, or -1 on an invalid configuration.
+int mo_layer_backward(const mo_config* c, const mo_inputs* in, const void* dY, mo_grads* g) {
+  const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
+  if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
+      (dt != MO_F32 && dt != MO_BF16))
+    return -1;
+  const long long S = static_cast<long long>(T) * k, Td = static_cast<long long>(T) * d;
+  const int es = dt == MO_BF16 ? 2 : 4;
+  // the forward's routing
+  std::vector<double> l(static_cast<size_t>(T) * E), w(S);
+  std::vector<int> idx(S), rank(S);
+  std::vector<long long> counts(E), kept(E), offsets(E + 1), pos(S);
+  mo_router_logits(T, d, E, dt, in->x, in->Wr, in->bias, in->noise, l.data());
+  mo_top_k(T, E, k, l.data(), idx.data(), w.data());
+  mo_usage_counts(T, k, E, idx.data(), counts.data());
+  const int C = mo_capacity(T, k, E, c->capacity_factor, c->min_capacity);
+  mo_assign_capacity(T, k, E, C, idx.data(), rank.data(), kept.data());
+  mo_dispatch_positions(T, k, E, idx.data(), rank.data(), kept.data(), offsets.data(), pos.data());
+
+  std::vector<double> dy(Td);
+  for (long long i = 0; i < Td; ++i) dy[i] = rd(dY, dt, i);
+  const auto zero = [](double* p, long long n) {
+    if (p)
+      for (long long i = 0; i < n; ++i) p[i] = 0.0;
+  };
+  const long long hd = static_cast<long long>(h) * d;
+  zero(g->dX, Td);
+  zero(g->dWr, static_cast<long long>(E) * d);
+  zero(g->dW1, E * hd);
+  zero(g->dW3, c->act == 1 ? E * hd : 0);
+  zero(g->dW2, E * hd);
+  zero(g->db1, c->act == 0 ? static_cast<long long>(E) * h : 0);
+  zero(g->db2, c->act == 0 ? static_cast<long long>(E) * d : 0);
+  zero(g->y, Td);
+  zero(g->dl, static_cast<long long>(T) * E);
+  std::vector<double> G(S, 0.0);
+  const auto at = [&](const void* base, long long elems) -> const void* {
+    return base ? static_cast<const char*>(base) + elems * es : nullptr;
+  };
+  // each expert over its kept slots, in slot order (token, then choice)
+  for (int e = 0; e < E; ++e) {
+    std::vector<long long> slots;
+    for (long long s = 0; s < S; ++s)
+      if (idx[s] == e && pos[s] >= 0) slots.push_back(s);
+    const int n = static_cast<int>(slots.size());
+    if (n == 0) continue;
+    std::vector<char> v(static_cast<size_t>(n) * d * es);
+    std::vector<double> go(static_cast<size_t>(n) * d), dv(static_cast<size_t>(n) * d), out(static_cast<size_t>(n) * d);
+    for (int r = 0; r < n; ++r) {
+      const long long t = slots[r] / k;
+      std::memcpy(v.data() + static_cast<long long>(r) * d * es, static_cast<const char*>(in->x) + t * d * es,
+                  static_cast<size_t>(d) * es);
+      for (int i = 0; i < d; ++i) go[static_cast<long long>(r) * d + i] = w[slots[r]] * dy[t * d + i];
+    }
+    mo_expert_ffn_backward(n, d, h, c->act, dt, v.data(), go.data(), at(in->W1, e * hd), at(in->W3, e * hd),
+                           at(in->b1, static_cast<long long>(e) * h), at(in->W2, e * hd),
+                           at(in->b2, static_cast<long long>(e) * d), dv.data(), out.data(), g->dW1 + e * hd,
+                           c->act == 1 ? g->dW3 + e * hd : nullptr, g->dW2 + e * hd,
+                           c->act == 0 && g->db1 ? g->db1 + static_cast<long long>(e) * h : nullptr,
+                           c->act == 0 && g->db2 ? g->db2 + static_cast<long long>(e) * d : nullptr);
+    for (int r = 0; r < n; ++r) {
+      const long long s = slots[r], t = s / k;
+      double dot = 0.0;
+      for (int i = 0; i < d; ++i) {
+        const double o = out[static_cast<long long>(r) * d + i];
+        dot += dy[t * d + i] * o;
+        g->y[t * d + i] += w[s] * o;
+        g->dX[t * d + i] += dv[static_cast<long long>(r) * d + i];
+      }
+      G[s] += dot;
+    }
+  }
+  if (c->has_shared) {
+    const long long sh = static_cast<long long>(h) * d;
+    zero(g->dWs1, sh);
+    zero(g->dWs3, c->act == 1 ? sh : 0);
+    zero(g->dWs2, sh);
+    zero(g->dbs1, c->act == 0 ? h : 0);
+    zero(g->dbs2, c->act == 0 ? d : 0);
+    std::vector<double> dv(Td), out(Td);
+    mo_expert_ffn_backward(T, d, h, c->act, dt, in->x, dy.data(), in->Ws1, in->Ws3, in->bs1, in->Ws2, in->bs2,
+                           dv.data(), out.data(), g->dWs1, c->act == 1 ? g->dWs3 : nullptr, g->dWs2,
+                           c->act == 0 ? g->dbs1 : nullptr, c->act == 0 ? g->dbs2 : nullptr);
+    for (long long i = 0; i < Td; ++i) {
+      g->dX[i] += dv[i];
+      g->y[i] += out[i];
+    }
+  }
+  std::vector<double> dB(S);
+  const double B = mo_balance_term_grad(T, k, E, idx.data(), w.data(), c->lam, dB.data());
+  for (long long s = 0; s < S; ++s) G[s] += dB[s];
+  // the logit gradient: the softmax over the selected logits
+  for (int t = 0; t < T; ++t) {
+    const long long s0 = static_cast<long long>(t) * k;
+    if (idx[s0] < 0) continue;
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) sum += w[s0 + j] * G[s0 + j];
+    for (int j = 0; j < k; ++j) g->dl[static_cast<long long>(t) * E + idx[s0 + j]] += w[s0 + j] * (G[s0 + j] - sum);
+  }
+  // dWr = dl^T x and dX += dl Wr
+  for (int e = 0; e < E; ++e) {
+    for (int t = 0; t < T; ++t) {
+      const double q = g->dl[static_cast<long long>(t) * E + e];
+      if (q == 0.0) continue;
+      for (int i = 0; i < d; ++i) {
+        g->dWr[static_cast<long long>(e) * d + i] += q * rd(in->x, dt, static_cast<long long>(t) * d + i);
+        g->dX[static_cast<long long>(t) * d + i] += q * rd(in->Wr, dt, static_cast<long long>(e) * d + i);
+      }
+    }
+  }
+  double ly = 0.0;
+  for (long long i = 0; i < Td; ++i) ly += dy[i] * g->y[i];
+  g->balance = B;
+  g->loss = ly + B;
   return 0;
 }
 

@@ -201,3 +201,142 @@ def test_layer_forward_matches_numpy_oracle(wl):
         assert abs(c["stats"][key] - n["stats"][key]) <= 1e-12 * max(1.0, abs(n["stats"][key])), key
     if wl.capacity_factor > 0:
         assert c["stats"]["dropped_slots"] > 0  # capacity binds
+
+
+# ----------------------------------------------------------------------------
+# the backward
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_expert_ffn_backward_against_autograd(act):
+    """One expert's input, weight and bias gradients for an upstream g_out
+    equal torch autograd's of <g_out, FFN(v)> in fp64, on rows and weights
+    stored in bf16; the forward output comes back too."""
+    g = torch.Generator().manual_seed(31)
+    n, d, h = 9, 24, 40
+    st = dict(v=torch.randn(n, d, generator=g), W1=torch.randn(h, d, generator=g) / d ** 0.5,
+              W3=torch.randn(h, d, generator=g) / d ** 0.5, W2=torch.randn(d, h, generator=g) / h ** 0.5,
+              b1=torch.randn(h, generator=g) * 0.3, b2=torch.randn(d, generator=g) * 0.3)
+    st = {k_: v_.to(torch.bfloat16) for k_, v_ in st.items()}
+    leaf = {k_: v_.double().requires_grad_(True) for k_, v_ in st.items()}
+    go = torch.randn(n, d, generator=g, dtype=torch.float64)
+    if act == "gelu":
+        out = torch.nn.functional.gelu(leaf["v"] @ leaf["W1"].T + leaf["b1"]) @ leaf["W2"].T + leaf["b2"]
+        got = cpp.expert_ffn_backward(st["v"], go.numpy(), "gelu", st["W1"], st["W2"], b1=st["b1"], b2=st["b2"])
+        names = ("v", "W1", "W2", "b1", "b2")
+    else:
+        out = (torch.nn.functional.silu(leaf["v"] @ leaf["W1"].T) * (leaf["v"] @ leaf["W3"].T)) @ leaf["W2"].T
+        got = cpp.expert_ffn_backward(st["v"], go.numpy(), "swiglu", st["W1"], st["W2"], W3=st["W3"])
+        names = ("v", "W1", "W2", "W3")
+    (out * go).sum().backward()
+    np.testing.assert_allclose(got["out"], out.detach().numpy(), rtol=1e-12, atol=1e-12)
+    for nm in names:
+        key = "dv" if nm == "v" else "d" + nm
+        ref = leaf[nm].grad.numpy()
+        np.testing.assert_allclose(got[key], ref, rtol=0, atol=1e-12 * max(1.0, float(np.abs(ref).max())),
+                                   err_msg=key)
+
+
+def test_balance_term_grad_against_autograd():
+    """The CV balance term on the importance and its per-slot weight
+    gradient, against torch autograd of lambda * std(I/T) / (mean(I/T) +
+    1e-8) in fp64 (an unrouted slot, -1, has none); equal importances give
+    a zero term."""
+    rng = np.random.default_rng(41)
+    T, k, E, lam = 30, 2, 5, 0.01
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    idx[4] = -1
+    w = rng.uniform(0.1, 0.9, size=(T, k))
+    wt = torch.tensor(w, requires_grad=True)
+    onehot = torch.zeros(T, k, E, dtype=torch.float64)
+    for t in range(T):
+        for j in range(k):
+            if idx[t, j] >= 0:
+                onehot[t, j, idx[t, j]] = 1.0
+    gI = (wt[:, :, None] * onehot).sum(dim=(0, 1)) / T
+    B = lam * gI.std(unbiased=True) / (gI.mean() + 1e-8)
+    B.backward()
+    val, dw = cpp.balance_term_grad(idx, w, E, T, lam)
+    assert abs(val - float(B.detach())) <= 1e-15
+    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=0, atol=1e-15)
+    assert (dw[4] == 0).all()
+    val, dw = cpp.balance_term_grad(np.array([[0], [1]], dtype=np.int32), np.array([[0.5], [0.5]]), 2, 2, lam)
+    assert val == 0.0 and np.all(np.abs(dw) <= 1e-6)
+
+
+BACKWARD_LAYERS = [
+    # GeLU in fp32 with biases, no capacity limit
+    S.WORKLOADS["tiny_fp32"].replace(T=24, d=16, h=24, seed=43, training=True),
+    # SwiGLU in bf16 with the shared expert, Gumbel noise and a binding capacity
+    S.WORKLOADS["training"].replace(T=64, d=24, h=32, E=6, capacity_factor=0.7, seed=47),
+]
+
+
+def _bwd_cfg(wl):
+    return dict(T=wl.T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act,
+                capacity_factor=float(np.float32(wl.capacity_factor)), min_capacity=wl.min_capacity,
+                lam=float(np.float32(wl.lam)), has_shared=wl.has_shared)
+
+
+@pytest.mark.parametrize("wl", BACKWARD_LAYERS, ids=lambda w: w.name)
+def test_layer_backward_matches_numpy_oracle(wl):
+    """Every gradient, the logit gradient, y and the loss of the C++
+    backward equal the numpy oracle's (itself pinned by finite differences)
+    to 1e-11 of each tensor's largest entry."""
+    t = S.make_inputs(wl, "cpu")
+    cfg = _bwd_cfg(wl)
+    c = cpp.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
+    n = O.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
+    keys = [k_ for k_ in c if k_ not in ("loss", "balance_term")]
+    assert set(keys) <= set(n), set(keys) - set(n)
+    for key in keys:
+        scale = max(1e-3, float(np.abs(n[key]).max()))
+        np.testing.assert_allclose(c[key], n[key], rtol=0, atol=1e-11 * scale, err_msg=key)
+    assert abs(c["loss"] - n["loss"]) <= 1e-11 * max(1.0, abs(n["loss"]))
+    assert abs(c["balance_term"] - n["balance_term"]) <= 1e-15
+    if wl.capacity_factor > 0:
+        assert (n["route"]["pos"] < 0).any()  # a dropped slot takes part
+
+
+def test_layer_backward_finite_differences():
+    """Central differences of the C++ oracle's own loss, on a GeLU layer
+    stored in fp32 with a shared expert, match its gradients: entries of x,
+    Wr, W1, b1, W2, b2 and the shared expert's weights.  The perturbation is 2^-9,
+    exact in fp32 for these magnitudes.  An entry of x or Wr whose
+    perturbation changes the routing (the loss is not differentiable
+    there) is passed over for another; each tensor gets three checks."""
+    wl = S.WORKLOADS["tiny_fp32"].replace(T=12, d=8, h=12, E=4, has_shared=True, capacity_factor=0.8, seed=53,
+                                          training=True)
+    t = S.make_inputs(wl, "cpu")
+    cfg = _bwd_cfg(wl)
+    base = cpp.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
+    fwd0 = cpp.layer_forward(cfg, t, t["x"], t.get("expert_bias"), t.get("noise"))
+    assert (fwd0["pos"] < 0).any()  # the capacity drops a slot
+    hstep = 2.0 ** -9
+    rng = np.random.default_rng(59)
+    checks = [("x", "dX"), ("Wr", "dWr"), ("W1", "dW1"), ("b1", "db1"), ("W2", "dW2"), ("b2", "db2"),
+              ("Ws1", "dWs1"), ("Ws2", "dWs2")]
+    for name, gname in checks:
+        done = 0
+        for _ in range(40):
+            flat = int(rng.integers(t[name].numel()))
+            vals, same = [], True
+            for sgn in (1, -1):
+                tt = dict(t)
+                a = t[name].clone().reshape(-1)
+                a[flat] += sgn * hstep
+                tt[name] = a.reshape(t[name].shape)
+                f = cpp.layer_forward(cfg, tt, tt["x"], tt.get("expert_bias"), tt.get("noise"))
+                same = same and np.array_equal(f["pos"], fwd0["pos"]) and np.array_equal(f["idx"], fwd0["idx"])
+                r = cpp.layer_backward(cfg, tt, tt["x"], tt["dY"], tt.get("expert_bias"), tt.get("noise"))
+                vals.append(r["loss"])
+            if not same:
+                assert name in ("x", "Wr")  # only the router's inputs move the routing
+                continue
+            fd = (vals[0] - vals[1]) / (2 * hstep)
+            an = float(base[gname].reshape(-1)[flat])
+            assert abs(fd - an) <= 1e-5 * max(1.0, abs(an)), (name, flat, fd, an)
+            done += 1
+            if done == 3:
+                break
+        assert done == 3, name
