@@ -43,7 +43,11 @@ class _Config(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("h", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("act", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("min_capacity", ctypes.c_int), ("has_shared", ctypes.c_int),
-                ("capacity_factor", ctypes.c_float), ("lam", ctypes.c_double)]
+                ("capacity_factor", ctypes.c_float), ("lam", ctypes.c_double), ("balance", ctypes.c_int),
+                ("gamma", ctypes.c_double)]
+
+
+BALANCE = {"cv": 0, "std_max": 1, "switch": 2}
 
 
 class _Inputs(ctypes.Structure):
@@ -84,7 +88,7 @@ def lib() -> ctypes.CDLL:
             "mo_balance_stat": ([i, i, vp, d], d),
             "mo_layer_forward": ([ctypes.POINTER(_Config), ctypes.POINTER(_Inputs), ctypes.POINTER(_Outputs)], i),
             "mo_expert_ffn_backward": ([i, i, i, i, i] + [vp] * 14, None),
-            "mo_balance_term_grad": ([i, i, i, vp, vp, d, vp], d),
+            "mo_balance_term_grad": ([i, i, i, vp, vp, d, i, d, vp], d),
             "mo_layer_backward": ([ctypes.POINTER(_Config), ctypes.POINTER(_Inputs), vp, ctypes.POINTER(_Grads)],
                                   i),
         }
@@ -231,10 +235,13 @@ STATS = ("routed_slots", "kept_slots", "dropped_slots", "capacity", "drop_rate",
 
 
 def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None) -> dict:
-    """The whole forward pass.  cfg: T, d, h, E, k, act, capacity_factor,
-    min_capacity, lam, has_shared (as for moe_oracle.layer_forward);
+    """The whole forward pass (the CV statistic).  cfg: T, d, h, E, k, act,
+    capacity_factor, min_capacity, lam, has_shared (as for
+    moe_oracle.layer_forward);
     weights: Wr, W1, W3, b1, W2, b2, Ws1, Ws3, bs1, Ws2, bs2 (stored
     tensors, absent or None where the layer has none)."""
+    if cfg.get("balance", "cv") != "cv":
+        raise ValueError("the C++ oracle's forward reports the CV statistic only")
     T, d, E, k = cfg["T"], cfg["d"], cfg["E"], cfg["k"]
     px, dt, kx = _stored(x)
     keep = [kx]
@@ -288,26 +295,27 @@ def expert_ffn_backward(v, g_out: np.ndarray, act: str, W1, W2, W3=None, b1=None
     return r
 
 
-def balance_term_grad(idx: np.ndarray, w: np.ndarray, E: int, T: int, lam: float):
-    """(B, dB/dw [T,k]) of the CV balance term on the importance I/T."""
+def balance_term_grad(idx: np.ndarray, w: np.ndarray, E: int, T: int, lam: float, variant: str = "cv",
+                      gamma: float = 100.0):
+    """(B, dB/dw [T,k]) of the balance term on the importance I/T in the
+    form `variant` (cv, std_max, switch) gives."""
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     w = np.ascontiguousarray(w, dtype=np.float64)
     dw = np.empty(idx.shape, dtype=np.float64)
-    val = lib().mo_balance_term_grad(T, idx.shape[1], E, idx.ctypes.data, w.ctypes.data, float(lam), dw.ctypes.data)
+    val = lib().mo_balance_term_grad(T, idx.shape[1], E, idx.ctypes.data, w.ctypes.data, float(lam),
+                                     BALANCE[variant], float(gamma), dw.ctypes.data)
     return val, dw
 
 
 def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None) -> dict:
-    """Gradients of L = <dY, y> + B(I/T) with the default routing and the CV
-    balance term (cfg and weights as for layer_forward; dY [T,d] stored like
-    x).  Keys as moe_oracle.layer_backward's: dX, dWr, dW1, dW2, dW3 or
+    """Gradients of L = <dY, y> + B(I/T) with the default routing and the
+    balance term of cfg["balance"] (cv, std_max or switch, with cfg["gamma"];
+    cfg and weights as for layer_forward; dY [T,d] stored like x).  Keys as moe_oracle.layer_backward's: dX, dWr, dW1, dW2, dW3 or
     db1/db2, the shared expert's dWs1, dWs2, dWs3 or dbs1/dbs2, dlogits, y,
     loss, balance_term."""
     for flag in ("raw_probs", "token_major", "layernorm", "reroute"):
         if cfg.get(flag):
             raise ValueError(f"the C++ oracle's backward has the default routing only (not {flag})")
-    if cfg.get("balance", "cv") != "cv":
-        raise ValueError("the C++ oracle's backward has the CV balance term only")
     T, d, h, E, k = cfg["T"], cfg["d"], cfg["h"], cfg["E"], cfg["k"]
     act = cfg["act"]
     px, dt, kx = _stored(x)
@@ -326,7 +334,8 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
     c = _Config(T=T, d=d, h=h, E=E, k=k, act=ACT[act], dtype=dt,
                 min_capacity=int(cfg.get("min_capacity", 0)), has_shared=int(bool(cfg.get("has_shared"))),
                 capacity_factor=float(np.float32(cfg.get("capacity_factor", 0.0))),
-                lam=float(cfg.get("lam", 0.01)))
+                lam=float(cfg.get("lam", 0.01)), balance=BALANCE[cfg.get("balance", "cv")],
+                gamma=float(cfg.get("gamma", 100.0)))
     r = dict(dX=np.empty((T, d)), dWr=np.empty((E, d)), dW1=np.empty((E, h, d)), dW2=np.empty((E, d, h)),
              dlogits=np.empty((T, E)), y=np.empty((T, d)))
     if act == "swiglu":

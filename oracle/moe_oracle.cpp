@@ -1,6 +1,6 @@
 // Plain fp64 CPU oracle of the sparse Mixture-of-Experts FFN layer's
-// forward pass and, with the default routing and the CV balance term, its
-// backward, in single-threaded C++.
+// forward pass and, with the default routing, its backward, in
+// single-threaded C++.
 //
 // TEST INFRASTRUCTURE ONLY.  This is a checker: the tests, the smoke check
 // and the benchmark's CPU-baseline leg may call it; the CUDA library never
@@ -319,6 +319,8 @@ struct mo_config {
   int has_shared;
   float capacity_factor;  // <= 0: no limit
   double lam;
+  int balance;   // the backward's balance term: 0 CV, 1 std + max, 2 switch (the forward's statistic is CV)
+  double gamma;  // its max weight (std + max)
 };
 
 // Stored inputs (pointers in the config's dtype unless noted; null where
@@ -348,7 +350,7 @@ struct mo_outputs {
 int mo_layer_forward(const mo_config* c, const mo_inputs* in, mo_outputs* out) {
   const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
   if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
-      (dt != MO_F32 && dt != MO_BF16))
+      (dt != MO_F32 && dt != MO_BF16) || c->balance != 0)
     return -1;
   const long long S = static_cast<long long>(T) * k;
   const int es = dt == MO_BF16 ? 2 : 4;
@@ -516,29 +518,59 @@ void mo_expert_ffn_backward(int n, int d, int h, int act, int dtype, const void*
 
 // The differentiable balance term on g = I/T, I[e] the sum of the routing
 // weights of the slots routed to e before capacity (the importance of [P4]
-// 2.2), in the CV form of [P1] 3.1 / 4.2: B = lambda * std_{n-1}(g) /
-// (mean(g) + 1e-8).  Returns B and writes dB/dw for every slot into dw
-// [T,k] (0 for an unrouted slot).  With dev = g - mean,
-//   dB/dg_e = lambda (dev_e / ((E-1) std) / (mean + 1e-8)
-//             - std / (mean + 1e-8)^2 / E),
-// the first term 0 when std = 0, and dg_e/dw = 1/T.
-double mo_balance_term_grad(int T, int k, int E, const int* idx, const double* w, double lam, double* dw) {
-  std::vector<double> g(static_cast<size_t>(E), 0.0), dB(static_cast<size_t>(E), 0.0);
+// 2.2), in the form `variant` gives.  Returns B and writes dB/dw for every
+// slot into dw [T,k] (0 for an unrouted slot); dg_e/dw = 1/T.
+//   0, CV ([P1] 3.1 / 4.2): B = lambda std_{n-1}(g) / (mean(g) + 1e-8);
+//      with dev = g - mean, dB/dg_e = lambda (dev_e / ((E-1) std) /
+//      (mean + 1e-8) - std / (mean + 1e-8)^2 / E), the first term 0 when
+//      std = 0.
+//   1, std + max ([P2] 3.2): B = lambda (std_{n-1}(g) + gamma max(g));
+//      dB/dg_e = lambda (dev_e / ((E-1) std) + gamma [e is the first
+//      largest]).
+//   2, switch ([P3] 2.3): B = lambda sum_e f_e g_e with f = counts / T the
+//      usage fraction, a constant; dB/dg_e = lambda f_e.
+double mo_balance_term_grad(int T, int k, int E, const int* idx, const double* w, double lam, int variant,
+                            double gamma, double* dw) {
+  std::vector<double> g(static_cast<size_t>(E), 0.0), f(static_cast<size_t>(E), 0.0), dB(static_cast<size_t>(E), 0.0);
   const long long S = static_cast<long long>(T) * k;
   for (long long s = 0; s < S; ++s)
-    if (idx[s] >= 0) g[idx[s]] += w[s];
-  for (int e = 0; e < E; ++e) g[e] /= T;
-  double val = 0.0;
+    if (idx[s] >= 0) {
+      g[idx[s]] += w[s];
+      f[idx[s]] += 1.0;
+    }
+  for (int e = 0; e < E; ++e) {
+    g[e] /= T;
+    f[e] /= T;
+  }
+  double mean = 0.0, sd = 0.0;
+  for (int e = 0; e < E; ++e) mean += g[e];
+  mean /= E;
   if (E > 1) {
-    double mean = 0.0;
-    for (int e = 0; e < E; ++e) mean += g[e];
-    mean /= E;
     double ss = 0.0;
     for (int e = 0; e < E; ++e) ss += (g[e] - mean) * (g[e] - mean);
-    const double sd = std::sqrt(ss / (E - 1)), m = mean + 1e-8;
-    val = lam * sd / m;
-    for (int e = 0; e < E; ++e)
-      dB[e] = lam * ((sd > 0.0 ? (g[e] - mean) / ((E - 1) * sd) : 0.0) / m - sd / (m * m) / E);
+    sd = std::sqrt(ss / (E - 1));
+  }
+  double val = 0.0;
+  if (variant == 0) {
+    if (E > 1) {
+      const double m = mean + 1e-8;
+      val = lam * sd / m;
+      for (int e = 0; e < E; ++e)
+        dB[e] = lam * ((sd > 0.0 ? (g[e] - mean) / ((E - 1) * sd) : 0.0) / m - sd / (m * m) / E);
+    }
+  } else if (variant == 1) {
+    int top = 0;
+    for (int e = 1; e < E; ++e)
+      if (g[e] > g[top]) top = e;
+    val = lam * (sd + gamma * g[top]);
+    for (int e = 0; e < E; ++e) dB[e] = lam * (E > 1 && sd > 0.0 ? (g[e] - mean) / ((E - 1) * sd) : 0.0);
+    dB[top] += lam * gamma;
+  } else {
+    for (int e = 0; e < E; ++e) {
+      val += f[e] * g[e];
+      dB[e] = lam * f[e];
+    }
+    val *= lam;
   }
   for (long long s = 0; s < S; ++s) dw[s] = idx[s] >= 0 ? dB[idx[s]] / T : 0.0;
   return val;
@@ -556,7 +588,8 @@ struct mo_grads {
 };
 
 // The training step's backward with the default routing (softmax over the
-// selected logits, slot-major capacity) and the CV balance term:
+// selected logits, slot-major capacity) and the balance term of
+// c->balance (mo_balance_term_grad):
 //   per slot, G[t,j] = [kept] <dY[t], FFN_e(x[t])> + dB/dw[t,j];
 //   dl[t, idx_j] = w_j (G_j - sum_j' w_j' G_j') (the softmax over the
 //   selected logits), other logits 0;
@@ -566,7 +599,7 @@ struct mo_grads {
 int mo_layer_backward(const mo_config* c, const mo_inputs* in, const void* dY, mo_grads* g) {
   const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
   if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
-      (dt != MO_F32 && dt != MO_BF16))
+      (dt != MO_F32 && dt != MO_BF16) || c->balance < 0 || c->balance > 2)
     return -1;
   const long long S = static_cast<long long>(T) * k, Td = static_cast<long long>(T) * d;
   const int es = dt == MO_BF16 ? 2 : 4;
@@ -651,7 +684,7 @@ int mo_layer_backward(const mo_config* c, const mo_inputs* in, const void* dY, m
     }
   }
   std::vector<double> dB(S);
-  const double B = mo_balance_term_grad(T, k, E, idx.data(), w.data(), c->lam, dB.data());
+  const double B = mo_balance_term_grad(T, k, E, idx.data(), w.data(), c->lam, c->balance, c->gamma, dB.data());
   for (long long s = 0; s < S; ++s) G[s] += dB[s];
   // the logit gradient: the softmax over the selected logits
   for (int t = 0; t < T; ++t) {

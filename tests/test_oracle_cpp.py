@@ -237,13 +237,16 @@ def test_expert_ffn_backward_against_autograd(act):
                                    err_msg=key)
 
 
-def test_balance_term_grad_against_autograd():
-    """The CV balance term on the importance and its per-slot weight
-    gradient, against torch autograd of lambda * std(I/T) / (mean(I/T) +
-    1e-8) in fp64 (an unrouted slot, -1, has none); equal importances give
-    a zero term."""
+@pytest.mark.parametrize("variant", ["cv", "std_max", "switch"])
+def test_balance_term_grad_against_autograd(variant):
+    """The balance term on the importance g = I/T and its per-slot weight
+    gradient, against torch autograd in fp64 (an unrouted slot, -1, has
+    none): cv lambda * std(g) / (mean(g) + 1e-8); std_max lambda * (std(g)
+    + gamma * max(g)) with a unique largest g; switch lambda * sum f g with
+    the usage f = counts / T held constant.  Equal importances give a zero
+    CV term."""
     rng = np.random.default_rng(41)
-    T, k, E, lam = 30, 2, 5, 0.01
+    T, k, E, lam, gamma = 30, 2, 5, 0.01, 100.0
     idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     idx[4] = -1
     w = rng.uniform(0.1, 0.9, size=(T, k))
@@ -254,37 +257,62 @@ def test_balance_term_grad_against_autograd():
             if idx[t, j] >= 0:
                 onehot[t, j, idx[t, j]] = 1.0
     gI = (wt[:, :, None] * onehot).sum(dim=(0, 1)) / T
-    B = lam * gI.std(unbiased=True) / (gI.mean() + 1e-8)
+    if variant == "cv":
+        B = lam * gI.std(unbiased=True) / (gI.mean() + 1e-8)
+    elif variant == "std_max":
+        assert int((gI == gI.max()).sum()) == 1
+        B = lam * (gI.std(unbiased=True) + gamma * gI.max())
+    else:
+        f = onehot.sum(dim=(0, 1)) / T
+        B = lam * (f * gI).sum()
     B.backward()
-    val, dw = cpp.balance_term_grad(idx, w, E, T, lam)
-    assert abs(val - float(B.detach())) <= 1e-15
-    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=0, atol=1e-15)
+    val, dw = cpp.balance_term_grad(idx, w, E, T, lam, variant, gamma)
+    assert abs(val - float(B.detach())) <= 1e-13 * max(1.0, abs(float(B.detach())))
+    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=0, atol=1e-13)
     assert (dw[4] == 0).all()
-    val, dw = cpp.balance_term_grad(np.array([[0], [1]], dtype=np.int32), np.array([[0.5], [0.5]]), 2, 2, lam)
-    assert val == 0.0 and np.all(np.abs(dw) <= 1e-6)
+    if variant == "cv":
+        val, dw = cpp.balance_term_grad(np.array([[0], [1]], dtype=np.int32), np.array([[0.5], [0.5]]), 2, 2, lam)
+        assert val == 0.0 and np.all(np.abs(dw) <= 1e-6)
+
+
+def test_balance_std_max_tie_goes_to_lower_index():
+    """With two experts tied for the largest importance, the max's
+    (sub)gradient goes to the lower expert index, as in the numpy oracle:
+    slots of expert 1 carry lambda*gamma/T more than slots of expert 3."""
+    T, lam, gamma = 4, 0.01, 100.0
+    idx = np.array([[1, 3], [3, 1], [0, 2], [2, 0]], dtype=np.int32)
+    w = np.array([[0.6, 0.4], [0.6, 0.4], [0.3, 0.2], [0.1, 0.2]])
+    _, dw = cpp.balance_term_grad(idx, w, 4, T, lam, "std_max", gamma)
+    # I = [0.5, 1.0, 0.3, 1.0]: experts 1 and 3 tie at the top, with the same std part
+    assert abs((dw[0, 0] - dw[0, 1]) - lam * gamma / T) <= 1e-15
+    _, dn = O.balance_term_grad(idx, w, 4, T, lam, "std_max", gamma)
+    np.testing.assert_allclose(dw, dn, rtol=0, atol=1e-15)
 
 
 BACKWARD_LAYERS = [
     # GeLU in fp32 with biases, no capacity limit
-    S.WORKLOADS["tiny_fp32"].replace(T=24, d=16, h=24, seed=43, training=True),
+    (S.WORKLOADS["tiny_fp32"].replace(T=24, d=16, h=24, seed=43, training=True), "cv"),
     # SwiGLU in bf16 with the shared expert, Gumbel noise and a binding capacity
-    S.WORKLOADS["training"].replace(T=64, d=24, h=32, E=6, capacity_factor=0.7, seed=47),
+    (S.WORKLOADS["training"].replace(T=64, d=24, h=32, E=6, capacity_factor=0.7, seed=47), "cv"),
+    # the other balance terms, with a lambda large enough to show
+    (S.WORKLOADS["training"].replace(T=48, d=16, h=24, E=5, capacity_factor=0.8, lam=0.3, seed=61), "std_max"),
+    (S.WORKLOADS["tiny_fp32"].replace(T=24, d=16, h=24, lam=0.3, seed=67, training=True), "switch"),
 ]
 
 
-def _bwd_cfg(wl):
+def _bwd_cfg(wl, balance="cv"):
     return dict(T=wl.T, d=wl.d, h=wl.h, E=wl.E, k=wl.k, act=wl.act,
                 capacity_factor=float(np.float32(wl.capacity_factor)), min_capacity=wl.min_capacity,
-                lam=float(np.float32(wl.lam)), has_shared=wl.has_shared)
+                lam=float(np.float32(wl.lam)), has_shared=wl.has_shared, balance=balance, gamma=100.0)
 
 
-@pytest.mark.parametrize("wl", BACKWARD_LAYERS, ids=lambda w: w.name)
-def test_layer_backward_matches_numpy_oracle(wl):
+@pytest.mark.parametrize("wl,balance", BACKWARD_LAYERS, ids=lambda p: p.name if hasattr(p, "name") else p)
+def test_layer_backward_matches_numpy_oracle(wl, balance):
     """Every gradient, the logit gradient, y and the loss of the C++
     backward equal the numpy oracle's (itself pinned by finite differences)
-    to 1e-11 of each tensor's largest entry."""
+    to 1e-11 of each tensor's largest entry, for each balance term."""
     t = S.make_inputs(wl, "cpu")
-    cfg = _bwd_cfg(wl)
+    cfg = _bwd_cfg(wl, balance)
     c = cpp.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
     n = O.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
     keys = [k_ for k_ in c if k_ not in ("loss", "balance_term")]
@@ -293,7 +321,7 @@ def test_layer_backward_matches_numpy_oracle(wl):
         scale = max(1e-3, float(np.abs(n[key]).max()))
         np.testing.assert_allclose(c[key], n[key], rtol=0, atol=1e-11 * scale, err_msg=key)
     assert abs(c["loss"] - n["loss"]) <= 1e-11 * max(1.0, abs(n["loss"]))
-    assert abs(c["balance_term"] - n["balance_term"]) <= 1e-15
+    assert abs(c["balance_term"] - n["balance_term"]) <= 1e-14 * max(1.0, abs(n["balance_term"]))
     if wl.capacity_factor > 0:
         assert (n["route"]["pos"] < 0).any()  # a dropped slot takes part
 
