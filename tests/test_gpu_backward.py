@@ -1,5 +1,6 @@
 """Parity of the layer backward (moe_layer_bwd through the C ABI) with the
-fp64 oracle's gradients of L = <dY, y> + lambda * CV(I/T).
+fp64 oracles' gradients of L = <dY, y> + lambda * CV(I/T) (the numpy
+oracle, and the C++ oracle's mo_layer_backward).
 
 Tolerances (bf16 storage, fp32 accumulation), the stated bf16 bounds:
 - dX: relative-Frobenius 1e-2 and max-abs 2e-2 (rows of unit scale).  The
@@ -27,6 +28,7 @@ import torch
 import moe_synth as S
 import sparse_mixture_experts_sum_b300 as M
 from moe_testlib import guarded_inputs, max_abs, oracle_cfg, rel_frob, to_np
+from oracle import cpp
 from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -119,6 +121,33 @@ def test_swiglu_backward_small(shared, noise, cf):
     np.testing.assert_array_equal(sv["pos"].cpu().numpy(), ref["route"]["pos"])
     if cf > 0:
         assert (ref["route"]["pos"] < 0).any()
+    check_all(wl, t, dY, g, ref)
+
+
+@pytest.mark.parametrize("act,balance,lam", [("swiglu", "cv", 0.01), ("gelu", "cv", 0.01),
+                                             ("swiglu", "std_max", 0.5), ("swiglu", "switch", 0.5)])
+def test_backward_against_cpp_oracle(act, balance, lam):
+    """The same gradients against the single-threaded C++ fp64 oracle
+    (mo_layer_backward): the shared expert, Gumbel noise and a binding
+    capacity; GeLU with biases on every expert; each balance term.  The
+    routing (pos) equals the C++ oracle's bit for bit."""
+    wl = _workload(act=act, has_shared=True, gumbel=True, capacity_factor=1.0, lam=lam, seed=79)
+    t = guarded_inputs(wl, "cpu")
+    dY = t.pop("dY")
+    if act == "gelu":
+        gen = torch.Generator().manual_seed(11)
+        bf = torch.bfloat16
+        for n, shape in (("b1", (wl.E, wl.h)), ("b2", (wl.E, wl.d)), ("bs1", (wl.h,)), ("bs2", (wl.d,))):
+            t[n] = (torch.randn(*shape, generator=gen) * 0.2).to(bf)
+    td = {n: v.to(DEV) for n, v in t.items()}
+    route = {} if balance == "cv" else dict(balance=balance, balance_gamma=100.0)
+    _, sv, g = run_fwd_bwd(wl, td, dY.to(DEV), **route)
+    w = {n: t[n] for n in WEIGHT_NAMES if t.get(n) is not None and n != "expert_bias"}
+    cfg = oracle_cfg(wl, **route)
+    ref = cpp.layer_backward(cfg, w, t["x"], dY, t.get("expert_bias"), t.get("noise"))
+    fwd = cpp.layer_forward(dict(cfg, balance="cv"), w, t["x"], t.get("expert_bias"), t.get("noise"))
+    np.testing.assert_array_equal(sv["pos"].cpu().numpy(), fwd["pos"])
+    assert (fwd["pos"] < 0).any()
     check_all(wl, t, dY, g, ref)
 
 
