@@ -44,10 +44,18 @@ class _Config(ctypes.Structure):
                 ("k", ctypes.c_int), ("act", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("min_capacity", ctypes.c_int), ("has_shared", ctypes.c_int),
                 ("capacity_factor", ctypes.c_float), ("lam", ctypes.c_double), ("balance", ctypes.c_int),
-                ("gamma", ctypes.c_double)]
+                ("gamma", ctypes.c_double), ("route", ctypes.c_int)]
 
 
 BALANCE = {"cv": 0, "std_max": 1, "switch": 2}
+ROUTE_BITS = {"raw_probs": 1, "token_major": 2, "layernorm": 4}
+
+
+def _route(cfg: dict) -> int:
+    """mo_config.route of an oracle cfg (rerouting is the numpy oracle's only)."""
+    if cfg.get("reroute"):
+        raise ValueError("rerouting is the numpy oracle's only")
+    return sum(bit for name, bit in ROUTE_BITS.items() if cfg.get(name))
 
 
 class _Inputs(ctypes.Structure):
@@ -89,6 +97,10 @@ def lib() -> ctypes.CDLL:
             "mo_layer_forward": ([ctypes.POINTER(_Config), ctypes.POINTER(_Inputs), ctypes.POINTER(_Outputs)], i),
             "mo_expert_ffn_backward": ([i, i, i, i, i] + [vp] * 14, None),
             "mo_balance_term_grad": ([i, i, i, vp, vp, d, i, d, vp], d),
+            "mo_layer_norm": ([i, i, i, vp, vp], None),
+            "mo_layer_norm_backward": ([i, i, i, vp, vp, vp], None),
+            "mo_top_k_probs": ([i, i, i, vp, i, vp, vp], i),
+            "mo_assign_capacity_token_major": ([i, i, i, i, vp, vp, vp], None),
             "mo_layer_backward": ([ctypes.POINTER(_Config), ctypes.POINTER(_Inputs), vp, ctypes.POINTER(_Grads)],
                                   i),
         }
@@ -236,8 +248,8 @@ STATS = ("routed_slots", "kept_slots", "dropped_slots", "capacity", "drop_rate",
 
 def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None) -> dict:
     """The whole forward pass (the CV statistic).  cfg: T, d, h, E, k, act,
-    capacity_factor, min_capacity, lam, has_shared (as for
-    moe_oracle.layer_forward);
+    capacity_factor, min_capacity, lam, has_shared and the routing flags
+    raw_probs, token_major, layernorm (as for moe_oracle.layer_forward);
     weights: Wr, W1, W3, b1, W2, b2, Ws1, Ws3, bs1, Ws2, bs2 (stored
     tensors, absent or None where the layer has none)."""
     if cfg.get("balance", "cv") != "cv":
@@ -257,7 +269,7 @@ def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None) -> 
     c = _Config(T=T, d=d, h=cfg["h"], E=E, k=k, act=ACT[cfg["act"]], dtype=dt,
                 min_capacity=int(cfg.get("min_capacity", 0)), has_shared=int(bool(cfg.get("has_shared"))),
                 capacity_factor=float(np.float32(cfg.get("capacity_factor", 0.0))),
-                lam=float(cfg.get("lam", 0.01)))
+                lam=float(cfg.get("lam", 0.01)), route=_route(cfg))
     r = dict(y=np.empty((T, d)), idx=np.empty((T, k), dtype=np.int32), w=np.empty((T, k)),
              counts=np.empty(E, dtype=np.int64), kept=np.empty(E, dtype=np.int64),
              offsets=np.empty(E + 1, dtype=np.int64), pos=np.empty((T, k), dtype=np.int64),
@@ -308,14 +320,12 @@ def balance_term_grad(idx: np.ndarray, w: np.ndarray, E: int, T: int, lam: float
 
 
 def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None) -> dict:
-    """Gradients of L = <dY, y> + B(I/T) with the default routing and the
-    balance term of cfg["balance"] (cv, std_max or switch, with cfg["gamma"];
-    cfg and weights as for layer_forward; dY [T,d] stored like x).  Keys as moe_oracle.layer_backward's: dX, dWr, dW1, dW2, dW3 or
+    """Gradients of L = <dY, y> + B(I/T) with the routing of cfg (raw_probs,
+    token_major, layernorm; not reroute) and the balance term of
+    cfg["balance"] (cv, std_max or switch, with cfg["gamma"]; cfg and
+    weights as for layer_forward; dY [T,d] stored like x).  Keys as moe_oracle.layer_backward's: dX, dWr, dW1, dW2, dW3 or
     db1/db2, the shared expert's dWs1, dWs2, dWs3 or dbs1/dbs2, dlogits, y,
     loss, balance_term."""
-    for flag in ("raw_probs", "token_major", "layernorm", "reroute"):
-        if cfg.get(flag):
-            raise ValueError(f"the C++ oracle's backward has the default routing only (not {flag})")
     T, d, h, E, k = cfg["T"], cfg["d"], cfg["h"], cfg["E"], cfg["k"]
     act = cfg["act"]
     px, dt, kx = _stored(x)
@@ -335,7 +345,7 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
                 min_capacity=int(cfg.get("min_capacity", 0)), has_shared=int(bool(cfg.get("has_shared"))),
                 capacity_factor=float(np.float32(cfg.get("capacity_factor", 0.0))),
                 lam=float(cfg.get("lam", 0.01)), balance=BALANCE[cfg.get("balance", "cv")],
-                gamma=float(cfg.get("gamma", 100.0)))
+                gamma=float(cfg.get("gamma", 100.0)), route=_route(cfg))
     r = dict(dX=np.empty((T, d)), dWr=np.empty((E, d)), dW1=np.empty((E, h, d)), dW2=np.empty((E, d, h)),
              dlogits=np.empty((T, E)), y=np.empty((T, d)))
     if act == "swiglu":
@@ -356,3 +366,42 @@ def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None
         raise ValueError("invalid configuration for the C++ oracle")
     r["loss"], r["balance_term"] = g.loss, g.balance
     return r
+
+
+def layer_norm(x) -> np.ndarray:
+    """Row-wise layer norm of the stored x [T,d] in fp64 (eps 1e-5)."""
+    px, dt, kx = _stored(x)
+    T, d = kx.shape
+    n = np.empty((T, d))
+    lib().mo_layer_norm(T, d, dt, px, n.ctypes.data)
+    return n
+
+
+def layer_norm_backward(x, g: np.ndarray) -> np.ndarray:
+    """d<g, layer_norm(x)>/dx for the stored x [T,d]."""
+    px, dt, kx = _stored(x)
+    T, d = kx.shape
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    dx = np.zeros((T, d))
+    lib().mo_layer_norm_backward(T, d, dt, px, g.ctypes.data, dx.ctypes.data)
+    return dx
+
+
+def top_k_probs(l: np.ndarray, k: int, raw: bool):
+    """top_k with raw probabilities (the softmax over all E, not renormalised) when raw."""
+    l = np.ascontiguousarray(l, dtype=np.float64)
+    T, E = l.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    nf = lib().mo_top_k_probs(T, E, k, l.ctypes.data, int(bool(raw)), idx.ctypes.data, w.ctypes.data)
+    return idx, w, nf
+
+
+def assign_capacity_token_major(idx: np.ndarray, E: int, C: int):
+    """(rank [T,k] int32, fill [E] int64), token-major priority."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    T, k = idx.shape
+    rank = np.empty((T, k), dtype=np.int32)
+    fill = np.empty(E, dtype=np.int64)
+    lib().mo_assign_capacity_token_major(T, k, E, C, idx.ctypes.data, rank.ctypes.data, fill.ctypes.data)
+    return rank, fill

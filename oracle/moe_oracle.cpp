@@ -1,6 +1,5 @@
 // Plain fp64 CPU oracle of the sparse Mixture-of-Experts FFN layer's
-// forward pass and, with the default routing, its backward, in
-// single-threaded C++.
+// forward pass and its backward, in single-threaded C++.
 //
 // TEST INFRASTRUCTURE ONLY.  This is a checker: the tests, the smoke check
 // and the benchmark's CPU-baseline leg may call it; the CUDA library never
@@ -35,9 +34,10 @@
 // is the exact erf form; SwiGLU is W2 (silu(W1 v) * (W3 v)); the shared
 // expert is added with weight 1; usage statistic lambda * std_{n-1}(f) /
 // (mean(f) + 1e-8) on pre-capacity counts f = counts / T; a token with a
-// non-finite logit is routed to no expert.  The routing variants (raw
-// probabilities, token-major priority, rerouting, a LayerNorm in front,
-// other balance statistics) are checked by the numpy oracle only.
+// non-finite logit is routed to no expert.  Of the routing variants, raw
+// probabilities, token-major priority and a LayerNorm in front are here
+// too (mo_config.route); rerouting and the forward's other balance
+// statistics are the numpy oracle's only.
 
 #include <cmath>
 #include <cstdint>
@@ -95,13 +95,88 @@ void mo_router_logits(int T, int d, int E, int dtype, const void* x, const void*
   }
 }
 
+// Row-wise layer norm of the stored x [T,d] into fp64 rows n [T,d]:
+// (x - mean) / sqrt(var + 1e-5), var the biased (1/d) variance -- [P2] 5.2's
+// LayerNorm in front of the router, at its initial identity scale and zero
+// shift.
+void mo_layer_norm(int T, int d, int dtype, const void* x, double* n) {
+  for (int t = 0; t < T; ++t) {
+    double mu = 0.0;
+    for (int i = 0; i < d; ++i) mu += rd(x, dtype, static_cast<long long>(t) * d + i);
+    mu /= d;
+    double var = 0.0;
+    for (int i = 0; i < d; ++i) {
+      const double c = rd(x, dtype, static_cast<long long>(t) * d + i) - mu;
+      var += c * c;
+    }
+    var /= d;
+    const double r = 1.0 / std::sqrt(var + 1e-5);
+    for (int i = 0; i < d; ++i)
+      n[static_cast<long long>(t) * d + i] = (rd(x, dtype, static_cast<long long>(t) * d + i) - mu) * r;
+  }
+}
+
+// The gradient with respect to x of <g, layer_norm(x)>, added to dx [T,d]:
+// with n the normalised row and r = 1 / sqrt(var + 1e-5), the chain rule of
+// the row normalisation gives r (g - mean(g) - n mean(g n)).
+void mo_layer_norm_backward(int T, int d, int dtype, const void* x, const double* g, double* dx) {
+  std::vector<double> n(static_cast<size_t>(d));
+  for (int t = 0; t < T; ++t) {
+    double mu = 0.0;
+    for (int i = 0; i < d; ++i) mu += rd(x, dtype, static_cast<long long>(t) * d + i);
+    mu /= d;
+    double var = 0.0;
+    for (int i = 0; i < d; ++i) {
+      const double c = rd(x, dtype, static_cast<long long>(t) * d + i) - mu;
+      var += c * c;
+    }
+    var /= d;
+    const double r = 1.0 / std::sqrt(var + 1e-5);
+    const double* gt = g + static_cast<long long>(t) * d;
+    double gm = 0.0, gn = 0.0;
+    for (int i = 0; i < d; ++i) {
+      n[i] = (rd(x, dtype, static_cast<long long>(t) * d + i) - mu) * r;
+      gm += gt[i];
+      gn += gt[i] * n[i];
+    }
+    gm /= d;
+    gn /= d;
+    for (int i = 0; i < d; ++i) dx[static_cast<long long>(t) * d + i] += r * (gt[i] - gm - n[i] * gn);
+  }
+}
+
+// Router logits from fp64 rows xr [T,d] (the layer-normed x): l[t,e] = sum_i
+// xr[t,i] Wr[e,i] (+ bias[e]) (+ noise[t,e]), Wr stored in `dtype`.
+void mo_router_logits_rows(int T, int d, int E, int dtype, const double* xr, const void* Wr, const float* bias,
+                           const float* noise, double* l) {
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int i = 0; i < d; ++i)
+        s += xr[static_cast<long long>(t) * d + i] * rd(Wr, dtype, static_cast<long long>(e) * d + i);
+      if (bias) s += bias[e];
+      if (noise) s += noise[static_cast<long long>(t) * E + e];
+      l[static_cast<long long>(t) * E + e] = s;
+    }
+  }
+}
+
 // Top-k experts per token by (logit descending, index ascending) -- softmax
 // is monotone, so this is [P1] 4.2's top-k of the probabilities -- and their
 // weights w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0), the softmax of the
 // selected logits ([P1] 3.3: p_i / (p_i + p_j); [P3] 3.3).  A token with a
 // non-finite logit gets idx = -1 and w = 0 in every slot.  Returns the
 // number of such tokens.
+int mo_top_k_probs(int T, int E, int k, const double* l, int raw, int* idx, double* w);
+
 int mo_top_k(int T, int E, int k, const double* l, int* idx, double* w) {
+  return mo_top_k_probs(T, E, k, l, 0, idx, w);
+}
+
+// mo_top_k with raw != 0: the weights are the selected entries of the
+// softmax over all E experts, not renormalised ([P2] 3.2: output = p1 e1 +
+// p2 e2; [P4] 5.1 uses the top-k probabilities as they are).
+int mo_top_k_probs(int T, int E, int k, const double* l, int raw, int* idx, double* w) {
   int nonfinite = 0;
   std::vector<char> taken(E);
   for (int t = 0; t < T; ++t) {
@@ -126,7 +201,10 @@ int mo_top_k(int T, int E, int k, const double* l, int* idx, double* w) {
       it[j] = best;
     }
     double z = 0.0;
-    for (int j = 0; j < k; ++j) z += std::exp(lt[it[j]] - lt[it[0]]);
+    if (raw)
+      for (int e = 0; e < E; ++e) z += std::exp(lt[e] - lt[it[0]]);
+    else
+      for (int j = 0; j < k; ++j) z += std::exp(lt[it[j]] - lt[it[0]]);
     for (int j = 0; j < k; ++j) wt[j] = std::exp(lt[it[j]] - lt[it[0]]) / z;
   }
   return nonfinite;
@@ -211,6 +289,17 @@ void mo_assign_capacity(int T, int k, int E, int C, const int* idx, int* rank, l
       if (e >= 0 && fill[e] < C) rank[s] = static_cast<int>(fill[e]++);
       else rank[s] = -1;
     }
+  }
+}
+
+// The same queue in token-major priority: token 0's choices in order, then
+// token 1's, and so on.
+void mo_assign_capacity_token_major(int T, int k, int E, int C, const int* idx, int* rank, long long* fill) {
+  for (int e = 0; e < E; ++e) fill[e] = 0;
+  for (long long s = 0; s < static_cast<long long>(T) * k; ++s) {
+    const int e = idx[s];
+    if (e >= 0 && fill[e] < C) rank[s] = static_cast<int>(fill[e]++);
+    else rank[s] = -1;
   }
 }
 
@@ -321,7 +410,12 @@ struct mo_config {
   double lam;
   int balance;   // the backward's balance term: 0 CV, 1 std + max, 2 switch (the forward's statistic is CV)
   double gamma;  // its max weight (std + max)
+  int route;     // MO_RAW_PROBS | MO_TOKEN_MAJOR | MO_LAYERNORM
 };
+
+enum { MO_RAW_PROBS = 1, MO_TOKEN_MAJOR = 2, MO_LAYERNORM = 4 };
+
+
 
 // Stored inputs (pointers in the config's dtype unless noted; null where
 // absent).  W1/W3 [E,h,d], W2 [E,d,h], b1 [E,h], b2 [E,d]; the shared
@@ -343,6 +437,29 @@ struct mo_outputs {
   double* stats;
 };
 
+// The routing of a layer, shared by the forward and the backward: logits
+// (from the layer-normed x with MO_LAYERNORM), top-k and weights, usage
+// counts, capacity, ranks in the configured priority, positions.
+static int route_layer(const mo_config* c, const mo_inputs* in, double* l, int* idx, double* w, long long* counts,
+                       int* rank, long long* kept, long long* offsets, long long* pos, int* C_out) {
+  const int T = c->T, d = c->d, E = c->E, k = c->k, dt = c->dtype;
+  if (c->route & MO_LAYERNORM) {
+    std::vector<double> n(static_cast<size_t>(T) * d);
+    mo_layer_norm(T, d, dt, in->x, n.data());
+    mo_router_logits_rows(T, d, E, dt, n.data(), in->Wr, in->bias, in->noise, l);
+  } else {
+    mo_router_logits(T, d, E, dt, in->x, in->Wr, in->bias, in->noise, l);
+  }
+  const int nonfinite = mo_top_k_probs(T, E, k, l, (c->route & MO_RAW_PROBS) != 0, idx, w);
+  mo_usage_counts(T, k, E, idx, counts);
+  const int C = mo_capacity(T, k, E, c->capacity_factor, c->min_capacity);
+  if (c->route & MO_TOKEN_MAJOR) mo_assign_capacity_token_major(T, k, E, C, idx, rank, kept);
+  else mo_assign_capacity(T, k, E, C, idx, rank, kept);
+  mo_dispatch_positions(T, k, E, idx, rank, kept, offsets, pos);
+  *C_out = C;
+  return nonfinite;
+}
+
 // The whole forward pass, steps in the pages' order: logits, top-k and
 // weights, usage counts, capacity, dispatch positions, each kept slot
 // through its expert, the shared expert, the combine, the statistics.
@@ -350,18 +467,15 @@ struct mo_outputs {
 int mo_layer_forward(const mo_config* c, const mo_inputs* in, mo_outputs* out) {
   const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
   if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
-      (dt != MO_F32 && dt != MO_BF16) || c->balance != 0)
+      (dt != MO_F32 && dt != MO_BF16) || c->balance != 0 || (c->route & ~7))
     return -1;
   const long long S = static_cast<long long>(T) * k;
   const int es = dt == MO_BF16 ? 2 : 4;
   std::vector<double> l(static_cast<size_t>(T) * E);
-  mo_router_logits(T, d, E, dt, in->x, in->Wr, in->bias, in->noise, l.data());
-  const int nonfinite = mo_top_k(T, E, k, l.data(), out->idx, out->w);
-  mo_usage_counts(T, k, E, out->idx, out->counts);
-  const int C = mo_capacity(T, k, E, c->capacity_factor, c->min_capacity);
   std::vector<int> rank(S);
-  mo_assign_capacity(T, k, E, C, out->idx, rank.data(), out->kept);
-  mo_dispatch_positions(T, k, E, out->idx, rank.data(), out->kept, out->offsets, out->pos);
+  int C = 0;
+  const int nonfinite = route_layer(c, in, l.data(), out->idx, out->w, out->counts, rank.data(), out->kept,
+                                    out->offsets, out->pos, &C);
 
   // dispatch ([P1] 4.2 step 2: the tokens bound for the same expert grouped
   // together): the stored row of x[t] copied to row pos[t,j] of Xp; then
@@ -587,9 +701,10 @@ struct mo_grads {
   double loss, balance;
 };
 
-// The training step's backward with the default routing (softmax over the
-// selected logits, slot-major capacity) and the balance term of
-// c->balance (mo_balance_term_grad):
+// The training step's backward with the routing of c->route (raw
+// probabilities, token-major priority, a LayerNorm in front; rerouting is
+// the numpy oracle's only) and the balance term of c->balance
+// (mo_balance_term_grad):
 //   per slot, G[t,j] = [kept] <dY[t], FFN_e(x[t])> + dB/dw[t,j];
 //   dl[t, idx_j] = w_j (G_j - sum_j' w_j' G_j') (the softmax over the
 //   selected logits), other logits 0;
@@ -599,7 +714,7 @@ struct mo_grads {
 int mo_layer_backward(const mo_config* c, const mo_inputs* in, const void* dY, mo_grads* g) {
   const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
   if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
-      (dt != MO_F32 && dt != MO_BF16) || c->balance < 0 || c->balance > 2)
+      (dt != MO_F32 && dt != MO_BF16) || c->balance < 0 || c->balance > 2 || (c->route & ~7))
     return -1;
   const long long S = static_cast<long long>(T) * k, Td = static_cast<long long>(T) * d;
   const int es = dt == MO_BF16 ? 2 : 4;
@@ -607,12 +722,9 @@ int mo_layer_backward(const mo_config* c, const mo_inputs* in, const void* dY, m
   std::vector<double> l(static_cast<size_t>(T) * E), w(S);
   std::vector<int> idx(S), rank(S);
   std::vector<long long> counts(E), kept(E), offsets(E + 1), pos(S);
-  mo_router_logits(T, d, E, dt, in->x, in->Wr, in->bias, in->noise, l.data());
-  mo_top_k(T, E, k, l.data(), idx.data(), w.data());
-  mo_usage_counts(T, k, E, idx.data(), counts.data());
-  const int C = mo_capacity(T, k, E, c->capacity_factor, c->min_capacity);
-  mo_assign_capacity(T, k, E, C, idx.data(), rank.data(), kept.data());
-  mo_dispatch_positions(T, k, E, idx.data(), rank.data(), kept.data(), offsets.data(), pos.data());
+  int C = 0;
+  route_layer(c, in, l.data(), idx.data(), w.data(), counts.data(), rank.data(), kept.data(), offsets.data(),
+              pos.data(), &C);
 
   std::vector<double> dy(Td);
   for (long long i = 0; i < Td; ++i) dy[i] = rd(dY, dt, i);
@@ -686,25 +798,50 @@ int mo_layer_backward(const mo_config* c, const mo_inputs* in, const void* dY, m
   std::vector<double> dB(S);
   const double B = mo_balance_term_grad(T, k, E, idx.data(), w.data(), c->lam, c->balance, c->gamma, dB.data());
   for (long long s = 0; s < S; ++s) G[s] += dB[s];
-  // the logit gradient: the softmax over the selected logits
+  // the logit gradient: the softmax over the selected logits, dl[t, idx_j]
+  // = w_j (G_j - sum_j' w_j' G_j'); with raw probabilities (w_j = p_{idx_j}
+  // of the softmax over all E) every logit e gets p_e ([e selected] G_e -
+  // sum_j w_j G_j)
+  const bool raw = (c->route & MO_RAW_PROBS) != 0;
+  std::vector<double> p(static_cast<size_t>(E));
   for (int t = 0; t < T; ++t) {
     const long long s0 = static_cast<long long>(t) * k;
     if (idx[s0] < 0) continue;
     double sum = 0.0;
     for (int j = 0; j < k; ++j) sum += w[s0 + j] * G[s0 + j];
-    for (int j = 0; j < k; ++j) g->dl[static_cast<long long>(t) * E + idx[s0 + j]] += w[s0 + j] * (G[s0 + j] - sum);
+    double* dlt = g->dl + static_cast<long long>(t) * E;
+    if (raw) {
+      const double* lt = l.data() + static_cast<long long>(t) * E;
+      double z = 0.0;
+      for (int e = 0; e < E; ++e) z += std::exp(lt[e] - lt[idx[s0]]);
+      for (int e = 0; e < E; ++e) {
+        p[e] = std::exp(lt[e] - lt[idx[s0]]) / z;
+        dlt[e] = -p[e] * sum;
+      }
+      for (int j = 0; j < k; ++j) dlt[idx[s0 + j]] += p[idx[s0 + j]] * G[s0 + j];
+    } else {
+      for (int j = 0; j < k; ++j) dlt[idx[s0 + j]] += w[s0 + j] * (G[s0 + j] - sum);
+    }
   }
-  // dWr = dl^T x and dX += dl Wr
+  // dWr = dl^T xr and the router's part of dX, xr = x or (MO_LAYERNORM) its
+  // layer-normed rows, whose backward the router's input gradient dl Wr
+  // then goes through
+  const bool ln = (c->route & MO_LAYERNORM) != 0;
+  std::vector<double> xr(ln ? Td : 0), gr(ln ? Td : 0, 0.0);
+  if (ln) mo_layer_norm(T, d, dt, in->x, xr.data());
   for (int e = 0; e < E; ++e) {
     for (int t = 0; t < T; ++t) {
       const double q = g->dl[static_cast<long long>(t) * E + e];
       if (q == 0.0) continue;
+      double* dxr = ln ? gr.data() + static_cast<long long>(t) * d : g->dX + static_cast<long long>(t) * d;
       for (int i = 0; i < d; ++i) {
-        g->dWr[static_cast<long long>(e) * d + i] += q * rd(in->x, dt, static_cast<long long>(t) * d + i);
-        g->dX[static_cast<long long>(t) * d + i] += q * rd(in->Wr, dt, static_cast<long long>(e) * d + i);
+        const long long o = static_cast<long long>(t) * d + i;
+        g->dWr[static_cast<long long>(e) * d + i] += q * (ln ? xr[o] : rd(in->x, dt, o));
+        dxr[i] += q * rd(in->Wr, dt, static_cast<long long>(e) * d + i);
       }
     }
   }
+  if (ln) mo_layer_norm_backward(T, d, dt, in->x, gr.data(), g->dX);
   double ly = 0.0;
   for (long long i = 0; i < Td; ++i) ly += dy[i] * g->y[i];
   g->balance = B;

@@ -124,15 +124,21 @@ def test_swiglu_backward_small(shared, noise, cf):
     check_all(wl, t, dY, g, ref)
 
 
-@pytest.mark.parametrize("act,balance,lam", [("swiglu", "cv", 0.01), ("gelu", "cv", 0.01),
-                                             ("swiglu", "std_max", 0.5), ("swiglu", "switch", 0.5)])
-def test_backward_against_cpp_oracle(act, balance, lam):
+@pytest.mark.parametrize("act,balance,lam,variant", [
+    ("swiglu", "cv", 0.01, {}), ("gelu", "cv", 0.01, {}), ("swiglu", "std_max", 0.5, {}),
+    ("swiglu", "switch", 0.5, {}), ("swiglu", "cv", 0.01, dict(raw_probs=True, token_major=True)),
+    ("swiglu", "cv", 0.01, dict(layernorm=True))], ids=lambda p: p if isinstance(p, str) else
+    ("+".join(p) or "default") if isinstance(p, dict) else str(p))
+def test_backward_against_cpp_oracle(act, balance, lam, variant):
     """The same gradients against the single-threaded C++ fp64 oracle
     (mo_layer_backward): the shared expert, Gumbel noise and a binding
-    capacity; GeLU with biases on every expert; each balance term.  The
+    capacity; GeLU with biases on every expert; each balance term; raw
+    probabilities with token-major priority; a LayerNorm in front of the
+    router (rows with their own offset and scale, dX bounded per row).  The
     routing (pos) equals the C++ oracle's bit for bit."""
-    wl = _workload(act=act, has_shared=True, gumbel=True, capacity_factor=1.0, lam=lam, seed=79)
-    t = guarded_inputs(wl, "cpu")
+    ln = bool(variant.get("layernorm"))
+    wl = _workload(act=act, has_shared=True, gumbel=True, capacity_factor=1.0, lam=lam, seed=79, x_affine=ln)
+    t = guarded_inputs(wl, "cpu", layernorm=ln)
     dY = t.pop("dY")
     if act == "gelu":
         gen = torch.Generator().manual_seed(11)
@@ -140,7 +146,7 @@ def test_backward_against_cpp_oracle(act, balance, lam):
         for n, shape in (("b1", (wl.E, wl.h)), ("b2", (wl.E, wl.d)), ("bs1", (wl.h,)), ("bs2", (wl.d,))):
             t[n] = (torch.randn(*shape, generator=gen) * 0.2).to(bf)
     td = {n: v.to(DEV) for n, v in t.items()}
-    route = {} if balance == "cv" else dict(balance=balance, balance_gamma=100.0)
+    route = dict(variant) if balance == "cv" else dict(variant, balance=balance, balance_gamma=100.0)
     _, sv, g = run_fwd_bwd(wl, td, dY.to(DEV), **route)
     w = {n: t[n] for n in WEIGHT_NAMES if t.get(n) is not None and n != "expert_bias"}
     cfg = oracle_cfg(wl, **route)
@@ -148,7 +154,7 @@ def test_backward_against_cpp_oracle(act, balance, lam):
     fwd = cpp.layer_forward(dict(cfg, balance="cv"), w, t["x"], t.get("expert_bias"), t.get("noise"))
     np.testing.assert_array_equal(sv["pos"].cpu().numpy(), fwd["pos"])
     assert (fwd["pos"] < 0).any()
-    check_all(wl, t, dY, g, ref)
+    check_all(wl, t, dY, g, ref, dx_row_scaled=ln)
 
 
 def test_gelu_backward_with_biases_and_shared():

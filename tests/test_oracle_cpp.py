@@ -368,3 +368,122 @@ def test_layer_backward_finite_differences():
             if done == 3:
                 break
         assert done == 3, name
+
+
+# ----------------------------------------------------------------------------
+# routing variants: raw probabilities, token-major priority, a LayerNorm in
+# front of the router
+# ----------------------------------------------------------------------------
+
+def test_layer_norm_against_torch():
+    """The router's LayerNorm (no affine, eps 1e-5, biased variance) and its
+    input gradient against torch's layer_norm and autograd in fp64, on rows
+    with their own offsets and scales stored in bf16."""
+    g = torch.Generator().manual_seed(71)
+    x = (torch.randn(7, 33, generator=g) * torch.rand(7, 1, generator=g) * 3 + torch.randn(7, 1, generator=g))
+    x = x.to(torch.bfloat16)
+    xd = x.double().requires_grad_(True)
+    ref = torch.nn.functional.layer_norm(xd, (33,), eps=1e-5)
+    np.testing.assert_allclose(cpp.layer_norm(x), ref.detach().numpy(), rtol=0, atol=1e-13)
+    gout = torch.randn(7, 33, generator=g, dtype=torch.float64)
+    (ref * gout).sum().backward()
+    np.testing.assert_allclose(cpp.layer_norm_backward(x, gout.numpy()), xd.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_top_k_raw_probabilities():
+    """With raw probabilities the weights are the selected entries of the
+    softmax over all E experts (torch.softmax), the same experts as the
+    default selection, and sum to at most 1."""
+    rng = np.random.default_rng(73)
+    l = rng.normal(size=(40, 9)) * 2
+    idx0, w0, _ = cpp.top_k(l, 3)
+    idx, w, nf = cpp.top_k_probs(l, 3, raw=True)
+    np.testing.assert_array_equal(idx, idx0)
+    p = torch.softmax(torch.tensor(l), dim=1).numpy()
+    np.testing.assert_allclose(w, np.take_along_axis(p, idx.astype(np.int64), axis=1), rtol=0, atol=1e-15)
+    assert nf == 0 and (w.sum(axis=1) <= 1 + 1e-15).all() and (w.sum(axis=1) < w0.sum(axis=1)).all()
+
+
+def test_token_major_capacity_queue():
+    """Token-major priority: a direct queue over (t, j) in token order; each
+    expert keeps its first C slots in that order."""
+    rng = np.random.default_rng(79)
+    T, k, E, C = 50, 3, 6, 17
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    idx[5] = -1
+    rank, fill = cpp.assign_capacity_token_major(idx, E, C)
+    seen = np.zeros(E, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            want = -1 if e < 0 or seen[e] >= C else seen[e]
+            assert rank[t, j] == want, (t, j)
+            if want >= 0:
+                seen[e] += 1
+    np.testing.assert_array_equal(fill, seen)
+    assert (fill == C).any()
+
+
+VARIANT_ROUTES = [dict(raw_probs=True), dict(token_major=True), dict(layernorm=True),
+                  dict(raw_probs=True, token_major=True, layernorm=True)]
+
+
+@pytest.mark.parametrize("route", VARIANT_ROUTES, ids=lambda r: "+".join(r))
+def test_routing_variants_match_numpy_oracle(route):
+    """Forward and backward of a SwiGLU bf16 layer with the shared expert, a
+    binding capacity and Gumbel noise, under each routing variant: routing
+    bit for bit and every output and gradient to 1e-11 of the numpy
+    oracle's."""
+    wl = S.WORKLOADS["training"].replace(T=64, d=24, h=32, E=6, capacity_factor=0.7, seed=83)
+    t = S.make_inputs(wl, "cpu")
+    cfg = dict(_bwd_cfg(wl), **route)
+    c = cpp.layer_forward(dict(cfg), t, t["x"], t.get("expert_bias"), t.get("noise"))
+    n = O.layer_forward(cfg, t, t["x"], t.get("expert_bias"), t.get("noise"))
+    for key in ("idx", "counts", "kept", "offsets", "pos"):
+        np.testing.assert_array_equal(c[key], n[key], err_msg=key)
+    np.testing.assert_allclose(c["w"], n["w"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(c["y"], n["y"], rtol=0, atol=1e-12 * max(1.0, float(np.abs(n["y"]).max())))
+    assert (c["pos"] < 0).any()
+    cb = cpp.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
+    nb = O.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
+    for key in [k_ for k_ in cb if k_ not in ("loss", "balance_term")]:
+        scale = max(1e-3, float(np.abs(nb[key]).max()))
+        np.testing.assert_allclose(cb[key], nb[key], rtol=0, atol=1e-11 * scale, err_msg=key)
+    assert abs(cb["loss"] - nb["loss"]) <= 1e-11 * max(1.0, abs(nb["loss"]))
+
+
+def test_routing_variants_finite_differences():
+    """Central differences of the C++ oracle's loss with raw probabilities
+    and a LayerNorm in front of the router (fp32 storage, 2^-9 steps, the
+    routing checked unchanged) match its x and Wr gradients."""
+    wl = S.WORKLOADS["tiny_fp32"].replace(T=12, d=8, h=12, E=4, has_shared=True, capacity_factor=0.8, seed=89,
+                                          training=True)
+    t = S.make_inputs(wl, "cpu")
+    cfg = dict(_bwd_cfg(wl), raw_probs=True, layernorm=True)
+    base = cpp.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
+    fwd0 = cpp.layer_forward(cfg, t, t["x"], t.get("expert_bias"), t.get("noise"))
+    hstep = 2.0 ** -9
+    rng = np.random.default_rng(97)
+    for name, gname in (("x", "dX"), ("Wr", "dWr")):
+        done = 0
+        for _ in range(60):
+            flat = int(rng.integers(t[name].numel()))
+            vals, same = [], True
+            for sgn in (1, -1):
+                tt = dict(t)
+                a = t[name].clone().reshape(-1)
+                a[flat] += sgn * hstep
+                tt[name] = a.reshape(t[name].shape)
+                f = cpp.layer_forward(cfg, tt, tt["x"], tt.get("expert_bias"), tt.get("noise"))
+                same = same and np.array_equal(f["pos"], fwd0["pos"]) and np.array_equal(f["idx"], fwd0["idx"])
+                vals.append(cpp.layer_backward(cfg, tt, tt["x"], tt["dY"], tt.get("expert_bias"),
+                                               tt.get("noise"))["loss"])
+            if not same:
+                continue
+            fd = (vals[0] - vals[1]) / (2 * hstep)
+            an = float(base[gname].reshape(-1)[flat])
+            assert abs(fd - an) <= 1e-5 * max(1.0, abs(an)), (name, flat, fd, an)
+            done += 1
+            if done == 4:
+                break
+        assert done == 4, name
