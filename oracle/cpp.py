@@ -48,13 +48,11 @@ class _Config(ctypes.Structure):
 
 
 BALANCE = {"cv": 0, "std_max": 1, "switch": 2}
-ROUTE_BITS = {"raw_probs": 1, "token_major": 2, "layernorm": 4}
+ROUTE_BITS = {"raw_probs": 1, "token_major": 2, "layernorm": 4, "reroute": 8}
 
 
 def _route(cfg: dict) -> int:
-    """mo_config.route of an oracle cfg (rerouting is the numpy oracle's only)."""
-    if cfg.get("reroute"):
-        raise ValueError("rerouting is the numpy oracle's only")
+    """mo_config.route of an oracle cfg."""
     return sum(bit for name, bit in ROUTE_BITS.items() if cfg.get(name))
 
 
@@ -101,6 +99,8 @@ def lib() -> ctypes.CDLL:
             "mo_layer_norm_backward": ([i, i, i, vp, vp, vp], None),
             "mo_top_k_probs": ([i, i, i, vp, i, vp, vp], i),
             "mo_assign_capacity_token_major": ([i, i, i, i, vp, vp, vp], None),
+            "mo_backup_experts": ([i, i, i, vp, vp], None),
+            "mo_reroute_overflow": ([i, i, i, i, vp, vp, vp, vp, i, vp, vp, vp], None),
             "mo_layer_backward": ([ctypes.POINTER(_Config), ctypes.POINTER(_Inputs), vp, ctypes.POINTER(_Grads)],
                                   i),
         }
@@ -243,13 +243,14 @@ def balance_stat(counts: np.ndarray, T: int, lam: float) -> float:
 
 
 STATS = ("routed_slots", "kept_slots", "dropped_slots", "capacity", "drop_rate", "balance_stat",
-         "numeric_error", "router_entropy")
+         "numeric_error", "router_entropy", "rerouted_slots")
 
 
 def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None) -> dict:
     """The whole forward pass (the CV statistic).  cfg: T, d, h, E, k, act,
     capacity_factor, min_capacity, lam, has_shared and the routing flags
-    raw_probs, token_major, layernorm (as for moe_oracle.layer_forward);
+    raw_probs, token_major, layernorm, reroute (as for
+    moe_oracle.layer_forward);
     weights: Wr, W1, W3, b1, W2, b2, Ws1, Ws3, bs1, Ws2, bs2 (stored
     tensors, absent or None where the layer has none)."""
     if cfg.get("balance", "cv") != "cv":
@@ -278,7 +279,7 @@ def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None) -> 
     if lib().mo_layer_forward(ctypes.byref(c), ctypes.byref(inp), ctypes.byref(out)) != 0:
         raise ValueError("invalid configuration for the C++ oracle")
     st = dict(zip(STATS, r.pop("stats").tolist()))
-    for n in ("routed_slots", "kept_slots", "dropped_slots", "capacity", "numeric_error"):
+    for n in ("routed_slots", "kept_slots", "dropped_slots", "capacity", "numeric_error", "rerouted_slots"):
         st[n] = int(st[n])
     r["stats"] = st
     return r
@@ -321,7 +322,7 @@ def balance_term_grad(idx: np.ndarray, w: np.ndarray, E: int, T: int, lam: float
 
 def layer_backward(cfg: dict, weights: dict, x, dY, expert_bias=None, noise=None) -> dict:
     """Gradients of L = <dY, y> + B(I/T) with the routing of cfg (raw_probs,
-    token_major, layernorm; not reroute) and the balance term of
+    token_major, layernorm, reroute) and the balance term of
     cfg["balance"] (cv, std_max or switch, with cfg["gamma"]; cfg and
     weights as for layer_forward; dY [T,d] stored like x).  Keys as moe_oracle.layer_backward's: dX, dWr, dW1, dW2, dW3 or
     db1/db2, the shared expert's dWs1, dWs2, dWs3 or dbs1/dbs2, dlogits, y,
@@ -405,3 +406,28 @@ def assign_capacity_token_major(idx: np.ndarray, E: int, C: int):
     fill = np.empty(E, dtype=np.int64)
     lib().mo_assign_capacity_token_major(T, k, E, C, idx.ctypes.data, rank.ctypes.data, fill.ctypes.data)
     return rank, fill
+
+
+def backup_experts(l: np.ndarray, k: int) -> np.ndarray:
+    """Each token's experts ranked k .. 2k-1 [T,k] int32, -1 where none."""
+    l = np.ascontiguousarray(l, dtype=np.float64)
+    T, E = l.shape
+    b = np.empty((T, k), dtype=np.int32)
+    lib().mo_backup_experts(T, E, k, l.ctypes.data, b.ctypes.data)
+    return b
+
+
+def reroute_overflow(idx, backup, rank, fill, C: int, token_major: bool = False):
+    """(served [T,k], rank2 [T,k], fill2 [E]) of the second capacity pass."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    backup = np.ascontiguousarray(backup, dtype=np.int32)
+    rank = np.ascontiguousarray(rank, dtype=np.int32)
+    fill = np.ascontiguousarray(fill, dtype=np.int64)
+    T, k = idx.shape
+    E = fill.shape[0]
+    served = np.empty((T, k), dtype=np.int32)
+    rank2 = np.empty((T, k), dtype=np.int32)
+    fill2 = np.empty(E, dtype=np.int64)
+    lib().mo_reroute_overflow(T, k, E, C, idx.ctypes.data, backup.ctypes.data, rank.ctypes.data, fill.ctypes.data,
+                              int(bool(token_major)), served.ctypes.data, rank2.ctypes.data, fill2.ctypes.data)
+    return served, rank2, fill2

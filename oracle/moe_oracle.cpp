@@ -34,10 +34,10 @@
 // is the exact erf form; SwiGLU is W2 (silu(W1 v) * (W3 v)); the shared
 // expert is added with weight 1; usage statistic lambda * std_{n-1}(f) /
 // (mean(f) + 1e-8) on pre-capacity counts f = counts / T; a token with a
-// non-finite logit is routed to no expert.  Of the routing variants, raw
-// probabilities, token-major priority and a LayerNorm in front are here
-// too (mo_config.route); rerouting and the forward's other balance
-// statistics are the numpy oracle's only.
+// non-finite logit is routed to no expert.  The routing variants -- raw
+// probabilities, token-major priority, a LayerNorm in front, rerouting --
+// are here too (mo_config.route); the forward's other balance statistics
+// are the numpy oracle's only.
 
 #include <cmath>
 #include <cstdint>
@@ -303,6 +303,68 @@ void mo_assign_capacity_token_major(int T, int k, int E, int C, const int* idx, 
   }
 }
 
+// Each token's experts ranked k .. 2k-1 by (logit descending, index
+// ascending): its next-best experts, which slots that overflow can be
+// rerouted to ([P3] 2.3).  -1 where fewer than 2k experts exist or the
+// token has a non-finite logit.  backup [T,k].
+void mo_backup_experts(int T, int E, int k, const double* l, int* backup) {
+  const int nb = std::max(0, std::min(k, E - k));
+  std::vector<char> taken(E);
+  for (int t = 0; t < T; ++t) {
+    const double* lt = l + static_cast<long long>(t) * E;
+    int* bt = backup + static_cast<long long>(t) * k;
+    for (int j = 0; j < k; ++j) bt[j] = -1;
+    if (!all_finite(lt, E)) continue;
+    std::fill(taken.begin(), taken.end(), 0);
+    for (int r = 0; r < k + nb; ++r) {
+      int best = -1;
+      for (int e = 0; e < E; ++e)
+        if (!taken[e] && (best < 0 || lt[e] > lt[best])) best = e;
+      taken[best] = 1;
+      if (r >= k) bt[r - k] = best;
+    }
+  }
+}
+
+// The second capacity pass ([P3] 2.3: tokens beyond capacity are dropped or
+// routed to the next-best expert).  The r-th slot of token t that the first
+// pass dropped (r counted in choice order) tries backup[t,r] once; slots
+// are visited in the first pass's priority order.  It is kept if that
+// expert has room left after the first pass and the slots rerouted to it
+// before, taking the next place after the expert's first-pass rows.
+// served [T,k]: the expert serving each slot (-1 none); rank2 [T,k]: place
+// among the expert's rerouted rows (-1 if not rerouted); fill2 [E]: rerouted
+// rows per expert.
+void mo_reroute_overflow(int T, int k, int E, int C, const int* idx, const int* backup, const int* rank,
+                         const long long* fill, int token_major, int* served, int* rank2, long long* fill2) {
+  const long long S = static_cast<long long>(T) * k;
+  std::vector<int> nth(S, -1);
+  for (int t = 0; t < T; ++t) {
+    int r = 0;
+    for (int j = 0; j < k; ++j) {
+      const long long s = static_cast<long long>(t) * k + j;
+      if (idx[s] >= 0 && rank[s] < 0) nth[s] = r++;
+    }
+  }
+  for (long long s = 0; s < S; ++s) {
+    served[s] = rank[s] >= 0 ? idx[s] : -1;
+    rank2[s] = -1;
+  }
+  for (int e = 0; e < E; ++e) fill2[e] = 0;
+  for (long long q = 0; q < S; ++q) {
+    // q-th slot in priority order: token-major (t, j) = (q / k, q % k), or
+    // slot-major (t, j) = (q % T, q / T)
+    const long long s = token_major ? q : (q % T) * k + q / T;
+    if (nth[s] < 0) continue;
+    const int b = backup[(s / k) * k + nth[s]];
+    if (b < 0) continue;
+    if (fill[b] + fill2[b] < C) {
+      rank2[s] = static_cast<int>(fill2[b]++);
+      served[s] = b;
+    }
+  }
+}
+
 // offsets = the exclusive scan of fill (expert e's rows are [offsets[e],
 // offsets[e+1]) of the expert-contiguous matrix); pos[t,j] = offsets[e] +
 // rank for a kept slot, else -1.
@@ -410,10 +472,10 @@ struct mo_config {
   double lam;
   int balance;   // the backward's balance term: 0 CV, 1 std + max, 2 switch (the forward's statistic is CV)
   double gamma;  // its max weight (std + max)
-  int route;     // MO_RAW_PROBS | MO_TOKEN_MAJOR | MO_LAYERNORM
+  int route;     // MO_RAW_PROBS | MO_TOKEN_MAJOR | MO_LAYERNORM | MO_REROUTE
 };
 
-enum { MO_RAW_PROBS = 1, MO_TOKEN_MAJOR = 2, MO_LAYERNORM = 4 };
+enum { MO_RAW_PROBS = 1, MO_TOKEN_MAJOR = 2, MO_LAYERNORM = 4, MO_REROUTE = 8 };
 
 
 
@@ -427,8 +489,9 @@ struct mo_inputs {
 };
 
 // Outputs: y [T,d], idx/pos [T,k], w [T,k], counts/kept [E], offsets
-// [E+1]; stats[0..7] = routed, kept and dropped slots, capacity, drop rate,
-// balance statistic, tokens with a non-finite logit, mean router entropy.
+// [E+1]; stats[0..8] = routed, kept and dropped slots, capacity, drop rate,
+// balance statistic, tokens with a non-finite logit, mean router entropy,
+// slots the rerouting pass kept.
 struct mo_outputs {
   double* y;
   int* idx;
@@ -439,10 +502,16 @@ struct mo_outputs {
 
 // The routing of a layer, shared by the forward and the backward: logits
 // (from the layer-normed x with MO_LAYERNORM), top-k and weights, usage
-// counts, capacity, ranks in the configured priority, positions.
+// counts, capacity, ranks in the configured priority, with MO_REROUTE the
+// second pass that offers the dropped slots their backups, and positions:
+// each expert's first-pass rows, then its rerouted rows.  served [T,k] is
+// the expert that serves each slot (-1 none); kept [E] counts both passes;
+// *rerouted the slots the second pass kept.
 static int route_layer(const mo_config* c, const mo_inputs* in, double* l, int* idx, double* w, long long* counts,
-                       int* rank, long long* kept, long long* offsets, long long* pos, int* C_out) {
+                       long long* kept, long long* offsets, long long* pos, int* served, int* C_out,
+                       long long* rerouted) {
   const int T = c->T, d = c->d, E = c->E, k = c->k, dt = c->dtype;
+  const long long S = static_cast<long long>(T) * k;
   if (c->route & MO_LAYERNORM) {
     std::vector<double> n(static_cast<size_t>(T) * d);
     mo_layer_norm(T, d, dt, in->x, n.data());
@@ -453,9 +522,31 @@ static int route_layer(const mo_config* c, const mo_inputs* in, double* l, int* 
   const int nonfinite = mo_top_k_probs(T, E, k, l, (c->route & MO_RAW_PROBS) != 0, idx, w);
   mo_usage_counts(T, k, E, idx, counts);
   const int C = mo_capacity(T, k, E, c->capacity_factor, c->min_capacity);
-  if (c->route & MO_TOKEN_MAJOR) mo_assign_capacity_token_major(T, k, E, C, idx, rank, kept);
-  else mo_assign_capacity(T, k, E, C, idx, rank, kept);
-  mo_dispatch_positions(T, k, E, idx, rank, kept, offsets, pos);
+  std::vector<int> rank(S);
+  const bool tm = (c->route & MO_TOKEN_MAJOR) != 0;
+  if (tm) mo_assign_capacity_token_major(T, k, E, C, idx, rank.data(), kept);
+  else mo_assign_capacity(T, k, E, C, idx, rank.data(), kept);
+  *rerouted = 0;
+  if (c->route & MO_REROUTE) {
+    std::vector<int> backup(S), rank2(S);
+    std::vector<long long> fill2(E);
+    mo_backup_experts(T, E, k, l, backup.data());
+    mo_reroute_overflow(T, k, E, C, idx, backup.data(), rank.data(), kept, tm, served, rank2.data(), fill2.data());
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + kept[e] + fill2[e];
+    for (long long s = 0; s < S; ++s) {
+      if (rank[s] >= 0) pos[s] = offsets[idx[s]] + rank[s];
+      else if (rank2[s] >= 0) pos[s] = offsets[served[s]] + kept[served[s]] + rank2[s];
+      else pos[s] = -1;
+    }
+    for (int e = 0; e < E; ++e) {
+      kept[e] += fill2[e];
+      *rerouted += fill2[e];
+    }
+  } else {
+    mo_dispatch_positions(T, k, E, idx, rank.data(), kept, offsets, pos);
+    for (long long s = 0; s < S; ++s) served[s] = rank[s] >= 0 ? idx[s] : -1;
+  }
   *C_out = C;
   return nonfinite;
 }
@@ -467,15 +558,16 @@ static int route_layer(const mo_config* c, const mo_inputs* in, double* l, int* 
 int mo_layer_forward(const mo_config* c, const mo_inputs* in, mo_outputs* out) {
   const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
   if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
-      (dt != MO_F32 && dt != MO_BF16) || c->balance != 0 || (c->route & ~7))
+      (dt != MO_F32 && dt != MO_BF16) || c->balance != 0 || (c->route & ~15))
     return -1;
   const long long S = static_cast<long long>(T) * k;
   const int es = dt == MO_BF16 ? 2 : 4;
   std::vector<double> l(static_cast<size_t>(T) * E);
-  std::vector<int> rank(S);
+  std::vector<int> served(S);
   int C = 0;
-  const int nonfinite = route_layer(c, in, l.data(), out->idx, out->w, out->counts, rank.data(), out->kept,
-                                    out->offsets, out->pos, &C);
+  long long rerouted = 0;
+  const int nonfinite = route_layer(c, in, l.data(), out->idx, out->w, out->counts, out->kept, out->offsets,
+                                    out->pos, served.data(), &C, &rerouted);
 
   // dispatch ([P1] 4.2 step 2: the tokens bound for the same expert grouped
   // together): the stored row of x[t] copied to row pos[t,j] of Xp; then
@@ -524,6 +616,7 @@ int mo_layer_forward(const mo_config* c, const mo_inputs* in, mo_outputs* out) {
   out->stats[5] = mo_balance_stat(E, T, out->counts, c->lam);
   out->stats[6] = nonfinite;
   out->stats[7] = mo_router_entropy(T, E, l.data());
+  out->stats[8] = static_cast<double>(rerouted);
   return 0;
 }
 
@@ -702,9 +795,8 @@ struct mo_grads {
 };
 
 // The training step's backward with the routing of c->route (raw
-// probabilities, token-major priority, a LayerNorm in front; rerouting is
-// the numpy oracle's only) and the balance term of c->balance
-// (mo_balance_term_grad):
+// probabilities, token-major priority, a LayerNorm in front, rerouting)
+// and the balance term of c->balance (mo_balance_term_grad):
 //   per slot, G[t,j] = [kept] <dY[t], FFN_e(x[t])> + dB/dw[t,j];
 //   dl[t, idx_j] = w_j (G_j - sum_j' w_j' G_j') (the softmax over the
 //   selected logits), other logits 0;
@@ -714,17 +806,18 @@ struct mo_grads {
 int mo_layer_backward(const mo_config* c, const mo_inputs* in, const void* dY, mo_grads* g) {
   const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
   if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
-      (dt != MO_F32 && dt != MO_BF16) || c->balance < 0 || c->balance > 2 || (c->route & ~7))
+      (dt != MO_F32 && dt != MO_BF16) || c->balance < 0 || c->balance > 2 || (c->route & ~15))
     return -1;
   const long long S = static_cast<long long>(T) * k, Td = static_cast<long long>(T) * d;
   const int es = dt == MO_BF16 ? 2 : 4;
   // the forward's routing
   std::vector<double> l(static_cast<size_t>(T) * E), w(S);
-  std::vector<int> idx(S), rank(S);
+  std::vector<int> idx(S), served(S);
   std::vector<long long> counts(E), kept(E), offsets(E + 1), pos(S);
   int C = 0;
-  route_layer(c, in, l.data(), idx.data(), w.data(), counts.data(), rank.data(), kept.data(), offsets.data(),
-              pos.data(), &C);
+  long long rerouted = 0;
+  route_layer(c, in, l.data(), idx.data(), w.data(), counts.data(), kept.data(), offsets.data(), pos.data(),
+              served.data(), &C, &rerouted);
 
   std::vector<double> dy(Td);
   for (long long i = 0; i < Td; ++i) dy[i] = rd(dY, dt, i);
@@ -746,11 +839,13 @@ int mo_layer_backward(const mo_config* c, const mo_inputs* in, const void* dY, m
   const auto at = [&](const void* base, long long elems) -> const void* {
     return base ? static_cast<const char*>(base) + elems * es : nullptr;
   };
-  // each expert over its kept slots, in slot order (token, then choice)
+  // each expert over the slots it serves, in slot order (token, then
+  // choice); a rerouted slot's output still carries its weight w_j, so its
+  // logit gradient stays on idx_j
   for (int e = 0; e < E; ++e) {
     std::vector<long long> slots;
     for (long long s = 0; s < S; ++s)
-      if (idx[s] == e && pos[s] >= 0) slots.push_back(s);
+      if (served[s] == e) slots.push_back(s);
     const int n = static_cast<int>(slots.size());
     if (n == 0) continue;
     std::vector<char> v(static_cast<size_t>(n) * d * es);

@@ -127,15 +127,17 @@ def test_swiglu_backward_small(shared, noise, cf):
 @pytest.mark.parametrize("act,balance,lam,variant", [
     ("swiglu", "cv", 0.01, {}), ("gelu", "cv", 0.01, {}), ("swiglu", "std_max", 0.5, {}),
     ("swiglu", "switch", 0.5, {}), ("swiglu", "cv", 0.01, dict(raw_probs=True, token_major=True)),
-    ("swiglu", "cv", 0.01, dict(layernorm=True))], ids=lambda p: p if isinstance(p, str) else
+    ("swiglu", "cv", 0.01, dict(layernorm=True)), ("swiglu", "cv", 0.01, dict(reroute=True))],
+    ids=lambda p: p if isinstance(p, str) else
     ("+".join(p) or "default") if isinstance(p, dict) else str(p))
 def test_backward_against_cpp_oracle(act, balance, lam, variant):
     """The same gradients against the single-threaded C++ fp64 oracle
     (mo_layer_backward): the shared expert, Gumbel noise and a binding
     capacity; GeLU with biases on every expert; each balance term; raw
     probabilities with token-major priority; a LayerNorm in front of the
-    router (rows with their own offset and scale, dX bounded per row).  The
-    routing (pos) equals the C++ oracle's bit for bit."""
+    router (rows with their own offset and scale, dX bounded per row);
+    rerouting of the overflow to backups.  The routing (pos) equals the C++
+    oracle's bit for bit."""
     ln = bool(variant.get("layernorm"))
     wl = _workload(act=act, has_shared=True, gumbel=True, capacity_factor=1.0, lam=lam, seed=79, x_affine=ln)
     t = guarded_inputs(wl, "cpu", layernorm=ln)
@@ -154,6 +156,7 @@ def test_backward_against_cpp_oracle(act, balance, lam, variant):
     fwd = cpp.layer_forward(dict(cfg, balance="cv"), w, t["x"], t.get("expert_bias"), t.get("noise"))
     np.testing.assert_array_equal(sv["pos"].cpu().numpy(), fwd["pos"])
     assert (fwd["pos"] < 0).any()
+    assert (fwd["stats"]["rerouted_slots"] > 0) == bool(variant.get("reroute"))
     check_all(wl, t, dY, g, ref, dx_row_scaled=ln)
 
 

@@ -424,16 +424,63 @@ def test_token_major_capacity_queue():
     assert (fill == C).any()
 
 
+def test_backup_experts_and_reroute_queue():
+    """Backups are each token's experts ranked k .. 2k-1 by (logit
+    descending, index ascending), against a sort; the second capacity pass
+    against a direct queue in either priority: the r-th dropped slot of a
+    token tries its r-th backup once, kept if the expert has room after
+    its first-pass rows and the slots rerouted to it before."""
+    rng = np.random.default_rng(101)
+    T, k, E = 60, 2, 7
+    l = np.round(rng.normal(size=(T, E)), 1)  # rounding makes ties
+    l[3, 2] = np.inf
+    b = cpp.backup_experts(l, k)
+    for t in range(T):
+        if not np.all(np.isfinite(l[t])):
+            assert (b[t] == -1).all()
+            continue
+        order = sorted(range(E), key=lambda e: (-l[t, e], e))
+        np.testing.assert_array_equal(b[t], order[k:2 * k])
+    idx, _, _ = cpp.top_k(l, k)
+    C = 15
+    for tm in (False, True):
+        rank, fill = cpp.assign_capacity_token_major(idx, E, C) if tm else cpp.assign_capacity(idx, E, C)
+        served, rank2, fill2 = cpp.reroute_overflow(idx, b, rank, fill, C, tm)
+        nth = -np.ones((T, k), dtype=np.int64)
+        for t in range(T):
+            r = 0
+            for j in range(k):
+                if idx[t, j] >= 0 and rank[t, j] < 0:
+                    nth[t, j] = r
+                    r += 1
+        used = fill.astype(np.int64).copy()
+        extra = np.zeros(E, dtype=np.int64)
+        order = [(t, j) for t in range(T) for j in range(k)] if tm else [(t, j) for j in range(k) for t in range(T)]
+        for t, j in order:
+            want_served = idx[t, j] if rank[t, j] >= 0 else -1
+            want_rank2 = -1
+            if nth[t, j] >= 0 and b[t, nth[t, j]] >= 0 and used[b[t, nth[t, j]]] < C:
+                e = b[t, nth[t, j]]
+                want_served, want_rank2 = e, extra[e]
+                extra[e] += 1
+                used[e] += 1
+            assert served[t, j] == want_served and rank2[t, j] == want_rank2, (tm, t, j)
+        np.testing.assert_array_equal(fill2, extra)
+        assert extra.sum() > 0
+
+
 VARIANT_ROUTES = [dict(raw_probs=True), dict(token_major=True), dict(layernorm=True),
-                  dict(raw_probs=True, token_major=True, layernorm=True)]
+                  dict(raw_probs=True, token_major=True, layernorm=True), dict(reroute=True),
+                  dict(reroute=True, token_major=True, raw_probs=True)]
 
 
 @pytest.mark.parametrize("route", VARIANT_ROUTES, ids=lambda r: "+".join(r))
 def test_routing_variants_match_numpy_oracle(route):
     """Forward and backward of a SwiGLU bf16 layer with the shared expert, a
-    binding capacity and Gumbel noise, under each routing variant: routing
-    bit for bit and every output and gradient to 1e-11 of the numpy
-    oracle's."""
+    binding capacity and Gumbel noise, under each routing variant (and
+    rerouting, which moves some dropped slots to backups): routing and the
+    slot counts bit for bit, every output and gradient to 1e-11 of the
+    numpy oracle's."""
     wl = S.WORKLOADS["training"].replace(T=64, d=24, h=32, E=6, capacity_factor=0.7, seed=83)
     t = S.make_inputs(wl, "cpu")
     cfg = dict(_bwd_cfg(wl), **route)
@@ -444,6 +491,9 @@ def test_routing_variants_match_numpy_oracle(route):
     np.testing.assert_allclose(c["w"], n["w"], rtol=0, atol=1e-14)
     np.testing.assert_allclose(c["y"], n["y"], rtol=0, atol=1e-12 * max(1.0, float(np.abs(n["y"]).max())))
     assert (c["pos"] < 0).any()
+    for key in ("kept_slots", "dropped_slots", "rerouted_slots"):
+        assert c["stats"][key] == n["stats"][key], key
+    assert (c["stats"]["rerouted_slots"] > 0) == bool(route.get("reroute"))
     cb = cpp.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
     nb = O.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
     for key in [k_ for k_ in cb if k_ not in ("loss", "balance_term")]:
