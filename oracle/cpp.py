@@ -247,14 +247,12 @@ STATS = ("routed_slots", "kept_slots", "dropped_slots", "capacity", "drop_rate",
 
 
 def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None) -> dict:
-    """The whole forward pass (the CV statistic).  cfg: T, d, h, E, k, act,
-    capacity_factor, min_capacity, lam, has_shared and the routing flags
+    """The whole forward pass.  cfg: T, d, h, E, k, act, capacity_factor,
+    min_capacity, lam, balance, gamma, has_shared and the routing flags
     raw_probs, token_major, layernorm, reroute (as for
     moe_oracle.layer_forward);
     weights: Wr, W1, W3, b1, W2, b2, Ws1, Ws3, bs1, Ws2, bs2 (stored
     tensors, absent or None where the layer has none)."""
-    if cfg.get("balance", "cv") != "cv":
-        raise ValueError("the C++ oracle's forward reports the CV statistic only")
     T, d, E, k = cfg["T"], cfg["d"], cfg["E"], cfg["k"]
     px, dt, kx = _stored(x)
     keep = [kx]
@@ -270,7 +268,8 @@ def layer_forward(cfg: dict, weights: dict, x, expert_bias=None, noise=None) -> 
     c = _Config(T=T, d=d, h=cfg["h"], E=E, k=k, act=ACT[cfg["act"]], dtype=dt,
                 min_capacity=int(cfg.get("min_capacity", 0)), has_shared=int(bool(cfg.get("has_shared"))),
                 capacity_factor=float(np.float32(cfg.get("capacity_factor", 0.0))),
-                lam=float(cfg.get("lam", 0.01)), route=_route(cfg))
+                lam=float(cfg.get("lam", 0.01)), balance=BALANCE[cfg.get("balance", "cv")],
+                gamma=float(cfg.get("gamma", 100.0)), route=_route(cfg))
     r = dict(y=np.empty((T, d)), idx=np.empty((T, k), dtype=np.int32), w=np.empty((T, k)),
              counts=np.empty(E, dtype=np.int64), kept=np.empty(E, dtype=np.int64),
              offsets=np.empty(E + 1, dtype=np.int64), pos=np.empty((T, k), dtype=np.int64),

@@ -36,8 +36,7 @@
 // (mean(f) + 1e-8) on pre-capacity counts f = counts / T; a token with a
 // non-finite logit is routed to no expert.  The routing variants -- raw
 // probabilities, token-major priority, a LayerNorm in front, rerouting --
-// are here too (mo_config.route); the forward's other balance statistics
-// are the numpy oracle's only.
+// and the other balance forms are here too (mo_config.route, .balance).
 
 #include <cmath>
 #include <cstdint>
@@ -458,6 +457,37 @@ double mo_balance_stat(int E, int T, const long long* counts, double lam) {
   return lam * std::sqrt(ss / (E - 1)) / (mean + 1e-8);
 }
 
+// The load statistic in the form `variant` gives, on the pre-capacity
+// usage f = counts / T: 0, CV (mo_balance_stat); 1, lambda (std_{n-1}(f) +
+// gamma max(f)) ([P2] 3.2's auxiliary loss on the experts' usage
+// frequency); 2, lambda sum_e f_e P_e with P = I / T, I[e] the sum of the
+// routing weights of the slots routed to e ([P3] 2.3's product of the
+// usage fraction and the mean routing weight).  idx, w [T,k].
+double mo_balance_stat_form(int E, int T, int k, const long long* counts, const int* idx, const double* w,
+                            double lam, int variant, double gamma) {
+  if (variant == 0) return mo_balance_stat(E, T, counts, lam);
+  std::vector<double> f(static_cast<size_t>(E));
+  for (int e = 0; e < E; ++e) f[e] = static_cast<double>(counts[e]) / T;
+  if (variant == 1) {
+    double mean = 0.0, mx = f[0];
+    for (int e = 0; e < E; ++e) {
+      mean += f[e];
+      mx = std::max(mx, f[e]);
+    }
+    mean /= E;
+    double ss = 0.0;
+    for (int e = 0; e < E; ++e) ss += (f[e] - mean) * (f[e] - mean);
+    const double sd = E > 1 ? std::sqrt(ss / (E - 1)) : 0.0;
+    return lam * (sd + gamma * mx);
+  }
+  std::vector<double> imp(static_cast<size_t>(E), 0.0);
+  for (long long s = 0; s < static_cast<long long>(T) * k; ++s)
+    if (idx[s] >= 0) imp[idx[s]] += w[s];
+  double v = 0.0;
+  for (int e = 0; e < E; ++e) v += f[e] * (imp[e] / T);
+  return lam * v;
+}
+
 // ---------------------------------------------------------------------------
 // the layer
 // ---------------------------------------------------------------------------
@@ -470,7 +500,7 @@ struct mo_config {
   int has_shared;
   float capacity_factor;  // <= 0: no limit
   double lam;
-  int balance;   // the backward's balance term: 0 CV, 1 std + max, 2 switch (the forward's statistic is CV)
+  int balance;   // the balance form: 0 CV, 1 std + max, 2 switch (the forward's statistic, the backward's term)
   double gamma;  // its max weight (std + max)
   int route;     // MO_RAW_PROBS | MO_TOKEN_MAJOR | MO_LAYERNORM | MO_REROUTE
 };
@@ -558,7 +588,7 @@ static int route_layer(const mo_config* c, const mo_inputs* in, double* l, int* 
 int mo_layer_forward(const mo_config* c, const mo_inputs* in, mo_outputs* out) {
   const int T = c->T, d = c->d, h = c->h, E = c->E, k = c->k, dt = c->dtype;
   if (T < 1 || d < 1 || h < 1 || E < 1 || k < 1 || k > E || (c->act != 0 && c->act != 1) ||
-      (dt != MO_F32 && dt != MO_BF16) || c->balance != 0 || (c->route & ~15))
+      (dt != MO_F32 && dt != MO_BF16) || c->balance < 0 || c->balance > 2 || (c->route & ~15))
     return -1;
   const long long S = static_cast<long long>(T) * k;
   const int es = dt == MO_BF16 ? 2 : 4;
@@ -613,7 +643,7 @@ int mo_layer_forward(const mo_config* c, const mo_inputs* in, mo_outputs* out) {
   out->stats[2] = static_cast<double>(S - kept);
   out->stats[3] = C;
   out->stats[4] = static_cast<double>(S - kept) / static_cast<double>(S);
-  out->stats[5] = mo_balance_stat(E, T, out->counts, c->lam);
+  out->stats[5] = mo_balance_stat_form(E, T, k, out->counts, out->idx, out->w, c->lam, c->balance, c->gamma);
   out->stats[6] = nonfinite;
   out->stats[7] = mo_router_entropy(T, E, l.data());
   out->stats[8] = static_cast<double>(rerouted);

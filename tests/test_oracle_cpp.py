@@ -310,7 +310,8 @@ def _bwd_cfg(wl, balance="cv"):
 def test_layer_backward_matches_numpy_oracle(wl, balance):
     """Every gradient, the logit gradient, y and the loss of the C++
     backward equal the numpy oracle's (itself pinned by finite differences)
-    to 1e-11 of each tensor's largest entry, for each balance term."""
+    to 1e-11 of each tensor's largest entry, for each balance term; the
+    forward's load statistic in that form to 1e-12."""
     t = S.make_inputs(wl, "cpu")
     cfg = _bwd_cfg(wl, balance)
     c = cpp.layer_backward(cfg, t, t["x"], t["dY"], t.get("expert_bias"), t.get("noise"))
@@ -324,6 +325,10 @@ def test_layer_backward_matches_numpy_oracle(wl, balance):
     assert abs(c["balance_term"] - n["balance_term"]) <= 1e-14 * max(1.0, abs(n["balance_term"]))
     if wl.capacity_factor > 0:
         assert (n["route"]["pos"] < 0).any()  # a dropped slot takes part
+    # the forward's load statistic in the same form
+    cf = cpp.layer_forward(cfg, t, t["x"], t.get("expert_bias"), t.get("noise"))
+    ref = n["route"]["stats"]["balance_stat"]
+    assert abs(cf["stats"]["balance_stat"] - ref) <= 1e-12 * max(1.0, abs(ref)), balance
 
 
 def test_layer_backward_finite_differences():
