@@ -830,3 +830,39 @@ def test_routing_and_balance_variants_combined():
     check_routing(r, sv, stats, t["x"])
     assert stats["rerouted_slots"] > 0 and stats["dropped_slots"] > 0
     assert_close_bf16_scaled(to_np(y), r["y"], "y")
+
+
+@pytest.mark.parametrize("route", [dict(), dict(raw_probs=True, token_major=True), dict(layernorm=True),
+                                   dict(reroute=True), dict(balance="std_max", balance_gamma=100.0),
+                                   dict(balance="switch")],
+                         ids=lambda r: "+".join(k for k in r if k != "balance_gamma") + (
+                             "-" + r["balance"] if "balance" in r else "") or "default")
+def test_forward_variants_against_cpp_oracle(route):
+    """The layer forward held to the single-threaded C++ fp64 oracle
+    (mo_layer_forward) under each routing variant and balance form: a
+    SwiGLU bf16 layer with the shared expert, Gumbel noise, a Zipf(1.1)
+    router bias and a binding capacity (rerouting keeps some of the
+    overflow).  idx, counts, kept, offsets, pos and the slot counts bit for
+    bit, weights to 1e-4, statistics as check_routing states (the switch
+    form from fp32 weights to relative 2e-6), y at the bf16 bounds (rows
+    with their own offset and scale under the LayerNorm router)."""
+    ln = bool(route.get("layernorm"))
+    wl = S.WORKLOADS["training"].replace(T=700, d=256, h=256, E=12, capacity_factor=0.9, zipf_s=1.1, seed=37,
+                                         x_affine=ln)
+    t = guarded_inputs(wl, DEV, layernorm=ln)
+    cfg = M.config_of(wl, **route)
+    sv = M.moe.alloc_saved(cfg)
+    y = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device=DEV)
+    st = M.moe.stats_buffer()
+    ws = M.moe.workspace(cfg, 1)
+    M.moe_layer_fwd(cfg, {n: t.get(n) for n in WEIGHT_NAMES}, t["x"], t.get("noise"), y, sv, st, ws)
+    assert M.moe_check_error(ws) == 0
+    r = cpp.layer_forward(oracle_cfg(wl, **route), oracle_weights(t), t["x"], t.get("expert_bias"), t.get("noise"))
+    stats = M.moe.read_stats(st)
+    check_routing(r, sv, stats, t["x"], bal_rtol=2e-6 if route.get("balance") == "switch" else 1e-12)
+    assert stats["dropped_slots"] > 0
+    assert (stats["rerouted_slots"] > 0) == bool(route.get("reroute"))
+    if ln:
+        assert_close_bf16_scaled(to_np(y), r["y"], "y")
+    else:
+        assert_close_bf16(to_np(y), r["y"], "y")
