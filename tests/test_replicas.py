@@ -63,3 +63,22 @@ def test_reference_arm_runs_on_rank_zero_only():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2"],
                        env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("name,mode", [("tiny_fp32", "whole"), ("small_prefill", "experts"), ("training", "train")])
+def test_cpu_baseline_runs_the_cpp_oracle_on_one_core(monkeypatch, name, mode):
+    """bench.cpu_baseline on each of its modes, on small stand-ins of the
+    workloads (inputs drawn on the host): the single-threaded C++ oracle
+    runs, on one core, and the result says what it timed."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import moe_synth as S
+    small = dict(tiny_fp32=S.WORKLOADS["tiny_fp32"].replace(T=32),
+                 small_prefill=S.WORKLOADS["small_prefill"].replace(T=128, d=64, h=96, E=4),
+                 training=S.WORKLOADS["training"].replace(T=64, d=64, h=96, E=4))
+    monkeypatch.setitem(S.WORKLOADS, name, small[name])
+    r = bench.cpu_baseline(name, mode=mode, max_rows=3)
+    assert r["value"] > 0 and r["cores"] == 1 and r["kind"] == "oracle"
+    assert r["impl"] == "C++ fp64 oracle, single thread"
+    assert r["extrapolated"] == (mode != "whole")
+    assert ("forward and backward" in r["sample"]) == (mode == "train")
