@@ -37,6 +37,11 @@
  *    shared Ws1, Ws3 [h,d]; Ws2 [d,h]; bs1 [h]; bs2 [d].
  *  - Asynchrony: work is enqueued on `stream`; no call synchronises the host
  *    except moe_check_error.  Statistics are written to device memory.
+ *  - Workspace: it serves one call at a time -- calls that share one must be
+ *    ordered (the same stream, or events).  Its first 256 bytes are a
+ *    header: the error word and the grouped GEMMs' tile counter, which every
+ *    entry point zeroes before its first launch, so a fresh workspace needs
+ *    no set-up; the rest is scratch that each call writes before it reads.
  *  - Errors: argument checks happen before any launch and return
  *    MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE with no
  *    work enqueued.  A failed launch returns MOE_ERR_CUDA.  Non-finite router
